@@ -1,0 +1,470 @@
+/*
+ * spec_ref.c -- plain, slow, fp64 CPU oracle for batched speculative-sampling
+ * verification.
+ *
+ * TEST INFRASTRUCTURE.  Only tests/, __graft_entry__.smoke() and bench.py's
+ * CPU-baseline / reference arm load this library.  The CUDA product path never
+ * calls, links or includes anything here, and this file includes nothing from
+ * the product (no shared headers, tables or helpers).
+ *
+ * What it computes, and where the pages define it:
+ *   - p = softmax(logits / T), q likewise, same T for target and draft:
+ *     "Speculative Decoding and the Art of Fast LLM Inference", "Why It Stays
+ *     Exact", key limitation (identical temperature for draft and target).
+ *   - accept g_i with probability min(1, p_i(g_i)/q_i(g_i)), left to right:
+ *     same page, "The Algorithm, Step by Step", step "Accept or reject";
+ *     "Speculative decoding: faster LLM inference" (thelatentsource),
+ *     "The correction that keeps the target in charge", the accept_token
+ *     snippet: draft_prob <= 0 is an error, target_prob >= draft_prob accepts,
+ *     otherwise accept iff a uniform in [0,1) is strictly below the ratio.
+ *   - stop at the first rejection and draw one token from
+ *     norm(max(0, p - q)) there: first page, step "Stop at the first
+ *     rejection"; second page, equation r(x).
+ *   - if all k are accepted, draw a bonus token from p_{k+1}: first page, step
+ *     "Bonus token"; interview page ("techaiinterview"), "Algorithm (one
+ *     round)", step 4.
+ *   - temperature 0: accept while the target's argmax equals the draft token:
+ *     interview page, "Deep dive: correctness and speedup" (greedy remark).
+ *
+ * Readings where the pages are silent (each one is listed in the design doc):
+ *   - a draw uses inverse-CDF: C(x) = sum_{y<=x} w(y) accumulated left to
+ *     right, R = C(V-1) (the scan's own total), token = smallest x with
+ *     C(x) > u*R; if rounding leaves no such x, the largest x with w(x) > 0.
+ *   - u_accept[b,i] drives accept test i; u_resample[b] drives the one draw.
+ *   - residual mass R == 0 at a rejection (impossible in exact arithmetic)
+ *     falls back to sampling p_j.
+ *   - argmax ties go to the lowest index.
+ *   - sequence errors (out_num_accepted = -1, tokens all -1): T NaN, negative,
+ *     infinite, or positive below FLT_MIN; a draft token outside [0,V); a NaN
+ *     or +inf logit in a row the call reads (all k+1 target rows, and the k
+ *     draft rows when T > 0); such a row whose logits are all -inf; q(g) <= 0
+ *     at a position the scan reaches.
+ *
+ * Everything is fp64 with plain sequential loops; no blocking, no fusion, no
+ * reordering beyond the definition.
+ */
+#include <math.h>
+#include <float.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+#include <pthread.h>
+
+#define REF_F32 0
+#define REF_BF16 1
+
+#define REF_OK 0
+#define REF_EINVAL 1
+#define REF_ENOMEM 2
+
+/* ---------------------------------------------------------------- decoding */
+
+/* bf16 is the upper half of an IEEE binary32; widening is exact. */
+static double ref_bf16_to_double(uint16_t bits)
+{
+    uint32_t w = ((uint32_t)bits) << 16;
+    float f;
+    memcpy(&f, &w, sizeof f);
+    return (double)f;
+}
+
+/* Read one logit of a row-major array as fp64. */
+static double ref_logit(const void *base, int dtype, size_t idx)
+{
+    if (dtype == REF_F32)
+        return (double)((const float *)base)[idx];
+    return ref_bf16_to_double(((const uint16_t *)base)[idx]);
+}
+
+/* Copy row `row` (V logits) of a typed array into an fp64 buffer. */
+static void ref_load_row(const void *base, int dtype, size_t row, int64_t V, double *out)
+{
+    for (int64_t x = 0; x < V; ++x)
+        out[x] = ref_logit(base, dtype, (size_t)row * (size_t)V + (size_t)x);
+}
+
+/* ------------------------------------------------------------- primitives */
+
+/* Maximum and lowest-index argmax of a row. */
+static double ref_max_argmax(const double *l, int64_t V, int64_t *arg)
+{
+    double m = l[0];
+    int64_t a = 0;
+    for (int64_t x = 1; x < V; ++x) {
+        if (l[x] > m) {
+            m = l[x];
+            a = x;
+        }
+    }
+    if (arg)
+        *arg = a;
+    return m;
+}
+
+/* 1 if the row holds a NaN or +inf, or every entry is -inf. */
+static int ref_row_invalid(const double *l, int64_t V)
+{
+    int all_neg_inf = 1;
+    for (int64_t x = 0; x < V; ++x) {
+        if (isnan(l[x]) || (isinf(l[x]) && l[x] > 0))
+            return 1;
+        if (!(isinf(l[x]) && l[x] < 0))
+            all_neg_inf = 0;
+    }
+    return all_neg_inf;
+}
+
+/*
+ * p = softmax(l / T) over V entries, T > 0, with the maximum subtracted
+ * before exponentiation (exp(-inf) = 0 for masked entries).
+ */
+int spec_ref_softmax(const double *l, int64_t V, double T, double *p)
+{
+    if (!(T > 0) || V < 1)
+        return REF_EINVAL;
+    double m = ref_max_argmax(l, V, NULL);
+    double Z = 0.0;
+    for (int64_t x = 0; x < V; ++x) {
+        p[x] = exp((l[x] - m) / T);
+        Z += p[x];
+    }
+    for (int64_t x = 0; x < V; ++x)
+        p[x] /= Z;
+    return REF_OK;
+}
+
+/*
+ * Residual (correction) weights w(x) = max(0, p(x) - q(x)); returns their
+ * total.  The normalised r(x) = w(x) / total is the second page's r(x).
+ */
+double spec_ref_residual(const double *p, const double *q, int64_t V, double *w)
+{
+    double R = 0.0;
+    for (int64_t x = 0; x < V; ++x) {
+        double d = p[x] - q[x];
+        w[x] = d > 0.0 ? d : 0.0;
+        R += w[x];
+    }
+    return R;
+}
+
+/*
+ * Inverse-CDF draw from non-negative weights w (not necessarily normalised):
+ * C(x) = sum_{y<=x} w(y), R = C(V-1); the smallest x with C(x) > u*R, else
+ * the largest x with w(x) > 0.  Returns -1 if every weight is zero.  When
+ * cell is non-NULL it receives [C(x-1)/R, C(x)/R, R] for the chosen x.
+ */
+int64_t spec_ref_inverse_cdf(const double *w, int64_t V, double u, double *cell)
+{
+    double R = 0.0;
+    for (int64_t x = 0; x < V; ++x)
+        R += w[x];
+    if (!(R > 0.0))
+        return -1;
+    double target = u * R;
+    double C = 0.0, Cprev = 0.0;
+    int64_t pick = -1;
+    for (int64_t x = 0; x < V; ++x) {
+        Cprev = C;
+        C += w[x];
+        if (C > target) {
+            pick = x;
+            break;
+        }
+    }
+    if (pick < 0) {
+        /* rounding left u*R at or above the total: clamp */
+        for (int64_t x = V - 1; x >= 0; --x) {
+            if (w[x] > 0.0) {
+                pick = x;
+                break;
+            }
+        }
+        C = 0.0;
+        for (int64_t x = 0; x <= pick; ++x) {
+            Cprev = C;
+            C += w[x];
+        }
+    }
+    if (cell) {
+        cell[0] = Cprev / R;
+        cell[1] = C / R;
+        cell[2] = R;
+    }
+    return pick;
+}
+
+/* ------------------------------------------------------------ one sequence */
+
+typedef struct {
+    const void *target;      /* [B, k+1, V] */
+    const void *draft;       /* [B, k, V] */
+    int dtype;
+    const int32_t *tokens;   /* [B, k] */
+    const double *u_accept;  /* [B, k] */
+    const double *u_resample;/* [B] */
+    const double *temperature;/* [B] */
+    int64_t B, k, V;
+    int32_t *out_tokens;     /* [B, k+1] */
+    int32_t *out_num_accepted;/* [B] */
+    double *trace;           /* [B, k+3] or NULL */
+    int64_t b0, b1;          /* sequence range for this worker */
+    int status;
+} ref_job_t;
+
+static void ref_fail_sequence(ref_job_t *J, int64_t b)
+{
+    for (int64_t i = 0; i <= J->k; ++i)
+        J->out_tokens[b * (J->k + 1) + i] = -1;
+    J->out_num_accepted[b] = -1;
+}
+
+/* Returns 0 on success, 1 if the sequence is an error row. */
+static int ref_one_sequence(ref_job_t *J, int64_t b, double *t, double *d,
+                            double *p, double *q, double *w)
+{
+    const int64_t k = J->k, V = J->V;
+    const double T = J->temperature[b];
+    double *tr = J->trace ? J->trace + b * (k + 3) : NULL;
+    if (tr)
+        for (int64_t i = 0; i < k + 3; ++i)
+            tr[i] = NAN;
+
+    /* temperature must be 0 (greedy) or a finite normal positive value */
+    if (isnan(T) || T < 0 || isinf(T) || (T > 0 && T < (double)FLT_MIN))
+        return 1;
+    for (int64_t i = 0; i < k; ++i) {
+        int32_t g = J->tokens[b * k + i];
+        if (g < 0 || g >= V)
+            return 1;
+    }
+    /* every row the call reads must be usable */
+    for (int64_t i = 0; i <= k; ++i) {
+        ref_load_row(J->target, J->dtype, (size_t)(b * (k + 1) + i), V, t);
+        if (ref_row_invalid(t, V))
+            return 1;
+    }
+    if (T > 0) {
+        for (int64_t i = 0; i < k; ++i) {
+            ref_load_row(J->draft, J->dtype, (size_t)(b * k + i), V, d);
+            if (ref_row_invalid(d, V))
+                return 1;
+        }
+    }
+
+    int64_t j = k;        /* first rejected position, k = all accepted */
+    int64_t token = -1;
+    if (T == 0) {
+        /* greedy: accept while the target's argmax equals the draft token */
+        for (int64_t i = 0; i < k; ++i) {
+            int64_t a;
+            ref_load_row(J->target, J->dtype, (size_t)(b * (k + 1) + i), V, t);
+            ref_max_argmax(t, V, &a);
+            if (J->tokens[b * k + i] != a) {
+                j = i;
+                token = a;
+                break;
+            }
+        }
+        if (j == k) {
+            int64_t a;
+            ref_load_row(J->target, J->dtype, (size_t)(b * (k + 1) + k), V, t);
+            ref_max_argmax(t, V, &a);
+            token = a;
+        }
+    } else {
+        for (int64_t i = 0; i < k; ++i) {
+            int32_t g = J->tokens[b * k + i];
+            ref_load_row(J->target, J->dtype, (size_t)(b * (k + 1) + i), V, t);
+            ref_load_row(J->draft, J->dtype, (size_t)(b * k + i), V, d);
+            spec_ref_softmax(t, V, T, p);
+            spec_ref_softmax(d, V, T, q);
+            double P = p[g], Q = q[g];
+            if (Q <= 0.0)
+                return 1; /* a sampled draft token must have positive probability */
+            double ratio = P / Q;
+            if (tr)
+                tr[i] = ratio < 1.0 ? ratio : 1.0;
+            int accept = (P >= Q) || (J->u_accept[b * k + i] < ratio);
+            if (!accept) {
+                j = i;
+                break;
+            }
+        }
+        double cell[3];
+        if (j < k) {
+            /* p and q still hold position j's distributions */
+            double R = spec_ref_residual(p, q, V, w);
+            if (!(R > 0.0))
+                memcpy(w, p, (size_t)V * sizeof(double)); /* rounding-only fallback */
+        } else {
+            ref_load_row(J->target, J->dtype, (size_t)(b * (k + 1) + k), V, t);
+            spec_ref_softmax(t, V, T, w);
+        }
+        token = spec_ref_inverse_cdf(w, V, J->u_resample[b], cell);
+        if (token < 0)
+            return 1;
+        if (tr) {
+            tr[k] = cell[0];
+            tr[k + 1] = cell[1];
+            tr[k + 2] = cell[2];
+        }
+    }
+
+    for (int64_t i = 0; i < j; ++i)
+        J->out_tokens[b * (k + 1) + i] = J->tokens[b * k + i];
+    J->out_tokens[b * (k + 1) + j] = (int32_t)token;
+    for (int64_t i = j + 1; i <= k; ++i)
+        J->out_tokens[b * (k + 1) + i] = -1;
+    J->out_num_accepted[b] = (int32_t)j;
+    return 0;
+}
+
+static void *ref_worker(void *arg)
+{
+    ref_job_t *J = (ref_job_t *)arg;
+    size_t n = (size_t)J->V;
+    double *buf = (double *)malloc(5 * n * sizeof(double));
+    if (!buf) {
+        J->status = REF_ENOMEM;
+        return NULL;
+    }
+    double *t = buf, *d = buf + n, *p = buf + 2 * n, *q = buf + 3 * n, *w = buf + 4 * n;
+    for (int64_t b = J->b0; b < J->b1; ++b)
+        if (ref_one_sequence(J, b, t, d, p, q, w))
+            ref_fail_sequence(J, b);
+    free(buf);
+    J->status = REF_OK;
+    return NULL;
+}
+
+/*
+ * The verification step for B sequences, split over `nthreads` host threads
+ * (contiguous ranges of sequences; the result does not depend on the split).
+ *
+ * target [B,k+1,V] and draft [B,k,V] are fp32 or bf16 bit patterns (dtype 0
+ * or 1).  Uniforms and temperatures are fp64 so that tests can place them
+ * anywhere in [0,1).  trace (nullable) receives per sequence k+3 doubles: the
+ * accept threshold min(1, P/Q) of each tested position (NaN if not tested or
+ * greedy), then the chosen draw cell [lo, hi) in u-units and the draw's total
+ * mass R (NaN for greedy).
+ */
+int spec_verify_ref_mt(const void *target, const void *draft, int dtype,
+                       const int32_t *tokens, const double *u_accept,
+                       const double *u_resample, const double *temperature,
+                       int64_t B, int64_t k, int64_t V,
+                       int32_t *out_tokens, int32_t *out_num_accepted,
+                       double *trace, int nthreads)
+{
+    if (!target || !tokens || !u_accept || !u_resample || !temperature ||
+        !out_tokens || !out_num_accepted)
+        return REF_EINVAL;
+    if (B < 0 || k < 1 || V < 2 || (dtype != REF_F32 && dtype != REF_BF16))
+        return REF_EINVAL;
+    if (!draft)
+        return REF_EINVAL;
+    if (B == 0)
+        return REF_OK;
+    if (nthreads < 1)
+        nthreads = 1;
+    if (nthreads > B)
+        nthreads = (int)B;
+
+    ref_job_t *jobs = (ref_job_t *)calloc((size_t)nthreads, sizeof(ref_job_t));
+    pthread_t *th = (pthread_t *)calloc((size_t)nthreads, sizeof(pthread_t));
+    if (!jobs || !th) {
+        free(jobs);
+        free(th);
+        return REF_ENOMEM;
+    }
+    for (int w = 0; w < nthreads; ++w) {
+        ref_job_t *J = &jobs[w];
+        J->target = target;
+        J->draft = draft;
+        J->dtype = dtype;
+        J->tokens = tokens;
+        J->u_accept = u_accept;
+        J->u_resample = u_resample;
+        J->temperature = temperature;
+        J->B = B;
+        J->k = k;
+        J->V = V;
+        J->out_tokens = out_tokens;
+        J->out_num_accepted = out_num_accepted;
+        J->trace = trace;
+        J->b0 = B * w / nthreads;
+        J->b1 = B * (w + 1) / nthreads;
+    }
+    int status = REF_OK;
+    if (nthreads == 1) {
+        ref_worker(&jobs[0]);
+        status = jobs[0].status;
+    } else {
+        int started = 0;
+        for (int w = 0; w < nthreads; ++w) {
+            if (pthread_create(&th[w], NULL, ref_worker, &jobs[w]) != 0)
+                break;
+            ++started;
+        }
+        for (int w = 0; w < started; ++w)
+            pthread_join(th[w], NULL);
+        for (int w = started; w < nthreads; ++w)
+            ref_worker(&jobs[w]);
+        for (int w = 0; w < nthreads; ++w)
+            if (jobs[w].status != REF_OK)
+                status = jobs[w].status;
+    }
+    free(jobs);
+    free(th);
+    return status;
+}
+
+int spec_verify_ref(const void *target, const void *draft, int dtype,
+                    const int32_t *tokens, const double *u_accept,
+                    const double *u_resample, const double *temperature,
+                    int64_t B, int64_t k, int64_t V,
+                    int32_t *out_tokens, int32_t *out_num_accepted, double *trace)
+{
+    return spec_verify_ref_mt(target, draft, dtype, tokens, u_accept, u_resample,
+                              temperature, B, k, V, out_tokens, out_num_accepted,
+                              trace, 1);
+}
+
+/*
+ * Intermediate probabilities P = p_i(g_i) and Q = q_i(g_i) at every draft
+ * position (not only the tested ones), out[B,k,2].  Greedy sequences and
+ * error rows get NaN.
+ */
+int spec_ref_probs(const void *target, const void *draft, int dtype,
+                   const int32_t *tokens, const double *temperature,
+                   int64_t B, int64_t k, int64_t V, double *out)
+{
+    if (!target || !draft || !tokens || !temperature || !out || V < 2 || k < 1)
+        return REF_EINVAL;
+    double *buf = (double *)malloc(3 * (size_t)V * sizeof(double));
+    if (!buf)
+        return REF_ENOMEM;
+    double *l = buf, *p = buf + V, *q = buf + 2 * V;
+    for (int64_t b = 0; b < B; ++b) {
+        double T = temperature[b];
+        for (int64_t i = 0; i < k; ++i) {
+            double *o = out + (b * k + i) * 2;
+            o[0] = o[1] = NAN;
+            int32_t g = tokens[b * k + i];
+            if (!(T > 0) || isinf(T) || g < 0 || g >= V)
+                continue;
+            ref_load_row(target, dtype, (size_t)(b * (k + 1) + i), V, l);
+            if (ref_row_invalid(l, V))
+                continue;
+            spec_ref_softmax(l, V, T, p);
+            ref_load_row(draft, dtype, (size_t)(b * k + i), V, l);
+            if (ref_row_invalid(l, V))
+                continue;
+            spec_ref_softmax(l, V, T, q);
+            o[0] = p[g];
+            o[1] = q[g];
+        }
+    }
+    free(buf);
+    return REF_OK;
+}
