@@ -1,0 +1,364 @@
+"""Benchmark of batched speculative-sampling verification on GB300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                    [--config 4]
+
+A step is one verification call over one batch of the workload (all accept
+tests, first-rejection scans and correction / bonus draws of every sequence).
+The default workload is the largest one by bytes: B=256 sequences, k=8 draft
+positions, V=151936, fp32 logits, per-sequence temperature from
+{0, 0.5, 1.0, 1.3} (2.6 GB of logits per step, far larger than the 129 MB L2,
+so no L2 flush is needed between steps).  Inputs are synthetic (seeded numpy,
+see speculative_decoding_verification_65_gb300/synth.py).
+
+Metric: verified draft positions per second (B*k / step time), summed over
+ranks.  Under torchrun every rank verifies its own batch of B sequences
+(weak scaling: sequences are independent, so there is no collective on the
+data path; one scalar all-reduce takes the max time over ranks).
+
+Prints one JSON line on rank 0.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+
+METRIC = "verified draft positions/sec"
+UNIT = "positions/s"
+KERNEL_SRC = os.path.join(ROOT, "speculative_decoding_verification_65_gb300", "csrc",
+                          "spec_verify.cu")
+
+
+def dist_env():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            return json.load(f), "measured"
+    except (OSError, ValueError):
+        return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0}, "fallback"
+
+
+def kernel_source_hash() -> str:
+    with open(KERNEL_SRC, "rb") as f:
+        return hashlib.sha256(f.read()).hexdigest()[:16]
+
+
+def recorded_traffic(workload: str):
+    """DRAM bytes per launch from an ncu capture, if it was taken on the
+    current kernel source (profiles/traffic.json)."""
+    try:
+        with open(os.path.join(ROOT, "profiles", "traffic.json")) as f:
+            rec = json.load(f)
+    except (OSError, ValueError):
+        return None
+    ent = rec.get(workload)
+    if not ent or ent.get("kernel_sha") != kernel_source_hash():
+        return None
+    return ent.get("dram_bytes_per_launch")
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle samples while the timed region runs."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = None
+
+    def __enter__(self):
+        fd, self.path = tempfile.mkstemp(suffix=".csv")
+        os.close(fd)
+        try:
+            self.out = open(self.path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=self.out, stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+            self.out.close()
+
+    def summary(self):
+        if self.proc is None or not self.path:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        with open(self.path) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) < 9:
+                    continue
+                try:
+                    sm.append(float(parts[1]))
+                    smax.append(float(parts[2]))
+                except ValueError:
+                    continue
+                for name, val in zip(names, parts[5:9]):
+                    if val.lower() == "active":
+                        reasons.add(name)
+        os.unlink(self.path)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax),
+                "samples": len(sm), "reasons": sorted(reasons)}
+
+
+def make_workload(cfg: int, rank: int, batch=None):
+    from speculative_decoding_verification_65_gb300 import synth
+    return synth.make_config(cfg, B=batch, seed_offset=100 * rank)
+
+
+def time_oracle(case, budget_s: float, threads: int):
+    """Oracle throughput on a bounded sample: chunks of `threads` sequences
+    until the time budget is spent or the batch is done."""
+    import oracle
+    done, t_used = 0, 0.0
+    chunk = max(threads, 1)
+    while done < case.B and t_used < budget_s:
+        idx = np.arange(done, min(case.B, done + chunk))
+        sub = case.subset(idx)
+        t0 = time.perf_counter()
+        oracle.verify(sub.target, sub.draft, sub.tokens, sub.u_accept, sub.u_resample,
+                      sub.temperature, nthreads=threads, want_trace=False)
+        t_used += time.perf_counter() - t0
+        done += len(idx)
+    return done * case.k / t_used, done, t_used
+
+
+def host_cores() -> int:
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count() or 1
+
+
+def run_reference(args):
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return
+    from speculative_decoding_verification_65_gb300 import synth
+    case = make_workload(args.config, 0, args.batch)
+    cores = host_cores()
+    # each step verifies a bounded sample of the batch on all host cores
+    per_step = min(case.B, max(cores, 16))
+    import oracle
+    oracle.build()
+    sub = case.subset(np.arange(per_step))
+    for _ in range(args.warmup):
+        oracle.verify(sub.target, sub.draft, sub.tokens, sub.u_accept, sub.u_resample,
+                      sub.temperature, nthreads=cores, want_trace=False)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        oracle.verify(sub.target, sub.draft, sub.tokens, sub.u_accept, sub.u_resample,
+                      sub.temperature, nthreads=cores, want_trace=False)
+    dt = time.perf_counter() - t0
+    value = per_step * case.k * args.steps / dt
+    sample = f"first {per_step} of {case.B} sequences per step, {synth.CONFIG_NAMES[args.config]}"
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT,
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": dt / args.steps * 1e3, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": synth.CONFIG_NAMES[args.config], "B": per_step, "k": case.k,
+                   "V": case.V, "input_dtype": case.dtype,
+                   "what": "fp64 CPU oracle (plain C, threads over sequences)"},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def run_ours(args):
+    import torch
+
+    import speculative_decoding_verification_65_gb300 as sv
+    from speculative_decoding_verification_65_gb300 import synth
+
+    rank, world, local = dist_env()
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+
+    case = make_workload(args.config, rank, args.batch)
+    B, k, V = case.B, case.k, case.V
+    d = sv.to_device(case, dev)
+    dt_code = sv.SPEC_F32 if case.dtype == synth.F32 else sv.SPEC_BF16
+    stream = torch.cuda.current_stream(dev)
+    ws = sv.workspace(B, k, V, dt_code, dev, stream)
+    out_t = torch.empty((B, k + 1), dtype=torch.int32, device=dev)
+    out_n = torch.empty((B,), dtype=torch.int32, device=dev)
+    alg_bytes = synth.algorithmic_bytes(case)
+
+    def step():
+        sv.spec_verify(**d, out_tokens=out_t, out_num_accepted=out_n, ws=ws, stream=stream)
+
+    def barrier():
+        if world > 1:
+            import torch.distributed as dist
+            dist.barrier()
+
+    for _ in range(max(args.warmup, 3)):
+        step()
+    torch.cuda.synchronize(dev)
+    if sv.spec_verify_read_status(ws) != sv.SPEC_DEV_OK:
+        raise RuntimeError("device status nonzero after warm-up")
+
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    barrier()
+    torch.cuda.synchronize(dev)
+    with ClockSampler(local) as clk:
+        t0.record(stream)
+        for i in range(args.steps):
+            starts[i].record(stream)
+            step()
+            ends[i].record(stream)
+        t1.record(stream)
+        torch.cuda.synchronize(dev)
+    barrier()
+    total_ms = t0.elapsed_time(t1)
+    kern_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
+    if world > 1:
+        import torch.distributed as dist
+        tt = torch.tensor([total_ms], device=dev)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        total_ms = float(tt.item())
+    ms_per_step = total_ms / args.steps
+    value = world * B * k * args.steps / (total_ms / 1e3)
+    status = sv.spec_verify_read_status(ws)
+
+    # end to end through the public API on host buffers (pinned), every step
+    # copies the inputs in and the results out
+    pin = lambda a: torch.from_numpy(a).pin_memory()
+    if case.dtype == synth.BF16:
+        h_t = pin(case.target.view(np.int16)).view(torch.bfloat16)
+        h_d = pin(case.draft.view(np.int16)).view(torch.bfloat16)
+    else:
+        h_t, h_d = pin(case.target), pin(case.draft)
+    h_g, h_ua, h_ur, h_T = pin(case.tokens), pin(case.u_accept), pin(case.u_resample), \
+        pin(case.temperature)
+    h_ot = torch.empty((B, k + 1), dtype=torch.int32).pin_memory()
+    h_on = torch.empty((B,), dtype=torch.int32).pin_memory()
+    del d
+    torch.cuda.empty_cache()
+    arena = torch.empty(sv.spec_verify_host_arena_size(B, k, V, dt_code), dtype=torch.uint8,
+                        device=dev)
+    e2e_steps = max(1, min(args.steps, 10))
+    sv.spec_verify_host(h_t, h_d, h_g, h_ua, h_ur, h_T, arena, h_ot, h_on, stream=stream)
+    barrier()
+    e0 = time.perf_counter()
+    for _ in range(e2e_steps):
+        sv.spec_verify_host(h_t, h_d, h_g, h_ua, h_ur, h_T, arena, h_ot, h_on, stream=stream)
+    e2e_s = time.perf_counter() - e0
+    if world > 1:
+        import torch.distributed as dist
+        tt = torch.tensor([e2e_s], device=dev)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        e2e_s = float(tt.item())
+    e2e_value = world * B * k * e2e_steps / e2e_s
+    h2d = sum(int(x.numel() * x.element_size()) for x in (h_t, h_d, h_g, h_ua, h_ur, h_T))
+    d2h = int(h_ot.numel() * 4 + h_on.numel() * 4)
+
+    if rank != 0:
+        if world > 1:
+            import torch.distributed as dist
+            dist.destroy_process_group()
+        return
+
+    peaks, peak_src = measured_peaks()
+    kern_avg_s = statistics.mean(kern_ms) / 1e3
+    achieved = alg_bytes / kern_avg_s / 1e9
+    peak = float(peaks.get("hbm_gbs", 6800.0))
+    workload = synth.CONFIG_NAMES[args.config] if args.batch is None else case.name
+    cpu = None
+    if world == 1 and not args.no_cpu_baseline:
+        cores = host_cores()
+        v, n_seq, used = time_oracle(case, args.cpu_budget, cores)
+        cpu = {"value": v, "unit": UNIT, "cores": cores, "kind": "oracle",
+               "sample": f"{n_seq} of {B} sequences of {workload}, {used:.1f} s on {cores} threads"}
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": max(args.warmup, 3), "ms_per_step": ms_per_step,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "f32", "data": "synthetic",
+        "config": {"workload": workload, "B_per_gpu": B, "k": k, "V": V,
+                   "input_dtype": case.dtype, "global_batch": B * world,
+                   "algorithmic_bytes_per_step": alg_bytes,
+                   "l2": "inputs larger than L2 (no flush)", "parallelism": f"dp{world}"},
+        "gpu_launches": args.steps,
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                     "frac": achieved / peak, "traffic": recorded_traffic(workload),
+                     "peak_source": f"{peak_src} copy bandwidth (MEASURED_PEAKS.json hbm_gbs)"
+                     if peak_src == "measured" else "fallback 6.8 TB/s",
+                     "kernel_ms_avg": kern_avg_s * 1e3, "kernel_ms_min": min(kern_ms),
+                     "frac_of_nominal_8TBs": achieved / 8000.0},
+        "clocks": clk.summary(),
+        "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h, "steps": e2e_steps},
+        "cpu_baseline": cpu,
+        "device_status": status,
+    }
+    print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--config", type=int, default=4, choices=[1, 2, 3, 4, 5])
+    ap.add_argument("--batch", type=int, default=None,
+                    help="smaller batch of the same recipe (profiling captures only)")
+    ap.add_argument("--cpu-budget", type=float, default=10.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

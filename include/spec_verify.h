@@ -1,0 +1,171 @@
+/*
+ * spec_verify.h -- C ABI of the GB300 speculative-sampling verification library
+ * (libspecverify.so).
+ *
+ * The operation (one round of speculative decoding's verification step, for a
+ * batch of B independent sequences):
+ *   - p_i = softmax(t_i / T) and q_i = softmax(d_i / T) with the same per-
+ *     sequence temperature T for target and draft ("Speculative Decoding and
+ *     the Art of Fast LLM Inference", "Why It Stays Exact", key limitation on
+ *     identical sampling parameters);
+ *   - left to right, draft token g_i is accepted when u_accept[b,i] is strictly
+ *     below p_i(g_i)/q_i(g_i) (always when p_i(g_i) >= q_i(g_i)); the first
+ *     rejection ends the scan (same page, "The Algorithm, Step by Step";
+ *     thelatentsource "speculative-decoding-llm-speed", "The correction that
+ *     keeps the target in charge", the accept_token snippet);
+ *   - at the rejected position j one correction token is drawn from
+ *     norm(max(0, p_j - q_j)) (second page, equation r(x)); if all k drafts are
+ *     accepted a bonus token is drawn from p_{k+1} (first page, step "Bonus
+ *     token");
+ *   - a draw is inverse-CDF with u_resample[b]: the smallest token x whose
+ *     running mass C(x) exceeds u * R, R the total mass (the pages say
+ *     "sample"; this is the plain reading);
+ *   - T == 0 is greedy mode: g_i is accepted while it equals argmax t_i, and the
+ *     correction or bonus is the target argmax ("How does speculative decoding
+ *     work, why is it lossless, and how much does it speed things up?",
+ *     techaiinterview, "Deep dive: correctness and speedup").  Argmax ties go to
+ *     the lowest index.  Draft logits are not read for greedy sequences.
+ *
+ * Conventions shared by every entry point:
+ *   - Sizes are int32; B >= 0 (B == 0 is a no-op), 1 <= k <= SPEC_MAX_K,
+ *     2 <= V <= SPEC_MAX_V.
+ *   - Logits are row-major; target [B, k+1, V], draft [B, k, V]; one dtype per
+ *     call (SPEC_F32 = IEEE binary32, SPEC_BF16 = bfloat16 bit patterns).
+ *     Their base addresses must be 16-byte aligned; V is arbitrary.
+ *   - Device entry points take device pointers and a cudaStream_t passed as
+ *     void* (NULL = the legacy default stream).  They launch on that stream and
+ *     return without synchronising; results are valid once the stream has
+ *     reached that point.
+ *   - The library allocates no memory and keeps no per-call global state.  The
+ *     caller owns every buffer.  Inputs are read-only; outputs are overwritten.
+ *   - The return value reports host-checkable errors only (spec_status_t).
+ *     Data-dependent problems are reported per sequence on the device:
+ *     out_num_accepted[b] = -1 and out_tokens[b, :] = -1 when T is NaN,
+ *     negative, infinite or positive below FLT_MIN; a draft token lies outside
+ *     [0, V); a logit the call reads is NaN or +inf; such a row is entirely
+ *     -inf; or the draft probability of a draft token the scan reaches is zero
+ *     (the accept_token snippet's ValueError).  Nothing traps and nothing
+ *     prints on the device.
+ */
+#ifndef SPEC_VERIFY_H
+#define SPEC_VERIFY_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define SPEC_VERIFY_ABI_VERSION 1
+#define SPEC_MAX_K 32
+#define SPEC_MAX_V (1 << 20)
+
+typedef enum { SPEC_F32 = 0, SPEC_BF16 = 1 } spec_dtype_t;
+
+typedef enum {
+    SPEC_OK = 0,
+    SPEC_EINVAL = 1,   /* a null pointer, a size out of range, misalignment, unknown dtype */
+    SPEC_ECUDA = 2,    /* a CUDA runtime call or the launch failed */
+    SPEC_ENOSPACE = 3  /* workspace (or arena) smaller than the size query returned */
+} spec_status_t;
+
+/* Device-side status words written into the workspace (read them with
+ * spec_verify_read_status).  Nonzero means the kernel stopped early: the
+ * outputs of that call are undefined and the workspace must be zeroed again
+ * (spec_verify_workspace_reset) before the next call. */
+#define SPEC_DEV_OK 0
+#define SPEC_DEV_WAIT_TIMEOUT 1
+
+/* ABI version of the loaded library (SPEC_VERIFY_ABI_VERSION). */
+int32_t spec_verify_abi_version(void);
+
+/* Human-readable name of a spec_status_t value (static string). */
+const char *spec_verify_strerror(int32_t status);
+
+/*
+ * Bytes of device workspace one spec_verify call needs for these sizes (a
+ * small header, one counter per sequence, 16 bytes per streamed tile).
+ * Returns 0 for sizes out of range.  Host-only; needs no GPU.
+ */
+size_t spec_verify_workspace_size(int32_t B, int32_t k, int32_t V, int32_t dtype);
+
+/*
+ * Zero a workspace on `stream` (cudaMemsetAsync).  Needed once after
+ * allocation and after any call whose device status was nonzero; correct
+ * calls leave the workspace zeroed themselves.
+ */
+int32_t spec_verify_workspace_reset(void *workspace, size_t workspace_bytes, void *stream);
+
+/*
+ * The verification step (see the file comment for the operation).
+ *   target_logits    device, [B, k+1, V] of dtype; t_1..t_k then the bonus row t_{k+1}
+ *   draft_logits     device, [B, k, V] of dtype; never read for sequences with T == 0
+ *   draft_tokens     device int32 [B, k]: g_1..g_k
+ *   u_accept         device float32 [B, k], each in [0, 1): accept test i uses u_accept[b, i]
+ *   u_resample       device float32 [B] in [0, 1): the one correction or bonus draw
+ *   temperature      device float32 [B] >= 0; 0 selects greedy mode
+ *   out_tokens       device int32 [B, k+1]: accepted prefix, then the correction or
+ *                    bonus token, then -1 padding (all -1 on a sequence error)
+ *   out_num_accepted device int32 [B]: accepted drafts in [0, k]; -1 = sequence error.
+ *                    The sequence emits out_num_accepted[b] + 1 tokens.
+ *   workspace        device, >= spec_verify_workspace_size(...) bytes, 16-byte aligned,
+ *                    zeroed once before first use (spec_verify_workspace_reset); calls
+ *                    leave it zeroed.  Two calls in flight at once must not share one.
+ *   stream           cudaStream_t as void*.
+ * Returns SPEC_OK once the kernel is launched; errors are listed above.
+ */
+int32_t spec_verify(const void *target_logits, const void *draft_logits,
+                    const int32_t *draft_tokens, const float *u_accept,
+                    const float *u_resample, const float *temperature,
+                    int32_t *out_tokens, int32_t *out_num_accepted,
+                    int32_t B, int32_t k, int32_t V, int32_t dtype,
+                    void *workspace, size_t workspace_bytes, void *stream);
+
+/*
+ * spec_verify plus the intermediate probabilities P = p_i(g_i) and
+ * Q = q_i(g_i) for every draft position, written to out_probs (device float32
+ * [B, k, 2]; NaN for greedy and error sequences).  Same arguments otherwise;
+ * used to check intermediates against an fp64 reference.
+ */
+int32_t spec_verify_probs(const void *target_logits, const void *draft_logits,
+                          const int32_t *draft_tokens, const float *u_accept,
+                          const float *u_resample, const float *temperature,
+                          int32_t *out_tokens, int32_t *out_num_accepted, float *out_probs,
+                          int32_t B, int32_t k, int32_t V, int32_t dtype,
+                          void *workspace, size_t workspace_bytes, void *stream);
+
+/*
+ * Copy the workspace's device status word to *status (host) and synchronise
+ * `stream`.  SPEC_DEV_OK (0) after a complete call.
+ */
+int32_t spec_verify_read_status(const void *workspace, int32_t *status, void *stream);
+
+/*
+ * Bytes of caller-owned device arena spec_verify_host needs: device copies of
+ * all inputs and outputs plus the workspace, each 256-byte aligned.
+ */
+size_t spec_verify_host_arena_size(int32_t B, int32_t k, int32_t V, int32_t dtype);
+
+/*
+ * End-to-end variant on HOST buffers: copies the inputs host->device into the
+ * caller's device arena (one cudaMemcpyAsync per buffer), runs spec_verify,
+ * and copies out_tokens / out_num_accepted back to the host buffers, all on
+ * `stream`; synchronises the stream before returning so the host outputs are
+ * ready.  Pinned host memory makes the copies asynchronous DMA.  The arena
+ * must be >= spec_verify_host_arena_size(...) bytes and 256-byte aligned; its
+ * workspace part is zeroed by this call.  Host pointers follow the device
+ * entry point's shapes.
+ */
+int32_t spec_verify_host(const void *target_logits, const void *draft_logits,
+                         const int32_t *draft_tokens, const float *u_accept,
+                         const float *u_resample, const float *temperature,
+                         int32_t *out_tokens, int32_t *out_num_accepted,
+                         int32_t B, int32_t k, int32_t V, int32_t dtype,
+                         void *device_arena, size_t arena_bytes, void *stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SPEC_VERIFY_H */

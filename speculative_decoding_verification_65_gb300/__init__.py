@@ -1,2 +1,267 @@
-"""GB300-native batched speculative-sampling verification (placeholder; the
-binding to the CUDA library is added with the kernels)."""
+"""GB300-native batched speculative-sampling verification.
+
+Thin Python binding over the C ABI of ``libspecverify.so`` (declared in
+``include/spec_verify.h``).  Every function here only checks and marshals
+arguments (shapes, dtypes, device pointers, the current CUDA stream) and calls
+the function of the same name in the library; all arithmetic runs in the CUDA
+kernels.  PyTorch is used for device memory and streams only.
+
+If the library has not been built the first call raises: there is no CPU
+fallback.  Build it with ``__graft_entry__.build()`` (or
+``python -m speculative_decoding_verification_65_gb300.build``).
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+SPEC_F32 = 0
+SPEC_BF16 = 1
+SPEC_OK = 0
+SPEC_EINVAL = 1
+SPEC_ECUDA = 2
+SPEC_ENOSPACE = 3
+SPEC_DEV_OK = 0
+SPEC_DEV_WAIT_TIMEOUT = 1
+SPEC_MAX_K = 32
+SPEC_MAX_V = 1 << 20
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libspecverify.so")
+_lib = None
+_lock = threading.Lock()
+
+
+class SpecVerifyError(RuntimeError):
+    pass
+
+
+def library():
+    """The loaded ctypes library (raises if it was never built)."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        if not os.path.exists(LIB_PATH):
+            raise SpecVerifyError(
+                f"{LIB_PATH} is missing: build the CUDA library first "
+                "(__graft_entry__.build()); there is no fallback")
+        lib = ctypes.CDLL(LIB_PATH)
+        vp, i32, sz = ctypes.c_void_p, ctypes.c_int32, ctypes.c_size_t
+        lib.spec_verify_abi_version.restype = i32
+        lib.spec_verify_abi_version.argtypes = []
+        lib.spec_verify_strerror.restype = ctypes.c_char_p
+        lib.spec_verify_strerror.argtypes = [i32]
+        lib.spec_verify_workspace_size.restype = sz
+        lib.spec_verify_workspace_size.argtypes = [i32, i32, i32, i32]
+        lib.spec_verify_workspace_reset.restype = i32
+        lib.spec_verify_workspace_reset.argtypes = [vp, sz, vp]
+        lib.spec_verify.restype = i32
+        lib.spec_verify.argtypes = [vp] * 8 + [i32] * 4 + [vp, sz, vp]
+        lib.spec_verify_probs.restype = i32
+        lib.spec_verify_probs.argtypes = [vp] * 9 + [i32] * 4 + [vp, sz, vp]
+        lib.spec_verify_read_status.restype = i32
+        lib.spec_verify_read_status.argtypes = [vp, vp, vp]
+        lib.spec_verify_host_arena_size.restype = sz
+        lib.spec_verify_host_arena_size.argtypes = [i32, i32, i32, i32]
+        lib.spec_verify_host.restype = i32
+        lib.spec_verify_host.argtypes = [vp] * 8 + [i32] * 4 + [vp, sz, vp]
+        _lib = lib
+        return lib
+
+
+def _check(rc: int, what: str):
+    if rc != SPEC_OK:
+        msg = library().spec_verify_strerror(rc).decode()
+        raise SpecVerifyError(f"{what} failed: {msg} (status {rc})")
+
+
+def _torch():
+    import torch
+    return torch
+
+
+def _dtype_code(t) -> int:
+    torch = _torch()
+    if t.dtype == torch.float32:
+        return SPEC_F32
+    if t.dtype == torch.bfloat16:
+        return SPEC_BF16
+    raise TypeError(f"logits must be float32 or bfloat16, got {t.dtype}")
+
+
+def _stream_handle(stream, device):
+    torch = _torch()
+    if stream is None:
+        stream = torch.cuda.current_stream(device)
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def _ptr(t):
+    return ctypes.c_void_p(t.data_ptr()) if t is not None else None
+
+
+def spec_verify_abi_version() -> int:
+    return int(library().spec_verify_abi_version())
+
+
+def spec_verify_workspace_size(B: int, k: int, V: int, dtype: int) -> int:
+    return int(library().spec_verify_workspace_size(B, k, V, dtype))
+
+
+def spec_verify_host_arena_size(B: int, k: int, V: int, dtype: int) -> int:
+    return int(library().spec_verify_host_arena_size(B, k, V, dtype))
+
+
+_ws_cache = {}
+
+
+def workspace(B: int, k: int, V: int, dtype: int, device=None, stream=None):
+    """A zeroed workspace tensor big enough for these sizes, cached per
+    (device, stream): calls in flight on one stream run in order, so they can
+    share it."""
+    torch = _torch()
+    device = torch.device(device if device is not None else "cuda")
+    if device.index is None:
+        device = torch.device("cuda", torch.cuda.current_device())
+    s = stream if stream is not None else torch.cuda.current_stream(device)
+    need = spec_verify_workspace_size(B, k, V, dtype)
+    if need == 0:
+        raise ValueError(f"sizes out of range: B={B} k={k} V={V} dtype={dtype}")
+    key = (device.index, s.cuda_stream)
+    ws = _ws_cache.get(key)
+    if ws is None or ws.numel() < need:
+        with torch.cuda.stream(s):
+            ws = torch.zeros(max(need, 1 << 20), dtype=torch.uint8, device=device)
+        _ws_cache[key] = ws
+    return ws
+
+
+def spec_verify_workspace_reset(ws, stream=None):
+    _check(library().spec_verify_workspace_reset(_ptr(ws), ws.numel(),
+                                                 _stream_handle(stream, ws.device)),
+           "spec_verify_workspace_reset")
+
+
+def spec_verify_read_status(ws, stream=None) -> int:
+    st = ctypes.c_int32(-99)
+    _check(library().spec_verify_read_status(_ptr(ws), ctypes.byref(st),
+                                             _stream_handle(stream, ws.device)),
+           "spec_verify_read_status")
+    return int(st.value)
+
+
+def _marshal(target, draft, tokens, u_accept, u_resample, temperature):
+    torch = _torch()
+    if target.dim() != 3 or draft.dim() != 3:
+        raise ValueError("target must be [B,k+1,V] and draft [B,k,V]")
+    B, k1, V = target.shape
+    k = k1 - 1
+    if tuple(draft.shape) != (B, k, V):
+        raise ValueError(f"draft shape {tuple(draft.shape)} != {(B, k, V)}")
+    dt = _dtype_code(target)
+    if draft.dtype != target.dtype:
+        raise TypeError("target and draft must share a dtype")
+    for name, t, shape, dtype in (("draft_tokens", tokens, (B, k), torch.int32),
+                                  ("u_accept", u_accept, (B, k), torch.float32),
+                                  ("u_resample", u_resample, (B,), torch.float32),
+                                  ("temperature", temperature, (B,), torch.float32)):
+        if tuple(t.shape) != shape or t.dtype != dtype:
+            raise ValueError(f"{name} must be {dtype} {shape}, got {t.dtype} {tuple(t.shape)}")
+    for t in (target, draft, tokens, u_accept, u_resample, temperature):
+        if not t.is_cuda or not t.is_contiguous():
+            raise ValueError("all inputs must be contiguous CUDA tensors")
+        if t.device != target.device:
+            raise ValueError("all inputs must be on one device")
+    return B, k, V, dt
+
+
+def spec_verify(target, draft, tokens, u_accept, u_resample, temperature,
+                out_tokens=None, out_num_accepted=None, ws=None, stream=None):
+    """Run the verification step on the current (or given) stream.
+
+    target [B,k+1,V] and draft [B,k,V]: float32 or bfloat16 CUDA tensors;
+    tokens int32 [B,k]; u_accept float32 [B,k]; u_resample, temperature
+    float32 [B].  Returns (out_tokens int32 [B,k+1], out_num_accepted int32
+    [B]); asynchronous like any CUDA op."""
+    torch = _torch()
+    B, k, V, dt = _marshal(target, draft, tokens, u_accept, u_resample, temperature)
+    dev = target.device
+    if out_tokens is None:
+        out_tokens = torch.empty((B, k + 1), dtype=torch.int32, device=dev)
+    if out_num_accepted is None:
+        out_num_accepted = torch.empty((B,), dtype=torch.int32, device=dev)
+    if ws is None:
+        ws = workspace(B, k, V, dt, dev, stream)
+    rc = library().spec_verify(_ptr(target), _ptr(draft), _ptr(tokens), _ptr(u_accept),
+                               _ptr(u_resample), _ptr(temperature), _ptr(out_tokens),
+                               _ptr(out_num_accepted), B, k, V, dt, _ptr(ws), ws.numel(),
+                               _stream_handle(stream, dev))
+    _check(rc, "spec_verify")
+    return out_tokens, out_num_accepted
+
+
+def spec_verify_probs(target, draft, tokens, u_accept, u_resample, temperature,
+                      ws=None, stream=None):
+    """spec_verify plus the fp32 intermediates P = p_i(g_i), Q = q_i(g_i):
+    returns (out_tokens, out_num_accepted, probs [B,k,2])."""
+    torch = _torch()
+    B, k, V, dt = _marshal(target, draft, tokens, u_accept, u_resample, temperature)
+    dev = target.device
+    out_tokens = torch.empty((B, k + 1), dtype=torch.int32, device=dev)
+    out_n = torch.empty((B,), dtype=torch.int32, device=dev)
+    probs = torch.empty((B, k, 2), dtype=torch.float32, device=dev)
+    if ws is None:
+        ws = workspace(B, k, V, dt, dev, stream)
+    rc = library().spec_verify_probs(_ptr(target), _ptr(draft), _ptr(tokens), _ptr(u_accept),
+                                     _ptr(u_resample), _ptr(temperature), _ptr(out_tokens),
+                                     _ptr(out_n), _ptr(probs), B, k, V, dt, _ptr(ws),
+                                     ws.numel(), _stream_handle(stream, dev))
+    _check(rc, "spec_verify_probs")
+    return out_tokens, out_n, probs
+
+
+def spec_verify_host(target, draft, tokens, u_accept, u_resample, temperature,
+                     arena, out_tokens=None, out_num_accepted=None, stream=None):
+    """End-to-end call on HOST tensors (CPU, ideally pinned): the library copies
+    the inputs into the device `arena` (a CUDA uint8 tensor of at least
+    spec_verify_host_arena_size bytes), verifies, copies the outputs back and
+    synchronises.  Returns host (out_tokens, out_num_accepted)."""
+    torch = _torch()
+    if target.is_cuda:
+        raise ValueError("spec_verify_host takes host tensors")
+    B, k1, V = target.shape
+    k = k1 - 1
+    dt = _dtype_code(target)
+    if out_tokens is None:
+        out_tokens = torch.empty((B, k + 1), dtype=torch.int32, pin_memory=True)
+    if out_num_accepted is None:
+        out_num_accepted = torch.empty((B,), dtype=torch.int32, pin_memory=True)
+    for t in (target, draft, tokens, u_accept, u_resample, temperature):
+        if t.is_cuda or not t.is_contiguous():
+            raise ValueError("host inputs must be contiguous CPU tensors")
+    rc = library().spec_verify_host(_ptr(target), _ptr(draft), _ptr(tokens), _ptr(u_accept),
+                                    _ptr(u_resample), _ptr(temperature), _ptr(out_tokens),
+                                    _ptr(out_num_accepted), B, k, V, dt, _ptr(arena),
+                                    arena.numel(), _stream_handle(stream, arena.device))
+    _check(rc, "spec_verify_host")
+    return out_tokens, out_num_accepted
+
+
+def to_device(case, device="cuda"):
+    """Copy a synth.Case's host arrays to device tensors (bf16 bit patterns
+    become torch.bfloat16)."""
+    import numpy as np
+    torch = _torch()
+
+    def logits(a):
+        if a.dtype == np.uint16:
+            return torch.from_numpy(a.view(np.int16)).view(torch.bfloat16).to(device)
+        return torch.from_numpy(a).to(device)
+
+    return dict(target=logits(case.target), draft=logits(case.draft),
+                tokens=torch.from_numpy(case.tokens).to(device),
+                u_accept=torch.from_numpy(case.u_accept).to(device),
+                u_resample=torch.from_numpy(case.u_resample).to(device),
+                temperature=torch.from_numpy(case.temperature).to(device))

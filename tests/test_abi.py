@@ -1,0 +1,126 @@
+"""The C ABI library loads, exports every symbol include/*.h declares, and its
+host-side checks behave as documented.  No GPU needed: every call here
+returns before any CUDA runtime call."""
+import ctypes
+import glob
+import os
+import re
+
+import pytest
+
+from tests.conftest import ROOT
+
+import speculative_decoding_verification_65_gb300 as sv
+from speculative_decoding_verification_65_gb300 import build as sv_build
+
+
+@pytest.fixture(scope="module")
+def lib():
+    sv_build.build()
+    return sv.library()
+
+
+def declared_functions():
+    names = []
+    for h in glob.glob(os.path.join(ROOT, "include", "*.h")):
+        text = open(h).read()
+        text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+        names += re.findall(r"^[A-Za-z_][\w \t\*]*?\b(spec_\w+)\s*\(", text, flags=re.M)
+    return sorted(set(names))
+
+
+def test_header_declares_the_entry_points():
+    names = declared_functions()
+    for must in ("spec_verify", "spec_verify_workspace_size", "spec_verify_host",
+                 "spec_verify_probs", "spec_verify_read_status", "spec_verify_workspace_reset"):
+        assert must in names
+
+
+def test_every_declared_symbol_is_exported(lib):
+    raw = ctypes.CDLL(sv.LIB_PATH)
+    missing = [n for n in declared_functions() if not hasattr(raw, n)]
+    assert not missing, missing
+
+
+def test_abi_version_and_strerror(lib):
+    assert sv.spec_verify_abi_version() == 1
+    for code in (0, 1, 2, 3):
+        assert lib.spec_verify_strerror(code)
+    assert b"unknown" in lib.spec_verify_strerror(99)
+
+
+@pytest.mark.parametrize("B,k,V,dt,ok", [
+    (4, 4, 1024, 0, True), (1024, 4, 128256, 1, True), (0, 1, 2, 0, True),
+    (1, 32, 2, 1, True), (1, 0, 10, 0, False), (1, 33, 10, 0, False), (1, 1, 1, 0, False),
+    (1, 1, (1 << 20) + 1, 0, False), (-1, 1, 10, 0, False), (1, 1, 10, 2, False),
+])
+def test_workspace_size(lib, B, k, V, dt, ok):
+    n = sv.spec_verify_workspace_size(B, k, V, dt)
+    if not ok:
+        assert n == 0
+        return
+    tile = 32768 // (4 if dt == 0 else 2)
+    ns = -(-V // tile)
+    assert n == 256 + (-(-B * 4 // 256) * 256) + B * (2 * k + 1) * ns * 16
+
+
+def _call(lib, ptrs, B=1, k=1, V=8, dt=0, wsb=1 << 20):
+    args = [ctypes.c_void_p(p) for p in ptrs[:8]]
+    return lib.spec_verify(*args, B, k, V, dt, ctypes.c_void_p(ptrs[8]), wsb, None)
+
+
+GOOD = [0x10000 * (i + 1) for i in range(9)]
+
+
+def test_zero_batch_is_noop(lib):
+    assert _call(lib, [0] * 9, B=0) == sv.SPEC_OK
+
+
+@pytest.mark.parametrize("which", range(9))
+def test_null_pointer_rejected(lib, which):
+    p = list(GOOD)
+    p[which] = 0
+    assert _call(lib, p) == sv.SPEC_EINVAL
+
+
+@pytest.mark.parametrize("which,off", [(0, 8), (1, 4), (2, 2), (8, 8)])
+def test_misaligned_pointer_rejected(lib, which, off):
+    p = list(GOOD)
+    p[which] += off
+    assert _call(lib, p) == sv.SPEC_EINVAL
+
+
+def test_bad_sizes_rejected(lib):
+    assert _call(lib, GOOD, k=0) == sv.SPEC_EINVAL
+    assert _call(lib, GOOD, V=1) == sv.SPEC_EINVAL
+    assert _call(lib, GOOD, dt=5) == sv.SPEC_EINVAL
+
+
+def test_small_workspace_rejected(lib):
+    need = sv.spec_verify_workspace_size(1, 1, 8, 0)
+    assert _call(lib, GOOD, wsb=need - 1) == sv.SPEC_ENOSPACE
+
+
+def test_probs_needs_output(lib):
+    args = [ctypes.c_void_p(p) for p in GOOD[:8]] + [None]
+    assert lib.spec_verify_probs(*args, 1, 1, 8, 0, ctypes.c_void_p(GOOD[8]), 1 << 20,
+                                 None) == sv.SPEC_EINVAL
+
+
+def test_host_entry_checks(lib):
+    n = sv.spec_verify_host_arena_size(2, 3, 100, 1)
+    assert n > sv.spec_verify_workspace_size(2, 3, 100, 1)
+    args = [ctypes.c_void_p(p) for p in GOOD[:8]]
+    # arena not 256-byte aligned
+    assert lib.spec_verify_host(*args, 2, 3, 100, 1, ctypes.c_void_p(GOOD[8] + 16), n,
+                                None) == sv.SPEC_EINVAL
+    assert lib.spec_verify_host(*args, 2, 3, 100, 1, ctypes.c_void_p(GOOD[8]), n - 1,
+                                None) == sv.SPEC_ENOSPACE
+
+
+def test_binding_fails_loudly_without_library(tmp_path, monkeypatch):
+    import importlib
+    monkeypatch.setattr(sv, "LIB_PATH", str(tmp_path / "missing.so"))
+    monkeypatch.setattr(sv, "_lib", None)
+    with pytest.raises(sv.SpecVerifyError):
+        sv.library()
