@@ -99,3 +99,41 @@ def enumerate_round(run, k: int):
 def softmax64(logits, T: float = 1.0):
     from scipy.special import softmax
     return softmax(np.asarray(logits, np.float64) / T)
+
+
+def enumerate_leaves(run, k: int):
+    """Like enumerate_round, but returns the cells themselves:
+    [(u_accept midpoints list, u_resample midpoint, probability, draw width,
+    emitted tuple)].  Used to replay every cell through another
+    implementation at its midpoint."""
+    leaves = []
+
+    def draw_leaves(pre, prob):
+        out = []
+
+        def tok(u):
+            return tuple(run(pre, u)[1])
+        # breakpoints of the draw as a function of u_resample
+        cells = []
+        acc = 0.0
+        for toks, w in draw_cells(tok):
+            cells.append((toks, acc, acc + w))
+            acc += w
+        for toks, lo, hi in cells:
+            out.append((list(pre), 0.5 * (lo + hi), prob * (hi - lo), hi - lo,
+                        tuple(t for t in toks if t >= 0)))
+        return out
+
+    def rec(i, ua, prob):
+        if i == k:
+            leaves.extend(draw_leaves(ua, prob))
+            return
+        th = threshold(lambda u: run(ua + [u] + [0.0] * (k - i - 1), 0.5)[0] > i)
+        if th < 1.0:
+            pre = ua + [0.5 * (th + 1.0)] + [0.0] * (k - i - 1)
+            leaves.extend(draw_leaves(pre, prob * (1.0 - th)))
+        if th > 0.0:
+            rec(i + 1, ua + [0.5 * th], prob * th)
+
+    rec(0, [], 1.0)
+    return leaves

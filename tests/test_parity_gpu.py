@@ -41,11 +41,24 @@ def run_oracle(case):
                          case.temperature, nthreads=NTHR)
 
 
-def check(case):
+# Exempt (in-band) mismatches allowed per call, as a fraction of its draws.
+# fp32 arithmetic cannot resolve inverse-CDF cells narrower than its rounding,
+# and over ~1e5-token vocabularies the CDF's tail cells are ~1e-6 wide.
+MAX_EXEMPT_PER_DRAW = 0.02
+
+
+def check(case, tag=None):
     g_t, g_n = run_gpu(case)
     r_t, r_n, tr = run_oracle(case)
     pu.check_invariants(case, g_t, g_n)
     rep = pu.compare(case, g_t, g_n, r_t, r_n, tr)
+    out = os.environ.get("PARITY_REPORT_DIR")
+    if out and tag:
+        import json
+        os.makedirs(out, exist_ok=True)
+        with open(os.path.join(out, f"parity_{tag}.json"), "w") as f:
+            json.dump(rep, f)
+    assert rep["exempt"] <= max(1, MAX_EXEMPT_PER_DRAW * rep["draws"]), rep
     return rep, g_t, g_n
 
 
@@ -54,7 +67,7 @@ def check(case):
 @pytest.mark.parametrize("cfg", [1, 2, 3])
 def test_workload_full_oracle(cfg):
     case = synth.make_config(cfg)
-    rep, _, g_n = check(case)
+    rep, _, g_n = check(case, f"cfg{cfg}")
     print(f"cfg{cfg}: {rep['decisions']} decisions, exempt {rep['exempt']}, "
           f"near-band {rep['near_band']}, mean accepted {np.mean(g_n):.3f}")
 
@@ -64,7 +77,7 @@ def test_workload_full_size(cfg):
     """The full-size workloads, as the benchmark launches them: every sequence
     against the oracle (the oracle is threaded over sequences)."""
     case = synth.make_config(cfg)
-    rep, g_t, g_n = check(case)
+    rep, g_t, g_n = check(case, f"cfg{cfg}")
     if cfg == 5:
         cls0 = np.arange(case.B) % 3 == 0  # target == draft bit for bit: always accepted
         assert np.all(g_n[cls0] == case.k)
@@ -212,6 +225,22 @@ def test_deterministic_and_workspace_self_resets():
     assert int(hdr[0]) == 0 and int(hdr[1]) == 0  # tile counter and CTA count re-armed
     seq = ws[256:256 + 4 * case.B].view(torch.int32).cpu()
     assert int(seq.abs().sum()) == 0  # every per-sequence ticket re-armed
+
+
+def test_workspace_reuse_across_shapes():
+    """One workspace serves calls of different shapes back to back: every call
+    leaves it all zero."""
+    a = synth.gauss_case(B=4, k=8, V=20000, dtype="f32", seed=1)
+    b = synth.gauss_case(B=40, k=4, V=20000, dtype="bf16", seed=2)
+    need = max(sv.spec_verify_workspace_size(4, 8, 20000, 0),
+               sv.spec_verify_workspace_size(40, 4, 20000, 1))
+    ws = torch.zeros(need, dtype=torch.uint8, device="cuda")
+    for case in (a, b, a, b):
+        d = sv.to_device(case)
+        t, n = sv.spec_verify(**d, ws=ws)
+        torch.cuda.synchronize()
+        assert int(ws.count_nonzero()) == 0
+        pu.compare(case, t.cpu().numpy(), n.cpu().numpy(), *run_oracle(case))
 
 
 def test_streams_and_workspaces_are_independent():
