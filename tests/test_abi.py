@@ -60,11 +60,12 @@ def test_workspace_size(lib, B, k, V, dt, ok):
         assert n == 0
         return
     tile = 32768 // (4 if dt == 0 else 2)
-    ns = -(-V // tile)          # stats tiles per row
+    ns = -(-V // tile)          # tiles per row
+    nss = -(-ns // 4)           # super-tiles per row (one partial each)
     ds = -(-V // (tile // 2))   # draw tiles per row
     up = lambda x, a: -(-x // a) * a
-    partials = 256 + up(B * 4, 256)
-    chunks = up(partials + B * (2 * k + 1) * ns * 16, 256)
+    jobs = up(256 + B * (2 * k + 1) * nss * 16, 256)
+    chunks = up(jobs + 64 * B, 256)
     assert n == chunks + B * up(ds * 4 * 8, 32) * 4
 
 

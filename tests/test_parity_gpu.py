@@ -209,27 +209,25 @@ def test_intermediate_probabilities(cfg):
 
 # ---------------------------------------------------- determinism, workspace
 
-def test_deterministic_and_workspace_self_resets():
+def test_deterministic_across_calls_and_workspaces():
     case = synth.make_config(2)
     d = sv.to_device(case)
     ws = sv.workspace(case.B, case.k, case.V, sv.SPEC_BF16)
     outs = []
-    for _ in range(3):
+    for i in range(3):
+        if i == 2:  # a workspace full of garbage gives the same answer: nothing carries over
+            ws = torch.randint(0, 255, (ws.numel(),), dtype=torch.uint8, device="cuda")
+            ws[:256] = 0
         t, n = sv.spec_verify(**d, ws=ws)
         outs.append((t.clone(), n.clone()))
     torch.cuda.synchronize()
     for t, n in outs[1:]:
         assert torch.equal(t, outs[0][0]) and torch.equal(n, outs[0][1])
     assert sv.spec_verify_read_status(ws) == sv.SPEC_DEV_OK
-    hdr = ws[:256].view(torch.int32).cpu()
-    assert int(hdr[0]) == 0 and int(hdr[1]) == 0  # tile counter and CTA count re-armed
-    seq = ws[256:256 + 4 * case.B].view(torch.int32).cpu()
-    assert int(seq.abs().sum()) == 0  # every per-sequence ticket re-armed
 
 
 def test_workspace_reuse_across_shapes():
-    """One workspace serves calls of different shapes back to back: every call
-    leaves it all zero."""
+    """One workspace serves calls of different shapes back to back."""
     a = synth.gauss_case(B=4, k=8, V=20000, dtype="f32", seed=1)
     b = synth.gauss_case(B=40, k=4, V=20000, dtype="bf16", seed=2)
     need = max(sv.spec_verify_workspace_size(4, 8, 20000, 0),
@@ -239,7 +237,6 @@ def test_workspace_reuse_across_shapes():
         d = sv.to_device(case)
         t, n = sv.spec_verify(**d, ws=ws)
         torch.cuda.synchronize()
-        assert int(ws.count_nonzero()) == 0
         pu.compare(case, t.cpu().numpy(), n.cpu().numpy(), *run_oracle(case))
 
 
