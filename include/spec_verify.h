@@ -70,10 +70,10 @@ typedef enum {
     SPEC_ENOSPACE = 3  /* workspace (or arena) smaller than the size query returned */
 } spec_status_t;
 
-/* Device-side status words written into the workspace (read them with
- * spec_verify_read_status).  Nonzero means the kernel stopped early: the
- * outputs of that call are undefined and the workspace must be zeroed again
- * (spec_verify_workspace_reset) before the next call. */
+/* Device-side status word, the first 4 bytes of the workspace (read it with
+ * spec_verify_read_status).  Nonzero means a kernel stopped early after a
+ * bounded wait ran out: the outputs of that call are undefined.  Only a
+ * timed-out wait writes it; zero it (spec_verify_workspace_reset) to clear. */
 #define SPEC_DEV_OK 0
 #define SPEC_DEV_WAIT_TIMEOUT 1
 
@@ -84,16 +84,18 @@ int32_t spec_verify_abi_version(void);
 const char *spec_verify_strerror(int32_t status);
 
 /*
- * Bytes of device workspace one spec_verify call needs for these sizes (a
- * small header, one counter per sequence, 16 bytes per streamed tile).
- * Returns 0 for sizes out of range.  Host-only; needs no GPU.
+ * Bytes of device workspace one spec_verify call needs for these sizes: a
+ * 256-byte header (the status word), one 16-byte partial per 128 KB of every
+ * row, a 64-byte draw record per sequence and the draws' inverse-CDF chunk
+ * totals.  Returns 0 for sizes out of range.  Host-only; needs no GPU.
  */
 size_t spec_verify_workspace_size(int32_t B, int32_t k, int32_t V, int32_t dtype);
 
 /*
- * Zero a workspace on `stream` (cudaMemsetAsync).  Needed once after
- * allocation and after any call whose device status was nonzero; correct
- * calls leave the workspace zeroed themselves.
+ * Zero a workspace on `stream` (cudaMemsetAsync).  Only the status word is
+ * read across calls: zero it once after allocation, and again after a call
+ * whose device status was nonzero.  Nothing else in the workspace carries
+ * over from one call to the next.
  */
 int32_t spec_verify_workspace_reset(void *workspace, size_t workspace_bytes, void *stream);
 
@@ -109,11 +111,14 @@ int32_t spec_verify_workspace_reset(void *workspace, size_t workspace_bytes, voi
  *                    bonus token, then -1 padding (all -1 on a sequence error)
  *   out_num_accepted device int32 [B]: accepted drafts in [0, k]; -1 = sequence error.
  *                    The sequence emits out_num_accepted[b] + 1 tokens.
- *   workspace        device, >= spec_verify_workspace_size(...) bytes, 16-byte aligned,
- *                    zeroed once before first use (spec_verify_workspace_reset); calls
- *                    leave it zeroed.  Two calls in flight at once must not share one.
+ *   workspace        device scratch, >= spec_verify_workspace_size(...) bytes, 16-byte
+ *                    aligned.  Its contents need no initialisation apart from the status
+ *                    word (see SPEC_DEV_OK).  Two calls in flight at once must not share
+ *                    one (the same stream runs calls in order, so one per stream suffices).
  *   stream           cudaStream_t as void*.
- * Returns SPEC_OK once the kernel is launched; errors are listed above.
+ * Four kernels run in order on `stream`: row statistics, accept scan, draw
+ * tiles, final search.  Returns SPEC_OK once they are launched; errors are
+ * listed above.
  */
 int32_t spec_verify(const void *target_logits, const void *draft_logits,
                     const int32_t *draft_tokens, const float *u_accept,
@@ -136,6 +141,22 @@ int32_t spec_verify_probs(const void *target_logits, const void *draft_logits,
                           void *workspace, size_t workspace_bytes, void *stream);
 
 /*
+ * spec_verify with per-stage timing: `stage_events` (nullable; entries may be
+ * NULL) holds SPEC_STAGES cudaEvent_t handles, created by the caller, that are
+ * recorded on `stream` after each stage: row statistics, accept scan, draw
+ * tiles, final search.  Same arguments and behaviour as spec_verify
+ * otherwise.  Lets a benchmark time the HBM-bound statistics stage alone.
+ */
+#define SPEC_STAGES 4
+int32_t spec_verify_timed(const void *target_logits, const void *draft_logits,
+                          const int32_t *draft_tokens, const float *u_accept,
+                          const float *u_resample, const float *temperature,
+                          int32_t *out_tokens, int32_t *out_num_accepted,
+                          int32_t B, int32_t k, int32_t V, int32_t dtype,
+                          void *workspace, size_t workspace_bytes, void *stream,
+                          void *const *stage_events);
+
+/*
  * Copy the workspace's device status word to *status (host) and synchronise
  * `stream`.  SPEC_DEV_OK (0) after a complete call.
  */
@@ -153,8 +174,8 @@ size_t spec_verify_host_arena_size(int32_t B, int32_t k, int32_t V, int32_t dtyp
  * and copies out_tokens / out_num_accepted back to the host buffers, all on
  * `stream`; synchronises the stream before returning so the host outputs are
  * ready.  Pinned host memory makes the copies asynchronous DMA.  The arena
- * must be >= spec_verify_host_arena_size(...) bytes and 256-byte aligned; its
- * workspace part is zeroed by this call.  Host pointers follow the device
+ * must be >= spec_verify_host_arena_size(...) bytes and 256-byte aligned; the
+ * status word of its workspace part is zeroed by this call.  Host pointers follow the device
  * entry point's shapes.
  */
 int32_t spec_verify_host(const void *target_logits, const void *draft_logits,

@@ -26,6 +26,7 @@ SPEC_DEV_OK = 0
 SPEC_DEV_WAIT_TIMEOUT = 1
 SPEC_MAX_K = 32
 SPEC_MAX_V = 1 << 20
+SPEC_STAGES = 4
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "libspecverify.so")
@@ -61,6 +62,8 @@ def library():
         lib.spec_verify.argtypes = [vp] * 8 + [i32] * 4 + [vp, sz, vp]
         lib.spec_verify_probs.restype = i32
         lib.spec_verify_probs.argtypes = [vp] * 9 + [i32] * 4 + [vp, sz, vp]
+        lib.spec_verify_timed.restype = i32
+        lib.spec_verify_timed.argtypes = [vp] * 8 + [i32] * 4 + [vp, sz, vp, vp]
         lib.spec_verify_read_status.restype = i32
         lib.spec_verify_read_status.argtypes = [vp, vp, vp]
         lib.spec_verify_host_arena_size.restype = sz
@@ -199,6 +202,21 @@ def spec_verify(target, draft, tokens, u_accept, u_resample, temperature,
                                _ptr(out_num_accepted), B, k, V, dt, _ptr(ws), ws.numel(),
                                _stream_handle(stream, dev))
     _check(rc, "spec_verify")
+    return out_tokens, out_num_accepted
+
+
+def spec_verify_timed(target, draft, tokens, u_accept, u_resample, temperature,
+                      out_tokens, out_num_accepted, ws, stage_events, stream=None):
+    """spec_verify recording the given torch.cuda.Event objects (SPEC_STAGES of
+    them, recorded once beforehand so that they exist) after each stage:
+    statistics, accept scan, draw tiles, final search."""
+    B, k, V, dt = _marshal(target, draft, tokens, u_accept, u_resample, temperature)
+    handles = (ctypes.c_void_p * SPEC_STAGES)(*[ctypes.c_void_p(e.cuda_event) for e in stage_events])
+    rc = library().spec_verify_timed(_ptr(target), _ptr(draft), _ptr(tokens), _ptr(u_accept),
+                                     _ptr(u_resample), _ptr(temperature), _ptr(out_tokens),
+                                     _ptr(out_num_accepted), B, k, V, dt, _ptr(ws), ws.numel(),
+                                     _stream_handle(stream, target.device), handles)
+    _check(rc, "spec_verify_timed")
     return out_tokens, out_num_accepted
 
 

@@ -1108,14 +1108,23 @@ size_t ws_bytes(int32_t B, int32_t k, int32_t V, int32_t dtype)
     return ws_layout(B, k, V, dtype).total;
 }
 
+// `events` (nullable): cudaEvent_t recorded after each of the four kernels.
 template <int DT>
-int launch_all(const Params &P, unsigned int grid1, cudaStream_t st)
+int launch_all(const Params &P, unsigned int grid1, cudaStream_t st, void *const *events)
 {
+    auto mark = [&](int i) {
+        if (events && events[i])
+            cudaEventRecord(reinterpret_cast<cudaEvent_t>(events[i]), st);
+    };
     stats_kernel<DT><<<grid1, NTHREADS, SMEM_BYTES, st>>>(P);
+    mark(0);
     const unsigned int gs = (unsigned int)((P.B + SCAN_WARPS - 1) / SCAN_WARPS);
     scan_kernel<DT><<<gs, SCAN_WARPS * 32, 0, st>>>(P);
+    mark(1);
     draw_kernel<DT><<<(unsigned int)P.DS * (unsigned int)P.B, NT, 0, st>>>(P);
+    mark(2);
     final_kernel<DT><<<gs, SCAN_WARPS * 32, 0, st>>>(P);
+    mark(3);
     if (cudaPeekAtLastError() != cudaSuccess) {
         (void)cudaGetLastError();
         return SPEC_ECUDA;
@@ -1126,7 +1135,7 @@ int launch_all(const Params &P, unsigned int grid1, cudaStream_t st)
 int launch(const void *target, const void *draft, const int32_t *tokens, const float *ua,
            const float *ur, const float *temp, int32_t *out_tokens, int32_t *out_n,
            float *out_probs, int32_t B, int32_t k, int32_t V, int32_t dtype, void *ws,
-           size_t ws_size, void *stream)
+           size_t ws_size, void *stream, void *const *events = nullptr)
 {
     if (!sizes_ok(B, k, V, dtype))
         return SPEC_EINVAL;
@@ -1200,8 +1209,8 @@ int launch(const void *target, const void *draft, const int32_t *tokens, const f
     P.draft_bytes = (unsigned long long)B * k * (unsigned long long)V * es;
 
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-    return (dtype == SPEC_F32) ? launch_all<SPEC_F32>(P, grid1, st)
-                               : launch_all<SPEC_BF16>(P, grid1, st);
+    return (dtype == SPEC_F32) ? launch_all<SPEC_F32>(P, grid1, st, events)
+                               : launch_all<SPEC_BF16>(P, grid1, st, events);
 }
 
 }  // namespace
@@ -1266,6 +1275,19 @@ int32_t spec_verify_probs(const void *target_logits, const void *draft_logits,
     return launch(target_logits, draft_logits, draft_tokens, u_accept, u_resample, temperature,
                   out_tokens, out_num_accepted, out_probs, B, k, V, dtype, workspace,
                   workspace_bytes, stream);
+}
+
+int32_t spec_verify_timed(const void *target_logits, const void *draft_logits,
+                          const int32_t *draft_tokens, const float *u_accept,
+                          const float *u_resample, const float *temperature,
+                          int32_t *out_tokens, int32_t *out_num_accepted,
+                          int32_t B, int32_t k, int32_t V, int32_t dtype,
+                          void *workspace, size_t workspace_bytes, void *stream,
+                          void *const *stage_events)
+{
+    return launch(target_logits, draft_logits, draft_tokens, u_accept, u_resample, temperature,
+                  out_tokens, out_num_accepted, nullptr, B, k, V, dtype, workspace,
+                  workspace_bytes, stream, stage_events);
 }
 
 int32_t spec_verify_read_status(const void *workspace, int32_t *status, void *stream)
@@ -1344,7 +1366,7 @@ int32_t spec_verify_host(const void *target_logits, const void *draft_logits,
     for (const auto &c : cps)
         if (cudaMemcpyAsync(c.dst, c.src, c.n, cudaMemcpyHostToDevice, st) != cudaSuccess)
             return SPEC_ECUDA;
-    if (cudaMemsetAsync(d_ws, 0, wsb, st) != cudaSuccess)
+    if (cudaMemsetAsync(d_ws, 0, sizeof(WsHeader), st) != cudaSuccess)
         return SPEC_ECUDA;
     int rc = launch(d_t, d_d, reinterpret_cast<const int32_t *>(d_g),
                     reinterpret_cast<const float *>(d_ua), reinterpret_cast<const float *>(d_ur),
