@@ -157,6 +157,38 @@ int32_t spec_verify_timed(const void *target_logits, const void *draft_logits,
                           void *const *stage_events);
 
 /*
+ * spec_verify for callers that cannot allocate device memory at the point of
+ * the call: for example a plugin inside a host runtime that owns all device
+ * memory through its own pool and hands the plugin none, or a latency-critical
+ * loop that must not call cudaMalloc (which can synchronise the device).
+ * The pages describe no such entry point; it has no counterpart there.
+ *
+ * Instead of a caller workspace it uses one scratch array of
+ * spec_verify_noalloc_max_bytes() bytes (8 MiB) that is part of this library's
+ * device code: every GPU that loads the library holds it until the process
+ * exits.  Calls whose spec_verify_workspace_size(B, k, V, dtype) exceeds that
+ * return SPEC_ENOSPACE and launch nothing (B=256, k=8, V=151936, fp32 needs
+ * about 1.6 MiB).  The call allocates nothing: no cudaMalloc, no cudaFree.
+ *
+ * The first call on a device looks up the array's device address with that
+ * device current (cudaGetSymbolAddress) and keeps it; make that first call
+ * before any stream capture.  Every call clears the array's status word on
+ * `stream` before launching.  All calls, on every stream, share the one
+ * array, which keeps the last call's contents: calls that overlap on the GPU
+ * race and give undefined outputs, so run them one after another (on one
+ * stream, or with your own ordering between streams).  Inputs, outputs,
+ * return codes and device-side sequence errors are as for spec_verify.
+ */
+int32_t spec_verify_noalloc(const void *target_logits, const void *draft_logits,
+                            const int32_t *draft_tokens, const float *u_accept,
+                            const float *u_resample, const float *temperature,
+                            int32_t *out_tokens, int32_t *out_num_accepted,
+                            int32_t B, int32_t k, int32_t V, int32_t dtype, void *stream);
+
+/* Size in bytes of the scratch array spec_verify_noalloc uses. */
+size_t spec_verify_noalloc_max_bytes(void);
+
+/*
  * Copy the workspace's device status word to *status (host) and synchronise
  * `stream`.  SPEC_DEV_OK (0) after a complete call.
  */

@@ -64,6 +64,10 @@ def library():
         lib.spec_verify_probs.argtypes = [vp] * 9 + [i32] * 4 + [vp, sz, vp]
         lib.spec_verify_timed.restype = i32
         lib.spec_verify_timed.argtypes = [vp] * 8 + [i32] * 4 + [vp, sz, vp, vp]
+        lib.spec_verify_noalloc.restype = i32
+        lib.spec_verify_noalloc.argtypes = [vp] * 8 + [i32] * 4 + [vp]
+        lib.spec_verify_noalloc_max_bytes.restype = sz
+        lib.spec_verify_noalloc_max_bytes.argtypes = []
         lib.spec_verify_read_status.restype = i32
         lib.spec_verify_read_status.argtypes = [vp, vp, vp]
         lib.spec_verify_host_arena_size.restype = sz
@@ -218,6 +222,26 @@ def spec_verify_timed(target, draft, tokens, u_accept, u_resample, temperature,
                                      _stream_handle(stream, target.device), handles)
     _check(rc, "spec_verify_timed")
     return out_tokens, out_num_accepted
+
+
+def spec_verify_noalloc(target, draft, tokens, u_accept, u_resample, temperature,
+                        out_tokens, out_num_accepted, stream=None):
+    """spec_verify without a workspace, for callers that cannot allocate device
+    memory when they verify: the library's own fixed scratch array is used
+    instead (see include/spec_verify.h).  The output tensors are supplied by
+    the caller, so this wrapper allocates nothing either.  Calls that overlap
+    on the GPU share that scratch and race."""
+    B, k, V, dt = _marshal(target, draft, tokens, u_accept, u_resample, temperature)
+    rc = library().spec_verify_noalloc(_ptr(target), _ptr(draft), _ptr(tokens), _ptr(u_accept),
+                                       _ptr(u_resample), _ptr(temperature), _ptr(out_tokens),
+                                       _ptr(out_num_accepted), B, k, V, dt,
+                                       _stream_handle(stream, target.device))
+    _check(rc, "spec_verify_noalloc")
+    return out_tokens, out_num_accepted
+
+
+def spec_verify_noalloc_max_bytes() -> int:
+    return int(library().spec_verify_noalloc_max_bytes())
 
 
 def spec_verify_probs(target, draft, tokens, u_accept, u_resample, temperature,

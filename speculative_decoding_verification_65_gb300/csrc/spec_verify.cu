@@ -1217,6 +1217,17 @@ int launch(const void *target, const void *draft, const int32_t *tokens, const f
 
 static_assert(SPEC_MAX_V / (NT * 4) + UD <= MAXBLK, "CDF blocks must cover the largest vocabulary");
 
+// ------------------------------------------------- scratch without allocation
+//
+// Device-resident scratch for spec_verify_noalloc.  It is part of the loaded
+// module: every GPU that loads this library holds these bytes until the
+// process exits.  Host code must not pass the symbol itself to a kernel (on
+// the host it names a host-side stand-in); the device address comes from
+// cudaGetSymbolAddress, once per device, with that device current.
+constexpr size_t NOALLOC_SCRATCH_BYTES = (size_t)8 << 20;
+static __device__ __align__(256) uint8_t g_noalloc_scratch[NOALLOC_SCRATCH_BYTES];
+static void *g_noalloc_addr[64];
+
 // ---------------------------------------------------------------- C ABI
 
 extern "C" {
@@ -1289,6 +1300,39 @@ int32_t spec_verify_timed(const void *target_logits, const void *draft_logits,
                   out_tokens, out_num_accepted, nullptr, B, k, V, dtype, workspace,
                   workspace_bytes, stream, stage_events);
 }
+
+int32_t spec_verify_noalloc(const void *target_logits, const void *draft_logits,
+                            const int32_t *draft_tokens, const float *u_accept,
+                            const float *u_resample, const float *temperature,
+                            int32_t *out_tokens, int32_t *out_num_accepted,
+                            int32_t B, int32_t k, int32_t V, int32_t dtype, void *stream)
+{
+    if (!sizes_ok(B, k, V, dtype))
+        return SPEC_EINVAL;
+    if (B == 0)
+        return SPEC_OK;
+    if (ws_bytes(B, k, V, dtype) > NOALLOC_SCRATCH_BYTES)
+        return SPEC_ENOSPACE;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64)
+        return SPEC_ECUDA;
+    if (!g_noalloc_addr[dev]) {
+        void *addr = nullptr;
+        if (cudaGetSymbolAddress(&addr, g_noalloc_scratch) != cudaSuccess || !addr)
+            return SPEC_ECUDA;
+        g_noalloc_addr[dev] = addr;
+    }
+    void *ws = g_noalloc_addr[dev];
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    // the status word is the only scratch contents a call reads before writing
+    if (cudaMemsetAsync(ws, 0, sizeof(WsHeader), st) != cudaSuccess)
+        return SPEC_ECUDA;
+    return launch(target_logits, draft_logits, draft_tokens, u_accept, u_resample, temperature,
+                  out_tokens, out_num_accepted, nullptr, B, k, V, dtype, ws,
+                  NOALLOC_SCRATCH_BYTES, stream);
+}
+
+size_t spec_verify_noalloc_max_bytes(void) { return NOALLOC_SCRATCH_BYTES; }
 
 int32_t spec_verify_read_status(const void *workspace, int32_t *status, void *stream)
 {
