@@ -151,6 +151,60 @@ __device__ __forceinline__ float fmax_nan(float a, float b)
     return d;
 }
 
+// Packed pairs of fp32 values (Blackwell f32x2 arithmetic).  add/mul .rn round
+// each half exactly like the scalar instructions, so packing changes no result.
+__device__ __forceinline__ unsigned long long f2(float lo, float hi)
+{
+    unsigned long long r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+    return r;
+}
+
+__device__ __forceinline__ unsigned long long f2_bits(uint32_t lo, uint32_t hi)
+{
+    unsigned long long r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "r"(lo), "r"(hi));
+    return r;
+}
+
+__device__ __forceinline__ void f2_split(unsigned long long v, float &lo, float &hi)
+{
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+}
+
+__device__ __forceinline__ unsigned long long add2(unsigned long long a, unsigned long long b)
+{
+    unsigned long long r;
+    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+    return r;
+}
+
+__device__ __forceinline__ unsigned long long mul2(unsigned long long a, unsigned long long b)
+{
+    unsigned long long r;
+    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+    return r;
+}
+
+// 2^((x - m) * c) for both halves; x - m is computed as x + (-m), which IEEE
+// defines to be the same operation.
+__device__ __forceinline__ void exp_pair(unsigned long long x2, unsigned long long negm2,
+                                         unsigned long long c2, float &e0, float &e1)
+{
+    float a0, a1;
+    f2_split(mul2(add2(x2, negm2), c2), a0, a1);
+    e0 = ex2(a0);
+    e1 = ex2(a1);
+}
+
+// NaN-propagating maximum of two pairs of bf16 values (exact)
+__device__ __forceinline__ uint32_t bmax2_nan(uint32_t a, uint32_t b)
+{
+    uint32_t d;
+    asm("max.NaN.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+    return d;
+}
+
 __device__ __forceinline__ unsigned long long globaltimer()
 {
     unsigned long long t;
@@ -248,6 +302,23 @@ struct Lg<SPEC_F32> {
     {
         return __ldg(reinterpret_cast<const float *>(base) + idx);
     }
+    // maximum of the vector's elements, NaN if any is NaN
+    __device__ static __forceinline__ float vmax(const uint4 &r)
+    {
+        const float a = fmax_nan(__uint_as_float(r.x), __uint_as_float(r.y));
+        return fmax_nan(a, fmax_nan(__uint_as_float(r.z), __uint_as_float(r.w)));
+    }
+    // sum of 2^((x-m)*c) over the vector: (e0 + e2) + (e1 + e3)
+    __device__ static __forceinline__ float expsum(const uint4 &r, unsigned long long negm2,
+                                                   unsigned long long c2)
+    {
+        float e0, e1, e2, e3;
+        exp_pair(f2_bits(r.x, r.y), negm2, c2, e0, e1);
+        exp_pair(f2_bits(r.z, r.w), negm2, c2, e2, e3);
+        float t0, t1;
+        f2_split(add2(f2(e0, e1), f2(e2, e3)), t0, t1);
+        return t0 + t1;
+    }
     // place element j's bit pattern into a raw vector
     __device__ static __forceinline__ void put(uint4 &r, int j, uint32_t bits)
     {
@@ -280,6 +351,32 @@ struct Lg<SPEC_BF16> {
     {
         const unsigned short h = __ldg(reinterpret_cast<const unsigned short *>(base) + idx);
         return __uint_as_float(((uint32_t)h) << 16);
+    }
+    // element 2i is the low half of word i, element 2i+1 the high half
+    __device__ static __forceinline__ unsigned long long pair(uint32_t w)
+    {
+        return f2_bits(w << 16, w & 0xffff0000u);
+    }
+    // maximum of the vector's elements, NaN if any is NaN (bf16 maxima are exact)
+    __device__ static __forceinline__ float vmax(const uint4 &r)
+    {
+        const uint32_t h = bmax2_nan(bmax2_nan(r.x, r.y), bmax2_nan(r.z, r.w));
+        return fmax_nan(__uint_as_float(h << 16), __uint_as_float(h & 0xffff0000u));
+    }
+    // sum of 2^((x-m)*c) over the vector: ((e0+e4) + (e2+e6)) + ((e1+e5) + (e3+e7))
+    __device__ static __forceinline__ float expsum(const uint4 &r, unsigned long long negm2,
+                                                   unsigned long long c2)
+    {
+        float e[8];
+        exp_pair(pair(r.x), negm2, c2, e[0], e[1]);
+        exp_pair(pair(r.y), negm2, c2, e[2], e[3]);
+        exp_pair(pair(r.z), negm2, c2, e[4], e[5]);
+        exp_pair(pair(r.w), negm2, c2, e[6], e[7]);
+        const unsigned long long a = add2(f2(e[0], e[1]), f2(e[4], e[5]));
+        const unsigned long long b = add2(f2(e[2], e[3]), f2(e[6], e[7]));
+        float t0, t1;
+        f2_split(add2(a, b), t0, t1);
+        return t0 + t1;
     }
     __device__ static __forceinline__ uint32_t merge(uint32_t word, int j, uint32_t bits)
     {
@@ -444,13 +541,7 @@ __device__ __forceinline__ void tile_accumulate(const Params &P, const Seg &g, i
     for (int u = 0; u < U; ++u) {
         const int v = v0 + tid + u * NT;
         raw[u] = (v < v1) ? seg_vec<DT>(P, g, v) : neg_inf_vec(L::NEG_INF_WORD);
-        float x[VEC];
-        L::unpack(raw[u], x);
-        float a = fmax_nan(x[0], x[1]);
-#pragma unroll
-        for (int j = 2; j < VEC; j += 2)
-            a = fmax_nan(a, fmax_nan(x[j], x[j + 1]));
-        vmax[u] = a;
+        vmax[u] = L::vmax(raw[u]);
     }
     float mt = vmax[0];
 #pragma unroll
@@ -484,22 +575,11 @@ __device__ __forceinline__ void tile_accumulate(const Params &P, const Seg &g, i
         st.s = rescale(st.s, st.m, mn, c);
     st.m = mn;
     if (mn != -INFINITY) {
+        const unsigned long long negm2 = f2(-mn, -mn), c2 = f2(c, c);
         float s = 0.0f;
 #pragma unroll
-        for (int u = 0; u < U; ++u) {
-            float x[VEC];
-            L::unpack(raw[u], x);
-            float sv[VEC];
-#pragma unroll
-            for (int j = 0; j < VEC; ++j)
-                sv[j] = ex2((x[j] - mn) * c);
-#pragma unroll
-            for (int w = VEC / 2; w > 0; w >>= 1)
-#pragma unroll
-                for (int j = 0; j < w; ++j)
-                    sv[j] = sv[j] + sv[j + w];
-            s += sv[0];
-        }
+        for (int u = 0; u < U; ++u)
+            s += L::expsum(raw[u], negm2, c2);
         st.s += s;
     }
 }
