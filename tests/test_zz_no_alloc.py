@@ -47,7 +47,7 @@ def test_noalloc_rejects_sizes_beyond_its_scratch():
     lib = sv.library()
     cap = sv.spec_verify_noalloc_max_bytes()
     assert cap == 8 << 20
-    B, k, V = 4096, 8, 151936  # needs far more than the fixed scratch
+    B, k, V = 8192, 32, 151936  # needs far more than the fixed scratch
     assert sv.spec_verify_workspace_size(B, k, V, sv.SPEC_F32) > cap
     fake = [ctypes.c_void_p(0x100000 * (i + 1)) for i in range(8)]
     rc = lib.spec_verify_noalloc(*fake, B, k, V, sv.SPEC_F32, None)
