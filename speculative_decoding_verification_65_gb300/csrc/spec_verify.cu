@@ -205,6 +205,21 @@ __device__ __forceinline__ uint32_t bmax2_nan(uint32_t a, uint32_t b)
     return d;
 }
 
+// Programmatic dependent launch: a kernel launched after another on the same
+// stream with programmatic serialisation may start early; it must wait here
+// before it reads what the previous kernel wrote.
+__device__ __forceinline__ void wait_previous_kernel()
+{
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
+// Let the next kernel on the stream begin launching (its CTAs still wait in
+// wait_previous_kernel until this grid has finished).
+__device__ __forceinline__ void allow_next_kernel()
+{
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 __device__ __forceinline__ unsigned long long globaltimer()
 {
     unsigned long long t;
@@ -308,6 +323,12 @@ struct Lg<SPEC_F32> {
         const float a = fmax_nan(__uint_as_float(r.x), __uint_as_float(r.y));
         return fmax_nan(a, fmax_nan(__uint_as_float(r.z), __uint_as_float(r.w)));
     }
+    // the vector as pairs (x0,x1), (x2,x3)
+    __device__ static __forceinline__ void pairs(const uint4 &r, unsigned long long (&p)[VEC / 2])
+    {
+        p[0] = f2_bits(r.x, r.y);
+        p[1] = f2_bits(r.z, r.w);
+    }
     // sum of 2^((x-m)*c) over the vector: (e0 + e2) + (e1 + e3)
     __device__ static __forceinline__ float expsum(const uint4 &r, unsigned long long negm2,
                                                    unsigned long long c2)
@@ -356,6 +377,14 @@ struct Lg<SPEC_BF16> {
     __device__ static __forceinline__ unsigned long long pair(uint32_t w)
     {
         return f2_bits(w << 16, w & 0xffff0000u);
+    }
+    // the vector as pairs (x0,x1) .. (x6,x7)
+    __device__ static __forceinline__ void pairs(const uint4 &r, unsigned long long (&p)[VEC / 2])
+    {
+        p[0] = pair(r.x);
+        p[1] = pair(r.y);
+        p[2] = pair(r.z);
+        p[3] = pair(r.w);
     }
     // maximum of the vector's elements, NaN if any is NaN (bf16 maxima are exact)
     __device__ static __forceinline__ float vmax(const uint4 &r)
@@ -779,7 +808,24 @@ __global__ void __launch_bounds__(SCAN_WARPS * 32) scan_kernel(const Params P)
     if (b >= P.B)
         return;
     const int k = P.k, V = P.V;
+    // every load that depends on no other goes out first: the temperature, the
+    // tokens and uniforms, and the partials of every row (whether or not the
+    // sequence's mode needs them)
     const float T = __ldg(P.temperature + b);
+    const int g = (lane < k) ? __ldg(P.tokens + (size_t)b * k + lane) : 0;
+    const float ua = (lane < k) ? __ldg(P.u_accept + (size_t)b * k + lane) : 0.0f;
+    const float ur = __ldg(P.u_resample + b);
+    allow_next_kernel();
+    wait_previous_kernel();  // the partials come from the statistics kernel
+    constexpr int PRE = 8;
+    float4 pre[PRE];
+    if (lane < P.rows) {
+        const float4 *pp = P.part + ((size_t)b * P.rows + lane) * P.NSS;
+#pragma unroll
+        for (int q = 0; q < PRE; ++q)
+            if (q < P.NSS)
+                pre[q] = __ldcg(pp + q);
+    }
     const bool tvalid = temperature_valid(T);
     const bool greedy = tvalid && T == 0.0f;
     const float c = (tvalid && !greedy) ? LOG2E / T : 0.0f;
@@ -789,9 +835,7 @@ __global__ void __launch_bounds__(SCAN_WARPS * 32) scan_kernel(const Params P)
     for (int r = lane; r < nrows; r += 32) {
         float m = -INFINITY, s = 0.0f;
         int idx = INT_MAX;
-        const float4 *pp = P.part + ((size_t)b * P.rows + r) * P.NSS;
-        for (int q = 0; q < P.NSS; ++q) {
-            const float4 pv = __ldcg(pp + q);
+        auto fold = [&](const float4 &pv) {
             const float pm = pv.x, ps = pv.y;
             const int pi = __float_as_int(pv.z);
             const float mn = fmax_nan(m, pm);
@@ -799,7 +843,18 @@ __global__ void __launch_bounds__(SCAN_WARPS * 32) scan_kernel(const Params P)
                 s = rescale(s, m, mn, c) + rescale(ps, pm, mn, c);
             idx = (m == mn && pm == mn) ? min(idx, pi) : (pm == mn ? pi : idx);
             m = mn;
+        };
+        const float4 *pp = P.part + ((size_t)b * P.rows + r) * P.NSS;
+        int q = 0;
+        if (r == lane) {
+#pragma unroll
+            for (int qq = 0; qq < PRE; ++qq)
+                if (qq < P.NSS)
+                    fold(pre[qq]);
+            q = PRE;
         }
+        for (; q < P.NSS; ++q)
+            fold(__ldcg(pp + q));
         rm[warp][r] = m;
         rZ[warp][r] = s;
         rarg[warp][r] = idx;
@@ -809,14 +864,10 @@ __global__ void __launch_bounds__(SCAN_WARPS * 32) scan_kernel(const Params P)
 
     // 2. accept scan: lane i tests position i
     bool err = !tvalid;
-    int g = 0;
     bool fail = false, qzero = false;
     if (!err) {
-        if (lane < k) {
-            g = __ldg(P.tokens + (size_t)b * k + lane);
-            if (g < 0 || g >= V)
-                err = true;
-        }
+        if (lane < k && (g < 0 || g >= V))
+            err = true;
         for (int r = lane; r < nrows; r += 32)
             if (rbad[warp][r])
                 err = true;
@@ -836,7 +887,6 @@ __global__ void __launch_bounds__(SCAN_WARPS * 32) scan_kernel(const Params P)
             const float dt = lt - mt, dd = ld - md;
             const float x = (dt - dd) * c;
             const float ratio = ((x == 0.0f) ? 1.0f : ex2(x)) * (zd / zt);
-            const float ua = __ldg(P.u_accept + (size_t)b * k + lane);
             fail = qzero || !((ratio >= 1.0f) || (ua < ratio));
             if (P.out_probs) {
                 P.out_probs[((size_t)b * k + lane) * 2 + 0] = ex2(dt * c) / zt;
@@ -876,7 +926,7 @@ __global__ void __launch_bounds__(SCAN_WARPS * 32) scan_kernel(const Params P)
     } else {
         // the residual at the rejected position, or the bonus row
         J.c = c;
-        J.u = __ldg(P.u_resample + b);
+        J.u = ur;
         J.t_row = (long long)b * (k + 1) + j;
         J.mt = rm[warp][j];
         J.rzt = 1.0f / rZ[warp][j];
@@ -963,6 +1013,8 @@ __global__ void __launch_bounds__(NT) draw_kernel(const Params P)
     constexpr int VEC = L::VEC;
     const int b = (int)(blockIdx.x / (unsigned int)P.DS);
     const int seg = (int)(blockIdx.x - (unsigned int)b * (unsigned int)P.DS);
+    allow_next_kernel();
+    wait_previous_kernel();  // the job comes from the scan kernel
     const JobRec J = load_job(P, b);
     if (J.mode == DRAW_NONE)
         return;
@@ -1005,41 +1057,65 @@ __device__ int locate(const Params &P, const JobRec &J, int mode, const float *c
 {
     using L = Lg<DT>;
     constexpr int VEC = L::VEC;
-    for (int blk = lane; blk < nblk; blk += 32) {
-        float c8[NCW];
+    // block totals: 8 chunk totals left to right (two 16-byte loads per block,
+    // four blocks per lane in flight)
+    for (int blk0 = lane; blk0 < nblk; blk0 += 4 * 32) {
+        float4 c8[4][NCW / 4];
 #pragma unroll
-        for (int w = 0; w < NCW; ++w)
-            c8[w] = ch[blk * NCW + w];
-        float bt = 0.0f;
+        for (int g = 0; g < 4; ++g)
+            if (blk0 + g * 32 < nblk)
 #pragma unroll
-        for (int w = 0; w < NCW; ++w)
-            bt = bt + c8[w];
-        btot[blk] = bt;
+                for (int w = 0; w < NCW / 4; ++w)
+                    c8[g][w] = *reinterpret_cast<const float4 *>(ch + (blk0 + g * 32) * NCW + 4 * w);
+#pragma unroll
+        for (int g = 0; g < 4; ++g) {
+            if (blk0 + g * 32 < nblk) {
+                float bt = 0.0f;
+#pragma unroll
+                for (int w = 0; w < NCW / 4; ++w)
+                    bt = (((bt + c8[g][w].x) + c8[g][w].y) + c8[g][w].z) + c8[g][w].w;
+                btot[blk0 + g * 32] = bt;
+            }
+        }
     }
     __syncwarp();
-    float R = 0.0f, uR = 0.0f, base = 0.0f;
-    int bstar = nblk - 1;
+    // the row level: an inclusive prefix of the block totals, left to right,
+    // by one lane; then the first block whose prefix exceeds u * R, found by
+    // the whole warp (the same additions as a sequential walk)
     if (lane == 0) {
-        for (int blk = 0; blk < nblk; ++blk)
-            R = R + btot[blk];
-        uR = J.u * R;
         float acc = 0.0f;
-        for (int blk = 0; blk < nblk; ++blk) {
-            const float nxt = acc + btot[blk];
-            if (nxt > uR) {
-                bstar = blk;
-                break;
-            }
-            acc = nxt;
+        int blk = 0;
+        for (; blk + 4 <= nblk; blk += 4) {
+            const float4 t4 = *reinterpret_cast<const float4 *>(btot + blk);
+            acc = acc + t4.x;
+            btot[blk] = acc;
+            acc = acc + t4.y;
+            btot[blk + 1] = acc;
+            acc = acc + t4.z;
+            btot[blk + 2] = acc;
+            acc = acc + t4.w;
+            btot[blk + 3] = acc;
         }
-        base = acc;
+        for (; blk < nblk; ++blk) {
+            acc = acc + btot[blk];
+            btot[blk] = acc;
+        }
     }
-    R = __shfl_sync(0xffffffffu, R, 0);
+    __syncwarp();
+    const float R = btot[nblk - 1];
     if (!(R > 0.0f))
         return -1;
-    uR = __shfl_sync(0xffffffffu, uR, 0);
-    base = __shfl_sync(0xffffffffu, base, 0);
-    bstar = __shfl_sync(0xffffffffu, bstar, 0);
+    const float uR = J.u * R;
+    int bstar = nblk - 1;
+    for (int blk0 = 0; blk0 < nblk; blk0 += 32) {
+        const int blk = blk0 + lane;
+        const unsigned hit = __ballot_sync(0xffffffffu, blk < nblk && btot[blk] > uR);
+        if (hit) {
+            bstar = blk0 + __ffs(hit) - 1;
+            break;
+        }
+    }
+    const float base = (bstar > 0) ? btot[bstar - 1] : 0.0f;
     const float cw = (lane < NCW) ? ch[bstar * NCW + lane] : 0.0f;
     float W = 0.0f;
     int wstar = NCW - 1;
@@ -1117,6 +1193,7 @@ __global__ void __launch_bounds__(SCAN_WARPS * 32) final_kernel(const Params P)
     __shared__ float btot[SCAN_WARPS][MAXBLK];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int b = blockIdx.x * SCAN_WARPS + warp;
+    wait_previous_kernel();  // chunk totals come from the draw kernel
     if (b >= P.B)
         return;
     const JobRec J = load_job(P, b);
@@ -1196,14 +1273,35 @@ int launch_all(const Params &P, unsigned int grid1, cudaStream_t st, void *const
         if (events && events[i])
             cudaEventRecord(reinterpret_cast<cudaEvent_t>(events[i]), st);
     };
+    // kernels 2..4 may start while their predecessor drains (programmatic
+    // dependent launch); each waits before reading its predecessor's output.
+    // With stage events requested, launches stay plainly ordered so each event
+    // marks the end of its own stage.
+    const bool pdl = !events;
+    auto dependent = [&](auto kern, unsigned int grid, unsigned int block) -> cudaError_t {
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3(grid);
+        cfg.blockDim = dim3(block);
+        cfg.dynamicSmemBytes = 0;
+        cfg.stream = st;
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[0].val.programmaticStreamSerializationAllowed = pdl ? 1 : 0;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        return cudaLaunchKernelEx(&cfg, kern, P);
+    };
     stats_kernel<DT><<<grid1, NTHREADS, SMEM_BYTES, st>>>(P);
     mark(0);
     const unsigned int gs = (unsigned int)((P.B + SCAN_WARPS - 1) / SCAN_WARPS);
-    scan_kernel<DT><<<gs, SCAN_WARPS * 32, 0, st>>>(P);
+    if (dependent(scan_kernel<DT>, gs, SCAN_WARPS * 32) != cudaSuccess)
+        return SPEC_ECUDA;
     mark(1);
-    draw_kernel<DT><<<(unsigned int)P.DS * (unsigned int)P.B, NT, 0, st>>>(P);
+    if (dependent(draw_kernel<DT>, (unsigned int)P.DS * (unsigned int)P.B, NT) != cudaSuccess)
+        return SPEC_ECUDA;
     mark(2);
-    final_kernel<DT><<<gs, SCAN_WARPS * 32, 0, st>>>(P);
+    if (dependent(final_kernel<DT>, gs, SCAN_WARPS * 32) != cudaSuccess)
+        return SPEC_ECUDA;
     mark(3);
     if (cudaPeekAtLastError() != cudaSuccess) {
         (void)cudaGetLastError();
