@@ -243,26 +243,33 @@ def run_ours(args):
     if sv.spec_verify_read_status(ws) != sv.SPEC_DEV_OK:
         raise RuntimeError("device status nonzero after warm-up")
 
-    # per step: an event before the call and one after each of its four kernels
-    # (statistics, accept scan, draw tiles, final search), on the launch stream
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    barrier()
+    torch.cuda.synchronize(dev)
+    # the timed region: K whole verification calls, as a user issues them
+    with ClockSampler(local) as clk:
+        t0.record(stream)
+        for i in range(args.steps):
+            step()
+        t1.record(stream)
+        torch.cuda.synchronize(dev)
+    barrier()
+    total_ms = t0.elapsed_time(t1)
+
+    # per-kernel durations: K more calls, each with an event before it and one
+    # after each stage (statistics, accept scan, draw tiles, final search) on
+    # the launch stream; stage events keep the kernels plainly ordered
     starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
     stages = [[torch.cuda.Event(enable_timing=True) for _ in range(sv.SPEC_STAGES)]
               for _ in range(args.steps)]
     for ev in [e for row in stages for e in row]:
         ev.record(stream)  # creates the underlying CUDA events
-    t0 = torch.cuda.Event(enable_timing=True)
-    t1 = torch.cuda.Event(enable_timing=True)
-    barrier()
     torch.cuda.synchronize(dev)
-    with ClockSampler(local) as clk:
-        t0.record(stream)
-        for i in range(args.steps):
-            starts[i].record(stream)
-            step(stages[i])
-        t1.record(stream)
-        torch.cuda.synchronize(dev)
-    barrier()
-    total_ms = t0.elapsed_time(t1)
+    for i in range(args.steps):
+        starts[i].record(stream)
+        step(stages[i])
+    torch.cuda.synchronize(dev)
     kern_ms = [s.elapsed_time(e[0]) for s, e in zip(starts, stages)]  # statistics kernel
     stage_ms = [statistics.mean(
         (starts[i] if j == 0 else stages[i][j - 1]).elapsed_time(stages[i][j])
@@ -292,7 +299,7 @@ def run_ours(args):
     torch.cuda.empty_cache()
     arena = torch.empty(sv.spec_verify_host_arena_size(B, k, V, dt_code), dtype=torch.uint8,
                         device=dev)
-    e2e_steps = max(1, min(args.steps, 10))
+    e2e_steps = max(1, min(args.steps, 20))
     sv.spec_verify_host(h_t, h_d, h_g, h_ua, h_ur, h_T, arena, h_ot, h_on, stream=stream)
     barrier()
     e0 = time.perf_counter()
@@ -340,6 +347,7 @@ def run_ours(args):
                      "peak_source": f"{peak_src} copy bandwidth (MEASURED_PEAKS.json hbm_gbs)"
                      if peak_src == "measured" else "fallback 6.8 TB/s",
                      "kernel": "stats_kernel (row statistics, the HBM-bound stage)",
+                     "kernel_timing": "CUDA events after each stage, K further steps",
                      "kernel_ms_avg": kern_avg_s * 1e3, "kernel_ms_min": min(kern_ms),
                      "frac_of_nominal_8TBs": achieved / 8000.0,
                      "step_GBps": alg_bytes / (ms_per_step / 1e3) / 1e9},
@@ -360,7 +368,7 @@ def run_ours(args):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--steps", type=int, default=2000)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--config", type=int, default=4, choices=[1, 2, 3, 4, 5])

@@ -323,22 +323,24 @@ struct Lg<SPEC_F32> {
         const float a = fmax_nan(__uint_as_float(r.x), __uint_as_float(r.y));
         return fmax_nan(a, fmax_nan(__uint_as_float(r.z), __uint_as_float(r.w)));
     }
-    // the vector as pairs (x0,x1), (x2,x3)
-    __device__ static __forceinline__ void pairs(const uint4 &r, unsigned long long (&p)[VEC / 2])
+    // sums of 2^((x-m)*c) over the vector as a pair (e0 + e2, e1 + e3)
+    __device__ static __forceinline__ unsigned long long expsum2(const uint4 &r, float negm,
+                                                                 unsigned long long c2)
     {
-        p[0] = f2_bits(r.x, r.y);
-        p[1] = f2_bits(r.z, r.w);
-    }
-    // sum of 2^((x-m)*c) over the vector: (e0 + e2) + (e1 + e3)
-    __device__ static __forceinline__ float expsum(const uint4 &r, unsigned long long negm2,
-                                                   unsigned long long c2)
-    {
+        const unsigned long long negm2 = f2(negm, negm);
         float e0, e1, e2, e3;
         exp_pair(f2_bits(r.x, r.y), negm2, c2, e0, e1);
         exp_pair(f2_bits(r.z, r.w), negm2, c2, e2, e3);
-        float t0, t1;
-        f2_split(add2(f2(e0, e1), f2(e2, e3)), t0, t1);
-        return t0 + t1;
+        return add2(f2(e0, e1), f2(e2, e3));
+    }
+    template <int N>
+    __device__ static __forceinline__ float tile_max(const uint4 (&raw)[N])
+    {
+        float m = vmax(raw[0]);
+#pragma unroll
+        for (int u = 1; u < N; ++u)
+            m = fmax_nan(m, vmax(raw[u]));
+        return m;
     }
     // place element j's bit pattern into a raw vector
     __device__ static __forceinline__ void put(uint4 &r, int j, uint32_t bits)
@@ -373,39 +375,48 @@ struct Lg<SPEC_BF16> {
         const unsigned short h = __ldg(reinterpret_cast<const unsigned short *>(base) + idx);
         return __uint_as_float(((uint32_t)h) << 16);
     }
-    // element 2i is the low half of word i, element 2i+1 the high half
-    __device__ static __forceinline__ unsigned long long pair(uint32_t w)
-    {
-        return f2_bits(w << 16, w & 0xffff0000u);
-    }
-    // the vector as pairs (x0,x1) .. (x6,x7)
-    __device__ static __forceinline__ void pairs(const uint4 &r, unsigned long long (&p)[VEC / 2])
-    {
-        p[0] = pair(r.x);
-        p[1] = pair(r.y);
-        p[2] = pair(r.z);
-        p[3] = pair(r.w);
-    }
     // maximum of the vector's elements, NaN if any is NaN (bf16 maxima are exact)
     __device__ static __forceinline__ float vmax(const uint4 &r)
     {
         const uint32_t h = bmax2_nan(bmax2_nan(r.x, r.y), bmax2_nan(r.z, r.w));
         return fmax_nan(__uint_as_float(h << 16), __uint_as_float(h & 0xffff0000u));
     }
-    // sum of 2^((x-m)*c) over the vector: ((e0+e4) + (e2+e6)) + ((e1+e5) + (e3+e7))
-    __device__ static __forceinline__ float expsum(const uint4 &r, unsigned long long negm2,
-                                                   unsigned long long c2)
+    // x - m for both halves of a word: each bf16 half is widened exactly and
+    // added to -m with one rounding, as the fp32 subtraction would do
+    __device__ static __forceinline__ unsigned long long sub_pair(uint32_t w, float negm)
     {
-        float e[8];
-        exp_pair(pair(r.x), negm2, c2, e[0], e[1]);
-        exp_pair(pair(r.y), negm2, c2, e[2], e[3]);
-        exp_pair(pair(r.z), negm2, c2, e[4], e[5]);
-        exp_pair(pair(r.w), negm2, c2, e[6], e[7]);
-        const unsigned long long a = add2(f2(e[0], e[1]), f2(e[4], e[5]));
-        const unsigned long long b = add2(f2(e[2], e[3]), f2(e[6], e[7]));
-        float t0, t1;
-        f2_split(add2(a, b), t0, t1);
-        return t0 + t1;
+        float lo, hi;
+        asm("{\n\t.reg .b16 l, h;\n\tmov.b32 {l, h}, %2;\n\t"
+            "add.rn.f32.bf16 %0, l, %3;\n\tadd.rn.f32.bf16 %1, h, %3;\n\t}"
+            : "=f"(lo), "=f"(hi)
+            : "r"(w), "f"(negm));
+        return f2(lo, hi);
+    }
+    __device__ static __forceinline__ unsigned long long exp2_pair(uint32_t w, float negm,
+                                                                   unsigned long long c2)
+    {
+        float a0, a1;
+        f2_split(mul2(sub_pair(w, negm), c2), a0, a1);
+        return f2(ex2(a0), ex2(a1));
+    }
+    // sums of 2^((x-m)*c) over the vector as a pair:
+    // ((e0+e4) + (e2+e6), (e1+e5) + (e3+e7))
+    __device__ static __forceinline__ unsigned long long expsum2(const uint4 &r, float negm,
+                                                                 unsigned long long c2)
+    {
+        const unsigned long long a = add2(exp2_pair(r.x, negm, c2), exp2_pair(r.z, negm, c2));
+        const unsigned long long b = add2(exp2_pair(r.y, negm, c2), exp2_pair(r.w, negm, c2));
+        return add2(a, b);
+    }
+    // NaN-propagating maximum over a whole tile's vectors, kept packed
+    template <int N>
+    __device__ static __forceinline__ float tile_max(const uint4 (&raw)[N])
+    {
+        uint32_t h = bmax2_nan(bmax2_nan(raw[0].x, raw[0].y), bmax2_nan(raw[0].z, raw[0].w));
+#pragma unroll
+        for (int u = 1; u < N; ++u)
+            h = bmax2_nan(h, bmax2_nan(bmax2_nan(raw[u].x, raw[u].y), bmax2_nan(raw[u].z, raw[u].w)));
+        return fmax_nan(__uint_as_float(h << 16), __uint_as_float(h & 0xffff0000u));
     }
     __device__ static __forceinline__ uint32_t merge(uint32_t word, int j, uint32_t bits)
     {
@@ -565,19 +576,28 @@ __device__ __forceinline__ void tile_accumulate(const Params &P, const Seg &g, i
     const int v1 = (g.e1 + VEC - 1) / VEC;
 
     uint4 raw[U];
-    float vmax[U];
+    if (g.fast && g.e1 - g.e0 == U * NT * VEC) {
+        // a whole tile, copied aligned: every vector is in range
 #pragma unroll
-    for (int u = 0; u < U; ++u) {
-        const int v = v0 + tid + u * NT;
-        raw[u] = (v < v1) ? seg_vec<DT>(P, g, v) : neg_inf_vec(L::NEG_INF_WORD);
-        vmax[u] = L::vmax(raw[u]);
+        for (int u = 0; u < U; ++u)
+            raw[u] = ld_shared_v4(g.slot + (size_t)(tid + u * NT) * 16);
+    } else {
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            const int v = v0 + tid + u * NT;
+            raw[u] = (v < v1) ? seg_vec<DT>(P, g, v) : neg_inf_vec(L::NEG_INF_WORD);
+        }
     }
-    float mt = vmax[0];
-#pragma unroll
-    for (int u = 1; u < U; ++u)
-        mt = fmax_nan(mt, vmax[u]);
 
     if (mode == MODE_GREEDY) {
+        float vmax[U];
+#pragma unroll
+        for (int u = 0; u < U; ++u)
+            vmax[u] = L::vmax(raw[u]);
+        float mt = vmax[0];
+#pragma unroll
+        for (int u = 1; u < U; ++u)
+            mt = fmax_nan(mt, vmax[u]);
         // the first occurrence over the super-tile lies in the earliest tile
         // holding a strictly larger maximum
         if (mt > st.m) {
@@ -599,17 +619,20 @@ __device__ __forceinline__ void tile_accumulate(const Params &P, const Seg &g, i
         return;
     }
     // sampling: online rescale when the running maximum grows
+    const float mt = L::tile_max(raw);
     const float mn = fmax_nan(st.m, mt);
     if (mn != st.m)
         st.s = rescale(st.s, st.m, mn, c);
     st.m = mn;
     if (mn != -INFINITY) {
-        const unsigned long long negm2 = f2(-mn, -mn), c2 = f2(c, c);
-        float s = 0.0f;
+        const unsigned long long c2 = f2(c, c);
+        unsigned long long acc = L::expsum2(raw[0], -mn, c2);
 #pragma unroll
-        for (int u = 0; u < U; ++u)
-            s += L::expsum(raw[u], negm2, c2);
-        st.s += s;
+        for (int u = 1; u < U; ++u)
+            acc = add2(acc, L::expsum2(raw[u], -mn, c2));
+        float s0, s1;
+        f2_split(acc, s0, s1);
+        st.s += s0 + s1;
     }
 }
 
