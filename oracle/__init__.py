@@ -64,6 +64,8 @@ def _load():
         lib.spec_ref_residual.restype = ctypes.c_double
         lib.spec_ref_inverse_cdf.argtypes = [dp, i64, ctypes.c_double, dp]
         lib.spec_ref_inverse_cdf.restype = i64
+        lib.spec_sample_ref_mt.argtypes = [vp, i32, dp, dp, i64, i64, vp, dp, i32]
+        lib.spec_sample_ref_mt.restype = i32
         _lib = lib
         return lib
 
@@ -127,6 +129,27 @@ def probs(target, draft, tokens, temperature):
     if rc != 0:
         raise RuntimeError(f"spec_ref_probs failed with status {rc}")
     return out
+
+
+def sample(logits, u, temperature, nthreads: int = 1, want_trace: bool = True):
+    """One token per row of logits [R, V] (float32, or uint16 bf16 bit
+    patterns) from softmax(logits / T) by inverse CDF with u, argmax at T = 0.
+    Returns (tokens int32 [R] with -1 on a row error, trace [R, 3] float64 =
+    the chosen cell [lo, hi) in u-units and the total, or None)."""
+    lib = _load()
+    logits, dt = _logits_and_dtype(logits)
+    if logits.ndim != 2:
+        raise ValueError("logits must be [R, V]")
+    R, V = logits.shape
+    uu = np.ascontiguousarray(u, dtype=np.float64).reshape(R)
+    tt = np.ascontiguousarray(temperature, dtype=np.float64).reshape(R)
+    out = np.empty((R,), np.int32)
+    trace = np.empty((R, 3), np.float64) if want_trace else None
+    rc = lib.spec_sample_ref_mt(_ptr(logits), dt, _ptr(uu), _ptr(tt), R, V, _ptr(out),
+                                _ptr(trace) if trace is not None else None, int(nthreads))
+    if rc != 0:
+        raise RuntimeError(f"spec_sample_ref failed with status {rc}")
+    return out, trace
 
 
 def softmax(logits, T: float):

@@ -40,6 +40,15 @@
  *     draft rows when T > 0); such a row whose logits are all -inf; q(g) <= 0
  *     at a position the scan reaches.
  *
+ * Sampling (spec_sample_ref): the draft model's step before verification,
+ * each proposed token sampled from its distribution q ("Speculative Decoding
+ * and the Art of Fast LLM Inference", "The Algorithm, Step by Step", the
+ * drafting step; interview page, "Algorithm (one round)", step 1).  One token
+ * per row: T > 0 draws from softmax(l / T) by the same inverse-CDF reading as
+ * the verification's draws; T == 0 takes the argmax (lowest index on ties);
+ * row errors (token -1): T invalid as above, a NaN or +inf logit, or every
+ * logit -inf.
+ *
  * Everything is fp64 with plain sequential loops; no blocking, no fusion, no
  * reordering beyond the definition.
  */
@@ -467,4 +476,123 @@ int spec_ref_probs(const void *target, const void *draft, int dtype,
     }
     free(buf);
     return REF_OK;
+}
+
+/* ----------------------------------------------------------------- sampling */
+
+typedef struct {
+    const void *logits;       /* [R, V] */
+    int dtype;
+    const double *u;          /* [R] */
+    const double *temperature;/* [R] */
+    int64_t V;
+    int32_t *out;             /* [R] */
+    double *trace;            /* [R, 3] or NULL */
+    int64_t r0, r1;
+    int status;
+} ref_sample_job_t;
+
+/* One row: returns the token, or -1 on a row error. */
+static int64_t ref_sample_row(const ref_sample_job_t *J, int64_t r, double *l, double *p,
+                              double *tr)
+{
+    const int64_t V = J->V;
+    const double T = J->temperature[r];
+    if (isnan(T) || T < 0 || isinf(T) || (T > 0 && T < (double)FLT_MIN))
+        return -1;
+    ref_load_row(J->logits, J->dtype, (size_t)r, V, l);
+    if (ref_row_invalid(l, V))
+        return -1;
+    if (T == 0) {
+        int64_t a;
+        ref_max_argmax(l, V, &a);
+        return a;
+    }
+    spec_ref_softmax(l, V, T, p);
+    double cell[3];
+    int64_t tok = spec_ref_inverse_cdf(p, V, J->u[r], cell);
+    if (tok >= 0 && tr) {
+        tr[0] = cell[0];
+        tr[1] = cell[1];
+        tr[2] = cell[2];
+    }
+    return tok;
+}
+
+static void *ref_sample_worker(void *arg)
+{
+    ref_sample_job_t *J = (ref_sample_job_t *)arg;
+    double *buf = (double *)malloc(2 * (size_t)J->V * sizeof(double));
+    if (!buf) {
+        J->status = REF_ENOMEM;
+        return NULL;
+    }
+    for (int64_t r = J->r0; r < J->r1; ++r) {
+        double *tr = J->trace ? J->trace + r * 3 : NULL;
+        if (tr)
+            tr[0] = tr[1] = tr[2] = NAN;
+        J->out[r] = (int32_t)ref_sample_row(J, r, buf, buf + J->V, tr);
+    }
+    free(buf);
+    J->status = REF_OK;
+    return NULL;
+}
+
+/*
+ * One token per row of logits [R, V] (fp32 or bf16 bit patterns), split over
+ * `nthreads` host threads (contiguous row ranges; the result does not depend
+ * on the split).  trace (nullable) receives per row the chosen draw cell
+ * [C(x-1)/R, C(x)/R) and the total R (NaN for greedy or error rows).
+ */
+int spec_sample_ref_mt(const void *logits, int dtype, const double *u,
+                       const double *temperature, int64_t R, int64_t V,
+                       int32_t *out_tokens, double *trace, int nthreads)
+{
+    if (!logits || !u || !temperature || !out_tokens)
+        return REF_EINVAL;
+    if (R < 0 || V < 2 || (dtype != REF_F32 && dtype != REF_BF16))
+        return REF_EINVAL;
+    if (R == 0)
+        return REF_OK;
+    if (nthreads < 1)
+        nthreads = 1;
+    if (nthreads > R)
+        nthreads = (int)R;
+    ref_sample_job_t *jobs = (ref_sample_job_t *)calloc((size_t)nthreads, sizeof *jobs);
+    pthread_t *th = (pthread_t *)calloc((size_t)nthreads, sizeof(pthread_t));
+    if (!jobs || !th) {
+        free(jobs);
+        free(th);
+        return REF_ENOMEM;
+    }
+    for (int w = 0; w < nthreads; ++w) {
+        ref_sample_job_t *J = &jobs[w];
+        J->logits = logits;
+        J->dtype = dtype;
+        J->u = u;
+        J->temperature = temperature;
+        J->V = V;
+        J->out = out_tokens;
+        J->trace = trace;
+        J->r0 = R * w / nthreads;
+        J->r1 = R * (w + 1) / nthreads;
+    }
+    int started = 0;
+    if (nthreads > 1)
+        for (int w = 0; w < nthreads; ++w) {
+            if (pthread_create(&th[w], NULL, ref_sample_worker, &jobs[w]) != 0)
+                break;
+            ++started;
+        }
+    for (int w = 0; w < started; ++w)
+        pthread_join(th[w], NULL);
+    for (int w = started; w < nthreads; ++w)
+        ref_sample_worker(&jobs[w]);
+    int status = REF_OK;
+    for (int w = 0; w < nthreads; ++w)
+        if (jobs[w].status != REF_OK)
+            status = jobs[w].status;
+    free(jobs);
+    free(th);
+    return status;
 }
