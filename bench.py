@@ -1,7 +1,7 @@
 """Benchmark of batched speculative-sampling verification on GB300.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                    [--config 4]
+                    [--config 4] [--op verify|sample]
 
 A step is one verification call over one batch of the workload (all accept
 tests, first-rejection scans and correction / bonus draws of every sequence).
@@ -15,6 +15,11 @@ Metric: verified draft positions per second (B*k / step time), summed over
 ranks.  Under torchrun every rank verifies its own batch of B sequences
 (weak scaling: sequences are independent, so there is no collective on the
 data path; one scalar all-reduce takes the max time over ranks).
+
+`--op sample` benchmarks the batched sampler instead (one token per row from
+softmax(logits / T), the draft model's step before verification): a step is
+one spec_sample call over the draft rows of a workload (default workload 5:
+4096 rows of V=128256 bf16, 1.05 GB), metric sampled tokens per second.
 
 Prints one JSON line on rank 0.
 """
@@ -37,8 +42,14 @@ import numpy as np  # noqa: E402
 
 METRIC = "verified draft positions/sec"
 UNIT = "positions/s"
-KERNEL_SRC = os.path.join(ROOT, "speculative_decoding_verification_65_gb300", "csrc",
-                          "spec_verify.cu")
+CSRC = os.path.join(ROOT, "speculative_decoding_verification_65_gb300", "csrc")
+# the sources each timed kernel is built from (keys of profiles/traffic.json)
+KERNEL_SRCS = {
+    "stats_kernel": [os.path.join(CSRC, "spec_verify.cu"), os.path.join(CSRC, "device_common.cuh")],
+    "chunk_kernel": [os.path.join(CSRC, "spec_sample.cu"), os.path.join(CSRC, "device_common.cuh")],
+}
+SAMPLE_METRIC = "sampled tokens/sec"
+SAMPLE_UNIT = "tokens/s"
 
 
 def dist_env():
@@ -57,21 +68,24 @@ def measured_peaks():
         return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0}, "fallback"
 
 
-def kernel_source_hash() -> str:
-    with open(KERNEL_SRC, "rb") as f:
-        return hashlib.sha256(f.read()).hexdigest()[:16]
+def kernel_source_hash(kernel: str = "stats_kernel") -> str:
+    h = hashlib.sha256()
+    for path in KERNEL_SRCS[kernel]:
+        with open(path, "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
 
 
-def recorded_traffic(workload: str):
+def recorded_traffic(workload: str, kernel: str = "stats_kernel"):
     """DRAM bytes per launch from an ncu capture, if it was taken on the
-    current kernel source (profiles/traffic.json)."""
+    current kernel sources (profiles/traffic.json)."""
     try:
         with open(os.path.join(ROOT, "profiles", "traffic.json")) as f:
             rec = json.load(f)
     except (OSError, ValueError):
         return None
     ent = rec.get(workload)
-    if not ent or ent.get("kernel_sha") != kernel_source_hash():
+    if not ent or ent.get("kernel") != kernel or ent.get("kernel_sha") != kernel_source_hash(kernel):
         return None
     return ent.get("dram_bytes_per_launch")
 
@@ -365,19 +379,237 @@ def run_ours(args):
         dist.destroy_process_group()
 
 
+# ------------------------------------------------------------------ sampling
+
+def make_sample_workload(cfg: int, rank: int, batch=None):
+    from speculative_decoding_verification_65_gb300 import synth
+    return synth.make_sample_config(cfg, B=batch, seed_offset=100 * rank)
+
+
+def time_oracle_sample(sc, budget_s: float, threads: int):
+    """Oracle sampling throughput on a bounded sample: blocks of rows until the
+    time budget is spent or every row is done."""
+    import oracle
+    done, t_used = 0, 0.0
+    block = max(4 * threads, 64)
+    while done < sc.R and t_used < budget_s:
+        sl = slice(done, min(sc.R, done + block))
+        t0 = time.perf_counter()
+        oracle.sample(sc.logits[sl], sc.u[sl], sc.temperature[sl], nthreads=threads,
+                      want_trace=False)
+        t_used += time.perf_counter() - t0
+        done = sl.stop
+    return done / t_used, done, t_used
+
+
+def sample_workload_name(args, sc):
+    return sc.name if args.batch is None else f"{sc.name} (B={args.batch} of workload {args.config})"
+
+
+def run_reference_sample(args):
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return
+    import oracle
+    oracle.build()
+    sc = make_sample_workload(args.config, 0, args.batch)
+    cores = host_cores()
+    per_step = min(sc.R, max(4 * cores, 64))
+    sl = slice(0, per_step)
+    run = lambda: oracle.sample(sc.logits[sl], sc.u[sl], sc.temperature[sl], nthreads=cores,
+                                want_trace=False)
+    for _ in range(args.warmup):
+        run()
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        run()
+    dt = time.perf_counter() - t0
+    value = per_step * args.steps / dt
+    line = {
+        "impl": "reference", "metric": SAMPLE_METRIC, "value": value, "unit": SAMPLE_UNIT,
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": dt / args.steps * 1e3, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": sample_workload_name(args, sc), "R": per_step, "V": sc.V,
+                   "input_dtype": sc.dtype,
+                   "what": "fp64 CPU oracle (plain C, threads over rows)"},
+        "cpu_baseline": {"value": value, "unit": SAMPLE_UNIT, "cores": cores, "kind": "oracle",
+                         "sample": f"first {per_step} of {sc.R} rows per step"},
+        "e2e": {"value": value, "unit": SAMPLE_UNIT, "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def run_ours_sample(args):
+    import torch
+
+    import speculative_decoding_verification_65_gb300 as sv
+    from speculative_decoding_verification_65_gb300 import synth
+
+    rank, world, local = dist_env()
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+
+    def barrier():
+        if world > 1:
+            import torch.distributed as dist
+            dist.barrier()
+
+    def max_over_ranks(x):
+        if world > 1:
+            import torch.distributed as dist
+            t = torch.tensor([x], device=dev)
+            dist.all_reduce(t, op=dist.ReduceOp.MAX)
+            return float(t.item())
+        return x
+
+    sc = make_sample_workload(args.config, rank, args.batch)
+    R, V = sc.R, sc.V
+    d = sv.sample_to_device(sc, dev)
+    dt_code = sv.SPEC_F32 if sc.dtype == synth.F32 else sv.SPEC_BF16
+    stream = torch.cuda.current_stream(dev)
+    ws = sv.sample_workspace(R, V, dt_code, dev, stream)
+    out = torch.empty((R,), dtype=torch.int32, device=dev)
+    alg_bytes = synth.sample_bytes(sc)
+
+    def step(events=None):
+        if events is None:
+            sv.spec_sample(**d, out=out, ws=ws, stream=stream)
+        else:
+            sv.spec_sample_timed(**d, out=out, ws=ws, stage_events=events, stream=stream)
+
+    for _ in range(max(args.warmup, 3)):
+        step()
+    torch.cuda.synchronize(dev)
+    if sv.spec_verify_read_status(ws) != sv.SPEC_DEV_OK:
+        raise RuntimeError("device status nonzero after warm-up")
+
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    barrier()
+    torch.cuda.synchronize(dev)
+    with ClockSampler(local) as clk:  # the timed region: K whole sampling calls
+        t0.record(stream)
+        for _ in range(args.steps):
+            step()
+        t1.record(stream)
+        torch.cuda.synchronize(dev)
+    barrier()
+    total_ms = max_over_ranks(t0.elapsed_time(t1))
+
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    stages = [[torch.cuda.Event(enable_timing=True) for _ in range(sv.SPEC_SAMPLE_STAGES)]
+              for _ in range(args.steps)]
+    for ev in [e for row in stages for e in row]:
+        ev.record(stream)
+    torch.cuda.synchronize(dev)
+    for i in range(args.steps):
+        starts[i].record(stream)
+        step(stages[i])
+    torch.cuda.synchronize(dev)
+    kern_ms = [s.elapsed_time(e[0]) for s, e in zip(starts, stages)]
+    pick_ms = statistics.mean(e[0].elapsed_time(e[1]) for e in stages)
+    ms_per_step = total_ms / args.steps
+    value = world * R * args.steps / (total_ms / 1e3)
+    status = sv.spec_verify_read_status(ws)
+
+    # end to end through the C ABI on pinned host buffers
+    if sc.dtype == synth.BF16:
+        h_l = torch.from_numpy(sc.logits.view(np.int16)).pin_memory().view(torch.bfloat16)
+    else:
+        h_l = torch.from_numpy(sc.logits).pin_memory()
+    h_u = torch.from_numpy(sc.u).pin_memory()
+    h_T = torch.from_numpy(sc.temperature).pin_memory()
+    h_o = torch.empty((R,), dtype=torch.int32).pin_memory()
+    del d
+    torch.cuda.empty_cache()
+    arena = torch.empty(sv.spec_sample_host_arena_size(R, V, dt_code), dtype=torch.uint8,
+                        device=dev)
+    e2e_steps = max(1, min(args.steps, 20))
+    sv.spec_sample_host(h_l, h_u, h_T, arena, h_o, stream=stream)
+    barrier()
+    e0 = time.perf_counter()
+    for _ in range(e2e_steps):
+        sv.spec_sample_host(h_l, h_u, h_T, arena, h_o, stream=stream)
+    e2e_s = max_over_ranks(time.perf_counter() - e0)
+    e2e_value = world * R * e2e_steps / e2e_s
+    h2d = sum(int(x.numel() * x.element_size()) for x in (h_l, h_u, h_T))
+
+    if rank != 0:
+        if world > 1:
+            import torch.distributed as dist
+            dist.destroy_process_group()
+        return
+    peaks, peak_src = measured_peaks()
+    kern_avg_s = statistics.mean(kern_ms) / 1e3
+    achieved = alg_bytes / kern_avg_s / 1e9
+    peak = float(peaks.get("hbm_gbs", 6800.0))
+    workload = sample_workload_name(args, sc)
+    cpu = None
+    if world == 1 and not args.no_cpu_baseline:
+        cores = host_cores()
+        v, n_rows, used = time_oracle_sample(sc, args.cpu_budget, cores)
+        cpu = {"value": v, "unit": SAMPLE_UNIT, "cores": cores, "kind": "oracle",
+               "sample": f"{n_rows} of {R} rows of {workload}, {used:.1f} s on {cores} threads"}
+    line = {
+        "metric": SAMPLE_METRIC, "value": value, "unit": SAMPLE_UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": max(args.warmup, 3), "ms_per_step": ms_per_step,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "f32", "data": "synthetic",
+        "config": {"workload": workload, "R_per_gpu": R, "V": V, "input_dtype": sc.dtype,
+                   "algorithmic_bytes_per_step": alg_bytes,
+                   "l2": "inputs larger than L2 (no flush)", "parallelism": f"dp{world}"},
+        "gpu_launches": sv.SPEC_SAMPLE_STAGES * args.steps,
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                     "frac": achieved / peak,
+                     "traffic": recorded_traffic(workload, "chunk_kernel"),
+                     "peak_source": f"{peak_src} copy bandwidth (MEASURED_PEAKS.json hbm_gbs)"
+                     if peak_src == "measured" else "fallback 6.8 TB/s",
+                     "kernel": "chunk_kernel (the one read of the logits)",
+                     "kernel_timing": "CUDA events after each kernel, K further steps",
+                     "kernel_ms_avg": kern_avg_s * 1e3, "kernel_ms_min": min(kern_ms),
+                     "frac_of_nominal_8TBs": achieved / 8000.0,
+                     "step_GBps": alg_bytes / (ms_per_step / 1e3) / 1e9},
+        "stage_ms": {"chunk": kern_avg_s * 1e3, "pick": pick_ms},
+        "clocks": clk.summary(),
+        "e2e": {"value": e2e_value, "unit": SAMPLE_UNIT, "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": R * 4, "steps": e2e_steps},
+        "cpu_baseline": cpu,
+        "device_status": status,
+    }
+    print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=2000)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--config", type=int, default=4, choices=[1, 2, 3, 4, 5])
+    ap.add_argument("--config", type=int, default=None, choices=[1, 2, 3, 4, 5],
+                    help="workload (default 4 for verify, 5 for sample)")
+    ap.add_argument("--op", choices=["verify", "sample"], default="verify")
     ap.add_argument("--batch", type=int, default=None,
                     help="smaller batch of the same recipe (profiling captures only)")
     ap.add_argument("--cpu-budget", type=float, default=10.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()
-    if args.impl == "reference":
+    if args.config is None:
+        args.config = 4 if args.op == "verify" else 5
+    if args.op == "sample":
+        if args.impl == "reference":
+            run_reference_sample(args)
+        else:
+            run_ours_sample(args)
+    elif args.impl == "reference":
         run_reference(args)
     else:
         run_ours(args)

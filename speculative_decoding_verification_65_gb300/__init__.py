@@ -1,7 +1,7 @@
 """GB300-native batched speculative-sampling verification.
 
 Thin Python binding over the C ABI of ``libspecverify.so`` (declared in
-``include/spec_verify.h``).  Every function here only checks and marshals
+``include/spec_verify.h`` and ``include/spec_sample.h``).  Every function here only checks and marshals
 arguments (shapes, dtypes, device pointers, the current CUDA stream) and calls
 the function of the same name in the library; all arithmetic runs in the CUDA
 kernels.  PyTorch is used for device memory and streams only.
@@ -27,6 +27,7 @@ SPEC_DEV_WAIT_TIMEOUT = 1
 SPEC_MAX_K = 32
 SPEC_MAX_V = 1 << 20
 SPEC_STAGES = 4
+SPEC_SAMPLE_STAGES = 2
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "libspecverify.so")
@@ -74,6 +75,16 @@ def library():
         lib.spec_verify_host_arena_size.argtypes = [i32, i32, i32, i32]
         lib.spec_verify_host.restype = i32
         lib.spec_verify_host.argtypes = [vp] * 8 + [i32] * 4 + [vp, sz, vp]
+        lib.spec_sample_workspace_size.restype = sz
+        lib.spec_sample_workspace_size.argtypes = [i32, i32, i32]
+        lib.spec_sample.restype = i32
+        lib.spec_sample.argtypes = [vp] * 4 + [i32] * 3 + [vp, sz, vp]
+        lib.spec_sample_timed.restype = i32
+        lib.spec_sample_timed.argtypes = [vp] * 4 + [i32] * 3 + [vp, sz, vp, vp]
+        lib.spec_sample_host_arena_size.restype = sz
+        lib.spec_sample_host_arena_size.argtypes = [i32, i32, i32]
+        lib.spec_sample_host.restype = i32
+        lib.spec_sample_host.argtypes = [vp] * 4 + [i32] * 3 + [vp, sz, vp]
         _lib = lib
         return lib
 
@@ -136,6 +147,11 @@ def workspace(B: int, k: int, V: int, dtype: int, device=None, stream=None):
     need = spec_verify_workspace_size(B, k, V, dtype)
     if need == 0:
         raise ValueError(f"sizes out of range: B={B} k={k} V={V} dtype={dtype}")
+    return _cached_workspace(need, device, s)
+
+
+def _cached_workspace(need: int, device, s):
+    torch = _torch()
     key = (device.index, s.cuda_stream)
     ws = _ws_cache.get(key)
     if ws is None or ws.numel() < need:
@@ -291,6 +307,73 @@ def spec_verify_host(target, draft, tokens, u_accept, u_resample, temperature,
     return out_tokens, out_num_accepted
 
 
+def spec_sample_workspace_size(R: int, V: int, dtype: int) -> int:
+    return int(library().spec_sample_workspace_size(R, V, dtype))
+
+
+def sample_workspace(R: int, V: int, dtype: int, device=None, stream=None):
+    """A zeroed workspace for spec_sample, shared with spec_verify's cache for
+    the same (device, stream)."""
+    torch = _torch()
+    device = torch.device(device if device is not None else "cuda")
+    if device.index is None:
+        device = torch.device("cuda", torch.cuda.current_device())
+    s = stream if stream is not None else torch.cuda.current_stream(device)
+    need = spec_sample_workspace_size(R, V, dtype)
+    if need == 0:
+        raise ValueError(f"sizes out of range: R={R} V={V} dtype={dtype}")
+    return _cached_workspace(need, device, s)
+
+
+def _marshal_sample(logits, u, temperature):
+    torch = _torch()
+    if logits.dim() != 2:
+        raise ValueError("logits must be [R, V]")
+    R, V = logits.shape
+    dt = _dtype_code(logits)
+    for name, t in (("u", u), ("temperature", temperature)):
+        if tuple(t.shape) != (R,) or t.dtype != torch.float32:
+            raise ValueError(f"{name} must be float32 ({R},), got {t.dtype} {tuple(t.shape)}")
+    for t in (logits, u, temperature):
+        if not t.is_cuda or not t.is_contiguous():
+            raise ValueError("all inputs must be contiguous CUDA tensors")
+        if t.device != logits.device:
+            raise ValueError("all inputs must be on one device")
+    return R, V, dt
+
+
+def spec_sample(logits, u, temperature, out=None, ws=None, stream=None):
+    """One token per row of logits [R, V] (float32 or bfloat16 CUDA tensor)
+    from softmax(logits / T) by inverse CDF with the row's uniform u (float32
+    [R] in [0, 1)); temperature float32 [R], 0 = argmax.  Returns int32 [R]
+    (-1 on a row error); asynchronous like any CUDA op."""
+    torch = _torch()
+    R, V, dt = _marshal_sample(logits, u, temperature)
+    dev = logits.device
+    if out is None:
+        out = torch.empty((R,), dtype=torch.int32, device=dev)
+    if ws is None:
+        ws = sample_workspace(R, V, dt, dev, stream)
+    rc = library().spec_sample(_ptr(logits), _ptr(u), _ptr(temperature), _ptr(out), R, V, dt,
+                               _ptr(ws), ws.numel(), _stream_handle(stream, dev))
+    _check(rc, "spec_sample")
+    return out
+
+
+def spec_sample_timed(logits, u, temperature, out, ws, stage_events, stream=None):
+    """spec_sample recording the given torch.cuda.Event objects
+    (SPEC_SAMPLE_STAGES of them, recorded once beforehand) after each kernel:
+    chunk records, pick."""
+    R, V, dt = _marshal_sample(logits, u, temperature)
+    handles = (ctypes.c_void_p * SPEC_SAMPLE_STAGES)(
+        *[ctypes.c_void_p(e.cuda_event) for e in stage_events])
+    rc = library().spec_sample_timed(_ptr(logits), _ptr(u), _ptr(temperature), _ptr(out), R, V,
+                                     dt, _ptr(ws), ws.numel(),
+                                     _stream_handle(stream, logits.device), handles)
+    _check(rc, "spec_sample_timed")
+    return out
+
+
 def to_device(case, device="cuda"):
     """Copy a synth.Case's host arrays to device tensors (bf16 bit patterns
     become torch.bfloat16)."""
@@ -307,3 +390,42 @@ def to_device(case, device="cuda"):
                 u_accept=torch.from_numpy(case.u_accept).to(device),
                 u_resample=torch.from_numpy(case.u_resample).to(device),
                 temperature=torch.from_numpy(case.temperature).to(device))
+
+
+def spec_sample_host_arena_size(R: int, V: int, dtype: int) -> int:
+    return int(library().spec_sample_host_arena_size(R, V, dtype))
+
+
+def spec_sample_host(logits, u, temperature, arena, out=None, stream=None):
+    """End-to-end call on HOST tensors (CPU, ideally pinned): the library copies
+    the inputs into the device `arena` (a CUDA uint8 tensor of at least
+    spec_sample_host_arena_size bytes), samples, copies the tokens back and
+    synchronises.  Returns the host int32 [R] tokens."""
+    torch = _torch()
+    if logits.is_cuda or logits.dim() != 2:
+        raise ValueError("spec_sample_host takes a host [R, V] tensor")
+    R, V = logits.shape
+    dt = _dtype_code(logits)
+    for t in (logits, u, temperature):
+        if t.is_cuda or not t.is_contiguous():
+            raise ValueError("host inputs must be contiguous CPU tensors")
+    if out is None:
+        out = torch.empty((R,), dtype=torch.int32, pin_memory=True)
+    rc = library().spec_sample_host(_ptr(logits), _ptr(u), _ptr(temperature), _ptr(out), R, V,
+                                    dt, _ptr(arena), arena.numel(),
+                                    _stream_handle(stream, arena.device))
+    _check(rc, "spec_sample_host")
+    return out
+
+
+def sample_to_device(sc, device="cuda"):
+    """Copy a synth.SampleCase's host arrays to device tensors."""
+    import numpy as np
+    torch = _torch()
+    a = sc.logits
+    if a.dtype == np.uint16:
+        logits = torch.from_numpy(a.view(np.int16)).view(torch.bfloat16).to(device)
+    else:
+        logits = torch.from_numpy(a).to(device)
+    return dict(logits=logits, u=torch.from_numpy(sc.u).to(device),
+                temperature=torch.from_numpy(sc.temperature).to(device))

@@ -1,19 +1,25 @@
 """Build libspecverify.so in-tree with nvcc for sm_103a (GB300).
 
-One translation unit, one -gencode, no cmake: a single nvcc invocation that
-takes well under a minute.  The library links the CUDA runtime statically so
-it only needs the driver at run time; PyTorch's own runtime is not involved.
+Two translation units (verification, sampling), one -gencode, no cmake: each
+is compiled by its own nvcc process in parallel, then one nvcc call links the
+shared library.  The library links the CUDA runtime statically so it only
+needs the driver at run time; PyTorch's own runtime is not involved.
 """
 from __future__ import annotations
 
 import os
 import shutil
 import subprocess
+from concurrent.futures import ThreadPoolExecutor
 
 PKG = os.path.dirname(os.path.abspath(__file__))
 ROOT = os.path.dirname(PKG)
-SRC = os.path.join(PKG, "csrc", "spec_verify.cu")
-HDR = os.path.join(ROOT, "include", "spec_verify.h")
+CSRC = os.path.join(PKG, "csrc")
+SRCS = [os.path.join(CSRC, "spec_verify.cu"), os.path.join(CSRC, "spec_sample.cu")]
+DEPS = [os.path.join(CSRC, "device_common.cuh"),
+        os.path.join(ROOT, "include", "spec_verify.h"),
+        os.path.join(ROOT, "include", "spec_sample.h")]
+SRC = SRCS[0]
 LIB = os.path.join(PKG, "libspecverify.so")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
@@ -28,34 +34,52 @@ def nvcc_path() -> str:
     return found
 
 
-def nvcc_command(out: str = LIB, extra=()) -> list:
-    return [nvcc_path(), *ARCH, "-O3", "-lineinfo", "-std=c++17", "--shared",
+def compile_command(src: str, obj: str, extra=()) -> list:
+    return [nvcc_path(), *ARCH, "-O3", "-lineinfo", "-std=c++17", "-c",
             "-Xcompiler", "-fPIC", "-Xcompiler", "-Wall",
-            "-I", os.path.join(ROOT, "include"), "-cudart", "static",
-            *extra, "-o", out, SRC]
+            "-I", os.path.join(ROOT, "include"), *extra, "-o", obj, src]
+
+
+def link_command(objs, out: str) -> list:
+    return [nvcc_path(), *ARCH, "--shared", "-cudart", "static", "-o", out, *objs]
 
 
 def stale() -> bool:
     if not os.path.exists(LIB):
         return True
     t = os.path.getmtime(LIB)
-    return any(os.path.getmtime(p) > t for p in (SRC, HDR, __file__))
+    return any(os.path.getmtime(p) > t for p in (*SRCS, *DEPS, __file__))
+
+
+def _run(cmd, verbose):
+    res = subprocess.run(cmd, capture_output=True, text=True)
+    if verbose or res.returncode != 0:
+        print(" ".join(cmd))
+        print(res.stdout)
+        print(res.stderr)
+    return res.returncode
 
 
 def build(force: bool = False, verbose: bool = False, extra=()) -> str:
     """Compile the CUDA library if it is missing or older than its sources."""
     if not force and not stale() and not extra:
         return LIB
-    tmp = LIB + f".tmp{os.getpid()}"
-    cmd = nvcc_command(tmp, extra)
-    res = subprocess.run(cmd, capture_output=True, text=True)
-    if verbose or res.returncode != 0:
-        print(" ".join(cmd))
-        print(res.stdout)
-        print(res.stderr)
-    if res.returncode != 0:
-        raise RuntimeError("nvcc failed building libspecverify.so")
-    os.replace(tmp, LIB)
+    tag = f".tmp{os.getpid()}"
+    objs = [os.path.join(CSRC, os.path.basename(s) + tag + ".o") for s in SRCS]
+    try:
+        with ThreadPoolExecutor(len(SRCS)) as ex:
+            rcs = list(ex.map(lambda so: _run(compile_command(so[0], so[1], extra), verbose),
+                              zip(SRCS, objs)))
+        if any(rcs):
+            raise RuntimeError("nvcc failed compiling the CUDA sources")
+        tmp = LIB + tag
+        if _run(link_command(objs, tmp), verbose):
+            raise RuntimeError("nvcc failed linking libspecverify.so")
+        os.replace(tmp, LIB)
+    finally:
+        for o in objs:
+            if os.path.exists(o):
+                os.remove(o)
     return LIB
 
 

@@ -1,0 +1,714 @@
+// spec_sample.cu -- GB300 (sm_103a) kernels and C ABI for batched token
+// sampling: one token per row from softmax(logits / T) by inverse CDF with a
+// caller uniform (the draft model's sampling step, "Speculative Decoding and
+// the Art of Fast LLM Inference", "The Algorithm, Step by Step"; the
+// techaiinterview answer, "Algorithm (one round)", step 1).
+//
+// Every logit is read from HBM once.  Two kernels run on the caller's stream:
+//   1. chunk_kernel: persistent and warp-specialised like the verification's
+//      statistics kernel.  A producer warp deals 32 KB row tiles round robin
+//      over CTAs and streams them with cp.async.bulk into a 3-stage
+//      shared-memory ring (mbarriers, bounded waits).  Consumer warp w owns the
+//      contiguous 4 KB chunk w of each tile (lane l reads the 16-byte vectors
+//      256*w + 32*u + l, u < 8) and writes one 8-byte record per chunk:
+//      (chunk maximum M, sum of 2^((x - M) * c)) for a sampled row, with
+//      c = log2(e) / T, or (M, lowest index attaining it) for a greedy row.
+//   2. pick_kernel: one warp per row.  It folds the records into the row
+//      maximum m, scales each chunk's sum by 2^((M - m) * c), takes running
+//      totals (each lane a contiguous range of chunks, then a Kogge-Stone scan
+//      over lanes) up to R, finds the chunk whose total crosses u * R, reads
+//      that one chunk again and searches it in index order (vectors u = 0..7
+//      of the chunk, a Kogge-Stone scan over the 32 lanes of each, elements
+//      left to right in a lane).
+// The exponentials of the search are the ones the first kernel summed, bit
+// for bit; only the order of the sums differs, and a threshold that rounding
+// leaves past the chunk's last running total takes the chunk's last positive
+// weight -- the clamp the method's reading already has for the whole row.
+#include <cuda_runtime.h>
+#include <float.h>
+#include <math.h>
+#include <stdint.h>
+
+#include "spec_sample.h"
+#include "spec_verify.h"
+#include "device_common.cuh"
+
+namespace {
+
+using namespace spec_dev;
+
+constexpr int NCW = 8;                           // consumer warps
+constexpr int WARP_P = NCW;                      // producer warp
+constexpr int NTHREADS = (NCW + 1) * 32;
+constexpr int STAGES = 3;
+constexpr int TILE_BYTES = 32768;
+constexpr int SLOT_BYTES = TILE_BYTES + 128;     // room for a misaligned head/tail
+constexpr int CHUNK_BYTES = 4096;                // one consumer warp's share of a tile
+constexpr int UV = CHUNK_BYTES / (32 * 16);      // vectors per lane per chunk
+constexpr int PICK_WARPS = 8;                    // rows per CTA of the pick kernel
+
+static_assert(NCW * CHUNK_BYTES == TILE_BYTES, "a tile is one chunk per consumer warp");
+
+enum { KIND_END = 0, KIND_TILE = 1 };
+enum { MODE_GREEDY = 1, MODE_SAMPLE = 2 };
+
+struct TileInfo {
+    int kind;
+    int row;
+    int seg;      // tile of the row
+    int mode;
+    float c;      // log2(e) / T
+    int phase0;   // bytes from the copy start to the tile's first element
+    int ncopied0; // bytes present in the slot
+    int pad;
+};
+
+struct SParams {
+    const void *logits;
+    const float *u;
+    const float *temperature;
+    int32_t *out;
+    WsHeader *hdr;
+    float2 *rec;       // [R][NC] chunk records
+    int R, V;
+    int NS;            // tiles per row
+    int NC;            // chunks per row
+    unsigned int total_tiles;
+    unsigned long long bytes;
+};
+
+struct Smem {
+    unsigned long long full[STAGES];
+    unsigned long long empty[STAGES];
+    TileInfo info[STAGES];
+    float tabT[32];    // the producer's temperatures for its next 32 tiles
+};
+
+constexpr size_t SMEM_BYTES = (size_t)STAGES * SLOT_BYTES + sizeof(Smem);
+
+// ----------------------------------------------------------- chunk records
+
+template <int DT>
+__global__ void __launch_bounds__(NTHREADS, 2) chunk_kernel(const SParams P)
+{
+    using L = Lg<DT>;
+    constexpr int VEC = L::VEC;
+    constexpr int SEG = TILE_BYTES / L::ES;  // elements per tile
+    extern __shared__ __align__(128) uint8_t smem_raw[];
+    uint8_t *slots = smem_raw;
+    Smem &S = *reinterpret_cast<Smem *>(smem_raw + (size_t)STAGES * SLOT_BYTES);
+    const int tid = threadIdx.x;
+    const int warp = tid >> 5, lane = tid & 31;
+
+    if (tid == 0) {
+        for (int s = 0; s < STAGES; ++s) {
+            mbar_init(&S.full[s], 1);
+            mbar_init(&S.empty[s], NCW);
+        }
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+    }
+    __syncthreads();
+    allow_next_kernel();
+
+    if (warp == WARP_P) {
+        // ------------------------------------------------------- producer
+        int stage = 0;
+        uint32_t phase = 0;
+        int issued_phase[STAGES];
+        for (int s = 0; s < STAGES; ++s)
+            issued_phase[s] = -1;
+        int ok = 1;
+        const unsigned int G = gridDim.x;
+        for (unsigned int base = blockIdx.x; base < P.total_tiles && ok; base += 32u * G) {
+            // each lane fetches the temperature of one of the next 32 tiles
+            const unsigned long long tl = base + (unsigned long long)lane * G;
+            const float Tl = (tl < P.total_tiles) ? __ldg(P.temperature + tl / (unsigned int)P.NS)
+                                                  : 0.0f;
+            __syncwarp();  // lane 0 is done with the previous batch
+            S.tabT[lane] = Tl;
+            __syncwarp();
+            if (lane == 0) {
+                for (int i = 0; i < 32; ++i) {
+                    const unsigned long long t = base + (unsigned long long)i * G;
+                    if (t >= P.total_tiles)
+                        break;
+                    const float T = S.tabT[i];
+                    if (!temperature_valid(T))
+                        continue;  // the row's token is -1; nobody reads its records
+                    if (!mbar_wait(&S.empty[stage], phase ^ 1u)) {
+                        atomicExch(&P.hdr->status, SPEC_DEV_WAIT_TIMEOUT);
+                        ok = 0;
+                        break;
+                    }
+                    const int row = (int)(t / (unsigned int)P.NS);
+                    const int seg = (int)(t - (unsigned long long)row * (unsigned int)P.NS);
+                    TileInfo &ti = S.info[stage];
+                    ti.kind = KIND_TILE;
+                    ti.row = row;
+                    ti.seg = seg;
+                    ti.mode = (T == 0.0f) ? MODE_GREEDY : MODE_SAMPLE;
+                    ti.c = (T == 0.0f) ? 0.0f : LOG2E / T;
+                    const int e0 = seg * SEG, e1 = min(P.V, e0 + SEG);
+                    const unsigned long long start = ((unsigned long long)row * P.V + e0) * L::ES;
+                    const unsigned long long end = ((unsigned long long)row * P.V + e1) * L::ES;
+                    const unsigned long long a0 = start & ~15ull;
+                    unsigned long long a1 = (end + 15) & ~15ull;
+                    if (a1 > (P.bytes & ~15ull))
+                        a1 = P.bytes & ~15ull;
+                    const uint32_t bytes = (a1 > a0) ? (uint32_t)(a1 - a0) : 0u;
+                    ti.phase0 = (int)(start - a0);
+                    ti.ncopied0 = (int)bytes;
+                    if (bytes) {
+                        mbar_arrive_expect_tx(&S.full[stage], bytes);
+                        bulk_copy_g2s(slots + (size_t)stage * SLOT_BYTES,
+                                      reinterpret_cast<const uint8_t *>(P.logits) + a0, bytes,
+                                      &S.full[stage]);
+                    } else {
+                        mbar_arrive(&S.full[stage]);
+                    }
+                    issued_phase[stage] = (int)phase;
+                    if (++stage == STAGES) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
+                }
+            }
+            ok = __shfl_sync(0xffffffffu, ok, 0);
+        }
+        if (lane != 0)
+            return;
+        if (ok) {
+            if (mbar_wait(&S.empty[stage], phase ^ 1u)) {
+                S.info[stage].kind = KIND_END;
+                mbar_arrive(&S.full[stage]);
+            } else {
+                atomicExch(&P.hdr->status, SPEC_DEV_WAIT_TIMEOUT);
+                ok = 0;
+            }
+        }
+        if (!ok) {
+            // let the copies already issued land before leaving
+            for (int s = 0; s < STAGES; ++s)
+                if (issued_phase[s] >= 0)
+                    (void)mbar_wait(&S.full[s], (uint32_t)issued_phase[s]);
+        }
+        return;
+    }
+
+    // ---------------------------------------------------------- consumers
+    int stage = 0;
+    uint32_t phase = 0;
+    while (true) {
+        if (!mbar_wait(&S.full[stage], phase)) {
+            if (lane == 0)
+                atomicExch(&P.hdr->status, SPEC_DEV_WAIT_TIMEOUT);
+            break;
+        }
+        const TileInfo ti = S.info[stage];
+        if (ti.kind == KIND_END)
+            break;
+        const uint8_t *slot = slots + (size_t)stage * SLOT_BYTES;
+        const int e0 = ti.seg * SEG, e1 = min(P.V, e0 + SEG);
+        const int chunk = ti.seg * NCW + warp;  // chunk index within the row
+        if (chunk < P.NC) {
+            const Seg g = make_seg<DT>(slot, P.logits, (size_t)ti.row, P.V, e0, e1, ti.phase0,
+                                       ti.ncopied0);
+            const int vb = e0 / VEC + warp * (32 * UV);  // row-relative first vector of the chunk
+            uint4 raw[UV];
+            if (g.fast && e1 - e0 == SEG) {
+#pragma unroll
+                for (int u = 0; u < UV; ++u)
+                    raw[u] = ld_shared_v4(slot + (size_t)(warp * 32 * UV + u * 32 + lane) * 16);
+            } else {
+#pragma unroll
+                for (int u = 0; u < UV; ++u)
+                    raw[u] = seg_vec<DT>(g, vb + u * 32 + lane);
+            }
+            float M, second;
+            if (ti.mode == MODE_GREEDY) {
+                float vmax[UV];
+#pragma unroll
+                for (int u = 0; u < UV; ++u)
+                    vmax[u] = L::vmax(raw[u]);
+                float ml = vmax[0];
+#pragma unroll
+                for (int u = 1; u < UV; ++u)
+                    ml = fmax_nan(ml, vmax[u]);
+                M = ml;
+#pragma unroll
+                for (int o = 16; o > 0; o >>= 1)
+                    M = fmax_nan(M, __shfl_xor_sync(0xffffffffu, M, o));
+                // lowest index attaining M: this lane's earliest, then the warp's
+                int idx = INT_MAX;
+#pragma unroll
+                for (int u = 0; u < UV; ++u) {
+                    if (idx == INT_MAX && vmax[u] == M) {
+                        float x[VEC];
+                        L::unpack(raw[u], x);
+#pragma unroll
+                        for (int j = VEC - 1; j >= 0; --j)
+                            if (x[j] == M)
+                                idx = (vb + u * 32 + lane) * VEC + j;
+                    }
+                }
+#pragma unroll
+                for (int o = 16; o > 0; o >>= 1)
+                    idx = min(idx, __shfl_xor_sync(0xffffffffu, idx, o));
+                second = __int_as_float(idx);
+            } else {
+                M = L::tile_max(raw);
+#pragma unroll
+                for (int o = 16; o > 0; o >>= 1)
+                    M = fmax_nan(M, __shfl_xor_sync(0xffffffffu, M, o));
+                float s = 0.0f;
+                if (M != -INFINITY) {
+                    const unsigned long long c2 = f2(ti.c, ti.c);
+                    unsigned long long acc = L::expsum2(raw[0], -M, c2);
+#pragma unroll
+                    for (int u = 1; u < UV; ++u)
+                        acc = add2(acc, L::expsum2(raw[u], -M, c2));
+                    float s0, s1;
+                    f2_split(acc, s0, s1);
+                    s = s0 + s1;
+#pragma unroll
+                    for (int o = 16; o > 0; o >>= 1)
+                        s += __shfl_xor_sync(0xffffffffu, s, o);
+                }
+                second = s;
+            }
+            if (lane == 0)
+                __stcg(P.rec + (size_t)ti.row * P.NC + chunk, make_float2(M, second));
+        }
+        __syncwarp();
+        if (lane == 0)
+            mbar_arrive(&S.empty[stage]);
+        if (++stage == STAGES) {
+            stage = 0;
+            phase ^= 1u;
+        }
+    }
+}
+
+// -------------------------------------------------------------------- pick
+
+// Inclusive Kogge-Stone scan of one value per lane.
+__device__ __forceinline__ float lane_scan(float x, int lane)
+{
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const float y = __shfl_up_sync(0xffffffffu, x, o);
+        if (lane >= o)
+            x = x + y;
+    }
+    return x;
+}
+
+template <int DT>
+__global__ void __launch_bounds__(PICK_WARPS * 32) pick_kernel(const SParams P)
+{
+    using L = Lg<DT>;
+    constexpr int VEC = L::VEC;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int r = blockIdx.x * PICK_WARPS + warp;
+    if (r >= P.R)
+        return;
+    const float T = __ldg(P.temperature + r);
+    const float uu = __ldg(P.u + r);
+    allow_next_kernel();
+    wait_previous_kernel();  // the records come from the chunk kernel
+    if (!temperature_valid(T)) {
+        if (lane == 0)
+            P.out[r] = -1;
+        return;
+    }
+    const bool greedy = (T == 0.0f);
+    const float c = greedy ? 0.0f : LOG2E / T;
+    const float2 *rc = P.rec + (size_t)r * P.NC;
+    const int per = (P.NC + 31) / 32;
+    const int c0 = min(P.NC, lane * per), c1 = min(P.NC, c0 + per);
+
+    // 1. row maximum (and, greedy, the earliest chunk holding it)
+    float ml = -INFINITY;
+    int il = INT_MAX;
+    for (int q = c0; q < c1; ++q) {
+        const float2 f = __ldcg(rc + q);
+        if (f.x > ml && greedy)
+            il = __float_as_int(f.y);
+        ml = fmax_nan(ml, f.x);
+    }
+    float m = ml;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1)
+        m = fmax_nan(m, __shfl_xor_sync(0xffffffffu, m, o));
+    if (isnan(m) || isinf(m)) {  // NaN, +inf, or every logit -inf
+        if (lane == 0)
+            P.out[r] = -1;
+        return;
+    }
+    if (greedy) {
+        int cand = (ml == m) ? il : INT_MAX;
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1)
+            cand = min(cand, __shfl_xor_sync(0xffffffffu, cand, o));
+        if (lane == 0)
+            P.out[r] = cand;
+        return;
+    }
+
+    // 2. running totals of the scaled chunk sums; R = the last
+    float sl = 0.0f;
+    for (int q = c0; q < c1; ++q) {
+        const float2 f = __ldcg(rc + q);
+        sl += rescale(f.y, f.x, m, c);
+    }
+    const float incl = lane_scan(sl, lane);
+    const float Rtot = __shfl_sync(0xffffffffu, incl, 31);
+    const float theta = uu * Rtot;
+    unsigned cross = __ballot_sync(0xffffffffu, incl > theta);
+    int Lw;
+    if (cross) {
+        Lw = __ffs(cross) - 1;
+    } else {
+        const unsigned pos = __ballot_sync(0xffffffffu, sl > 0.0f);
+        Lw = pos ? 31 - __clz(pos) : -1;
+    }
+    if (Lw < 0) {
+        if (lane == 0)
+            P.out[r] = -1;
+        return;
+    }
+    // the crossing lane walks its chunks; the running total before lane Lw is
+    // the inclusive scan of lane Lw - 1
+    const float before_lane = __shfl_sync(0xffffffffu, incl, Lw > 0 ? Lw - 1 : 0);
+    int chunk = -1;
+    float cbefore = 0.0f, Mc = 0.0f, scale = 0.0f;
+    if (lane == Lw) {
+        float C = (Lw > 0) ? before_lane : 0.0f;
+        const int q0 = min(P.NC, Lw * per), q1 = min(P.NC, q0 + per);
+        int lastpos = -1;
+        float lastC = 0.0f;
+        for (int q = q0; q < q1; ++q) {
+            const float2 f = __ldcg(rc + q);
+            const float w = rescale(f.y, f.x, m, c);
+            if (w > 0.0f) {
+                if (C + w > theta) {
+                    chunk = q;
+                    cbefore = C;
+                    break;
+                }
+                lastpos = q;
+                lastC = C;
+            }
+            C += w;
+        }
+        if (chunk < 0) {  // rounding left the threshold past the lane's total
+            chunk = lastpos;
+            cbefore = lastC;
+        }
+        if (chunk >= 0) {
+            const float2 f = __ldcg(rc + chunk);
+            Mc = f.x;
+            scale = ex2((f.x - m) * c);
+        }
+    }
+    chunk = __shfl_sync(0xffffffffu, chunk, Lw);
+    cbefore = __shfl_sync(0xffffffffu, cbefore, Lw);
+    Mc = __shfl_sync(0xffffffffu, Mc, Lw);
+    scale = __shfl_sync(0xffffffffu, scale, Lw);
+    if (chunk < 0) {
+        if (lane == 0)
+            P.out[r] = -1;
+        return;
+    }
+
+    // 3. the chunk again, in index order, in units of 2^((x - Mc) * c)
+    const float tloc = (theta - cbefore) / scale;
+    const unsigned long long c2 = f2(c, c);
+    const int vb = chunk * (32 * UV);
+    float carry = 0.0f;
+    int tok = -1, last_u = -1, last_lane = -1;
+    for (int u = 0; u < UV && tok < 0; ++u) {
+        const int v = vb + u * 32 + lane;
+        const uint4 raw = row_vec<DT>(P.logits, (size_t)r, v, P.V);
+        float e[VEC];
+        L::exp2_vec(raw, -Mc, c2, e);
+        float tau = 0.0f;
+#pragma unroll
+        for (int j = 0; j < VEC; ++j)
+            tau = tau + e[j];
+        const float in_l = lane_scan(tau, lane);
+        const unsigned hit = __ballot_sync(0xffffffffu, carry + in_l > tloc && tau > 0.0f);
+        if (hit) {
+            const int hl = __ffs(hit) - 1;
+            if (lane == hl) {
+                float run = carry + (in_l - tau);
+                int lastj = -1;
+                for (int j = 0; j < VEC; ++j) {
+                    if (e[j] > 0.0f) {
+                        run = run + e[j];
+                        lastj = j;
+                        if (run > tloc) {
+                            tok = v * VEC + j;
+                            break;
+                        }
+                    }
+                }
+                if (tok < 0)
+                    tok = v * VEC + lastj;  // rounding within the lane: its last positive weight
+            }
+            tok = __shfl_sync(0xffffffffu, tok, hl);
+        } else {
+            const unsigned pos = __ballot_sync(0xffffffffu, tau > 0.0f);
+            if (pos) {
+                last_u = u;
+                last_lane = 31 - __clz(pos);
+            }
+            carry = carry + __shfl_sync(0xffffffffu, in_l, 31);
+        }
+    }
+    if (tok < 0 && last_u >= 0) {
+        // rounding left the threshold past the chunk's running total: its
+        // last positive weight
+        const int v = vb + last_u * 32 + last_lane;
+        const uint4 raw = row_vec<DT>(P.logits, (size_t)r, v, P.V);
+        float e[VEC];
+        L::exp2_vec(raw, -Mc, c2, e);
+        int lastj = -1;
+#pragma unroll
+        for (int j = 0; j < VEC; ++j)
+            if (e[j] > 0.0f)
+                lastj = j;
+        tok = v * VEC + lastj;
+    }
+    if (lane == 0)
+        P.out[r] = tok;
+}
+
+// --------------------------------------------------------------- host side
+
+struct DevCache {
+    int sms = 0;
+    int ctas_per_sm[2] = {0, 0};
+    bool attr_set[2] = {false, false};
+};
+DevCache g_dev[64];
+
+size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+bool sizes_ok(int32_t R, int32_t V, int32_t dtype)
+{
+    return R >= 0 && V >= 2 && V <= SPEC_MAX_V && (dtype == SPEC_F32 || dtype == SPEC_BF16);
+}
+
+struct Layout {
+    size_t rec, total;
+    size_t NS, NC;
+};
+
+// header | chunk records [R][NC]
+Layout layout(int32_t R, int32_t V, int32_t dtype)
+{
+    Layout w;
+    const size_t es = (dtype == SPEC_F32) ? 4 : 2;
+    const size_t row_bytes = (size_t)V * es;
+    w.NS = (row_bytes + TILE_BYTES - 1) / TILE_BYTES;
+    w.NC = (row_bytes + CHUNK_BYTES - 1) / CHUNK_BYTES;
+    w.rec = sizeof(WsHeader);
+    w.total = align_up(w.rec + (size_t)R * w.NC * sizeof(float2), 256);
+    return w;
+}
+
+template <int DT>
+int launch_all(const SParams &P, unsigned int grid1, cudaStream_t st, void *const *events)
+{
+    auto mark = [&](int i) {
+        if (events && events[i])
+            cudaEventRecord(reinterpret_cast<cudaEvent_t>(events[i]), st);
+    };
+    chunk_kernel<DT><<<grid1, NTHREADS, SMEM_BYTES, st>>>(P);
+    mark(0);
+    // the pick kernel may start while the chunk kernel drains (programmatic
+    // dependent launch); it waits before reading the records.  Plain order
+    // when stage events are requested.
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned int)((P.R + PICK_WARPS - 1) / PICK_WARPS));
+    cfg.blockDim = dim3(PICK_WARPS * 32);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = events ? 0 : 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    if (cudaLaunchKernelEx(&cfg, pick_kernel<DT>, P) != cudaSuccess)
+        return SPEC_ECUDA;
+    mark(1);
+    if (cudaPeekAtLastError() != cudaSuccess) {
+        (void)cudaGetLastError();
+        return SPEC_ECUDA;
+    }
+    return SPEC_OK;
+}
+
+int launch(const void *logits, const float *u, const float *temp, int32_t *out, int32_t R,
+           int32_t V, int32_t dtype, void *ws, size_t ws_size, void *stream,
+           void *const *events)
+{
+    if (!sizes_ok(R, V, dtype))
+        return SPEC_EINVAL;
+    if (R == 0)
+        return SPEC_OK;
+    if (!logits || !u || !temp || !out || !ws)
+        return SPEC_EINVAL;
+    if ((reinterpret_cast<uintptr_t>(logits) & 15) || (reinterpret_cast<uintptr_t>(ws) & 15) ||
+        (reinterpret_cast<uintptr_t>(u) & 3) || (reinterpret_cast<uintptr_t>(temp) & 3) ||
+        (reinterpret_cast<uintptr_t>(out) & 3))
+        return SPEC_EINVAL;
+    const Layout lay = layout(R, V, dtype);
+    if (ws_size < lay.total)
+        return SPEC_ENOSPACE;
+    const size_t tiles = (size_t)R * lay.NS;
+    if (tiles >= 0x7fffffffull)
+        return SPEC_EINVAL;
+
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64)
+        return SPEC_ECUDA;
+    DevCache &dc = g_dev[dev];
+    const int di = (dtype == SPEC_F32) ? 0 : 1;
+    const void *fn = (dtype == SPEC_F32) ? (const void *)chunk_kernel<SPEC_F32>
+                                         : (const void *)chunk_kernel<SPEC_BF16>;
+    if (!dc.attr_set[di]) {
+        if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 (int)SMEM_BYTES) != cudaSuccess)
+            return SPEC_ECUDA;
+        int n = 0;
+        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, fn, NTHREADS, SMEM_BYTES) != cudaSuccess)
+            return SPEC_ECUDA;
+        int sms = 0;
+        if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+            return SPEC_ECUDA;
+        dc.sms = sms;
+        dc.ctas_per_sm[di] = n > 0 ? n : 1;
+        dc.attr_set[di] = true;
+    }
+    const size_t resident = (size_t)dc.sms * dc.ctas_per_sm[di];
+    const unsigned int grid1 = (unsigned int)(tiles < resident ? tiles : resident);
+
+    SParams P;
+    P.logits = logits;
+    P.u = u;
+    P.temperature = temp;
+    P.out = out;
+    uint8_t *w = reinterpret_cast<uint8_t *>(ws);
+    P.hdr = reinterpret_cast<WsHeader *>(w);
+    P.rec = reinterpret_cast<float2 *>(w + lay.rec);
+    P.R = R;
+    P.V = V;
+    P.NS = (int)lay.NS;
+    P.NC = (int)lay.NC;
+    P.total_tiles = (unsigned int)tiles;
+    P.bytes = (unsigned long long)R * (unsigned long long)V * ((dtype == SPEC_F32) ? 4 : 2);
+
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    return (dtype == SPEC_F32) ? launch_all<SPEC_F32>(P, grid1, st, events)
+                               : launch_all<SPEC_BF16>(P, grid1, st, events);
+}
+
+// host arena: logits | u | temperature | out | workspace, each 256-byte aligned
+struct HostArena {
+    size_t logits, u, temp, out, ws, total;
+};
+
+HostArena host_arena(int32_t R, int32_t V, int32_t dtype)
+{
+    HostArena h;
+    const size_t es = (dtype == SPEC_F32) ? 4 : 2;
+    h.logits = 0;
+    h.u = align_up((size_t)R * V * es, 256);
+    h.temp = h.u + align_up((size_t)R * 4, 256);
+    h.out = h.temp + align_up((size_t)R * 4, 256);
+    h.ws = h.out + align_up((size_t)R * 4, 256);
+    h.total = h.ws + layout(R, V, dtype).total;
+    return h;
+}
+
+}  // namespace
+
+// ------------------------------------------------------------------- C ABI
+
+extern "C" {
+
+size_t spec_sample_workspace_size(int32_t R, int32_t V, int32_t dtype)
+{
+    if (!sizes_ok(R, V, dtype))
+        return 0;
+    return layout(R, V, dtype).total;
+}
+
+int32_t spec_sample(const void *logits, const float *u, const float *temperature,
+                    int32_t *out_tokens, int32_t R, int32_t V, int32_t dtype,
+                    void *workspace, size_t workspace_bytes, void *stream)
+{
+    return launch(logits, u, temperature, out_tokens, R, V, dtype, workspace, workspace_bytes,
+                  stream, nullptr);
+}
+
+int32_t spec_sample_timed(const void *logits, const float *u, const float *temperature,
+                          int32_t *out_tokens, int32_t R, int32_t V, int32_t dtype,
+                          void *workspace, size_t workspace_bytes, void *stream,
+                          void *const *stage_events)
+{
+    return launch(logits, u, temperature, out_tokens, R, V, dtype, workspace, workspace_bytes,
+                  stream, stage_events);
+}
+
+size_t spec_sample_host_arena_size(int32_t R, int32_t V, int32_t dtype)
+{
+    if (!sizes_ok(R, V, dtype))
+        return 0;
+    return host_arena(R, V, dtype).total;
+}
+
+int32_t spec_sample_host(const void *logits, const float *u, const float *temperature,
+                         int32_t *out_tokens, int32_t R, int32_t V, int32_t dtype,
+                         void *device_arena, size_t arena_bytes, void *stream)
+{
+    if (!sizes_ok(R, V, dtype))
+        return SPEC_EINVAL;
+    if (R == 0)
+        return SPEC_OK;
+    if (!logits || !u || !temperature || !out_tokens || !device_arena)
+        return SPEC_EINVAL;
+    if (reinterpret_cast<uintptr_t>(device_arena) & 255)
+        return SPEC_EINVAL;
+    const HostArena h = host_arena(R, V, dtype);
+    if (arena_bytes < h.total)
+        return SPEC_ENOSPACE;
+    const size_t es = (dtype == SPEC_F32) ? 4 : 2;
+    uint8_t *a = reinterpret_cast<uint8_t *>(device_arena);
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    if (cudaMemcpyAsync(a + h.logits, logits, (size_t)R * V * es, cudaMemcpyHostToDevice, st) !=
+            cudaSuccess ||
+        cudaMemcpyAsync(a + h.u, u, (size_t)R * 4, cudaMemcpyHostToDevice, st) != cudaSuccess ||
+        cudaMemcpyAsync(a + h.temp, temperature, (size_t)R * 4, cudaMemcpyHostToDevice, st) !=
+            cudaSuccess)
+        return SPEC_ECUDA;
+    if (cudaMemsetAsync(a + h.ws, 0, sizeof(WsHeader), st) != cudaSuccess)
+        return SPEC_ECUDA;
+    const int rc = launch(a + h.logits, reinterpret_cast<const float *>(a + h.u),
+                          reinterpret_cast<const float *>(a + h.temp),
+                          reinterpret_cast<int32_t *>(a + h.out), R, V, dtype, a + h.ws,
+                          h.total - h.ws, stream, nullptr);
+    if (rc != SPEC_OK)
+        return rc;
+    if (cudaMemcpyAsync(out_tokens, a + h.out, (size_t)R * 4, cudaMemcpyDeviceToHost, st) !=
+        cudaSuccess)
+        return SPEC_ECUDA;
+    if (cudaStreamSynchronize(st) != cudaSuccess)
+        return SPEC_ECUDA;
+    return SPEC_OK;
+}
+
+}  // extern "C"

@@ -308,3 +308,57 @@ def algorithmic_bytes(case: Case) -> int:
     n_sampling = int(np.count_nonzero(case.temperature > 0))
     rows = case.B * (case.k + 1) + n_sampling * case.k
     return rows * case.V * case.elem_size
+
+
+# ------------------------------------------------------------------ sampling
+
+@dataclass
+class SampleCase:
+    """One batch of sampling inputs (host numpy arrays): one token per row."""
+    logits: np.ndarray       # [R, V] float32, or uint16 bf16 bit patterns
+    u: np.ndarray            # [R] float32 in [0, 1)
+    temperature: np.ndarray  # [R] float32 >= 0
+    dtype: str
+    name: str = ""
+
+    @property
+    def R(self) -> int:
+        return int(self.logits.shape[0])
+
+    @property
+    def V(self) -> int:
+        return int(self.logits.shape[1])
+
+    @property
+    def elem_size(self) -> int:
+        return 4 if self.dtype == F32 else 2
+
+
+def sample_case_from(case: Case, seed: int, name: str = "") -> SampleCase:
+    """The draft rows of a verification case as sampling inputs: the logits the
+    draft model samples its k tokens from, each sequence's temperature for its
+    k rows, and a fresh uniform per row (numpy PCG64, `seed`)."""
+    R = case.B * case.k
+    logits = np.ascontiguousarray(case.draft.reshape(R, case.V))
+    temperature = np.repeat(case.temperature, case.k).astype(np.float32)
+    u = np.random.default_rng(seed).random(R, dtype=np.float32)
+    return SampleCase(logits, u, temperature, case.dtype,
+                      name or f"draft rows of {case.name}")
+
+
+def make_sample_config(cfg: int, B: int | None = None, V: int | None = None,
+                       k: int | None = None, seed_offset: int = 0,
+                       threads: int | None = None) -> SampleCase:
+    """Sampling workload from workload `cfg`'s draft rows (R = B*k rows)."""
+    case = make_config(cfg, B=B, V=V, k=k, seed_offset=seed_offset, threads=threads)
+    name = (f"sample_R{case.B * case.k}_V{case.V}_{case.dtype}_cfg{cfg}rows"
+            if B is None and V is None and k is None else "")
+    return sample_case_from(case, seed=1000 * cfg + 3 + seed_offset, name=name)
+
+
+def sample_bytes(sc: SampleCase) -> int:
+    """Bytes a sampling call must read once: every row of every valid-T row
+    (rows whose temperature is invalid are never read)."""
+    T = sc.temperature
+    ok = ~(np.isnan(T) | (T < 0) | np.isinf(T) | ((T > 0) & (T < np.finfo(np.float32).tiny)))
+    return int(np.count_nonzero(ok)) * sc.V * sc.elem_size

@@ -129,3 +129,50 @@ def test_binding_fails_loudly_without_library(tmp_path, monkeypatch):
     monkeypatch.setattr(sv, "_lib", None)
     with pytest.raises(sv.SpecVerifyError):
         sv.library()
+
+
+# ------------------------------------------------------------ spec_sample
+
+@pytest.mark.parametrize("R,V,dt,ok", [
+    (4096, 128256, 1, True), (1, 2, 0, True), (0, 2, 0, True), (3, (1 << 20), 0, True),
+    (1, 1, 0, False), (-1, 8, 0, False), (1, (1 << 20) + 1, 1, False), (1, 8, 3, False),
+])
+def test_sample_workspace_size(lib, R, V, dt, ok):
+    n = sv.spec_sample_workspace_size(R, V, dt)
+    if not ok:
+        assert n == 0
+        return
+    es = 4 if dt == 0 else 2
+    chunks = -(-(V * es) // 4096)  # one 8-byte record per 4 KB chunk of a row
+    assert n == -(-(256 + R * chunks * 8) // 256) * 256
+
+
+def _scall(lib, ptrs, R=2, V=100, dt=0, wsb=1 << 20):
+    args = [ctypes.c_void_p(p) for p in ptrs[:4]]
+    return lib.spec_sample(*args, R, V, dt, ctypes.c_void_p(ptrs[4]), wsb, None)
+
+
+def test_sample_zero_rows_is_noop(lib):
+    assert _scall(lib, [0] * 5, R=0) == sv.SPEC_OK
+
+
+@pytest.mark.parametrize("which", range(5))
+def test_sample_null_pointer_rejected(lib, which):
+    p = list(GOOD[:5])
+    p[which] = 0
+    assert _scall(lib, p) == sv.SPEC_EINVAL
+
+
+@pytest.mark.parametrize("which,off", [(0, 8), (1, 2), (2, 2), (3, 2), (4, 8)])
+def test_sample_misaligned_pointer_rejected(lib, which, off):
+    p = list(GOOD[:5])
+    p[which] += off
+    assert _scall(lib, p) == sv.SPEC_EINVAL
+
+
+def test_sample_bad_sizes_and_small_workspace(lib):
+    assert _scall(lib, GOOD, V=1) == sv.SPEC_EINVAL
+    assert _scall(lib, GOOD, dt=7) == sv.SPEC_EINVAL
+    assert _scall(lib, GOOD, R=-3) == sv.SPEC_EINVAL
+    need = sv.spec_sample_workspace_size(2, 100, 0)
+    assert _scall(lib, GOOD, wsb=need - 1) == sv.SPEC_ENOSPACE
