@@ -6,13 +6,16 @@
 //
 // Every logit is read from HBM once.  Two kernels run on the caller's stream:
 //   1. chunk_kernel: persistent and warp-specialised like the verification's
-//      statistics kernel.  A producer warp deals 32 KB row tiles round robin
-//      over CTAs and streams them with cp.async.bulk into a 3-stage
+//      statistics kernel.  A producer warp deals groups of four consecutive
+//      32 KB tiles of a row round robin over CTAs and streams the tiles with
+//      cp.async.bulk into a 3-stage
 //      shared-memory ring (mbarriers, bounded waits).  Consumer warp w owns the
 //      contiguous 4 KB chunk w of each tile (lane l reads the 16-byte vectors
 //      256*w + 32*u + l, u < 8) and writes one 8-byte record per chunk:
 //      (chunk maximum M, sum of 2^((x - M) * c)) for a sampled row, with
 //      c = log2(e) / T, or (M, lowest index attaining it) for a greedy row.
+//      A lane sums 2^((x - m_l) * c) against its own maximum m_l and scales
+//      the sum by 2^((m_l - M) * c) once, after the warp maximum is known.
 //   2. pick_kernel: one warp per row.  It folds the records into the row
 //      maximum m, scales each chunk's sum by 2^((M - m) * c), takes running
 //      totals (each lane a contiguous range of chunks, then a Kogge-Stone scan
@@ -20,10 +23,12 @@
 //      that one chunk again and searches it in index order (vectors u = 0..7
 //      of the chunk, a Kogge-Stone scan over the 32 lanes of each, elements
 //      left to right in a lane).
-// The exponentials of the search are the ones the first kernel summed, bit
-// for bit; only the order of the sums differs, and a threshold that rounding
-// leaves past the chunk's last running total takes the chunk's last positive
-// weight -- the clamp the method's reading already has for the whole row.
+// The first kernel sums each lane's exponentials relative to the lane's own
+// maximum and rescales the lane sums to the chunk maximum; the search takes
+// them relative to the chunk maximum directly.  The two agree to fp32
+// rounding, and a threshold that rounding leaves past the chunk's last running
+// total takes the chunk's last positive weight -- the clamp the method's
+// reading already has for the whole row.
 #include <cuda_runtime.h>
 #include <float.h>
 #include <math.h>
@@ -46,6 +51,7 @@ constexpr int SLOT_BYTES = TILE_BYTES + 128;     // room for a misaligned head/t
 constexpr int CHUNK_BYTES = 4096;                // one consumer warp's share of a tile
 constexpr int UV = CHUNK_BYTES / (32 * 16);      // vectors per lane per chunk
 constexpr int PICK_WARPS = 8;                    // rows per CTA of the pick kernel
+constexpr int GROUP = 8;                         // consecutive tiles of a row per deal
 
 static_assert(NCW * CHUNK_BYTES == TILE_BYTES, "a tile is one chunk per consumer warp");
 
@@ -73,7 +79,8 @@ struct SParams {
     int R, V;
     int NS;            // tiles per row
     int NC;            // chunks per row
-    unsigned int total_tiles;
+    int NG;            // groups of GROUP tiles per row
+    unsigned int total_groups;
     unsigned long long bytes;
 };
 
@@ -81,7 +88,7 @@ struct Smem {
     unsigned long long full[STAGES];
     unsigned long long empty[STAGES];
     TileInfo info[STAGES];
-    float tabT[32];    // the producer's temperatures for its next 32 tiles
+    float tabT[32];    // the producer's temperatures for its next 32 groups
 };
 
 constexpr size_t SMEM_BYTES = (size_t)STAGES * SLOT_BYTES + sizeof(Smem);
@@ -120,57 +127,62 @@ __global__ void __launch_bounds__(NTHREADS, 2) chunk_kernel(const SParams P)
             issued_phase[s] = -1;
         int ok = 1;
         const unsigned int G = gridDim.x;
-        for (unsigned int base = blockIdx.x; base < P.total_tiles && ok; base += 32u * G) {
-            // each lane fetches the temperature of one of the next 32 tiles
-            const unsigned long long tl = base + (unsigned long long)lane * G;
-            const float Tl = (tl < P.total_tiles) ? __ldg(P.temperature + tl / (unsigned int)P.NS)
-                                                  : 0.0f;
+        // groups of GROUP consecutive tiles of one row are dealt round robin
+        for (unsigned int base = blockIdx.x; base < P.total_groups && ok; base += 32u * G) {
+            // each lane fetches the temperature of one of the next 32 groups
+            const unsigned long long gl = base + (unsigned long long)lane * G;
+            const float Tl = (gl < P.total_groups) ? __ldg(P.temperature + gl / (unsigned int)P.NG)
+                                                   : 0.0f;
             __syncwarp();  // lane 0 is done with the previous batch
             S.tabT[lane] = Tl;
             __syncwarp();
             if (lane == 0) {
-                for (int i = 0; i < 32; ++i) {
-                    const unsigned long long t = base + (unsigned long long)i * G;
-                    if (t >= P.total_tiles)
+                for (int i = 0; i < 32 && ok; ++i) {
+                    const unsigned long long gi = base + (unsigned long long)i * G;
+                    if (gi >= P.total_groups)
                         break;
                     const float T = S.tabT[i];
                     if (!temperature_valid(T))
                         continue;  // the row's token is -1; nobody reads its records
-                    if (!mbar_wait(&S.empty[stage], phase ^ 1u)) {
-                        atomicExch(&P.hdr->status, SPEC_DEV_WAIT_TIMEOUT);
-                        ok = 0;
-                        break;
-                    }
-                    const int row = (int)(t / (unsigned int)P.NS);
-                    const int seg = (int)(t - (unsigned long long)row * (unsigned int)P.NS);
-                    TileInfo &ti = S.info[stage];
-                    ti.kind = KIND_TILE;
-                    ti.row = row;
-                    ti.seg = seg;
-                    ti.mode = (T == 0.0f) ? MODE_GREEDY : MODE_SAMPLE;
-                    ti.c = (T == 0.0f) ? 0.0f : LOG2E / T;
-                    const int e0 = seg * SEG, e1 = min(P.V, e0 + SEG);
-                    const unsigned long long start = ((unsigned long long)row * P.V + e0) * L::ES;
-                    const unsigned long long end = ((unsigned long long)row * P.V + e1) * L::ES;
-                    const unsigned long long a0 = start & ~15ull;
-                    unsigned long long a1 = (end + 15) & ~15ull;
-                    if (a1 > (P.bytes & ~15ull))
-                        a1 = P.bytes & ~15ull;
-                    const uint32_t bytes = (a1 > a0) ? (uint32_t)(a1 - a0) : 0u;
-                    ti.phase0 = (int)(start - a0);
-                    ti.ncopied0 = (int)bytes;
-                    if (bytes) {
-                        mbar_arrive_expect_tx(&S.full[stage], bytes);
-                        bulk_copy_g2s(slots + (size_t)stage * SLOT_BYTES,
-                                      reinterpret_cast<const uint8_t *>(P.logits) + a0, bytes,
-                                      &S.full[stage]);
-                    } else {
-                        mbar_arrive(&S.full[stage]);
-                    }
-                    issued_phase[stage] = (int)phase;
-                    if (++stage == STAGES) {
-                        stage = 0;
-                        phase ^= 1u;
+                    const int row = (int)(gi / (unsigned int)P.NG);
+                    const int grp = (int)(gi - (unsigned long long)row * (unsigned int)P.NG);
+                    const int seg1 = min(P.NS, (grp + 1) * GROUP);
+                    for (int seg = grp * GROUP; seg < seg1; ++seg) {
+                        if (!mbar_wait(&S.empty[stage], phase ^ 1u)) {
+                            atomicExch(&P.hdr->status, SPEC_DEV_WAIT_TIMEOUT);
+                            ok = 0;
+                            break;
+                        }
+                        TileInfo &ti = S.info[stage];
+                        ti.kind = KIND_TILE;
+                        ti.row = row;
+                        ti.seg = seg;
+                        ti.mode = (T == 0.0f) ? MODE_GREEDY : MODE_SAMPLE;
+                        ti.c = (T == 0.0f) ? 0.0f : LOG2E / T;
+                        const int e0 = seg * SEG, e1 = min(P.V, e0 + SEG);
+                        const unsigned long long start =
+                            ((unsigned long long)row * P.V + e0) * L::ES;
+                        const unsigned long long end = ((unsigned long long)row * P.V + e1) * L::ES;
+                        const unsigned long long a0 = start & ~15ull;
+                        unsigned long long a1 = (end + 15) & ~15ull;
+                        if (a1 > (P.bytes & ~15ull))
+                            a1 = P.bytes & ~15ull;
+                        const uint32_t bytes = (a1 > a0) ? (uint32_t)(a1 - a0) : 0u;
+                        ti.phase0 = (int)(start - a0);
+                        ti.ncopied0 = (int)bytes;
+                        if (bytes) {
+                            mbar_arrive_expect_tx(&S.full[stage], bytes);
+                            bulk_copy_g2s(slots + (size_t)stage * SLOT_BYTES,
+                                          reinterpret_cast<const uint8_t *>(P.logits) + a0, bytes,
+                                          &S.full[stage]);
+                        } else {
+                            mbar_arrive(&S.full[stage]);
+                        }
+                        issued_phase[stage] = (int)phase;
+                        if (++stage == STAGES) {
+                            stage = 0;
+                            phase ^= 1u;
+                        }
                     }
                 }
             }
@@ -257,24 +269,29 @@ __global__ void __launch_bounds__(NTHREADS, 2) chunk_kernel(const SParams P)
                     idx = min(idx, __shfl_xor_sync(0xffffffffu, idx, o));
                 second = __int_as_float(idx);
             } else {
-                M = L::tile_max(raw);
-#pragma unroll
-                for (int o = 16; o > 0; o >>= 1)
-                    M = fmax_nan(M, __shfl_xor_sync(0xffffffffu, M, o));
+                // exponentials relative to the lane's own maximum, so they need
+                // no warp-wide value; the lane sums are rescaled to the chunk
+                // maximum at the end
+                const float ml = L::tile_max(raw);
                 float s = 0.0f;
-                if (M != -INFINITY) {
+                if (ml != -INFINITY) {
                     const unsigned long long c2 = f2(ti.c, ti.c);
-                    unsigned long long acc = L::expsum2(raw[0], -M, c2);
+                    unsigned long long acc = L::expsum2(raw[0], -ml, c2);
 #pragma unroll
                     for (int u = 1; u < UV; ++u)
-                        acc = add2(acc, L::expsum2(raw[u], -M, c2));
+                        acc = add2(acc, L::expsum2(raw[u], -ml, c2));
                     float s0, s1;
                     f2_split(acc, s0, s1);
                     s = s0 + s1;
-#pragma unroll
-                    for (int o = 16; o > 0; o >>= 1)
-                        s += __shfl_xor_sync(0xffffffffu, s, o);
                 }
+                M = ml;
+#pragma unroll
+                for (int o = 16; o > 0; o >>= 1)
+                    M = fmax_nan(M, __shfl_xor_sync(0xffffffffu, M, o));
+                s = rescale(s, ml, M, ti.c);
+#pragma unroll
+                for (int o = 16; o > 0; o >>= 1)
+                    s += __shfl_xor_sync(0xffffffffu, s, o);
                 second = s;
             }
             if (lane == 0)
@@ -568,8 +585,9 @@ int launch(const void *logits, const float *u, const float *temp, int32_t *out, 
     const Layout lay = layout(R, V, dtype);
     if (ws_size < lay.total)
         return SPEC_ENOSPACE;
-    const size_t tiles = (size_t)R * lay.NS;
-    if (tiles >= 0x7fffffffull)
+    const size_t NG = (lay.NS + GROUP - 1) / GROUP;
+    const size_t groups = (size_t)R * NG;
+    if ((size_t)R * lay.NS >= 0x7fffffffull)
         return SPEC_EINVAL;
 
     int dev = 0;
@@ -594,7 +612,7 @@ int launch(const void *logits, const float *u, const float *temp, int32_t *out, 
         dc.attr_set[di] = true;
     }
     const size_t resident = (size_t)dc.sms * dc.ctas_per_sm[di];
-    const unsigned int grid1 = (unsigned int)(tiles < resident ? tiles : resident);
+    const unsigned int grid1 = (unsigned int)(groups < resident ? groups : resident);
 
     SParams P;
     P.logits = logits;
@@ -608,7 +626,8 @@ int launch(const void *logits, const float *u, const float *temp, int32_t *out, 
     P.V = V;
     P.NS = (int)lay.NS;
     P.NC = (int)lay.NC;
-    P.total_tiles = (unsigned int)tiles;
+    P.NG = (int)NG;
+    P.total_groups = (unsigned int)groups;
     P.bytes = (unsigned long long)R * (unsigned long long)V * ((dtype == SPEC_F32) ? 4 : 2);
 
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
