@@ -469,4 +469,164 @@ __device__ __forceinline__ bool temperature_valid(float T)
     return !(isnan(T) || T < 0.0f || isinf(T) || (T > 0.0f && T < FLT_MIN));
 }
 
+// ------------------------------------------------------ draws from chunk records
+//
+// A row summarised by chunk records: chunk q is the contiguous 4 KB of the row
+// starting at byte 4096*q (lane l of the chunk holds its 16-byte vectors
+// 256*q + 32*u + l, u < CHUNK_UV), and its record is (M_q, S_q) = the chunk
+// maximum and the sum of 2^((x - M_q) * c) over it.
+
+constexpr int CHUNK_BYTES = 4096;
+constexpr int CHUNK_UV = CHUNK_BYTES / (32 * 16);  // vectors per lane per chunk
+
+// Inclusive Kogge-Stone scan of one value per lane.
+__device__ __forceinline__ float lane_scan(float x, int lane)
+{
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const float y = __shfl_up_sync(0xffffffffu, x, o);
+        if (lane >= o)
+            x = x + y;
+    }
+    return x;
+}
+
+// Inverse-CDF draw with uniform u from weights 2^((x - m) * c), m the row
+// maximum, for one row given its NC chunk records (one warp; every lane gets
+// the result).  C(x) runs over the chunks' scaled sums S_q * 2^((M_q - m) * c)
+// in chunk order, then, inside the crossing chunk (read again from `logits`),
+// over its elements in index order; the token is the smallest x with
+// C(x) > u * R.  A threshold that rounding leaves past a running total takes
+// the last positive weight before it.  Returns -1 if no weight is positive.
+template <int DT>
+__device__ int records_draw(const float2 *rc, int NC, float m, float c, float u,
+                            const void *logits, size_t row, int V, int lane)
+{
+    using L = Lg<DT>;
+    constexpr int VEC = L::VEC;
+    const int per = (NC + 31) / 32;
+    const int c0 = min(NC, lane * per), c1 = min(NC, c0 + per);
+    // running totals of the scaled chunk sums (each lane a contiguous range,
+    // then a scan over lanes); R = the last
+    float sl = 0.0f;
+    for (int q = c0; q < c1; ++q) {
+        const float2 f = __ldcg(rc + q);
+        sl += rescale(f.y, f.x, m, c);
+    }
+    const float incl = lane_scan(sl, lane);
+    const float Rtot = __shfl_sync(0xffffffffu, incl, 31);
+    const float theta = u * Rtot;
+    unsigned cross = __ballot_sync(0xffffffffu, incl > theta);
+    int Lw;
+    if (cross) {
+        Lw = __ffs(cross) - 1;
+    } else {
+        const unsigned pos = __ballot_sync(0xffffffffu, sl > 0.0f);
+        Lw = pos ? 31 - __clz(pos) : -1;
+    }
+    if (Lw < 0)
+        return -1;
+    // the crossing lane walks its chunks; the running total before lane Lw is
+    // the inclusive scan of lane Lw - 1
+    const float before_lane = __shfl_sync(0xffffffffu, incl, Lw > 0 ? Lw - 1 : 0);
+    int chunk = -1;
+    float cbefore = 0.0f, Mc = 0.0f, scale = 0.0f;
+    if (lane == Lw) {
+        float C = (Lw > 0) ? before_lane : 0.0f;
+        const int q0 = min(NC, Lw * per), q1 = min(NC, q0 + per);
+        int lastpos = -1;
+        float lastC = 0.0f;
+        for (int q = q0; q < q1; ++q) {
+            const float2 f = __ldcg(rc + q);
+            const float w = rescale(f.y, f.x, m, c);
+            if (w > 0.0f) {
+                if (C + w > theta) {
+                    chunk = q;
+                    cbefore = C;
+                    break;
+                }
+                lastpos = q;
+                lastC = C;
+            }
+            C += w;
+        }
+        if (chunk < 0) {  // rounding left the threshold past the lane's total
+            chunk = lastpos;
+            cbefore = lastC;
+        }
+        if (chunk >= 0) {
+            const float2 f = __ldcg(rc + chunk);
+            Mc = f.x;
+            scale = ex2((f.x - m) * c);
+        }
+    }
+    chunk = __shfl_sync(0xffffffffu, chunk, Lw);
+    cbefore = __shfl_sync(0xffffffffu, cbefore, Lw);
+    Mc = __shfl_sync(0xffffffffu, Mc, Lw);
+    scale = __shfl_sync(0xffffffffu, scale, Lw);
+    if (chunk < 0)
+        return -1;
+
+    // the chunk again, in index order, in units of 2^((x - Mc) * c)
+    const float tloc = (theta - cbefore) / scale;
+    const unsigned long long c2 = f2(c, c);
+    const int vb = chunk * (32 * CHUNK_UV);
+    float carry = 0.0f;
+    int tok = -1, last_u = -1, last_lane = -1;
+    for (int uv = 0; uv < CHUNK_UV && tok < 0; ++uv) {
+        const int v = vb + uv * 32 + lane;
+        const uint4 raw = row_vec<DT>(logits, row, v, V);
+        float e[VEC];
+        L::exp2_vec(raw, -Mc, c2, e);
+        float tau = 0.0f;
+#pragma unroll
+        for (int j = 0; j < VEC; ++j)
+            tau = tau + e[j];
+        const float in_l = lane_scan(tau, lane);
+        const unsigned hit = __ballot_sync(0xffffffffu, carry + in_l > tloc && tau > 0.0f);
+        if (hit) {
+            const int hl = __ffs(hit) - 1;
+            if (lane == hl) {
+                float run = carry + (in_l - tau);
+                int lastj = -1;
+                for (int j = 0; j < VEC; ++j) {
+                    if (e[j] > 0.0f) {
+                        run = run + e[j];
+                        lastj = j;
+                        if (run > tloc) {
+                            tok = v * VEC + j;
+                            break;
+                        }
+                    }
+                }
+                if (tok < 0)
+                    tok = v * VEC + lastj;  // rounding within the lane: its last positive weight
+            }
+            tok = __shfl_sync(0xffffffffu, tok, hl);
+        } else {
+            const unsigned pos = __ballot_sync(0xffffffffu, tau > 0.0f);
+            if (pos) {
+                last_u = uv;
+                last_lane = 31 - __clz(pos);
+            }
+            carry = carry + __shfl_sync(0xffffffffu, in_l, 31);
+        }
+    }
+    if (tok < 0 && last_u >= 0) {
+        // rounding left the threshold past the chunk's running total: its
+        // last positive weight
+        const int v = vb + last_u * 32 + last_lane;
+        const uint4 raw = row_vec<DT>(logits, row, v, V);
+        float e[VEC];
+        L::exp2_vec(raw, -Mc, c2, e);
+        int lastj = -1;
+#pragma unroll
+        for (int j = 0; j < VEC; ++j)
+            if (e[j] > 0.0f)
+                lastj = j;
+        tok = v * VEC + lastj;
+    }
+    return tok;
+}
+
 }  // namespace spec_dev

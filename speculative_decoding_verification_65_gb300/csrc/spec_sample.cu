@@ -48,8 +48,7 @@ constexpr int NTHREADS = (NCW + 1) * 32;
 constexpr int STAGES = 3;
 constexpr int TILE_BYTES = 32768;
 constexpr int SLOT_BYTES = TILE_BYTES + 128;     // room for a misaligned head/tail
-constexpr int CHUNK_BYTES = 4096;                // one consumer warp's share of a tile
-constexpr int UV = CHUNK_BYTES / (32 * 16);      // vectors per lane per chunk
+constexpr int UV = CHUNK_UV;                     // vectors per lane per chunk
 constexpr int PICK_WARPS = 8;                    // rows per CTA of the pick kernel
 constexpr int GROUP = 8;                         // consecutive tiles of a row per deal
 
@@ -309,23 +308,9 @@ __global__ void __launch_bounds__(NTHREADS, 2) chunk_kernel(const SParams P)
 
 // -------------------------------------------------------------------- pick
 
-// Inclusive Kogge-Stone scan of one value per lane.
-__device__ __forceinline__ float lane_scan(float x, int lane)
-{
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-        const float y = __shfl_up_sync(0xffffffffu, x, o);
-        if (lane >= o)
-            x = x + y;
-    }
-    return x;
-}
-
 template <int DT>
 __global__ void __launch_bounds__(PICK_WARPS * 32) pick_kernel(const SParams P)
 {
-    using L = Lg<DT>;
-    constexpr int VEC = L::VEC;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int r = blockIdx.x * PICK_WARPS + warp;
     if (r >= P.R)
@@ -373,131 +358,7 @@ __global__ void __launch_bounds__(PICK_WARPS * 32) pick_kernel(const SParams P)
         return;
     }
 
-    // 2. running totals of the scaled chunk sums; R = the last
-    float sl = 0.0f;
-    for (int q = c0; q < c1; ++q) {
-        const float2 f = __ldcg(rc + q);
-        sl += rescale(f.y, f.x, m, c);
-    }
-    const float incl = lane_scan(sl, lane);
-    const float Rtot = __shfl_sync(0xffffffffu, incl, 31);
-    const float theta = uu * Rtot;
-    unsigned cross = __ballot_sync(0xffffffffu, incl > theta);
-    int Lw;
-    if (cross) {
-        Lw = __ffs(cross) - 1;
-    } else {
-        const unsigned pos = __ballot_sync(0xffffffffu, sl > 0.0f);
-        Lw = pos ? 31 - __clz(pos) : -1;
-    }
-    if (Lw < 0) {
-        if (lane == 0)
-            P.out[r] = -1;
-        return;
-    }
-    // the crossing lane walks its chunks; the running total before lane Lw is
-    // the inclusive scan of lane Lw - 1
-    const float before_lane = __shfl_sync(0xffffffffu, incl, Lw > 0 ? Lw - 1 : 0);
-    int chunk = -1;
-    float cbefore = 0.0f, Mc = 0.0f, scale = 0.0f;
-    if (lane == Lw) {
-        float C = (Lw > 0) ? before_lane : 0.0f;
-        const int q0 = min(P.NC, Lw * per), q1 = min(P.NC, q0 + per);
-        int lastpos = -1;
-        float lastC = 0.0f;
-        for (int q = q0; q < q1; ++q) {
-            const float2 f = __ldcg(rc + q);
-            const float w = rescale(f.y, f.x, m, c);
-            if (w > 0.0f) {
-                if (C + w > theta) {
-                    chunk = q;
-                    cbefore = C;
-                    break;
-                }
-                lastpos = q;
-                lastC = C;
-            }
-            C += w;
-        }
-        if (chunk < 0) {  // rounding left the threshold past the lane's total
-            chunk = lastpos;
-            cbefore = lastC;
-        }
-        if (chunk >= 0) {
-            const float2 f = __ldcg(rc + chunk);
-            Mc = f.x;
-            scale = ex2((f.x - m) * c);
-        }
-    }
-    chunk = __shfl_sync(0xffffffffu, chunk, Lw);
-    cbefore = __shfl_sync(0xffffffffu, cbefore, Lw);
-    Mc = __shfl_sync(0xffffffffu, Mc, Lw);
-    scale = __shfl_sync(0xffffffffu, scale, Lw);
-    if (chunk < 0) {
-        if (lane == 0)
-            P.out[r] = -1;
-        return;
-    }
-
-    // 3. the chunk again, in index order, in units of 2^((x - Mc) * c)
-    const float tloc = (theta - cbefore) / scale;
-    const unsigned long long c2 = f2(c, c);
-    const int vb = chunk * (32 * UV);
-    float carry = 0.0f;
-    int tok = -1, last_u = -1, last_lane = -1;
-    for (int u = 0; u < UV && tok < 0; ++u) {
-        const int v = vb + u * 32 + lane;
-        const uint4 raw = row_vec<DT>(P.logits, (size_t)r, v, P.V);
-        float e[VEC];
-        L::exp2_vec(raw, -Mc, c2, e);
-        float tau = 0.0f;
-#pragma unroll
-        for (int j = 0; j < VEC; ++j)
-            tau = tau + e[j];
-        const float in_l = lane_scan(tau, lane);
-        const unsigned hit = __ballot_sync(0xffffffffu, carry + in_l > tloc && tau > 0.0f);
-        if (hit) {
-            const int hl = __ffs(hit) - 1;
-            if (lane == hl) {
-                float run = carry + (in_l - tau);
-                int lastj = -1;
-                for (int j = 0; j < VEC; ++j) {
-                    if (e[j] > 0.0f) {
-                        run = run + e[j];
-                        lastj = j;
-                        if (run > tloc) {
-                            tok = v * VEC + j;
-                            break;
-                        }
-                    }
-                }
-                if (tok < 0)
-                    tok = v * VEC + lastj;  // rounding within the lane: its last positive weight
-            }
-            tok = __shfl_sync(0xffffffffu, tok, hl);
-        } else {
-            const unsigned pos = __ballot_sync(0xffffffffu, tau > 0.0f);
-            if (pos) {
-                last_u = u;
-                last_lane = 31 - __clz(pos);
-            }
-            carry = carry + __shfl_sync(0xffffffffu, in_l, 31);
-        }
-    }
-    if (tok < 0 && last_u >= 0) {
-        // rounding left the threshold past the chunk's running total: its
-        // last positive weight
-        const int v = vb + last_u * 32 + last_lane;
-        const uint4 raw = row_vec<DT>(P.logits, (size_t)r, v, P.V);
-        float e[VEC];
-        L::exp2_vec(raw, -Mc, c2, e);
-        int lastj = -1;
-#pragma unroll
-        for (int j = 0; j < VEC; ++j)
-            if (e[j] > 0.0f)
-                lastj = j;
-        tok = v * VEC + lastj;
-    }
+    const int tok = records_draw<DT>(rc, P.NC, m, c, uu, P.logits, (size_t)r, P.V, lane);
     if (lane == 0)
         P.out[r] = tok;
 }

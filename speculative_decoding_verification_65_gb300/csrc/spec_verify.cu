@@ -62,6 +62,8 @@ constexpr int SCAN_WARPS = 8;                    // sequences per CTA in kernels
 
 static_assert(U * NT * 16 == TILE_BYTES, "stats tile must split evenly over consumers");
 static_assert(UD * NT * 16 == HALF_BYTES, "draw tile must split evenly over consumers");
+static_assert(NCW * CHUNK_BYTES == TILE_BYTES, "a stats tile is one 4 KB chunk per consumer warp");
+static_assert(CHUNK_UV == U, "a consumer lane holds one chunk's vectors");
 
 
 enum { KIND_END = 0, KIND_STATS = 1 };
@@ -88,7 +90,8 @@ struct TileInfo {
     float c;       // log2(e) / T
     int phase0;    // bytes from the copy start to the tile's first element
     int ncopied0;  // bytes present in the slot
-    int pad[3];
+    int bonus;     // the bonus row of a sampling sequence: write chunk records
+    int pad[2];
 };
 
 struct Params {
@@ -105,12 +108,14 @@ struct Params {
     float4 *part;      // [B][rows][NSS]
     JobRec *jobs;      // [B]
     float *chunks;     // [B][chunk_stride]
+    float2 *rec;       // [B][NCH] chunk records of each sequence's bonus row
     int B, k, V;
     int NS;            // tiles per row
     int NSS;           // super-tiles per row
     int rows;          // rows per sequence (2k+1)
     int DS;            // draw tiles per row
     int chunk_stride;  // floats of chunk totals per sequence
+    int NCH;           // 4 KB chunks per row
     unsigned int total_super;  // super-tiles in the call
     unsigned long long target_bytes, draft_bytes;
 };
@@ -136,25 +141,29 @@ struct LaneStat {
     int idx;
 };
 
+// Consumer warp w owns the contiguous 4 KB chunk w of a tile: lane l reads the
+// tile's vectors 256*w + 32*u + l, u < U.  `rec` (nullable) receives the
+// chunk's record (maximum, sum of 2^((x - max) * c)) on a bonus row.
 template <int DT>
-__device__ __forceinline__ void tile_accumulate(const Params &P, const Seg &g, int tid, int mode,
-                                                float c, LaneStat &st)
+__device__ __forceinline__ void tile_accumulate(const Seg &g, int warp, int lane, int mode, float c,
+                                                LaneStat &st, float2 *rec)
 {
     using L = Lg<DT>;
     constexpr int VEC = L::VEC;
     const int v0 = g.e0 / VEC;
     const int v1 = (g.e1 + VEC - 1) / VEC;
+    const int base = warp * 32 * U + lane;  // tile-relative vector of u = 0
 
     uint4 raw[U];
     if (g.fast && g.e1 - g.e0 == U * NT * VEC) {
         // a whole tile, copied aligned: every vector is in range
 #pragma unroll
         for (int u = 0; u < U; ++u)
-            raw[u] = ld_shared_v4(g.slot + (size_t)(tid + u * NT) * 16);
+            raw[u] = ld_shared_v4(g.slot + (size_t)(base + u * 32) * 16);
     } else {
 #pragma unroll
         for (int u = 0; u < U; ++u) {
-            const int v = v0 + tid + u * NT;
+            const int v = v0 + base + u * 32;
             raw[u] = (v < v1) ? seg_vec<DT>(g, v) : neg_inf_vec(L::NEG_INF_WORD);
         }
     }
@@ -168,8 +177,8 @@ __device__ __forceinline__ void tile_accumulate(const Params &P, const Seg &g, i
 #pragma unroll
         for (int u = 1; u < U; ++u)
             mt = fmax_nan(mt, vmax[u]);
-        // the first occurrence over the super-tile lies in the earliest tile
-        // holding a strictly larger maximum
+        // the lane's indices grow with u, and the first occurrence over the
+        // super-tile lies in the earliest tile holding a strictly larger maximum
         if (mt > st.m) {
             int idx = INT_MAX;
 #pragma unroll
@@ -180,7 +189,7 @@ __device__ __forceinline__ void tile_accumulate(const Params &P, const Seg &g, i
 #pragma unroll
                     for (int j = VEC - 1; j >= 0; --j)
                         if (x[j] == mt)
-                            idx = (v0 + tid + u * NT) * VEC + j;
+                            idx = (v0 + base + u * 32) * VEC + j;
                 }
             }
             st.idx = idx;
@@ -188,21 +197,36 @@ __device__ __forceinline__ void tile_accumulate(const Params &P, const Seg &g, i
         st.m = fmax_nan(st.m, mt);
         return;
     }
-    // sampling: online rescale when the running maximum grows
+    // sampling: the tile's sum against the lane's tile maximum, folded into the
+    // running (m, s) with one rescale of each side
     const float mt = L::tile_max(raw);
+    float ts = 0.0f;
+    if (mt != -INFINITY) {
+        const unsigned long long c2 = f2(c, c);
+        unsigned long long acc = L::expsum2(raw[0], -mt, c2);
+#pragma unroll
+        for (int u = 1; u < U; ++u)
+            acc = add2(acc, L::expsum2(raw[u], -mt, c2));
+        float s0, s1;
+        f2_split(acc, s0, s1);
+        ts = s0 + s1;
+    }
     const float mn = fmax_nan(st.m, mt);
     if (mn != st.m)
         st.s = rescale(st.s, st.m, mn, c);
+    st.s += (mt == mn) ? ts : rescale(ts, mt, mn, c);
     st.m = mn;
-    if (mn != -INFINITY) {
-        const unsigned long long c2 = f2(c, c);
-        unsigned long long acc = L::expsum2(raw[0], -mn, c2);
+    if (rec) {
+        float M = mt;
 #pragma unroll
-        for (int u = 1; u < U; ++u)
-            acc = add2(acc, L::expsum2(raw[u], -mn, c2));
-        float s0, s1;
-        f2_split(acc, s0, s1);
-        st.s += s0 + s1;
+        for (int o = 16; o > 0; o >>= 1)
+            M = fmax_nan(M, __shfl_xor_sync(0xffffffffu, M, o));
+        float S = (mt == M) ? ts : rescale(ts, mt, M, c);
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1)
+            S += __shfl_xor_sync(0xffffffffu, S, o);
+        if (lane == 0)
+            __stcg(rec, make_float2(M, S));
     }
 }
 
@@ -276,6 +300,7 @@ __global__ void __launch_bounds__(NTHREADS, 2) stats_kernel(const Params P)
                 ti.mode = mode;
                 ti.last = (seg == seg1 - 1) ? 1 : 0;
                 ti.c = (mode == MODE_SAMPLE) ? LOG2E / T : 0.0f;
+                ti.bonus = (mode == MODE_SAMPLE && rsq == P.k) ? 1 : 0;
                 const int e0 = seg * SEG, e1 = min(P.V, e0 + SEG);
                 const unsigned long long start = (row * P.V + e0) * L::ES;
                 const unsigned long long end = (row * P.V + e1) * L::ES;
@@ -337,7 +362,13 @@ __global__ void __launch_bounds__(NTHREADS, 2) stats_kernel(const Params P)
         const int e0 = ti.seg * SEG, e1 = min(P.V, e0 + SEG);
         const Seg g = make_seg<DT>(slot, is_target ? P.target : P.draft, row, P.V, e0, e1, ti.phase0,
                                    ti.ncopied0);
-        tile_accumulate<DT>(P, g, tid, ti.mode, ti.c, st);
+        float2 *rec = nullptr;
+        if (ti.bonus) {
+            const int q = ti.seg * NCW + warp;  // 4 KB chunk of the bonus row
+            if (q < P.NCH)
+                rec = P.rec + (size_t)ti.b * P.NCH + q;
+        }
+        tile_accumulate<DT>(g, warp, lane, ti.mode, ti.c, st, rec);
         if (!ti.last) {
             // the slot is free once every warp has read it
             __syncwarp();
@@ -600,7 +631,7 @@ __device__ __forceinline__ JobRec load_job(const Params &P, int b)
 //   k*NT + 32*w .. k*NT + 32*w + 31.  A draw tile (one CTA) holds UD blocks;
 //   warp w writes the totals of chunk w of each.
 template <int DT>
-__global__ void __launch_bounds__(NT) draw_kernel(const Params P)
+__global__ void __launch_bounds__(NT, 6) draw_kernel(const Params P)
 {
     using L = Lg<DT>;
     constexpr int VEC = L::VEC;
@@ -609,8 +640,8 @@ __global__ void __launch_bounds__(NT) draw_kernel(const Params P)
     allow_next_kernel();
     wait_previous_kernel();  // the job comes from the scan kernel
     const JobRec J = load_job(P, b);
-    if (J.mode == DRAW_NONE)
-        return;
+    if (J.mode != DRAW_RESIDUAL)
+        return;  // bonus draws use the statistics kernel's chunk records
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     float *out = P.chunks + (size_t)b * P.chunk_stride + (size_t)seg * UD * NCW;
     uint4 rt[UD], rd[UD];
@@ -795,7 +826,12 @@ __global__ void __launch_bounds__(SCAN_WARPS * 32) final_kernel(const Params P)
     const int k = P.k;
     const int nblk = P.DS * UD;
     float *ch = P.chunks + (size_t)b * P.chunk_stride;
-    int tok = locate<DT>(P, J, J.mode, ch, btot[warp], nblk, lane);
+    int tok;
+    if (J.mode == DRAW_TARGET)
+        tok = records_draw<DT>(P.rec + (size_t)b * P.NCH, P.NCH, J.mt, J.c, J.u, P.target,
+                               (size_t)J.t_row, P.V, lane);
+    else
+        tok = locate<DT>(P, J, J.mode, ch, btot[warp], nblk, lane);
     if (tok < 0 && J.mode == DRAW_RESIDUAL) {
         // the residual vanished by rounding alone: draw from p_j instead
         warp_row_chunks<DT>(P, J, DRAW_TARGET, ch, nblk, lane);
@@ -832,24 +868,27 @@ bool sizes_ok(int32_t B, int32_t k, int32_t V, int32_t dtype)
 int tile_elems(int32_t dtype) { return TILE_BYTES / (dtype == SPEC_F32 ? 4 : 2); }
 
 struct WsLayout {
-    size_t partials, jobs, chunks, total;
-    size_t NS, NSS, DS, chunk_stride;
+    size_t partials, jobs, chunks, rec, total;
+    size_t NS, NSS, DS, chunk_stride, NCH;
 };
 
 // header | one 16-byte partial per super-tile [B][2k+1][NSS] | draw jobs [B] |
-// inverse-CDF chunk totals [B][chunk_stride]
+// inverse-CDF chunk totals [B][chunk_stride] | bonus-row chunk records [B][NCH]
 WsLayout ws_layout(int32_t B, int32_t k, int32_t V, int32_t dtype)
 {
     WsLayout w;
     const size_t te = tile_elems(dtype);
+    const size_t es = (dtype == SPEC_F32) ? 4 : 2;
     w.NS = ((size_t)V + te - 1) / te;
     w.NSS = (w.NS + SUPER - 1) / SUPER;
     w.DS = ((size_t)V + te / 2 - 1) / (te / 2);
+    w.NCH = ((size_t)V * es + CHUNK_BYTES - 1) / CHUNK_BYTES;
     w.partials = sizeof(WsHeader);
     w.jobs = align_up(w.partials + (size_t)B * (2 * (size_t)k + 1) * w.NSS * 16, 256);
     w.chunks = align_up(w.jobs + (size_t)B * sizeof(JobRec), 256);
     w.chunk_stride = align_up(w.DS * UD * NCW, 32);  // floats, 128-byte rows
-    w.total = w.chunks + (size_t)B * w.chunk_stride * 4;
+    w.rec = align_up(w.chunks + (size_t)B * w.chunk_stride * 4, 256);
+    w.total = w.rec + (size_t)B * w.NCH * sizeof(float2);
     return w;
 }
 
@@ -966,6 +1005,8 @@ int launch(const void *target, const void *draft, const int32_t *tokens, const f
     P.part = reinterpret_cast<float4 *>(w + lay.partials);
     P.jobs = reinterpret_cast<JobRec *>(w + lay.jobs);
     P.chunks = reinterpret_cast<float *>(w + lay.chunks);
+    P.rec = reinterpret_cast<float2 *>(w + lay.rec);
+    P.NCH = (int)lay.NCH;
     P.B = B;
     P.k = k;
     P.V = V;

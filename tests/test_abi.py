@@ -64,9 +64,11 @@ def test_workspace_size(lib, B, k, V, dt, ok):
     nss = -(-ns // 4)           # super-tiles per row (one partial each)
     ds = -(-V // (tile // 2))   # draw tiles per row
     up = lambda x, a: -(-x // a) * a
+    nch = -(-(V * (4 if dt == 0 else 2)) // 4096)  # 4 KB chunks per row
     jobs = up(256 + B * (2 * k + 1) * nss * 16, 256)
     chunks = up(jobs + 64 * B, 256)
-    assert n == chunks + B * up(ds * 4 * 8, 32) * 4
+    rec = up(chunks + B * up(ds * 4 * 8, 32) * 4, 256)
+    assert n == rec + B * nch * 8
 
 
 def _call(lib, ptrs, B=1, k=1, V=8, dt=0, wsb=1 << 20):
