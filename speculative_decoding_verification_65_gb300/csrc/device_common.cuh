@@ -504,19 +504,44 @@ __device__ int records_draw(const float2 *rc, int NC, float m, float c, float u,
 {
     using L = Lg<DT>;
     constexpr int VEC = L::VEC;
+    constexpr int RC = 8;  // records a lane keeps in registers
     const int per = (NC + 31) / 32;
     const int c0 = min(NC, lane * per), c1 = min(NC, c0 + per);
+    const bool cached = per <= RC;
+    float2 cache[RC];
+#pragma unroll
+    for (int i = 0; i < RC; ++i)
+        cache[i] = (cached && c0 + i < c1) ? __ldcg(rc + c0 + i) : make_float2(-INFINITY, 0.0f);
+    auto rec_at = [&](int i) -> float2 {  // the lane's i-th record
+        if (cached) {
+            float2 f = cache[0];
+#pragma unroll
+            for (int t = 1; t < RC; ++t)
+                if (t == i)
+                    f = cache[t];
+            return f;
+        }
+        return __ldcg(rc + c0 + i);
+    };
+
     // running totals of the scaled chunk sums (each lane a contiguous range,
     // then a scan over lanes); R = the last
     float sl = 0.0f;
-    for (int q = c0; q < c1; ++q) {
-        const float2 f = __ldcg(rc + q);
-        sl += rescale(f.y, f.x, m, c);
+    if (cached) {
+#pragma unroll
+        for (int i = 0; i < RC; ++i)
+            if (c0 + i < c1)
+                sl += rescale(cache[i].y, cache[i].x, m, c);
+    } else {
+        for (int q = c0; q < c1; ++q) {
+            const float2 f = __ldcg(rc + q);
+            sl += rescale(f.y, f.x, m, c);
+        }
     }
     const float incl = lane_scan(sl, lane);
     const float Rtot = __shfl_sync(0xffffffffu, incl, 31);
     const float theta = u * Rtot;
-    unsigned cross = __ballot_sync(0xffffffffu, incl > theta);
+    const unsigned cross = __ballot_sync(0xffffffffu, incl > theta);
     int Lw;
     if (cross) {
         Lw = __ffs(cross) - 1;
@@ -526,58 +551,61 @@ __device__ int records_draw(const float2 *rc, int NC, float m, float c, float u,
     }
     if (Lw < 0)
         return -1;
-    // the crossing lane walks its chunks; the running total before lane Lw is
-    // the inclusive scan of lane Lw - 1
+
+    // the crossing lane walks its chunks from the running total before it
     const float before_lane = __shfl_sync(0xffffffffu, incl, Lw > 0 ? Lw - 1 : 0);
     int chunk = -1;
-    float cbefore = 0.0f, Mc = 0.0f, scale = 0.0f;
+    float cbefore = 0.0f, Mc = 0.0f;
     if (lane == Lw) {
         float C = (Lw > 0) ? before_lane : 0.0f;
-        const int q0 = min(NC, Lw * per), q1 = min(NC, q0 + per);
         int lastpos = -1;
-        float lastC = 0.0f;
-        for (int q = q0; q < q1; ++q) {
-            const float2 f = __ldcg(rc + q);
+        float lastC = 0.0f, lastM = 0.0f;
+        for (int i = 0; i < c1 - c0 && chunk < 0; ++i) {
+            const float2 f = rec_at(i);
             const float w = rescale(f.y, f.x, m, c);
             if (w > 0.0f) {
                 if (C + w > theta) {
-                    chunk = q;
+                    chunk = c0 + i;
                     cbefore = C;
-                    break;
+                    Mc = f.x;
+                } else {
+                    lastpos = c0 + i;
+                    lastC = C;
+                    lastM = f.x;
                 }
-                lastpos = q;
-                lastC = C;
             }
             C += w;
         }
         if (chunk < 0) {  // rounding left the threshold past the lane's total
             chunk = lastpos;
             cbefore = lastC;
-        }
-        if (chunk >= 0) {
-            const float2 f = __ldcg(rc + chunk);
-            Mc = f.x;
-            scale = ex2((f.x - m) * c);
+            Mc = lastM;
         }
     }
     chunk = __shfl_sync(0xffffffffu, chunk, Lw);
-    cbefore = __shfl_sync(0xffffffffu, cbefore, Lw);
-    Mc = __shfl_sync(0xffffffffu, Mc, Lw);
-    scale = __shfl_sync(0xffffffffu, scale, Lw);
     if (chunk < 0)
         return -1;
+    cbefore = __shfl_sync(0xffffffffu, cbefore, Lw);
+    Mc = __shfl_sync(0xffffffffu, Mc, Lw);
 
-    // the chunk again, in index order, in units of 2^((x - Mc) * c)
-    const float tloc = (theta - cbefore) / scale;
-    const unsigned long long c2 = f2(c, c);
+    // the chunk again (all its vectors in one round trip), in index order, in
+    // units of 2^((x - Mc) * c)
     const int vb = chunk * (32 * CHUNK_UV);
+    uint4 raw[CHUNK_UV];
+#pragma unroll
+    for (int uv = 0; uv < CHUNK_UV; ++uv)
+        raw[uv] = row_vec<DT>(logits, row, vb + uv * 32 + lane, V);
+    const float tloc = (theta - cbefore) / ex2((Mc - m) * c);
+    const unsigned long long c2 = f2(c, c);
     float carry = 0.0f;
     int tok = -1, last_u = -1, last_lane = -1;
-    for (int uv = 0; uv < CHUNK_UV && tok < 0; ++uv) {
+#pragma unroll
+    for (int uv = 0; uv < CHUNK_UV; ++uv) {
+        if (tok >= 0)
+            continue;
         const int v = vb + uv * 32 + lane;
-        const uint4 raw = row_vec<DT>(logits, row, v, V);
         float e[VEC];
-        L::exp2_vec(raw, -Mc, c2, e);
+        L::exp2_vec(raw[uv], -Mc, c2, e);
         float tau = 0.0f;
 #pragma unroll
         for (int j = 0; j < VEC; ++j)
@@ -586,23 +614,23 @@ __device__ int records_draw(const float2 *rc, int NC, float m, float c, float u,
         const unsigned hit = __ballot_sync(0xffffffffu, carry + in_l > tloc && tau > 0.0f);
         if (hit) {
             const int hl = __ffs(hit) - 1;
+            int t = -1;
             if (lane == hl) {
                 float run = carry + (in_l - tau);
                 int lastj = -1;
+#pragma unroll
                 for (int j = 0; j < VEC; ++j) {
-                    if (e[j] > 0.0f) {
+                    if (t < 0 && e[j] > 0.0f) {
                         run = run + e[j];
                         lastj = j;
-                        if (run > tloc) {
-                            tok = v * VEC + j;
-                            break;
-                        }
+                        if (run > tloc)
+                            t = v * VEC + j;
                     }
                 }
-                if (tok < 0)
-                    tok = v * VEC + lastj;  // rounding within the lane: its last positive weight
+                if (t < 0)
+                    t = v * VEC + lastj;  // rounding within the lane: its last positive weight
             }
-            tok = __shfl_sync(0xffffffffu, tok, hl);
+            tok = __shfl_sync(0xffffffffu, t, hl);
         } else {
             const unsigned pos = __ballot_sync(0xffffffffu, tau > 0.0f);
             if (pos) {
@@ -615,16 +643,21 @@ __device__ int records_draw(const float2 *rc, int NC, float m, float c, float u,
     if (tok < 0 && last_u >= 0) {
         // rounding left the threshold past the chunk's running total: its
         // last positive weight
-        const int v = vb + last_u * 32 + last_lane;
-        const uint4 raw = row_vec<DT>(logits, row, v, V);
-        float e[VEC];
-        L::exp2_vec(raw, -Mc, c2, e);
-        int lastj = -1;
+        int t = -1;
+        if (lane == last_lane) {
 #pragma unroll
-        for (int j = 0; j < VEC; ++j)
-            if (e[j] > 0.0f)
-                lastj = j;
-        tok = v * VEC + lastj;
+            for (int uv = 0; uv < CHUNK_UV; ++uv) {
+                if (uv == last_u) {
+                    float e[VEC];
+                    L::exp2_vec(raw[uv], -Mc, c2, e);
+#pragma unroll
+                    for (int j = 0; j < VEC; ++j)
+                        if (e[j] > 0.0f)
+                            t = (vb + uv * 32 + lane) * VEC + j;
+                }
+            }
+        }
+        tok = __shfl_sync(0xffffffffu, t, last_lane);
     }
     return tok;
 }
