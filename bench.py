@@ -59,6 +59,48 @@ def dist_env():
     return rank, world, local
 
 
+def reduce_max(x: float, world: int, device=None) -> float:
+    """The maximum of a scalar over all ranks (the step time every rank waits
+    for); a no-op on one rank.  Works on nccl (device tensor) and gloo (host
+    tensor) process groups."""
+    if world <= 1:
+        return float(x)
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([float(x)], dtype=torch.float64,
+                     device=device if dist.get_backend() == "nccl" else "cpu")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def aggregate_rate(units_per_rank: int, steps: int, world: int, max_seconds: float) -> float:
+    """Whole-job throughput: the units all ranks processed over the slowest
+    rank's time (weak scaling: every rank has its own batch)."""
+    return world * units_per_rank * steps / max_seconds
+
+
+def read_probe_gbs(dev, reps: int = 20, nbytes: int = 4 << 30):
+    """Read bandwidth of the library's streaming read probe over a buffer far
+    larger than L2 (CUDA events on the launch stream, after warm-up)."""
+    import torch
+    import speculative_decoding_verification_65_gb300 as sv
+    buf = torch.empty(nbytes, dtype=torch.uint8, device=dev)
+    sink = torch.empty(sv.spec_bench_read_sink_words(), dtype=torch.int32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    for _ in range(3):
+        sv.spec_bench_read(buf, sink, stream)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(reps):
+        sv.spec_bench_read(buf, sink, stream)
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    gbs = nbytes * reps / (e0.elapsed_time(e1) / 1e3) / 1e9
+    del buf, sink
+    torch.cuda.empty_cache()
+    return gbs
+
+
 def measured_peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -259,17 +301,35 @@ def run_ours(args):
 
     t0 = torch.cuda.Event(enable_timing=True)
     t1 = torch.cuda.Event(enable_timing=True)
+    graph, per_graph = None, 1
+    if args.graph:
+        # capture a batch of whole calls into one CUDA graph and replay it:
+        # for launch-bound sizes this removes the host's launch cost per call
+        per_graph = min(args.steps, 50)
+        while args.steps % per_graph:
+            per_graph -= 1
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph):
+            for _ in range(per_graph):
+                sv.spec_verify(**d, out_tokens=out_t, out_num_accepted=out_n, ws=ws)
+        graph.replay()
+        torch.cuda.synchronize(dev)
     barrier()
     torch.cuda.synchronize(dev)
     # the timed region: K whole verification calls, as a user issues them
     with ClockSampler(local) as clk:
         t0.record(stream)
-        for i in range(args.steps):
-            step()
+        if graph is not None:
+            for _ in range(args.steps // per_graph):
+                graph.replay()
+        else:
+            for i in range(args.steps):
+                step()
         t1.record(stream)
         torch.cuda.synchronize(dev)
     barrier()
     total_ms = t0.elapsed_time(t1)
+    del graph
 
     # per-kernel durations: K more calls, each with an event before it and one
     # after each stage (statistics, accept scan, draw tiles, final search) on
@@ -288,13 +348,9 @@ def run_ours(args):
     stage_ms = [statistics.mean(
         (starts[i] if j == 0 else stages[i][j - 1]).elapsed_time(stages[i][j])
         for i in range(args.steps)) for j in range(sv.SPEC_STAGES)]
-    if world > 1:
-        import torch.distributed as dist
-        tt = torch.tensor([total_ms], device=dev)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        total_ms = float(tt.item())
+    total_ms = reduce_max(total_ms, world, dev)
     ms_per_step = total_ms / args.steps
-    value = world * B * k * args.steps / (total_ms / 1e3)
+    value = aggregate_rate(B * k, args.steps, world, total_ms / 1e3)
     status = sv.spec_verify_read_status(ws)
 
     # end to end through the public API on host buffers (pinned), every step
@@ -319,13 +375,8 @@ def run_ours(args):
     e0 = time.perf_counter()
     for _ in range(e2e_steps):
         sv.spec_verify_host(h_t, h_d, h_g, h_ua, h_ur, h_T, arena, h_ot, h_on, stream=stream)
-    e2e_s = time.perf_counter() - e0
-    if world > 1:
-        import torch.distributed as dist
-        tt = torch.tensor([e2e_s], device=dev)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        e2e_s = float(tt.item())
-    e2e_value = world * B * k * e2e_steps / e2e_s
+    e2e_s = reduce_max(time.perf_counter() - e0, world, dev)
+    e2e_value = aggregate_rate(B * k, e2e_steps, world, e2e_s)
     h2d = sum(int(x.numel() * x.element_size()) for x in (h_t, h_d, h_g, h_ua, h_ur, h_T))
     d2h = int(h_ot.numel() * 4 + h_on.numel() * 4)
 
@@ -340,12 +391,16 @@ def run_ours(args):
     achieved = alg_bytes / kern_avg_s / 1e9
     peak = float(peaks.get("hbm_gbs", 6800.0))
     workload = synth.CONFIG_NAMES[args.config] if args.batch is None else case.name
+    read_gbs = None if args.no_read_probe else read_probe_gbs(dev)
     cpu = None
     if world == 1 and not args.no_cpu_baseline:
         cores = host_cores()
         v, n_seq, used = time_oracle(case, args.cpu_budget, cores)
+        v1, n1, used1 = time_oracle(case, args.cpu_budget / 4, 1)
         cpu = {"value": v, "unit": UNIT, "cores": cores, "kind": "oracle",
-               "sample": f"{n_seq} of {B} sequences of {workload}, {used:.1f} s on {cores} threads"}
+               "sample": f"{n_seq} of {B} sequences of {workload}, {used:.1f} s on {cores} threads",
+               "value_1thread": v1,
+               "sample_1thread": f"{n1} sequences, {used1:.1f} s on 1 thread"}
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
         "steps": args.steps, "warmup": max(args.warmup, 3), "ms_per_step": ms_per_step,
@@ -354,7 +409,10 @@ def run_ours(args):
         "config": {"workload": workload, "B_per_gpu": B, "k": k, "V": V,
                    "input_dtype": case.dtype, "global_batch": B * world,
                    "algorithmic_bytes_per_step": alg_bytes,
-                   "l2": "inputs larger than L2 (no flush)", "parallelism": f"dp{world}"},
+                   "l2": "inputs larger than L2 (no flush)" if alg_bytes > (129 << 20)
+                   else "inputs smaller than L2 (no flush; launch-bound size)",
+                   "launch": f"CUDA graph replay of {per_graph} calls" if args.graph
+                   else "one library call per step", "parallelism": f"dp{world}"},
         "gpu_launches": sv.SPEC_STAGES * args.steps,
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak, "traffic": recorded_traffic(workload),
@@ -364,9 +422,13 @@ def run_ours(args):
                      "kernel_timing": "CUDA events after each stage, K further steps",
                      "kernel_ms_avg": kern_avg_s * 1e3, "kernel_ms_min": min(kern_ms),
                      "frac_of_nominal_8TBs": achieved / 8000.0,
+                     "read_probe_gbs": read_gbs,
+                     "frac_of_read_probe": achieved / read_gbs if read_gbs else None,
                      "step_GBps": alg_bytes / (ms_per_step / 1e3) / 1e9},
         "stage_ms": {"stats": stage_ms[0], "scan": stage_ms[1], "draw": stage_ms[2],
                      "final": stage_ms[3]},
+        "ms_per_step_median_staged": statistics.median(
+            s.elapsed_time(e[-1]) for s, e in zip(starts, stages)),
         "clocks": clk.summary(),
         "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "steps": e2e_steps},
@@ -461,12 +523,7 @@ def run_ours_sample(args):
             dist.barrier()
 
     def max_over_ranks(x):
-        if world > 1:
-            import torch.distributed as dist
-            t = torch.tensor([x], device=dev)
-            dist.all_reduce(t, op=dist.ReduceOp.MAX)
-            return float(t.item())
-        return x
+        return reduce_max(x, world, dev)
 
     sc = make_sample_workload(args.config, rank, args.batch)
     R, V = sc.R, sc.V
@@ -515,7 +572,7 @@ def run_ours_sample(args):
     kern_ms = [s.elapsed_time(e[0]) for s, e in zip(starts, stages)]
     pick_ms = statistics.mean(e[0].elapsed_time(e[1]) for e in stages)
     ms_per_step = total_ms / args.steps
-    value = world * R * args.steps / (total_ms / 1e3)
+    value = aggregate_rate(R, args.steps, world, total_ms / 1e3)
     status = sv.spec_verify_read_status(ws)
 
     # end to end through the C ABI on pinned host buffers
@@ -537,7 +594,7 @@ def run_ours_sample(args):
     for _ in range(e2e_steps):
         sv.spec_sample_host(h_l, h_u, h_T, arena, h_o, stream=stream)
     e2e_s = max_over_ranks(time.perf_counter() - e0)
-    e2e_value = world * R * e2e_steps / e2e_s
+    e2e_value = aggregate_rate(R, e2e_steps, world, e2e_s)
     h2d = sum(int(x.numel() * x.element_size()) for x in (h_l, h_u, h_T))
 
     if rank != 0:
@@ -601,6 +658,9 @@ def main():
                     help="smaller batch of the same recipe (profiling captures only)")
     ap.add_argument("--cpu-budget", type=float, default=10.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-read-probe", action="store_true")
+    ap.add_argument("--graph", action="store_true",
+                    help="time CUDA-graph replays of the verification calls")
     args = ap.parse_args()
     if args.config is None:
         args.config = 4 if args.op == "verify" else 5

@@ -85,6 +85,10 @@ def library():
         lib.spec_sample_host_arena_size.argtypes = [i32, i32, i32]
         lib.spec_sample_host.restype = i32
         lib.spec_sample_host.argtypes = [vp] * 4 + [i32] * 3 + [vp, sz, vp]
+        lib.spec_bench_read.restype = i32
+        lib.spec_bench_read.argtypes = [vp, sz, vp, vp]
+        lib.spec_bench_read_sink_words.restype = i32
+        lib.spec_bench_read_sink_words.argtypes = []
         _lib = lib
         return lib
 
@@ -416,6 +420,19 @@ def spec_sample_host(logits, u, temperature, arena, out=None, stream=None):
                                     _stream_handle(stream, arena.device))
     _check(rc, "spec_sample_host")
     return out
+
+
+def spec_bench_read(buf, sink, stream=None):
+    """The benchmark's read-only probe over a CUDA tensor `buf` (16-byte
+    aligned, size a multiple of 16 bytes); `sink` is an int32 CUDA tensor of
+    at least spec_bench_read_sink_words() elements."""
+    rc = library().spec_bench_read(_ptr(buf), buf.numel() * buf.element_size(), _ptr(sink),
+                                   _stream_handle(stream, buf.device))
+    _check(rc, "spec_bench_read")
+
+
+def spec_bench_read_sink_words() -> int:
+    return int(library().spec_bench_read_sink_words())
 
 
 def sample_to_device(sc, device="cuda"):
