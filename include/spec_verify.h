@@ -86,8 +86,9 @@ const char *spec_verify_strerror(int32_t status);
 /*
  * Bytes of device workspace one spec_verify call needs for these sizes: a
  * 256-byte header (the status word), one 16-byte partial per 128 KB of every
- * row, and per sequence a 64-byte draw record and its inverse-CDF chunk
- * totals (32 bytes per 16 KB of a row).  Returns 0 for sizes out of range.
+ * row, and per sequence a 64-byte draw record, its inverse-CDF chunk totals
+ * (32 bytes per 16 KB of a row) and its bonus row's chunk records (8 bytes
+ * per 4 KB of a row).  Returns 0 for sizes out of range.
  * Host-only; needs no GPU.
  */
 size_t spec_verify_workspace_size(int32_t B, int32_t k, int32_t V, int32_t dtype);
@@ -169,7 +170,7 @@ int32_t spec_verify_timed(const void *target_logits, const void *draft_logits,
  * device code: every GPU that loads the library holds it until the process
  * exits.  Calls whose spec_verify_workspace_size(B, k, V, dtype) exceeds that
  * return SPEC_ENOSPACE and launch nothing (B=256, k=8, V=151936, fp32 needs
- * about 1.6 MiB).  The call allocates nothing: no cudaMalloc, no cudaFree.
+ * about 1.8 MiB).  The call allocates nothing: no cudaMalloc, no cudaFree.
  *
  * The first call on a device looks up the array's device address with that
  * device current (cudaGetSymbolAddress) and keeps it; make that first call
