@@ -89,6 +89,8 @@ def library():
         lib.spec_bench_read.argtypes = [vp, sz, vp, vp]
         lib.spec_bench_read_sink_words.restype = i32
         lib.spec_bench_read_sink_words.argtypes = []
+        lib.spec_selftest_wait_timeout.restype = i32
+        lib.spec_selftest_wait_timeout.argtypes = [vp, ctypes.c_uint64, vp]
         _lib = lib
         return lib
 
@@ -429,6 +431,14 @@ def spec_bench_read(buf, sink, stream=None):
     rc = library().spec_bench_read(_ptr(buf), buf.numel() * buf.element_size(), _ptr(sink),
                                    _stream_handle(stream, buf.device))
     _check(rc, "spec_bench_read")
+
+
+def spec_selftest_wait_timeout(ws, limit_ns: int, stream=None):
+    """Launch the bounded-wait self-test on workspace `ws` (see
+    include/spec_bench.h); read its outcome with spec_verify_read_status."""
+    _check(library().spec_selftest_wait_timeout(_ptr(ws), int(limit_ns),
+                                                _stream_handle(stream, ws.device)),
+           "spec_selftest_wait_timeout")
 
 
 def spec_bench_read_sink_words() -> int:

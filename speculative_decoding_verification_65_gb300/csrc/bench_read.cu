@@ -1,12 +1,17 @@
-// bench_read.cu -- read-only streaming probe (a measurement helper of the
-// benchmark, not part of the method): every SM runs a few CTAs that stream
-// 16-byte vectors with eight loads in flight per thread, so the only limit is
-// the memory system's read bandwidth.
+// bench_read.cu -- helpers around the method, not part of it:
+//   * a read-only streaming probe for the benchmark: every SM runs a few CTAs
+//     that stream 16-byte vectors with eight loads in flight per thread, so
+//     the only limit is the memory system's read bandwidth;
+//   * a self-test of the bounded mbarrier wait every ring of the kernels uses:
+//     one CTA waits on a barrier nothing arrives at, gives up after the given
+//     limit and records SPEC_DEV_WAIT_TIMEOUT in the workspace status word,
+//     exactly as a kernel whose copy never landed would.
 #include <cuda_runtime.h>
 #include <stdint.h>
 
 #include "spec_bench.h"
 #include "spec_verify.h"
+#include "device_common.cuh"
 
 namespace {
 
@@ -48,6 +53,16 @@ __global__ void __launch_bounds__(THREADS) read_kernel(const uint4 *__restrict__
     }
 }
 
+// One thread waits on a fresh mbarrier that no thread arrives at.
+__global__ void wait_selftest_kernel(spec_dev::WsHeader *hdr, unsigned long long limit_ns)
+{
+    __shared__ unsigned long long bar;
+    spec_dev::mbar_init(&bar, 1);
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    if (!spec_dev::mbar_wait_for(&bar, 0, limit_ns))
+        atomicExch(&hdr->status, SPEC_DEV_WAIT_TIMEOUT);
+}
+
 int grid_size()
 {
     int dev = 0, sms = 0;
@@ -75,6 +90,16 @@ int32_t spec_bench_read(const void *buf, size_t bytes, uint32_t *sink, void *str
         return SPEC_ECUDA;
     read_kernel<<<grid, THREADS, 0, reinterpret_cast<cudaStream_t>(stream)>>>(
         reinterpret_cast<const uint4 *>(buf), bytes / 16, sink);
+    return cudaPeekAtLastError() == cudaSuccess ? SPEC_OK : SPEC_ECUDA;
+}
+
+int32_t spec_selftest_wait_timeout(void *workspace, uint64_t limit_ns, void *stream)
+{
+    if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 15) || limit_ns == 0 ||
+        limit_ns > 100000000ull)
+        return SPEC_EINVAL;
+    wait_selftest_kernel<<<1, 1, 0, reinterpret_cast<cudaStream_t>(stream)>>>(
+        reinterpret_cast<spec_dev::WsHeader *>(workspace), (unsigned long long)limit_ns);
     return cudaPeekAtLastError() == cudaSuccess ? SPEC_OK : SPEC_ECUDA;
 }
 

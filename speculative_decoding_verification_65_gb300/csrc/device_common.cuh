@@ -153,8 +153,10 @@ __device__ __forceinline__ bool mbar_try_wait(unsigned long long *bar, uint32_t 
     return ok != 0;
 }
 
-// Bounded wait for the phase with the given parity to complete.
-__device__ __forceinline__ bool mbar_wait(unsigned long long *bar, uint32_t parity)
+// Bounded wait for the phase with the given parity to complete: false once
+// `limit_ns` of global time has passed without it.
+__device__ __forceinline__ bool mbar_wait_for(unsigned long long *bar, uint32_t parity,
+                                              unsigned long long limit_ns)
 {
     if (mbar_try_wait(bar, parity))
         return true;
@@ -163,9 +165,15 @@ __device__ __forceinline__ bool mbar_wait(unsigned long long *bar, uint32_t pari
         for (int i = 0; i < 64; ++i)
             if (mbar_try_wait(bar, parity))
                 return true;
-        if (globaltimer() - t0 > WAIT_NS)
+        if (globaltimer() - t0 > limit_ns)
             return false;
     }
+}
+
+// The kernels' wait: bounded by WAIT_NS.
+__device__ __forceinline__ bool mbar_wait(unsigned long long *bar, uint32_t parity)
+{
+    return mbar_wait_for(bar, parity, WAIT_NS);
 }
 
 __device__ __forceinline__ void bulk_copy_g2s(void *dst, const void *src, uint32_t bytes,

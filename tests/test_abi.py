@@ -178,3 +178,10 @@ def test_sample_bad_sizes_and_small_workspace(lib):
     assert _scall(lib, GOOD, R=-3) == sv.SPEC_EINVAL
     need = sv.spec_sample_workspace_size(2, 100, 0)
     assert _scall(lib, GOOD, wsb=need - 1) == sv.SPEC_ENOSPACE
+
+
+def test_wait_selftest_argument_checks(lib):
+    assert lib.spec_selftest_wait_timeout(None, 1000, None) == sv.SPEC_EINVAL
+    assert lib.spec_selftest_wait_timeout(ctypes.c_void_p(GOOD[0] + 4), 1000, None) == sv.SPEC_EINVAL
+    assert lib.spec_selftest_wait_timeout(ctypes.c_void_p(GOOD[0]), 0, None) == sv.SPEC_EINVAL
+    assert lib.spec_selftest_wait_timeout(ctypes.c_void_p(GOOD[0]), 10**9, None) == sv.SPEC_EINVAL
