@@ -65,6 +65,12 @@ def _load():
         lib.spec_ref_inverse_cdf.argtypes = [dp, i64, ctypes.c_double, dp]
         lib.spec_ref_inverse_cdf.restype = i64
         lib.spec_sample_ref_mt.argtypes = [vp, i32, dp, dp, i64, i64, vp, dp, i32]
+        lib.spec_verify_ref_filtered_mt.argtypes = [vp, vp, i32, vp, dp, dp, dp, vp, dp,
+                                                    i64, i64, i64, vp, vp, dp, i32]
+        lib.spec_verify_ref_filtered_mt.restype = i32
+        lib.spec_ref_filtered_softmax.argtypes = [dp, i64, ctypes.c_double, i64,
+                                                  ctypes.c_double, dp, dp]
+        lib.spec_ref_filtered_softmax.restype = i64
         lib.spec_sample_ref_mt.restype = i32
         _lib = lib
         return lib
@@ -129,6 +135,48 @@ def probs(target, draft, tokens, temperature):
     if rc != 0:
         raise RuntimeError(f"spec_ref_probs failed with status {rc}")
     return out
+
+
+def verify_filtered(target, draft, tokens, u_accept, u_resample, temperature, top_k, top_p,
+                    nthreads: int = 1, want_trace: bool = True):
+    """verify() with top-k / top-p filtered distributions (top_k int [B], 0 =
+    none; top_p float [B], >= 1 = none; either may be None).  The trace has a
+    last column: the smallest top-p margin over the rows read."""
+    lib = _load()
+    target, dt = _logits_and_dtype(target)
+    draft, _ = _logits_and_dtype(draft)
+    B, k1, V = target.shape
+    k = k1 - 1
+    tokens = np.ascontiguousarray(tokens, dtype=np.int32).reshape(B, k)
+    ua = np.ascontiguousarray(u_accept, dtype=np.float64).reshape(B, k)
+    ur = np.ascontiguousarray(u_resample, dtype=np.float64).reshape(B)
+    tt = np.ascontiguousarray(temperature, dtype=np.float64).reshape(B)
+    tk = None if top_k is None else np.ascontiguousarray(top_k, dtype=np.int32).reshape(B)
+    tp = None if top_p is None else np.ascontiguousarray(top_p, dtype=np.float64).reshape(B)
+    out_tokens = np.empty((B, k + 1), np.int32)
+    out_n = np.empty((B,), np.int32)
+    trace = np.empty((B, k + 4), np.float64) if want_trace else None
+    rc = lib.spec_verify_ref_filtered_mt(
+        _ptr(target), _ptr(draft), dt, _ptr(tokens), _ptr(ua), _ptr(ur), _ptr(tt),
+        _ptr(tk) if tk is not None else None, _ptr(tp) if tp is not None else None,
+        B, k, V, _ptr(out_tokens), _ptr(out_n), _ptr(trace) if trace is not None else None,
+        int(nthreads))
+    if rc != 0:
+        raise RuntimeError(f"spec_verify_ref_filtered failed with status {rc}")
+    return out_tokens, out_n, trace
+
+
+def filtered_softmax(logits, T: float, K: int, P: float):
+    """Top-k / top-p filtered softmax of one row (fp64): (p, kept count, margin)."""
+    lib = _load()
+    l = np.ascontiguousarray(logits, dtype=np.float64)
+    p = np.empty_like(l)
+    mg = np.empty(1, np.float64)
+    n = lib.spec_ref_filtered_softmax(_ptr(l), l.size, float(T), int(K), float(P), _ptr(p),
+                                      _ptr(mg))
+    if n < 0:
+        raise ValueError("bad arguments")
+    return p, int(n), float(mg[0])
 
 
 def sample(logits, u, temperature, nthreads: int = 1, want_trace: bool = True):

@@ -52,6 +52,7 @@
  * Everything is fp64 with plain sequential loops; no blocking, no fusion, no
  * reordering beyond the definition.
  */
+#define _GNU_SOURCE /* qsort_r */
 #include <math.h>
 #include <float.h>
 #include <stdint.h>
@@ -142,6 +143,89 @@ int spec_ref_softmax(const double *l, int64_t V, double T, double *p)
     return REF_OK;
 }
 
+/* Order of a sort by logit descending, index ascending (keys in `arg`). */
+static int ref_order_cmp(const void *a, const void *b, void *arg)
+{
+    const double *l = (const double *)arg;
+    const int64_t i = *(const int64_t *)a, j = *(const int64_t *)b;
+    if (l[i] > l[j])
+        return -1;
+    if (l[i] < l[j])
+        return 1;
+    return (i < j) ? -1 : (i > j);
+}
+
+/*
+ * Top-k / top-p filtered softmax.  Tokens are ranked by logit, descending,
+ * ties by index ascending.  top-k keeps the first K of them (K <= 0 or
+ * K >= V: all).  top-p keeps, among those, a token while the mass ranked
+ * strictly before it is below P * Z_K, Z_K the mass of the top-k set (P >= 1:
+ * all of them); at least one token is always kept.  p receives the
+ * distribution renormalised over the kept set (0 elsewhere).  *margin (if
+ * non-NULL) receives the distance of the two decisive running masses from
+ * P * Z_K, relative to Z_K (NaN without top-p).  Returns the kept count, or
+ * -1 on bad arguments.
+ */
+int64_t spec_ref_filtered_softmax(const double *l, int64_t V, double T, int64_t K, double P,
+                                  double *p, double *margin)
+{
+    if (!(T > 0) || V < 1)
+        return -1;
+    int64_t *order = (int64_t *)malloc((size_t)V * sizeof(int64_t));
+    double *e = (double *)malloc((size_t)V * sizeof(double));
+    if (!order || !e) {
+        free(order);
+        free(e);
+        return -1;
+    }
+    double m = ref_max_argmax(l, V, NULL);
+    for (int64_t x = 0; x < V; ++x) {
+        e[x] = exp((l[x] - m) / T);
+        order[x] = x;
+    }
+    qsort_r(order, (size_t)V, sizeof(int64_t), ref_order_cmp, (void *)l);
+    const int64_t Keff = (K > 0 && K < V) ? K : V;
+    double ZK = 0.0;
+    for (int64_t i = 0; i < Keff; ++i)
+        ZK += e[order[i]];
+    int64_t N = Keff;
+    double mg = NAN;
+    if (P < 1.0) {
+        const double target = P * ZK;
+        double cum = 0.0, before_last = 0.0;
+        for (int64_t i = 0; i < Keff; ++i) {
+            if (cum >= target) {
+                N = i;
+                break;
+            }
+            before_last = cum;
+            cum += e[order[i]];
+        }
+        /* decisive comparisons: the last kept token (before < target) and,
+           if any token was cut, the first cut one (before >= target) */
+        mg = (target - before_last) / ZK;
+        if (N < Keff) {
+            const double m2 = (cum - target) / ZK;
+            if (m2 < mg)
+                mg = m2;
+        }
+    }
+    double Z = 0.0;
+    for (int64_t x = 0; x < V; ++x)
+        p[x] = 0.0;
+    for (int64_t i = 0; i < N; ++i) {
+        p[order[i]] = e[order[i]];
+        Z += e[order[i]];
+    }
+    for (int64_t i = 0; i < N; ++i)
+        p[order[i]] /= Z;
+    if (margin)
+        *margin = mg;
+    free(order);
+    free(e);
+    return N;
+}
+
 /*
  * Residual (correction) weights w(x) = max(0, p(x) - q(x)); returns their
  * total.  The normalised r(x) = w(x) / total is the second page's r(x).
@@ -216,10 +300,31 @@ typedef struct {
     int64_t B, k, V;
     int32_t *out_tokens;     /* [B, k+1] */
     int32_t *out_num_accepted;/* [B] */
-    double *trace;           /* [B, k+3] or NULL */
+    double *trace;           /* [B, tw] or NULL */
+    int64_t tw;              /* trace width: k+3, or k+4 with the filter margin */
+    const int32_t *top_k;    /* [B] or NULL (no top-k) */
+    const double *top_p;     /* [B] or NULL (no top-p) */
     int64_t b0, b1;          /* sequence range for this worker */
     int status;
 } ref_job_t;
+
+/* The sequence's sampling distribution of one row: softmax(l/T), filtered by
+   the sequence's top-k / top-p when the call has them; tracks the smallest
+   top-p margin seen. */
+static void ref_dist(const ref_job_t *J, int64_t b, const double *l, double T, double *p,
+                     double *min_margin)
+{
+    const int64_t K = J->top_k ? J->top_k[b] : 0;
+    const double P = J->top_p ? J->top_p[b] : 1.0;
+    if ((K <= 0 || K >= J->V) && !(P < 1.0)) {  /* no filter at all */
+        spec_ref_softmax(l, J->V, T, p);
+        return;
+    }
+    double mg = NAN;
+    spec_ref_filtered_softmax(l, J->V, T, K, P, p, &mg);
+    if (!isnan(mg) && (isnan(*min_margin) || mg < *min_margin))
+        *min_margin = mg;
+}
 
 static void ref_fail_sequence(ref_job_t *J, int64_t b)
 {
@@ -234,13 +339,19 @@ static int ref_one_sequence(ref_job_t *J, int64_t b, double *t, double *d,
 {
     const int64_t k = J->k, V = J->V;
     const double T = J->temperature[b];
-    double *tr = J->trace ? J->trace + b * (k + 3) : NULL;
+    double *tr = J->trace ? J->trace + b * J->tw : NULL;
     if (tr)
-        for (int64_t i = 0; i < k + 3; ++i)
+        for (int64_t i = 0; i < J->tw; ++i)
             tr[i] = NAN;
+    double min_margin = NAN;
 
     /* temperature must be 0 (greedy) or a finite normal positive value */
     if (isnan(T) || T < 0 || isinf(T) || (T > 0 && T < (double)FLT_MIN))
+        return 1;
+    /* filter parameters: top-k >= 0, top-p in (0, 1] or above (no top-p) */
+    if (J->top_k && J->top_k[b] < 0)
+        return 1;
+    if (J->top_p && (isnan(J->top_p[b]) || !(J->top_p[b] > 0.0)))
         return 1;
     for (int64_t i = 0; i < k; ++i) {
         int32_t g = J->tokens[b * k + i];
@@ -286,8 +397,8 @@ static int ref_one_sequence(ref_job_t *J, int64_t b, double *t, double *d,
             int32_t g = J->tokens[b * k + i];
             ref_load_row(J->target, J->dtype, (size_t)(b * (k + 1) + i), V, t);
             ref_load_row(J->draft, J->dtype, (size_t)(b * k + i), V, d);
-            spec_ref_softmax(t, V, T, p);
-            spec_ref_softmax(d, V, T, q);
+            ref_dist(J, b, t, T, p, &min_margin);
+            ref_dist(J, b, d, T, q, &min_margin);
             double P = p[g], Q = q[g];
             if (Q <= 0.0)
                 return 1; /* a sampled draft token must have positive probability */
@@ -308,7 +419,7 @@ static int ref_one_sequence(ref_job_t *J, int64_t b, double *t, double *d,
                 memcpy(w, p, (size_t)V * sizeof(double)); /* rounding-only fallback */
         } else {
             ref_load_row(J->target, J->dtype, (size_t)(b * (k + 1) + k), V, t);
-            spec_ref_softmax(t, V, T, w);
+            ref_dist(J, b, t, T, w, &min_margin);
         }
         token = spec_ref_inverse_cdf(w, V, J->u_resample[b], cell);
         if (token < 0)
@@ -317,6 +428,8 @@ static int ref_one_sequence(ref_job_t *J, int64_t b, double *t, double *d,
             tr[k] = cell[0];
             tr[k + 1] = cell[1];
             tr[k + 2] = cell[2];
+            if (J->tw > k + 3)
+                tr[k + 3] = min_margin;
         }
     }
 
@@ -358,12 +471,54 @@ static void *ref_worker(void *arg)
  * greedy), then the chosen draw cell [lo, hi) in u-units and the draw's total
  * mass R (NaN for greedy).
  */
+static int ref_verify_core(const void *target, const void *draft, int dtype,
+                           const int32_t *tokens, const double *u_accept,
+                           const double *u_resample, const double *temperature,
+                           const int32_t *top_k, const double *top_p, int filtered,
+                           int64_t B, int64_t k, int64_t V,
+                           int32_t *out_tokens, int32_t *out_num_accepted,
+                           double *trace, int nthreads);
+
 int spec_verify_ref_mt(const void *target, const void *draft, int dtype,
                        const int32_t *tokens, const double *u_accept,
                        const double *u_resample, const double *temperature,
                        int64_t B, int64_t k, int64_t V,
                        int32_t *out_tokens, int32_t *out_num_accepted,
                        double *trace, int nthreads)
+{
+    return ref_verify_core(target, draft, dtype, tokens, u_accept, u_resample, temperature,
+                           NULL, NULL, 0, B, k, V, out_tokens, out_num_accepted, trace,
+                           nthreads);
+}
+
+/*
+ * The verification step with top-k / top-p filtered distributions
+ * (spec_ref_filtered_softmax) for every row of a sequence at T > 0, the same
+ * parameters for target and draft.  top_k [B] (0: none; < 0: sequence error)
+ * and top_p [B] (>= 1: none; NaN or <= 0: sequence error) may each be NULL.
+ * trace (nullable) is [B, k+4]: the k+3 columns of spec_verify_ref_mt and the
+ * smallest top-p margin over the rows the sequence read (NaN if none).
+ */
+int spec_verify_ref_filtered_mt(const void *target, const void *draft, int dtype,
+                                const int32_t *tokens, const double *u_accept,
+                                const double *u_resample, const double *temperature,
+                                const int32_t *top_k, const double *top_p,
+                                int64_t B, int64_t k, int64_t V,
+                                int32_t *out_tokens, int32_t *out_num_accepted,
+                                double *trace, int nthreads)
+{
+    return ref_verify_core(target, draft, dtype, tokens, u_accept, u_resample, temperature,
+                           top_k, top_p, 1, B, k, V, out_tokens, out_num_accepted, trace,
+                           nthreads);
+}
+
+static int ref_verify_core(const void *target, const void *draft, int dtype,
+                           const int32_t *tokens, const double *u_accept,
+                           const double *u_resample, const double *temperature,
+                           const int32_t *top_k, const double *top_p, int filtered,
+                           int64_t B, int64_t k, int64_t V,
+                           int32_t *out_tokens, int32_t *out_num_accepted,
+                           double *trace, int nthreads)
 {
     if (!target || !tokens || !u_accept || !u_resample || !temperature ||
         !out_tokens || !out_num_accepted)
@@ -401,6 +556,9 @@ int spec_verify_ref_mt(const void *target, const void *draft, int dtype,
         J->out_tokens = out_tokens;
         J->out_num_accepted = out_num_accepted;
         J->trace = trace;
+        J->tw = filtered ? k + 4 : k + 3;
+        J->top_k = top_k;
+        J->top_p = top_p;
         J->b0 = B * w / nthreads;
         J->b1 = B * (w + 1) / nthreads;
     }
