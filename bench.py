@@ -16,6 +16,10 @@ ranks.  Under torchrun every rank verifies its own batch of B sequences
 (weak scaling: sequences are independent, so there is no collective on the
 data path; one scalar all-reduce takes the max time over ranks).
 
+`--op filtered` benchmarks top-k / top-p filtered verification on the same
+workloads (default workload 5, top-k 50, top-p 0.9), the draft tokens drawn
+from the filtered draft distribution.
+
 `--op sample` benchmarks the batched sampler instead (one token per row from
 softmax(logits / T), the draft model's step before verification): a step is
 one spec_sample call over the draft rows of a workload (default workload 5:
@@ -441,6 +445,238 @@ def run_ours(args):
         dist.destroy_process_group()
 
 
+# ------------------------------------------------------------------ filtered
+
+def filtered_draft_tokens(draft, temperature, top_k: int, top_p: float, seed: int):
+    """Input generation: draft tokens g_i drawn from the top-k / top-p filtered
+    draft distribution (greedy sequences: the draft argmax), on the GPU with
+    torch (ranking by logit with ties in index order, as the filter reads)."""
+    import torch
+    B, k, V = draft.shape
+    gen = torch.Generator(device=draft.device)
+    gen.manual_seed(seed)
+    toks = torch.empty((B, k), dtype=torch.int32, device=draft.device)
+    for b0 in range(0, B, 64):
+        d = draft[b0:b0 + 64].float()
+        T = temperature[b0:b0 + 64].view(-1, 1, 1)
+        vals, idx = torch.sort(d, dim=-1, descending=True, stable=True)
+        greedy = (T == 0).view(-1)
+        z = (vals - vals[..., :1]) / torch.where(T > 0, T, torch.ones_like(T))
+        w = torch.exp(z)
+        K = top_k if 0 < top_k < V else V
+        w[..., K:] = 0.0
+        if top_p < 1.0:
+            tot = w.sum(-1, keepdim=True)
+            before = torch.cumsum(w, -1) - w
+            w = torch.where(before < top_p * tot, w, torch.zeros_like(w))
+        pick = torch.multinomial(w.view(-1, V), 1, generator=gen).view(d.shape[0], k)
+        g = torch.gather(idx, -1, pick.unsqueeze(-1)).squeeze(-1)
+        g[greedy] = idx[greedy][..., 0]
+        toks[b0:b0 + 64] = g.to(torch.int32)
+    return toks
+
+
+def run_reference_filtered(args):
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return
+    import oracle
+    import torch
+    oracle.build()
+    case = make_workload(args.config, 0, args.batch)
+    cores = host_cores()
+    per_step = min(case.B, max(cores, 16))
+    sub = case.subset(np.arange(per_step))
+    # tokens from the filtered draft distribution (generated on the CPU here)
+    d = torch.from_numpy(synth_decode(sub.draft))
+    sub.tokens = filtered_draft_tokens(d, torch.from_numpy(sub.temperature), args.top_k,
+                                       args.top_p, 1234).numpy()
+    tk = np.full(per_step, args.top_k, np.int32)
+    tp = np.full(per_step, args.top_p)
+    run = lambda: oracle.verify_filtered(sub.target, sub.draft, sub.tokens, sub.u_accept,
+                                         sub.u_resample, sub.temperature, tk, tp,
+                                         nthreads=cores, want_trace=False)
+    for _ in range(args.warmup):
+        run()
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        run()
+    dt = time.perf_counter() - t0
+    value = per_step * case.k * args.steps / dt
+    from speculative_decoding_verification_65_gb300 import synth
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT,
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": dt / args.steps * 1e3, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": synth.CONFIG_NAMES[args.config], "B": per_step, "k": case.k,
+                   "V": case.V, "top_k": args.top_k, "top_p": args.top_p,
+                   "what": "fp64 CPU oracle, filtered (plain C, threads over sequences)"},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
+                         "sample": f"first {per_step} of {case.B} sequences per step"},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def synth_decode(a):
+    from speculative_decoding_verification_65_gb300 import synth
+    return synth.decode(a)
+
+
+def run_ours_filtered(args):
+    import torch
+
+    import speculative_decoding_verification_65_gb300 as sv
+    from speculative_decoding_verification_65_gb300 import synth
+
+    rank, world, local = dist_env()
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+
+    def barrier():
+        if world > 1:
+            import torch.distributed as dist
+            dist.barrier()
+
+    case = make_workload(args.config, rank, args.batch)
+    B, k, V = case.B, case.k, case.V
+    d = sv.to_device(case, dev)
+    d["tokens"] = filtered_draft_tokens(d["draft"], d["temperature"], args.top_k, args.top_p,
+                                        1234 + rank)
+    top_k = torch.full((B,), args.top_k, dtype=torch.int32, device=dev)
+    top_p = torch.full((B,), args.top_p, dtype=torch.float32, device=dev)
+    dt_code = sv.SPEC_F32 if case.dtype == synth.F32 else sv.SPEC_BF16
+    stream = torch.cuda.current_stream(dev)
+    ws = sv.workspace(B, k, V, dt_code, dev, stream)
+    out_t = torch.empty((B, k + 1), dtype=torch.int32, device=dev)
+    out_n = torch.empty((B,), dtype=torch.int32, device=dev)
+    alg_bytes = synth.algorithmic_bytes(case)
+
+    def step(events=None):
+        if events is None:
+            sv.spec_verify_filtered(**d, top_k=top_k, top_p=top_p, out_tokens=out_t,
+                                    out_num_accepted=out_n, ws=ws, stream=stream)
+        else:
+            sv.spec_verify_filtered_timed(**d, top_k=top_k, top_p=top_p, out_tokens=out_t,
+                                          out_num_accepted=out_n, ws=ws, stage_events=events,
+                                          stream=stream)
+
+    for _ in range(max(args.warmup, 3)):
+        step()
+    torch.cuda.synchronize(dev)
+    if sv.spec_verify_read_status(ws) != sv.SPEC_DEV_OK:
+        raise RuntimeError("device status nonzero after warm-up")
+    n_err = int((out_n < 0).sum().item())
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    barrier()
+    torch.cuda.synchronize(dev)
+    with ClockSampler(local) as clk:
+        t0.record(stream)
+        for _ in range(args.steps):
+            step()
+        t1.record(stream)
+        torch.cuda.synchronize(dev)
+    barrier()
+    total_ms = reduce_max(t0.elapsed_time(t1), world, dev)
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    stages = [[torch.cuda.Event(enable_timing=True) for _ in range(sv.SPEC_FILTERED_STAGES)]
+              for _ in range(args.steps)]
+    for ev in [e for row in stages for e in row]:
+        ev.record(stream)
+    torch.cuda.synchronize(dev)
+    for i in range(args.steps):
+        starts[i].record(stream)
+        step(stages[i])
+    torch.cuda.synchronize(dev)
+    stage_ms = [statistics.mean(
+        (starts[i] if j == 0 else stages[i][j - 1]).elapsed_time(stages[i][j])
+        for i in range(args.steps)) for j in range(sv.SPEC_FILTERED_STAGES)]
+    ms_per_step = total_ms / args.steps
+    value = aggregate_rate(B * k, args.steps, world, total_ms / 1e3)
+    status = sv.spec_verify_read_status(ws)
+
+    # end to end: pinned host inputs copied in, the call, the outputs copied back
+    pin = lambda t: t.cpu().pin_memory()
+    host = {n: pin(t) for n, t in d.items()}
+    h_k, h_p = pin(top_k), pin(top_p)
+    h_ot = torch.empty((B, k + 1), dtype=torch.int32).pin_memory()
+    h_on = torch.empty((B,), dtype=torch.int32).pin_memory()
+    e2e_steps = max(1, min(args.steps, 20))
+    barrier()
+    e0 = time.perf_counter()
+    for _ in range(e2e_steps):
+        dd = {n: t.to(dev, non_blocking=True) for n, t in host.items()}
+        tk, tp = h_k.to(dev, non_blocking=True), h_p.to(dev, non_blocking=True)
+        sv.spec_verify_filtered(**dd, top_k=tk, top_p=tp, out_tokens=out_t,
+                                out_num_accepted=out_n, ws=ws, stream=stream)
+        h_ot.copy_(out_t, non_blocking=True)
+        h_on.copy_(out_n, non_blocking=True)
+        torch.cuda.synchronize(dev)
+    e2e_s = reduce_max(time.perf_counter() - e0, world, dev)
+    e2e_value = aggregate_rate(B * k, e2e_steps, world, e2e_s)
+    h2d = sum(int(t.numel() * t.element_size()) for t in host.values()) + 8 * B
+    if rank != 0:
+        if world > 1:
+            import torch.distributed as dist
+            dist.destroy_process_group()
+        return
+    peaks, peak_src = measured_peaks()
+    achieved = alg_bytes / (stage_ms[0] / 1e3) / 1e9
+    peak = float(peaks.get("hbm_gbs", 6800.0))
+    workload = synth.CONFIG_NAMES[args.config] if args.batch is None else case.name
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": max(args.warmup, 3), "ms_per_step": ms_per_step,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "f32", "data": "synthetic",
+        "config": {"workload": workload, "B_per_gpu": B, "k": k, "V": V,
+                   "input_dtype": case.dtype, "top_k": args.top_k, "top_p": args.top_p,
+                   "draft_tokens": "drawn from the filtered draft distribution",
+                   "error_sequences": n_err, "algorithmic_bytes_per_step": alg_bytes,
+                   "l2": "inputs larger than L2 (no flush)", "parallelism": f"dp{world}"},
+        "gpu_launches": sv.SPEC_FILTERED_STAGES * args.steps,
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                     "frac": achieved / peak, "traffic": None,
+                     "peak_source": f"{peak_src} copy bandwidth (MEASURED_PEAKS.json hbm_gbs)"
+                     if peak_src == "measured" else "fallback 6.8 TB/s",
+                     "kernel": "stats_kernel (row statistics, the HBM-bound stage)",
+                     "kernel_timing": "CUDA events after each kernel, K further steps",
+                     "step_GBps": alg_bytes / (ms_per_step / 1e3) / 1e9},
+        "stage_ms": {"stats": stage_ms[0], "filter": stage_ms[1], "scan": stage_ms[2],
+                     "draw": stage_ms[3], "final": stage_ms[4]},
+        "clocks": clk.summary(),
+        "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": int(B * (k + 2) * 4), "steps": e2e_steps,
+                "path": "torch copies of pinned host tensors around spec_verify_filtered"},
+        "cpu_baseline": None,
+        "device_status": status,
+    }
+    if world == 1 and not args.no_cpu_baseline:
+        import oracle
+        cores = host_cores()
+        sub = case.subset(np.arange(min(B, max(cores, 16))))
+        sub.tokens = d["tokens"][:sub.B].cpu().numpy()
+        tk_n = np.full(sub.B, args.top_k, np.int32)
+        tp_n = np.full(sub.B, args.top_p)
+        c0 = time.perf_counter()
+        oracle.verify_filtered(sub.target, sub.draft, sub.tokens, sub.u_accept, sub.u_resample,
+                               sub.temperature, tk_n, tp_n, nthreads=cores, want_trace=False)
+        used = time.perf_counter() - c0
+        line["cpu_baseline"] = {"value": sub.B * k / used, "unit": UNIT, "cores": cores,
+                                "kind": "oracle",
+                                "sample": f"{sub.B} of {B} sequences, {used:.1f} s on {cores} threads"}
+    print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
 # ------------------------------------------------------------------ sampling
 
 def make_sample_workload(cfg: int, rank: int, batch=None):
@@ -653,7 +889,9 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--config", type=int, default=None, choices=[1, 2, 3, 4, 5],
                     help="workload (default 4 for verify, 5 for sample)")
-    ap.add_argument("--op", choices=["verify", "sample"], default="verify")
+    ap.add_argument("--op", choices=["verify", "sample", "filtered"], default="verify")
+    ap.add_argument("--top-k", type=int, default=50, help="top-k of --op filtered (0: none)")
+    ap.add_argument("--top-p", type=float, default=0.9, help="top-p of --op filtered (1: none)")
     ap.add_argument("--batch", type=int, default=None,
                     help="smaller batch of the same recipe (profiling captures only)")
     ap.add_argument("--cpu-budget", type=float, default=10.0)
@@ -669,6 +907,11 @@ def main():
             run_reference_sample(args)
         else:
             run_ours_sample(args)
+    elif args.op == "filtered":
+        if args.impl == "reference":
+            run_reference_filtered(args)
+        else:
+            run_ours_filtered(args)
     elif args.impl == "reference":
         run_reference(args)
     else:

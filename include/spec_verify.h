@@ -86,9 +86,10 @@ const char *spec_verify_strerror(int32_t status);
 /*
  * Bytes of device workspace one spec_verify call needs for these sizes: a
  * 256-byte header (the status word), one 16-byte partial per 128 KB of every
- * row, and per sequence a 64-byte draw record, its inverse-CDF chunk totals
- * (32 bytes per 16 KB of a row) and its bonus row's chunk records (8 bytes
- * per 4 KB of a row).  Returns 0 for sizes out of range.
+ * row, and per sequence an 80-byte draw record, its inverse-CDF chunk totals
+ * (32 bytes per 16 KB of a row), its bonus row's chunk records (8 bytes per
+ * 4 KB of a row) and a 16-byte top-k / top-p record per row (read by
+ * spec_verify_filtered only).  Returns 0 for sizes out of range.
  * Host-only; needs no GPU.
  */
 size_t spec_verify_workspace_size(int32_t B, int32_t k, int32_t V, int32_t dtype);
@@ -141,6 +142,49 @@ int32_t spec_verify_probs(const void *target_logits, const void *draft_logits,
                           int32_t *out_tokens, int32_t *out_num_accepted, float *out_probs,
                           int32_t B, int32_t k, int32_t V, int32_t dtype,
                           void *workspace, size_t workspace_bytes, void *stream);
+
+/*
+ * spec_verify with top-k / top-p filtered distributions.  The pages require
+ * draft and target to share their sampling parameters, top-p among them
+ * ("Speculative Decoding and the Art of Fast LLM Inference", "Why It Stays
+ * Exact", key limitation), without defining the filters; the reading taken:
+ * the tokens of a row are ranked by logit, descending, ties by index
+ * ascending; top-k keeps the first K of them; top-p keeps, among those, a
+ * token while the mass ranked before it is below P times the top-k mass (at
+ * least one token stays); p and q are renormalised over their kept sets before
+ * the accept test, the residual and the bonus draw.  Greedy sequences (T = 0)
+ * are unaffected.
+ *   top_k  device int32 [B] or NULL: 0 or >= V = no top-k; < 0 = sequence error
+ *   top_p  device float32 [B] or NULL: >= 1 = no top-p; NaN or <= 0 = sequence error
+ *   out_probs  device float32 [B, k, 2] or NULL: the filtered P = p~_i(g_i),
+ *          Q = q~_i(g_i) (NaN for greedy and error sequences)
+ * A draft token outside the draft's kept set (q~(g) = 0) is a sequence error.
+ * Other arguments, the workspace (spec_verify_workspace_size) and errors as
+ * spec_verify.  Five kernels run: statistics, filter (per row, a radix search
+ * for the end of the kept set), accept scan, draw tiles, final search.
+ */
+int32_t spec_verify_filtered(const void *target_logits, const void *draft_logits,
+                             const int32_t *draft_tokens, const float *u_accept,
+                             const float *u_resample, const float *temperature,
+                             const int32_t *top_k, const float *top_p,
+                             int32_t *out_tokens, int32_t *out_num_accepted, float *out_probs,
+                             int32_t B, int32_t k, int32_t V, int32_t dtype,
+                             void *workspace, size_t workspace_bytes, void *stream);
+
+/*
+ * spec_verify_filtered with stage events as in spec_verify_timed, one per
+ * kernel: SPEC_FILTERED_STAGES of them (statistics, filter, accept scan, draw
+ * tiles, final search).
+ */
+#define SPEC_FILTERED_STAGES 5
+int32_t spec_verify_filtered_timed(const void *target_logits, const void *draft_logits,
+                                   const int32_t *draft_tokens, const float *u_accept,
+                                   const float *u_resample, const float *temperature,
+                                   const int32_t *top_k, const float *top_p,
+                                   int32_t *out_tokens, int32_t *out_num_accepted,
+                                   int32_t B, int32_t k, int32_t V, int32_t dtype,
+                                   void *workspace, size_t workspace_bytes, void *stream,
+                                   void *const *stage_events);
 
 /*
  * spec_verify with per-stage timing: `stage_events` (nullable; entries may be

@@ -28,6 +28,7 @@ SPEC_MAX_K = 32
 SPEC_MAX_V = 1 << 20
 SPEC_STAGES = 4
 SPEC_SAMPLE_STAGES = 2
+SPEC_FILTERED_STAGES = 5
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "libspecverify.so")
@@ -65,6 +66,10 @@ def library():
         lib.spec_verify_probs.argtypes = [vp] * 9 + [i32] * 4 + [vp, sz, vp]
         lib.spec_verify_timed.restype = i32
         lib.spec_verify_timed.argtypes = [vp] * 8 + [i32] * 4 + [vp, sz, vp, vp]
+        lib.spec_verify_filtered.restype = i32
+        lib.spec_verify_filtered.argtypes = [vp] * 11 + [i32] * 4 + [vp, sz, vp]
+        lib.spec_verify_filtered_timed.restype = i32
+        lib.spec_verify_filtered_timed.argtypes = [vp] * 10 + [i32] * 4 + [vp, sz, vp, vp]
         lib.spec_verify_noalloc.restype = i32
         lib.spec_verify_noalloc.argtypes = [vp] * 8 + [i32] * 4 + [vp]
         lib.spec_verify_noalloc_max_bytes.restype = sz
@@ -228,6 +233,60 @@ def spec_verify(target, draft, tokens, u_accept, u_resample, temperature,
                                _ptr(out_num_accepted), B, k, V, dt, _ptr(ws), ws.numel(),
                                _stream_handle(stream, dev))
     _check(rc, "spec_verify")
+    return out_tokens, out_num_accepted
+
+
+def _filters(B, dev, top_k, top_p):
+    torch = _torch()
+    for name, t, dtype in (("top_k", top_k, torch.int32), ("top_p", top_p, torch.float32)):
+        if t is not None and (tuple(t.shape) != (B,) or t.dtype != dtype or not t.is_cuda
+                              or not t.is_contiguous() or t.device != dev):
+            raise ValueError(f"{name} must be a contiguous {dtype} CUDA tensor of shape ({B},)")
+
+
+def spec_verify_filtered(target, draft, tokens, u_accept, u_resample, temperature,
+                         top_k=None, top_p=None, out_tokens=None, out_num_accepted=None,
+                         want_probs=False, ws=None, stream=None):
+    """spec_verify with top-k / top-p filtered distributions (see
+    include/spec_verify.h): top_k int32 [B] (0 = none), top_p float32 [B]
+    (>= 1 = none), either may be None.  Returns (out_tokens, out_num_accepted)
+    and, with want_probs, the filtered P, Q [B, k, 2] as a third value."""
+    torch = _torch()
+    B, k, V, dt = _marshal(target, draft, tokens, u_accept, u_resample, temperature)
+    dev = target.device
+    _filters(B, dev, top_k, top_p)
+    if out_tokens is None:
+        out_tokens = torch.empty((B, k + 1), dtype=torch.int32, device=dev)
+    if out_num_accepted is None:
+        out_num_accepted = torch.empty((B,), dtype=torch.int32, device=dev)
+    probs = torch.empty((B, k, 2), dtype=torch.float32, device=dev) if want_probs else None
+    if ws is None:
+        ws = workspace(B, k, V, dt, dev, stream)
+    rc = library().spec_verify_filtered(_ptr(target), _ptr(draft), _ptr(tokens), _ptr(u_accept),
+                                        _ptr(u_resample), _ptr(temperature), _ptr(top_k),
+                                        _ptr(top_p), _ptr(out_tokens), _ptr(out_num_accepted),
+                                        _ptr(probs), B, k, V, dt, _ptr(ws), ws.numel(),
+                                        _stream_handle(stream, dev))
+    _check(rc, "spec_verify_filtered")
+    if want_probs:
+        return out_tokens, out_num_accepted, probs
+    return out_tokens, out_num_accepted
+
+
+def spec_verify_filtered_timed(target, draft, tokens, u_accept, u_resample, temperature,
+                               top_k, top_p, out_tokens, out_num_accepted, ws, stage_events,
+                               stream=None):
+    """spec_verify_filtered recording SPEC_FILTERED_STAGES events, one after
+    each kernel (statistics, filter, accept scan, draw tiles, final search)."""
+    B, k, V, dt = _marshal(target, draft, tokens, u_accept, u_resample, temperature)
+    _filters(B, target.device, top_k, top_p)
+    handles = (ctypes.c_void_p * SPEC_FILTERED_STAGES)(
+        *[ctypes.c_void_p(e.cuda_event) for e in stage_events])
+    rc = library().spec_verify_filtered_timed(
+        _ptr(target), _ptr(draft), _ptr(tokens), _ptr(u_accept), _ptr(u_resample),
+        _ptr(temperature), _ptr(top_k), _ptr(top_p), _ptr(out_tokens), _ptr(out_num_accepted),
+        B, k, V, dt, _ptr(ws), ws.numel(), _stream_handle(stream, target.device), handles)
+    _check(rc, "spec_verify_filtered_timed")
     return out_tokens, out_num_accepted
 
 

@@ -70,15 +70,48 @@ enum { KIND_END = 0, KIND_STATS = 1 };
 enum { MODE_SKIP = 0, MODE_GREEDY = 1, MODE_SAMPLE = 2 };   // stats work
 enum { DRAW_NONE = 0, DRAW_RESIDUAL = 1, DRAW_TARGET = 2 };
 
-// The draw of one sequence (kernel 2 -> kernels 3 and 4).
+// The draw of one sequence (kernel 2 -> kernels 3 and 4).  With top-k /
+// top-p filtering (filt = 1), x is in the target row's kept set iff
+// key(x) > kt or (key(x) == kt and x <= it), likewise for the draft row, and
+// rzt / rzd are the reciprocals of the kept sets' masses.
 struct alignas(16) JobRec {
-    int mode, j, b, pad;
+    int mode, j, b, filt;
     float mt, rzt, md, rzd;
     float c, u;
     int pad0, pad1;
     long long t_row, d_row;
+    unsigned int kt;
+    int it;
+    unsigned int kd;
+    int id;
 };
-static_assert(sizeof(JobRec) == 64, "job record is 64 bytes");
+static_assert(sizeof(JobRec) == 80, "job record is 80 bytes");
+constexpr int JOB_VECS = (int)(sizeof(JobRec) / 16);
+
+// Top-k / top-p boundary of one row (filter kernel -> scan kernel).
+struct alignas(16) FiltRec {
+    unsigned int kappa;  // key of the last kept token
+    int iota;            // its index (ties at kappa are kept up to it)
+    float zt;            // mass of the kept set, relative to the row maximum
+    int flags;           // FILT_OFF, FILT_ON, FILT_ERR
+};
+enum { FILT_OFF = 0, FILT_ON = 1, FILT_ERR = 2 };
+
+// Order-preserving unsigned key of an fp32 bit pattern (bf16 values widen
+// exactly, so their keys order the same way).
+__host__ __device__ __forceinline__ unsigned int okey(unsigned int b)
+{
+    return (b & 0x80000000u) ? ~b : (b | 0x80000000u);
+}
+
+// The key of a logit of dtype DT: for bf16 only the top 16 bits carry it (a
+// widened bf16 has 16 zero low bits, which the complement of a negative
+// value would turn into ones).
+template <int DT>
+__device__ __forceinline__ unsigned int key_of(float x)
+{
+    return okey(__float_as_uint(x)) & ((DT == SPEC_BF16) ? 0xffff0000u : 0xffffffffu);
+}
 
 struct TileInfo {
     int kind;
@@ -109,6 +142,9 @@ struct Params {
     JobRec *jobs;      // [B]
     float *chunks;     // [B][chunk_stride]
     float2 *rec;       // [B][NCH] chunk records of each sequence's bonus row
+    const int32_t *top_k;  // [B] or null (filtered calls)
+    const float *top_p;    // [B] or null (filtered calls)
+    FiltRec *filt;     // [B][rows] (filtered calls)
     int B, k, V;
     int NS;            // tiles per row
     int NSS;           // super-tiles per row
@@ -419,14 +455,589 @@ __global__ void __launch_bounds__(NTHREADS, 2) stats_kernel(const Params P)
     }
 }
 
-// -------------------------------------------------------------- accept scan
+// ---------------------------------------------------- top-k / top-p filter
+//
+// One CTA per row of every sequence whose call asks for filtering.  The kept
+// set is a prefix of the row ranked by (logit descending, index ascending):
+// top-k keeps the first K; top-p keeps, among those, a token while the mass
+// ranked before it is below P times the top-k mass.  Its end (the last kept
+// token) is found by a radix search on the order-preserving key, four bits per
+// pass from the top.  Each pass reads the row (from L2 after the first) and
+// fills per-thread columns of a shared-memory histogram -- counts, and masses
+// 2^((x - m) * c) in 2^-40 fixed point -- that are summed in a fixed order, so
+// every decision is deterministic.  As soon as the bucket holding the end has
+// at most FCAP tokens, they are gathered in index order, sorted by (key desc,
+// index asc) and the end is read off the sorted list; if a single key value
+// holds more ties than that, a pass in index order counts them instead.
+
+constexpr int FTH = 512;         // filter threads
+constexpr int FBINS = 16;        // buckets per pass (4-bit digits)
+constexpr int FCAP = 4096;       // tokens finished by a sort in shared memory
+constexpr int FUNR = 4;          // 16-byte vectors per thread in flight in a row pass
+constexpr float FIX = 1099511627776.0f;  // 2^40
+
+struct FiltSmem {
+    union {
+        struct {
+            unsigned int cnt[FBINS][FTH];
+            unsigned long long mass[FBINS][FTH];
+        } h;
+        struct {
+            unsigned long long key[FCAP];   // (key << 32) | ~index: descending = the ranking
+            unsigned long long mass[FCAP];
+        } c;
+    } u;
+    unsigned int bcnt[FBINS];
+    unsigned long long bmass[FBINS];
+    unsigned int wcnt[FTH / 32];
+    unsigned long long wmass[FTH / 32];
+    float m;
+    int flags;
+    int sel;                 // selected bucket, or -1
+    int found;               // index found by a tie pass
+    unsigned long long acc;  // scratch sum
+};
+constexpr size_t FILT_SMEM = sizeof(FiltSmem);
+
+__device__ __forceinline__ unsigned long long fixmass(float x, float m, float c)
+{
+    return __float2ull_rn(ex2((x - m) * c) * FIX);
+}
+
+__device__ __forceinline__ unsigned long long sortkey(unsigned int key, int idx)
+{
+    return ((unsigned long long)key << 32) | (unsigned long long)(0xffffffffu - (unsigned int)idx);
+}
+
+// Block-wide exclusive prefix of one count per thread (index order = thread
+// order) and the block total.
+__device__ __forceinline__ unsigned int block_excl_scan(unsigned int x, FiltSmem &S,
+                                                        unsigned int &total)
+{
+    const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
+    unsigned int incl = x;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const unsigned int y = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o)
+            incl += y;
+    }
+    if (lane == 31)
+        S.wcnt[warp] = incl;
+    __syncthreads();
+    unsigned int wbase = 0, tot = 0;
+    for (int w = 0; w < FTH / 32; ++w) {
+        const unsigned int v = S.wcnt[w];
+        if (w < warp)
+            wbase += v;
+        tot += v;
+    }
+    __syncthreads();
+    total = tot;
+    return wbase + incl - x;
+}
 
 template <int DT>
+__global__ void __launch_bounds__(FTH, 2) filter_kernel(const Params P)
+{
+    using L = Lg<DT>;
+    constexpr int VEC = L::VEC;
+    constexpr int LOW_SHIFT = (DT == SPEC_F32) ? 0 : 16;  // bf16 keys end at bit 16
+    extern __shared__ __align__(16) uint8_t fsm_raw[];
+    FiltSmem &S = *reinterpret_cast<FiltSmem *>(fsm_raw);
+    const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
+    const int V = P.V;
+    const int nvec = (V + VEC - 1) / VEC;
+    const int items = P.B * P.rows;
+    allow_next_kernel();
+    wait_previous_kernel();  // partials come from the statistics kernel
+
+    for (int item = blockIdx.x; item < items; item += gridDim.x) {
+        const int b = item / P.rows, rsq = item - b * P.rows;
+        const bool is_target = rsq <= P.k;
+        const void *arr = is_target ? P.target : P.draft;
+        const size_t row = is_target ? (size_t)b * (P.k + 1) + rsq
+                                     : (size_t)b * P.k + (rsq - P.k - 1);
+        const float T = __ldg(P.temperature + b);
+        const int K = P.top_k ? __ldg(P.top_k + b) : 0;
+        const float Pp = P.top_p ? __ldg(P.top_p + b) : 1.0f;
+        FiltRec out;
+        out.kappa = 0u;
+        out.iota = INT_MAX;
+        out.zt = 0.0f;
+        out.flags = FILT_OFF;
+        const bool topk = K > 0 && K < V;
+        const bool topp = Pp < 1.0f;
+        const bool bad = K < 0 || isnan(Pp) || !(Pp > 0.0f);
+        if (temperature_valid(T) && bad) {
+            out.flags = FILT_ERR;  // bad filter parameters fail the sequence, greedy too
+            if (t == 0)
+                P.filt[item] = out;
+            continue;
+        }
+        if (!temperature_valid(T) || T == 0.0f || (!topk && !topp)) {
+            if (t == 0)
+                P.filt[item] = out;  // greedy, invalid or unfiltered: nothing to keep out
+            continue;
+        }
+        // the row maximum and total mass from the statistics kernel's partials
+        const float c = LOG2E / T;
+        if (warp == 0) {
+            const float4 *pp = P.part + ((size_t)b * P.rows + rsq) * P.NSS;
+            float m = -INFINITY;
+            for (int q = lane; q < P.NSS; q += 32)
+                m = fmax_nan(m, __ldcg(pp + q).x);
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1)
+                m = fmax_nan(m, __shfl_xor_sync(0xffffffffu, m, o));
+            float z = 0.0f;
+            for (int q = lane; q < P.NSS; q += 32) {
+                const float4 pv = __ldcg(pp + q);
+                z += rescale(pv.y, pv.x, m, c);
+            }
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1)
+                z += __shfl_xor_sync(0xffffffffu, z, o);
+            if (lane == 0) {
+                S.m = m;
+                S.acc = (unsigned long long)((double)z * 1099511627776.0);
+            }
+        }
+        __syncthreads();
+        const float m = S.m;
+        const unsigned long long Zrow = S.acc;  // 2^-40 fixed point
+        __syncthreads();
+        if (isnan(m) || isinf(m)) {
+            if (t == 0)
+                P.filt[item] = out;  // the scan reports the row as an error
+            continue;
+        }
+
+        // Row passes keep FUNR 16-byte vectors per thread in flight.  The
+        // unordered pass gives thread t the vectors t*FUNR + i*FTH*FUNR + u;
+        // the ordered one, round by round, the FUNR consecutive vectors after
+        // those of thread t-1, so thread order is index order.
+        auto load_vecs = [&](int v0, uint4 (&r)[FUNR]) {
+#pragma unroll
+            for (int u = 0; u < FUNR; ++u)
+                r[u] = (v0 + u < nvec) ? row_vec<DT>(arr, row, v0 + u, V)
+                                       : neg_inf_vec(L::NEG_INF_WORD);
+        };
+        auto member = [](unsigned int key, int idx, unsigned int kk, int ik) {
+            return key > kk || (key == kk && idx <= ik);
+        };
+        // histogram of bin_of(x, key, idx) (-1: not counted): counts and masses
+        auto hist = [&](auto bin_of, auto vskip) {
+#pragma unroll
+            for (int bb = 0; bb < FBINS; ++bb) {
+                S.u.h.cnt[bb][t] = 0u;
+                S.u.h.mass[bb][t] = 0ull;
+            }
+            for (int v0 = t * FUNR; v0 < nvec; v0 += FTH * FUNR) {
+                uint4 r[FUNR];
+                load_vecs(v0, r);
+#pragma unroll
+                for (int u = 0; u < FUNR; ++u) {
+                    if (vskip(r[u]))
+                        continue;  // no token of this vector can count
+                    float x[VEC];
+                    L::unpack(r[u], x);
+#pragma unroll
+                    for (int j = 0; j < VEC; ++j) {
+                        const int idx = (v0 + u) * VEC + j;
+                        const int bin = (idx < V) ? bin_of(x[j], key_of<DT>(x[j]), idx) : -1;
+                        if (bin >= 0) {
+                            S.u.h.cnt[bin][t] += 1u;
+                            S.u.h.mass[bin][t] += fixmass(x[j], m, c);
+                        }
+                    }
+                }
+            }
+            __syncthreads();
+            // fixed-order sums: warp w adds the columns of buckets w, w+16, ...
+            for (int bin = warp; bin < FBINS; bin += FTH / 32) {
+                unsigned int cs = 0u;
+                unsigned long long ms = 0ull;
+                for (int i = lane; i < FTH; i += 32) {
+                    cs += S.u.h.cnt[bin][i];
+                    ms += S.u.h.mass[bin][i];
+                }
+#pragma unroll
+                for (int o = 16; o > 0; o >>= 1) {
+                    cs += __shfl_xor_sync(0xffffffffu, cs, o);
+                    ms += __shfl_xor_sync(0xffffffffu, ms, o);
+                }
+                if (lane == 0) {
+                    S.bcnt[bin] = cs;
+                    S.bmass[bin] = ms;
+                }
+            }
+            __syncthreads();
+        };
+        // the tokens with pred(x, key, idx), in index order, into the sort buffer
+        auto gather = [&](auto pred, auto vskip) -> int {
+            unsigned int base = 0u;
+            for (int vb = 0; vb < nvec; vb += FTH * FUNR) {
+                const int v0 = vb + t * FUNR;
+                uint4 r[FUNR];
+                load_vecs(v0, r);
+                unsigned int n = 0u;
+                bool live[FUNR];
+#pragma unroll
+                for (int u = 0; u < FUNR; ++u) {
+                    live[u] = !vskip(r[u]);
+                    if (!live[u])
+                        continue;
+                    float x[VEC];
+                    L::unpack(r[u], x);
+#pragma unroll
+                    for (int j = 0; j < VEC; ++j) {
+                        const int idx = (v0 + u) * VEC + j;
+                        n += (idx < V && pred(x[j], key_of<DT>(x[j]), idx)) ? 1u : 0u;
+                    }
+                }
+                unsigned int tot;
+                unsigned int pos = base + block_excl_scan(n, S, tot);
+                if (n) {
+#pragma unroll
+                    for (int u = 0; u < FUNR; ++u) {
+                        if (!live[u])
+                            continue;
+                        float x[VEC];
+                        L::unpack(r[u], x);
+#pragma unroll
+                        for (int j = 0; j < VEC; ++j) {
+                            const int idx = (v0 + u) * VEC + j;
+                            const unsigned int key = key_of<DT>(x[j]);
+                            if (idx < V && pred(x[j], key, idx)) {
+                                if (pos < (unsigned int)FCAP) {  // never past the buffer
+                                    S.u.c.key[pos] = sortkey(key, idx);
+                                    S.u.c.mass[pos] = fixmass(x[j], m, c);
+                                }
+                                ++pos;
+                            }
+                        }
+                    }
+                }
+                base += tot;
+            }
+            __syncthreads();
+            return (int)(base < (unsigned int)FCAP ? base : (unsigned int)FCAP);
+        };
+        // bitonic sort of the first n gathered tokens, descending
+        auto sort_desc = [&](int n) {
+            int p2 = 1;
+            while (p2 < n)
+                p2 <<= 1;
+            for (int i = n + t; i < p2; i += FTH) {
+                S.u.c.key[i] = 0ull;
+                S.u.c.mass[i] = 0ull;
+            }
+            __syncthreads();
+            for (int kk = 2; kk <= p2; kk <<= 1) {
+                for (int jj = kk >> 1; jj > 0; jj >>= 1) {
+                    for (int i = t; i < p2; i += FTH) {
+                        const int ixj = i ^ jj;
+                        if (ixj > i) {
+                            const unsigned long long a = S.u.c.key[i], bq = S.u.c.key[ixj];
+                            const bool desc = (i & kk) == 0;
+                            if (desc ? (a < bq) : (a > bq)) {
+                                S.u.c.key[i] = bq;
+                                S.u.c.key[ixj] = a;
+                                const unsigned long long ma = S.u.c.mass[i];
+                                S.u.c.mass[i] = S.u.c.mass[ixj];
+                                S.u.c.mass[ixj] = ma;
+                            }
+                        }
+                    }
+                    __syncthreads();
+                }
+            }
+        };
+        // mass of the first r sorted tokens (fixed order)
+        auto sorted_prefix_mass = [&](int r) -> unsigned long long {
+            if (warp == 0) {
+                unsigned long long ms = 0ull;
+                for (int i = lane; i < r; i += 32)
+                    ms += S.u.c.mass[i];
+#pragma unroll
+                for (int o = 16; o > 0; o >>= 1)
+                    ms += __shfl_xor_sync(0xffffffffu, ms, o);
+                if (lane == 0)
+                    S.acc = ms;
+            }
+            __syncthreads();
+            const unsigned long long v = S.acc;
+            __syncthreads();
+            return v;
+        };
+        // the first of the first n sorted tokens whose running mass (from
+        // `start`) reaches the target; its position and that running mass
+        auto sorted_cut = [&](int n, unsigned long long start, unsigned long long target,
+                              unsigned long long &run_out) -> int {
+            if (warp == 0) {
+                unsigned long long run = start;
+                int istar = -1;
+                for (int i0 = 0; i0 < n && istar < 0; i0 += 32) {
+                    const int i = i0 + lane;
+                    unsigned long long x = (i < n) ? S.u.c.mass[i] : 0ull;
+#pragma unroll
+                    for (int o = 1; o < 32; o <<= 1) {
+                        const unsigned long long y = __shfl_up_sync(0xffffffffu, x, o);
+                        if (lane >= o)
+                            x += y;
+                    }
+                    const unsigned long long incl = run + x;
+                    const unsigned hit = __ballot_sync(0xffffffffu, i < n && incl >= target);
+                    if (hit) {
+                        const int hl = __ffs(hit) - 1;
+                        istar = i0 + hl;
+                        run = __shfl_sync(0xffffffffu, incl, hl);
+                    } else {
+                        run = __shfl_sync(0xffffffffu, incl, 31);
+                    }
+                }
+                if (istar < 0)
+                    istar = n - 1;  // rounding: all of them
+                if (lane == 0) {
+                    S.sel = istar;
+                    S.acc = run;
+                }
+            }
+            __syncthreads();
+            const int i = S.sel;
+            run_out = S.acc;
+            __syncthreads();
+            return i;
+        };
+        auto sorted_at = [&](int i, unsigned int &key, int &idx) {
+            const unsigned long long e = S.u.c.key[i];
+            key = (unsigned int)(e >> 32);
+            idx = (int)(0xffffffffu - (unsigned int)(e & 0xffffffffu));
+        };
+        // the r-th (1-based) token in index order with key == kap (restricted)
+        auto tie_pass = [&](unsigned int kap, unsigned int r, bool rk, unsigned int kK,
+                            int iK) -> int {
+            if (t == 0)
+                S.found = -1;
+            __syncthreads();
+            unsigned int base = 0u;
+            for (int vb = 0; vb < nvec; vb += FTH * FUNR) {
+                const int v0 = vb + t * FUNR;
+                uint4 r4[FUNR];
+                load_vecs(v0, r4);
+                unsigned int n = 0u;
+#pragma unroll
+                for (int u = 0; u < FUNR; ++u) {
+                    float x[VEC];
+                    L::unpack(r4[u], x);
+#pragma unroll
+                    for (int j = 0; j < VEC; ++j) {
+                        const int idx = (v0 + u) * VEC + j;
+                        const unsigned int key = key_of<DT>(x[j]);
+                        n += (idx < V && key == kap && (!rk || member(key, idx, kK, iK))) ? 1u : 0u;
+                    }
+                }
+                unsigned int tot;
+                const unsigned int ex = base + block_excl_scan(n, S, tot);
+                if (n && ex < r && r <= ex + n) {
+                    unsigned int cnt = ex;
+#pragma unroll
+                    for (int u = 0; u < FUNR; ++u) {
+                        float x[VEC];
+                        L::unpack(r4[u], x);
+#pragma unroll
+                        for (int j = 0; j < VEC; ++j) {
+                            const int idx = (v0 + u) * VEC + j;
+                            const unsigned int key = key_of<DT>(x[j]);
+                            if (idx < V && key == kap && (!rk || member(key, idx, kK, iK))) {
+                                if (++cnt == r)
+                                    S.found = idx;
+                            }
+                        }
+                    }
+                }
+                base += tot;
+                __syncthreads();
+                if (S.found >= 0 || base >= r)
+                    break;
+            }
+            __syncthreads();
+            return S.found;
+        };
+        auto fix_of_key = [&](unsigned int key) {
+            unsigned int bits = (key & 0x80000000u) ? (key & 0x7fffffffu) : ~key;
+            if (DT == SPEC_BF16)
+                bits &= 0xffff0000u;
+            return fixmass(__uint_as_float(bits), m, c);
+        };
+
+        unsigned int kap = 0u;
+        int iota = INT_MAX;
+        unsigned long long Zt = 0ull;
+        auto vnone = [](const uint4 &) { return false; };
+
+        // ---- first pass: buckets by distance below the row maximum, one bit
+        // of probability each; tokens more than FBINS bits down are not
+        // counted (they join a kept set only through the general case).  A
+        // bucket set {0..b} is a prefix of the ranking.
+        auto dist_bin = [&](float x) {
+            const float dd = fmaxf((m - x) * c, 0.0f);
+            return (dd < (float)FBINS) ? (int)dd : -1;
+        };
+        // a vector whose maximum is more than FBINS + 1 bits below the row's
+        // holds no counted token (the spare bit absorbs rounding)
+        const float far = m - (float)(FBINS + 1) / c;
+        auto vfar = [&](const uint4 &r) { return !(L::vmax(r) > far) && !isnan(L::vmax(r)); };
+        hist([&](float x, unsigned int, int) { return dist_bin(x); }, vfar);
+        const unsigned long long Ztot = Zrow;
+        int bsel = -1;
+        unsigned int ncum = 0u;
+        {
+            unsigned long long mcum = 0ull;
+            const unsigned long long target0 =
+                topk ? 0ull : (unsigned long long)((double)Pp * (double)Ztot);
+            for (int bb = 0; bb < FBINS; ++bb) {
+                ncum += S.bcnt[bb];
+                mcum += S.bmass[bb];
+                if (topk ? (ncum >= (unsigned int)K) : (mcum >= target0)) {
+                    bsel = bb;
+                    break;
+                }
+            }
+        }
+        if (bsel >= 0 && ncum <= (unsigned int)FCAP) {
+            // ---- the top of the ranking fits the sort buffer: read both cuts
+            // off the sorted list
+            const int n = gather([&](float x, unsigned int, int) {
+                const int bb = dist_bin(x);
+                return bb >= 0 && bb <= bsel;  // the same tokens the histogram counted
+            }, vfar);
+            sort_desc(n);
+            const int nk = topk ? K : n;
+            const unsigned long long ZK = topk ? sorted_prefix_mass(K) : Ztot;
+            int last = nk - 1;
+            Zt = ZK;
+            if (topp) {
+                unsigned long long target = (unsigned long long)((double)Pp * (double)ZK);
+                if (target == 0ull)
+                    target = 1ull;
+                last = sorted_cut(nk, 0ull, target, Zt);
+            }
+            sorted_at(last, kap, iota);
+        } else {
+            // ---- general case: radix search on the key, 4 bits per pass
+            unsigned int kK = 0u;
+            int iK = INT_MAX;
+            unsigned long long ZK = Ztot;
+            if (topk) {
+                unsigned int prefix = 0u, pmask = 0u, above = 0u;
+                unsigned long long amass = 0ull;
+                for (int shift = 28; shift >= LOW_SHIFT; shift -= 4) {
+                    hist([&](float, unsigned int key, int) {
+                        return ((key & pmask) == prefix) ? (int)((key >> shift) & (FBINS - 1)) : -1;
+                    }, vnone);
+                    int sel = 0;
+                    for (int bb = FBINS - 1; bb >= 0; --bb) {
+                        if (above + S.bcnt[bb] >= (unsigned int)K) {
+                            sel = bb;
+                            break;
+                        }
+                        above += S.bcnt[bb];
+                        amass += S.bmass[bb];
+                    }
+                    const unsigned int nsel = S.bcnt[sel];
+                    prefix |= (unsigned int)sel << shift;
+                    pmask |= (unsigned int)(FBINS - 1) << shift;
+                    const unsigned int r = (unsigned int)K - above;
+                    if (nsel <= (unsigned int)FCAP) {
+                        const int n = gather([&](float, unsigned int key, int) {
+                            return (key & pmask) == prefix;
+                        }, vnone);
+                        sort_desc(n);
+                        ZK = amass + sorted_prefix_mass((int)r);
+                        sorted_at((int)r - 1, kK, iK);
+                        break;
+                    }
+                    if (shift == LOW_SHIFT) {  // one key value with more ties than the buffer
+                        kK = prefix;
+                        iK = tie_pass(kK, r, false, 0u, INT_MAX);
+                        ZK = amass + (unsigned long long)r * fix_of_key(kK);
+                    }
+                }
+            }
+            kap = kK;
+            iota = iK;
+            Zt = ZK;
+            if (topp) {
+                unsigned int prefix = 0u, pmask = 0u;
+                unsigned long long amass = 0ull;
+                unsigned long long target = (unsigned long long)((double)Pp * (double)ZK);
+                if (target == 0ull)
+                    target = 1ull;
+                for (int shift = 28; shift >= LOW_SHIFT; shift -= 4) {
+                    hist([&](float, unsigned int key, int idx) {
+                        return ((key & pmask) == prefix && (!topk || member(key, idx, kK, iK)))
+                                   ? (int)((key >> shift) & (FBINS - 1))
+                                   : -1;
+                    }, vnone);
+                    int sel = -1;
+                    for (int bb = FBINS - 1; bb >= 0; --bb) {
+                        if (amass + S.bmass[bb] >= target) {
+                            sel = bb;
+                            break;
+                        }
+                        amass += S.bmass[bb];
+                    }
+                    if (sel < 0)
+                        break;  // rounding: the whole top-k set stays
+                    const unsigned int nsel = S.bcnt[sel];
+                    prefix |= (unsigned int)sel << shift;
+                    pmask |= (unsigned int)(FBINS - 1) << shift;
+                    if (nsel <= (unsigned int)FCAP) {
+                        const int n = gather([&](float, unsigned int key, int idx) {
+                            return (key & pmask) == prefix && (!topk || member(key, idx, kK, iK));
+                        }, vnone);
+                        sort_desc(n);
+                        const int last = sorted_cut(n, amass, target, Zt);
+                        sorted_at(last, kap, iota);
+                        break;
+                    }
+                    if (shift == LOW_SHIFT) {  // ties at one key value: keep r, in index order
+                        const unsigned long long e = fix_of_key(prefix);
+                        unsigned long long r = (target - amass + e - 1) / e;
+                        if (r < 1ull)
+                            r = 1ull;
+                        if (r > nsel)
+                            r = nsel;
+                        kap = prefix;
+                        iota = tie_pass(kap, (unsigned int)r, topk, kK, iK);
+                        Zt = amass + r * e;
+                    }
+                }
+            }
+        }
+        if (t == 0) {
+            out.kappa = kap;
+            out.iota = iota;
+            out.zt = (float)((double)Zt * (1.0 / 1099511627776.0));
+            out.flags = FILT_ON;
+            P.filt[item] = out;
+        }
+        __syncthreads();
+    }
+}
+
+// -------------------------------------------------------------- accept scan
+
+template <int DT, bool FILT>
 __global__ void __launch_bounds__(SCAN_WARPS * 32) scan_kernel(const Params P)
 {
     using L = Lg<DT>;
     __shared__ float rm[SCAN_WARPS][MAX_ROWS], rZ[SCAN_WARPS][MAX_ROWS];
     __shared__ int rarg[SCAN_WARPS][MAX_ROWS], rbad[SCAN_WARPS][MAX_ROWS];
+    __shared__ unsigned int rkap[FILT ? SCAN_WARPS : 1][FILT ? MAX_ROWS : 1];
+    __shared__ int riota[FILT ? SCAN_WARPS : 1][FILT ? MAX_ROWS : 1];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int b = blockIdx.x * SCAN_WARPS + warp;
     if (b >= P.B)
@@ -484,10 +1095,25 @@ __global__ void __launch_bounds__(SCAN_WARPS * 32) scan_kernel(const Params P)
         rarg[warp][r] = idx;
         rbad[warp][r] = (isnan(m) || isinf(m)) ? 1 : 0;  // NaN, +inf, or all -inf
     }
+    // filtered calls: the kept set of each row (the whole row when unfiltered)
+    bool ferr = false, fon = false;
+    if constexpr (FILT) {
+        for (int r = lane; r < P.rows; r += 32) {
+            const FiltRec f = P.filt[(size_t)b * P.rows + r];
+            rkap[warp][r] = f.kappa;
+            riota[warp][r] = f.iota;
+            if (f.flags == FILT_ON && r < nrows)
+                rZ[warp][r] = f.zt;
+            ferr |= f.flags == FILT_ERR;
+            fon |= f.flags == FILT_ON;
+        }
+        ferr = __any_sync(0xffffffffu, ferr);
+        fon = __any_sync(0xffffffffu, fon);
+    }
     __syncwarp();
 
     // 2. accept scan: lane i tests position i
-    bool err = !tvalid;
+    bool err = !tvalid || ferr;
     bool fail = false, qzero = false;
     if (!err) {
         if (lane < k && (g < 0 || g >= V))
@@ -507,14 +1133,21 @@ __global__ void __launch_bounds__(SCAN_WARPS * 32) scan_kernel(const Params P)
             const float ld = L::load1(P.draft, rd * V + g);
             const float mt = rm[warp][lane], zt = rZ[warp][lane];
             const float md = rm[warp][k + 1 + lane], zd = rZ[warp][k + 1 + lane];
-            qzero = (ld == -INFINITY);
+            bool in_t = true, in_d = true;  // g in the target's / draft's kept set
+            if constexpr (FILT) {
+                const unsigned int kt_ = key_of<DT>(lt), kd_ = key_of<DT>(ld);
+                in_t = kt_ > rkap[warp][lane] || (kt_ == rkap[warp][lane] && g <= riota[warp][lane]);
+                in_d = kd_ > rkap[warp][k + 1 + lane] ||
+                       (kd_ == rkap[warp][k + 1 + lane] && g <= riota[warp][k + 1 + lane]);
+            }
+            qzero = (ld == -INFINITY) || !in_d;
             const float dt = lt - mt, dd = ld - md;
             const float x = (dt - dd) * c;
-            const float ratio = ((x == 0.0f) ? 1.0f : ex2(x)) * (zd / zt);
+            const float ratio = in_t ? ((x == 0.0f) ? 1.0f : ex2(x)) * (zd / zt) : 0.0f;
             fail = qzero || !((ratio >= 1.0f) || (ua < ratio));
             if (P.out_probs) {
-                P.out_probs[((size_t)b * k + lane) * 2 + 0] = ex2(dt * c) / zt;
-                P.out_probs[((size_t)b * k + lane) * 2 + 1] = ex2(dd * c) / zd;
+                P.out_probs[((size_t)b * k + lane) * 2 + 0] = in_t ? ex2(dt * c) / zt : 0.0f;
+                P.out_probs[((size_t)b * k + lane) * 2 + 1] = in_d ? ex2(dd * c) / zd : 0.0f;
             }
         }
         const unsigned fm = __ballot_sync(0xffffffffu, fail);
@@ -534,7 +1167,10 @@ __global__ void __launch_bounds__(SCAN_WARPS * 32) scan_kernel(const Params P)
     JobRec J;
     J.b = b;
     J.j = j;
-    J.pad = J.pad0 = J.pad1 = 0;
+    J.filt = 0;
+    J.pad0 = J.pad1 = 0;
+    J.kt = J.kd = 0u;
+    J.it = J.id = INT_MAX;
     if (err || greedy) {
         for (int i = lane; i <= k; i += 32) {
             int o = -1;
@@ -565,8 +1201,17 @@ __global__ void __launch_bounds__(SCAN_WARPS * 32) scan_kernel(const Params P)
             J.md = J.mt;
             J.rzd = J.rzt;
         }
+        if constexpr (FILT) {
+            if (fon) {
+                J.filt = 1;
+                J.kt = rkap[warp][j];
+                J.it = riota[warp][j];
+                J.kd = (j < k) ? rkap[warp][k + 1 + j] : J.kt;
+                J.id = (j < k) ? riota[warp][k + 1 + j] : J.it;
+            }
+        }
     }
-    if (lane < 4)
+    if (lane < JOB_VECS)
         reinterpret_cast<uint4 *>(P.jobs + b)[lane] = reinterpret_cast<const uint4 *>(&J)[lane];
 }
 
@@ -575,26 +1220,37 @@ __global__ void __launch_bounds__(SCAN_WARPS * 32) scan_kernel(const Params P)
 // w(x) = max(0, p(x) - q(x)) (residual) or the unnormalised target weight
 // 2^((t(x)-m)*c) (bonus, or the rounding-only fallback).  -inf padding gives 0.
 
-template <int DT>
+template <int DT, bool FILT>
 __device__ __forceinline__ void draw_weights(const JobRec &J, int mode, const uint4 &rt,
-                                             const uint4 &rd, float (&w)[Lg<DT>::VEC])
+                                             const uint4 &rd, float (&w)[Lg<DT>::VEC], int e0)
 {
     using L = Lg<DT>;
     float xt[L::VEC];
     L::unpack(rt, xt);
+    // top-k / top-p: tokens outside a row's kept set weigh nothing in it
+    auto kept = [&](float x, int j, unsigned int kap, int iota) {
+        if constexpr (!FILT) {
+            return true;
+        } else {
+            if (!J.filt)
+                return true;
+            const unsigned int key = key_of<DT>(x);
+            return key > kap || (key == kap && e0 + j <= iota);
+        }
+    };
     if (mode == DRAW_RESIDUAL) {
         float xd[L::VEC];
         L::unpack(rd, xd);
 #pragma unroll
         for (int j = 0; j < L::VEC; ++j) {
-            const float p = ex2((xt[j] - J.mt) * J.c) * J.rzt;
-            const float q = ex2((xd[j] - J.md) * J.c) * J.rzd;
+            const float p = kept(xt[j], j, J.kt, J.it) ? ex2((xt[j] - J.mt) * J.c) * J.rzt : 0.0f;
+            const float q = kept(xd[j], j, J.kd, J.id) ? ex2((xd[j] - J.md) * J.c) * J.rzd : 0.0f;
             w[j] = fmaxf(p - q, 0.0f);
         }
     } else {
 #pragma unroll
         for (int j = 0; j < L::VEC; ++j)
-            w[j] = ex2((xt[j] - J.mt) * J.c);
+            w[j] = kept(xt[j], j, J.kt, J.it) ? ex2((xt[j] - J.mt) * J.c) : 0.0f;
     }
 }
 
@@ -619,7 +1275,7 @@ __device__ __forceinline__ JobRec load_job(const Params &P, int b)
     uint4 *dst = reinterpret_cast<uint4 *>(&J);
     const uint4 *src = reinterpret_cast<const uint4 *>(P.jobs + b);
 #pragma unroll
-    for (int i = 0; i < 4; ++i)
+    for (int i = 0; i < JOB_VECS; ++i)
         dst[i] = __ldg(src + i);
     return J;
 }
@@ -630,8 +1286,8 @@ __device__ __forceinline__ JobRec load_job(const Params &P, int b)
 //   right).  A block is NT vectors; chunk w of block k holds vectors
 //   k*NT + 32*w .. k*NT + 32*w + 31.  A draw tile (one CTA) holds UD blocks;
 //   warp w writes the totals of chunk w of each.
-template <int DT>
-__global__ void __launch_bounds__(NT, 6) draw_kernel(const Params P)
+template <int DT, bool FILT>
+__global__ void __launch_bounds__(NT, FILT ? 4 : 6) draw_kernel(const Params P)
 {
     using L = Lg<DT>;
     constexpr int VEC = L::VEC;
@@ -640,8 +1296,8 @@ __global__ void __launch_bounds__(NT, 6) draw_kernel(const Params P)
     allow_next_kernel();
     wait_previous_kernel();  // the job comes from the scan kernel
     const JobRec J = load_job(P, b);
-    if (J.mode != DRAW_RESIDUAL)
-        return;  // bonus draws use the statistics kernel's chunk records
+    if (J.mode == DRAW_NONE || (J.mode == DRAW_TARGET && !(FILT && J.filt)))
+        return;  // unfiltered bonus draws use the statistics kernel's chunk records
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     float *out = P.chunks + (size_t)b * P.chunk_stride + (size_t)seg * UD * NCW;
     uint4 rt[UD], rd[UD];
@@ -651,10 +1307,11 @@ __global__ void __launch_bounds__(NT, 6) draw_kernel(const Params P)
         rt[u] = row_vec<DT>(P.target, (size_t)J.t_row, v, P.V);
         rd[u] = (J.mode == DRAW_RESIDUAL) ? row_vec<DT>(P.draft, (size_t)J.d_row, v, P.V) : rt[u];
     }
+    (void)VEC;
 #pragma unroll
     for (int u = 0; u < UD; ++u) {
         float w[VEC];
-        draw_weights<DT>(J, J.mode, rt[u], rd[u], w);
+        draw_weights<DT, FILT>(J, J.mode, rt[u], rd[u], w, ((seg * UD + u) * NT + warp * 32 + lane) * VEC);
         float tau = 0.0f;
 #pragma unroll
         for (int j = 0; j < VEC; ++j)
@@ -675,7 +1332,7 @@ __global__ void __launch_bounds__(NT, 6) draw_kernel(const Params P)
 // smallest x with w(x) > 0 and C(x) > u * R, R the row total; if rounding
 // leaves none in the chunk found, the chunk's last positive-weight token.
 // Returns -1 when the total mass is zero.
-template <int DT>
+template <int DT, bool FILT>
 __device__ int locate(const Params &P, const JobRec &J, int mode, const float *ch, float *btot,
                       int nblk, int lane)
 {
@@ -755,7 +1412,7 @@ __device__ int locate(const Params &P, const JobRec &J, int mode, const float *c
     const uint4 rt = row_vec<DT>(P.target, (size_t)J.t_row, v, P.V);
     const uint4 rd = (mode == DRAW_RESIDUAL) ? row_vec<DT>(P.draft, (size_t)J.d_row, v, P.V) : rt;
     float w[VEC];
-    draw_weights<DT>(J, mode, rt, rd, w);
+    draw_weights<DT, FILT>(J, mode, rt, rd, w, v * VEC);
     float sacc[VEC];
     float s = 0.0f;
 #pragma unroll
@@ -786,7 +1443,7 @@ __device__ int locate(const Params &P, const JobRec &J, int mode, const float *c
 
 // Chunk totals of a whole row computed by one warp (the rounding-only
 // fallback when a residual vanished), in the same hierarchy as draw_kernel.
-template <int DT>
+template <int DT, bool FILT>
 __device__ void warp_row_chunks(const Params &P, const JobRec &J, int mode, float *ch, int nblk,
                                 int lane)
 {
@@ -797,7 +1454,7 @@ __device__ void warp_row_chunks(const Params &P, const JobRec &J, int mode, floa
             const int v = blk * NT + w * 32 + lane;
             const uint4 rt = row_vec<DT>(P.target, (size_t)J.t_row, v, P.V);
             float x[VEC];
-            draw_weights<DT>(J, mode, rt, rt, x);
+            draw_weights<DT, FILT>(J, mode, rt, rt, x, v * VEC);
             float tau = 0.0f;
 #pragma unroll
             for (int j = 0; j < VEC; ++j)
@@ -811,7 +1468,7 @@ __device__ void warp_row_chunks(const Params &P, const JobRec &J, int mode, floa
     __syncwarp();
 }
 
-template <int DT>
+template <int DT, bool FILT>
 __global__ void __launch_bounds__(SCAN_WARPS * 32) final_kernel(const Params P)
 {
     __shared__ float btot[SCAN_WARPS][MAXBLK];
@@ -827,15 +1484,15 @@ __global__ void __launch_bounds__(SCAN_WARPS * 32) final_kernel(const Params P)
     const int nblk = P.DS * UD;
     float *ch = P.chunks + (size_t)b * P.chunk_stride;
     int tok;
-    if (J.mode == DRAW_TARGET)
+    if (J.mode == DRAW_TARGET && !(FILT && J.filt))
         tok = records_draw<DT>(P.rec + (size_t)b * P.NCH, P.NCH, J.mt, J.c, J.u, P.target,
                                (size_t)J.t_row, P.V, lane);
     else
-        tok = locate<DT>(P, J, J.mode, ch, btot[warp], nblk, lane);
+        tok = locate<DT, FILT>(P, J, J.mode, ch, btot[warp], nblk, lane);
     if (tok < 0 && J.mode == DRAW_RESIDUAL) {
         // the residual vanished by rounding alone: draw from p_j instead
-        warp_row_chunks<DT>(P, J, DRAW_TARGET, ch, nblk, lane);
-        tok = locate<DT>(P, J, DRAW_TARGET, ch, btot[warp], nblk, lane);
+        warp_row_chunks<DT, FILT>(P, J, DRAW_TARGET, ch, nblk, lane);
+        tok = locate<DT, FILT>(P, J, DRAW_TARGET, ch, btot[warp], nblk, lane);
     }
     const bool err = tok < 0;
     for (int i = lane; i <= k; i += 32) {
@@ -852,8 +1509,9 @@ __global__ void __launch_bounds__(SCAN_WARPS * 32) final_kernel(const Params P)
 
 struct DevCache {
     int sms = 0;
-    int ctas_per_sm[2] = {0, 0};
+    int ctas_per_sm[2] = {0, 0};        // statistics kernel, per dtype
     bool attr_set[2] = {false, false};
+    bool filt_set[2] = {false, false};  // filter kernel's shared-memory size set
 };
 DevCache g_dev[64];
 
@@ -868,12 +1526,13 @@ bool sizes_ok(int32_t B, int32_t k, int32_t V, int32_t dtype)
 int tile_elems(int32_t dtype) { return TILE_BYTES / (dtype == SPEC_F32 ? 4 : 2); }
 
 struct WsLayout {
-    size_t partials, jobs, chunks, rec, total;
+    size_t partials, jobs, chunks, rec, filt, total;
     size_t NS, NSS, DS, chunk_stride, NCH;
 };
 
 // header | one 16-byte partial per super-tile [B][2k+1][NSS] | draw jobs [B] |
 // inverse-CDF chunk totals [B][chunk_stride] | bonus-row chunk records [B][NCH]
+// | top-k / top-p records [B][2k+1] (filtered calls)
 WsLayout ws_layout(int32_t B, int32_t k, int32_t V, int32_t dtype)
 {
     WsLayout w;
@@ -888,7 +1547,8 @@ WsLayout ws_layout(int32_t B, int32_t k, int32_t V, int32_t dtype)
     w.chunks = align_up(w.jobs + (size_t)B * sizeof(JobRec), 256);
     w.chunk_stride = align_up(w.DS * UD * NCW, 32);  // floats, 128-byte rows
     w.rec = align_up(w.chunks + (size_t)B * w.chunk_stride * 4, 256);
-    w.total = w.rec + (size_t)B * w.NCH * sizeof(float2);
+    w.filt = align_up(w.rec + (size_t)B * w.NCH * sizeof(float2), 256);
+    w.total = w.filt + (size_t)B * (2 * (size_t)k + 1) * sizeof(FiltRec);
     return w;
 }
 
@@ -897,24 +1557,29 @@ size_t ws_bytes(int32_t B, int32_t k, int32_t V, int32_t dtype)
     return ws_layout(B, k, V, dtype).total;
 }
 
-// `events` (nullable): cudaEvent_t recorded after each of the four kernels.
-template <int DT>
-int launch_all(const Params &P, unsigned int grid1, cudaStream_t st, void *const *events)
+// `events` (nullable): cudaEvent_t recorded after each kernel (four, or five
+// with the filter kernel of a filtered call).
+template <int DT, bool FILT>
+int launch_all(const Params &P, unsigned int grid1, unsigned int gridf, cudaStream_t st,
+               void *const *events)
 {
+    // filtered calls record one more event, after the filter kernel
     auto mark = [&](int i) {
-        if (events && events[i])
-            cudaEventRecord(reinterpret_cast<cudaEvent_t>(events[i]), st);
+        const int e = (FILT && i > 0) ? i + 1 : i;
+        if (events && events[e])
+            cudaEventRecord(reinterpret_cast<cudaEvent_t>(events[e]), st);
     };
     // kernels 2..4 may start while their predecessor drains (programmatic
     // dependent launch); each waits before reading its predecessor's output.
     // With stage events requested, launches stay plainly ordered so each event
     // marks the end of its own stage.
     const bool pdl = !events;
-    auto dependent = [&](auto kern, unsigned int grid, unsigned int block) -> cudaError_t {
+    auto dependent = [&](auto kern, unsigned int grid, unsigned int block,
+                         size_t smem = 0) -> cudaError_t {
         cudaLaunchConfig_t cfg = {};
         cfg.gridDim = dim3(grid);
         cfg.blockDim = dim3(block);
-        cfg.dynamicSmemBytes = 0;
+        cfg.dynamicSmemBytes = smem;
         cfg.stream = st;
         cudaLaunchAttribute attr[1];
         attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
@@ -925,14 +1590,20 @@ int launch_all(const Params &P, unsigned int grid1, cudaStream_t st, void *const
     };
     stats_kernel<DT><<<grid1, NTHREADS, SMEM_BYTES, st>>>(P);
     mark(0);
+    if constexpr (FILT) {
+        if (dependent(filter_kernel<DT>, gridf, FTH, FILT_SMEM) != cudaSuccess)
+            return SPEC_ECUDA;
+        if (events && events[1])
+            cudaEventRecord(reinterpret_cast<cudaEvent_t>(events[1]), st);
+    }
     const unsigned int gs = (unsigned int)((P.B + SCAN_WARPS - 1) / SCAN_WARPS);
-    if (dependent(scan_kernel<DT>, gs, SCAN_WARPS * 32) != cudaSuccess)
+    if (dependent(scan_kernel<DT, FILT>, gs, SCAN_WARPS * 32) != cudaSuccess)
         return SPEC_ECUDA;
     mark(1);
-    if (dependent(draw_kernel<DT>, (unsigned int)P.DS * (unsigned int)P.B, NT) != cudaSuccess)
+    if (dependent(draw_kernel<DT, FILT>, (unsigned int)P.DS * (unsigned int)P.B, NT) != cudaSuccess)
         return SPEC_ECUDA;
     mark(2);
-    if (dependent(final_kernel<DT>, gs, SCAN_WARPS * 32) != cudaSuccess)
+    if (dependent(final_kernel<DT, FILT>, gs, SCAN_WARPS * 32) != cudaSuccess)
         return SPEC_ECUDA;
     mark(3);
     if (cudaPeekAtLastError() != cudaSuccess) {
@@ -945,7 +1616,8 @@ int launch_all(const Params &P, unsigned int grid1, cudaStream_t st, void *const
 int launch(const void *target, const void *draft, const int32_t *tokens, const float *ua,
            const float *ur, const float *temp, int32_t *out_tokens, int32_t *out_n,
            float *out_probs, int32_t B, int32_t k, int32_t V, int32_t dtype, void *ws,
-           size_t ws_size, void *stream, void *const *events = nullptr)
+           size_t ws_size, void *stream, void *const *events = nullptr, bool filtered = false,
+           const int32_t *top_k = nullptr, const float *top_p = nullptr)
 {
     if (!sizes_ok(B, k, V, dtype))
         return SPEC_EINVAL;
@@ -957,7 +1629,8 @@ int launch(const void *target, const void *draft, const int32_t *tokens, const f
         (reinterpret_cast<uintptr_t>(ws) & 15) || (reinterpret_cast<uintptr_t>(tokens) & 3) ||
         (reinterpret_cast<uintptr_t>(ua) & 3) || (reinterpret_cast<uintptr_t>(ur) & 3) ||
         (reinterpret_cast<uintptr_t>(temp) & 3) || (reinterpret_cast<uintptr_t>(out_tokens) & 3) ||
-        (reinterpret_cast<uintptr_t>(out_n) & 3) || (reinterpret_cast<uintptr_t>(out_probs) & 3))
+        (reinterpret_cast<uintptr_t>(out_n) & 3) || (reinterpret_cast<uintptr_t>(out_probs) & 3) ||
+        (reinterpret_cast<uintptr_t>(top_k) & 3) || (reinterpret_cast<uintptr_t>(top_p) & 3))
         return SPEC_EINVAL;
     const WsLayout lay = ws_layout(B, k, V, dtype);
     if (ws_size < lay.total)
@@ -987,6 +1660,22 @@ int launch(const void *target, const void *draft, const int32_t *tokens, const f
         dc.ctas_per_sm[di] = n > 0 ? n : 1;
         dc.attr_set[di] = true;
     }
+    unsigned int gridf = 0;
+    if (filtered) {
+        if (!dc.filt_set[di]) {
+            const void *ff = (dtype == SPEC_F32) ? (const void *)filter_kernel<SPEC_F32>
+                                                 : (const void *)filter_kernel<SPEC_BF16>;
+            if (cudaFuncSetAttribute(ff, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     (int)FILT_SMEM) != cudaSuccess)
+                return SPEC_ECUDA;
+            dc.filt_set[di] = true;
+        }
+        // rows are read several times by one CTA: at most two rows per SM in
+        // flight (bf16) or one (fp32) keeps them all within L2
+        const size_t rows = (size_t)B * (2 * (size_t)k + 1);
+        const size_t cap = (size_t)dc.sms * ((dtype == SPEC_F32) ? 1 : 2);
+        gridf = (unsigned int)(rows < cap ? rows : cap);
+    }
     const size_t resident = (size_t)dc.sms * dc.ctas_per_sm[di];
     const unsigned int grid1 = (unsigned int)(total < resident ? total : resident);
 
@@ -1006,6 +1695,9 @@ int launch(const void *target, const void *draft, const int32_t *tokens, const f
     P.jobs = reinterpret_cast<JobRec *>(w + lay.jobs);
     P.chunks = reinterpret_cast<float *>(w + lay.chunks);
     P.rec = reinterpret_cast<float2 *>(w + lay.rec);
+    P.top_k = top_k;
+    P.top_p = top_p;
+    P.filt = reinterpret_cast<FiltRec *>(w + lay.filt);
     P.NCH = (int)lay.NCH;
     P.B = B;
     P.k = k;
@@ -1021,8 +1713,11 @@ int launch(const void *target, const void *draft, const int32_t *tokens, const f
     P.draft_bytes = (unsigned long long)B * k * (unsigned long long)V * es;
 
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-    return (dtype == SPEC_F32) ? launch_all<SPEC_F32>(P, grid1, st, events)
-                               : launch_all<SPEC_BF16>(P, grid1, st, events);
+    if (filtered)
+        return (dtype == SPEC_F32) ? launch_all<SPEC_F32, true>(P, grid1, gridf, st, events)
+                                   : launch_all<SPEC_BF16, true>(P, grid1, gridf, st, events);
+    return (dtype == SPEC_F32) ? launch_all<SPEC_F32, false>(P, grid1, 0, st, events)
+                               : launch_all<SPEC_BF16, false>(P, grid1, 0, st, events);
 }
 
 }  // namespace
@@ -1084,6 +1779,33 @@ int32_t spec_verify(const void *target_logits, const void *draft_logits,
     return launch(target_logits, draft_logits, draft_tokens, u_accept, u_resample, temperature,
                   out_tokens, out_num_accepted, nullptr, B, k, V, dtype, workspace,
                   workspace_bytes, stream);
+}
+
+int32_t spec_verify_filtered(const void *target_logits, const void *draft_logits,
+                             const int32_t *draft_tokens, const float *u_accept,
+                             const float *u_resample, const float *temperature,
+                             const int32_t *top_k, const float *top_p,
+                             int32_t *out_tokens, int32_t *out_num_accepted, float *out_probs,
+                             int32_t B, int32_t k, int32_t V, int32_t dtype,
+                             void *workspace, size_t workspace_bytes, void *stream)
+{
+    return launch(target_logits, draft_logits, draft_tokens, u_accept, u_resample, temperature,
+                  out_tokens, out_num_accepted, out_probs, B, k, V, dtype, workspace,
+                  workspace_bytes, stream, nullptr, true, top_k, top_p);
+}
+
+int32_t spec_verify_filtered_timed(const void *target_logits, const void *draft_logits,
+                                   const int32_t *draft_tokens, const float *u_accept,
+                                   const float *u_resample, const float *temperature,
+                                   const int32_t *top_k, const float *top_p,
+                                   int32_t *out_tokens, int32_t *out_num_accepted,
+                                   int32_t B, int32_t k, int32_t V, int32_t dtype,
+                                   void *workspace, size_t workspace_bytes, void *stream,
+                                   void *const *stage_events)
+{
+    return launch(target_logits, draft_logits, draft_tokens, u_accept, u_resample, temperature,
+                  out_tokens, out_num_accepted, nullptr, B, k, V, dtype, workspace,
+                  workspace_bytes, stream, stage_events, true, top_k, top_p);
 }
 
 int32_t spec_verify_probs(const void *target_logits, const void *draft_logits,

@@ -66,9 +66,10 @@ def test_workspace_size(lib, B, k, V, dt, ok):
     up = lambda x, a: -(-x // a) * a
     nch = -(-(V * (4 if dt == 0 else 2)) // 4096)  # 4 KB chunks per row
     jobs = up(256 + B * (2 * k + 1) * nss * 16, 256)
-    chunks = up(jobs + 64 * B, 256)
+    chunks = up(jobs + 80 * B, 256)
     rec = up(chunks + B * up(ds * 4 * 8, 32) * 4, 256)
-    assert n == rec + B * nch * 8
+    filt = up(rec + B * nch * 8, 256)
+    assert n == filt + B * (2 * k + 1) * 16
 
 
 def _call(lib, ptrs, B=1, k=1, V=8, dt=0, wsb=1 << 20):

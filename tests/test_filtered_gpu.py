@@ -1,0 +1,174 @@
+"""Parity of top-k / top-p filtered verification (spec_verify_filtered) with
+the fp64 oracle (oracle.verify_filtered).
+
+Integer outputs must equal the oracle's.  Exempt, and counted: a sequence
+whose oracle decision had its uniform within BAND of a threshold or draw-cell
+boundary (as for the unfiltered path), or whose top-p cut had a running mass
+within BAND of P times the top-k mass (fp32 masses may cut there differently).
+Draft tokens are drawn from the filtered draft distribution, as a draft model
+sampling with the same parameters would.
+"""
+import os
+
+import numpy as np
+import pytest
+
+torch = pytest.importorskip("torch")
+pytestmark = pytest.mark.gpu
+
+import oracle  # noqa: E402
+import speculative_decoding_verification_65_gb300 as sv  # noqa: E402
+from speculative_decoding_verification_65_gb300 import synth  # noqa: E402
+from tests.parity_util import compare  # noqa: E402
+
+BAND = 1e-5
+NTHREADS = os.cpu_count() or 1
+
+
+def filtered_tokens(case, top_k, top_p, seed):
+    """Draft tokens g_i ~ the filtered q_i (greedy sequences: the draft argmax)."""
+    rng = np.random.default_rng(seed)
+    d = synth.decode(case.draft)
+    g = np.empty((case.B, case.k), np.int32)
+    for b in range(case.B):
+        T = float(case.temperature[b])
+        for i in range(case.k):
+            if T == 0.0:
+                g[b, i] = int(np.argmax(d[b, i]))
+                continue
+            K = 0 if top_k is None else int(top_k[b])
+            P = 1.0 if top_p is None else float(top_p[b])
+            q, _, _ = oracle.filtered_softmax(d[b, i].astype(np.float64), T, max(K, 0),
+                                              P if P > 0 else 1.0)
+            g[b, i] = int(rng.choice(case.V, p=q / q.sum()))
+    return g
+
+
+def run_gpu(case, tokens, top_k, top_p, want_probs=False, ws=None):
+    d = sv.to_device(case)
+    d["tokens"] = torch.from_numpy(tokens).cuda()
+    tk = None if top_k is None else torch.from_numpy(np.asarray(top_k, np.int32)).cuda()
+    tp = None if top_p is None else torch.from_numpy(np.asarray(top_p, np.float32)).cuda()
+    out = sv.spec_verify_filtered(**d, top_k=tk, top_p=tp, want_probs=want_probs, ws=ws)
+    torch.cuda.synchronize()
+    return tuple(x.cpu().numpy() for x in out)
+
+
+def check(case, tokens, top_k, top_p):
+    gt, gn = run_gpu(case, tokens, top_k, top_p)
+    rt, rn, tr = oracle.verify_filtered(case.target, case.draft, tokens, case.u_accept,
+                                        case.u_resample, case.temperature, top_k, top_p,
+                                        nthreads=NTHREADS)
+    near = np.nan_to_num(tr[:, case.k + 3], nan=1.0) < BAND
+    keep = np.nonzero(~near)[0]
+    sub = case.subset(keep)
+    sub.tokens = tokens[keep]
+    rep = compare(sub, gt[keep], gn[keep], rt[keep], rn[keep], tr[keep][:, :case.k + 3])
+    exempt = rep["exempt"] + int(np.sum(near & ((gn != rn) | np.any(gt != rt, axis=1))))
+    draws = max(1, int(np.sum(rn >= 0)))
+    assert exempt <= max(1, 0.02 * draws), (exempt, draws)
+    return gn, rn
+
+
+PARAMS = {
+    "topk50": lambda B, rng: (np.full(B, 50, np.int32), None),
+    "topp0.9": lambda B, rng: (None, np.full(B, 0.9, np.float32)),
+    "both": lambda B, rng: (np.full(B, 20, np.int32), np.full(B, 0.8, np.float32)),
+    "mixed": lambda B, rng: (rng.choice([0, 1, 5, 50, 1000], B).astype(np.int32),
+                             rng.choice([1.0, 0.5, 0.9, 0.99], B).astype(np.float32)),
+}
+
+
+@pytest.mark.parametrize("params", list(PARAMS))
+@pytest.mark.parametrize("cfg,B", [(2, 12), (3, 8), (4, 8), (5, 24)])
+def test_workloads(cfg, B, params):
+    case = synth.make_config(cfg, B=B)
+    top_k, top_p = PARAMS[params](B, np.random.default_rng(cfg))
+    tokens = filtered_tokens(case, top_k, top_p, seed=cfg + 17)
+    gn, rn = check(case, tokens, top_k, top_p)
+    assert np.all(rn[case.temperature > 0] >= 0)  # drawn from the filtered q: no errors
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_filters_off_equal_spec_verify(dtype):
+    case = synth.gauss_case(B=16, k=4, V=5000, dtype=dtype, seed=3, T=(0.0, 0.7, 1.2))
+    d = sv.to_device(case)
+    t0, n0 = sv.spec_verify(**d)
+    zk = torch.zeros(case.B, dtype=torch.int32, device="cuda")
+    op = torch.ones(case.B, dtype=torch.float32, device="cuda")
+    for tk, tp in ((None, None), (zk, op), (zk + case.V, op * 2)):
+        t1, n1 = sv.spec_verify_filtered(**d, top_k=tk, top_p=tp)
+        torch.cuda.synchronize()
+        assert torch.equal(t0, t1) and torch.equal(n0, n1)
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_wide_nucleus_and_massive_ties(dtype):
+    # flat rows: the top-p end sits deep in the ranking (several narrowing
+    # passes); integer-valued logits: one key value holds thousands of ties,
+    # past the sort buffer, so the index-order tie pass decides
+    rng = np.random.default_rng(11)
+    B, k, V = 6, 2, 40000
+    case = synth.gauss_case(B=B, k=k, V=V, dtype=dtype, seed=12, T=(1.0,), sigma_d=0.05,
+                            sigma_n=0.02)
+    top_p = np.full(B, 0.97, np.float32)
+    tokens = filtered_tokens(case, None, top_p, seed=5)
+    check(case, tokens, None, top_p)
+    ints = rng.integers(-2, 3, size=(B, k + 1, V)).astype(np.float32)
+    intd = rng.integers(-2, 3, size=(B, k, V)).astype(np.float32)
+    if dtype == "bf16":
+        ints, intd = synth.f32_to_bf16_bits(ints), synth.f32_to_bf16_bits(intd)
+    case2 = synth.Case(ints, intd, case.tokens, case.u_accept, case.u_resample,
+                       case.temperature, dtype)
+    top_k = np.array([9000, 12000, 30000, 100, 1, 20000], np.int32)
+    tokens2 = filtered_tokens(case2, top_k, None, seed=6)
+    check(case2, tokens2, top_k, None)
+    check(case2, tokens2, top_k, np.full(B, 0.6, np.float32))
+
+
+def test_bad_parameters_fail_the_sequence():
+    case = synth.gauss_case(B=5, k=3, V=3000, seed=4, T=(1.0,))
+    top_k = np.array([0, -1, 0, 0, 0], np.int32)
+    top_p = np.array([1.0, 1.0, np.nan, 0.0, -0.5], np.float32)
+    case.temperature[:] = np.array([1.0, 0.0, 1.0, 1.0, 0.0], np.float32)
+    gt, gn = run_gpu(case, case.tokens, top_k, top_p)
+    rt, rn, _ = oracle.verify_filtered(case.target, case.draft, case.tokens, case.u_accept,
+                                       case.u_resample, case.temperature, top_k, top_p)
+    assert np.array_equal(gn, rn) and np.array_equal(gt, rt)
+    assert np.all(gn[1:] == -1)
+
+
+def test_filtered_intermediates_within_tolerance():
+    case = synth.make_config(5, B=12)
+    top_k = np.full(case.B, 40, np.int32)
+    top_p = np.full(case.B, 0.9, np.float32)
+    tokens = filtered_tokens(case, top_k, top_p, seed=8)
+    _, _, probs = run_gpu(case, tokens, top_k, top_p, want_probs=True)
+    d = synth.decode(case.target), synth.decode(case.draft)
+    for b in range(case.B):
+        T = float(case.temperature[b])
+        for i in range(case.k):
+            p, _, mp = oracle.filtered_softmax(d[0][b, i].astype(np.float64), T, 40, 0.9)
+            q, _, mq = oracle.filtered_softmax(d[1][b, i].astype(np.float64), T, 40, 0.9)
+            if min(mp, mq) < BAND:
+                continue
+            g = tokens[b, i]
+            for got, want in ((probs[b, i, 0], p[g]), (probs[b, i, 1], q[g])):
+                if want == 0.0:
+                    assert got == 0.0
+                else:
+                    assert abs(got - want) <= 1e-5 * want, (b, i, got, want)
+
+
+def test_deterministic_with_garbage_workspace():
+    case = synth.make_config(3, B=8)
+    top_k = np.full(case.B, 30, np.int32)
+    top_p = np.full(case.B, 0.85, np.float32)
+    tokens = filtered_tokens(case, top_k, top_p, seed=9)
+    need = sv.spec_verify_workspace_size(case.B, case.k, case.V, sv.SPEC_BF16)
+    ws = torch.randint(0, 256, (need,), dtype=torch.uint8, device="cuda")
+    ws[:256] = 0
+    a = run_gpu(case, tokens, top_k, top_p, ws=ws)
+    b = run_gpu(case, tokens, top_k, top_p, ws=ws)
+    assert all(np.array_equal(x, y) for x, y in zip(a, b))
+    assert sv.spec_verify_read_status(ws) == sv.SPEC_DEV_OK
