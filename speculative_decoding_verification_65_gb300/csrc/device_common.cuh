@@ -20,7 +20,8 @@ constexpr unsigned long long WAIT_NS = 2000000000ull;  // 2 s bound on any wait
 // First 256 bytes of every workspace: the device status word (SPEC_DEV_*).
 struct WsHeader {
     int status;
-    unsigned int pad[63];
+    unsigned int next_item;  // row counter of the filter kernel (zeroed by the first kernel)
+    unsigned int pad[62];
 };
 static_assert(sizeof(WsHeader) == 256, "header is 256 bytes");
 

@@ -278,6 +278,8 @@ __global__ void __launch_bounds__(NTHREADS, 2) stats_kernel(const Params P)
     constexpr int SEG = TILE_BYTES / L::ES;
 
     if (tid == 0) {
+        if (blockIdx.x == 0)
+            P.hdr->next_item = 0u;  // the filter kernel's row counter (it runs after this grid)
         for (int s = 0; s < STAGES; ++s) {
             mbar_init(&S.full[s], 1);
             mbar_init(&S.empty[s], NCW);
@@ -470,23 +472,48 @@ __global__ void __launch_bounds__(NTHREADS, 2) stats_kernel(const Params P)
 // index asc) and the end is read off the sorted list; if a single key value
 // holds more ties than that, a pass in index order counts them instead.
 
-constexpr int FTH = 512;         // filter threads
+constexpr int FTH = 256;         // filter threads
 constexpr int FBINS = 16;        // buckets per pass (4-bit digits)
-constexpr int FCAP = 4096;       // tokens finished by a sort in shared memory
-constexpr int FUNR = 4;          // 16-byte vectors per thread in flight in a row pass
+constexpr int WBINS = 64;        // half-bit distance bins of the one-pass window
+static_assert(WBINS == 64, "the window statistics give each lane of a warp two bins");
+constexpr int FCAP = 1024;       // tokens finished by a sort in shared memory
+constexpr int FSLOTS = 4;        // ring slots of a row pass
+constexpr int FTILE = 16384;     // bytes of a row per slot
+constexpr int FSLOT_BYTES = FTILE + 128;  // room for a misaligned head/tail
+constexpr int FVPT = FTILE / (16 * 256);  // 16-byte vectors per thread per tile
 constexpr float FIX = 1099511627776.0f;  // 2^40
 
+struct FiltTile {
+    int e0, e1, phase0, ncopied;
+};
+
 struct FiltSmem {
-    union {
+    uint8_t ring[FSLOTS][FSLOT_BYTES];  // a row pass streams through these
+    unsigned long long fbar[FSLOTS];
+    FiltTile tile[FSLOTS];
+    int waitok;
+    union __align__(16) {  // 16-byte aligned: the histogram is zeroed with uint4 stores
         struct {
-            unsigned int cnt[FBINS][FTH];
-            unsigned long long mass[FBINS][FTH];
-        } h;
+            struct {
+                unsigned long long key[FCAP];  // (key << 32) | ~index: descending = the ranking
+                unsigned long long mass[FCAP];
+            } c;  // gathered tokens (any order), sorted in place by bitonic
+            struct {
+                unsigned long long key[FCAP];
+                unsigned long long mass[FCAP];
+            } r;  // rank placement's output, or the window's second buffer
+        } cr;
         struct {
-            unsigned long long key[FCAP];   // (key << 32) | ~index: descending = the ranking
-            unsigned long long mass[FCAP];
-        } c;
+            unsigned int cnt[4][FBINS][32];  // a column per lane: no two lanes of a
+            unsigned long long mass[4][FBINS][32];  // warp add to one word (warps w, w+4 share)
+        } h;  // the general case's histogram (not live while tokens are gathered)
     } u;
+    unsigned int ncand;                 // tokens gathered so far
+    unsigned int fh_cnt[WBINS];         // window histogram: tokens per half-bit bin
+    unsigned long long fh_mass[WBINS];  // and their masses (integer atomics)
+    int wnb;                            // window bin limit / bin of the cut
+    unsigned int wcum;                  // tokens through the cut's bin
+    int whalf;                          // last bin holding at most FCAP / 2 tokens through it
     unsigned int bcnt[FBINS];
     unsigned long long bmass[FBINS];
     unsigned int wcnt[FTH / 32];
@@ -498,10 +525,26 @@ struct FiltSmem {
     unsigned long long acc;  // scratch sum
 };
 constexpr size_t FILT_SMEM = sizeof(FiltSmem);
+static_assert(FVPT * 16 * FTH == FTILE, "a filter tile splits evenly over the threads");
+static_assert(FTH == 16 * FBINS && FTH / 32 == 8, "the histogram reduction's thread map");
+static_assert(offsetof(FiltSmem, u) % 16 == 0 && sizeof(FiltSmem::u) % 16 == 0,
+              "the sort / histogram union takes uint4 stores");
 
 __device__ __forceinline__ unsigned long long fixmass(float x, float m, float c)
 {
     return __float2ull_rn(ex2((x - m) * c) * FIX);
+}
+
+// A slot in the sort buffer for every lane with `want`, one shared atomic per
+// warp; the whole warp must call it.
+__device__ __forceinline__ unsigned int warp_slot(bool want, unsigned int *counter, int lane)
+{
+    const unsigned int mask = __ballot_sync(0xffffffffu, want);
+    unsigned int base = 0u;
+    if (mask && lane == __ffs(mask) - 1)
+        base = atomicAdd(counter, (unsigned int)__popc(mask));
+    base = __shfl_sync(0xffffffffu, base, mask ? __ffs(mask) - 1 : 0);
+    return base + (unsigned int)__popc(mask & ((1u << lane) - 1u));
 }
 
 __device__ __forceinline__ unsigned long long sortkey(unsigned int key, int idx)
@@ -547,12 +590,32 @@ __global__ void __launch_bounds__(FTH, 2) filter_kernel(const Params P)
     FiltSmem &S = *reinterpret_cast<FiltSmem *>(fsm_raw);
     const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
     const int V = P.V;
-    const int nvec = (V + VEC - 1) / VEC;
     const int items = P.B * P.rows;
+    if (t == 0) {
+        for (int q = 0; q < FSLOTS; ++q)
+            mbar_init(&S.fbar[q], 1);
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+    }
+    __syncthreads();
+    unsigned int par = 0u;  // completed-phase parity of each ring slot (same in every thread)
+    bool failed = false;    // a bulk copy never landed: stop this CTA
     allow_next_kernel();
     wait_previous_kernel();  // partials come from the statistics kernel
 
-    for (int item = blockIdx.x; item < items; item += gridDim.x) {
+    // rows are handed out one at a time (row cost varies: a few take the
+    // radix search): each CTA's first row is its index, the next come from
+    // the header counter, which the statistics kernel zeroed
+    auto next_item = [&]() -> int {
+        __syncthreads();
+        if (t == 0)
+            S.found = (int)gridDim.x + (int)atomicAdd(&P.hdr->next_item, 1u);
+        __syncthreads();
+        const int nx = S.found;
+        __syncthreads();
+        return nx;
+    };
+    for (int item = blockIdx.x; item < items && !failed; item = next_item()) {
         const int b = item / P.rows, rsq = item - b * P.rows;
         const bool is_target = rsq <= P.k;
         const void *arr = is_target ? P.target : P.draft;
@@ -613,116 +676,171 @@ __global__ void __launch_bounds__(FTH, 2) filter_kernel(const Params P)
             continue;
         }
 
-        // Row passes keep FUNR 16-byte vectors per thread in flight.  The
-        // unordered pass gives thread t the vectors t*FUNR + i*FTH*FUNR + u;
-        // the ordered one, round by round, the FUNR consecutive vectors after
-        // those of thread t-1, so thread order is index order.
-        auto load_vecs = [&](int v0, uint4 (&r)[FUNR]) {
+        // A row pass streams the row through the ring: thread 0 keeps up to
+        // FSLOTS 16 KB bulk copies in flight; every thread reads its FVPT
+        // vectors of each tile from shared memory (thread t: vectors
+        // t + q * FTH of the tile).  Waits are decided by thread 0 and shared,
+        // so every thread takes the same path; a copy that never lands
+        // (bounded wait) stops the CTA with SPEC_DEV_WAIT_TIMEOUT.
+        constexpr int TE = FTILE / L::ES;  // elements per tile
+        const int ntiles = (V + TE - 1) / TE;
+        const unsigned long long arr_bytes = is_target ? P.target_bytes : P.draft_bytes;
+        auto issue = [&](int i) {  // thread 0: tile i into slot i % FSLOTS
+            const int q = i % FSLOTS;
+            const int e0 = i * TE, e1 = min(V, e0 + TE);
+            const unsigned long long start = ((unsigned long long)row * V + e0) * L::ES;
+            const unsigned long long end = ((unsigned long long)row * V + e1) * L::ES;
+            const unsigned long long a0 = start & ~15ull;
+            unsigned long long a1 = (end + 15) & ~15ull;
+            if (a1 > (arr_bytes & ~15ull))
+                a1 = arr_bytes & ~15ull;
+            const uint32_t bytes = (a1 > a0) ? (uint32_t)(a1 - a0) : 0u;
+            S.tile[q].e0 = e0;
+            S.tile[q].e1 = e1;
+            S.tile[q].phase0 = (int)(start - a0);
+            S.tile[q].ncopied = (int)bytes;
+            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+            if (bytes) {
+                mbar_arrive_expect_tx(&S.fbar[q], bytes);
+                bulk_copy_g2s(S.ring[q], reinterpret_cast<const uint8_t *>(arr) + a0, bytes,
+                              &S.fbar[q]);
+            } else {
+                mbar_arrive(&S.fbar[q]);
+            }
+        };
+        // fn(raw[FVPT], vt0): the thread's vectors vt0 + q * FTH of one tile
+        // after(raw, vt0, e0, e1), if given, runs in every thread once the tile
+        // is done and its slot refilled (the thread's vectors are still in raw)
+        auto stream_row_then = [&](auto fn, auto after) {
+            if (failed)
+                return;
+            if (t == 0)
+                for (int i = 0; i < min(FSLOTS, ntiles); ++i)
+                    issue(i);
+            for (int i = 0; i < ntiles; ++i) {
+                const int q = i % FSLOTS;
+                const uint32_t pq = (par >> q) & 1u;
+                if (t == 0)
+                    S.waitok = mbar_wait(&S.fbar[q], pq) ? 1 : 0;
+                __syncthreads();
+                if (!S.waitok) {
+                    failed = true;
+                    if (t == 0) {
+                        atomicExch(&P.hdr->status, SPEC_DEV_WAIT_TIMEOUT);
+                        // let the other copies in flight land (bounded)
+                        for (int i2 = i + 1; i2 < min(i + FSLOTS, ntiles); ++i2)
+                            (void)mbar_wait(&S.fbar[i2 % FSLOTS], (par >> (i2 % FSLOTS)) & 1u);
+                    }
+                    __syncthreads();
+                    return;
+                }
+                (void)mbar_try_wait(&S.fbar[q], pq);  // acquire the landed bytes
+                const FiltTile ti = S.tile[q];
+                const Seg g = make_seg<DT>(S.ring[q], arr, row, V, ti.e0, ti.e1, ti.phase0,
+                                           ti.ncopied);
+                const int vt0 = ti.e0 / VEC;
+                uint4 raw[FVPT];
+                if (g.fast && ti.e1 - ti.e0 == TE) {
 #pragma unroll
-            for (int u = 0; u < FUNR; ++u)
-                r[u] = (v0 + u < nvec) ? row_vec<DT>(arr, row, v0 + u, V)
-                                       : neg_inf_vec(L::NEG_INF_WORD);
+                    for (int u = 0; u < FVPT; ++u)
+                        raw[u] = ld_shared_v4(S.ring[q] + (size_t)(t + u * FTH) * 16);
+                } else {
+#pragma unroll
+                    for (int u = 0; u < FVPT; ++u)
+                        raw[u] = seg_vec<DT>(g, vt0 + t + u * FTH);
+                }
+                fn(raw, vt0);
+                __syncthreads();  // every thread is done with slot q
+                par ^= 1u << q;
+                if (t == 0 && i + FSLOTS < ntiles)
+                    issue(i + FSLOTS);
+                after(raw, vt0, ti.e0, ti.e1);
+            }
+        };
+        auto stream_row = [&](auto fn) {
+            stream_row_then(fn, [](const uint4 (&)[FVPT], int, int, int) {});
         };
         auto member = [](unsigned int key, int idx, unsigned int kk, int ik) {
             return key > kk || (key == kk && idx <= ik);
         };
         // histogram of bin_of(x, key, idx) (-1: not counted): counts and masses
         auto hist = [&](auto bin_of, auto vskip) {
+            for (int i = t; i < (int)(sizeof(S.u.h) / 16); i += FTH)
+                reinterpret_cast<uint4 *>(&S.u.h)[i] = make_uint4(0u, 0u, 0u, 0u);
+            __syncthreads();
+            unsigned int *hc = &S.u.h.cnt[warp & 3][0][lane];
+            unsigned long long *hm = &S.u.h.mass[warp & 3][0][lane];
+            stream_row([&](const uint4 (&r)[FVPT], int vt0) {
 #pragma unroll
-            for (int bb = 0; bb < FBINS; ++bb) {
-                S.u.h.cnt[bb][t] = 0u;
-                S.u.h.mass[bb][t] = 0ull;
-            }
-            for (int v0 = t * FUNR; v0 < nvec; v0 += FTH * FUNR) {
-                uint4 r[FUNR];
-                load_vecs(v0, r);
-#pragma unroll
-                for (int u = 0; u < FUNR; ++u) {
+                for (int u = 0; u < FVPT; ++u) {
                     if (vskip(r[u]))
                         continue;  // no token of this vector can count
                     float x[VEC];
                     L::unpack(r[u], x);
 #pragma unroll
                     for (int j = 0; j < VEC; ++j) {
-                        const int idx = (v0 + u) * VEC + j;
+                        const int idx = (vt0 + t + u * FTH) * VEC + j;
                         const int bin = (idx < V) ? bin_of(x[j], key_of<DT>(x[j]), idx) : -1;
                         if (bin >= 0) {
-                            S.u.h.cnt[bin][t] += 1u;
-                            S.u.h.mass[bin][t] += fixmass(x[j], m, c);
+                            atomicAdd(hc + bin * 32, 1u);
+                            atomicAdd(hm + bin * 32, fixmass(x[j], m, c));
                         }
                     }
                 }
-            }
+            });
             __syncthreads();
-            // fixed-order sums: warp w adds the columns of buckets w, w+16, ...
-            for (int bin = warp; bin < FBINS; bin += FTH / 32) {
+            {  // bin t / 16: sixteen threads sum its 128 columns
+                const int bb = t >> 4, part = t & 15;
                 unsigned int cs = 0u;
                 unsigned long long ms = 0ull;
-                for (int i = lane; i < FTH; i += 32) {
-                    cs += S.u.h.cnt[bin][i];
-                    ms += S.u.h.mass[bin][i];
+                for (int q = part; q < 128; q += 16) {
+                    cs += S.u.h.cnt[q >> 5][bb][q & 31];
+                    ms += S.u.h.mass[q >> 5][bb][q & 31];
                 }
 #pragma unroll
-                for (int o = 16; o > 0; o >>= 1) {
+                for (int o = 8; o > 0; o >>= 1) {
                     cs += __shfl_xor_sync(0xffffffffu, cs, o);
                     ms += __shfl_xor_sync(0xffffffffu, ms, o);
                 }
-                if (lane == 0) {
-                    S.bcnt[bin] = cs;
-                    S.bmass[bin] = ms;
+                if (part == 0) {
+                    S.bcnt[bb] = cs;
+                    S.bmass[bb] = ms;
                 }
             }
             __syncthreads();
         };
-        // the tokens with pred(x, key, idx), in index order, into the sort buffer
+        // the tokens with pred(x, key, idx) into the sort buffer, in no
+        // particular order (the sort key carries the index); returns how many
+        // there are, which may exceed FCAP (only the first FCAP are stored)
         auto gather = [&](auto pred, auto vskip) -> int {
-            unsigned int base = 0u;
-            for (int vb = 0; vb < nvec; vb += FTH * FUNR) {
-                const int v0 = vb + t * FUNR;
-                uint4 r[FUNR];
-                load_vecs(v0, r);
-                unsigned int n = 0u;
-                bool live[FUNR];
+            if (t == 0)
+                S.ncand = 0u;
+            __syncthreads();
+            stream_row([&](const uint4 (&r)[FVPT], int vt0) {
 #pragma unroll
-                for (int u = 0; u < FUNR; ++u) {
-                    live[u] = !vskip(r[u]);
-                    if (!live[u])
+                for (int u = 0; u < FVPT; ++u) {
+                    const bool live = !vskip(r[u]);
+                    if (!__any_sync(0xffffffffu, live))
                         continue;
                     float x[VEC];
                     L::unpack(r[u], x);
 #pragma unroll
                     for (int j = 0; j < VEC; ++j) {
-                        const int idx = (v0 + u) * VEC + j;
-                        n += (idx < V && pred(x[j], key_of<DT>(x[j]), idx)) ? 1u : 0u;
-                    }
-                }
-                unsigned int tot;
-                unsigned int pos = base + block_excl_scan(n, S, tot);
-                if (n) {
-#pragma unroll
-                    for (int u = 0; u < FUNR; ++u) {
-                        if (!live[u])
-                            continue;
-                        float x[VEC];
-                        L::unpack(r[u], x);
-#pragma unroll
-                        for (int j = 0; j < VEC; ++j) {
-                            const int idx = (v0 + u) * VEC + j;
-                            const unsigned int key = key_of<DT>(x[j]);
-                            if (idx < V && pred(x[j], key, idx)) {
-                                if (pos < (unsigned int)FCAP) {  // never past the buffer
-                                    S.u.c.key[pos] = sortkey(key, idx);
-                                    S.u.c.mass[pos] = fixmass(x[j], m, c);
-                                }
-                                ++pos;
-                            }
+                        const int idx = (vt0 + t + u * FTH) * VEC + j;
+                        const unsigned int key = key_of<DT>(x[j]);
+                        const bool take = live && idx < V && pred(x[j], key, idx);
+                        const unsigned int pos = warp_slot(take, &S.ncand, lane);
+                        if (take && pos < (unsigned int)FCAP) {  // never past the buffer
+                            S.u.cr.c.key[pos] = sortkey(key, idx);
+                            S.u.cr.c.mass[pos] = fixmass(x[j], m, c);
                         }
                     }
                 }
-                base += tot;
-            }
+            });
             __syncthreads();
-            return (int)(base < (unsigned int)FCAP ? base : (unsigned int)FCAP);
+            const int n = (int)S.ncand;
+            __syncthreads();
+            return n;
         };
         // bitonic sort of the first n gathered tokens, descending
         auto sort_desc = [&](int n) {
@@ -730,8 +848,8 @@ __global__ void __launch_bounds__(FTH, 2) filter_kernel(const Params P)
             while (p2 < n)
                 p2 <<= 1;
             for (int i = n + t; i < p2; i += FTH) {
-                S.u.c.key[i] = 0ull;
-                S.u.c.mass[i] = 0ull;
+                S.u.cr.c.key[i] = 0ull;
+                S.u.cr.c.mass[i] = 0ull;
             }
             __syncthreads();
             for (int kk = 2; kk <= p2; kk <<= 1) {
@@ -739,14 +857,14 @@ __global__ void __launch_bounds__(FTH, 2) filter_kernel(const Params P)
                     for (int i = t; i < p2; i += FTH) {
                         const int ixj = i ^ jj;
                         if (ixj > i) {
-                            const unsigned long long a = S.u.c.key[i], bq = S.u.c.key[ixj];
+                            const unsigned long long a = S.u.cr.c.key[i], bq = S.u.cr.c.key[ixj];
                             const bool desc = (i & kk) == 0;
                             if (desc ? (a < bq) : (a > bq)) {
-                                S.u.c.key[i] = bq;
-                                S.u.c.key[ixj] = a;
-                                const unsigned long long ma = S.u.c.mass[i];
-                                S.u.c.mass[i] = S.u.c.mass[ixj];
-                                S.u.c.mass[ixj] = ma;
+                                S.u.cr.c.key[i] = bq;
+                                S.u.cr.c.key[ixj] = a;
+                                const unsigned long long ma = S.u.cr.c.mass[i];
+                                S.u.cr.c.mass[i] = S.u.cr.c.mass[ixj];
+                                S.u.cr.c.mass[ixj] = ma;
                             }
                         }
                     }
@@ -754,12 +872,73 @@ __global__ void __launch_bounds__(FTH, 2) filter_kernel(const Params P)
                 }
             }
         };
+        // the sorted list: S.c after a bitonic sort, S.r after rank placement
+        unsigned long long *skey = S.u.cr.c.key, *smass = S.u.cr.c.mass;
+        // rank placement of n <= FCAP gathered tokens (keys are unique): the
+        // rank of a token is the number of larger keys; from one buffer into
+        // the other
+        auto rank_sort = [&](int n, unsigned long long *ikey, unsigned long long *imass,
+                             unsigned long long *okey_, unsigned long long *omass) {
+            constexpr int PER = FCAP / FTH;
+            unsigned long long mine[PER];
+            int rk[PER];
+#pragma unroll
+            for (int q = 0; q < PER; ++q) {
+                const int i = t + q * FTH;
+                mine[q] = (i < n) ? ikey[i] : 0ull;
+                rk[q] = 0;
+            }
+            for (int jj = 0; jj < n; ++jj) {
+                const unsigned long long kj = ikey[jj];
+#pragma unroll
+                for (int q = 0; q < PER; ++q)
+                    rk[q] += (kj > mine[q]) ? 1 : 0;
+            }
+            unsigned long long mm[PER];
+#pragma unroll
+            for (int q = 0; q < PER; ++q) {
+                const int i = t + q * FTH;
+                mm[q] = (i < n) ? imass[i] : 0ull;
+            }
+            __syncthreads();  // the output may overlap nothing the others still read
+#pragma unroll
+            for (int q = 0; q < PER; ++q) {
+                const int i = t + q * FTH;
+                if (i < n) {
+                    okey_[rk[q]] = mine[q];
+                    omass[rk[q]] = mm[q];
+                }
+            }
+            __syncthreads();
+            skey = okey_;
+            smass = omass;
+        };
+        // sort the n tokens gathered in S.c (from_r: in S.r) into descending order
+        auto sort_any = [&](int n, bool from_r = false) {
+            if (n <= FCAP / 2) {
+                if (from_r)
+                    rank_sort(n, S.u.cr.r.key, S.u.cr.r.mass, S.u.cr.c.key, S.u.cr.c.mass);
+                else
+                    rank_sort(n, S.u.cr.c.key, S.u.cr.c.mass, S.u.cr.r.key, S.u.cr.r.mass);
+            } else {
+                if (from_r) {
+                    for (int i = t; i < n; i += FTH) {
+                        S.u.cr.c.key[i] = S.u.cr.r.key[i];
+                        S.u.cr.c.mass[i] = S.u.cr.r.mass[i];
+                    }
+                    __syncthreads();
+                }
+                sort_desc(n);
+                skey = S.u.cr.c.key;
+                smass = S.u.cr.c.mass;
+            }
+        };
         // mass of the first r sorted tokens (fixed order)
         auto sorted_prefix_mass = [&](int r) -> unsigned long long {
             if (warp == 0) {
                 unsigned long long ms = 0ull;
                 for (int i = lane; i < r; i += 32)
-                    ms += S.u.c.mass[i];
+                    ms += smass[i];
 #pragma unroll
                 for (int o = 16; o > 0; o >>= 1)
                     ms += __shfl_xor_sync(0xffffffffu, ms, o);
@@ -780,7 +959,7 @@ __global__ void __launch_bounds__(FTH, 2) filter_kernel(const Params P)
                 int istar = -1;
                 for (int i0 = 0; i0 < n && istar < 0; i0 += 32) {
                     const int i = i0 + lane;
-                    unsigned long long x = (i < n) ? S.u.c.mass[i] : 0ull;
+                    unsigned long long x = (i < n) ? smass[i] : 0ull;
 #pragma unroll
                     for (int o = 1; o < 32; o <<= 1) {
                         const unsigned long long y = __shfl_up_sync(0xffffffffu, x, o);
@@ -811,7 +990,7 @@ __global__ void __launch_bounds__(FTH, 2) filter_kernel(const Params P)
             return i;
         };
         auto sorted_at = [&](int i, unsigned int &key, int &idx) {
-            const unsigned long long e = S.u.c.key[i];
+            const unsigned long long e = skey[i];
             key = (unsigned int)(e >> 32);
             idx = (int)(0xffffffffu - (unsigned int)(e & 0xffffffffu));
         };
@@ -822,33 +1001,27 @@ __global__ void __launch_bounds__(FTH, 2) filter_kernel(const Params P)
                 S.found = -1;
             __syncthreads();
             unsigned int base = 0u;
-            for (int vb = 0; vb < nvec; vb += FTH * FUNR) {
-                const int v0 = vb + t * FUNR;
-                uint4 r4[FUNR];
-                load_vecs(v0, r4);
-                unsigned int n = 0u;
+            stream_row([&](const uint4 (&r4)[FVPT], int vt0) {
+                // round u covers vectors vt0 + u*FTH .. +FTH-1: thread order is index order
 #pragma unroll
-                for (int u = 0; u < FUNR; ++u) {
+                for (int u = 0; u < FVPT; ++u) {
                     float x[VEC];
                     L::unpack(r4[u], x);
+                    const int v = vt0 + t + u * FTH;
+                    unsigned int n = 0u;
 #pragma unroll
                     for (int j = 0; j < VEC; ++j) {
-                        const int idx = (v0 + u) * VEC + j;
+                        const int idx = v * VEC + j;
                         const unsigned int key = key_of<DT>(x[j]);
                         n += (idx < V && key == kap && (!rk || member(key, idx, kK, iK))) ? 1u : 0u;
                     }
-                }
-                unsigned int tot;
-                const unsigned int ex = base + block_excl_scan(n, S, tot);
-                if (n && ex < r && r <= ex + n) {
-                    unsigned int cnt = ex;
-#pragma unroll
-                    for (int u = 0; u < FUNR; ++u) {
-                        float x[VEC];
-                        L::unpack(r4[u], x);
+                    unsigned int tot;
+                    const unsigned int ex = base + block_excl_scan(n, S, tot);
+                    if (n && ex < r && r <= ex + n) {
+                        unsigned int cnt = ex;
 #pragma unroll
                         for (int j = 0; j < VEC; ++j) {
-                            const int idx = (v0 + u) * VEC + j;
+                            const int idx = v * VEC + j;
                             const unsigned int key = key_of<DT>(x[j]);
                             if (idx < V && key == kap && (!rk || member(key, idx, kK, iK))) {
                                 if (++cnt == r)
@@ -856,14 +1029,17 @@ __global__ void __launch_bounds__(FTH, 2) filter_kernel(const Params P)
                             }
                         }
                     }
+                    base += tot;
                 }
-                base += tot;
-                __syncthreads();
-                if (S.found >= 0 || base >= r)
-                    break;
-            }
+            });
             __syncthreads();
             return S.found;
+        };
+        auto val_of_key = [&](unsigned int key) {
+            unsigned int bits = (key & 0x80000000u) ? (key & 0x7fffffffu) : ~key;
+            if (DT == SPEC_BF16)
+                bits &= 0xffff0000u;
+            return __uint_as_float(bits);
         };
         auto fix_of_key = [&](unsigned int key) {
             unsigned int bits = (key & 0x80000000u) ? (key & 0x7fffffffu) : ~key;
@@ -877,43 +1053,270 @@ __global__ void __launch_bounds__(FTH, 2) filter_kernel(const Params P)
         unsigned long long Zt = 0ull;
         auto vnone = [](const uint4 &) { return false; };
 
-        // ---- first pass: buckets by distance below the row maximum, one bit
-        // of probability each; tokens more than FBINS bits down are not
-        // counted (they join a kept set only through the general case).  A
-        // bucket set {0..b} is a prefix of the ranking.
-        auto dist_bin = [&](float x) {
-            const float dd = fmaxf((m - x) * c, 0.0f);
-            return (dd < (float)FBINS) ? (int)dd : -1;
-        };
-        // a vector whose maximum is more than FBINS + 1 bits below the row's
-        // holds no counted token (the spare bit absorbs rounding)
-        const float far = m - (float)(FBINS + 1) / c;
-        auto vfar = [&](const uint4 &r) { return !(L::vmax(r) > far) && !isnan(L::vmax(r)); };
-        hist([&](float x, unsigned int, int) { return dist_bin(x); }, vfar);
         const unsigned long long Ztot = Zrow;
-        int bsel = -1;
-        unsigned int ncum = 0u;
-        {
-            unsigned long long mcum = 0ull;
-            const unsigned long long target0 =
-                topk ? 0ull : (unsigned long long)((double)Pp * (double)Ztot);
-            for (int bb = 0; bb < FBINS; ++bb) {
-                ncum += S.bcnt[bb];
-                mcum += S.bmass[bb];
-                if (topk ? (ncum >= (unsigned int)K) : (mcum >= target0)) {
-                    bsel = bb;
-                    break;
+        const unsigned long long target0 =
+            topk ? 0ull : (unsigned long long)((double)Pp * (double)Ztot);
+        bool done = false;
+
+        // ---- one pass, an adaptive window.  A token's distance below the row
+        // maximum, in bits of probability, is dd = (m - x) * log2(e) / T; its
+        // window bin is floor(2 dd) (half-bit bins, WBINS of them: 32 bits,
+        // past which a token's fixed-point mass is zero).  The pass gathers
+        // every token whose bin is at most nbw into the sort buffer and counts
+        // them per bin (with their masses when top-p stands alone).  A bin set
+        // {0..b} is a prefix of the ranking, so once the counts (masses)
+        // through some bin b reach K (P times the row mass) the cut lies
+        // among the gathered tokens of bins 0..b, and the window narrows to
+        // that bin after each tile.  When the buffer overflows in a tile, the
+        // window narrows the same way (or, before the counts reach the cut,
+        // to the widest set holding at most FCAP / 2 tokens), the buffer is
+        // compacted to it, and the tile's own tokens -- of which some were not
+        // stored -- are gathered again.  A row whose cut the window cannot
+        // hold (cut bin too crowded, or deeper than 32 bits) takes the radix
+        // search.
+        auto wbin = [&](float x) {
+            const float dd = (m - x) * c;
+            return (dd < (float)(WBINS / 2)) ? (int)(dd * 2.0f) : WBINS;
+        };
+        auto wbin_of_entry = [&](unsigned long long e) { return wbin(val_of_key((unsigned int)(e >> 32))); };
+        auto idx_of_entry = [](unsigned long long e) {
+            return (int)(0xffffffffu - (unsigned int)(e & 0xffffffffull));
+        };
+        // the n entries of (ik, im) with keep(entry) into (ok, om), in
+        // order; returns how many (every thread)
+        auto compact = [&](const unsigned long long *ik, const unsigned long long *im, int n,
+                           unsigned long long *ok, unsigned long long *om, auto keep) -> int {
+            constexpr int PER = FCAP / FTH;
+            bool kp[PER];
+            unsigned int cnt = 0u;
+#pragma unroll
+            for (int q = 0; q < PER; ++q) {
+                const int i = t * PER + q;
+                kp[q] = i < n && keep(ik[i]);
+                cnt += kp[q] ? 1u : 0u;
+            }
+            unsigned int total;
+            unsigned int o = block_excl_scan(cnt, S, total);
+#pragma unroll
+            for (int q = 0; q < PER; ++q) {
+                const int i = t * PER + q;
+                if (kp[q]) {
+                    ok[o] = ik[i];
+                    om[o] = im[i];
+                    ++o;
                 }
             }
+            __syncthreads();
+            return (int)total;
+        };
+        const bool need_mass = !topk;
+        // The first window: fewer than Z * 2^D tokens lie within D bits (each
+        // weighs more than 2^-D of the maximum's), so D = log2(FCAP / Z) bits
+        // surely fit; 8 more bits usually still fit and usually hold the cut.
+        // If that window ends without the cut and never overflowed, the pass
+        // runs once more over all WBINS bins.
+        const float zrow = (float)((double)Zrow * (1.0 / 1099511627776.0));
+        const int Dg = (int)floorf(log2f((float)FCAP / (fmaxf(zrow, 1.0f) * 1.01f))) + 8;
+        int nbw0 = 2 * min(WBINS / 2, max(1, Dg)) - 1;
+        int nbw = nbw0;        // the window: bins 0..nbw
+        bool overflowed = false;
+        unsigned int last_nc = 0u;
+        unsigned long long *wk = S.u.cr.c.key, *wm = S.u.cr.c.mass;  // the buffer holding it
+        unsigned long long *xk = S.u.cr.r.key, *xm = S.u.cr.r.mass;  // the other one
+        const unsigned int kmin = topk ? (unsigned int)K : 1u;
+        // gather the thread's tokens of one tile within the window (counted
+        // in the histogram unless `recount` is false)
+        // Each lane marks its tokens of the tile inside the window (no warp
+        // collective per token: most vectors hold none), the warp reserves
+        // their slots with one scan and one atomic, and only marked tokens
+        // are written (and counted in the histogram unless `recount` is
+        // false).
+        auto gather_window = [&](const uint4 (&r)[FVPT], int vt0, bool recount) {
+            uint32_t tb[FVPT];
+            unsigned int cnt = 0u;
+#pragma unroll
+            for (int u = 0; u < FVPT; ++u) {
+                tb[u] = 0u;
+                if (wbin(L::vmax(r[u])) <= nbw) {  // else no token of the vector is in
+                    float x[VEC];
+                    L::unpack(r[u], x);
+#pragma unroll
+                    for (int j = 0; j < VEC; ++j) {
+                        const int idx = (vt0 + t + u * FTH) * VEC + j;
+                        if (idx < V && wbin(x[j]) <= nbw)
+                            tb[u] |= 1u << j;
+                    }
+                }
+                cnt += (unsigned int)__popc(tb[u]);
+            }
+            unsigned int incl = cnt;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const unsigned int y = __shfl_up_sync(0xffffffffu, incl, o);
+                if (lane >= o)
+                    incl += y;
+            }
+            const unsigned int wtot = __shfl_sync(0xffffffffu, incl, 31);
+            if (wtot == 0u)
+                return;  // (uniform over the warp)
+            unsigned int base = 0u;
+            if (lane == 31)
+                base = atomicAdd(&S.ncand, wtot);
+            unsigned int pos = __shfl_sync(0xffffffffu, base, 31) + incl - cnt;
+#pragma unroll
+            for (int u = 0; u < FVPT; ++u) {
+                if (tb[u] == 0u)
+                    continue;
+                float x[VEC];
+                L::unpack(r[u], x);
+#pragma unroll
+                for (int j = 0; j < VEC; ++j) {
+                    if (!((tb[u] >> j) & 1u))
+                        continue;
+                    const int idx = (vt0 + t + u * FTH) * VEC + j;
+                    const bool keep = pos < (unsigned int)FCAP;  // never past the buffer
+                    const unsigned long long e =
+                        (keep || (recount && need_mass)) ? fixmass(x[j], m, c) : 0ull;
+                    if (recount) {
+                        const int wb = wbin(x[j]);
+                        atomicAdd(&S.fh_cnt[wb], 1u);
+                        if (need_mass)
+                            atomicAdd(&S.fh_mass[wb], e);
+                    }
+                    if (keep) {
+                        wk[pos] = sortkey(key_of<DT>(x[j]), idx);
+                        wm[pos] = e;
+                    }
+                    ++pos;
+                }
+            }
+        };
+        // warp 0: over the bins 0..nbw, the first bin through which the
+        // counts (masses) reach the cut (S.wnb, -1 if none) with the count
+        // through it (S.wcum), and the last bin through which at most FCAP / 2
+        // tokens lie (S.whalf, -1 if none).  Lane l holds bins 2l and 2l + 1.
+        auto window_stats = [&]() {
+            const int b0 = 2 * lane, b1 = b0 + 1;
+            const unsigned int c0 = (b0 <= nbw) ? S.fh_cnt[b0] : 0u;
+            const unsigned int c1 = (b1 <= nbw) ? S.fh_cnt[b1] : 0u;
+            const unsigned long long m0 = (b0 <= nbw) ? S.fh_mass[b0] : 0ull;
+            const unsigned long long m1 = (b1 <= nbw) ? S.fh_mass[b1] : 0ull;
+            unsigned int ci = c0 + c1;
+            unsigned long long mi = m0 + m1;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const unsigned int y = __shfl_up_sync(0xffffffffu, ci, o);
+                const unsigned long long ym = __shfl_up_sync(0xffffffffu, mi, o);
+                if (lane >= o) {
+                    ci += y;
+                    mi += ym;
+                }
+            }
+            const unsigned int ce0 = ci - c1;  // through bin b0
+            const unsigned long long me0 = mi - m1;
+            auto hits = [&](unsigned int cc, unsigned long long mm) {
+                return topk ? cc >= (unsigned int)K : mm >= target0;
+            };
+            const bool h0 = b0 <= nbw && hits(ce0, me0);
+            const bool h1 = b1 <= nbw && hits(ci, mi);
+            const unsigned int hb = __ballot_sync(0xffffffffu, h0 || h1);
+            const unsigned int nh =
+                (unsigned int)__popc(__ballot_sync(0xffffffffu, b0 <= nbw && ce0 <= FCAP / 2)) +
+                (unsigned int)__popc(__ballot_sync(0xffffffffu, b1 <= nbw && ci <= FCAP / 2));
+            if (hb) {
+                const int L0 = __ffs(hb) - 1;
+                const bool first0 = __shfl_sync(0xffffffffu, h0, L0);
+                const unsigned int cb = __shfl_sync(0xffffffffu, first0 ? ce0 : ci, L0);
+                if (lane == 0) {
+                    S.wnb = first0 ? 2 * L0 : 2 * L0 + 1;
+                    S.wcum = cb;
+                }
+            } else if (lane == 0) {
+                S.wnb = -1;
+                S.wcum = 0u;
+            }
+            if (lane == 0)
+                S.whalf = (int)nh - 1;
+        };
+        int bk = -1, ncut = 0, n = 0;
+        for (;;) {
+            if (t < WBINS) {
+                S.fh_cnt[t] = 0u;
+                S.fh_mass[t] = 0ull;
+            }
+            if (t == 0)
+                S.ncand = 0u;
+            __syncthreads();
+            stream_row_then([&](const uint4 (&r)[FVPT], int vt0) { gather_window(r, vt0, true); },
+                            [&](const uint4 (&r)[FVPT], int vt0, int e0, int e1) {
+                const unsigned int nc = S.ncand;  // (read by every thread after the tile's barrier)
+                if (nc <= (unsigned int)FCAP) {
+                    // no overflow: once the tokens so far can hold the cut,
+                    // narrow the window to the cut's bin (the buffer may keep
+                    // tokens past it; they are dropped before the sort).
+                    // Checked each time the count has doubled: a few times
+                    // a row.
+                    if (nc < kmin || nc < 2u * last_nc)
+                        return;
+                    last_nc = nc;
+                    if (warp == 0)
+                        window_stats();
+                    __syncthreads();
+                    if (S.wnb >= 0 && S.wnb < nbw)
+                        nbw = S.wnb;
+                    __syncthreads();
+                    return;
+                }
+                overflowed = true;
+                if (warp == 0)
+                    window_stats();
+                __syncthreads();
+                if (t == 0)
+                    S.wnb = (S.wnb >= 0) ? ((S.wcum <= (unsigned int)FCAP) ? S.wnb : -1) : S.whalf;
+                __syncthreads();
+                nbw = S.wnb;
+                // keep the stored tokens of the narrower window, except this
+                // tile's, which are gathered again in full
+                const int nk = compact(wk, wm, FCAP, xk, xm, [&](unsigned long long en) {
+                    const int ix = idx_of_entry(en);
+                    return (ix < e0 || ix >= e1) && wbin_of_entry(en) <= nbw;
+                });
+                unsigned long long *tk_ = wk, *tm_ = wm;
+                wk = xk;
+                wm = xm;
+                xk = tk_;
+                xm = tm_;
+                if (t == 0)
+                    S.ncand = (unsigned int)nk;
+                __syncthreads();
+                gather_window(r, vt0, false);
+                __syncthreads();
+            });
+            __syncthreads();
+            n = (int)S.ncand;  // <= FCAP: every overflow was resolved
+            if (warp == 0)
+                window_stats();
+            __syncthreads();
+            bk = S.wnb;
+            ncut = (int)S.wcum;
+            __syncthreads();
+            if (bk >= 0 || failed || overflowed || nbw0 == WBINS - 1)
+                break;
+            nbw0 = nbw = WBINS - 1;  // the first window was too narrow: all bins
+            last_nc = 0u;
+            wk = S.u.cr.c.key;
+            wm = S.u.cr.c.mass;
+            xk = S.u.cr.r.key;
+            xm = S.u.cr.r.mass;
         }
-        if (bsel >= 0 && ncum <= (unsigned int)FCAP) {
-            // ---- the top of the ranking fits the sort buffer: read both cuts
-            // off the sorted list
-            const int n = gather([&](float x, unsigned int, int) {
-                const int bb = dist_bin(x);
-                return bb >= 0 && bb <= bsel;  // the same tokens the histogram counted
-            }, vfar);
-            sort_desc(n);
+        if (bk >= 0 && !failed) {
+            if (ncut < n) {  // sort only the bins through the cut's
+                n = compact(wk, wm, n, xk, xm,
+                            [&](unsigned long long en) { return wbin_of_entry(en) <= bk; });
+                wk = xk;
+                wm = xm;
+            }
+            sort_any(n, wk == S.u.cr.r.key);
             const int nk = topk ? K : n;
             const unsigned long long ZK = topk ? sorted_prefix_mass(K) : Ztot;
             int last = nk - 1;
@@ -925,7 +1328,9 @@ __global__ void __launch_bounds__(FTH, 2) filter_kernel(const Params P)
                 last = sorted_cut(nk, 0ull, target, Zt);
             }
             sorted_at(last, kap, iota);
-        } else {
+            done = true;
+        }
+        if (!done) {
             // ---- general case: radix search on the key, 4 bits per pass
             unsigned int kK = 0u;
             int iK = INT_MAX;
@@ -954,7 +1359,7 @@ __global__ void __launch_bounds__(FTH, 2) filter_kernel(const Params P)
                         const int n = gather([&](float, unsigned int key, int) {
                             return (key & pmask) == prefix;
                         }, vnone);
-                        sort_desc(n);
+                        sort_any(n);
                         ZK = amass + sorted_prefix_mass((int)r);
                         sorted_at((int)r - 1, kK, iK);
                         break;
@@ -998,7 +1403,7 @@ __global__ void __launch_bounds__(FTH, 2) filter_kernel(const Params P)
                         const int n = gather([&](float, unsigned int key, int idx) {
                             return (key & pmask) == prefix && (!topk || member(key, idx, kK, iK));
                         }, vnone);
-                        sort_desc(n);
+                        sort_any(n);
                         const int last = sorted_cut(n, amass, target, Zt);
                         sorted_at(last, kap, iota);
                         break;
@@ -1670,10 +2075,9 @@ int launch(const void *target, const void *draft, const int32_t *tokens, const f
                 return SPEC_ECUDA;
             dc.filt_set[di] = true;
         }
-        // rows are read several times by one CTA: at most two rows per SM in
-        // flight (bf16) or one (fp32) keeps them all within L2
+        // two rows per SM in flight (one CTA each, streaming through a ring)
         const size_t rows = (size_t)B * (2 * (size_t)k + 1);
-        const size_t cap = (size_t)dc.sms * ((dtype == SPEC_F32) ? 1 : 2);
+        const size_t cap = (size_t)dc.sms * 2;
         gridf = (unsigned int)(rows < cap ? rows : cap);
     }
     const size_t resident = (size_t)dc.sms * dc.ctas_per_sm[di];
