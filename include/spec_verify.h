@@ -160,8 +160,10 @@ int32_t spec_verify_probs(const void *target_logits, const void *draft_logits,
  *          Q = q~_i(g_i) (NaN for greedy and error sequences)
  * A draft token outside the draft's kept set (q~(g) = 0) is a sequence error.
  * Other arguments, the workspace (spec_verify_workspace_size) and errors as
- * spec_verify.  Five kernels run: statistics, filter (per row, a radix search
- * for the end of the kept set), accept scan, draw tiles, final search.
+ * spec_verify.  Five kernels run: statistics, filter (per row, the end of the
+ * kept set: one streaming pass over the row in the common case, a radix
+ * search over the order key otherwise), accept scan, draw tiles, final
+ * search.
  */
 int32_t spec_verify_filtered(const void *target_logits, const void *draft_logits,
                              const int32_t *draft_tokens, const float *u_accept,
