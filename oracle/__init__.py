@@ -227,3 +227,43 @@ def inverse_cdf(w, u: float):
     cell = np.empty(3, np.float64)
     x = lib.spec_ref_inverse_cdf(_ptr(w), w.size, float(u), _ptr(cell))
     return int(x), cell
+
+
+# ------------------------------------------------ LM-head-fused verification
+
+def _bf16_to_f64(bits) -> np.ndarray:
+    """bf16 bit patterns (uint16) to float64, exactly: a bf16 pattern is the
+    upper half of the float32 of the same value."""
+    b = np.ascontiguousarray(bits, dtype=np.uint16)
+    return (b.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+
+
+def lmhead_logits(hidden, lm_head) -> np.ndarray:
+    """Target logits of the LM head, t[..., x] = sum_j h[..., j] * W[x, j].
+
+    The verify step scores the k+1 positions with one target forward pass
+    ("Speculative Decoding and the Art of Fast LLM Inference", "The Algorithm,
+    Step by Step", the verify step), whose last layer is this product.
+    hidden: uint16 bf16 bits [..., d]; lm_head: uint16 bf16 bits [V, d].
+    Products of two bf16 values are exact in fp64; the sums are fp64 (numpy
+    matmul as the one library step)."""
+    h = _bf16_to_f64(hidden)
+    w = _bf16_to_f64(lm_head)
+    lead = h.shape[:-1]
+    t = h.reshape(-1, h.shape[-1]) @ w.T
+    return t.reshape(*lead, w.shape[0])
+
+
+def verify_lmhead(hidden, lm_head, draft, tokens, u_accept, u_resample, temperature,
+                  nthreads: int = 1, want_trace: bool = True):
+    """verify() with the target logits formed from the LM head:
+    target = lmhead_logits(hidden, lm_head) rounded once to fp32 (the GPU
+    accumulates in fp32; on inputs whose partial sums are all exact in fp32
+    the rounding changes nothing).  A bf16 draft is widened to fp32, exactly.
+    hidden [B, k+1, d], lm_head [V, d] (uint16 bf16 bits), draft [B, k, V]."""
+    t = lmhead_logits(hidden, lm_head).astype(np.float32)
+    d, dd = _logits_and_dtype(draft)
+    if dd == BF16:
+        d = (d.astype(np.uint32) << 16).view(np.float32)
+    return verify(t, d, tokens, u_accept, u_resample, temperature, nthreads=nthreads,
+                  want_trace=want_trace)

@@ -1,7 +1,8 @@
 """GB300-native batched speculative-sampling verification.
 
 Thin Python binding over the C ABI of ``libspecverify.so`` (declared in
-``include/spec_verify.h`` and ``include/spec_sample.h``).  Every function here only checks and marshals
+``include/spec_verify.h``, ``include/spec_sample.h`` and
+``include/spec_lmhead.h``).  Every function here only checks and marshals
 arguments (shapes, dtypes, device pointers, the current CUDA stream) and calls
 the function of the same name in the library; all arithmetic runs in the CUDA
 kernels.  PyTorch is used for device memory and streams only.
@@ -29,6 +30,7 @@ SPEC_MAX_V = 1 << 20
 SPEC_STAGES = 4
 SPEC_SAMPLE_STAGES = 2
 SPEC_FILTERED_STAGES = 5
+SPEC_LMHEAD_STAGES = 5
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "libspecverify.so")
@@ -96,6 +98,14 @@ def library():
         lib.spec_bench_read_sink_words.argtypes = []
         lib.spec_selftest_wait_timeout.restype = i32
         lib.spec_selftest_wait_timeout.argtypes = [vp, ctypes.c_uint64, vp]
+        lib.spec_verify_lmhead_workspace_size.restype = sz
+        lib.spec_verify_lmhead_workspace_size.argtypes = [i32] * 5
+        lib.spec_verify_lmhead.restype = i32
+        lib.spec_verify_lmhead.argtypes = [vp] * 9 + [i32] * 5 + [vp, sz, vp]
+        lib.spec_verify_lmhead_timed.restype = i32
+        lib.spec_verify_lmhead_timed.argtypes = [vp] * 10 + [i32] * 5 + [vp, sz, vp, vp]
+        lib.spec_lmhead_logits.restype = i32
+        lib.spec_lmhead_logits.argtypes = [vp, vp, vp, i32, i32, i32, vp, vp]
         _lib = lib
         return lib
 
@@ -515,3 +525,108 @@ def sample_to_device(sc, device="cuda"):
         logits = torch.from_numpy(a).to(device)
     return dict(logits=logits, u=torch.from_numpy(sc.u).to(device),
                 temperature=torch.from_numpy(sc.temperature).to(device))
+
+
+# ------------------------------------------------ LM-head-fused verification
+
+def spec_verify_lmhead_workspace_size(B: int, k: int, V: int, d: int, draft_dtype: int) -> int:
+    return int(library().spec_verify_lmhead_workspace_size(B, k, V, d, draft_dtype))
+
+
+def _marshal_lmhead(hidden, lm_head, draft, tokens, u_accept, u_resample, temperature):
+    torch = _torch()
+    if hidden.dtype != torch.bfloat16 or lm_head.dtype != torch.bfloat16:
+        raise TypeError("hidden and lm_head must be bfloat16")
+    if hidden.dim() != 3 or lm_head.dim() != 2 or draft.dim() != 3:
+        raise ValueError("hidden [B,k+1,d], lm_head [V,d], draft [B,k,V] expected")
+    B, k1, d = hidden.shape
+    V = lm_head.shape[0]
+    k = k1 - 1
+    if lm_head.shape[1] != d or tuple(draft.shape) != (B, k, V):
+        raise ValueError("shape mismatch between hidden, lm_head and draft")
+    for name, t, shape in (("tokens", tokens, (B, k)), ("u_accept", u_accept, (B, k)),
+                           ("u_resample", u_resample, (B,)), ("temperature", temperature, (B,))):
+        if tuple(t.shape) != shape:
+            raise ValueError(f"{name} must have shape {shape}")
+    for t in (hidden, lm_head, draft, tokens, u_accept, u_resample, temperature):
+        if not t.is_cuda or not t.is_contiguous():
+            raise ValueError("all tensors must be contiguous CUDA tensors")
+    return B, k, V, d, _dtype_code(draft)
+
+
+def lmhead_workspace(B: int, k: int, V: int, d: int, draft_dtype: int, device=None):
+    torch = _torch()
+    need = spec_verify_lmhead_workspace_size(B, k, V, d, draft_dtype)
+    if need == 0:
+        raise SpecVerifyError("sizes out of range for spec_verify_lmhead")
+    return torch.zeros(need, dtype=torch.uint8, device=device or "cuda")
+
+
+def spec_verify_lmhead(hidden, lm_head, draft, tokens, u_accept, u_resample, temperature,
+                       out_tokens=None, out_num_accepted=None, ws=None, want_probs=False,
+                       stream=None):
+    """Verification with the target's LM head fused in: target logits
+    t = hidden @ lm_head^T are formed on the tensor cores and never stored.
+    hidden bf16 [B,k+1,d], lm_head bf16 [V,d], draft [B,k,V] f32 or bf16.
+    Returns (out_tokens, out_num_accepted) or, with want_probs, also the fp32
+    P = p_i(g_i), Q = q_i(g_i) as [B,k,2]."""
+    torch = _torch()
+    B, k, V, d, ddt = _marshal_lmhead(hidden, lm_head, draft, tokens, u_accept, u_resample,
+                                      temperature)
+    dev = hidden.device
+    if out_tokens is None:
+        out_tokens = torch.empty((B, k + 1), dtype=torch.int32, device=dev)
+    if out_num_accepted is None:
+        out_num_accepted = torch.empty((B,), dtype=torch.int32, device=dev)
+    if ws is None:
+        ws = lmhead_workspace(B, k, V, d, ddt, dev)
+    probs = torch.empty((B, k, 2), dtype=torch.float32, device=dev) if want_probs else None
+    h = _stream_handle(stream, dev)
+    if want_probs:
+        rc = library().spec_verify_lmhead_timed(
+            _ptr(hidden), _ptr(lm_head), _ptr(draft), _ptr(tokens), _ptr(u_accept),
+            _ptr(u_resample), _ptr(temperature), _ptr(out_tokens), _ptr(out_num_accepted),
+            _ptr(probs), B, k, V, d, ddt, _ptr(ws), ws.numel(), h, None)
+    else:
+        rc = library().spec_verify_lmhead(
+            _ptr(hidden), _ptr(lm_head), _ptr(draft), _ptr(tokens), _ptr(u_accept),
+            _ptr(u_resample), _ptr(temperature), _ptr(out_tokens), _ptr(out_num_accepted),
+            B, k, V, d, ddt, _ptr(ws), ws.numel(), h)
+    _check(rc, "spec_verify_lmhead")
+    if want_probs:
+        return out_tokens, out_num_accepted, probs
+    return out_tokens, out_num_accepted
+
+
+def spec_verify_lmhead_timed(hidden, lm_head, draft, tokens, u_accept, u_resample, temperature,
+                             out_tokens, out_num_accepted, ws, stage_events, stream=None):
+    """spec_verify_lmhead recording SPEC_LMHEAD_STAGES events, one after each
+    kernel (draft chunk records, statistics GEMM, accept scan, draw GEMM,
+    final search)."""
+    B, k, V, d, ddt = _marshal_lmhead(hidden, lm_head, draft, tokens, u_accept, u_resample,
+                                      temperature)
+    handles = (ctypes.c_void_p * SPEC_LMHEAD_STAGES)(
+        *[ctypes.c_void_p(e.cuda_event) for e in stage_events])
+    rc = library().spec_verify_lmhead_timed(
+        _ptr(hidden), _ptr(lm_head), _ptr(draft), _ptr(tokens), _ptr(u_accept), _ptr(u_resample),
+        _ptr(temperature), _ptr(out_tokens), _ptr(out_num_accepted), None, B, k, V, d, ddt,
+        _ptr(ws), ws.numel(), _stream_handle(stream, hidden.device), handles)
+    _check(rc, "spec_verify_lmhead_timed")
+    return out_tokens, out_num_accepted
+
+
+def spec_lmhead_logits(hidden, lm_head, out=None, stream=None):
+    """The fused GEMM alone, storing out[r][x] = sum_j hidden[r][j] lm_head[x][j]
+    (fp32) for checking the tensor-core product.  hidden bf16 [M,d]."""
+    torch = _torch()
+    if hidden.dtype != torch.bfloat16 or lm_head.dtype != torch.bfloat16:
+        raise TypeError("hidden and lm_head must be bfloat16")
+    M, d = hidden.shape
+    V = lm_head.shape[0]
+    if out is None:
+        out = torch.empty((M, V), dtype=torch.float32, device=hidden.device)
+    status = torch.zeros(1, dtype=torch.int32, device=hidden.device)
+    rc = library().spec_lmhead_logits(_ptr(hidden), _ptr(lm_head), _ptr(out), M, V, d,
+                                      _ptr(status), _stream_handle(stream, hidden.device))
+    _check(rc, "spec_lmhead_logits")
+    return out, status

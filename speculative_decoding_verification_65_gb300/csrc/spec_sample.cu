@@ -35,6 +35,7 @@
 #include <stdint.h>
 
 #include "spec_sample.h"
+#include "internal.h"
 #include "spec_verify.h"
 #include "device_common.cuh"
 
@@ -81,6 +82,8 @@ struct SParams {
     int NG;            // groups of GROUP tiles per row
     unsigned int total_groups;
     unsigned long long bytes;
+    int rows_per_temp;  // row r's temperature is temperature[r / rows_per_temp]
+    int skip_greedy;    // rows at T = 0 are not read (their records are not used)
 };
 
 struct Smem {
@@ -130,8 +133,10 @@ __global__ void __launch_bounds__(NTHREADS, 2) chunk_kernel(const SParams P)
         for (unsigned int base = blockIdx.x; base < P.total_groups && ok; base += 32u * G) {
             // each lane fetches the temperature of one of the next 32 groups
             const unsigned long long gl = base + (unsigned long long)lane * G;
-            const float Tl = (gl < P.total_groups) ? __ldg(P.temperature + gl / (unsigned int)P.NG)
-                                                   : 0.0f;
+            const float Tl = (gl < P.total_groups)
+                                 ? __ldg(P.temperature + gl / (unsigned int)P.NG /
+                                                             (unsigned int)P.rows_per_temp)
+                                 : 0.0f;
             __syncwarp();  // lane 0 is done with the previous batch
             S.tabT[lane] = Tl;
             __syncwarp();
@@ -141,8 +146,8 @@ __global__ void __launch_bounds__(NTHREADS, 2) chunk_kernel(const SParams P)
                     if (gi >= P.total_groups)
                         break;
                     const float T = S.tabT[i];
-                    if (!temperature_valid(T))
-                        continue;  // the row's token is -1; nobody reads its records
+                    if (!temperature_valid(T) || (P.skip_greedy && T == 0.0f))
+                        continue;  // nobody reads this row's records
                     const int row = (int)(gi / (unsigned int)P.NG);
                     const int grp = (int)(gi - (unsigned long long)row * (unsigned int)P.NG);
                     const int seg1 = min(P.NS, (grp + 1) * GROUP);
@@ -429,23 +434,12 @@ int launch_all(const SParams &P, unsigned int grid1, cudaStream_t st, void *cons
     return SPEC_OK;
 }
 
-int launch(const void *logits, const float *u, const float *temp, int32_t *out, int32_t R,
-           int32_t V, int32_t dtype, void *ws, size_t ws_size, void *stream,
-           void *const *events)
+// The chunk kernel's parameters and grid for R rows of V logits; the
+// records go to `rec`, the status to `hdr`.
+int setup_chunks(SParams &P, unsigned int &grid1, const void *logits, const float *temp,
+                 float2 *rec, WsHeader *hdr, int32_t R, int32_t V, int32_t dtype)
 {
-    if (!sizes_ok(R, V, dtype))
-        return SPEC_EINVAL;
-    if (R == 0)
-        return SPEC_OK;
-    if (!logits || !u || !temp || !out || !ws)
-        return SPEC_EINVAL;
-    if ((reinterpret_cast<uintptr_t>(logits) & 15) || (reinterpret_cast<uintptr_t>(ws) & 15) ||
-        (reinterpret_cast<uintptr_t>(u) & 3) || (reinterpret_cast<uintptr_t>(temp) & 3) ||
-        (reinterpret_cast<uintptr_t>(out) & 3))
-        return SPEC_EINVAL;
     const Layout lay = layout(R, V, dtype);
-    if (ws_size < lay.total)
-        return SPEC_ENOSPACE;
     const size_t NG = (lay.NS + GROUP - 1) / GROUP;
     const size_t groups = (size_t)R * NG;
     if ((size_t)R * lay.NS >= 0x7fffffffull)
@@ -473,16 +467,14 @@ int launch(const void *logits, const float *u, const float *temp, int32_t *out, 
         dc.attr_set[di] = true;
     }
     const size_t resident = (size_t)dc.sms * dc.ctas_per_sm[di];
-    const unsigned int grid1 = (unsigned int)(groups < resident ? groups : resident);
+    grid1 = (unsigned int)(groups < resident ? groups : resident);
 
-    SParams P;
     P.logits = logits;
-    P.u = u;
+    P.u = nullptr;
     P.temperature = temp;
-    P.out = out;
-    uint8_t *w = reinterpret_cast<uint8_t *>(ws);
-    P.hdr = reinterpret_cast<WsHeader *>(w);
-    P.rec = reinterpret_cast<float2 *>(w + lay.rec);
+    P.out = nullptr;
+    P.hdr = hdr;
+    P.rec = rec;
     P.R = R;
     P.V = V;
     P.NS = (int)lay.NS;
@@ -490,6 +482,37 @@ int launch(const void *logits, const float *u, const float *temp, int32_t *out, 
     P.NG = (int)NG;
     P.total_groups = (unsigned int)groups;
     P.bytes = (unsigned long long)R * (unsigned long long)V * ((dtype == SPEC_F32) ? 4 : 2);
+    P.rows_per_temp = 1;
+    P.skip_greedy = 0;
+    return SPEC_OK;
+}
+
+int launch(const void *logits, const float *u, const float *temp, int32_t *out, int32_t R,
+           int32_t V, int32_t dtype, void *ws, size_t ws_size, void *stream,
+           void *const *events)
+{
+    if (!sizes_ok(R, V, dtype))
+        return SPEC_EINVAL;
+    if (R == 0)
+        return SPEC_OK;
+    if (!logits || !u || !temp || !out || !ws)
+        return SPEC_EINVAL;
+    if ((reinterpret_cast<uintptr_t>(logits) & 15) || (reinterpret_cast<uintptr_t>(ws) & 15) ||
+        (reinterpret_cast<uintptr_t>(u) & 3) || (reinterpret_cast<uintptr_t>(temp) & 3) ||
+        (reinterpret_cast<uintptr_t>(out) & 3))
+        return SPEC_EINVAL;
+    const Layout lay = layout(R, V, dtype);
+    if (ws_size < lay.total)
+        return SPEC_ENOSPACE;
+    uint8_t *w = reinterpret_cast<uint8_t *>(ws);
+    SParams P;
+    unsigned int grid1 = 0;
+    const int rc = setup_chunks(P, grid1, logits, temp, reinterpret_cast<float2 *>(w + lay.rec),
+                                reinterpret_cast<WsHeader *>(w), R, V, dtype);
+    if (rc != SPEC_OK)
+        return rc;
+    P.u = u;
+    P.out = out;
 
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
     return (dtype == SPEC_F32) ? launch_all<SPEC_F32>(P, grid1, st, events)
@@ -515,6 +538,42 @@ HostArena host_arena(int32_t R, int32_t V, int32_t dtype)
 }
 
 }  // namespace
+
+namespace spec_internal {
+
+size_t chunk_count(int32_t V, int32_t dtype)
+{
+    return layout(1, V, dtype).NC;
+}
+
+int chunk_records(const void *logits, const float *temperature, int32_t rows_per_temp,
+                  float2 *rec, void *hdr, int32_t R, int32_t V, int32_t dtype,
+                  cudaStream_t stream)
+{
+    if (!sizes_ok(R, V, dtype) || rows_per_temp < 1)
+        return SPEC_EINVAL;
+    if (R == 0)
+        return SPEC_OK;
+    SParams P;
+    unsigned int grid1 = 0;
+    const int rc = setup_chunks(P, grid1, logits, temperature, rec,
+                                reinterpret_cast<WsHeader *>(hdr), R, V, dtype);
+    if (rc != SPEC_OK)
+        return rc;
+    P.rows_per_temp = rows_per_temp;
+    P.skip_greedy = 1;
+    if (dtype == SPEC_F32)
+        chunk_kernel<SPEC_F32><<<grid1, NTHREADS, SMEM_BYTES, stream>>>(P);
+    else
+        chunk_kernel<SPEC_BF16><<<grid1, NTHREADS, SMEM_BYTES, stream>>>(P);
+    if (cudaPeekAtLastError() != cudaSuccess) {
+        (void)cudaGetLastError();
+        return SPEC_ECUDA;
+    }
+    return SPEC_OK;
+}
+
+}  // namespace spec_internal
 
 // ------------------------------------------------------------------- C ABI
 

@@ -362,3 +362,85 @@ def sample_bytes(sc: SampleCase) -> int:
     T = sc.temperature
     ok = ~(np.isnan(T) | (T < 0) | np.isinf(T) | ((T > 0) & (T < np.finfo(np.float32).tiny)))
     return int(np.count_nonzero(ok)) * sc.V * sc.elem_size
+
+
+# ----------------------------------------------- LM-head-fused verification
+
+@dataclass
+class LmheadCase:
+    """Inputs of the LM-head-fused verification (host numpy arrays)."""
+    hidden: np.ndarray       # [B, k+1, d] uint16 bf16 bits: target hidden states
+    lm_head: np.ndarray      # [V, d] uint16 bf16 bits: W
+    draft: np.ndarray        # [B, k, V] float32, or uint16 bf16 bits
+    tokens: np.ndarray       # [B, k] int32
+    u_accept: np.ndarray     # [B, k] float32
+    u_resample: np.ndarray   # [B] float32
+    temperature: np.ndarray  # [B] float32
+    dtype: str               # the draft's dtype
+    name: str = ""
+
+    @property
+    def B(self) -> int:
+        return int(self.hidden.shape[0])
+
+    @property
+    def k(self) -> int:
+        return int(self.hidden.shape[1]) - 1
+
+    @property
+    def d(self) -> int:
+        return int(self.hidden.shape[2])
+
+    @property
+    def V(self) -> int:
+        return int(self.lm_head.shape[0])
+
+
+def make_lmhead_case(B: int, k: int, V: int, d: int, dtype: str = BF16, recipe: str = "grid",
+                     seed: int = 11, T=(1.0,), sigma_h: float = 0.3) -> LmheadCase:
+    """Random target hidden states and LM head, and draft logits from a draft
+    model that shares the head but sees perturbed hidden states.
+
+    recipe "grid": h in {-4..4}/4 and W in {-8..8}/32, so every product and
+    partial sum of h.W is a multiple of 2^-7 below 2^17 in size: the logits
+    are exact in fp32 whatever the order of accumulation (d <= 4096), and
+    their spread is about sqrt(d/100).
+    recipe "gauss": h ~ N(0, 1), W ~ N(0, (2.5 / sqrt d)^2), both rounded to
+    bf16: logits of spread about 2.5, rounded by any fp32 accumulation.
+    Draft hidden states are the target's plus N(0, sigma_h^2) per element
+    (on the grid recipe rounded back to the grid); draft logits are their
+    product with W in float64, stored as `dtype`.  Draft tokens are sampled
+    from the draft logits at the sequence's temperature (argmax at T = 0);
+    uniforms are float32 in [0, 1).  The bonus position has no draft row."""
+    rng = np.random.default_rng(seed)
+    if recipe == "grid":
+        h = rng.integers(-4, 5, size=(B, k + 1, d)).astype(np.float32) / 4.0
+        w = rng.integers(-8, 9, size=(V, d)).astype(np.float32) / 32.0
+        hd = h[:, :k] + np.round(rng.normal(0.0, sigma_h, size=(B, k, d)) * 4.0) / 4.0
+        hd = np.clip(hd, -1.0, 1.0).astype(np.float32)
+    elif recipe == "gauss":
+        h = rng.standard_normal((B, k + 1, d)).astype(np.float32)
+        w = (rng.standard_normal((V, d)) * (2.5 / np.sqrt(d))).astype(np.float32)
+        hd = (h[:, :k] + rng.normal(0.0, sigma_h, size=(B, k, d))).astype(np.float32)
+    else:
+        raise ValueError(f"unknown recipe {recipe}")
+    hb = f32_to_bf16_bits(h)
+    wb = f32_to_bf16_bits(w)
+    hdb = f32_to_bf16_bits(hd)
+    w64 = bf16_bits_to_f32(wb).astype(np.float64)
+    dl = (bf16_bits_to_f32(hdb).astype(np.float64).reshape(-1, d) @ w64.T).reshape(B, k, V)
+    dl32 = dl.astype(np.float32)
+    draft = f32_to_bf16_bits(dl32) if dtype == BF16 else dl32
+    temps = tuple(T) if isinstance(T, (tuple, list)) else (float(T),)
+    temperature = np.asarray(rng.choice(temps, size=B), np.float32)
+    rows = decode(draft)
+    tokens = np.stack([_sample_tokens(rng, rows[b], float(temperature[b])) for b in range(B)])
+    u_accept = rng.random((B, k), dtype=np.float32)
+    u_resample = rng.random(B, dtype=np.float32)
+    return LmheadCase(hb, wb, draft, tokens.astype(np.int32), u_accept, u_resample,
+                      temperature, dtype, name=f"lmhead {recipe} B{B} k{k} V{V} d{d} {dtype}")
+
+
+def lmhead_flops(c: LmheadCase) -> int:
+    """Multiply-add flops of the statistics GEMM (2 per product, B(k+1) rows)."""
+    return 2 * c.B * (c.k + 1) * c.V * c.d

@@ -21,8 +21,10 @@ def decisions_of(n_ref, k, greedy):
     return tests + 1
 
 
-def compare(case, g_tokens, g_n, r_tokens, r_n, trace):
-    """Returns a report dict; raises AssertionError on a non-exempt mismatch."""
+def compare(case, g_tokens, g_n, r_tokens, r_n, trace, band=BAND):
+    """Returns a report dict; raises AssertionError on a non-exempt mismatch.
+    `band` widens the exemption where the GPU's inputs to the decisions carry
+    a known extra rounding (the fused LM head's fp32 logits)."""
     B, k = case.B, case.k
     g_tokens = np.asarray(g_tokens)
     g_n = np.asarray(g_n)
@@ -33,10 +35,10 @@ def compare(case, g_tokens, g_n, r_tokens, r_n, trace):
         if not greedy and r_n[b] >= 0:
             tested = min(int(r_n[b]) + 1, k)
             th = trace[b, :tested]
-            report["near_band"] += int(np.sum(np.abs(case.u_accept[b, :tested] - th) < BAND))
+            report["near_band"] += int(np.sum(np.abs(case.u_accept[b, :tested] - th) < band))
             lo, hi = trace[b, k], trace[b, k + 1]
             u = float(case.u_resample[b])
-            if min(u - lo, hi - u) < BAND:
+            if min(u - lo, hi - u) < band:
                 report["near_band"] += 1
         if g_n[b] == r_n[b] and np.array_equal(g_tokens[b], r_tokens[b]):
             continue
@@ -53,8 +55,8 @@ def compare(case, g_tokens, g_n, r_tokens, r_n, trace):
             u = float(case.u_resample[b])
             margin = min(u - lo, hi - u)
             kind = "bonus" if r_n[b] == k else "residual"
-        if not margin < BAND:
-            raise AssertionError(f"mismatch outside the {BAND} band (margin {margin:.3g}): " + why)
+        if not margin < band:
+            raise AssertionError(f"mismatch outside the {band} band (margin {margin:.3g}): " + why)
         report["exempt"] += 1
         report["mismatched"].append((b, kind, float(margin)))
     report["draws"] = int(np.sum(np.asarray(r_n) >= 0))
