@@ -892,6 +892,236 @@ def run_ours_sample(args):
         dist.destroy_process_group()
 
 
+# ------------------------------------------------ LM-head-fused verification
+
+LMHEAD_SHAPE = dict(B=1024, k=4, V=128256, d=4096)  # workload 5's shape, d of an 8B-class model
+
+
+def lmhead_inputs(B, k, V, d, seed, device):
+    """Input generation for the fused workload with torch on `device`: target
+    hidden states h ~ N(0, 1), LM head W ~ N(0, (2.5 / sqrt d)^2), both bf16;
+    a draft model sharing W that sees h + N(0, 0.3^2) gives the draft logits
+    (bf16, computed by torch); draft tokens sampled from them at T = 1;
+    uniforms in [0, 1)."""
+    import torch
+    g = torch.Generator(device=device)
+    g.manual_seed(seed)
+    hidden = torch.randn((B, k + 1, d), generator=g, device=device).to(torch.bfloat16)
+    W = torch.empty((V, d), dtype=torch.bfloat16, device=device)
+    for r0 in range(0, V, 16384):  # in slices: no 2 GB fp32 temporary
+        r1 = min(V, r0 + 16384)
+        W[r0:r1] = (torch.randn((r1 - r0, d), generator=g, device=device)
+                    * (2.5 / d ** 0.5)).to(torch.bfloat16)
+    hd = (hidden[:, :k].float()
+          + 0.3 * torch.randn((B, k, d), generator=g, device=device)).to(torch.bfloat16)
+    draft = torch.empty((B, k, V), dtype=torch.bfloat16, device=device)
+    for b0 in range(0, B, 64):
+        b1 = min(B, b0 + 64)
+        mm = hd[b0:b1].reshape(-1, d).float() @ W.float().T if device == "cpu" else \
+            hd[b0:b1].reshape(-1, d) @ W.T
+        draft[b0:b1] = mm.reshape(b1 - b0, k, V).to(torch.bfloat16)
+    temperature = torch.ones((B,), dtype=torch.float32, device=device)
+    u_accept = torch.rand((B, k), generator=g, device=device)
+    u_resample = torch.rand((B,), generator=g, device=device)
+    tokens = filtered_draft_tokens(draft, temperature, 0, 1.0, seed + 1)
+    return dict(hidden=hidden, lm_head=W, draft=draft, tokens=tokens, u_accept=u_accept,
+                u_resample=u_resample, temperature=temperature)
+
+
+def lmhead_name(B, k, V, d):
+    return f"lmhead_B{B}_k{k}_V{V}_d{d}_bf16"
+
+
+def _bits(t):
+    import torch
+    return t.contiguous().view(torch.int16).cpu().numpy().view(np.uint16)
+
+
+def run_ours_lmhead(args):
+    import torch
+
+    import speculative_decoding_verification_65_gb300 as sv
+
+    rank, world, local = dist_env()
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    sh = dict(LMHEAD_SHAPE)
+    if args.batch is not None:
+        sh["B"] = args.batch
+    B, k, V, d = sh["B"], sh["k"], sh["V"], sh["d"]
+    x = lmhead_inputs(B, k, V, d, 4321 + rank, dev)
+    stream = torch.cuda.current_stream(dev)
+    ws = sv.lmhead_workspace(B, k, V, d, sv.SPEC_BF16, dev)
+    out_t = torch.empty((B, k + 1), dtype=torch.int32, device=dev)
+    out_n = torch.empty((B,), dtype=torch.int32, device=dev)
+
+    def step(events=None):
+        if events is None:
+            sv.spec_verify_lmhead(**x, out_tokens=out_t, out_num_accepted=out_n, ws=ws,
+                                  stream=stream)
+        else:
+            sv.spec_verify_lmhead_timed(**x, out_tokens=out_t, out_num_accepted=out_n, ws=ws,
+                                        stage_events=events, stream=stream)
+
+    for _ in range(max(args.warmup, 3)):
+        step()
+    torch.cuda.synchronize(dev)
+    if sv.spec_verify_read_status(ws) != sv.SPEC_DEV_OK:
+        raise RuntimeError("device status nonzero after warm-up")
+    n_err = int((out_n < 0).sum().item())
+    acc_mean = float(out_n[out_n >= 0].float().mean().item())
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+    torch.cuda.synchronize(dev)
+    with ClockSampler(local) as clk:
+        t0.record(stream)
+        for _ in range(args.steps):
+            step()
+        t1.record(stream)
+        torch.cuda.synchronize(dev)
+    total_ms = reduce_max(t0.elapsed_time(t1), world, dev)
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    stages = [[torch.cuda.Event(enable_timing=True) for _ in range(sv.SPEC_LMHEAD_STAGES)]
+              for _ in range(args.steps)]
+    for ev in [e for row in stages for e in row]:
+        ev.record(stream)
+    torch.cuda.synchronize(dev)
+    for i in range(args.steps):
+        starts[i].record(stream)
+        step(stages[i])
+    torch.cuda.synchronize(dev)
+    stage_ms = [statistics.mean(
+        (starts[i] if j == 0 else stages[i][j - 1]).elapsed_time(stages[i][j])
+        for i in range(args.steps)) for j in range(sv.SPEC_LMHEAD_STAGES)]
+    ms_per_step = total_ms / args.steps
+    value = aggregate_rate(B * k, args.steps, world, total_ms / 1e3)
+    status = sv.spec_verify_read_status(ws)
+    # end to end: the step's inputs (hidden states, draft logits, tokens,
+    # uniforms, temperatures) copied in from pinned host memory each step, the
+    # outputs copied back; the LM head is a model weight and stays resident
+    host = {n: t.cpu().pin_memory() for n, t in x.items() if n != "lm_head"}
+    h_ot = torch.empty((B, k + 1), dtype=torch.int32).pin_memory()
+    h_on = torch.empty((B,), dtype=torch.int32).pin_memory()
+    e2e_steps = max(1, min(args.steps, 10))
+    e0 = time.perf_counter()
+    for _ in range(e2e_steps):
+        dd = {n: t.to(dev, non_blocking=True) for n, t in host.items()}
+        sv.spec_verify_lmhead(**dd, lm_head=x["lm_head"], out_tokens=out_t,
+                              out_num_accepted=out_n, ws=ws, stream=stream)
+        h_ot.copy_(out_t, non_blocking=True)
+        h_on.copy_(out_n, non_blocking=True)
+        torch.cuda.synchronize(dev)
+    e2e_s = reduce_max(time.perf_counter() - e0, world, dev)
+    h2d = sum(int(t.numel() * t.element_size()) for t in host.values())
+    if rank != 0:
+        if world > 1:
+            import torch.distributed as dist
+            dist.destroy_process_group()
+        return
+    peaks, peak_src = measured_peaks()
+    flops = 2 * B * (k + 1) * V * d
+    tflops = flops / (stage_ms[1] / 1e3) / 1e12
+    # the burst peak while the timed region kept the SM clock at its maximum
+    # (no power cap reached), the sustained one once the clock came down
+    cs = clk.summary()
+    at_max = (cs.get("sm_mhz") is not None and cs.get("sm_max_mhz")
+              and cs["sm_mhz"] >= 0.95 * cs["sm_max_mhz"])
+    which = "bf16_tflops" if at_max else "bf16_tflops_sustained"
+    peak = float(peaks.get(which, 1900.0 if at_max else 1700.0))
+    draw_flops = 2 * B * V * d
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": max(args.warmup, 3), "ms_per_step": ms_per_step,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "bf16", "data": "synthetic (random weights and hidden states, see DESIGN)",
+        "config": {"workload": lmhead_name(B, k, V, d), "B_per_gpu": B, "k": k, "V": V, "d": d,
+                   "draft_dtype": "bf16", "temperature": 1.0, "error_sequences": n_err,
+                   "mean_accepted": acc_mean, "gemm_flops_per_step": flops + draw_flops,
+                   "l2": "the 1 GB LM head and 1 GB of draft logits per step exceed L2",
+                   "parallelism": f"dp{world}"},
+        "gpu_launches": sv.SPEC_LMHEAD_STAGES * args.steps,
+        "roofline": {"bound": "tensor", "achieved": tflops, "peak": peak, "unit": "TFLOP/s",
+                     "frac": tflops / peak, "traffic": None,
+                     "peak_source": (f"measured cuBLAS bf16 (MEASURED_PEAKS.json {which}; "
+                                     f"SM clock median {cs.get('sm_mhz')} MHz)")
+                     if peak_src == "measured" else f"fallback for {which}",
+                     "kernel": "gemm_kernel<STATS> (h W^T on tcgen05, statistics epilogue)",
+                     "flops_per_launch": flops,
+                     "kernel_timing": "CUDA events after each kernel, K further steps",
+                     "draw_gemm_tflops": draw_flops / (stage_ms[3] / 1e3) / 1e12},
+        "stage_ms": {"draft_records": stage_ms[0], "stats_gemm": stage_ms[1],
+                     "scan": stage_ms[2], "draw_gemm": stage_ms[3], "final": stage_ms[4]},
+        "clocks": cs,
+        "e2e": {"value": aggregate_rate(B * k, e2e_steps, world, e2e_s), "unit": UNIT,
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": int(B * (k + 2) * 4),
+                "steps": e2e_steps,
+                "path": "torch copies of pinned host tensors around spec_verify_lmhead"},
+        "cpu_baseline": None,
+        "device_status": status,
+    }
+    if world == 1 and not args.no_cpu_baseline:
+        import oracle
+        cores = host_cores()
+        bs = min(B, 8)
+        W = _bits(x["lm_head"])
+        sub = [_bits(x["hidden"][:bs]), W, _bits(x["draft"][:bs])]
+        rest = [x[n][:bs].cpu().numpy() for n in ("tokens", "u_accept", "u_resample",
+                                                  "temperature")]
+        c0 = time.perf_counter()
+        oracle.verify_lmhead(*sub, *rest, nthreads=cores, want_trace=False)
+        used = time.perf_counter() - c0
+        line["cpu_baseline"] = {"value": bs * k / used, "unit": UNIT, "cores": cores,
+                                "kind": "oracle",
+                                "sample": f"{bs} of {B} sequences (fp64 LM head product and "
+                                          f"verification), {used:.1f} s"}
+    print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+def run_reference_lmhead(args):
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return
+    import oracle
+    oracle.build()
+    sh = dict(LMHEAD_SHAPE)
+    B, k, V, d = sh["B"], sh["k"], sh["V"], sh["d"]
+    per_step = 4
+    x = lmhead_inputs(per_step, k, V, d, 4321, "cpu")
+    cores = host_cores()
+    args_np = [_bits(x["hidden"]), _bits(x["lm_head"]), _bits(x["draft"])] + \
+        [x[n].numpy() for n in ("tokens", "u_accept", "u_resample", "temperature")]
+    run = lambda: oracle.verify_lmhead(*args_np, nthreads=cores, want_trace=False)
+    for _ in range(args.warmup):
+        run()
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        run()
+    dt = time.perf_counter() - t0
+    value = per_step * k * args.steps / dt
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT,
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": dt / args.steps * 1e3, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": lmhead_name(B, k, V, d), "B": per_step, "k": k, "V": V, "d": d,
+                   "what": "fp64 CPU oracle: LM head product (numpy) and verification (C)"},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
+                         "sample": f"{per_step} of {B} sequences per step"},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -900,7 +1130,7 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--config", type=int, default=None, choices=[1, 2, 3, 4, 5],
                     help="workload (default 4 for verify, 5 for sample)")
-    ap.add_argument("--op", choices=["verify", "sample", "filtered"], default="verify")
+    ap.add_argument("--op", choices=["verify", "sample", "filtered", "lmhead"], default="verify")
     ap.add_argument("--top-k", type=int, default=50, help="top-k of --op filtered (0: none)")
     ap.add_argument("--top-p", type=float, default=0.9, help="top-p of --op filtered (1: none)")
     ap.add_argument("--batch", type=int, default=None,
@@ -923,6 +1153,11 @@ def main():
             run_reference_filtered(args)
         else:
             run_ours_filtered(args)
+    elif args.op == "lmhead":
+        if args.impl == "reference":
+            run_reference_lmhead(args)
+        else:
+            run_ours_lmhead(args)
     elif args.impl == "reference":
         run_reference(args)
     else:

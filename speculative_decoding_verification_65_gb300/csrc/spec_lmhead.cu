@@ -64,7 +64,7 @@ constexpr int TMEM_COLS = NACC * BN;      // 512: all of TMEM
 constexpr int GTHREADS = 192;             // 6 warps
 constexpr int GROUP = 32;                 // tokens per draw record
 
-enum { MODE_STORE = 0, MODE_STATS = 1, MODE_DRAW = 2 };
+enum { MODE_STORE = 0, MODE_STATS = 1, MODE_DRAW_F32 = 2, MODE_DRAW_BF16 = 3 };
 
 struct GSmemTail {
     unsigned long long full[STAGES];
@@ -209,7 +209,7 @@ struct GParams {
     const int32_t *tokens;   // [B][k]
     const float *temperature;
     int k;                   // rows per sequence are k + 1
-    // MODE_DRAW
+    // MODE_DRAW_F32 / MODE_DRAW_BF16
     const DrawJob *jobs;     // [M] (one row per sequence)
     float *grp;              // [M][ng]: weight sum of each GROUP-token group
     float *grp_p;            // [M][ng]: the same for p alone (residual rows: the
@@ -317,7 +317,8 @@ __device__ __forceinline__ void epilogue(const GParams &P, uint32_t taddr, int r
             if (has_tg)
                 P.tg[row] = tgv;
         }
-    } else {  // MODE_DRAW
+    } else {  // MODE_DRAW_F32 / MODE_DRAW_BF16: the draft's element size is fixed
+        constexpr int es = (MODE == MODE_DRAW_F32) ? 4 : 2;
         const bool inrow = row < P.M;
         DrawJob J;
         J.mode = JOB_NONE;
@@ -325,11 +326,40 @@ __device__ __forceinline__ void epilogue(const GParams &P, uint32_t taddr, int r
             J = P.jobs[row];
         const bool resid = J.mode == JOB_RESIDUAL;
         const size_t drow = resid ? ((size_t)J.b * P.k + J.j) * (size_t)P.N : 0;
+        const uint8_t *dbase = reinterpret_cast<const uint8_t *>(P.draft) + drow * es;
+        // 16-byte loads of the draft row where it is aligned and whole
+        const bool vec = resid && ((reinterpret_cast<uintptr_t>(dbase) & 15) == 0);
+        // the draft values of one 32-column chunk: 64 (bf16) or 128 (f32) bytes
+        auto load_draft = [&](int col0, uint4 (&dv)[8]) {
+            if (vec && col0 + 32 <= P.N) {
+                const uint4 *src = reinterpret_cast<const uint4 *>(dbase + (size_t)col0 * es);
+#pragma unroll
+                for (int q = 0; q < 8; ++q)
+                    if (q < 2 * es)
+                        dv[q] = __ldcs(src + q);
+            }
+        };
+        auto draft_val = [&](const uint4 (&dv)[8], int col0, int j) -> float {
+            if (vec && col0 + 32 <= P.N) {
+                const uint4 w4 = dv[(j * es) >> 4];
+                const int e = ((j * es) & 15) >> 2;  // 32-bit word within the 16 bytes
+                const uint32_t word = (e == 0) ? w4.x : (e == 1) ? w4.y : (e == 2) ? w4.z : w4.w;
+                if (es == 4)
+                    return __uint_as_float(word);
+                return __uint_as_float((j & 1) ? (word & 0xffff0000u) : (word << 16));
+            }
+            return draft_at(P, drow + col0 + j);
+        };
+        uint4 dv[8], dn[8];
+        if (resid)
+            load_draft(col_base, dv);
 #pragma unroll 1
         for (int ch = 0; ch < BN / 32; ++ch) {
+            const int col0 = col_base + ch * 32;
+            if (resid && ch + 1 < BN / 32)
+                load_draft(col0 + 32, dn);  // one chunk ahead
             float v[32];
             tmem_ld32(taddr + (uint32_t)(ch * 32), v);
-            const int col0 = col_base + ch * 32;
             if (J.mode != JOB_NONE && col0 < P.N) {
                 float ws = 0.0f, ps = 0.0f;
 #pragma unroll
@@ -339,7 +369,7 @@ __device__ __forceinline__ void epilogue(const GParams &P, uint32_t taddr, int r
                         const float p = ex2((v[j] - J.mt) * J.c) * J.rzt;
                         float w = p;
                         if (resid)
-                            w = fmaxf(p - ex2((draft_at(P, drow + col) - J.md) * J.c) * J.rzd,
+                            w = fmaxf(p - ex2((draft_val(dv, col0, j) - J.md) * J.c) * J.rzd,
                                       0.0f);
                         ws += w;
                         ps += p;
@@ -349,8 +379,35 @@ __device__ __forceinline__ void epilogue(const GParams &P, uint32_t taddr, int r
                 if (resid)
                     P.grp_p[(size_t)row * P.ng + col0 / GROUP] = ps;
             }
+            if (resid) {
+#pragma unroll
+                for (int q = 0; q < 8; ++q)
+                    dv[q] = dn[q];
+            }
         }
     }
+}
+
+// Draw GEMM: the draft values the epilogue will read for row `row` of the
+// tile at column block n, requested into L2 one tile ahead (a tile's MMAs
+// take longer than an HBM round trip, so the loads then hit L2).
+template <int MODE>
+__device__ __forceinline__ void prefetch_draft(const GParams &P, int row, int n)
+{
+    if (MODE != MODE_DRAW_F32 && MODE != MODE_DRAW_BF16)
+        return;
+    if (row >= P.M)
+        return;
+    const int mode = P.jobs[row].mode;
+    if (mode != JOB_RESIDUAL)
+        return;
+    constexpr int es = (MODE == MODE_DRAW_F32) ? 4 : 2;
+    const DrawJob &J = P.jobs[row];
+    const uint8_t *base = reinterpret_cast<const uint8_t *>(P.draft) +
+                          (((size_t)J.b * P.k + J.j) * (size_t)P.N) * es;
+    const int c1 = min(P.N, n * BN + BN);
+    for (int c = n * BN; c < c1; c += 128 / es)
+        asm volatile("prefetch.global.L2 [%0];" :: "l"(base + (size_t)c * es));
 }
 
 template <int MODE>
@@ -495,6 +552,10 @@ __global__ void __launch_bounds__(GTHREADS, 1)
             }
             tc_fence_after();
             const int row = m * BM + q * 32 + lane;
+            if (t + G < P.total) {  // this thread's row of its next tile
+                const int n2 = (t + G) / P.mt, m2 = (t + G) - n2 * P.mt;
+                prefetch_draft<MODE>(P, m2 * BM + q * 32 + lane, n2);
+            }
             epilogue<MODE>(P, tbase + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * BN), row, n);
             tc_fence_before();
             __syncwarp();
@@ -524,6 +585,7 @@ __global__ void __launch_bounds__(GTHREADS, 1)
 namespace {
 
 constexpr int SCAN_WARPS = 4;
+constexpr int MAX_CHUNKS = (SPEC_MAX_V / GROUP + 127) / 128;  // 256 for 2^20 tokens
 
 struct VParams {
     int B, k, V, d;
@@ -574,6 +636,7 @@ __device__ __forceinline__ void fold_row(const float4 *base, int n, float c, boo
     m = -INFINITY;
     s = 0.0f;
     ix = INT_MAX;
+#pragma unroll 4
     for (int q = lane; q < n; q += 32) {
         const float4 v = __ldcg(base + q);
         fold2(m, s, ix, v.x, v.y, __float_as_int(v.z), c, sample);
@@ -593,6 +656,7 @@ __device__ __forceinline__ void fold_rec(const float2 *base, int n, float c, int
 {
     m = -INFINITY;
     s = 0.0f;
+#pragma unroll 4
     for (int q = lane; q < n; q += 32) {
         const float2 v = __ldcg(base + q);
         const float mn = fmax_nan(m, v.x);
@@ -731,8 +795,8 @@ __global__ void __launch_bounds__(SCAN_WARPS * 32) scan_kernel(const VParams P)
 
 // One warp per sequence with a draw: the inverse CDF over the group sums in
 // index order (each lane a contiguous range of groups, Kogge-Stone across
-// lanes), then the crossing group's 32 logits recomputed as dot products
-// (lane x: t(x) = h . W[x], sequential fp32 over d) and searched in order.
+// lanes), then the crossing group's 32 logits recomputed as dot products and
+// searched in order.
 // The group's recomputed weights may differ from the GEMM's by rounding; a
 // threshold they leave past the group's end takes its last positive weight.
 __global__ void __launch_bounds__(SCAN_WARPS * 32) final_kernel(const VParams P)
@@ -747,109 +811,161 @@ __global__ void __launch_bounds__(SCAN_WARPS * 32) final_kernel(const VParams P)
     if (J.mode == JOB_NONE)
         return;
     const int ng = P.ng;
-    const float *w = P.grp + (size_t)b * ng;
-    // each lane: groups [lo, hi)
-    const int per = (ng + 31) / 32;
-    const int lo = min(ng, lane * per), hi = min(ng, lo + per);
-    auto range_sum = [&](const float *a) {
-        float s = 0.0f;
-        for (int q = lo; q < hi; ++q)
-            s += __ldcg(a + q);
-        return s;
+    // The group sums are read as chunks of 128 (32 lanes x float4, coalesced):
+    // chunk c holds groups 128c .. 128c+127 with lane l's float4 groups
+    // 128c+4l .. 128c+4l+3, so lane order within a chunk is group order.
+    // Totals: per chunk in shared memory, then the row's R = their sum in
+    // chunk order; the crossing chunk, lane and group follow the same order.
+    __shared__ float ctot[SCAN_WARPS][MAX_CHUNKS];
+    const int nch = (ng + 127) / 128;
+    auto group4 = [&](const float *a, int c) {
+        const int g0 = c * 128 + lane * 4;
+        if (g0 + 3 < ng && (ng & 3) == 0)
+            return __ldcg(reinterpret_cast<const float4 *>(a + g0));
+        float4 r = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+        if (g0 < ng) r.x = __ldcg(a + g0);
+        if (g0 + 1 < ng) r.y = __ldcg(a + g0 + 1);
+        if (g0 + 2 < ng) r.z = __ldcg(a + g0 + 2);
+        if (g0 + 3 < ng) r.w = __ldcg(a + g0 + 3);
+        return r;
     };
-    float ls = range_sum(w);
-    float tot = ls;
+    auto totals = [&](const float *a) {  // chunk totals; returns R
+        float R = 0.0f;
+#pragma unroll 4
+        for (int c = 0; c < nch; ++c) {
+            const float4 v = group4(a, c);
+            float s4 = ((v.x + v.y) + v.z) + v.w;
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1)
-        tot += __shfl_xor_sync(0xffffffffu, tot, o);
+            for (int o = 16; o > 0; o >>= 1)
+                s4 += __shfl_xor_sync(0xffffffffu, s4, o);
+            if (lane == 0)
+                ctot[warp][c] = s4;
+            R += s4;
+        }
+        __syncwarp();
+        return R;
+    };
+    const float *w = P.grp + (size_t)b * ng;
+    float tot = totals(w);
     if (J.mode == JOB_RESIDUAL && !(tot > 0.0f)) {
         // rounding left no residual mass: draw from p_j instead
         w = P.grp_p + (size_t)b * ng;
         J.mode = JOB_BONUS;
-        ls = range_sum(w);
-        tot = ls;
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1)
-            tot += __shfl_xor_sync(0xffffffffu, tot, o);
-    }
-    float incl = ls;  // inclusive scan of the lane sums, in lane order
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-        const float y = __shfl_up_sync(0xffffffffu, incl, o);
-        if (lane >= o)
-            incl += y;
+        tot = totals(w);
     }
     const float tau = J.u * tot;
-    const unsigned int cross = __ballot_sync(0xffffffffu, incl > tau && hi > lo);
-    int G = -1;
+    // the crossing chunk: the first whose running total passes tau
+    int C = -1;
     float before = 0.0f;
-    if (cross) {
-        const int L = __ffs(cross) - 1;
-        if (lane == L) {
-            float run = incl - ls;
-            for (int q = lo; q < hi; ++q) {
-                const float x = __ldcg(w + q);
-                if (run + x > tau) {
-                    G = q;
-                    before = run;
-                    break;
+    {
+        float run = 0.0f;
+        for (int c = 0; c < nch; ++c) {
+            const float x = ctot[warp][c];
+            if (run + x > tau) {
+                C = c;
+                break;
+            }
+            run += x;
+        }
+        if (C < 0) {  // rounding: the last chunk with positive weight
+            run = 0.0f;
+            float lastrun = 0.0f;
+            for (int c = 0; c < nch; ++c) {
+                const float x = ctot[warp][c];
+                if (x > 0.0f) {
+                    C = c;
+                    lastrun = run;
                 }
                 run += x;
             }
-            if (G < 0) {  // rounding inside the lane's range: its last positive group
-                run = incl - ls;
-                for (int q = lo; q < hi; ++q) {
-                    const float x = __ldcg(w + q);
-                    if (x > 0.0f) {
-                        G = q;
-                        before = run;
-                    }
-                    run += x;
-                }
-            }
+            run = lastrun;
+            if (C < 0)
+                C = 0;
         }
-        G = __shfl_sync(0xffffffffu, G, L);
-        before = __shfl_sync(0xffffffffu, before, L);
+        before = run;
     }
-    if (G < 0) {  // no lane crossed (rounding): the last group with positive weight
-        int lastq = -1;
-        for (int q = lo; q < hi; ++q)
-            if (__ldcg(w + q) > 0.0f)
-                lastq = q;
-        const unsigned int has = __ballot_sync(0xffffffffu, lastq >= 0);
-        const int L = has ? (31 - __clz(has)) : 0;
-        G = __shfl_sync(0xffffffffu, lastq, L);
-        if (G < 0)
-            G = 0;
-        // the prefix before G: the sum of the groups before it
-        float pre = 0.0f;
-        for (int q = lo; q < hi; ++q)
-            if (q < G)
-                pre += __ldcg(w + q);
+    // within the chunk: lanes in order, then the lane's four groups
+    int G;
+    {
+        const float4 v = group4(w, C);
+        const float s4 = ((v.x + v.y) + v.z) + v.w;
+        float incl = s4;
 #pragma unroll
-        for (int o = 16; o > 0; o >>= 1)
-            pre += __shfl_xor_sync(0xffffffffu, pre, o);
-        before = pre;
+        for (int o = 1; o < 32; o <<= 1) {
+            const float y = __shfl_up_sync(0xffffffffu, incl, o);
+            if (lane >= o)
+                incl += y;
+        }
+        const unsigned int cross = __ballot_sync(0xffffffffu, before + incl > tau);
+        const unsigned int posm = __ballot_sync(0xffffffffu, s4 > 0.0f);
+        const int L = cross ? (__ffs(cross) - 1) : (posm ? (31 - __clz(posm)) : 0);
+        float run = before + __shfl_sync(0xffffffffu, incl - s4, L);
+        const float4 vl = make_float4(__shfl_sync(0xffffffffu, v.x, L),
+                                      __shfl_sync(0xffffffffu, v.y, L),
+                                      __shfl_sync(0xffffffffu, v.z, L),
+                                      __shfl_sync(0xffffffffu, v.w, L));
+        const float e4[4] = {vl.x, vl.y, vl.z, vl.w};
+        int gi = -1, lastpos = -1;
+        float runpos = run;
+        for (int e = 0; e < 4; ++e) {
+            if (e4[e] > 0.0f) {
+                lastpos = e;
+                runpos = run;
+            }
+            if (gi < 0 && run + e4[e] > tau) {
+                gi = e;
+                break;
+            }
+            run += e4[e];
+        }
+        if (gi < 0) {  // rounding inside the lane's groups: its last positive one
+            gi = lastpos >= 0 ? lastpos : 0;
+            run = runpos;
+        }
+        G = C * 128 + L * 4 + gi;
+        before = run;
     }
+    if (G >= ng)
+        G = ng - 1;
 
-    // the group's 32 logits again: lane x of the group, t = h . W[x]
+    // the group's 32 logits again, t(x) = h . W[x]: the warp reads each of
+    // the 32 rows of W coalesced (lane l takes the 16-byte pieces l, l+32, ...),
+    // sums its products in order and the lanes' sums are added by a butterfly;
+    // lane r keeps row r's logit
     const int x = G * GROUP + lane;
     float t = -INFINITY;
-    if (x < P.V) {
+    {
         const uint4 *hv = reinterpret_cast<const uint4 *>(P.hdraw + (size_t)b * P.d);
-        const uint4 *wv = reinterpret_cast<const uint4 *>(P.lm_head + (size_t)x * P.d);
-        float acc = 0.0f;
-        for (int q = 0; q < P.d / 8; ++q) {
-            const uint4 h4 = __ldcg(hv + q), w4 = __ldg(wv + q);
-            const uint32_t hw[4] = {h4.x, h4.y, h4.z, h4.w}, ww[4] = {w4.x, w4.y, w4.z, w4.w};
+        const int nq = P.d / 8;  // 16-byte pieces per row
+        for (int r0 = 0; r0 < 32; r0 += 4) {
+            float acc[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+            for (int q = lane; q < nq; q += 32) {
+                const uint4 h4 = __ldcg(hv + q);
+                const uint32_t hw[4] = {h4.x, h4.y, h4.z, h4.w};
 #pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                acc = fmaf(__uint_as_float(hw[e] << 16), __uint_as_float(ww[e] << 16), acc);
-                acc = fmaf(__uint_as_float(hw[e] & 0xffff0000u),
-                           __uint_as_float(ww[e] & 0xffff0000u), acc);
+                for (int r = 0; r < 4; ++r) {
+                    const int xr = min(G * GROUP + r0 + r, P.V - 1);  // rows past V: unused
+                    const uint4 w4 = __ldg(reinterpret_cast<const uint4 *>(
+                                               P.lm_head + (size_t)xr * P.d) + q);
+                    const uint32_t ww[4] = {w4.x, w4.y, w4.z, w4.w};
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        acc[r] = fmaf(__uint_as_float(hw[e] << 16),
+                                      __uint_as_float(ww[e] << 16), acc[r]);
+                        acc[r] = fmaf(__uint_as_float(hw[e] & 0xffff0000u),
+                                      __uint_as_float(ww[e] & 0xffff0000u), acc[r]);
+                    }
+                }
+            }
+#pragma unroll
+            for (int r = 0; r < 4; ++r) {
+#pragma unroll
+                for (int o = 16; o > 0; o >>= 1)
+                    acc[r] += __shfl_xor_sync(0xffffffffu, acc[r], o);
+                if (lane == r0 + r && x < P.V)
+                    t = acc[r];
             }
         }
-        t = acc;
     }
     float wx = 0.0f;
     if (x < P.V) {
@@ -959,7 +1075,7 @@ Layout layout(int32_t B, int32_t k, int32_t V, int32_t d, int32_t ddt)
 
 struct DevInfo {
     int sms = 0;
-    bool attr[3] = {false, false, false};
+    bool attr[4] = {false, false, false, false};
 };
 DevInfo g_dev[64];
 
@@ -1120,7 +1236,8 @@ int verify_lmhead(const void *hidden, const void *lm_head, const void *draft,
     Gd.k = k;
     Gd.draft = draft;
     Gd.draft_dtype = ddt;
-    rc = launch_gemm<MODE_DRAW>(md, mw, Gd, B, V, d, st, false);
+    rc = (ddt == SPEC_F32) ? launch_gemm<MODE_DRAW_F32>(md, mw, Gd, B, V, d, st, false)
+                           : launch_gemm<MODE_DRAW_BF16>(md, mw, Gd, B, V, d, st, false);
     if (rc != SPEC_OK)
         return rc;
     mark(3);
