@@ -51,6 +51,8 @@ CSRC = os.path.join(ROOT, "speculative_decoding_verification_65_gb300", "csrc")
 KERNEL_SRCS = {
     "stats_kernel": [os.path.join(CSRC, "spec_verify.cu"), os.path.join(CSRC, "device_common.cuh")],
     "chunk_kernel": [os.path.join(CSRC, "spec_sample.cu"), os.path.join(CSRC, "device_common.cuh")],
+    "filter_kernel": [os.path.join(CSRC, "spec_verify.cu"), os.path.join(CSRC, "device_common.cuh")],
+    "gemm_kernel": [os.path.join(CSRC, "spec_lmhead.cu"), os.path.join(CSRC, "device_common.cuh")],
 }
 SAMPLE_METRIC = "sampled tokens/sec"
 SAMPLE_UNIT = "tokens/s"
@@ -649,7 +651,9 @@ def run_ours_filtered(args):
                    "l2": "inputs larger than L2 (no flush)", "parallelism": f"dp{world}"},
         "gpu_launches": sv.SPEC_FILTERED_STAGES * args.steps,
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
-                     "frac": achieved / peak, "traffic": None,
+                     "frac": achieved / peak,
+                     "traffic": recorded_traffic(f"{workload}_top{args.top_k}_p{args.top_p}",
+                                                 "filter_kernel"),
                      "peak_source": f"{peak_src} copy bandwidth (MEASURED_PEAKS.json hbm_gbs)"
                      if peak_src == "measured" else "fallback 6.8 TB/s",
                      "kernel": "filter_kernel (top-k / top-p cut per row, one read of "
@@ -1048,7 +1052,8 @@ def run_ours_lmhead(args):
                    "parallelism": f"dp{world}"},
         "gpu_launches": sv.SPEC_LMHEAD_STAGES * args.steps,
         "roofline": {"bound": "tensor", "achieved": tflops, "peak": peak, "unit": "TFLOP/s",
-                     "frac": tflops / peak, "traffic": None,
+                     "frac": tflops / peak,
+                     "traffic": recorded_traffic(lmhead_name(B, k, V, d), "gemm_kernel"),
                      "peak_source": (f"measured cuBLAS bf16 (MEASURED_PEAKS.json {which}; "
                                      f"SM clock median {cs.get('sm_mhz')} MHz)")
                      if peak_src == "measured" else f"fallback for {which}",
