@@ -51,7 +51,7 @@ CSRC = os.path.join(ROOT, "speculative_decoding_verification_65_gb300", "csrc")
 KERNEL_SRCS = {
     "stats_kernel": [os.path.join(CSRC, "spec_verify.cu"), os.path.join(CSRC, "device_common.cuh")],
     "chunk_kernel": [os.path.join(CSRC, "spec_sample.cu"), os.path.join(CSRC, "device_common.cuh")],
-    "filter_kernel": [os.path.join(CSRC, "spec_verify.cu"), os.path.join(CSRC, "device_common.cuh")],
+    "wfilter_kernel": [os.path.join(CSRC, "spec_verify.cu"), os.path.join(CSRC, "device_common.cuh")],
     "gemm_kernel": [os.path.join(CSRC, "spec_lmhead.cu"), os.path.join(CSRC, "device_common.cuh")],
 }
 SAMPLE_METRIC = "sampled tokens/sec"
@@ -653,11 +653,12 @@ def run_ours_filtered(args):
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak,
                      "traffic": recorded_traffic(f"{workload}_top{args.top_k}_p{args.top_p}",
-                                                 "filter_kernel"),
+                                                 "wfilter_kernel"),
                      "peak_source": f"{peak_src} copy bandwidth (MEASURED_PEAKS.json hbm_gbs)"
                      if peak_src == "measured" else "fallback 6.8 TB/s",
-                     "kernel": "filter_kernel (top-k / top-p cut per row, one read of "
-                               "each filtered row)",
+                     "kernel": "wfilter_kernel + filter_kernel (top-k / top-p cut per row: "
+                               "one read of each filtered row; the second kernel only "
+                               "finishes rows the first flags)",
                      "algorithmic_bytes_per_launch": filt_bytes,
                      "kernel_timing": "CUDA events after each kernel, K further steps",
                      "step_GBps": alg_bytes / (ms_per_step / 1e3) / 1e9,

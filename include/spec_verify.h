@@ -160,10 +160,10 @@ int32_t spec_verify_probs(const void *target_logits, const void *draft_logits,
  *          Q = q~_i(g_i) (NaN for greedy and error sequences)
  * A draft token outside the draft's kept set (q~(g) = 0) is a sequence error.
  * Other arguments, the workspace (spec_verify_workspace_size) and errors as
- * spec_verify.  Five kernels run: statistics, filter (per row, the end of the
- * kept set: one streaming pass over the row in the common case, a radix
- * search over the order key otherwise), accept scan, draw tiles, final
- * search.
+ * spec_verify.  Six kernels run: statistics; the filter in two (per row,
+ * the end of the kept set: one streaming pass over the row in the common
+ * case, then the rows it could not cut, by a second pass or a radix search
+ * over the order key); accept scan; draw tiles; final search.
  */
 int32_t spec_verify_filtered(const void *target_logits, const void *draft_logits,
                              const int32_t *draft_tokens, const float *u_accept,
@@ -174,9 +174,9 @@ int32_t spec_verify_filtered(const void *target_logits, const void *draft_logits
                              void *workspace, size_t workspace_bytes, void *stream);
 
 /*
- * spec_verify_filtered with stage events as in spec_verify_timed, one per
- * kernel: SPEC_FILTERED_STAGES of them (statistics, filter, accept scan, draw
- * tiles, final search).
+ * spec_verify_filtered with stage events as in spec_verify_timed:
+ * SPEC_FILTERED_STAGES of them, after the statistics, the filter (both of
+ * its kernels), the accept scan, the draw tiles and the final search.
  */
 #define SPEC_FILTERED_STAGES 5
 int32_t spec_verify_filtered_timed(const void *target_logits, const void *draft_logits,

@@ -286,8 +286,9 @@ def spec_verify_filtered(target, draft, tokens, u_accept, u_resample, temperatur
 def spec_verify_filtered_timed(target, draft, tokens, u_accept, u_resample, temperature,
                                top_k, top_p, out_tokens, out_num_accepted, ws, stage_events,
                                stream=None):
-    """spec_verify_filtered recording SPEC_FILTERED_STAGES events, one after
-    each kernel (statistics, filter, accept scan, draw tiles, final search)."""
+    """spec_verify_filtered recording SPEC_FILTERED_STAGES events: after the
+    statistics, the filter (both of its kernels), the accept scan, the draw
+    tiles and the final search."""
     B, k, V, dt = _marshal(target, draft, tokens, u_accept, u_resample, temperature)
     _filters(B, target.device, top_k, top_p)
     handles = (ctypes.c_void_p * SPEC_FILTERED_STAGES)(

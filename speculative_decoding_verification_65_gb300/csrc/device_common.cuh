@@ -20,8 +20,9 @@ constexpr unsigned long long WAIT_NS = 2000000000ull;  // 2 s bound on any wait
 // First 256 bytes of every workspace: the device status word (SPEC_DEV_*).
 struct WsHeader {
     int status;
-    unsigned int next_item;  // row counter of the filter kernel (zeroed by the first kernel)
-    unsigned int pad[62];
+    unsigned int next_item;   // row counter of the window filter kernel (zeroed by the first kernel)
+    unsigned int next_item2;  // chunk counter of the radix filter kernel (likewise)
+    unsigned int pad[61];
 };
 static_assert(sizeof(WsHeader) == 256, "header is 256 bytes");
 

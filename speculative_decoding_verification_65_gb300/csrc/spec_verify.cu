@@ -95,7 +95,9 @@ struct alignas(16) FiltRec {
     float zt;            // mass of the kept set, relative to the row maximum
     int flags;           // FILT_OFF, FILT_ON, FILT_ERR
 };
-enum { FILT_OFF = 0, FILT_ON = 1, FILT_ERR = 2 };
+enum { FILT_OFF = 0, FILT_ON = 1, FILT_ERR = 2, FILT_RADIX = 3 };  // RADIX: the window
+                                                                   // kernel left the row to
+                                                                   // the radix search
 
 // Order-preserving unsigned key of an fp32 bit pattern (bf16 values widen
 // exactly, so their keys order the same way).
@@ -278,8 +280,10 @@ __global__ void __launch_bounds__(NTHREADS, 2) stats_kernel(const Params P)
     constexpr int SEG = TILE_BYTES / L::ES;
 
     if (tid == 0) {
-        if (blockIdx.x == 0)
-            P.hdr->next_item = 0u;  // the filter kernel's row counter (it runs after this grid)
+        if (blockIdx.x == 0) {  // the filter kernels' counters (they run after this grid)
+            P.hdr->next_item = 0u;
+            P.hdr->next_item2 = 0u;
+        }
         for (int s = 0; s < STAGES; ++s) {
             mbar_init(&S.full[s], 1);
             mbar_init(&S.empty[s], NCW);
@@ -603,19 +607,41 @@ __global__ void __launch_bounds__(FTH, 2) filter_kernel(const Params P)
     allow_next_kernel();
     wait_previous_kernel();  // partials come from the statistics kernel
 
-    // rows are handed out one at a time (row cost varies: a few take the
-    // radix search): each CTA's first row is its index, the next come from
-    // the header counter, which the statistics kernel zeroed
+    // This kernel finishes the rows the window kernel recorded FILT_RADIX
+    // (its buffer overflowed, or its window ended short of the cut).  Rows
+    // are taken in chunks of up to 32 from the second header counter (zeroed
+    // by the statistics kernel), small enough that each CTA gets several;
+    // a chunk's flags are read by one warp.
+    const int chunk = max(1, min(32, items / ((int)gridDim.x * 8)));
+    unsigned int fmask = 0u;
+    int fbase = 0;
     auto next_item = [&]() -> int {
-        __syncthreads();
-        if (t == 0)
-            S.found = (int)gridDim.x + (int)atomicAdd(&P.hdr->next_item, 1u);
-        __syncthreads();
-        const int nx = S.found;
-        __syncthreads();
-        return nx;
+        for (;;) {
+            if (fmask) {
+                const int i = __ffs(fmask) - 1;
+                fmask &= fmask - 1u;
+                return fbase + i;
+            }
+            __syncthreads();
+            if (t == 0)
+                S.found = (int)atomicAdd(&P.hdr->next_item2, (unsigned int)chunk);
+            __syncthreads();
+            fbase = S.found;
+            if (fbase >= items)
+                return items;
+            if (warp == 0) {
+                const int it = fbase + lane;
+                const bool f = lane < chunk && it < items &&
+                               __ldcg(&P.filt[it].flags) == FILT_RADIX;
+                const unsigned int bm = __ballot_sync(0xffffffffu, f);
+                if (lane == 0)
+                    S.sel = (int)bm;
+            }
+            __syncthreads();
+            fmask = (unsigned int)S.sel;
+        }
     };
-    for (int item = blockIdx.x; item < items && !failed; item = next_item()) {
+    for (int item = next_item(); item < items && !failed; item = next_item()) {
         const int b = item / P.rows, rsq = item - b * P.rows;
         const bool is_target = rsq <= P.k;
         const void *arr = is_target ? P.target : P.draft;
@@ -1433,6 +1459,655 @@ __global__ void __launch_bounds__(FTH, 2) filter_kernel(const Params P)
     }
 }
 
+// ------------------------------------ top-k / top-p: the one-pass window kernel
+//
+// The common case of the filter, warp-specialized like the statistics kernel:
+// a producer warp deals rows (the header counter) and streams each filtered
+// row through a ring of 16 KB bulk copies without stopping between rows;
+// eight consumer warps each take a contiguous 2 KB of every tile into
+// registers, free the slot, and gather the row's window tokens (the
+// adaptive window of filter_kernel, described there).  Each warp narrows its
+// own copy of the window from the shared histogram: counts only grow, so the
+// bin it reads as the cut's is never below the row's final one, and every
+// token of the bins through the final cut is gathered by every warp.  Block
+// work (the cut from the sorted window) is done once per row between named
+// barriers of the consumer warps.  A row whose buffer overflowed, or whose
+// window ended short of the cut, is recorded FILT_RADIX and finished by
+// filter_kernel.
+constexpr int WCW = 8;                            // consumer warps
+constexpr int WPW = WCW;                          // the producer's warp
+constexpr int WTH = (WCW + 1) * 32;
+constexpr int WSLOTS = 4;
+constexpr int WVPL = FTILE / (16 * 32 * WCW);     // 16-byte vectors per lane per tile
+static_assert(WVPL * 16 * 32 * WCW == FTILE, "a window tile splits evenly over the consumers");
+static_assert(WCW * 32 == FTH, "the consumers are the filter's thread count");
+enum { WKIND_ROW = 1, WKIND_END = 2 };
+
+struct WTile {
+    int kind;
+    int item;          // the row (sequence * rows + row in sequence)
+    int e0, e1;        // elements of the row in the slot
+    int phase0, ncopied;
+    int first, last;   // first / last tile of the row
+};
+
+struct WSmem {
+    uint8_t ring[WSLOTS][FSLOT_BYTES];
+    unsigned long long full[WSLOTS];
+    unsigned long long empty[WSLOTS];
+    WTile tile[WSLOTS];
+    unsigned long long ckey[FCAP], cmass[FCAP];  // the window's tokens
+    unsigned long long rkey[FCAP], rmass[FCAP];  // compaction / sort output
+    unsigned int fh_cnt[WBINS];
+    unsigned long long fh_mass[WBINS];
+    unsigned int ncand;
+    int overflow;
+    unsigned int wcnt[WCW];
+    int wnb;
+    unsigned int wcum;
+    int sel;
+    unsigned long long acc;
+    unsigned long long cbar;  // the consumers' barrier (every consumer thread arrives)
+    int abort_flag;
+};
+constexpr size_t WFILT_SMEM = sizeof(WSmem);
+
+template <int DT>
+__global__ void __launch_bounds__(WTH, 2) wfilter_kernel(const Params P)
+{
+    using L = Lg<DT>;
+    constexpr int VEC = L::VEC;
+    constexpr int TE = FTILE / L::ES;  // elements per tile
+    extern __shared__ __align__(16) uint8_t wsm_raw[];
+    WSmem &S = *reinterpret_cast<WSmem *>(wsm_raw);
+    volatile int *abort_flag = &S.abort_flag;
+    const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
+    const int V = P.V;
+    const int items = P.B * P.rows;
+    const int ntiles = (V + TE - 1) / TE;
+    if (t == 0) {
+        for (int q = 0; q < WSLOTS; ++q) {
+            mbar_init(&S.full[q], 1);
+            mbar_init(&S.empty[q], WCW);
+        }
+        mbar_init(&S.cbar, WCW * 32);
+        S.abort_flag = 0;
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+    }
+    __syncthreads();
+    allow_next_kernel();
+    wait_previous_kernel();  // the partials and the zeroed row counter
+
+    if (warp == WPW) {
+        // ---------------------------------------------------------- producer
+        if (lane != 0)
+            return;
+        int stage = 0;
+        uint32_t phase = 0;
+        uint32_t issued = 0u, issued_phase = 0u;
+        bool ok = true;
+        for (int item = blockIdx.x; item < items && ok;
+             item = (int)gridDim.x + (int)atomicAdd(&P.hdr->next_item, 1u)) {
+            const int b = item / P.rows, rsq = item - b * P.rows;
+            const float T = __ldg(P.temperature + b);
+            const int K = P.top_k ? __ldg(P.top_k + b) : 0;
+            const float Pp = P.top_p ? __ldg(P.top_p + b) : 1.0f;
+            const bool topk = K > 0 && K < V;
+            const bool topp = Pp < 1.0f;
+            const bool bad = K < 0 || isnan(Pp) || !(Pp > 0.0f);
+            if (!temperature_valid(T) || T == 0.0f || (!topk && !topp) || bad) {
+                FiltRec out;
+                out.kappa = 0u;
+                out.iota = INT_MAX;
+                out.zt = 0.0f;
+                // bad filter parameters fail the sequence, greedy too; greedy,
+                // invalid and unfiltered rows keep everything
+                out.flags = (temperature_valid(T) && bad) ? FILT_ERR : FILT_OFF;
+                P.filt[item] = out;
+                continue;
+            }
+            const bool is_target = rsq <= P.k;
+            const uint8_t *arr = reinterpret_cast<const uint8_t *>(is_target ? P.target : P.draft);
+            const size_t row = is_target ? (size_t)b * (P.k + 1) + rsq
+                                         : (size_t)b * P.k + (rsq - P.k - 1);
+            const unsigned long long arr_bytes = is_target ? P.target_bytes : P.draft_bytes;
+            for (int i = 0; i < ntiles; ++i) {
+                if (*abort_flag || !mbar_wait(&S.empty[stage], phase ^ 1u)) {
+                    ok = false;
+                    break;
+                }
+                const int e0 = i * TE, e1 = min(V, e0 + TE);
+                const unsigned long long start = ((unsigned long long)row * V + e0) * L::ES;
+                const unsigned long long end = ((unsigned long long)row * V + e1) * L::ES;
+                const unsigned long long a0 = start & ~15ull;
+                unsigned long long a1 = (end + 15) & ~15ull;
+                if (a1 > (arr_bytes & ~15ull))
+                    a1 = arr_bytes & ~15ull;
+                const uint32_t bytes = (a1 > a0) ? (uint32_t)(a1 - a0) : 0u;
+                WTile &ti = S.tile[stage];
+                ti.kind = WKIND_ROW;
+                ti.item = item;
+                ti.e0 = e0;
+                ti.e1 = e1;
+                ti.phase0 = (int)(start - a0);
+                ti.ncopied = (int)bytes;
+                ti.first = (i == 0) ? 1 : 0;
+                ti.last = (i == ntiles - 1) ? 1 : 0;
+                asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+                if (bytes) {
+                    mbar_arrive_expect_tx(&S.full[stage], bytes);
+                    bulk_copy_g2s(S.ring[stage], arr + a0, bytes, &S.full[stage]);
+                    issued |= 1u << stage;
+                    issued_phase = (issued_phase & ~(1u << stage)) | (phase << stage);
+                } else {
+                    mbar_arrive(&S.full[stage]);
+                }
+                if (++stage == WSLOTS) {
+                    stage = 0;
+                    phase ^= 1u;
+                }
+            }
+        }
+        if (ok) {  // the end marker
+            if (!*abort_flag && mbar_wait(&S.empty[stage], phase ^ 1u)) {
+                S.tile[stage].kind = WKIND_END;
+                mbar_arrive(&S.full[stage]);
+            } else {
+                ok = false;
+            }
+        }
+        if (!ok) {
+            atomicExch(&P.hdr->status, SPEC_DEV_WAIT_TIMEOUT);
+            *abort_flag = 1;
+            for (int q = 0; q < WSLOTS; ++q)  // the copies in flight land first (bounded)
+                if ((issued >> q) & 1u)
+                    (void)mbar_wait(&S.full[q], (issued_phase >> q) & 1u);
+        }
+        return;
+    }
+
+    // -------------------------------------------------------------- consumers
+    const int vwarp = warp * 32 * WVPL;  // this warp's first vector of a tile
+    int stage = 0;
+    uint32_t phase = 0;
+    // the current row (the same in every warp)
+    int item = -1;
+    float m = 0.0f, c = 0.0f, Pp = 1.0f;
+    int K = 0, nbw0 = -1, nbw = -1;  // nbw: this warp's window (bins 0..nbw)
+    bool topk = false, topp = false, need_mass = false, row_bad = false;
+    unsigned long long Zrow = 0ull, target0 = 0ull;
+    unsigned int kmin = 1u, last_nc = 0u;
+    // The consumers' barrier is an mbarrier every consumer thread arrives at
+    // and waits on with the bounded wait, so a warp that gave up on a copy
+    // makes the others give up too instead of stopping them for good.  A
+    // thread that gave up (dead) skips the rest; the verdict is per warp.
+    uint32_t cphase = 0u;
+    bool dead = false;
+    auto cbar = [&]() {
+        if (dead)
+            return;
+        mbar_arrive(&S.cbar);
+        const bool ok = __all_sync(0xffffffffu, mbar_wait(&S.cbar, cphase));
+        cphase ^= 1u;
+        if (!ok) {
+            dead = true;
+            if (lane == 0) {
+                atomicExch(&P.hdr->status, SPEC_DEV_WAIT_TIMEOUT);
+                *abort_flag = 1;
+            }
+        }
+    };
+    // exclusive prefix over the consumer threads (index order = thread order)
+    auto block_scan = [&](unsigned int x, unsigned int &total) -> unsigned int {
+        unsigned int incl = x;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const unsigned int y = __shfl_up_sync(0xffffffffu, incl, o);
+            if (lane >= o)
+                incl += y;
+        }
+        if (lane == 31)
+            S.wcnt[warp] = incl;
+        cbar();
+        unsigned int wbase = 0, tot = 0;
+        for (int w = 0; w < WCW; ++w) {
+            const unsigned int v = S.wcnt[w];
+            if (w < warp)
+                wbase += v;
+            tot += v;
+        }
+        cbar();
+        total = tot;
+        return wbase + incl - x;
+    };
+
+    auto wbin = [&](float x) {
+        const float dd = (m - x) * c;
+        return (dd < (float)(WBINS / 2)) ? (int)(dd * 2.0f) : WBINS;
+    };
+    auto val_of_key = [&](unsigned int key) {
+        unsigned int bits = (key & 0x80000000u) ? (key & 0x7fffffffu) : ~key;
+        if (DT == SPEC_BF16)
+            bits &= 0xffff0000u;
+        return __uint_as_float(bits);
+    };
+    // this warp's reading of the first bin (<= lim) whose counts (masses)
+    // reach the cut, and the count through it; -1 if none
+    auto warp_bk = [&](int lim, unsigned int &cum_out) -> int {
+        volatile unsigned int *fc = S.fh_cnt;
+        volatile unsigned long long *fm = S.fh_mass;
+        const int b0 = 2 * lane, b1 = b0 + 1;
+        const unsigned int c0 = (b0 <= lim) ? fc[b0] : 0u;
+        const unsigned int c1 = (b1 <= lim) ? fc[b1] : 0u;
+        const unsigned long long m0 = (need_mass && b0 <= lim) ? fm[b0] : 0ull;
+        const unsigned long long m1 = (need_mass && b1 <= lim) ? fm[b1] : 0ull;
+        unsigned int ci = c0 + c1;
+        unsigned long long mi = m0 + m1;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const unsigned int y = __shfl_up_sync(0xffffffffu, ci, o);
+            const unsigned long long ym = __shfl_up_sync(0xffffffffu, mi, o);
+            if (lane >= o) {
+                ci += y;
+                mi += ym;
+            }
+        }
+        const unsigned int ce0 = ci - c1;
+        const unsigned long long me0 = mi - m1;
+        auto hits = [&](unsigned int cc, unsigned long long mm) {
+            return topk ? cc >= (unsigned int)K : mm >= target0;
+        };
+        const bool h0 = b0 <= lim && hits(ce0, me0);
+        const bool h1 = b1 <= lim && hits(ci, mi);
+        const unsigned int hb = __ballot_sync(0xffffffffu, h0 || h1);
+        if (!hb) {
+            cum_out = 0u;
+            return -1;
+        }
+        const int L0 = __ffs(hb) - 1;
+        const bool first0 = __shfl_sync(0xffffffffu, h0, L0);
+        cum_out = __shfl_sync(0xffffffffu, first0 ? ce0 : ci, L0);
+        return first0 ? 2 * L0 : 2 * L0 + 1;
+    };
+
+    for (;;) {
+        if (dead)
+            break;
+        int ok = 1;
+        if (lane == 0)
+            ok = mbar_wait(&S.full[stage], phase) ? 1 : 0;
+        ok = __shfl_sync(0xffffffffu, ok, 0);
+        if (!ok) {
+            if (lane == 0) {
+                atomicExch(&P.hdr->status, SPEC_DEV_WAIT_TIMEOUT);
+                *abort_flag = 1;
+            }
+            break;
+        }
+        (void)mbar_try_wait(&S.full[stage], phase);  // acquire the landed bytes
+        const WTile ti = S.tile[stage];
+        if (ti.kind == WKIND_END)
+            break;
+        if (ti.first) {
+            // a new row: its parameters (each warp computes the same values)
+            item = ti.item;
+            const int b = item / P.rows, rsq = item - b * P.rows;
+            const float T = __ldg(P.temperature + b);
+            K = P.top_k ? __ldg(P.top_k + b) : 0;
+            Pp = P.top_p ? __ldg(P.top_p + b) : 1.0f;
+            topk = K > 0 && K < V;
+            topp = Pp < 1.0f;
+            need_mass = !topk;
+            c = LOG2E / T;
+            const float4 *pp = P.part + ((size_t)b * P.rows + rsq) * P.NSS;
+            float mm = -INFINITY;
+            for (int q = lane; q < P.NSS; q += 32)
+                mm = fmax_nan(mm, __ldcg(pp + q).x);
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1)
+                mm = fmax_nan(mm, __shfl_xor_sync(0xffffffffu, mm, o));
+            float z = 0.0f;
+            for (int q = lane; q < P.NSS; q += 32) {
+                const float4 pv = __ldcg(pp + q);
+                z += rescale(pv.y, pv.x, mm, c);
+            }
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1)
+                z += __shfl_xor_sync(0xffffffffu, z, o);
+            m = mm;
+            row_bad = isnan(m) || isinf(m);  // the scan reports the row as an error
+            Zrow = (unsigned long long)((double)z * 1099511627776.0);
+            target0 = topk ? 0ull : (unsigned long long)((double)Pp * (double)Zrow);
+            const float zrow = (float)((double)Zrow * (1.0 / 1099511627776.0));
+            const int Dg = (int)floorf(log2f((float)FCAP / (fmaxf(zrow, 1.0f) * 1.01f))) + 8;
+            nbw0 = nbw = row_bad ? -1 : 2 * min(WBINS / 2, max(1, Dg)) - 1;
+            kmin = topk ? (unsigned int)K : 1u;
+            last_nc = 0u;
+            if (t == 0) {
+                S.ncand = 0u;
+                S.overflow = 0;
+            }
+            if (t < WBINS) {
+                S.fh_cnt[t] = 0u;
+                S.fh_mass[t] = 0ull;
+            }
+            cbar();  // the previous row's cut is done; the window state is reset
+        }
+        // this warp's 2 KB of the tile into registers, then the slot is free
+        const Seg g = make_seg<DT>(S.ring[stage], nullptr, 0, V, ti.e0, ti.e1, ti.phase0,
+                                   ti.ncopied);
+        const int vt0 = ti.e0 / VEC;
+        uint4 raw[WVPL];
+        if (g.fast && ti.e1 - ti.e0 == TE) {
+#pragma unroll
+            for (int u = 0; u < WVPL; ++u)
+                raw[u] = ld_shared_v4(S.ring[stage] + (size_t)(vwarp + lane + 32 * u) * 16);
+        } else {
+            // the row's array is only read for bytes the copy left out (none
+            // when the row is 16-byte aligned)
+            const bool is_t = (item % P.rows) <= P.k;
+            const int bq = item / P.rows, rq = item - bq * P.rows;
+            const size_t rrow = is_t ? (size_t)bq * (P.k + 1) + rq : (size_t)bq * P.k + (rq - P.k - 1);
+            const Seg g2 = make_seg<DT>(S.ring[stage], is_t ? P.target : P.draft, rrow, V, ti.e0,
+                                        ti.e1, ti.phase0, ti.ncopied);
+#pragma unroll
+            for (int u = 0; u < WVPL; ++u)
+                raw[u] = seg_vec<DT>(g2, vt0 + vwarp + lane + 32 * u);
+        }
+        __syncwarp();
+        if (lane == 0)
+            mbar_arrive(&S.empty[stage]);
+        if (++stage == WSLOTS) {
+            stage = 0;
+            phase ^= 1u;
+        }
+
+        // ---- the window gather (per lane marks, one slot reservation per warp).
+        // The vectors rotate through r0..r3 so that each loop below is one
+        // short body, not unrolled: the hot loop stays small enough for the
+        // instruction cache (four rotations bring them back in order).
+        // A row's first tile goes through twice: first its tokens inside the
+        // first window are only counted, and every warp narrows to the bin
+        // where those counts reach the cut (the counts of the whole row can
+        // only be larger, so the row's cut bin is not past it); then the
+        // tile's tokens inside that window are stored.  A wide first window
+        // on a flat row therefore does not flood the buffer.
+        if (!row_bad && !*(volatile int *)&S.overflow) {
+            const int npass = ti.first ? 2 : 1;
+#pragma unroll 1
+            for (int pass = 0; pass < npass; ++pass) {
+                const bool count_only = ti.first && pass == 0;
+                const bool count = !ti.first || pass == 0;
+                const int lim = count_only ? nbw0 : nbw;
+                uint4 r0 = raw[0], r1 = raw[1], r2 = raw[2], r3 = raw[3];
+                static_assert(WVPL == 4 && VEC <= 8, "four vectors of at most 8 tokens per lane");
+                uint32_t tball = 0u;  // 8 bits per vector: the tokens in the window
+                unsigned int cnt = 0u;
+#pragma unroll 1
+                for (int u = 0; u < WVPL; ++u) {
+                    uint32_t tb = 0u;
+                    if (wbin(L::vmax(r0)) <= lim) {  // else no token of the vector is in
+                        float x[VEC];
+                        L::unpack(r0, x);
+#pragma unroll
+                        for (int j = 0; j < VEC; ++j) {
+                            const int idx = (vt0 + vwarp + lane + 32 * u) * VEC + j;
+                            if (idx < V && wbin(x[j]) <= lim)
+                                tb |= 1u << j;
+                        }
+                    }
+                    tball |= tb << (8 * u);
+                    cnt += (unsigned int)__popc(tb);
+                    const uint4 rt = r0;
+                    r0 = r1;
+                    r1 = r2;
+                    r2 = r3;
+                    r3 = rt;
+                }
+                unsigned int pos = 0u;
+                bool any = true;
+                if (!count_only) {
+                    unsigned int incl = cnt;
+#pragma unroll
+                    for (int o = 1; o < 32; o <<= 1) {
+                        const unsigned int y = __shfl_up_sync(0xffffffffu, incl, o);
+                        if (lane >= o)
+                            incl += y;
+                    }
+                    const unsigned int wtot = __shfl_sync(0xffffffffu, incl, 31);
+                    any = wtot != 0u;
+                    if (any) {
+                        unsigned int base = 0u;
+                        if (lane == 31)
+                            base = atomicAdd(&S.ncand, wtot);
+                        base = __shfl_sync(0xffffffffu, base, 31);
+                        if (base + wtot > (unsigned int)FCAP && lane == 0)
+                            S.overflow = 1;  // tokens not stored: the radix search finishes the row
+                        pos = base + incl - cnt;
+                    }
+                }
+                if (any && tball) {
+#pragma unroll 1
+                    for (int u = 0; u < WVPL; ++u) {
+                        const uint32_t tb = (tball >> (8 * u)) & 0xffu;
+                        if (tb) {
+                            float x[VEC];
+                            L::unpack(r0, x);
+#pragma unroll
+                            for (int j = 0; j < VEC; ++j) {
+                                if ((tb >> j) & 1u) {
+                                    const bool keep = !count_only && pos < (unsigned int)FCAP;
+                                    const unsigned long long e =
+                                        (keep || (count && need_mass)) ? fixmass(x[j], m, c) : 0ull;
+                                    if (count) {
+                                        const int wb = wbin(x[j]);
+                                        atomicAdd(&S.fh_cnt[wb], 1u);
+                                        if (need_mass)
+                                            atomicAdd(&S.fh_mass[wb], e);
+                                    }
+                                    if (keep) {
+                                        const int idx = (vt0 + vwarp + lane + 32 * u) * VEC + j;
+                                        S.ckey[pos] = sortkey(key_of<DT>(x[j]), idx);
+                                        S.cmass[pos] = e;
+                                    }
+                                    ++pos;
+                                }
+                            }
+                        }
+                        const uint4 rt = r0;
+                        r0 = r1;
+                        r1 = r2;
+                        r2 = r3;
+                        r3 = rt;
+                    }
+                }
+                if (count_only) {
+                    cbar();  // every warp's counts of the first tile are in
+                    unsigned int cum0;
+                    const int bk0 = warp_bk(nbw0, cum0);
+                    if (bk0 >= 0 && bk0 < nbw)
+                        nbw = bk0;
+                }
+            }
+            // narrow this warp's window once the gathered count has doubled
+            const unsigned int nc = *(volatile unsigned int *)&S.ncand;
+            if (nc >= kmin && nc >= 2u * last_nc) {
+                last_nc = nc;
+                unsigned int cum;
+                const int bk = warp_bk(nbw, cum);
+                if (bk >= 0 && bk < nbw)
+                    nbw = bk;
+            }
+        }
+        if (!ti.last)
+            continue;
+
+        // ---- end of the row: the cut from the sorted window (all consumers)
+        cbar();  // every warp's tokens of the row are in
+        if (dead)
+            break;
+        FiltRec out;
+        out.kappa = 0u;
+        out.iota = INT_MAX;
+        out.zt = 0.0f;
+        out.flags = FILT_OFF;
+        if (!row_bad) {
+            unsigned int ncut = 0u;
+            const int bk = S.overflow ? -1 : warp_bk(nbw0, ncut);  // the same in every warp
+            if (bk < 0) {
+                out.flags = FILT_RADIX;
+            } else {
+                int n = (int)S.ncand;
+                const unsigned long long *sk = S.ckey, *sm = S.cmass;
+                if ((int)ncut < n) {
+                    // only the bins through the cut's (wider warps gathered more)
+                    constexpr int PER = FCAP / FTH;
+                    bool kp[PER];
+                    unsigned int cnt = 0u;
+#pragma unroll
+                    for (int q = 0; q < PER; ++q) {
+                        const int i = t * PER + q;
+                        kp[q] = i < n && wbin(val_of_key((unsigned int)(S.ckey[i] >> 32))) <= bk;
+                        cnt += kp[q] ? 1u : 0u;
+                    }
+                    unsigned int total;
+                    unsigned int o = block_scan(cnt, total);
+#pragma unroll
+                    for (int q = 0; q < PER; ++q) {
+                        const int i = t * PER + q;
+                        if (kp[q]) {
+                            S.rkey[o] = S.ckey[i];
+                            S.rmass[o] = S.cmass[i];
+                            ++o;
+                        }
+                    }
+                    cbar();
+                    n = (int)total;
+                    sk = S.rkey;
+                    sm = S.rmass;
+                }
+                // sort descending by (key, -index): the ranking
+                unsigned long long *dk, *dm;
+                if (n <= FCAP / 2) {
+                    // rank placement (keys are unique) into the other buffer
+                    dk = (sk == S.ckey) ? S.rkey : S.ckey;
+                    dm = (sk == S.ckey) ? S.rmass : S.cmass;
+                    constexpr int PER2 = FCAP / 2 / FTH;
+                    unsigned long long mine[PER2], mm[PER2];
+                    int rk[PER2];
+#pragma unroll
+                    for (int q = 0; q < PER2; ++q) {
+                        const int i = t + q * FTH;
+                        mine[q] = (i < n) ? sk[i] : 0ull;
+                        mm[q] = (i < n) ? sm[i] : 0ull;
+                        rk[q] = 0;
+                    }
+                    for (int jj = 0; jj < n; ++jj) {
+                        const unsigned long long kj = sk[jj];
+#pragma unroll
+                        for (int q = 0; q < PER2; ++q)
+                            rk[q] += (kj > mine[q]) ? 1 : 0;
+                    }
+#pragma unroll
+                    for (int q = 0; q < PER2; ++q) {
+                        const int i = t + q * FTH;
+                        if (i < n) {
+                            dk[rk[q]] = mine[q];
+                            dm[rk[q]] = mm[q];
+                        }
+                    }
+                    cbar();
+                } else {
+                    // bitonic, in place, padded to a power of two
+                    dk = const_cast<unsigned long long *>(sk);
+                    dm = const_cast<unsigned long long *>(sm);
+                    int p2 = 1;
+                    while (p2 < n)
+                        p2 <<= 1;
+                    for (int i = n + t; i < p2; i += FTH) {
+                        dk[i] = 0ull;
+                        dm[i] = 0ull;
+                    }
+                    cbar();
+                    for (int kk = 2; kk <= p2; kk <<= 1) {
+                        for (int jj = kk >> 1; jj > 0; jj >>= 1) {
+                            for (int i = t; i < p2; i += FTH) {
+                                const int ixj = i ^ jj;
+                                if (ixj > i) {
+                                    const unsigned long long a = dk[i], bq = dk[ixj];
+                                    const bool desc = (i & kk) == 0;
+                                    if (desc ? (a < bq) : (a > bq)) {
+                                        dk[i] = bq;
+                                        dk[ixj] = a;
+                                        const unsigned long long ma = dm[i];
+                                        dm[i] = dm[ixj];
+                                        dm[ixj] = ma;
+                                    }
+                                }
+                            }
+                            cbar();
+                        }
+                    }
+                }
+                // the cuts, read off the sorted list by every warp alike
+                // (K <= n: the counts through the cut's bin reached K)
+                const int nk = min(topk ? K : n, n);
+                unsigned long long ZK;
+                {
+                    unsigned long long ms = 0ull;
+                    for (int i = lane; i < nk; i += 32)
+                        ms += dm[i];
+#pragma unroll
+                    for (int o = 16; o > 0; o >>= 1)
+                        ms += __shfl_xor_sync(0xffffffffu, ms, o);
+                    ZK = topk ? ms : Zrow;
+                }
+                int last = nk - 1;
+                unsigned long long Zt = ZK;
+                if (topp) {
+                    unsigned long long target = (unsigned long long)((double)Pp * (double)ZK);
+                    if (target == 0ull)
+                        target = 1ull;
+                    unsigned long long run = 0ull;
+                    int istar = -1;
+                    for (int i0 = 0; i0 < nk && istar < 0; i0 += 32) {
+                        const int i = i0 + lane;
+                        unsigned long long x = (i < nk) ? dm[i] : 0ull;
+#pragma unroll
+                        for (int o = 1; o < 32; o <<= 1) {
+                            const unsigned long long y = __shfl_up_sync(0xffffffffu, x, o);
+                            if (lane >= o)
+                                x += y;
+                        }
+                        const unsigned long long inc = run + x;
+                        const unsigned int hit = __ballot_sync(0xffffffffu, i < nk && inc >= target);
+                        if (hit) {
+                            const int hl = __ffs(hit) - 1;
+                            istar = i0 + hl;
+                            run = __shfl_sync(0xffffffffu, inc, hl);
+                        } else {
+                            run = __shfl_sync(0xffffffffu, inc, 31);
+                        }
+                    }
+                    if (istar < 0)
+                        istar = nk - 1;  // rounding: all of them
+                    last = istar;
+                    Zt = run;
+                }
+                const unsigned long long e = dk[last];
+                out.kappa = (unsigned int)(e >> 32);
+                out.iota = (int)(0xffffffffu - (unsigned int)(e & 0xffffffffu));
+                out.zt = (float)((double)Zt * (1.0 / 1099511627776.0));
+                out.flags = FILT_ON;
+            }
+        }
+        if (t == 0)
+            P.filt[item] = out;
+        cbar();  // every warp is done with the row's shared state
+    }
+}
+
 // -------------------------------------------------------------- accept scan
 
 template <int DT, bool FILT>
@@ -1996,6 +2671,10 @@ int launch_all(const Params &P, unsigned int grid1, unsigned int gridf, cudaStre
     stats_kernel<DT><<<grid1, NTHREADS, SMEM_BYTES, st>>>(P);
     mark(0);
     if constexpr (FILT) {
+        // the window kernel cuts most rows in one pass; the radix kernel
+        // finishes the rows it flagged
+        if (dependent(wfilter_kernel<DT>, gridf, WTH, WFILT_SMEM) != cudaSuccess)
+            return SPEC_ECUDA;
         if (dependent(filter_kernel<DT>, gridf, FTH, FILT_SMEM) != cudaSuccess)
             return SPEC_ECUDA;
         if (events && events[1])
@@ -2072,6 +2751,11 @@ int launch(const void *target, const void *draft, const int32_t *tokens, const f
                                                  : (const void *)filter_kernel<SPEC_BF16>;
             if (cudaFuncSetAttribute(ff, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                      (int)FILT_SMEM) != cudaSuccess)
+                return SPEC_ECUDA;
+            const void *fw = (dtype == SPEC_F32) ? (const void *)wfilter_kernel<SPEC_F32>
+                                                 : (const void *)wfilter_kernel<SPEC_BF16>;
+            if (cudaFuncSetAttribute(fw, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     (int)WFILT_SMEM) != cudaSuccess)
                 return SPEC_ECUDA;
             dc.filt_set[di] = true;
         }
