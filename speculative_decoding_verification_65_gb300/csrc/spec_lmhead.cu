@@ -29,7 +29,8 @@
 //     of STAGES stages of 64 K-elements (16 KB of h, 32 KB of W)
 //   - warp 1: TMEM allocation, and one thread issuing tcgen05.mma (M=128,
 //     N=256, K=16, bf16 in, fp32 accumulate), committing to mbarriers
-//   - warps 2..5: the epilogue, one TMEM lane (one row) per thread
+//   - warps 2..: the epilogue, one TMEM lane (one row) per thread; in the
+//     draw GEMM two warps share a lane quarter, one half of the columns each
 //   - tiles are ordered column-block major, so the CTAs working at one time
 //     share a few 2 MB W tiles in L2 and W is read from HBM about once
 // Every mbarrier wait is bounded; a wait that gives up sets
@@ -61,10 +62,19 @@ constexpr int B_BYTES = BN * BK * 2;      // 32 KB
 constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
 constexpr int NACC = 2;                   // accumulators in TMEM
 constexpr int TMEM_COLS = NACC * BN;      // 512: all of TMEM
-constexpr int GTHREADS = 192;             // 6 warps
+
 constexpr int GROUP = 32;                 // tokens per draw record
 
 enum { MODE_STORE = 0, MODE_STATS = 1, MODE_DRAW_F32 = 2, MODE_DRAW_BF16 = 3 };
+
+// Epilogue warps: the statistics epilogue (one exponential per logit) keeps
+// up with the MMAs with one warp per TMEM lane quarter; the draw epilogue
+// (two exponentials and a draft read per logit) needs two per quarter, each
+// taking one half of the tile's columns.
+template <int MODE>
+__host__ __device__ constexpr int epi_warps() { return (MODE == MODE_DRAW_F32 || MODE == MODE_DRAW_BF16) ? 8 : 4; }
+template <int MODE>
+__host__ __device__ constexpr int gthreads() { return (2 + epi_warps<MODE>()) * 32; }  // + TMA warp, MMA warp
 
 struct GSmemTail {
     unsigned long long full[STAGES];
@@ -247,15 +257,16 @@ __device__ __forceinline__ float pick32(const float (&v)[32], int o)
     return (o & 1) ? d[1] : d[0];
 }
 
-// The epilogue of one tile for one thread: row `row` of the tile's 128, the
-// accumulator's 256 columns starting at TMEM address taddr.
+// The epilogue of one thread's share of a tile: row `row` of the tile's 128,
+// the COLS accumulator columns of part h (h * COLS on) at TMEM address taddr.
 template <int MODE>
-__device__ __forceinline__ void epilogue(const GParams &P, uint32_t taddr, int row, int n)
+__device__ __forceinline__ void epilogue(const GParams &P, uint32_t taddr, int row, int n, int h)
 {
-    const int col_base = n * BN;
+    constexpr int COLS = BN / (epi_warps<MODE>() / 4);
+    const int col_base = n * BN + h * COLS;
     if (MODE == MODE_STORE) {
 #pragma unroll 1
-        for (int ch = 0; ch < BN / 32; ++ch) {
+        for (int ch = 0; ch < COLS / 32; ++ch) {
             float v[32];
             tmem_ld32(taddr + (uint32_t)(ch * 32), v);
             if (row < P.M) {
@@ -280,7 +291,7 @@ __device__ __forceinline__ void epilogue(const GParams &P, uint32_t taddr, int r
         int idx = INT_MAX;
         bool has_tg = false;
 #pragma unroll 1
-        for (int ch = 0; ch < BN / 32; ++ch) {
+        for (int ch = 0; ch < COLS / 32; ++ch) {
             float v[32];
             tmem_ld32(taddr + (uint32_t)(ch * 32), v);
             const int col0 = col_base + ch * 32;
@@ -354,9 +365,9 @@ __device__ __forceinline__ void epilogue(const GParams &P, uint32_t taddr, int r
         if (resid)
             load_draft(col_base, dv);
 #pragma unroll 1
-        for (int ch = 0; ch < BN / 32; ++ch) {
+        for (int ch = 0; ch < COLS / 32; ++ch) {
             const int col0 = col_base + ch * 32;
-            if (resid && ch + 1 < BN / 32)
+            if (resid && ch + 1 < COLS / 32)
                 load_draft(col0 + 32, dn);  // one chunk ahead
             float v[32];
             tmem_ld32(taddr + (uint32_t)(ch * 32), v);
@@ -388,30 +399,8 @@ __device__ __forceinline__ void epilogue(const GParams &P, uint32_t taddr, int r
     }
 }
 
-// Draw GEMM: the draft values the epilogue will read for row `row` of the
-// tile at column block n, requested into L2 one tile ahead (a tile's MMAs
-// take longer than an HBM round trip, so the loads then hit L2).
 template <int MODE>
-__device__ __forceinline__ void prefetch_draft(const GParams &P, int row, int n)
-{
-    if (MODE != MODE_DRAW_F32 && MODE != MODE_DRAW_BF16)
-        return;
-    if (row >= P.M)
-        return;
-    const int mode = P.jobs[row].mode;
-    if (mode != JOB_RESIDUAL)
-        return;
-    constexpr int es = (MODE == MODE_DRAW_F32) ? 4 : 2;
-    const DrawJob &J = P.jobs[row];
-    const uint8_t *base = reinterpret_cast<const uint8_t *>(P.draft) +
-                          (((size_t)J.b * P.k + J.j) * (size_t)P.N) * es;
-    const int c1 = min(P.N, n * BN + BN);
-    for (int c = n * BN; c < c1; c += 128 / es)
-        asm volatile("prefetch.global.L2 [%0];" :: "l"(base + (size_t)c * es));
-}
-
-template <int MODE>
-__global__ void __launch_bounds__(GTHREADS, 1)
+__global__ void __launch_bounds__(gthreads<MODE>(), 1)
     gemm_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_constant__ CUtensorMap mapB,
                 const GParams P)
 {
@@ -430,7 +419,7 @@ __global__ void __launch_bounds__(GTHREADS, 1)
         }
         for (int a = 0; a < NACC; ++a) {
             mbar_init(&S.acc_full[a], 1);
-            mbar_init(&S.acc_empty[a], 4);
+            mbar_init(&S.acc_empty[a], epi_warps<MODE>());
         }
         mbar_init(&S.drain, 1);
         S.abort_flag = 0;
@@ -534,7 +523,9 @@ __global__ void __launch_bounds__(GTHREADS, 1)
         }
     } else {
         // --------------------------------------------------------- epilogue
-        const int q = warp & 3;  // the TMEM lane quarter this warp may read
+        const int q = warp & 3;              // the TMEM lane quarter this warp may read
+        const int h = (warp - 2) >> 2;       // its part of the columns (draw GEMM: a half)
+        constexpr int COLS = BN / (epi_warps<MODE>() / 4);
         int acc = 0;
         uint32_t acc_phase = 0;
         for (int t = blockIdx.x; t < P.total; t += G) {
@@ -552,11 +543,8 @@ __global__ void __launch_bounds__(GTHREADS, 1)
             }
             tc_fence_after();
             const int row = m * BM + q * 32 + lane;
-            if (t + G < P.total) {  // this thread's row of its next tile
-                const int n2 = (t + G) / P.mt, m2 = (t + G) - n2 * P.mt;
-                prefetch_draft<MODE>(P, m2 * BM + q * 32 + lane, n2);
-            }
-            epilogue<MODE>(P, tbase + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * BN), row, n);
+            epilogue<MODE>(P, tbase + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * BN + h * COLS),
+                           row, n, h);
             tc_fence_before();
             __syncwarp();
             if (lane == 0)
@@ -589,7 +577,7 @@ constexpr int MAX_CHUNKS = (SPEC_MAX_V / GROUP + 127) / 128;  // 256 for 2^20 to
 
 struct VParams {
     int B, k, V, d;
-    int nt;                   // statistics tiles per target row
+    int nt;                   // statistics records (tiles) per target row
     int NC;                   // draft chunk records per row
     int ng;                   // draw groups per row
     int draft_dtype;
@@ -1106,7 +1094,7 @@ int launch_gemm(const CUtensorMap &ma, const CUtensorMap &mb, GParams &P, int M,
     const int grid = P.total < di.sms ? P.total : di.sms;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned int)grid);
-    cfg.blockDim = dim3(GTHREADS);
+    cfg.blockDim = dim3(gthreads<MODE>());
     cfg.dynamicSmemBytes = GSMEM_BYTES;
     cfg.stream = st;
     cudaLaunchAttribute attr[1];
