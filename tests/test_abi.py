@@ -186,3 +186,70 @@ def test_wait_selftest_argument_checks(lib):
     assert lib.spec_selftest_wait_timeout(ctypes.c_void_p(GOOD[0] + 4), 1000, None) == sv.SPEC_EINVAL
     assert lib.spec_selftest_wait_timeout(ctypes.c_void_p(GOOD[0]), 0, None) == sv.SPEC_EINVAL
     assert lib.spec_selftest_wait_timeout(ctypes.c_void_p(GOOD[0]), 10**9, None) == sv.SPEC_EINVAL
+
+
+# ------------------------------------------------ LM-head-fused verification
+
+def _up(x, a=256):
+    return -(-x // a) * a
+
+
+@pytest.mark.parametrize("B,k,V,d,dt,ok", [
+    (1024, 4, 128256, 4096, 1, True), (1, 1, 2, 64, 0, True), (3, 31, 1000, 16384, 0, True),
+    (0, 4, 100, 64, 0, False), (1, 0, 100, 64, 0, False), (1, 32, 100, 64, 0, False),
+    (1, 4, 1, 64, 0, False), (1, 4, 100, 96, 0, False), (1, 4, 100, 16448, 0, False),
+    (1, 4, 100, 64, 2, False), (1, 4, (1 << 20) + 1, 64, 0, False),
+])
+def test_lmhead_workspace_size(lib, B, k, V, d, dt, ok):
+    n = sv.spec_verify_lmhead_workspace_size(B, k, V, d, dt)
+    if not ok:
+        assert n == 0
+        return
+    M = B * (k + 1)
+    nt, ng = -(-V // 256), -(-V // 32)
+    nc = -(-(V * (4 if dt == 0 else 2)) // 4096)
+    part = 256
+    tg = _up(part + M * nt * 16)
+    rec = _up(tg + M * 4)
+    jobs = _up(rec + B * k * nc * 8)
+    hdraw = _up(jobs + B * 36)
+    grp = _up(hdraw + B * d * 2)
+    grp_p = _up(grp + B * ng * 4)
+    assert n == _up(grp_p + B * ng * 4)
+
+
+def _lcall(lib, ptrs, B=2, k=3, V=300, d=64, dt=0, wsb=1 << 26):
+    args = [ctypes.c_void_p(p) for p in ptrs[:9]]
+    return lib.spec_verify_lmhead(*args, B, k, V, d, dt, ctypes.c_void_p(ptrs[9]), wsb, None)
+
+
+LGOOD = [0x10000 * (i + 1) for i in range(10)]
+
+
+@pytest.mark.parametrize("which", range(10))
+def test_lmhead_null_pointer_rejected(lib, which):
+    p = list(LGOOD)
+    p[which] = 0
+    assert _lcall(lib, p) == sv.SPEC_EINVAL
+
+
+@pytest.mark.parametrize("which,off", [(0, 8), (1, 8), (2, 8), (3, 2), (4, 2), (5, 2), (6, 2),
+                                       (7, 2), (8, 2), (9, 8)])
+def test_lmhead_misaligned_pointer_rejected(lib, which, off):
+    p = list(LGOOD)
+    p[which] += off
+    assert _lcall(lib, p) == sv.SPEC_EINVAL
+
+
+def test_lmhead_bad_sizes_and_small_workspace(lib):
+    assert _lcall(lib, LGOOD, d=100) == sv.SPEC_EINVAL
+    assert _lcall(lib, LGOOD, k=32) == sv.SPEC_EINVAL
+    assert _lcall(lib, LGOOD, V=1) == sv.SPEC_EINVAL
+    assert _lcall(lib, LGOOD, dt=4) == sv.SPEC_EINVAL
+    need = sv.spec_verify_lmhead_workspace_size(2, 3, 300, 64, 0)
+    assert _lcall(lib, LGOOD, wsb=need - 1) == sv.SPEC_ENOSPACE
+    vp = ctypes.c_void_p
+    assert lib.spec_lmhead_logits(vp(LGOOD[0]), vp(LGOOD[1]), vp(LGOOD[2]), 4, 300, 96,
+                                  vp(LGOOD[3]), None) == sv.SPEC_EINVAL
+    assert lib.spec_lmhead_logits(None, vp(LGOOD[1]), vp(LGOOD[2]), 4, 300, 64,
+                                  vp(LGOOD[3]), None) == sv.SPEC_EINVAL
