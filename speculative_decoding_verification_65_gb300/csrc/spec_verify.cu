@@ -1692,6 +1692,29 @@ __global__ void __launch_bounds__(WTH, 2) wfilter_kernel(const Params P)
             bits &= 0xffff0000u;
         return __uint_as_float(bits);
     };
+    // The window's lower edge: the smallest float x with wbin(x) <= lim.
+    // wbin is monotone in x (each rounding step is), so a token is inside the
+    // window iff x >= edge, one compare instead of the bin computation.
+    // Found by bisection on the order keys between a value one bit outside
+    // the window and the row maximum (inside); each step evaluates wbin, the
+    // same expression the bins are counted with.
+    auto edge_of = [&](int lim) -> float {
+        auto fkey = [](float x) { return okey(__float_as_uint(x)); };
+        auto kval = [](unsigned int k) {
+            return __uint_as_float((k & 0x80000000u) ? (k & 0x7fffffffu) : ~k);
+        };
+        unsigned int lo = fkey(m - ((float)lim * 0.5f + 2.0f) / c);  // wbin(lo) > lim
+        unsigned int hi = fkey(m);                                      // wbin(m) = 0 <= lim
+        while (hi - lo > 1u) {
+            const unsigned int mid = lo + (hi - lo) / 2u;
+            if (wbin(kval(mid)) <= lim)
+                hi = mid;
+            else
+                lo = mid;
+        }
+        return kval(hi);
+    };
+    float xs = 0.0f, xs0 = 0.0f;  // the edges of this warp's window and of the first
     // this warp's reading of the first bin (<= lim) whose counts (masses)
     // reach the cut, and the count through it; -1 if none
     auto warp_bk = [&](int lim, unsigned int &cum_out) -> int {
@@ -1782,6 +1805,8 @@ __global__ void __launch_bounds__(WTH, 2) wfilter_kernel(const Params P)
             const float zrow = (float)((double)Zrow * (1.0 / 1099511627776.0));
             const int Dg = (int)floorf(log2f((float)FCAP / (fmaxf(zrow, 1.0f) * 1.01f))) + 8;
             nbw0 = nbw = row_bad ? -1 : 2 * min(WBINS / 2, max(1, Dg)) - 1;
+            if (!row_bad)
+                xs0 = xs = edge_of(nbw0);
             kmin = topk ? (unsigned int)K : 1u;
             last_nc = 0u;
             if (t == 0) {
@@ -1839,31 +1864,26 @@ __global__ void __launch_bounds__(WTH, 2) wfilter_kernel(const Params P)
             for (int pass = 0; pass < npass; ++pass) {
                 const bool count_only = ti.first && pass == 0;
                 const bool count = !ti.first || pass == 0;
-                const int lim = count_only ? nbw0 : nbw;
+                const float xe = count_only ? xs0 : xs;  // the window: x >= xe
                 uint4 r0 = raw[0], r1 = raw[1], r2 = raw[2], r3 = raw[3];
                 static_assert(WVPL == 4 && VEC <= 8, "four vectors of at most 8 tokens per lane");
                 uint32_t tball = 0u;  // 8 bits per vector: the tokens in the window
                 unsigned int cnt = 0u;
-#pragma unroll 1
+#pragma unroll
                 for (int u = 0; u < WVPL; ++u) {
                     uint32_t tb = 0u;
-                    if (wbin(L::vmax(r0)) <= lim) {  // else no token of the vector is in
+                    if (L::vmax(raw[u]) >= xe) {  // else no token of the vector is in
                         float x[VEC];
-                        L::unpack(r0, x);
+                        L::unpack(raw[u], x);
 #pragma unroll
-                        for (int j = 0; j < VEC; ++j) {
-                            const int idx = (vt0 + vwarp + lane + 32 * u) * VEC + j;
-                            if (idx < V && wbin(x[j]) <= lim)
-                                tb |= 1u << j;
-                        }
+                        for (int j = 0; j < VEC; ++j)
+                            tb |= (x[j] >= xe) ? (1u << j) : 0u;
+                        const int idx0 = (vt0 + vwarp + lane + 32 * u) * VEC;
+                        if (idx0 + VEC > V)  // the row's end
+                            tb &= (V > idx0) ? ((1u << (V - idx0)) - 1u) : 0u;
                     }
                     tball |= tb << (8 * u);
                     cnt += (unsigned int)__popc(tb);
-                    const uint4 rt = r0;
-                    r0 = r1;
-                    r1 = r2;
-                    r2 = r3;
-                    r3 = rt;
                 }
                 unsigned int pos = 0u;
                 bool any = true;
@@ -1926,8 +1946,10 @@ __global__ void __launch_bounds__(WTH, 2) wfilter_kernel(const Params P)
                     cbar();  // every warp's counts of the first tile are in
                     unsigned int cum0;
                     const int bk0 = warp_bk(nbw0, cum0);
-                    if (bk0 >= 0 && bk0 < nbw)
+                    if (bk0 >= 0 && bk0 < nbw) {
                         nbw = bk0;
+                        xs = edge_of(nbw);
+                    }
                 }
             }
             // narrow this warp's window once the gathered count has doubled
@@ -1936,8 +1958,10 @@ __global__ void __launch_bounds__(WTH, 2) wfilter_kernel(const Params P)
                 last_nc = nc;
                 unsigned int cum;
                 const int bk = warp_bk(nbw, cum);
-                if (bk >= 0 && bk < nbw)
+                if (bk >= 0 && bk < nbw) {
                     nbw = bk;
+                    xs = edge_of(nbw);
+                }
             }
         }
         if (!ti.last)
