@@ -1858,7 +1858,14 @@ __global__ void __launch_bounds__(WTH, 2) wfilter_kernel(const Params P)
         // only be larger, so the row's cut bin is not past it); then the
         // tile's tokens inside that window are stored.  A wide first window
         // on a flat row therefore does not flood the buffer.
-        if (!row_bad && !*(volatile int *)&S.overflow) {
+        // Decisions that guard warp collectives are taken from lane 0's read
+        // of shared state and broadcast: lanes reading it at different times
+        // (another warp may change it in between) must not split the warp.
+        int ovf = 0;
+        if (lane == 0)
+            ovf = *(volatile int *)&S.overflow;
+        ovf = __shfl_sync(0xffffffffu, ovf, 0);
+        if (!row_bad && !ovf) {
             const int npass = ti.first ? 2 : 1;
 #pragma unroll 1
             for (int pass = 0; pass < npass; ++pass) {
@@ -1953,7 +1960,10 @@ __global__ void __launch_bounds__(WTH, 2) wfilter_kernel(const Params P)
                 }
             }
             // narrow this warp's window once the gathered count has doubled
-            const unsigned int nc = *(volatile unsigned int *)&S.ncand;
+            unsigned int nc = 0u;
+            if (lane == 0)
+                nc = *(volatile unsigned int *)&S.ncand;
+            nc = __shfl_sync(0xffffffffu, nc, 0);  // (the same decision in every lane)
             if (nc >= kmin && nc >= 2u * last_nc) {
                 last_nc = nc;
                 unsigned int cum;
