@@ -1470,10 +1470,10 @@ __global__ void __launch_bounds__(FTH, 2) filter_kernel(const Params P)
 // own copy of the window from the shared histogram: counts only grow, so the
 // bin it reads as the cut's is never below the row's final one, and every
 // token of the bins through the final cut is gathered by every warp.  Block
-// work (the cut from the sorted window) is done once per row between named
-// barriers of the consumer warps.  A row whose buffer overflowed, or whose
-// window ended short of the cut, is recorded FILT_RADIX and finished by
-// filter_kernel.
+// work (the cut from the sorted window) is done once per row between
+// barriers of the consumer warps, each a bounded mbarrier wait.  A row whose
+// buffer overflowed, or whose window ended short of the cut, is recorded
+// FILT_RADIX and finished by filter_kernel.
 constexpr int WCW = 8;                            // consumer warps
 constexpr int WPW = WCW;                          // the producer's warp
 constexpr int WTH = (WCW + 1) * 32;
