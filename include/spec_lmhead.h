@@ -27,8 +27,13 @@
  *   draft_logits [B, k, V] of draft_dtype (SPEC_F32 or SPEC_BF16), 16-byte
  *                                   aligned base
  *   other arguments as spec_verify.
- * Sizes: B >= 1, 1 <= k <= SPEC_MAX_K, 2 <= V <= SPEC_MAX_V, d a multiple of
- * 64 in [64, 16384].
+ * Sizes: B >= 1, 1 <= k <= 31 (the accept scan holds a sequence's k+1
+ * positions in one warp), 2 <= V <= SPEC_MAX_V, d a multiple of 64 in
+ * [64, 16384], and at most 2^30 GEMM tiles of 128 rows x 256 columns over
+ * the B(k+1) x V target logits.
+ *
+ * Calls may come from several host threads at once, each with its own
+ * workspace.
  */
 #ifndef SPEC_LMHEAD_H
 #define SPEC_LMHEAD_H
@@ -91,7 +96,8 @@ int32_t spec_verify_lmhead_timed(const void *hidden, const void *lm_head,
  * hidden[r][j] * lm_head[x][j] for r < M, x < V (out device float32 [M, V]).
  * For checking the tensor-core product; the verification never stores it.
  * hidden bf16 [M, d], lm_head bf16 [V, d]; `status` device int32 (the bounded
- * waits' status word, zero beforehand).  Returns a SPEC_* code as above.
+ * waits' status word, zero beforehand).  M >= 1, V and d as above, with the
+ * same tile-count limit.  Returns a SPEC_* code as above.
  */
 int32_t spec_lmhead_logits(const void *hidden, const void *lm_head, float *out, int32_t M,
                            int32_t V, int32_t d, int32_t *status, void *stream);

@@ -38,6 +38,9 @@
  *     reached that point.
  *   - The library allocates no memory and keeps no per-call global state.  The
  *     caller owns every buffer.  Inputs are read-only; outputs are overwritten.
+ *   - Entry points may be called from several host threads at once, each call
+ *     with its own workspace (the library's only shared state is a per-device
+ *     cache of launch facts, published atomically).
  *   - The return value reports host-checkable errors only (spec_status_t).
  *     Data-dependent problems are reported per sequence on the device:
  *     out_num_accepted[b] = -1 and out_tokens[b, :] = -1 when T is NaN,

@@ -44,6 +44,8 @@
 #include <stdint.h>
 #include <string.h>
 
+#include <atomic>
+
 #include "spec_lmhead.h"
 #include "internal.h"
 #include "device_common.cuh"
@@ -993,21 +995,20 @@ typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t
                                   const cuuint32_t *, CUtensorMapInterleave, CUtensorMapSwizzle,
                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
 
+// The driver's tensor-map encoder, looked up once (a function-local static:
+// its initialisation is thread-safe).
 EncodeTiledFn encode_fn()
 {
-    static EncodeTiledFn fn = nullptr;
-    static bool tried = false;
-    if (!tried) {
-        tried = true;
+    static const EncodeTiledFn fn = []() -> EncodeTiledFn {
         void *p = nullptr;
         cudaDriverEntryPointQueryResult q;
         if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000,
                                              cudaEnableDefault, &q) == cudaSuccess &&
             q == cudaDriverEntryPointSuccess)
-            fn = reinterpret_cast<EncodeTiledFn>(p);
-        else
-            (void)cudaGetLastError();
-    }
+            return reinterpret_cast<EncodeTiledFn>(p);
+        (void)cudaGetLastError();
+        return nullptr;
+    }();
     return fn;
 }
 
@@ -1029,11 +1030,17 @@ bool make_map(CUtensorMap *map, const void *base, int rows, int d, int box_rows)
 
 size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
+// The GEMMs count tiles in int: keep M x V's tile count well inside it.
+bool tiles_ok(size_t M, int32_t V)
+{
+    return ((M + BM - 1) / BM) * (((size_t)V + BN - 1) / BN) <= ((size_t)1 << 30);
+}
+
 bool sizes_ok(int32_t B, int32_t k, int32_t V, int32_t d, int32_t ddt)
 {
     return B >= 1 && k >= 1 && k <= 31 && V >= 2 && V <= SPEC_MAX_V && d >= 64 && d <= 16384 &&
            d % 64 == 0 && (ddt == SPEC_F32 || ddt == SPEC_BF16) &&
-           (size_t)B * (k + 1) <= 0x7fffffffull / 2;
+           (size_t)B * (k + 1) <= 0x7fffffffull / 2 && tiles_ok((size_t)B * (k + 1), V);
 }
 
 struct Layout {
@@ -1061,9 +1068,12 @@ Layout layout(int32_t B, int32_t k, int32_t V, int32_t d, int32_t ddt)
     return w;
 }
 
+// Per-device launch facts, filled by the first call on each device; a flag
+// is published with release order after what it guards (host threads may
+// race here, repeating the same idempotent calls).
 struct DevInfo {
-    int sms = 0;
-    bool attr[4] = {false, false, false, false};
+    std::atomic<int> sms;
+    std::atomic<bool> attr[4];
 };
 DevInfo g_dev[64];
 
@@ -1075,14 +1085,18 @@ int launch_gemm(const CUtensorMap &ma, const CUtensorMap &mb, GParams &P, int M,
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64)
         return SPEC_ECUDA;
     DevInfo &di = g_dev[dev];
-    if (!di.sms && cudaDeviceGetAttribute(&di.sms, cudaDevAttrMultiProcessorCount, dev) !=
-                       cudaSuccess)
-        return SPEC_ECUDA;
-    if (!di.attr[MODE]) {
+    int sms = di.sms.load(std::memory_order_relaxed);
+    if (!sms) {
+        if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+            sms < 1)
+            return SPEC_ECUDA;
+        di.sms.store(sms, std::memory_order_relaxed);
+    }
+    if (!di.attr[MODE].load(std::memory_order_acquire)) {
         if (cudaFuncSetAttribute(gemm_kernel<MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  (int)GSMEM_BYTES) != cudaSuccess)
             return SPEC_ECUDA;
-        di.attr[MODE] = true;
+        di.attr[MODE].store(true, std::memory_order_release);
     }
     P.M = M;
     P.N = N;
@@ -1091,7 +1105,7 @@ int launch_gemm(const CUtensorMap &ma, const CUtensorMap &mb, GParams &P, int M,
     P.nt = (N + BN - 1) / BN;
     P.kbs = Kd / BK;
     P.total = P.mt * P.nt;
-    const int grid = P.total < di.sms ? P.total : di.sms;
+    const int grid = P.total < sms ? P.total : sms;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned int)grid);
     cfg.blockDim = dim3(gthreads<MODE>());
@@ -1282,7 +1296,8 @@ int32_t spec_verify_lmhead_timed(const void *hidden, const void *lm_head,
 int32_t spec_lmhead_logits(const void *hidden, const void *lm_head, float *out, int32_t M,
                            int32_t V, int32_t d, int32_t *status, void *stream)
 {
-    if (M < 1 || V < 2 || V > SPEC_MAX_V || d < 64 || d > 16384 || d % 64 != 0)
+    if (M < 1 || V < 2 || V > SPEC_MAX_V || d < 64 || d > 16384 || d % 64 != 0 ||
+        !tiles_ok((size_t)M, V))
         return SPEC_EINVAL;
     if (!hidden || !lm_head || !out || !status || !al16(hidden) || !al16(lm_head) || !al4(out) ||
         !al4(status))

@@ -34,6 +34,8 @@
 #include <math.h>
 #include <stdint.h>
 
+#include <atomic>
+
 #include "spec_sample.h"
 #include "internal.h"
 #include "spec_verify.h"
@@ -370,10 +372,13 @@ __global__ void __launch_bounds__(PICK_WARPS * 32) pick_kernel(const SParams P)
 
 // --------------------------------------------------------------- host side
 
+// Per-device launch facts, filled by the first call on each device; the flag
+// is published with release order after the values (host threads may race
+// here, repeating the same idempotent queries).
 struct DevCache {
-    int sms = 0;
-    int ctas_per_sm[2] = {0, 0};
-    bool attr_set[2] = {false, false};
+    std::atomic<int> sms;
+    std::atomic<int> ctas_per_sm[2];
+    std::atomic<bool> attr_set[2];
 };
 DevCache g_dev[64];
 
@@ -452,7 +457,7 @@ int setup_chunks(SParams &P, unsigned int &grid1, const void *logits, const floa
     const int di = (dtype == SPEC_F32) ? 0 : 1;
     const void *fn = (dtype == SPEC_F32) ? (const void *)chunk_kernel<SPEC_F32>
                                          : (const void *)chunk_kernel<SPEC_BF16>;
-    if (!dc.attr_set[di]) {
+    if (!dc.attr_set[di].load(std::memory_order_acquire)) {
         if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  (int)SMEM_BYTES) != cudaSuccess)
             return SPEC_ECUDA;
@@ -462,11 +467,12 @@ int setup_chunks(SParams &P, unsigned int &grid1, const void *logits, const floa
         int sms = 0;
         if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
             return SPEC_ECUDA;
-        dc.sms = sms;
-        dc.ctas_per_sm[di] = n > 0 ? n : 1;
-        dc.attr_set[di] = true;
+        dc.sms.store(sms, std::memory_order_relaxed);
+        dc.ctas_per_sm[di].store(n > 0 ? n : 1, std::memory_order_relaxed);
+        dc.attr_set[di].store(true, std::memory_order_release);
     }
-    const size_t resident = (size_t)dc.sms * dc.ctas_per_sm[di];
+    const size_t resident = (size_t)dc.sms.load(std::memory_order_relaxed) *
+                            (size_t)dc.ctas_per_sm[di].load(std::memory_order_relaxed);
     grid1 = (unsigned int)(groups < resident ? groups : resident);
 
     P.logits = logits;

@@ -38,6 +38,8 @@
 #include <stdint.h>
 #include <string.h>
 
+#include <atomic>
+
 #include "spec_verify.h"
 #include "device_common.cuh"
 
@@ -2621,11 +2623,15 @@ __global__ void __launch_bounds__(SCAN_WARPS * 32) final_kernel(const Params P)
 
 // ------------------------------------------------------------------ host side
 
+// Per-device launch facts, filled by the first call on each device.  Host
+// threads may call at once: a flag is published with release order after the
+// values it guards, and read with acquire order (a race only repeats the same
+// idempotent queries).
 struct DevCache {
-    int sms = 0;
-    int ctas_per_sm[2] = {0, 0};        // statistics kernel, per dtype
-    bool attr_set[2] = {false, false};
-    bool filt_set[2] = {false, false};  // filter kernel's shared-memory size set
+    std::atomic<int> sms;
+    std::atomic<int> ctas_per_sm[2];     // statistics kernel, per dtype
+    std::atomic<bool> attr_set[2];
+    std::atomic<bool> filt_set[2];       // filter kernels' shared-memory sizes set
 };
 DevCache g_dev[64];
 
@@ -2764,7 +2770,7 @@ int launch(const void *target, const void *draft, const int32_t *tokens, const f
     const int di = (dtype == SPEC_F32) ? 0 : 1;
     const void *fn = (dtype == SPEC_F32) ? (const void *)stats_kernel<SPEC_F32>
                                          : (const void *)stats_kernel<SPEC_BF16>;
-    if (!dc.attr_set[di]) {
+    if (!dc.attr_set[di].load(std::memory_order_acquire)) {
         if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  (int)SMEM_BYTES) != cudaSuccess)
             return SPEC_ECUDA;
@@ -2774,13 +2780,14 @@ int launch(const void *target, const void *draft, const int32_t *tokens, const f
         int sms = 0;
         if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
             return SPEC_ECUDA;
-        dc.sms = sms;
-        dc.ctas_per_sm[di] = n > 0 ? n : 1;
-        dc.attr_set[di] = true;
+        dc.sms.store(sms, std::memory_order_relaxed);
+        dc.ctas_per_sm[di].store(n > 0 ? n : 1, std::memory_order_relaxed);
+        dc.attr_set[di].store(true, std::memory_order_release);
     }
+    const size_t n_sms = (size_t)dc.sms.load(std::memory_order_relaxed);
     unsigned int gridf = 0;
     if (filtered) {
-        if (!dc.filt_set[di]) {
+        if (!dc.filt_set[di].load(std::memory_order_acquire)) {
             const void *ff = (dtype == SPEC_F32) ? (const void *)filter_kernel<SPEC_F32>
                                                  : (const void *)filter_kernel<SPEC_BF16>;
             if (cudaFuncSetAttribute(ff, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -2791,14 +2798,14 @@ int launch(const void *target, const void *draft, const int32_t *tokens, const f
             if (cudaFuncSetAttribute(fw, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                      (int)WFILT_SMEM) != cudaSuccess)
                 return SPEC_ECUDA;
-            dc.filt_set[di] = true;
+            dc.filt_set[di].store(true, std::memory_order_release);
         }
         // two rows per SM in flight (one CTA each, streaming through a ring)
         const size_t rows = (size_t)B * (2 * (size_t)k + 1);
-        const size_t cap = (size_t)dc.sms * 2;
+        const size_t cap = n_sms * 2;
         gridf = (unsigned int)(rows < cap ? rows : cap);
     }
-    const size_t resident = (size_t)dc.sms * dc.ctas_per_sm[di];
+    const size_t resident = n_sms * (size_t)dc.ctas_per_sm[di].load(std::memory_order_relaxed);
     const unsigned int grid1 = (unsigned int)(total < resident ? total : resident);
 
     Params P;
@@ -2855,7 +2862,7 @@ static_assert(SPEC_MAX_V / (NT * 4) + UD <= MAXBLK, "CDF blocks must cover the l
 // cudaGetSymbolAddress, once per device, with that device current.
 constexpr size_t NOALLOC_SCRATCH_BYTES = (size_t)8 << 20;
 static __device__ __align__(256) uint8_t g_noalloc_scratch[NOALLOC_SCRATCH_BYTES];
-static void *g_noalloc_addr[64];
+static std::atomic<void *> g_noalloc_addr[64];
 
 // ---------------------------------------------------------------- C ABI
 
@@ -2972,13 +2979,12 @@ int32_t spec_verify_noalloc(const void *target_logits, const void *draft_logits,
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64)
         return SPEC_ECUDA;
-    if (!g_noalloc_addr[dev]) {
-        void *addr = nullptr;
-        if (cudaGetSymbolAddress(&addr, g_noalloc_scratch) != cudaSuccess || !addr)
+    void *ws = g_noalloc_addr[dev].load(std::memory_order_relaxed);
+    if (!ws) {
+        if (cudaGetSymbolAddress(&ws, g_noalloc_scratch) != cudaSuccess || !ws)
             return SPEC_ECUDA;
-        g_noalloc_addr[dev] = addr;
+        g_noalloc_addr[dev].store(ws, std::memory_order_relaxed);
     }
-    void *ws = g_noalloc_addr[dev];
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
     // the status word is the only scratch contents a call reads before writing
     if (cudaMemsetAsync(ws, 0, sizeof(WsHeader), st) != cudaSuccess)

@@ -199,6 +199,8 @@ def _up(x, a=256):
     (0, 4, 100, 64, 0, False), (1, 0, 100, 64, 0, False), (1, 32, 100, 64, 0, False),
     (1, 4, 1, 64, 0, False), (1, 4, 100, 96, 0, False), (1, 4, 100, 16448, 0, False),
     (1, 4, 100, 64, 2, False), (1, 4, (1 << 20) + 1, 64, 0, False),
+    # the GEMMs' tile count (128-row x 256-column tiles) must stay within 2^30
+    ((1 << 22), 3, 1 << 20, 64, 0, True), ((1 << 24), 3, 1 << 20, 64, 0, False),
 ])
 def test_lmhead_workspace_size(lib, B, k, V, d, dt, ok):
     n = sv.spec_verify_lmhead_workspace_size(B, k, V, d, dt)
@@ -252,4 +254,7 @@ def test_lmhead_bad_sizes_and_small_workspace(lib):
     assert lib.spec_lmhead_logits(vp(LGOOD[0]), vp(LGOOD[1]), vp(LGOOD[2]), 4, 300, 96,
                                   vp(LGOOD[3]), None) == sv.SPEC_EINVAL
     assert lib.spec_lmhead_logits(None, vp(LGOOD[1]), vp(LGOOD[2]), 4, 300, 64,
+                                  vp(LGOOD[3]), None) == sv.SPEC_EINVAL
+    # 2^26 rows x 2^20 columns: 2^31 tiles, more than the GEMM counts
+    assert lib.spec_lmhead_logits(vp(LGOOD[0]), vp(LGOOD[1]), vp(LGOOD[2]), 1 << 26, 1 << 20, 64,
                                   vp(LGOOD[3]), None) == sv.SPEC_EINVAL
