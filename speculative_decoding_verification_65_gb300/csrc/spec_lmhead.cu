@@ -44,6 +44,8 @@
 #include <stdint.h>
 #include <string.h>
 
+#include <atomic>
+
 #include "spec_lmhead.h"
 #include "internal.h"
 #include "device_common.cuh"
@@ -985,8 +987,6 @@ __global__ void __launch_bounds__(SCAN_WARPS * 32) final_kernel(const VParams P)
 }  // namespace
 
 // ---------------------------------------------------------------- host side
-
-#include <atomic>
 
 namespace {
 

@@ -34,6 +34,8 @@
 #include <math.h>
 #include <stdint.h>
 
+#include <atomic>
+
 #include "spec_sample.h"
 #include "internal.h"
 #include "spec_verify.h"
@@ -369,8 +371,6 @@ __global__ void __launch_bounds__(PICK_WARPS * 32) pick_kernel(const SParams P)
 }
 
 // --------------------------------------------------------------- host side
-
-#include <atomic>
 
 // Per-device launch facts, filled by the first call on each device; the flag
 // is published with release order after the values (host threads may race

@@ -38,6 +38,8 @@
 #include <stdint.h>
 #include <string.h>
 
+#include <atomic>
+
 #include "spec_verify.h"
 #include "device_common.cuh"
 
@@ -2620,8 +2622,6 @@ __global__ void __launch_bounds__(SCAN_WARPS * 32) final_kernel(const Params P)
 }
 
 // ------------------------------------------------------------------ host side
-
-#include <atomic>
 
 // Per-device launch facts, filled by the first call on each device.  Host
 // threads may call at once: a flag is published with release order after the
