@@ -26,7 +26,8 @@
  *   - temperature 0: accept while the target's argmax equals the draft token:
  *     interview page, "Deep dive: correctness and speedup" (greedy remark).
  *
- * Readings where the pages are silent (each one is listed in the design doc):
+ * Readings where the pages are silent (taken as the plainest reading the rest
+ * of the pages supports):
  *   - a draw uses inverse-CDF: C(x) = sum_{y<=x} w(y) accumulated left to
  *     right, R = C(V-1) (the scan's own total), token = smallest x with
  *     C(x) > u*R; if rounding leaves no such x, the largest x with w(x) > 0.
