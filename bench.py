@@ -1111,7 +1111,7 @@ def run_reference_lmhead(args):
     args_np = [_bits(x["hidden"]), _bits(x["lm_head"]), _bits(x["draft"])] + \
         [x[n].numpy() for n in ("tokens", "u_accept", "u_resample", "temperature")]
     run = lambda: oracle.verify_lmhead(*args_np, nthreads=cores, want_trace=False)
-    for _ in range(min(args.warmup, 1)):
+    for _ in range(args.warmup):
         run()
     # each step takes about a second on 16 cores: stop at the CPU budget
     t0 = time.perf_counter()
@@ -1123,7 +1123,7 @@ def run_reference_lmhead(args):
     value = per_step * k * steps / dt
     line = {
         "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT,
-        "n_gpus": world, "steps": steps, "warmup": min(args.warmup, 1),
+        "n_gpus": world, "steps": steps, "warmup": args.warmup,
         "ms_per_step": dt / steps * 1e3, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
         "config": {"workload": lmhead_name(B, k, V, d), "B": per_step, "k": k, "V": V, "d": d,
