@@ -555,12 +555,24 @@ def _marshal_lmhead(hidden, lm_head, draft, tokens, u_accept, u_resample, temper
     return B, k, V, d, _dtype_code(draft)
 
 
-def lmhead_workspace(B: int, k: int, V: int, d: int, draft_dtype: int, device=None):
+def _zeros_on(stream, device, n, dtype):
+    """A zero-filled device tensor whose fill is ordered before later work on
+    `stream` (the current stream when None)."""
+    torch = _torch()
+    device = torch.device(device if device is not None else "cuda")
+    s = stream if stream is not None else torch.cuda.current_stream(device)
+    with torch.cuda.stream(s):
+        return torch.zeros(n, dtype=dtype, device=device)
+
+
+def lmhead_workspace(B: int, k: int, V: int, d: int, draft_dtype: int, device=None,
+                     stream=None):
+    """A zeroed workspace for spec_verify_lmhead, zero-filled on `stream`."""
     torch = _torch()
     need = spec_verify_lmhead_workspace_size(B, k, V, d, draft_dtype)
     if need == 0:
         raise SpecVerifyError("sizes out of range for spec_verify_lmhead")
-    return torch.zeros(need, dtype=torch.uint8, device=device or "cuda")
+    return _zeros_on(stream, device, need, torch.uint8)
 
 
 def spec_verify_lmhead(hidden, lm_head, draft, tokens, u_accept, u_resample, temperature,
@@ -580,7 +592,7 @@ def spec_verify_lmhead(hidden, lm_head, draft, tokens, u_accept, u_resample, tem
     if out_num_accepted is None:
         out_num_accepted = torch.empty((B,), dtype=torch.int32, device=dev)
     if ws is None:
-        ws = lmhead_workspace(B, k, V, d, ddt, dev)
+        ws = lmhead_workspace(B, k, V, d, ddt, dev, stream)
     probs = torch.empty((B, k, 2), dtype=torch.float32, device=dev) if want_probs else None
     h = _stream_handle(stream, dev)
     if want_probs:
@@ -626,7 +638,7 @@ def spec_lmhead_logits(hidden, lm_head, out=None, stream=None):
     V = lm_head.shape[0]
     if out is None:
         out = torch.empty((M, V), dtype=torch.float32, device=hidden.device)
-    status = torch.zeros(1, dtype=torch.int32, device=hidden.device)
+    status = _zeros_on(stream, hidden.device, 1, torch.int32)
     rc = library().spec_lmhead_logits(_ptr(hidden), _ptr(lm_head), _ptr(out), M, V, d,
                                       _ptr(status), _stream_handle(stream, hidden.device))
     _check(rc, "spec_lmhead_logits")

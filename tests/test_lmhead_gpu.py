@@ -153,3 +153,26 @@ def test_bad_sizes_are_rejected():
     with pytest.raises(sv.SpecVerifyError):
         sv.spec_verify_lmhead(**bad)  # d = 96 is not a multiple of 64
     assert sv.spec_verify_lmhead_workspace_size(2, 32, 300, 64, sv.SPEC_F32) == 0
+
+
+def test_explicit_side_stream():
+    """Called on a stream other than the current one, with no workspace given:
+    the binding zero-fills its workspace (and the product's status word) on
+    that stream, so the kernels see them zeroed."""
+    c = synth.make_lmhead_case(20, 3, 3000, 256, "bf16", recipe="grid", seed=13, T=(0.0, 1.0))
+    d = to_device(c)
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    out = sv.spec_verify_lmhead(**d, stream=side)
+    logits, status = sv.spec_lmhead_logits(d["hidden"].view(-1, c.d), d["lm_head"], stream=side)
+    side.synchronize()
+    gt, gn = (x.cpu().numpy() for x in out)
+    rt, rn, tr = oracle.verify_lmhead(c.hidden, c.lm_head, c.draft, c.tokens, c.u_accept,
+                                      c.u_resample, c.temperature, nthreads=NTHREADS)
+    check_invariants(c, gt, gn)
+    rep = compare(c, gt, gn, rt, rn, tr)
+    assert rep["exempt"] <= max(1, rep["decisions"] // 1000), rep
+    # grid inputs: every logit is exact in fp32
+    want = oracle.lmhead_logits(c.hidden, c.lm_head).reshape(-1, c.V)
+    assert int(status.item()) == 0
+    assert np.array_equal(logits.cpu().numpy().astype(np.float64), want)
