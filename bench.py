@@ -219,6 +219,23 @@ def time_oracle(case, budget_s: float, threads: int):
     return done * case.k / t_used, done, t_used
 
 
+def oracle_alpha(case, n_seq: int):
+    """Analytic acceptance of the workload: alpha_i = sum_x min(p_i, q_i)
+    = 1 - sum_x max(0, p_i - q_i), averaged over the drafted positions of the
+    first `n_seq` sampling sequences (fp64, the oracle's softmax and residual).
+    Returns (mean, positions)."""
+    import oracle
+    from speculative_decoding_verification_65_gb300 import synth
+    vals = []
+    for b in np.flatnonzero(case.temperature > 0)[:n_seq]:
+        T = float(case.temperature[b])
+        for i in range(case.k):
+            p = oracle.softmax(synth.decode(case.target[b, i]), T)
+            q = oracle.softmax(synth.decode(case.draft[b, i]), T)
+            vals.append(1.0 - oracle.residual(p, q)[1])
+    return (float(np.mean(vals)) if vals else None), len(vals)
+
+
 def host_cores() -> int:
     try:
         return len(os.sched_getaffinity(0))
@@ -358,6 +375,10 @@ def run_ours(args):
     ms_per_step = total_ms / args.steps
     value = aggregate_rate(B * k, args.steps, world, total_ms / 1e3)
     status = sv.spec_verify_read_status(ws)
+    n_host = out_n.cpu().numpy()  # the last call's accept counts
+    ok_rows = n_host >= 0
+    acceptance = {"mean_accepted": float(n_host[ok_rows].mean()) if ok_rows.any() else None,
+                  "error_sequences": int((~ok_rows).sum()), "sequences": int(B)}
 
     # end to end through the public API on host buffers (pinned), every step
     # copies the inputs in and the results out
@@ -407,6 +428,9 @@ def run_ours(args):
                "sample": f"{n_seq} of {B} sequences of {workload}, {used:.1f} s on {cores} threads",
                "value_1thread": v1,
                "sample_1thread": f"{n1} sequences, {used1:.1f} s on 1 thread"}
+        a, n_pos = oracle_alpha(case, 16)
+        acceptance["oracle_alpha"] = a
+        acceptance["oracle_alpha_sample"] = f"{n_pos} drafted positions of the first 16 sampling sequences"
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
         "steps": args.steps, "warmup": max(args.warmup, 3), "ms_per_step": ms_per_step,
@@ -439,6 +463,7 @@ def run_ours(args):
         "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "steps": e2e_steps},
         "cpu_baseline": cpu,
+        "acceptance": acceptance,
         "device_status": status,
     }
     print(json.dumps(line), flush=True)

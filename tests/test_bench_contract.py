@@ -50,3 +50,21 @@ def test_reference_line(op, metric, monkeypatch):
     assert cb["value"] == d["value"] and cb["unit"] == d["unit"]
     assert d["e2e"] == {"value": d["value"], "unit": d["unit"], "h2d_bytes_per_step": 0,
                         "d2h_bytes_per_step": 0}
+
+
+@pytest.mark.parametrize("cfg,B,V", [(1, None, None), (4, 12, 2048)])
+def test_oracle_alpha_is_the_overlap_of_p_and_q(cfg, B, V):
+    """The verify line's analytic acceptance: the mean over drafted positions
+    of the sampling sequences of sum_x min(p, q), against scipy's softmax."""
+    import numpy as np
+    from scipy import special
+    from speculative_decoding_verification_65_gb300 import synth
+    case = synth.make_config(cfg, B=B, V=V)
+    a, n = bench.oracle_alpha(case, 16)
+    seqs = np.flatnonzero(case.temperature > 0)[:16]
+    assert n == len(seqs) * case.k
+    t, d = synth.decode(case.target), synth.decode(case.draft)
+    want = [np.minimum(special.softmax(t[b, i].astype(np.float64) / case.temperature[b]),
+                       special.softmax(d[b, i].astype(np.float64) / case.temperature[b])).sum()
+            for b in seqs for i in range(case.k)]
+    assert abs(a - float(np.mean(want))) < 1e-12
