@@ -196,7 +196,8 @@ def spec_verify_read_status(ws, stream=None) -> int:
     return int(st.value)
 
 
-def _marshal(target, draft, tokens, u_accept, u_resample, temperature):
+def _shapes(target, draft, tokens, u_accept, u_resample, temperature):
+    """Shapes and dtypes of the verification inputs: (B, k, V, dtype code)."""
     torch = _torch()
     if target.dim() != 3 or draft.dim() != 3:
         raise ValueError("target must be [B,k+1,V] and draft [B,k,V]")
@@ -213,6 +214,31 @@ def _marshal(target, draft, tokens, u_accept, u_resample, temperature):
                                   ("temperature", temperature, (B,), torch.float32)):
         if tuple(t.shape) != shape or t.dtype != dtype:
             raise ValueError(f"{name} must be {dtype} {shape}, got {t.dtype} {tuple(t.shape)}")
+    return B, k, V, dt
+
+
+def _check_out(name, t, shape, dtype):
+    if tuple(t.shape) != shape or t.dtype != dtype or not t.is_contiguous():
+        raise ValueError(f"{name} must be a contiguous {dtype} {shape} tensor, "
+                         f"got {t.dtype} {tuple(t.shape)}")
+
+
+def _dev_out(name, t, shape, dtype, dev):
+    """A caller-supplied output: contiguous, of the call's shape and dtype, on
+    the inputs' device (the kernels write every element of it)."""
+    _check_out(name, t, shape, dtype)
+    if not t.is_cuda or t.device != dev:
+        raise ValueError(f"{name} must be on {dev}, got {t.device}")
+
+
+def _check_ws(ws, dev):
+    torch = _torch()
+    if not ws.is_cuda or ws.device != dev or ws.dtype != torch.uint8 or not ws.is_contiguous():
+        raise ValueError(f"ws must be a contiguous uint8 tensor on {dev}")
+
+
+def _marshal(target, draft, tokens, u_accept, u_resample, temperature):
+    B, k, V, dt = _shapes(target, draft, tokens, u_accept, u_resample, temperature)
     for t in (target, draft, tokens, u_accept, u_resample, temperature):
         if not t.is_cuda or not t.is_contiguous():
             raise ValueError("all inputs must be contiguous CUDA tensors")
@@ -236,8 +262,11 @@ def spec_verify(target, draft, tokens, u_accept, u_resample, temperature,
         out_tokens = torch.empty((B, k + 1), dtype=torch.int32, device=dev)
     if out_num_accepted is None:
         out_num_accepted = torch.empty((B,), dtype=torch.int32, device=dev)
+    _dev_out("out_tokens", out_tokens, (B, k + 1), torch.int32, dev)
+    _dev_out("out_num_accepted", out_num_accepted, (B,), torch.int32, dev)
     if ws is None:
         ws = workspace(B, k, V, dt, dev, stream)
+    _check_ws(ws, dev)
     rc = library().spec_verify(_ptr(target), _ptr(draft), _ptr(tokens), _ptr(u_accept),
                                _ptr(u_resample), _ptr(temperature), _ptr(out_tokens),
                                _ptr(out_num_accepted), B, k, V, dt, _ptr(ws), ws.numel(),
@@ -269,9 +298,12 @@ def spec_verify_filtered(target, draft, tokens, u_accept, u_resample, temperatur
         out_tokens = torch.empty((B, k + 1), dtype=torch.int32, device=dev)
     if out_num_accepted is None:
         out_num_accepted = torch.empty((B,), dtype=torch.int32, device=dev)
+    _dev_out("out_tokens", out_tokens, (B, k + 1), torch.int32, dev)
+    _dev_out("out_num_accepted", out_num_accepted, (B,), torch.int32, dev)
     probs = torch.empty((B, k, 2), dtype=torch.float32, device=dev) if want_probs else None
     if ws is None:
         ws = workspace(B, k, V, dt, dev, stream)
+    _check_ws(ws, dev)
     rc = library().spec_verify_filtered(_ptr(target), _ptr(draft), _ptr(tokens), _ptr(u_accept),
                                         _ptr(u_resample), _ptr(temperature), _ptr(top_k),
                                         _ptr(top_p), _ptr(out_tokens), _ptr(out_num_accepted),
@@ -289,8 +321,13 @@ def spec_verify_filtered_timed(target, draft, tokens, u_accept, u_resample, temp
     """spec_verify_filtered recording SPEC_FILTERED_STAGES events: after the
     statistics, the filter (both of its kernels), the accept scan, the draw
     tiles and the final search."""
+    torch = _torch()
     B, k, V, dt = _marshal(target, draft, tokens, u_accept, u_resample, temperature)
-    _filters(B, target.device, top_k, top_p)
+    dev = target.device
+    _filters(B, dev, top_k, top_p)
+    _dev_out("out_tokens", out_tokens, (B, k + 1), torch.int32, dev)
+    _dev_out("out_num_accepted", out_num_accepted, (B,), torch.int32, dev)
+    _check_ws(ws, dev)
     handles = (ctypes.c_void_p * SPEC_FILTERED_STAGES)(
         *[ctypes.c_void_p(e.cuda_event) for e in stage_events])
     rc = library().spec_verify_filtered_timed(
@@ -306,7 +343,12 @@ def spec_verify_timed(target, draft, tokens, u_accept, u_resample, temperature,
     """spec_verify recording the given torch.cuda.Event objects (SPEC_STAGES of
     them, recorded once beforehand so that they exist) after each stage:
     statistics, accept scan, draw tiles, final search."""
+    torch = _torch()
     B, k, V, dt = _marshal(target, draft, tokens, u_accept, u_resample, temperature)
+    dev = target.device
+    _dev_out("out_tokens", out_tokens, (B, k + 1), torch.int32, dev)
+    _dev_out("out_num_accepted", out_num_accepted, (B,), torch.int32, dev)
+    _check_ws(ws, dev)
     handles = (ctypes.c_void_p * SPEC_STAGES)(*[ctypes.c_void_p(e.cuda_event) for e in stage_events])
     rc = library().spec_verify_timed(_ptr(target), _ptr(draft), _ptr(tokens), _ptr(u_accept),
                                      _ptr(u_resample), _ptr(temperature), _ptr(out_tokens),
@@ -323,7 +365,10 @@ def spec_verify_noalloc(target, draft, tokens, u_accept, u_resample, temperature
     instead (see include/spec_verify.h).  The output tensors are supplied by
     the caller, so this wrapper allocates nothing either.  Calls that overlap
     on the GPU share that scratch and race."""
+    torch = _torch()
     B, k, V, dt = _marshal(target, draft, tokens, u_accept, u_resample, temperature)
+    _dev_out("out_tokens", out_tokens, (B, k + 1), torch.int32, target.device)
+    _dev_out("out_num_accepted", out_num_accepted, (B,), torch.int32, target.device)
     rc = library().spec_verify_noalloc(_ptr(target), _ptr(draft), _ptr(tokens), _ptr(u_accept),
                                        _ptr(u_resample), _ptr(temperature), _ptr(out_tokens),
                                        _ptr(out_num_accepted), B, k, V, dt,
@@ -348,6 +393,7 @@ def spec_verify_probs(target, draft, tokens, u_accept, u_resample, temperature,
     probs = torch.empty((B, k, 2), dtype=torch.float32, device=dev)
     if ws is None:
         ws = workspace(B, k, V, dt, dev, stream)
+    _check_ws(ws, dev)
     rc = library().spec_verify_probs(_ptr(target), _ptr(draft), _ptr(tokens), _ptr(u_accept),
                                      _ptr(u_resample), _ptr(temperature), _ptr(out_tokens),
                                      _ptr(out_n), _ptr(probs), B, k, V, dt, _ptr(ws),
@@ -363,18 +409,22 @@ def spec_verify_host(target, draft, tokens, u_accept, u_resample, temperature,
     spec_verify_host_arena_size bytes), verifies, copies the outputs back and
     synchronises.  Returns host (out_tokens, out_num_accepted)."""
     torch = _torch()
-    if target.is_cuda:
-        raise ValueError("spec_verify_host takes host tensors")
-    B, k1, V = target.shape
-    k = k1 - 1
-    dt = _dtype_code(target)
+    B, k, V, dt = _shapes(target, draft, tokens, u_accept, u_resample, temperature)
+    for t in (target, draft, tokens, u_accept, u_resample, temperature):
+        if t.is_cuda or not t.is_contiguous():
+            raise ValueError("host inputs must be contiguous CPU tensors")
+    if not arena.is_cuda or arena.dtype != torch.uint8 or not arena.is_contiguous():
+        raise ValueError("arena must be a contiguous uint8 CUDA tensor")
+    for name, t, shape in (("out_tokens", out_tokens, (B, k + 1)),
+                           ("out_num_accepted", out_num_accepted, (B,))):
+        if t is not None:
+            _check_out(name, t, shape, torch.int32)
+            if t.is_cuda:
+                raise ValueError(f"{name} must be a host tensor")
     if out_tokens is None:
         out_tokens = torch.empty((B, k + 1), dtype=torch.int32, pin_memory=True)
     if out_num_accepted is None:
         out_num_accepted = torch.empty((B,), dtype=torch.int32, pin_memory=True)
-    for t in (target, draft, tokens, u_accept, u_resample, temperature):
-        if t.is_cuda or not t.is_contiguous():
-            raise ValueError("host inputs must be contiguous CPU tensors")
     rc = library().spec_verify_host(_ptr(target), _ptr(draft), _ptr(tokens), _ptr(u_accept),
                                     _ptr(u_resample), _ptr(temperature), _ptr(out_tokens),
                                     _ptr(out_num_accepted), B, k, V, dt, _ptr(arena),
@@ -401,7 +451,8 @@ def sample_workspace(R: int, V: int, dtype: int, device=None, stream=None):
     return _cached_workspace(need, device, s)
 
 
-def _marshal_sample(logits, u, temperature):
+def _sample_shapes(logits, u, temperature):
+    """Shapes and dtypes of the sampling inputs: (R, V, dtype code)."""
     torch = _torch()
     if logits.dim() != 2:
         raise ValueError("logits must be [R, V]")
@@ -410,6 +461,11 @@ def _marshal_sample(logits, u, temperature):
     for name, t in (("u", u), ("temperature", temperature)):
         if tuple(t.shape) != (R,) or t.dtype != torch.float32:
             raise ValueError(f"{name} must be float32 ({R},), got {t.dtype} {tuple(t.shape)}")
+    return R, V, dt
+
+
+def _marshal_sample(logits, u, temperature):
+    R, V, dt = _sample_shapes(logits, u, temperature)
     for t in (logits, u, temperature):
         if not t.is_cuda or not t.is_contiguous():
             raise ValueError("all inputs must be contiguous CUDA tensors")
@@ -428,8 +484,10 @@ def spec_sample(logits, u, temperature, out=None, ws=None, stream=None):
     dev = logits.device
     if out is None:
         out = torch.empty((R,), dtype=torch.int32, device=dev)
+    _dev_out("out", out, (R,), torch.int32, dev)
     if ws is None:
         ws = sample_workspace(R, V, dt, dev, stream)
+    _check_ws(ws, dev)
     rc = library().spec_sample(_ptr(logits), _ptr(u), _ptr(temperature), _ptr(out), R, V, dt,
                                _ptr(ws), ws.numel(), _stream_handle(stream, dev))
     _check(rc, "spec_sample")
@@ -440,7 +498,10 @@ def spec_sample_timed(logits, u, temperature, out, ws, stage_events, stream=None
     """spec_sample recording the given torch.cuda.Event objects
     (SPEC_SAMPLE_STAGES of them, recorded once beforehand) after each kernel:
     chunk records, pick."""
+    torch = _torch()
     R, V, dt = _marshal_sample(logits, u, temperature)
+    _dev_out("out", out, (R,), torch.int32, logits.device)
+    _check_ws(ws, logits.device)
     handles = (ctypes.c_void_p * SPEC_SAMPLE_STAGES)(
         *[ctypes.c_void_p(e.cuda_event) for e in stage_events])
     rc = library().spec_sample_timed(_ptr(logits), _ptr(u), _ptr(temperature), _ptr(out), R, V,
@@ -478,14 +539,17 @@ def spec_sample_host(logits, u, temperature, arena, out=None, stream=None):
     spec_sample_host_arena_size bytes), samples, copies the tokens back and
     synchronises.  Returns the host int32 [R] tokens."""
     torch = _torch()
-    if logits.is_cuda or logits.dim() != 2:
-        raise ValueError("spec_sample_host takes a host [R, V] tensor")
-    R, V = logits.shape
-    dt = _dtype_code(logits)
+    R, V, dt = _sample_shapes(logits, u, temperature)
     for t in (logits, u, temperature):
         if t.is_cuda or not t.is_contiguous():
             raise ValueError("host inputs must be contiguous CPU tensors")
-    if out is None:
+    if not arena.is_cuda or arena.dtype != torch.uint8 or not arena.is_contiguous():
+        raise ValueError("arena must be a contiguous uint8 CUDA tensor")
+    if out is not None:
+        _check_out("out", out, (R,), torch.int32)
+        if out.is_cuda:
+            raise ValueError("out must be a host tensor")
+    else:
         out = torch.empty((R,), dtype=torch.int32, pin_memory=True)
     rc = library().spec_sample_host(_ptr(logits), _ptr(u), _ptr(temperature), _ptr(out), R, V,
                                     dt, _ptr(arena), arena.numel(),
@@ -591,8 +655,11 @@ def spec_verify_lmhead(hidden, lm_head, draft, tokens, u_accept, u_resample, tem
         out_tokens = torch.empty((B, k + 1), dtype=torch.int32, device=dev)
     if out_num_accepted is None:
         out_num_accepted = torch.empty((B,), dtype=torch.int32, device=dev)
+    _dev_out("out_tokens", out_tokens, (B, k + 1), torch.int32, dev)
+    _dev_out("out_num_accepted", out_num_accepted, (B,), torch.int32, dev)
     if ws is None:
         ws = lmhead_workspace(B, k, V, d, ddt, dev, stream)
+    _check_ws(ws, dev)
     probs = torch.empty((B, k, 2), dtype=torch.float32, device=dev) if want_probs else None
     h = _stream_handle(stream, dev)
     if want_probs:
@@ -616,8 +683,13 @@ def spec_verify_lmhead_timed(hidden, lm_head, draft, tokens, u_accept, u_resampl
     """spec_verify_lmhead recording SPEC_LMHEAD_STAGES events, one after each
     kernel (draft chunk records, statistics GEMM, accept scan, draw GEMM,
     final search)."""
+    torch = _torch()
     B, k, V, d, ddt = _marshal_lmhead(hidden, lm_head, draft, tokens, u_accept, u_resample,
                                       temperature)
+    dev = hidden.device
+    _dev_out("out_tokens", out_tokens, (B, k + 1), torch.int32, dev)
+    _dev_out("out_num_accepted", out_num_accepted, (B,), torch.int32, dev)
+    _check_ws(ws, dev)
     handles = (ctypes.c_void_p * SPEC_LMHEAD_STAGES)(
         *[ctypes.c_void_p(e.cuda_event) for e in stage_events])
     rc = library().spec_verify_lmhead_timed(
@@ -634,10 +706,16 @@ def spec_lmhead_logits(hidden, lm_head, out=None, stream=None):
     torch = _torch()
     if hidden.dtype != torch.bfloat16 or lm_head.dtype != torch.bfloat16:
         raise TypeError("hidden and lm_head must be bfloat16")
+    if hidden.dim() != 2 or lm_head.dim() != 2 or lm_head.shape[1] != hidden.shape[1]:
+        raise ValueError("hidden [M,d] and lm_head [V,d] expected")
+    for t in (hidden, lm_head):
+        if not t.is_cuda or not t.is_contiguous() or t.device != hidden.device:
+            raise ValueError("hidden and lm_head must be contiguous CUDA tensors on one device")
     M, d = hidden.shape
     V = lm_head.shape[0]
     if out is None:
         out = torch.empty((M, V), dtype=torch.float32, device=hidden.device)
+    _dev_out("out", out, (M, V), torch.float32, hidden.device)
     status = _zeros_on(stream, hidden.device, 1, torch.int32)
     rc = library().spec_lmhead_logits(_ptr(hidden), _ptr(lm_head), _ptr(out), M, V, d,
                                       _ptr(status), _stream_handle(stream, hidden.device))

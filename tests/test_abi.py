@@ -258,3 +258,4 @@ def test_lmhead_bad_sizes_and_small_workspace(lib):
     # 2^26 rows x 2^20 columns: 2^31 tiles, more than the GEMM counts
     assert lib.spec_lmhead_logits(vp(LGOOD[0]), vp(LGOOD[1]), vp(LGOOD[2]), 1 << 26, 1 << 20, 64,
                                   vp(LGOOD[3]), None) == sv.SPEC_EINVAL
+
