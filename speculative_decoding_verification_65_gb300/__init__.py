@@ -609,10 +609,12 @@ def _marshal_lmhead(hidden, lm_head, draft, tokens, u_accept, u_resample, temper
     k = k1 - 1
     if lm_head.shape[1] != d or tuple(draft.shape) != (B, k, V):
         raise ValueError("shape mismatch between hidden, lm_head and draft")
-    for name, t, shape in (("tokens", tokens, (B, k)), ("u_accept", u_accept, (B, k)),
-                           ("u_resample", u_resample, (B,)), ("temperature", temperature, (B,))):
-        if tuple(t.shape) != shape:
-            raise ValueError(f"{name} must have shape {shape}")
+    for name, t, shape, dtype in (("tokens", tokens, (B, k), torch.int32),
+                                  ("u_accept", u_accept, (B, k), torch.float32),
+                                  ("u_resample", u_resample, (B,), torch.float32),
+                                  ("temperature", temperature, (B,), torch.float32)):
+        if tuple(t.shape) != shape or t.dtype != dtype:
+            raise ValueError(f"{name} must be {dtype} {shape}, got {t.dtype} {tuple(t.shape)}")
     for t in (hidden, lm_head, draft, tokens, u_accept, u_resample, temperature):
         if not t.is_cuda or not t.is_contiguous():
             raise ValueError("all tensors must be contiguous CUDA tensors")
