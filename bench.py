@@ -456,7 +456,7 @@ def run_ours(args):
                      "frac_of_read_probe": achieved / read_gbs if read_gbs else None,
                      "step_GBps": alg_bytes / (ms_per_step / 1e3) / 1e9},
         "stage_ms": {"stats": stage_ms[0], "scan": stage_ms[1], "draw": stage_ms[2],
-                     "final": stage_ms[3]},
+                     "final": stage_ms[3], "exact_draws": stage_ms[4]},
         "ms_per_step_median_staged": statistics.median(
             s.elapsed_time(e[-1]) for s, e in zip(starts, stages)),
         "clocks": clk.summary(),
@@ -694,7 +694,7 @@ def run_ours_filtered(args):
                      "stats_kernel": {"achieved": stats_achieved,
                                       "frac": stats_achieved / peak}},
         "stage_ms": {"stats": stage_ms[0], "filter": stage_ms[1], "scan": stage_ms[2],
-                     "draw": stage_ms[3], "final": stage_ms[4]},
+                     "draw": stage_ms[3], "final": stage_ms[4], "exact_draws": stage_ms[5]},
         "clocks": clk.summary(),
         "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": int(B * (k + 2) * 4), "steps": e2e_steps,

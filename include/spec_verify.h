@@ -19,7 +19,11 @@
  *     token");
  *   - a draw is inverse-CDF with u_resample[b]: the smallest token x whose
  *     running mass C(x) exceeds u * R, R the total mass (the pages say
- *     "sample"; this is the plain reading);
+ *     "sample"; this is the plain reading).  Draws are computed in fp32; a
+ *     draw whose u * R falls within a few 1e-6 of its cell's edge in fp32 is
+ *     computed again in float-float arithmetic with exact fixed-point sums
+ *     (about 1e-12 of R), so the token equals the exactly rounded result
+ *     except for uniforms within ~1e-12 of an edge;
  *   - T == 0 is greedy mode: g_i is accepted while it equals argmax t_i, and the
  *     correction or bonus is the target argmax ("How does speculative decoding
  *     work, why is it lossless, and how much does it speed things up?",
@@ -60,7 +64,7 @@
 extern "C" {
 #endif
 
-#define SPEC_VERIFY_ABI_VERSION 1
+#define SPEC_VERIFY_ABI_VERSION 2
 #define SPEC_MAX_K 32
 #define SPEC_MAX_V (1 << 20)
 
@@ -91,8 +95,9 @@ const char *spec_verify_strerror(int32_t status);
  * 256-byte header (the status word), one 16-byte partial per 128 KB of every
  * row, and per sequence an 80-byte draw record, its inverse-CDF chunk totals
  * (32 bytes per 16 KB of a row), its bonus row's chunk records (8 bytes per
- * 4 KB of a row) and a 16-byte top-k / top-p record per row (read by
- * spec_verify_filtered only).  Returns 0 for sizes out of range.
+ * 4 KB of a row), a 16-byte top-k / top-p record per row (read by
+ * spec_verify_filtered only), and room for its exact draw (2156 bytes plus
+ * 32 bytes per 2048 elements of a row).  Returns 0 for sizes out of range.
  * Host-only; needs no GPU.
  */
 size_t spec_verify_workspace_size(int32_t B, int32_t k, int32_t V, int32_t dtype);
@@ -122,9 +127,10 @@ int32_t spec_verify_workspace_reset(void *workspace, size_t workspace_bytes, voi
  *                    word (see SPEC_DEV_OK).  Two calls in flight at once must not share
  *                    one (the same stream runs calls in order, so one per stream suffices).
  *   stream           cudaStream_t as void*.
- * Four kernels run in order on `stream`: row statistics, accept scan, draw
- * tiles, final search.  Returns SPEC_OK once they are launched; errors are
- * listed above.
+ * Five kernels run in order on `stream`: row statistics, accept scan, draw
+ * tiles, final search, exact draws (of the sequences the final search listed;
+ * with none listed it only reads the count).  Returns SPEC_OK once they are
+ * launched; errors are listed above.
  */
 int32_t spec_verify(const void *target_logits, const void *draft_logits,
                     const int32_t *draft_tokens, const float *u_accept,
@@ -147,6 +153,27 @@ int32_t spec_verify_probs(const void *target_logits, const void *draft_logits,
                           void *workspace, size_t workspace_bytes, void *stream);
 
 /*
+ * spec_verify with a trace of each draw, for checking the draw against a
+ * reference: out_draw (device int32 [B, 4]) receives, for every sequence that
+ * draws from a distribution (T > 0, no sequence error), [0] the token of the
+ * fp32 search, [1] 1 if the draw was listed for the exact recomputation,
+ * [2] the token written to out_tokens, [3] the bits of a float: the fp32
+ * search's distance from u to the nearer edge of the cell it chose, as a
+ * fraction of the total mass R (0 when a rounding fallback was taken).
+ * Other sequences' entries
+ * are left as they were.  resolve_all != 0 lists every draw (the exact draw
+ * then decides every token).  out_probs as spec_verify_probs, or NULL.
+ * Same arguments and behaviour as spec_verify otherwise.
+ */
+int32_t spec_verify_trace(const void *target_logits, const void *draft_logits,
+                          const int32_t *draft_tokens, const float *u_accept,
+                          const float *u_resample, const float *temperature,
+                          int32_t *out_tokens, int32_t *out_num_accepted, float *out_probs,
+                          int32_t *out_draw, int32_t resolve_all,
+                          int32_t B, int32_t k, int32_t V, int32_t dtype,
+                          void *workspace, size_t workspace_bytes, void *stream);
+
+/*
  * spec_verify with top-k / top-p filtered distributions.  The pages require
  * draft and target to share their sampling parameters, top-p among them
  * ("Speculative Decoding and the Art of Fast LLM Inference", "Why It Stays
@@ -163,10 +190,10 @@ int32_t spec_verify_probs(const void *target_logits, const void *draft_logits,
  *          Q = q~_i(g_i) (NaN for greedy and error sequences)
  * A draft token outside the draft's kept set (q~(g) = 0) is a sequence error.
  * Other arguments, the workspace (spec_verify_workspace_size) and errors as
- * spec_verify.  Six kernels run: statistics; the filter in two (per row,
+ * spec_verify.  Seven kernels run: statistics; the filter in two (per row,
  * the end of the kept set: one streaming pass over the row in the common
  * case, then the rows it could not cut, by a second pass or a radix search
- * over the order key); accept scan; draw tiles; final search.
+ * over the order key); accept scan; draw tiles; final search; exact draws.
  */
 int32_t spec_verify_filtered(const void *target_logits, const void *draft_logits,
                              const int32_t *draft_tokens, const float *u_accept,
@@ -179,9 +206,10 @@ int32_t spec_verify_filtered(const void *target_logits, const void *draft_logits
 /*
  * spec_verify_filtered with stage events as in spec_verify_timed:
  * SPEC_FILTERED_STAGES of them, after the statistics, the filter (both of
- * its kernels), the accept scan, the draw tiles and the final search.
+ * its kernels), the accept scan, the draw tiles, the final search and the
+ * exact draws.
  */
-#define SPEC_FILTERED_STAGES 5
+#define SPEC_FILTERED_STAGES 6
 int32_t spec_verify_filtered_timed(const void *target_logits, const void *draft_logits,
                                    const int32_t *draft_tokens, const float *u_accept,
                                    const float *u_resample, const float *temperature,
@@ -195,10 +223,11 @@ int32_t spec_verify_filtered_timed(const void *target_logits, const void *draft_
  * spec_verify with per-stage timing: `stage_events` (nullable; entries may be
  * NULL) holds SPEC_STAGES cudaEvent_t handles, created by the caller, that are
  * recorded on `stream` after each stage: row statistics, accept scan, draw
- * tiles, final search.  Same arguments and behaviour as spec_verify
- * otherwise.  Lets a benchmark time the HBM-bound statistics stage alone.
+ * tiles, final search, exact draws.  Same arguments and behaviour as
+ * spec_verify otherwise.  Lets a benchmark time the HBM-bound statistics
+ * stage alone.
  */
-#define SPEC_STAGES 4
+#define SPEC_STAGES 5
 int32_t spec_verify_timed(const void *target_logits, const void *draft_logits,
                           const int32_t *draft_tokens, const float *u_accept,
                           const float *u_resample, const float *temperature,

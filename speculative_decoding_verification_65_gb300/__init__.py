@@ -27,9 +27,9 @@ SPEC_DEV_OK = 0
 SPEC_DEV_WAIT_TIMEOUT = 1
 SPEC_MAX_K = 32
 SPEC_MAX_V = 1 << 20
-SPEC_STAGES = 4
+SPEC_STAGES = 5
 SPEC_SAMPLE_STAGES = 2
-SPEC_FILTERED_STAGES = 5
+SPEC_FILTERED_STAGES = 6
 SPEC_LMHEAD_STAGES = 5
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
@@ -66,6 +66,8 @@ def library():
         lib.spec_verify.argtypes = [vp] * 8 + [i32] * 4 + [vp, sz, vp]
         lib.spec_verify_probs.restype = i32
         lib.spec_verify_probs.argtypes = [vp] * 9 + [i32] * 4 + [vp, sz, vp]
+        lib.spec_verify_trace.restype = i32
+        lib.spec_verify_trace.argtypes = [vp] * 10 + [i32] * 5 + [vp, sz, vp]
         lib.spec_verify_timed.restype = i32
         lib.spec_verify_timed.argtypes = [vp] * 8 + [i32] * 4 + [vp, sz, vp, vp]
         lib.spec_verify_filtered.restype = i32
@@ -320,7 +322,7 @@ def spec_verify_filtered_timed(target, draft, tokens, u_accept, u_resample, temp
                                stream=None):
     """spec_verify_filtered recording SPEC_FILTERED_STAGES events: after the
     statistics, the filter (both of its kernels), the accept scan, the draw
-    tiles and the final search."""
+    tiles, the final search and the exact draws."""
     torch = _torch()
     B, k, V, dt = _marshal(target, draft, tokens, u_accept, u_resample, temperature)
     dev = target.device
@@ -342,7 +344,7 @@ def spec_verify_timed(target, draft, tokens, u_accept, u_resample, temperature,
                       out_tokens, out_num_accepted, ws, stage_events, stream=None):
     """spec_verify recording the given torch.cuda.Event objects (SPEC_STAGES of
     them, recorded once beforehand so that they exist) after each stage:
-    statistics, accept scan, draw tiles, final search."""
+    statistics, accept scan, draw tiles, final search, exact draws."""
     torch = _torch()
     B, k, V, dt = _marshal(target, draft, tokens, u_accept, u_resample, temperature)
     dev = target.device
@@ -400,6 +402,33 @@ def spec_verify_probs(target, draft, tokens, u_accept, u_resample, temperature,
                                      ws.numel(), _stream_handle(stream, dev))
     _check(rc, "spec_verify_probs")
     return out_tokens, out_n, probs
+
+
+def spec_verify_trace(target, draft, tokens, u_accept, u_resample, temperature,
+                      resolve_all=False, want_probs=False, ws=None, stream=None):
+    """spec_verify with the trace of each draw (include/spec_verify.h):
+    returns (out_tokens, out_num_accepted, draw [B,4] int32, probs or None).
+    draw[b] = (fp32 token, listed for the exact draw, token written, the fp32
+    distance of u to its cell's nearer edge as float32 bits);
+    sequences that draw nothing keep -2 everywhere.  resolve_all lists every
+    draw."""
+    torch = _torch()
+    B, k, V, dt = _marshal(target, draft, tokens, u_accept, u_resample, temperature)
+    dev = target.device
+    out_tokens = torch.empty((B, k + 1), dtype=torch.int32, device=dev)
+    out_n = torch.empty((B,), dtype=torch.int32, device=dev)
+    draw = torch.full((B, 4), -2, dtype=torch.int32, device=dev)
+    probs = torch.empty((B, k, 2), dtype=torch.float32, device=dev) if want_probs else None
+    if ws is None:
+        ws = workspace(B, k, V, dt, dev, stream)
+    _check_ws(ws, dev)
+    rc = library().spec_verify_trace(_ptr(target), _ptr(draft), _ptr(tokens), _ptr(u_accept),
+                                     _ptr(u_resample), _ptr(temperature), _ptr(out_tokens),
+                                     _ptr(out_n), _ptr(probs), _ptr(draw),
+                                     1 if resolve_all else 0, B, k, V, dt, _ptr(ws),
+                                     ws.numel(), _stream_handle(stream, dev))
+    _check(rc, "spec_verify_trace")
+    return out_tokens, out_n, draw, probs
 
 
 def spec_verify_host(target, draft, tokens, u_accept, u_resample, temperature,

@@ -19,6 +19,7 @@ CSRC = os.path.join(PKG, "csrc")
 SRCS = [os.path.join(CSRC, "spec_verify.cu"), os.path.join(CSRC, "spec_sample.cu"),
         os.path.join(CSRC, "spec_lmhead.cu"), os.path.join(CSRC, "bench_read.cu")]
 DEPS = [os.path.join(CSRC, "device_common.cuh"), os.path.join(CSRC, "internal.h"),
+        os.path.join(CSRC, "resolve.cuh"), os.path.join(CSRC, "exp2_table.h"),
         os.path.join(ROOT, "include", "spec_lmhead.h"),
         os.path.join(ROOT, "include", "spec_verify.h"),
         os.path.join(ROOT, "include", "spec_sample.h"),

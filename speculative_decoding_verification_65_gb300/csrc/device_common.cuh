@@ -22,7 +22,11 @@ struct WsHeader {
     int status;
     unsigned int next_item;   // row counter of the window filter kernel (zeroed by the first kernel)
     unsigned int next_item2;  // chunk counter of the radix filter kernel (likewise)
-    unsigned int pad[61];
+    unsigned int n_flag;      // rows listed for an exact draw (likewise)
+    unsigned int next_resolve;  // work-item counter of the exact draws (likewise)
+    unsigned int n_slow_ratio;  // exact draws whose fp32 mass ratio was too far off (diagnostic)
+    unsigned int n_slow_kinks;  // exact draws with too many undecided elements (diagnostic)
+    unsigned int pad[57];
 };
 static_assert(sizeof(WsHeader) == 256, "header is 256 bytes");
 
@@ -508,10 +512,17 @@ __device__ __forceinline__ float lane_scan(float x, int lane)
 // over its elements in index order; the token is the smallest x with
 // C(x) > u * R.  A threshold that rounding leaves past a running total takes
 // the last positive weight before it.  Returns -1 if no weight is positive.
+// *near (every lane) is set when u * R lies within guard * R of the chosen
+// cell's edges as computed here, or a rounding fallback was taken: the fp32
+// sums cannot tell such a draw apart from its neighbour's.
 template <int DT>
 __device__ int records_draw(const float2 *rc, int NC, float m, float c, float u,
-                            const void *logits, size_t row, int V, int lane)
+                            const void *logits, size_t row, int V, int lane, float guard,
+                            bool &near, float *gap_u = nullptr)
 {
+    near = false;
+    if (gap_u)
+        *gap_u = 0.0f;
     using L = Lg<DT>;
     constexpr int VEC = L::VEC;
     constexpr int RC = 8;  // records a lane keeps in registers
@@ -590,8 +601,10 @@ __device__ int records_draw(const float2 *rc, int NC, float m, float c, float u,
             chunk = lastpos;
             cbefore = lastC;
             Mc = lastM;
+            near = true;
         }
     }
+    near = __shfl_sync(0xffffffffu, near ? 1 : 0, Lw) != 0 || !cross;
     chunk = __shfl_sync(0xffffffffu, chunk, Lw);
     if (chunk < 0)
         return -1;
@@ -605,7 +618,9 @@ __device__ int records_draw(const float2 *rc, int NC, float m, float c, float u,
 #pragma unroll
     for (int uv = 0; uv < CHUNK_UV; ++uv)
         raw[uv] = row_vec<DT>(logits, row, vb + uv * 32 + lane, V);
-    const float tloc = (theta - cbefore) / ex2((Mc - m) * c);
+    const float csc = ex2((Mc - m) * c);
+    const float tloc = (theta - cbefore) / csc;
+    const float gloc = guard * (Rtot / csc);  // the guard in the chunk's units
     const unsigned long long c2 = f2(c, c);
     float carry = 0.0f;
     int tok = -1, last_u = -1, last_lane = -1;
@@ -625,22 +640,34 @@ __device__ int records_draw(const float2 *rc, int NC, float m, float c, float u,
         if (hit) {
             const int hl = __ffs(hit) - 1;
             int t = -1;
+            int nr = 0;
+            float gl = 0.0f;
             if (lane == hl) {
                 float run = carry + (in_l - tau);
                 int lastj = -1;
 #pragma unroll
                 for (int j = 0; j < VEC; ++j) {
                     if (t < 0 && e[j] > 0.0f) {
+                        const float prev = run;
                         run = run + e[j];
                         lastj = j;
-                        if (run > tloc)
+                        if (run > tloc) {
                             t = v * VEC + j;
+                            nr = (tloc - prev < gloc || run - tloc < gloc) ? 1 : 0;
+                            gl = fminf(tloc - prev, run - tloc) * (csc / Rtot);
+                        }
                     }
                 }
-                if (t < 0)
+                if (t < 0) {
                     t = v * VEC + lastj;  // rounding within the lane: its last positive weight
+                    nr = 1;
+                }
             }
             tok = __shfl_sync(0xffffffffu, t, hl);
+            near = near || __shfl_sync(0xffffffffu, nr, hl) != 0;
+            gl = __shfl_sync(0xffffffffu, gl, hl);
+            if (gap_u)
+                *gap_u = gl;
         } else {
             const unsigned pos = __ballot_sync(0xffffffffu, tau > 0.0f);
             if (pos) {
@@ -668,6 +695,7 @@ __device__ int records_draw(const float2 *rc, int NC, float m, float c, float u,
             }
         }
         tok = __shfl_sync(0xffffffffu, t, last_lane);
+        near = true;
     }
     return tok;
 }

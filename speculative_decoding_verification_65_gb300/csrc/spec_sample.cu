@@ -365,7 +365,8 @@ __global__ void __launch_bounds__(PICK_WARPS * 32) pick_kernel(const SParams P)
         return;
     }
 
-    const int tok = records_draw<DT>(rc, P.NC, m, c, uu, P.logits, (size_t)r, P.V, lane);
+    bool near = false;
+    const int tok = records_draw<DT>(rc, P.NC, m, c, uu, P.logits, (size_t)r, P.V, lane, 0.0f, near);
     if (lane == 0)
         P.out[r] = tok;
 }

@@ -42,6 +42,7 @@
 
 #include "spec_verify.h"
 #include "device_common.cuh"
+#include "resolve.cuh"
 
 namespace {
 
@@ -149,6 +150,17 @@ struct Params {
     const int32_t *top_k;  // [B] or null (filtered calls)
     const float *top_p;    // [B] or null (filtered calls)
     FiltRec *filt;     // [B][rows] (filtered calls)
+    // exact draws of the rows whose fp32 draw is near a cell boundary
+    int *rlist;            // [B] sequences listed (count in hdr->n_flag)
+    RJob *rjob;            // [B] their exact-draw records (written with the list)
+    unsigned int *rdone;   // [B] chunks finished per listed sequence
+    unsigned int *rkcnt;   // [B] undecided elements per listed sequence
+    RkRec *rkink;          // [B][RKCAP]
+    RzRec *rrec;           // [B][RNC] chunk records
+    int RNC;               // resolve chunks per row
+    float guard_abs;       // residual draws: list when u*R is within this of a cell edge
+    float guard_rel;       // bonus / target-row draws: within this times R
+    int32_t *out_draw;     // nullable [B][4]: fp32 token, listed, exact token, reserved
     int B, k, V;
     int NS;            // tiles per row
     int NSS;           // super-tiles per row
@@ -282,9 +294,13 @@ __global__ void __launch_bounds__(NTHREADS, 2) stats_kernel(const Params P)
     constexpr int SEG = TILE_BYTES / L::ES;
 
     if (tid == 0) {
-        if (blockIdx.x == 0) {  // the filter kernels' counters (they run after this grid)
+        if (blockIdx.x == 0) {  // later kernels' counters (they run after this grid)
             P.hdr->next_item = 0u;
             P.hdr->next_item2 = 0u;
+            P.hdr->n_flag = 0u;
+            P.hdr->next_resolve = 0u;
+            P.hdr->n_slow_ratio = 0u;
+            P.hdr->n_slow_kinks = 0u;
         }
         for (int s = 0; s < STAGES; ++s) {
             mbar_init(&S.full[s], 1);
@@ -2447,11 +2463,16 @@ __global__ void __launch_bounds__(NT, FILT ? 4 : 6) draw_kernel(const Params P)
 // E the lane's exclusive scan and s the lane's running sum.  The token is the
 // smallest x with w(x) > 0 and C(x) > u * R, R the row total; if rounding
 // leaves none in the chunk found, the chunk's last positive-weight token.
-// Returns -1 when the total mass is zero.
+// Returns -1 when the total mass is zero.  `near` is set (every lane) when
+// u * R lies within the guard of the chosen cell's edges, or a rounding
+// fallback was taken: residual weights are probabilities, so their guard is
+// absolute; target-row weights are unnormalised, so theirs is relative to R.
 template <int DT, bool FILT>
 __device__ int locate(const Params &P, const JobRec &J, int mode, const float *ch, float *btot,
-                      int nblk, int lane)
+                      int nblk, int lane, bool &near, float &gap_u)
 {
+    near = true;
+    gap_u = 0.0f;
     using L = Lg<DT>;
     constexpr int VEC = L::VEC;
     // block totals: 8 chunk totals left to right (two 16-byte loads per block,
@@ -2540,19 +2561,32 @@ __device__ int locate(const Params &P, const JobRec &J, int mode, const float *c
     warp_scan(s, lane, incl, excl);
     const float pre = W + excl;
     int cand = INT_MAX, lastp = -1;
+    float gap = 0.0f;  // distance of u * R to the nearer edge of the lane's crossing cell
 #pragma unroll
     for (int j = 0; j < VEC; ++j) {
         const int e = v * VEC + j;
         if (w[j] > 0.0f) {
             lastp = e;
-            if (cand == INT_MAX && base + (pre + sacc[j]) > uR)
+            const float cur = base + (pre + sacc[j]);
+            if (cand == INT_MAX && cur > uR) {
                 cand = e;
+                const float prev = base + (pre + (j > 0 ? sacc[j - 1] : 0.0f));
+                gap = fminf(uR - prev, cur - uR);
+            }
         }
     }
+    const int mine = cand;
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) {
         cand = min(cand, __shfl_xor_sync(0xffffffffu, cand, o));
         lastp = max(lastp, __shfl_xor_sync(0xffffffffu, lastp, o));
+    }
+    if (cand != INT_MAX) {
+        const unsigned owner = __ballot_sync(0xffffffffu, mine == cand);
+        gap = __shfl_sync(0xffffffffu, gap, __ffs(owner) - 1);
+        const float guard = (mode == DRAW_RESIDUAL) ? P.guard_abs : P.guard_rel * R;
+        near = !(gap >= guard);
+        gap_u = gap / R;
     }
     return (cand != INT_MAX) ? cand : lastp;
 }
@@ -2584,12 +2618,40 @@ __device__ void warp_row_chunks(const Params &P, const JobRec &J, int mode, floa
     __syncwarp();
 }
 
+// The exact-draw record of a listed sequence (resolve.cuh).
+template <int DT, bool FILT>
+__device__ __forceinline__ RJob make_rjob(const Params &P, const JobRec &Jr, int b)
+{
+    RJob J;
+    J.t_arr = P.target;
+    J.d_arr = P.draft;
+    J.t_row = Jr.t_row;
+    J.d_row = Jr.d_row;
+    J.mode = (Jr.mode == DRAW_RESIDUAL) ? RJ_RESIDUAL : RJ_TARGET;
+    J.mt = Jr.mt;
+    J.md = Jr.md;
+    J.rzt = Jr.rzt;
+    J.rzd = Jr.rzd;
+    exp_coef(__ldg(P.temperature + b), J.ch, J.cl);
+    J.u = Jr.u;
+    J.filt = (FILT && Jr.filt) ? 1 : 0;
+    J.kt = Jr.kt;
+    J.it = Jr.it;
+    J.kd = Jr.kd;
+    J.id = Jr.id;
+    J.j = Jr.j;
+    return J;
+}
+
+
+
 template <int DT, bool FILT>
 __global__ void __launch_bounds__(SCAN_WARPS * 32) final_kernel(const Params P)
 {
     __shared__ float btot[SCAN_WARPS][MAXBLK];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int b = blockIdx.x * SCAN_WARPS + warp;
+    allow_next_kernel();     // the exact-draw kernel may launch; it waits for this grid
     wait_previous_kernel();  // chunk totals come from the draw kernel
     if (b >= P.B)
         return;
@@ -2600,17 +2662,34 @@ __global__ void __launch_bounds__(SCAN_WARPS * 32) final_kernel(const Params P)
     const int nblk = P.DS * UD;
     float *ch = P.chunks + (size_t)b * P.chunk_stride;
     int tok;
+    bool near;
+    float gap_u;  // the fp32 distance of u to the chosen cell's nearer edge (trace only)
     if (J.mode == DRAW_TARGET && !(FILT && J.filt))
         tok = records_draw<DT>(P.rec + (size_t)b * P.NCH, P.NCH, J.mt, J.c, J.u, P.target,
-                               (size_t)J.t_row, P.V, lane);
+                               (size_t)J.t_row, P.V, lane, P.guard_rel, near, &gap_u);
     else
-        tok = locate<DT, FILT>(P, J, J.mode, ch, btot[warp], nblk, lane);
+        tok = locate<DT, FILT>(P, J, J.mode, ch, btot[warp], nblk, lane, near, gap_u);
     if (tok < 0 && J.mode == DRAW_RESIDUAL) {
         // the residual vanished by rounding alone: draw from p_j instead
         warp_row_chunks<DT, FILT>(P, J, DRAW_TARGET, ch, nblk, lane);
-        tok = locate<DT, FILT>(P, J, DRAW_TARGET, ch, btot[warp], nblk, lane);
+        tok = locate<DT, FILT>(P, J, DRAW_TARGET, ch, btot[warp], nblk, lane, near, gap_u);
+        near = true;
     }
     const bool err = tok < 0;
+    if (!err && near && lane == 0) {
+        // list the sequence for the exact draw, which rewrites out_tokens[b][j]
+        const unsigned int f = atomicAdd(&P.hdr->n_flag, 1u);
+        P.rlist[f] = b;
+        P.rjob[f] = make_rjob<DT, FILT>(P, J, b);
+        P.rdone[f] = 0u;
+        P.rkcnt[f] = 0u;
+    }
+    if (P.out_draw && lane == 0) {
+        P.out_draw[(size_t)b * 4 + 0] = tok;
+        P.out_draw[(size_t)b * 4 + 1] = (!err && near) ? 1 : 0;
+        P.out_draw[(size_t)b * 4 + 2] = tok;
+        P.out_draw[(size_t)b * 4 + 3] = __float_as_int(gap_u);
+    }
     for (int i = lane; i <= k; i += 32) {
         int o = -1;
         if (!err)
@@ -2619,6 +2698,65 @@ __global__ void __launch_bounds__(SCAN_WARPS * 32) final_kernel(const Params P)
     }
     if (lane == 0)
         P.out_num_accepted[b] = err ? -1 : J.j;
+}
+
+// ------------------------------------------------------------ exact draws
+//
+// The sequences final_kernel listed (their fp32 draw landed within the guard
+// of a cell edge) are drawn again exactly (resolve.cuh).  Work items are
+// (listed sequence, chunk of 2048 elements), dealt round robin over a
+// persistent grid; the CTA that finishes a sequence's last chunk (a ticket
+// counter, no waiting) forms the draw and rewrites out_tokens[b][j].
+
+template <int DT, bool FILT>
+__global__ void __launch_bounds__(RTH, 3) resolve_kernel(const Params P)
+{
+    __shared__ RSmem S;
+    const int tid = threadIdx.x;
+    load_exp2_table(S.tab);
+    wait_previous_kernel();  // the list comes from the final kernel
+    const unsigned int nf = *reinterpret_cast<volatile unsigned int *>(&P.hdr->n_flag);
+    const long long NC = P.RNC;
+    const long long items = (long long)nf * NC;
+    // items are handed out by a counter (the first gridDim.x implicitly), so a
+    // CTA busy finishing a sequence does not hold up the items behind it
+    long long it = blockIdx.x;
+    __syncthreads();
+    while (it < items) {
+        const int f = (int)(it / NC);
+        const int q = (int)(it - (long long)f * NC);
+        if (tid == 0)
+            S.next = (long long)gridDim.x + (long long)atomicAdd(&P.hdr->next_resolve, 1u);
+        if (tid < (int)(sizeof(RJob) / 16))
+            reinterpret_cast<uint4 *>(&S.job)[tid] =
+                __ldcg(reinterpret_cast<const uint4 *>(P.rjob + f) + tid);
+        __syncthreads();
+        const long long nx = S.next;  // read here: thread 0 rewrites it next iteration
+        const RJob &J = S.job;
+        RzRec *recs = P.rrec + (size_t)f * NC;
+        resolve_chunk<DT>(J, q, P.V, recs + q, P.rkink + (size_t)f * RKCAP, P.rkcnt + f, S);
+        if (tid == 0) {
+            __threadfence();
+            const unsigned int t = atomicAdd(P.rdone + f, 1u);
+            S.last = (t == (unsigned int)NC - 1u) ? 1 : 0;
+        }
+        __syncthreads();
+        if (S.last) {
+            __threadfence();
+            const unsigned int kc = *reinterpret_cast<volatile unsigned int *>(P.rkcnt + f);
+            const int tok =
+                resolve_finish<DT>(J, P.V, recs, P.rkink + (size_t)f * RKCAP, kc, S, P.hdr);
+            if (tid == 0) {
+                const int b = __ldcg(P.rlist + f);
+                if (tok >= 0)
+                    P.out_tokens[(size_t)b * (P.k + 1) + J.j] = tok;
+                if (P.out_draw)
+                    P.out_draw[(size_t)b * 4 + 2] = tok;
+            }
+        }
+        __syncthreads();
+        it = nx;
+    }
 }
 
 // ------------------------------------------------------------------ host side
@@ -2646,13 +2784,15 @@ bool sizes_ok(int32_t B, int32_t k, int32_t V, int32_t dtype)
 int tile_elems(int32_t dtype) { return TILE_BYTES / (dtype == SPEC_F32 ? 4 : 2); }
 
 struct WsLayout {
-    size_t partials, jobs, chunks, rec, filt, total;
-    size_t NS, NSS, DS, chunk_stride, NCH;
+    size_t partials, jobs, chunks, rec, filt, rlist, rjob, rdone, rkcnt, rkink, rrec, total;
+    size_t NS, NSS, DS, chunk_stride, NCH, RNC;
 };
 
 // header | one 16-byte partial per super-tile [B][2k+1][NSS] | draw jobs [B] |
 // inverse-CDF chunk totals [B][chunk_stride] | bonus-row chunk records [B][NCH]
-// | top-k / top-p records [B][2k+1] (filtered calls)
+// | top-k / top-p records [B][2k+1] (filtered calls) | exact-draw list [B],
+// their records [B], tickets [B], undecided counts [B], groups of undecided
+// elements [B][RKCAP], chunk records [B][RNC]
 WsLayout ws_layout(int32_t B, int32_t k, int32_t V, int32_t dtype)
 {
     WsLayout w;
@@ -2668,7 +2808,14 @@ WsLayout ws_layout(int32_t B, int32_t k, int32_t V, int32_t dtype)
     w.chunk_stride = align_up(w.DS * UD * NCW, 32);  // floats, 128-byte rows
     w.rec = align_up(w.chunks + (size_t)B * w.chunk_stride * 4, 256);
     w.filt = align_up(w.rec + (size_t)B * w.NCH * sizeof(float2), 256);
-    w.total = w.filt + (size_t)B * (2 * (size_t)k + 1) * sizeof(FiltRec);
+    w.RNC = ((size_t)V + RCH - 1) / RCH;
+    w.rlist = align_up(w.filt + (size_t)B * (2 * (size_t)k + 1) * sizeof(FiltRec), 256);
+    w.rjob = align_up(w.rlist + (size_t)B * 4, 256);
+    w.rdone = align_up(w.rjob + (size_t)B * sizeof(RJob), 256);
+    w.rkcnt = align_up(w.rdone + (size_t)B * 4, 256);
+    w.rkink = align_up(w.rkcnt + (size_t)B * 4, 256);
+    w.rrec = align_up(w.rkink + (size_t)B * RKCAP * sizeof(RkRec), 256);
+    w.total = w.rrec + (size_t)B * w.RNC * sizeof(RzRec);
     return w;
 }
 
@@ -2677,11 +2824,11 @@ size_t ws_bytes(int32_t B, int32_t k, int32_t V, int32_t dtype)
     return ws_layout(B, k, V, dtype).total;
 }
 
-// `events` (nullable): cudaEvent_t recorded after each kernel (four, or five
-// with the filter kernel of a filtered call).
+// `events` (nullable): cudaEvent_t recorded after each kernel (five, or six
+// with the filter kernels of a filtered call).
 template <int DT, bool FILT>
-int launch_all(const Params &P, unsigned int grid1, unsigned int gridf, cudaStream_t st,
-               void *const *events)
+int launch_all(const Params &P, unsigned int grid1, unsigned int gridf, unsigned int gridr,
+               cudaStream_t st, void *const *events)
 {
     // filtered calls record one more event, after the filter kernel
     auto mark = [&](int i) {
@@ -2730,6 +2877,9 @@ int launch_all(const Params &P, unsigned int grid1, unsigned int gridf, cudaStre
     if (dependent(final_kernel<DT, FILT>, gs, SCAN_WARPS * 32) != cudaSuccess)
         return SPEC_ECUDA;
     mark(3);
+    if (dependent(resolve_kernel<DT, FILT>, gridr, RTH) != cudaSuccess)
+        return SPEC_ECUDA;
+    mark(4);
     if (cudaPeekAtLastError() != cudaSuccess) {
         (void)cudaGetLastError();
         return SPEC_ECUDA;
@@ -2737,11 +2887,21 @@ int launch_all(const Params &P, unsigned int grid1, unsigned int gridf, cudaStre
     return SPEC_OK;
 }
 
+// Guards of the fp32 draw, below which a draw is redone exactly.  The fp32
+// running sums carry errors below 8e-7 of R (ex2.approx, the fp32 exponent,
+// the fp32 masses and sums; measured against the fp64 oracle over ~6000
+// draws of the synthetic workloads): residual weights are probabilities
+// (R <= 1), so their guard is absolute; target-row weights are relative to
+// their total R.
+constexpr float GUARD_ABS = 2e-6f;
+constexpr float GUARD_REL = 2e-6f;
+
 int launch(const void *target, const void *draft, const int32_t *tokens, const float *ua,
            const float *ur, const float *temp, int32_t *out_tokens, int32_t *out_n,
            float *out_probs, int32_t B, int32_t k, int32_t V, int32_t dtype, void *ws,
            size_t ws_size, void *stream, void *const *events = nullptr, bool filtered = false,
-           const int32_t *top_k = nullptr, const float *top_p = nullptr)
+           const int32_t *top_k = nullptr, const float *top_p = nullptr,
+           int32_t *out_draw = nullptr, bool resolve_all = false)
 {
     if (!sizes_ok(B, k, V, dtype))
         return SPEC_EINVAL;
@@ -2827,6 +2987,16 @@ int launch(const void *target, const void *draft, const int32_t *tokens, const f
     P.top_k = top_k;
     P.top_p = top_p;
     P.filt = reinterpret_cast<FiltRec *>(w + lay.filt);
+    P.rlist = reinterpret_cast<int *>(w + lay.rlist);
+    P.rjob = reinterpret_cast<RJob *>(w + lay.rjob);
+    P.rdone = reinterpret_cast<unsigned int *>(w + lay.rdone);
+    P.rkcnt = reinterpret_cast<unsigned int *>(w + lay.rkcnt);
+    P.rkink = reinterpret_cast<RkRec *>(w + lay.rkink);
+    P.rrec = reinterpret_cast<RzRec *>(w + lay.rrec);
+    P.RNC = (int)lay.RNC;
+    P.guard_abs = resolve_all ? INFINITY : GUARD_ABS;
+    P.guard_rel = resolve_all ? INFINITY : GUARD_REL;
+    P.out_draw = out_draw;
     P.NCH = (int)lay.NCH;
     P.B = B;
     P.k = k;
@@ -2841,12 +3011,15 @@ int launch(const void *target, const void *draft, const int32_t *tokens, const f
     P.target_bytes = (unsigned long long)B * (k + 1) * (unsigned long long)V * es;
     P.draft_bytes = (unsigned long long)B * k * (unsigned long long)V * es;
 
+    // the exact draws: two CTAs per SM, at most one work item each to begin with
+    const size_t ritems = (size_t)B * lay.RNC;
+    const unsigned int gridr = (unsigned int)(ritems < 3 * n_sms ? ritems : 3 * n_sms);
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
     if (filtered)
-        return (dtype == SPEC_F32) ? launch_all<SPEC_F32, true>(P, grid1, gridf, st, events)
-                                   : launch_all<SPEC_BF16, true>(P, grid1, gridf, st, events);
-    return (dtype == SPEC_F32) ? launch_all<SPEC_F32, false>(P, grid1, 0, st, events)
-                               : launch_all<SPEC_BF16, false>(P, grid1, 0, st, events);
+        return (dtype == SPEC_F32) ? launch_all<SPEC_F32, true>(P, grid1, gridf, gridr, st, events)
+                                   : launch_all<SPEC_BF16, true>(P, grid1, gridf, gridr, st, events);
+    return (dtype == SPEC_F32) ? launch_all<SPEC_F32, false>(P, grid1, 0, gridr, st, events)
+                               : launch_all<SPEC_BF16, false>(P, grid1, 0, gridr, st, events);
 }
 
 }  // namespace
@@ -2949,6 +3122,24 @@ int32_t spec_verify_probs(const void *target_logits, const void *draft_logits,
     return launch(target_logits, draft_logits, draft_tokens, u_accept, u_resample, temperature,
                   out_tokens, out_num_accepted, out_probs, B, k, V, dtype, workspace,
                   workspace_bytes, stream);
+}
+
+int32_t spec_verify_trace(const void *target_logits, const void *draft_logits,
+                          const int32_t *draft_tokens, const float *u_accept,
+                          const float *u_resample, const float *temperature,
+                          int32_t *out_tokens, int32_t *out_num_accepted, float *out_probs,
+                          int32_t *out_draw, int32_t resolve_all,
+                          int32_t B, int32_t k, int32_t V, int32_t dtype,
+                          void *workspace, size_t workspace_bytes, void *stream)
+{
+    if (!out_draw && B > 0)
+        return SPEC_EINVAL;
+    if (reinterpret_cast<uintptr_t>(out_draw) & 3)
+        return SPEC_EINVAL;
+    return launch(target_logits, draft_logits, draft_tokens, u_accept, u_resample, temperature,
+                  out_tokens, out_num_accepted, out_probs, B, k, V, dtype, workspace,
+                  workspace_bytes, stream, nullptr, false, nullptr, nullptr, out_draw,
+                  resolve_all != 0);
 }
 
 int32_t spec_verify_timed(const void *target_logits, const void *draft_logits,

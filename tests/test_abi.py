@@ -43,7 +43,7 @@ def test_every_declared_symbol_is_exported(lib):
 
 
 def test_abi_version_and_strerror(lib):
-    assert sv.spec_verify_abi_version() == 1
+    assert sv.spec_verify_abi_version() == 2
     for code in (0, 1, 2, 3):
         assert lib.spec_verify_strerror(code)
     assert b"unknown" in lib.spec_verify_strerror(99)
@@ -69,7 +69,17 @@ def test_workspace_size(lib, B, k, V, dt, ok):
     chunks = up(jobs + 80 * B, 256)
     rec = up(chunks + B * up(ds * 4 * 8, 32) * 4, 256)
     filt = up(rec + B * nch * 8, 256)
-    assert n == filt + B * (2 * k + 1) * 16
+    # the exact draw: per sequence a list entry, a 96-byte draw record, a
+    # ticket, a group count, 64 groups of 32 bytes, and a 32-byte record per
+    # 2048 elements
+    rnc = -(-V // 2048)
+    rlist = up(filt + B * (2 * k + 1) * 16, 256)
+    rjob = up(rlist + 4 * B, 256)
+    rdone = up(rjob + 96 * B, 256)
+    rkcnt = up(rdone + 4 * B, 256)
+    rkink = up(rkcnt + 4 * B, 256)
+    rrec = up(rkink + 32 * 64 * B, 256)
+    assert n == rrec + B * rnc * 32
 
 
 def _call(lib, ptrs, B=1, k=1, V=8, dt=0, wsb=1 << 20):
