@@ -44,8 +44,7 @@ constexpr int FIXB = 51;             // fixed-point weights in units of 2^-51
 constexpr int RSHIFT = 40;           // residual products are kept in units of 2^40
 constexpr int RMAXC = SPEC_MAX_V / RCH;
 static_assert(RPT == 8, "a chunk gives each thread 8 elements");
-static_assert(2 * RTH >= RMAXC, "the finishing CTA holds two chunk records per thread");
-static_assert(RKCAP <= RTH && RKG <= RTH, "one thread per listed group");
+static_assert(RKG <= RTH, "one thread per group of a chunk");
 static_assert((long long)RCH << FIXB <= (1ll << 62), "chunk sums fit a signed 64-bit integer");
 
 constexpr float LN2_HI = 0x1.62e430p-1f;     // ln 2 = LN2_HI + LN2_LO to ~2^-54
@@ -98,19 +97,10 @@ struct RSmem {
     RJob job;  // the current work item's draw
     float2 tab[256];
     long long red[RTH / 32][4];
-    unsigned long long wsum[RTH / 32][2];
-    unsigned long long W[RMAXC][2];   // chunk masses (i128 as lo, hi)
     unsigned int gkey[RKG][2];        // undecided groups of the current chunk: t - d as a float pair
     unsigned long long gsum[RKG][2];
-    unsigned long long kw[RKCAP][2];  // weights of the listed groups (finishing step)
-    int kc[RKCAP];
     int gcnt;
     long long next;
-    int last;
-    int tok;
-    int cstar;
-    int lastp;
-    unsigned long long before[2];
 };
 
 __device__ __forceinline__ i128 mk128(unsigned long long lo, unsigned long long hi)
@@ -149,59 +139,8 @@ __device__ __forceinline__ long long fix_of(float rh, float rl, int n)
     return (long long)hi + (long long)lo;
 }
 
-// e = 2^((x - m) * c) as an integer in units of 2^-51 (x <= m, so e <= 1),
-// rounded to nearest; 0 when the exponent is below -60 (e < 2^-60, under
-// 2^-9 of a unit) or x is -inf.  `approx` receives e as a float (without the
-// 2^51 scale) for sign decisions.  Every operation an exact split relies on
-// is an explicitly rounded intrinsic, which the compiler does not fuse.
-__device__ __forceinline__ long long efix(float x, float m, float ch, float cl, const float2 *tab,
-                                          float &approx)
-{
-    // d = x - m exactly as dh + dl
-    const float dh = __fsub_rn(x, m);
-    const float sh = __fmul_rn(dh, ch);
-    if (!(sh >= -60.0f)) {  // also -inf and NaN
-        approx = 0.0f;
-        return 0;
-    }
-    const float bb = __fsub_rn(dh, x);
-    const float dl = __fadd_rn(__fsub_rn(x, __fsub_rn(dh, bb)), __fsub_rn(-m, bb));
-    // s = d * c = sh + sl
-    const float sl = __fadd_rn(__fmaf_rn(dh, ch, -sh), __fmaf_rn(dh, cl, __fmul_rn(dl, ch)));
-    // s = j/256 + f + sl with j an integer, |f| <= 1/512 (exact): adding
-    // 1.5 * 2^23 rounds t (|t| <= 15360) to an integer in the low mantissa bits
-    const float t = __fmul_rn(sh, 256.0f);
-    const float tm = __fadd_rn(t, 0x1.8p23f);
-    const int j = __float_as_int(tm) - 0x4b400000;
-    const float jf = __fsub_rn(tm, 0x1.8p23f);
-    const float f = __fmul_rn(__fsub_rn(t, jf), 0x1p-8f);
-    // g = f + sl exactly as gh + gl
-    const float gh = __fadd_rn(f, sl);
-    const float gb = __fsub_rn(gh, f);
-    const float gl = __fadd_rn(__fsub_rn(f, __fsub_rn(gh, gb)), __fsub_rn(sl, gb));
-    // a = g * ln2 as ah + al
-    const float ah = __fmul_rn(gh, LN2_HI);
-    const float al = __fadd_rn(__fmaf_rn(gh, LN2_HI, -ah),
-                               __fmaf_rn(gh, LN2_LO, __fmul_rn(gl, LN2_HI)));
-    // e^a - 1 = ah + ml, ml = al + ah*al + ah^2 (1/2 + ah/6 + ah^2/24)
-    float p = __fmaf_rn(ah, 1.0f / 24.0f, 1.0f / 6.0f);
-    p = __fmaf_rn(ah, p, 0.5f);
-    p = __fmul_rn(__fmul_rn(ah, ah), p);
-    const float ml = __fadd_rn(al, __fmaf_rn(ah, al, p));
-    // 2^((j mod 256) / 256) * (1 + ah + ml) as rh + rl, rh in [1, 2.0003)
-    const float2 T = tab[j & 255];
-    const float ph = __fmul_rn(T.x, ah);
-    const float pl = __fmaf_rn(T.x, ah, -ph);
-    const float rest = __fadd_rn(pl, __fmaf_rn(T.x, ml, __fmaf_rn(T.y, ah, T.y)));
-    const float rh = __fadd_rn(T.x, ph);
-    const float rl = __fadd_rn(__fsub_rn(ph, __fsub_rn(rh, T.x)), rest);
-    const int n = j >> 8;  // floor(j / 256), in [-60, 0]
-    approx = __fmul_rn(rh, __int_as_float((n + 127) << 23));
-    return fix_of(rh, rl, n);
-}
-
-// ---- two weights at once, in packed f32x2 arithmetic (each half rounds
-// exactly like the scalar instruction, so the results equal efix's)
+// ---- weights two at a time, in packed f32x2 arithmetic (each half rounds
+// exactly like the scalar instruction)
 
 __device__ __forceinline__ unsigned long long fx2(float lo, float hi)
 {
@@ -239,8 +178,13 @@ __device__ __forceinline__ unsigned long long fmax2(unsigned long long a, unsign
     return r;
 }
 
-// efix for two elements at once: x0 against maximum m0 and x1 against m1,
-// the same coefficient.  ok0 / ok1 false give 0 (masked or absent elements).
+// e = 2^((x - m) * c) as an integer in units of 2^-51 (x <= m, so e <= 1),
+// rounded to nearest, for two elements at once: x0 against maximum m0 and x1
+// against m1, the same coefficient c = ch + cl.  0 when the exponent is below
+// -60 (e < 2^-60, under 2^-9 of a unit), x is -inf, or ok0 / ok1 is false
+// (masked or absent elements).  a0 / a1 receive e as floats (without the
+// 2^51 scale) for sign decisions.  Every operation an exact split relies on
+// is an explicitly rounded instruction, which the compiler does not fuse.
 __device__ __forceinline__ void efix2(float x0, float x1, float m0, float m1, bool ok0, bool ok1,
                                       float ch, float cl, const float2 *tab, long long &E0,
                                       long long &E1, float &a0, float &a1)
@@ -309,61 +253,12 @@ __device__ __forceinline__ bool rj_kept(const RJob &J, float v, int x, bool draf
     return key > kap || (key == kap && x <= iota);
 }
 
-// Logits e0 .. e0+7 of a row (e0 a multiple of 8; -inf past V).
-template <int DT>
-__device__ __forceinline__ void rj_load8(const void *arr, long long row, int e0, int V,
-                                         float (&x)[RPT])
-{
-    using L = Lg<DT>;
-#pragma unroll
-    for (int h = 0; h < RPT / L::VEC; ++h) {
-        const uint4 r = row_vec<DT>(arr, (size_t)row, e0 / L::VEC + h, V);
-        float y[L::VEC];
-        L::unpack(r, y);
-#pragma unroll
-        for (int i = 0; i < L::VEC; ++i)
-            x[h * L::VEC + i] = y[i];
-    }
-}
-
 __device__ __forceinline__ long long warp_sum_ll(long long v)
 {
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1)
         v += __shfl_xor_sync(0xffffffffu, v, o);
     return v;
-}
-
-// Fixed-point weights of elements e0 .. e0+7 of both rows (the draft's are 0
-// unless `residual`), with their float approximations.
-template <int DT>
-__device__ __forceinline__ void rj_fix8(const RJob &J, bool residual, int e0, int V,
-                                        const float2 *tab, long long (&Et)[RPT],
-                                        long long (&Ed)[RPT], float (&ft)[RPT], float (&fd)[RPT],
-                                        float (&xt)[RPT], float (&xd)[RPT])
-{
-    rj_load8<DT>(J.t_arr, J.t_row, e0, V, xt);
-    if (residual)
-        rj_load8<DT>(J.d_arr, J.d_row, e0, V, xd);
-    if (residual) {
-#pragma unroll
-        for (int i = 0; i < RPT; ++i) {
-            const int x = e0 + i;
-            efix2(xt[i], xd[i], J.mt, J.md, x < V && rj_kept<DT>(J, xt[i], x, false),
-                  x < V && rj_kept<DT>(J, xd[i], x, true), J.ch, J.cl, tab, Et[i], Ed[i], ft[i],
-                  fd[i]);
-        }
-    } else {
-#pragma unroll
-        for (int i = 0; i < RPT; i += 2) {
-            const int x = e0 + i;
-            efix2(xt[i], xt[i + 1], J.mt, J.mt, x < V && rj_kept<DT>(J, xt[i], x, false),
-                  x + 1 < V && rj_kept<DT>(J, xt[i + 1], x + 1, false), J.ch, J.cl, tab, Et[i],
-                  Et[i + 1], ft[i], ft[i + 1]);
-            Ed[i] = Ed[i + 1] = 0;
-            fd[i] = fd[i + 1] = 0.0f;
-        }
-    }
 }
 
 // One chunk (elements q*RCH .. q*RCH + RCH - 1) of a job: the CTA writes the
@@ -498,11 +393,36 @@ __device__ void resolve_chunk(const RJob &J, int q, int V, RzRec *rec, RkRec *ki
     }
 }
 
+// ------------------------------------------------------------ finishing
+//
+// One CTA of RFTH threads per listed row, after every chunk is done: the
+// row's masses, the chunk masses, their prefix, the crossing chunk, and in
+// it the crossing element.  Thread t holds chunk record t, and RFPT
+// consecutive elements of the crossing chunk.
+
+constexpr int RFTH = 512;
+constexpr int RFPT = RCH / RFTH;
+static_assert(RFTH >= RMAXC, "the finishing CTA holds one chunk record per thread");
+static_assert(RFPT == 4, "the crossing chunk gives each finishing thread 4 elements");
+static_assert(RKCAP <= RFTH, "one finishing thread per listed group");
+
+struct RFSmem {
+    float2 tab[256];
+    unsigned long long zsum[RFTH / 32][4];
+    unsigned long long wsum[RFTH / 32][2];
+    unsigned long long W[RMAXC][2];   // chunk masses (i128 as lo, hi)
+    int tok;
+    int cstar;
+    int lastp;
+    int pad;
+    unsigned long long before[2];
+};
+
 // Exclusive prefix of one i128 per thread in thread order; `total` gets the
 // CTA's sum.  Called by every thread.
-__device__ __forceinline__ i128 cta_excl_scan(i128 v, i128 &total, RSmem &S)
+__device__ __forceinline__ i128 cta_excl_scan(i128 v, i128 &total, RFSmem &S)
 {
-    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     i128 x = v;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
@@ -517,7 +437,8 @@ __device__ __forceinline__ i128 cta_excl_scan(i128 v, i128 &total, RSmem &S)
     }
     __syncthreads();
     i128 before = 0, tot = 0;
-    for (int w = 0; w < RTH / 32; ++w) {
+#pragma unroll 4
+    for (int w = 0; w < RFTH / 32; ++w) {
         const i128 sw = mk128(S.wsum[w][0], S.wsum[w][1]);
         if (w < warp)
             before += sw;
@@ -525,7 +446,6 @@ __device__ __forceinline__ i128 cta_excl_scan(i128 v, i128 &total, RSmem &S)
     }
     total = tot;
     __syncthreads();
-    (void)tid;
     return before + (x - v);
 }
 
@@ -538,18 +458,56 @@ __device__ __forceinline__ i128 res_weight(long long Et, long long Ed, unsigned 
     return d > 0 ? (d >> RSHIFT) : (i128)0;
 }
 
-// Weights of elements e0 .. e0+7 in the exact draw: residual or E_t.
+// Logits e0 .. e0+3 of a row (e0 a multiple of 4; -inf past V).
 template <int DT>
-__device__ __forceinline__ void rj_weights8(const RJob &J, int e0, int V, bool residual,
-                                            unsigned long long Zt, unsigned long long Zd,
-                                            i128 (&w)[RPT], const float2 *tab)
+__device__ __forceinline__ void rj_load4(const void *arr, long long row, int e0, int V,
+                                         float (&x)[RFPT])
 {
-    long long Et[RPT], Ed[RPT];
-    float ft[RPT], fd[RPT], xt[RPT], xd[RPT];
-    rj_fix8<DT>(J, residual, e0, V, tab, Et, Ed, ft, fd, xt, xd);
+    using L = Lg<DT>;
+    const uint4 r = row_vec<DT>(arr, (size_t)row, e0 / L::VEC, V);
+    float y[L::VEC];
+    L::unpack(r, y);
+    const int o = e0 % L::VEC;
 #pragma unroll
-    for (int i = 0; i < RPT; ++i)
-        w[i] = residual ? res_weight(Et[i], Ed[i], Zt, Zd) : (i128)Et[i];
+    for (int i = 0; i < RFPT; ++i)
+        x[i] = y[(L::VEC == RFPT) ? i : (o + i) % L::VEC];
+}
+
+// Weights of elements e0 .. e0+3 in the exact draw: residual or E_t.
+template <int DT>
+__device__ __forceinline__ void rj_weights4(const RJob &J, int e0, int V, bool residual,
+                                            unsigned long long Zt, unsigned long long Zd,
+                                            i128 (&w)[RFPT], const float2 *tab)
+{
+    float xt[RFPT], xd[RFPT];
+    rj_load4<DT>(J.t_arr, J.t_row, e0, V, xt);
+    if (residual)
+        rj_load4<DT>(J.d_arr, J.d_row, e0, V, xd);
+    const bool filt = J.filt != 0;
+    if (residual) {
+#pragma unroll
+        for (int i = 0; i < RFPT; ++i) {
+            const int x = e0 + i;
+            long long Et, Ed;
+            float a0, a1;
+            efix2(xt[i], xd[i], J.mt, J.md, x < V && (!filt || rj_kept<DT>(J, xt[i], x, false)),
+                  x < V && (!filt || rj_kept<DT>(J, xd[i], x, true)), J.ch, J.cl, tab, Et, Ed, a0,
+                  a1);
+            w[i] = res_weight(Et, Ed, Zt, Zd);
+        }
+    } else {
+#pragma unroll
+        for (int i = 0; i < RFPT; i += 2) {
+            const int x = e0 + i;
+            long long E0, E1;
+            float a0, a1;
+            efix2(xt[i], xt[i + 1], J.mt, J.mt, x < V && (!filt || rj_kept<DT>(J, xt[i], x, false)),
+                  x + 1 < V && (!filt || rj_kept<DT>(J, xt[i + 1], x + 1, false)), J.ch, J.cl, tab,
+                  E0, E1, a0, a1);
+            w[i] = (i128)E0;
+            w[i + 1] = (i128)E1;
+        }
+    }
 }
 
 // floor(u * R) for u in [0, 1) (a float) and 0 <= R < 2^100.
@@ -570,30 +528,36 @@ __device__ __forceinline__ i128 floor_uR(float u, i128 R)
 // it; every thread returns the token).  Returns -1 if no weight is positive.
 template <int DT>
 __device__ int resolve_finish(const RJob &J, int V, const RzRec *recs, const RkRec *kinks,
-                              unsigned int kcnt, RSmem &S, WsHeader *hdr)
+                              unsigned int kcnt, RFSmem &S, WsHeader *hdr)
 {
     const int tid = threadIdx.x;
     const int NC = (V + RCH - 1) / RCH;
-    long long at[2] = {0, 0}, ad[2] = {0, 0}, zt[2] = {0, 0}, zd[2] = {0, 0};
-#pragma unroll
-    for (int h = 0; h < 2; ++h) {
-        const int c = 2 * tid + h;  // a thread's chunks are adjacent (for the prefix)
-        if (c < NC) {
-            const longlong2 r0 = __ldcg(reinterpret_cast<const longlong2 *>(recs + c));
-            const longlong2 r1 = __ldcg(reinterpret_cast<const longlong2 *>(recs + c) + 1);
-            at[h] = r0.x;
-            ad[h] = r0.y;
-            zt[h] = r1.x;
-            zd[h] = r1.y;
-        }
+    long long at = 0, ad = 0, zt = 0, zd = 0;
+    if (tid < NC) {
+        const longlong2 r0 = __ldcg(reinterpret_cast<const longlong2 *>(recs + tid));
+        const longlong2 r1 = __ldcg(reinterpret_cast<const longlong2 *>(recs + tid) + 1);
+        at = r0.x;
+        ad = r0.y;
+        zt = r1.x;
+        zd = r1.y;
+    }
+    // the listed groups, one per thread, fetched early
+    long long get = 0, ged = 0;
+    int gc = 0;
+    const bool has_group = tid < (int)min(kcnt, (unsigned int)RKCAP);
+    if (has_group) {
+        const longlong2 e = __ldcg(reinterpret_cast<const longlong2 *>(kinks + tid));
+        get = e.x;
+        ged = e.y;
+        gc = __ldcg(&kinks[tid].chunk);
     }
     bool residual = J.mode == RJ_RESIDUAL;
     unsigned long long Zt = 0, Zd = 0;  // the masses, scaled below 2^62
     if (residual) {
         // exact masses (128-bit), then one common scale
         i128 ta, tb;
-        (void)cta_excl_scan((i128)zt[0] + zt[1], ta, S);
-        (void)cta_excl_scan((i128)zd[0] + zd[1], tb, S);
+        (void)cta_excl_scan((i128)zt, ta, S);
+        (void)cta_excl_scan((i128)zd, tb, S);
         const u128 mx = (u128)(ta > tb ? ta : tb);
         const unsigned long long mh = (unsigned long long)(mx >> 64), ml = (unsigned long long)mx;
         const int bits = mh ? 128 - __clzll((long long)mh) : 64 - __clzll((long long)ml);
@@ -609,48 +573,37 @@ __device__ int resolve_finish(const RJob &J, int V, const RzRec *recs, const RkR
         if (tid == 0 && kcnt > (unsigned int)RKCAP)
             atomicAdd(&hdr->n_slow_kinks, 1u);
         if (sorted_ok) {
-#pragma unroll
-            for (int h = 0; h < 2; ++h) {
-                const int c = 2 * tid + h;
-                if (c < NC) {
-                    const i128 d = (i128)((u128)(unsigned long long)at[h] * Zd) -
-                                   (i128)((u128)(unsigned long long)ad[h] * Zt);
-                    const i128 wc = d >> RSHIFT;
-                    S.W[c][0] = lo64(wc);
-                    S.W[c][1] = hi64(wc);
-                }
-            }
-            // groups of undecided elements, weighed with the exact masses
-            // (one thread each) and added to their chunks by one thread
-            // (integer sums: any order gives the same result)
-            if (tid < (int)kcnt) {
-                const longlong2 e = __ldcg(reinterpret_cast<const longlong2 *>(kinks + tid));
-                const int c = __ldcg(&kinks[tid].chunk);
-                const i128 d = (i128)((u128)(unsigned long long)e.x * Zd) -
-                               (i128)((u128)(unsigned long long)e.y * Zt);
-                const i128 wg = d > 0 ? (d >> RSHIFT) : (i128)0;
-                S.kw[tid][0] = lo64(wg);
-                S.kw[tid][1] = hi64(wg);
-                S.kc[tid] = c;
+            if (tid < NC) {
+                const i128 d = (i128)((u128)(unsigned long long)at * Zd) -
+                               (i128)((u128)(unsigned long long)ad * Zt);
+                const i128 wc = d >> RSHIFT;
+                S.W[tid][0] = lo64(wc);
+                S.W[tid][1] = hi64(wc);
             }
             __syncthreads();
-            if (tid == 0) {
-                for (int g = 0; g < (int)kcnt; ++g) {
-                    const int c = S.kc[g];
-                    const i128 nv = mk128(S.W[c][0], S.W[c][1]) + mk128(S.kw[g][0], S.kw[g][1]);
-                    S.W[c][0] = lo64(nv);
-                    S.W[c][1] = hi64(nv);
+            // the groups of undecided elements, weighed with the exact masses
+            // and added to their chunks (integer sums: any order gives the
+            // same result; 64-bit atomics with the carry done by hand)
+            if (has_group) {
+                const i128 d = (i128)((u128)(unsigned long long)get * Zd) -
+                               (i128)((u128)(unsigned long long)ged * Zt);
+                if (d > 0) {
+                    const i128 wg = d >> RSHIFT;
+                    const unsigned long long lo = lo64(wg), hi = hi64(wg);
+                    const unsigned long long old = atomicAdd(&S.W[gc][0], lo);
+                    const unsigned long long carry = (old + lo < old) ? 1ull : 0ull;
+                    atomicAdd(&S.W[gc][1], hi + carry);
                 }
             }
         } else {
             // the sort was not safe (fp32 ratio too far off, or too many
             // undecided elements): every chunk again with the exact masses
             for (int c = 0; c < NC; ++c) {
-                i128 w[RPT];
-                rj_weights8<DT>(J, c * RCH + tid * RPT, V, true, Zt, Zd, w, S.tab);
+                i128 w[RFPT];
+                rj_weights4<DT>(J, c * RCH + tid * RFPT, V, true, Zt, Zd, w, S.tab);
                 i128 s = 0;
 #pragma unroll
-                for (int i = 0; i < RPT; ++i)
+                for (int i = 0; i < RFPT; ++i)
                     s += w[i];
                 i128 tot;
                 (void)cta_excl_scan(s, tot, S);
@@ -660,37 +613,25 @@ __device__ int resolve_finish(const RJob &J, int V, const RzRec *recs, const RkR
                 }
             }
         }
-    } else {
-#pragma unroll
-        for (int h = 0; h < 2; ++h) {
-            const int c = 2 * tid + h;
-            if (c < NC) {
-                S.W[c][0] = (unsigned long long)zt[h];
-                S.W[c][1] = 0ull;
-            }
-        }
+    } else if (tid < NC) {
+        S.W[tid][0] = (unsigned long long)zt;
+        S.W[tid][1] = 0ull;
     }
     __syncthreads();
 
     for (int attempt = 0; attempt < 2; ++attempt) {
         // prefix over chunks; the crossing chunk is the first positive one
         // whose running mass exceeds floor(u * R)
-        const i128 w0 = (2 * tid < NC) ? mk128(S.W[2 * tid][0], S.W[2 * tid][1]) : (i128)0;
-        const i128 w1 =
-            (2 * tid + 1 < NC) ? mk128(S.W[2 * tid + 1][0], S.W[2 * tid + 1][1]) : (i128)0;
+        const i128 w0 = (tid < NC) ? mk128(S.W[tid][0], S.W[tid][1]) : (i128)0;
         i128 R;
-        const i128 ex = cta_excl_scan(w0 + w1, R, S);
+        const i128 ex = cta_excl_scan(w0, R, S);
         if (!(R > 0)) {
             if (residual) {
                 // the residual vanished (rounding only): draw from the target row
                 residual = false;
-#pragma unroll
-                for (int h = 0; h < 2; ++h) {
-                    const int c = 2 * tid + h;
-                    if (c < NC) {
-                        S.W[c][0] = (unsigned long long)zt[h];
-                        S.W[c][1] = 0ull;
-                    }
+                if (tid < NC) {
+                    S.W[tid][0] = (unsigned long long)zt;
+                    S.W[tid][1] = 0ull;
                 }
                 __syncthreads();
                 continue;
@@ -704,18 +645,9 @@ __device__ int resolve_finish(const RJob &J, int V, const RzRec *recs, const RkR
             S.lastp = -1;
         }
         __syncthreads();
-        const i128 in0 = ex + w0, in1 = in0 + w1;
-        int mine = INT_MAX;
-        i128 bef = 0;
-        if (w0 > 0 && in0 > theta) {
-            mine = 2 * tid;
-            bef = ex;
-        } else if (w1 > 0 && in1 > theta) {
-            mine = 2 * tid + 1;
-            bef = in0;
-        }
-        if (mine != INT_MAX)
-            atomicMin(&S.cstar, mine);
+        const bool mine = w0 > 0 && ex + w0 > theta;
+        if (mine)
+            atomicMin(&S.cstar, tid);
         __syncthreads();
         if (S.cstar == INT_MAX) {
             // floor(u * R) at or past the total: the last positive chunk
@@ -735,28 +667,28 @@ __device__ int resolve_finish(const RJob &J, int V, const RzRec *recs, const RkR
                 S.before[0] = lo64(bl);
                 S.before[1] = hi64(bl);
             }
-        } else if (mine == S.cstar) {
-            S.before[0] = lo64(bef);
-            S.before[1] = hi64(bef);
+        } else if (mine && tid == S.cstar) {
+            S.before[0] = lo64(ex);
+            S.before[1] = hi64(ex);
         }
         __syncthreads();
         const int cs = S.cstar;
         // the crossing chunk, element by element in index order
-        i128 w[RPT];
-        rj_weights8<DT>(J, cs * RCH + tid * RPT, V, residual, Zt, Zd, w, S.tab);
+        i128 w[RFPT];
+        rj_weights4<DT>(J, cs * RCH + tid * RFPT, V, residual, Zt, Zd, w, S.tab);
         i128 s = 0;
 #pragma unroll
-        for (int i = 0; i < RPT; ++i)
+        for (int i = 0; i < RFPT; ++i)
             s += w[i];
         i128 tot;
         const i128 exv = cta_excl_scan(s, tot, S);
         i128 run = mk128(S.before[0], S.before[1]) + exv;
         int cand = INT_MAX, lastp = -1;
 #pragma unroll
-        for (int i = 0; i < RPT; ++i) {
+        for (int i = 0; i < RFPT; ++i) {
             if (w[i] > 0) {
                 run += w[i];
-                lastp = cs * RCH + tid * RPT + i;
+                lastp = cs * RCH + tid * RFPT + i;
                 if (cand == INT_MAX && run > theta)
                     cand = lastp;
             }

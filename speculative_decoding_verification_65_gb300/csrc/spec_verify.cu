@@ -153,7 +153,6 @@ struct Params {
     // exact draws of the rows whose fp32 draw is near a cell boundary
     int *rlist;            // [B] sequences listed (count in hdr->n_flag)
     RJob *rjob;            // [B] their exact-draw records (written with the list)
-    unsigned int *rdone;   // [B] chunks finished per listed sequence
     unsigned int *rkcnt;   // [B] undecided elements per listed sequence
     RkRec *rkink;          // [B][RKCAP]
     RzRec *rrec;           // [B][RNC] chunk records
@@ -2681,7 +2680,6 @@ __global__ void __launch_bounds__(SCAN_WARPS * 32) final_kernel(const Params P)
         const unsigned int f = atomicAdd(&P.hdr->n_flag, 1u);
         P.rlist[f] = b;
         P.rjob[f] = make_rjob<DT, FILT>(P, J, b);
-        P.rdone[f] = 0u;
         P.rkcnt[f] = 0u;
     }
     if (P.out_draw && lane == 0) {
@@ -2714,12 +2712,12 @@ __global__ void __launch_bounds__(RTH, 3) resolve_kernel(const Params P)
     __shared__ RSmem S;
     const int tid = threadIdx.x;
     load_exp2_table(S.tab);
+    allow_next_kernel();     // the finishing kernel may launch; it waits for this grid
     wait_previous_kernel();  // the list comes from the final kernel
     const unsigned int nf = *reinterpret_cast<volatile unsigned int *>(&P.hdr->n_flag);
     const long long NC = P.RNC;
     const long long items = (long long)nf * NC;
-    // items are handed out by a counter (the first gridDim.x implicitly), so a
-    // CTA busy finishing a sequence does not hold up the items behind it
+    // items are handed out by a counter (the first gridDim.x implicitly)
     long long it = blockIdx.x;
     __syncthreads();
     while (it < items) {
@@ -2732,30 +2730,41 @@ __global__ void __launch_bounds__(RTH, 3) resolve_kernel(const Params P)
                 __ldcg(reinterpret_cast<const uint4 *>(P.rjob + f) + tid);
         __syncthreads();
         const long long nx = S.next;  // read here: thread 0 rewrites it next iteration
-        const RJob &J = S.job;
-        RzRec *recs = P.rrec + (size_t)f * NC;
-        resolve_chunk<DT>(J, q, P.V, recs + q, P.rkink + (size_t)f * RKCAP, P.rkcnt + f, S);
-        if (tid == 0) {
-            __threadfence();
-            const unsigned int t = atomicAdd(P.rdone + f, 1u);
-            S.last = (t == (unsigned int)NC - 1u) ? 1 : 0;
-        }
-        __syncthreads();
-        if (S.last) {
-            __threadfence();
-            const unsigned int kc = *reinterpret_cast<volatile unsigned int *>(P.rkcnt + f);
-            const int tok =
-                resolve_finish<DT>(J, P.V, recs, P.rkink + (size_t)f * RKCAP, kc, S, P.hdr);
-            if (tid == 0) {
-                const int b = __ldcg(P.rlist + f);
-                if (tok >= 0)
-                    P.out_tokens[(size_t)b * (P.k + 1) + J.j] = tok;
-                if (P.out_draw)
-                    P.out_draw[(size_t)b * 4 + 2] = tok;
-            }
-        }
+        resolve_chunk<DT>(S.job, q, P.V, P.rrec + (size_t)f * NC + q,
+                          P.rkink + (size_t)f * RKCAP, P.rkcnt + f, S);
         __syncthreads();
         it = nx;
+    }
+}
+
+// One CTA per listed sequence (grid-stride): the exact draw from the chunk
+// records, written to out_tokens[b][j].
+template <int DT, bool FILT>
+__global__ void __launch_bounds__(RFTH, 1) resolve_final_kernel(const Params P)
+{
+    __shared__ RFSmem S;
+    __shared__ RJob job;
+    const int tid = threadIdx.x;
+    load_exp2_table(S.tab);
+    wait_previous_kernel();  // chunk records come from the chunk kernel
+    const unsigned int nf = *reinterpret_cast<volatile unsigned int *>(&P.hdr->n_flag);
+    const long long NC = P.RNC;
+    for (unsigned int f = blockIdx.x; f < nf; f += gridDim.x) {
+        if (tid < (int)(sizeof(RJob) / 16))
+            reinterpret_cast<uint4 *>(&job)[tid] =
+                __ldcg(reinterpret_cast<const uint4 *>(P.rjob + f) + tid);
+        __syncthreads();
+        const unsigned int kc = __ldcg(P.rkcnt + f);
+        const int tok = resolve_finish<DT>(job, P.V, P.rrec + (size_t)f * NC,
+                                           P.rkink + (size_t)f * RKCAP, kc, S, P.hdr);
+        if (tid == 0) {
+            const int b = __ldcg(P.rlist + f);
+            if (tok >= 0)
+                P.out_tokens[(size_t)b * (P.k + 1) + job.j] = tok;
+            if (P.out_draw)
+                P.out_draw[(size_t)b * 4 + 2] = tok;
+        }
+        __syncthreads();
     }
 }
 
@@ -2784,15 +2793,15 @@ bool sizes_ok(int32_t B, int32_t k, int32_t V, int32_t dtype)
 int tile_elems(int32_t dtype) { return TILE_BYTES / (dtype == SPEC_F32 ? 4 : 2); }
 
 struct WsLayout {
-    size_t partials, jobs, chunks, rec, filt, rlist, rjob, rdone, rkcnt, rkink, rrec, total;
+    size_t partials, jobs, chunks, rec, filt, rlist, rjob, rkcnt, rkink, rrec, total;
     size_t NS, NSS, DS, chunk_stride, NCH, RNC;
 };
 
 // header | one 16-byte partial per super-tile [B][2k+1][NSS] | draw jobs [B] |
 // inverse-CDF chunk totals [B][chunk_stride] | bonus-row chunk records [B][NCH]
 // | top-k / top-p records [B][2k+1] (filtered calls) | exact-draw list [B],
-// their records [B], tickets [B], undecided counts [B], groups of undecided
-// elements [B][RKCAP], chunk records [B][RNC]
+// their records [B], undecided counts [B], groups of undecided elements
+// [B][RKCAP], chunk records [B][RNC]
 WsLayout ws_layout(int32_t B, int32_t k, int32_t V, int32_t dtype)
 {
     WsLayout w;
@@ -2811,8 +2820,7 @@ WsLayout ws_layout(int32_t B, int32_t k, int32_t V, int32_t dtype)
     w.RNC = ((size_t)V + RCH - 1) / RCH;
     w.rlist = align_up(w.filt + (size_t)B * (2 * (size_t)k + 1) * sizeof(FiltRec), 256);
     w.rjob = align_up(w.rlist + (size_t)B * 4, 256);
-    w.rdone = align_up(w.rjob + (size_t)B * sizeof(RJob), 256);
-    w.rkcnt = align_up(w.rdone + (size_t)B * 4, 256);
+    w.rkcnt = align_up(w.rjob + (size_t)B * sizeof(RJob), 256);
     w.rkink = align_up(w.rkcnt + (size_t)B * 4, 256);
     w.rrec = align_up(w.rkink + (size_t)B * RKCAP * sizeof(RkRec), 256);
     w.total = w.rrec + (size_t)B * w.RNC * sizeof(RzRec);
@@ -2828,7 +2836,7 @@ size_t ws_bytes(int32_t B, int32_t k, int32_t V, int32_t dtype)
 // with the filter kernels of a filtered call).
 template <int DT, bool FILT>
 int launch_all(const Params &P, unsigned int grid1, unsigned int gridf, unsigned int gridr,
-               cudaStream_t st, void *const *events)
+               unsigned int gridrf, cudaStream_t st, void *const *events)
 {
     // filtered calls record one more event, after the filter kernel
     auto mark = [&](int i) {
@@ -2878,6 +2886,8 @@ int launch_all(const Params &P, unsigned int grid1, unsigned int gridf, unsigned
         return SPEC_ECUDA;
     mark(3);
     if (dependent(resolve_kernel<DT, FILT>, gridr, RTH) != cudaSuccess)
+        return SPEC_ECUDA;
+    if (dependent(resolve_final_kernel<DT, FILT>, gridrf, RFTH) != cudaSuccess)
         return SPEC_ECUDA;
     mark(4);
     if (cudaPeekAtLastError() != cudaSuccess) {
@@ -2989,7 +2999,6 @@ int launch(const void *target, const void *draft, const int32_t *tokens, const f
     P.filt = reinterpret_cast<FiltRec *>(w + lay.filt);
     P.rlist = reinterpret_cast<int *>(w + lay.rlist);
     P.rjob = reinterpret_cast<RJob *>(w + lay.rjob);
-    P.rdone = reinterpret_cast<unsigned int *>(w + lay.rdone);
     P.rkcnt = reinterpret_cast<unsigned int *>(w + lay.rkcnt);
     P.rkink = reinterpret_cast<RkRec *>(w + lay.rkink);
     P.rrec = reinterpret_cast<RzRec *>(w + lay.rrec);
@@ -3014,12 +3023,13 @@ int launch(const void *target, const void *draft, const int32_t *tokens, const f
     // the exact draws: two CTAs per SM, at most one work item each to begin with
     const size_t ritems = (size_t)B * lay.RNC;
     const unsigned int gridr = (unsigned int)(ritems < 3 * n_sms ? ritems : 3 * n_sms);
+    const unsigned int gridrf = (unsigned int)((size_t)B < n_sms ? (size_t)B : n_sms);
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
     if (filtered)
-        return (dtype == SPEC_F32) ? launch_all<SPEC_F32, true>(P, grid1, gridf, gridr, st, events)
-                                   : launch_all<SPEC_BF16, true>(P, grid1, gridf, gridr, st, events);
-    return (dtype == SPEC_F32) ? launch_all<SPEC_F32, false>(P, grid1, 0, gridr, st, events)
-                               : launch_all<SPEC_BF16, false>(P, grid1, 0, gridr, st, events);
+        return (dtype == SPEC_F32) ? launch_all<SPEC_F32, true>(P, grid1, gridf, gridr, gridrf, st, events)
+                                   : launch_all<SPEC_BF16, true>(P, grid1, gridf, gridr, gridrf, st, events);
+    return (dtype == SPEC_F32) ? launch_all<SPEC_F32, false>(P, grid1, 0, gridr, gridrf, st, events)
+                               : launch_all<SPEC_BF16, false>(P, grid1, 0, gridr, gridrf, st, events);
 }
 
 }  // namespace

@@ -70,13 +70,12 @@ def test_workspace_size(lib, B, k, V, dt, ok):
     rec = up(chunks + B * up(ds * 4 * 8, 32) * 4, 256)
     filt = up(rec + B * nch * 8, 256)
     # the exact draw: per sequence a list entry, a 96-byte draw record, a
-    # ticket, a group count, 64 groups of 32 bytes, and a 32-byte record per
-    # 2048 elements
+    # group count, 64 groups of 32 bytes, and a 32-byte record per 2048
+    # elements
     rnc = -(-V // 2048)
     rlist = up(filt + B * (2 * k + 1) * 16, 256)
     rjob = up(rlist + 4 * B, 256)
-    rdone = up(rjob + 96 * B, 256)
-    rkcnt = up(rdone + 4 * B, 256)
+    rkcnt = up(rjob + 96 * B, 256)
     rkink = up(rkcnt + 4 * B, 256)
     rrec = up(rkink + 32 * 64 * B, 256)
     assert n == rrec + B * rnc * 32
