@@ -852,6 +852,7 @@ def run_ours_sample(args):
     torch.cuda.synchronize(dev)
     kern_ms = [s.elapsed_time(e[0]) for s, e in zip(starts, stages)]
     pick_ms = statistics.mean(e[0].elapsed_time(e[1]) for e in stages)
+    exact_ms = statistics.mean(e[1].elapsed_time(e[2]) for e in stages)
     ms_per_step = total_ms / args.steps
     value = aggregate_rate(R, args.steps, world, total_ms / 1e3)
     status = sv.spec_verify_read_status(ws)
@@ -913,7 +914,7 @@ def run_ours_sample(args):
                      "kernel_ms_avg": kern_avg_s * 1e3, "kernel_ms_min": min(kern_ms),
                      "frac_of_nominal_8TBs": achieved / 8000.0,
                      "step_GBps": alg_bytes / (ms_per_step / 1e3) / 1e9},
-        "stage_ms": {"chunk": kern_avg_s * 1e3, "pick": pick_ms},
+        "stage_ms": {"chunk": kern_avg_s * 1e3, "pick": pick_ms, "exact_draws": exact_ms},
         "clocks": clk.summary(),
         "e2e": {"value": e2e_value, "unit": SAMPLE_UNIT, "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": R * 4, "steps": e2e_steps},

@@ -40,10 +40,11 @@ extern "C" {
 #endif
 
 /*
- * Bytes of device workspace one spec_sample call needs: the 256-byte header
- * and an 8-byte record per 4 KB chunk of every row (R * ceil(V * elem / 4096)
- * records).  Returns 0 for sizes out of range (R < 0, V < 2, V > SPEC_MAX_V,
- * unknown dtype).  Host-only; needs no GPU.
+ * Bytes of device workspace one spec_sample call needs: the 256-byte header,
+ * an 8-byte record per 4 KB chunk of every row (R * ceil(V * elem / 4096)
+ * records), and room for the exact draw of every row (100 bytes plus 32 bytes
+ * per 2048 elements of a row).  Returns 0 for sizes out of range (R < 0,
+ * V < 2, V > SPEC_MAX_V, unknown dtype).  Host-only; needs no GPU.
  */
 size_t spec_sample_workspace_size(int32_t R, int32_t V, int32_t dtype);
 
@@ -58,8 +59,13 @@ size_t spec_sample_workspace_size(int32_t R, int32_t V, int32_t dtype);
  *                beforehand (see SPEC_DEV_OK).  Two calls in flight at once
  *                must not share one.
  *   stream       cudaStream_t as void*.
- * Two kernels run in order on `stream`: chunk records (the one read of the
- * logits), then the per-row pick.  Returns SPEC_OK once they are launched
+ * Four kernels run in order on `stream`: chunk records (the one read of the
+ * logits), the per-row pick, and the exact draws (two kernels) of the rows
+ * whose fp32 pick landed within 2e-6 of R of a cell edge: their weights in
+ * float-float arithmetic and exact fixed-point sums (about 1e-12 of R), so a
+ * token equals the exactly rounded draw unless u lies within ~1e-12 of an
+ * edge.  With no row listed the last two only read the count.  Returns
+ * SPEC_OK once they are launched
  * (R == 0 launches nothing); SPEC_EINVAL for bad sizes, null or misaligned
  * pointers; SPEC_ENOSPACE for a short workspace; SPEC_ECUDA for a failed
  * launch.
@@ -71,9 +77,10 @@ int32_t spec_sample(const void *logits, const float *u, const float *temperature
 /*
  * spec_sample recording the caller's cudaEvent_t handles (SPEC_SAMPLE_STAGES
  * of them; the array and its entries may be NULL) on `stream` after each
- * kernel: chunk records, then pick.  Used to time the HBM-bound first kernel.
+ * stage: chunk records, pick, exact draws.  Used to time the HBM-bound first
+ * kernel.
  */
-#define SPEC_SAMPLE_STAGES 2
+#define SPEC_SAMPLE_STAGES 3
 int32_t spec_sample_timed(const void *logits, const float *u, const float *temperature,
                           int32_t *out_tokens, int32_t R, int32_t V, int32_t dtype,
                           void *workspace, size_t workspace_bytes, void *stream,

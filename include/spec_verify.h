@@ -96,7 +96,7 @@ const char *spec_verify_strerror(int32_t status);
  * row, and per sequence an 80-byte draw record, its inverse-CDF chunk totals
  * (32 bytes per 16 KB of a row), its bonus row's chunk records (8 bytes per
  * 4 KB of a row), a 16-byte top-k / top-p record per row (read by
- * spec_verify_filtered only), and room for its exact draw (2152 bytes plus
+ * spec_verify_filtered only), and room for its exact draw (2148 bytes plus
  * 32 bytes per 2048 elements of a row).  Returns 0 for sizes out of range.
  * Host-only; needs no GPU.
  */

@@ -28,7 +28,7 @@ SPEC_DEV_WAIT_TIMEOUT = 1
 SPEC_MAX_K = 32
 SPEC_MAX_V = 1 << 20
 SPEC_STAGES = 5
-SPEC_SAMPLE_STAGES = 2
+SPEC_SAMPLE_STAGES = 3
 SPEC_FILTERED_STAGES = 6
 SPEC_LMHEAD_STAGES = 5
 
@@ -525,8 +525,8 @@ def spec_sample(logits, u, temperature, out=None, ws=None, stream=None):
 
 def spec_sample_timed(logits, u, temperature, out, ws, stage_events, stream=None):
     """spec_sample recording the given torch.cuda.Event objects
-    (SPEC_SAMPLE_STAGES of them, recorded once beforehand) after each kernel:
-    chunk records, pick."""
+    (SPEC_SAMPLE_STAGES of them, recorded once beforehand) after each stage:
+    chunk records, pick, exact draws."""
     torch = _torch()
     R, V, dt = _marshal_sample(logits, u, temperature)
     _dev_out("out", out, (R,), torch.int32, logits.device)

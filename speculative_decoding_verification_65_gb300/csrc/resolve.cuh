@@ -72,8 +72,8 @@ struct alignas(16) RJob {
     int filt;        // top-k / top-p: x counts in a row iff key > k_ or (key == k_ and x <= i_)
     unsigned int kt, kd;
     int it, id;
-    int j;           // the position drawn (out_tokens[b][j])
-    int pad[2];
+    int b;           // the trace row (spec_verify_trace), or unused
+    long long out_pos;  // where the token goes in the output array
 };
 static_assert(sizeof(RJob) % 16 == 0, "an exact-draw record is whole 16-byte vectors");
 
@@ -706,6 +706,136 @@ __device__ int resolve_finish(const RJob &J, int V, const RzRec *recs, const RkR
         return tok;
     }
     return -1;
+}
+
+// ------------------------------------------------------------ the kernels
+//
+// Listed rows are drawn again in two kernels: the chunk pass (work items
+// (listed row, chunk of 2048 elements), handed out by a counter over a
+// persistent grid) and the finishing (one CTA per listed row).  The list,
+// its records and the counters live in the caller's workspace; the first
+// kernel of each call zeroes hdr->n_flag and hdr->next_resolve.
+
+struct RParams {
+    WsHeader *hdr;
+    const RJob *rjob;      // [cap] the listed draws (count in hdr->n_flag)
+    RkRec *rkink;          // [cap][RKCAP] groups of undecided elements
+    unsigned int *rkcnt;   // [cap] their counts (zeroed when listed)
+    RzRec *rrec;           // [cap][RNC] chunk records
+    int RNC, V;
+    int32_t *out;          // the token goes to out[out_pos]
+    int32_t *out_draw;     // nullable [B][4]: the exact token goes to out_draw[4b + 2]
+};
+
+template <int DT>
+__global__ void __launch_bounds__(RTH, 3) resolve_chunks_kernel(const RParams P)
+{
+    __shared__ RSmem S;
+    const int tid = threadIdx.x;
+    load_exp2_table(S.tab);
+    allow_next_kernel();     // the finishing kernel may launch; it waits for this grid
+    wait_previous_kernel();  // the list comes from the previous kernel
+    const unsigned int nf = *reinterpret_cast<volatile unsigned int *>(&P.hdr->n_flag);
+    const long long NC = P.RNC;
+    const long long items = (long long)nf * NC;
+    // items are handed out by a counter (the first gridDim.x implicitly)
+    long long it = blockIdx.x;
+    __syncthreads();
+    while (it < items) {
+        const int f = (int)(it / NC);
+        const int q = (int)(it - (long long)f * NC);
+        if (tid == 0)
+            S.next = (long long)gridDim.x + (long long)atomicAdd(&P.hdr->next_resolve, 1u);
+        if (tid < (int)(sizeof(RJob) / 16))
+            reinterpret_cast<uint4 *>(&S.job)[tid] =
+                __ldcg(reinterpret_cast<const uint4 *>(P.rjob + f) + tid);
+        __syncthreads();
+        const long long nx = S.next;  // read here: thread 0 rewrites it next iteration
+        resolve_chunk<DT>(S.job, q, P.V, P.rrec + (size_t)f * NC + q,
+                          P.rkink + (size_t)f * RKCAP, P.rkcnt + f, S);
+        __syncthreads();
+        it = nx;
+    }
+}
+
+template <int DT>
+__global__ void __launch_bounds__(RFTH, 1) resolve_final_kernel(const RParams P)
+{
+    __shared__ RFSmem S;
+    __shared__ RJob job;
+    const int tid = threadIdx.x;
+    load_exp2_table(S.tab);
+    wait_previous_kernel();  // chunk records come from the chunk pass
+    const unsigned int nf = *reinterpret_cast<volatile unsigned int *>(&P.hdr->n_flag);
+    const long long NC = P.RNC;
+    for (unsigned int f = blockIdx.x; f < nf; f += gridDim.x) {
+        if (tid < (int)(sizeof(RJob) / 16))
+            reinterpret_cast<uint4 *>(&job)[tid] =
+                __ldcg(reinterpret_cast<const uint4 *>(P.rjob + f) + tid);
+        __syncthreads();
+        const unsigned int kc = __ldcg(P.rkcnt + f);
+        const int tok = resolve_finish<DT>(job, P.V, P.rrec + (size_t)f * NC,
+                                           P.rkink + (size_t)f * RKCAP, kc, S, P.hdr);
+        if (tid == 0) {
+            if (tok >= 0)
+                P.out[job.out_pos] = tok;
+            if (P.out_draw)
+                P.out_draw[(size_t)job.b * 4 + 2] = tok;
+        }
+        __syncthreads();
+    }
+}
+
+// Launches both kernels on `st` as programmatic dependents of the kernel
+// before them (plainly ordered when `pdl` is false).  grid_chunks CTAs of the
+// chunk pass, grid_final of the finishing.
+template <int DT>
+inline cudaError_t launch_resolve(const RParams &P, unsigned int grid_chunks,
+                                  unsigned int grid_final, cudaStream_t st, bool pdl)
+{
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = pdl ? 1 : 0;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid_chunks);
+    cfg.blockDim = dim3(RTH);
+    cfg.stream = st;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    cudaError_t e = cudaLaunchKernelEx(&cfg, resolve_chunks_kernel<DT>, P);
+    if (e != cudaSuccess)
+        return e;
+    cfg.gridDim = dim3(grid_final);
+    cfg.blockDim = dim3(RFTH);
+    return cudaLaunchKernelEx(&cfg, resolve_final_kernel<DT>, P);
+}
+
+// Workspace bytes for the exact draws of up to `cap` listed rows of V
+// elements: their records, counts, groups (residual draws only) and chunk
+// records.
+inline size_t resolve_bytes(size_t cap, int V, bool residual)
+{
+    const size_t rnc = ((size_t)V + RCH - 1) / RCH;
+    auto up = [](size_t x) { return (x + 255) / 256 * 256; };
+    return up(cap * sizeof(RJob)) + up(cap * 4) +
+           (residual ? up(cap * RKCAP * sizeof(RkRec)) : 0) + up(cap * rnc * sizeof(RzRec));
+}
+
+// The exact-draw regions of a workspace starting at `base` (from resolve_bytes).
+inline void resolve_regions(RParams &P, void *base, size_t cap, int V, bool residual)
+{
+    const size_t rnc = ((size_t)V + RCH - 1) / RCH;
+    auto up = [](size_t x) { return (x + 255) / 256 * 256; };
+    uint8_t *w = reinterpret_cast<uint8_t *>(base);
+    P.rjob = reinterpret_cast<const RJob *>(w);
+    w += up(cap * sizeof(RJob));
+    P.rkcnt = reinterpret_cast<unsigned int *>(w);
+    w += up(cap * 4);
+    P.rkink = residual ? reinterpret_cast<RkRec *>(w) : nullptr;
+    w += residual ? up(cap * RKCAP * sizeof(RkRec)) : 0;
+    P.rrec = reinterpret_cast<RzRec *>(w);
+    P.RNC = (int)rnc;
+    P.V = V;
 }
 
 }  // namespace spec_dev

@@ -40,6 +40,7 @@
 #include "internal.h"
 #include "spec_verify.h"
 #include "device_common.cuh"
+#include "resolve.cuh"
 
 namespace {
 
@@ -86,6 +87,10 @@ struct SParams {
     unsigned long long bytes;
     int rows_per_temp;  // row r's temperature is temperature[r / rows_per_temp]
     int skip_greedy;    // rows at T = 0 are not read (their records are not used)
+    // the exact draw of rows whose fp32 draw lands near a cell edge
+    RJob *rjob;          // [R] the listed rows (count in hdr->n_flag)
+    unsigned int *rkcnt; // [R]
+    float guard;         // list when u*R is within guard*R of a cell edge
 };
 
 struct Smem {
@@ -112,6 +117,10 @@ __global__ void __launch_bounds__(NTHREADS, 2) chunk_kernel(const SParams P)
     const int warp = tid >> 5, lane = tid & 31;
 
     if (tid == 0) {
+        if (blockIdx.x == 0) {  // the exact draws' counters (used after this grid)
+            P.hdr->n_flag = 0u;
+            P.hdr->next_resolve = 0u;
+        }
         for (int s = 0; s < STAGES; ++s) {
             mbar_init(&S.full[s], 1);
             mbar_init(&S.empty[s], NCW);
@@ -366,9 +375,29 @@ __global__ void __launch_bounds__(PICK_WARPS * 32) pick_kernel(const SParams P)
     }
 
     bool near = false;
-    const int tok = records_draw<DT>(rc, P.NC, m, c, uu, P.logits, (size_t)r, P.V, lane, 0.0f, near);
-    if (lane == 0)
+    const int tok = records_draw<DT>(rc, P.NC, m, c, uu, P.logits, (size_t)r, P.V, lane, P.guard, near);
+    if (lane == 0) {
         P.out[r] = tok;
+        if (near && tok >= 0 && P.rjob) {
+            // list the row for the exact draw (resolve.cuh), which rewrites out[r]
+            const unsigned int f = atomicAdd(&P.hdr->n_flag, 1u);
+            RJob J;
+            J.t_arr = J.d_arr = P.logits;
+            J.t_row = J.d_row = r;
+            J.mode = RJ_TARGET;
+            J.mt = J.md = m;
+            J.rzt = J.rzd = 1.0f;
+            exp_coef(T, J.ch, J.cl);
+            J.u = uu;
+            J.filt = 0;
+            J.kt = J.kd = 0u;
+            J.it = J.id = 0;
+            J.b = r;
+            J.out_pos = r;
+            P.rjob[f] = J;
+            P.rkcnt[f] = 0u;
+        }
+    }
 }
 
 // --------------------------------------------------------------- host side
@@ -391,11 +420,12 @@ bool sizes_ok(int32_t R, int32_t V, int32_t dtype)
 }
 
 struct Layout {
-    size_t rec, total;
+    size_t rec, resolve, total;
     size_t NS, NC;
 };
 
-// header | chunk records [R][NC]
+// header | chunk records [R][NC] | the exact draws of up to R listed rows
+// (resolve.cuh)
 Layout layout(int32_t R, int32_t V, int32_t dtype)
 {
     Layout w;
@@ -404,12 +434,14 @@ Layout layout(int32_t R, int32_t V, int32_t dtype)
     w.NS = (row_bytes + TILE_BYTES - 1) / TILE_BYTES;
     w.NC = (row_bytes + CHUNK_BYTES - 1) / CHUNK_BYTES;
     w.rec = sizeof(WsHeader);
-    w.total = align_up(w.rec + (size_t)R * w.NC * sizeof(float2), 256);
+    w.resolve = align_up(w.rec + (size_t)R * w.NC * sizeof(float2), 256);
+    w.total = w.resolve + resolve_bytes((size_t)R, V, false);
     return w;
 }
 
 template <int DT>
-int launch_all(const SParams &P, unsigned int grid1, cudaStream_t st, void *const *events)
+int launch_all(const SParams &P, const RParams &RP, unsigned int gridr, unsigned int gridrf,
+               unsigned int grid1, cudaStream_t st, void *const *events)
 {
     auto mark = [&](int i) {
         if (events && events[i])
@@ -433,6 +465,9 @@ int launch_all(const SParams &P, unsigned int grid1, cudaStream_t st, void *cons
     if (cudaLaunchKernelEx(&cfg, pick_kernel<DT>, P) != cudaSuccess)
         return SPEC_ECUDA;
     mark(1);
+    if (launch_resolve<DT>(RP, gridr, gridrf, st, !events) != cudaSuccess)
+        return SPEC_ECUDA;
+    mark(2);
     if (cudaPeekAtLastError() != cudaSuccess) {
         (void)cudaGetLastError();
         return SPEC_ECUDA;
@@ -491,8 +526,17 @@ int setup_chunks(SParams &P, unsigned int &grid1, const void *logits, const floa
     P.bytes = (unsigned long long)R * (unsigned long long)V * ((dtype == SPEC_F32) ? 4 : 2);
     P.rows_per_temp = 1;
     P.skip_greedy = 0;
+    P.rjob = nullptr;
+    P.rkcnt = nullptr;
+    P.guard = 0.0f;
     return SPEC_OK;
 }
+
+// The fp32 draw's guard: a draw whose u * R lies within this fraction of R
+// of the chosen cell's edges is drawn again exactly.  The fp32 record sums
+// err by under 3e-7 of R (measured against the fp64 oracle on the sampled
+// rows of the synthetic workloads).
+constexpr float SAMPLE_GUARD = 2e-6f;
 
 int launch(const void *logits, const float *u, const float *temp, int32_t *out, int32_t R,
            int32_t V, int32_t dtype, void *ws, size_t ws_size, void *stream,
@@ -520,10 +564,26 @@ int launch(const void *logits, const float *u, const float *temp, int32_t *out, 
         return rc;
     P.u = u;
     P.out = out;
+    RParams RP;
+    resolve_regions(RP, w + lay.resolve, (size_t)R, V, false);
+    RP.hdr = P.hdr;
+    RP.out = out;
+    RP.out_draw = nullptr;
+    RP.rkink = nullptr;
+    P.rjob = const_cast<RJob *>(RP.rjob);
+    P.rkcnt = RP.rkcnt;
+    P.guard = SAMPLE_GUARD;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64)
+        return SPEC_ECUDA;
+    const size_t n_sms = (size_t)g_dev[dev].sms.load(std::memory_order_relaxed);  // set by setup_chunks
+    const size_t ritems = (size_t)R * (size_t)RP.RNC;
+    const unsigned int gridr = (unsigned int)(ritems < 3 * n_sms ? ritems : 3 * n_sms);
+    const unsigned int gridrf = (unsigned int)((size_t)R < n_sms ? (size_t)R : n_sms);
 
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-    return (dtype == SPEC_F32) ? launch_all<SPEC_F32>(P, grid1, st, events)
-                               : launch_all<SPEC_BF16>(P, grid1, st, events);
+    return (dtype == SPEC_F32) ? launch_all<SPEC_F32>(P, RP, gridr, gridrf, grid1, st, events)
+                               : launch_all<SPEC_BF16>(P, RP, gridr, gridrf, grid1, st, events);
 }
 
 // host arena: logits | u | temperature | out | workspace, each 256-byte aligned

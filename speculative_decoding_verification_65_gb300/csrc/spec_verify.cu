@@ -151,12 +151,8 @@ struct Params {
     const float *top_p;    // [B] or null (filtered calls)
     FiltRec *filt;     // [B][rows] (filtered calls)
     // exact draws of the rows whose fp32 draw is near a cell boundary
-    int *rlist;            // [B] sequences listed (count in hdr->n_flag)
-    RJob *rjob;            // [B] their exact-draw records (written with the list)
-    unsigned int *rkcnt;   // [B] undecided elements per listed sequence
-    RkRec *rkink;          // [B][RKCAP]
-    RzRec *rrec;           // [B][RNC] chunk records
-    int RNC;               // resolve chunks per row
+    RJob *rjob;            // [B] the listed draws (count in hdr->n_flag)
+    unsigned int *rkcnt;   // [B] their counts of groups of undecided elements
     float guard_abs;       // residual draws: list when u*R is within this of a cell edge
     float guard_rel;       // bonus / target-row draws: within this times R
     int32_t *out_draw;     // nullable [B][4]: fp32 token, listed, exact token, reserved
@@ -2638,7 +2634,8 @@ __device__ __forceinline__ RJob make_rjob(const Params &P, const JobRec &Jr, int
     J.it = Jr.it;
     J.kd = Jr.kd;
     J.id = Jr.id;
-    J.j = Jr.j;
+    J.b = b;
+    J.out_pos = (long long)b * (P.k + 1) + Jr.j;
     return J;
 }
 
@@ -2678,7 +2675,6 @@ __global__ void __launch_bounds__(SCAN_WARPS * 32) final_kernel(const Params P)
     if (!err && near && lane == 0) {
         // list the sequence for the exact draw, which rewrites out_tokens[b][j]
         const unsigned int f = atomicAdd(&P.hdr->n_flag, 1u);
-        P.rlist[f] = b;
         P.rjob[f] = make_rjob<DT, FILT>(P, J, b);
         P.rkcnt[f] = 0u;
     }
@@ -2706,68 +2702,6 @@ __global__ void __launch_bounds__(SCAN_WARPS * 32) final_kernel(const Params P)
 // persistent grid; the CTA that finishes a sequence's last chunk (a ticket
 // counter, no waiting) forms the draw and rewrites out_tokens[b][j].
 
-template <int DT, bool FILT>
-__global__ void __launch_bounds__(RTH, 3) resolve_kernel(const Params P)
-{
-    __shared__ RSmem S;
-    const int tid = threadIdx.x;
-    load_exp2_table(S.tab);
-    allow_next_kernel();     // the finishing kernel may launch; it waits for this grid
-    wait_previous_kernel();  // the list comes from the final kernel
-    const unsigned int nf = *reinterpret_cast<volatile unsigned int *>(&P.hdr->n_flag);
-    const long long NC = P.RNC;
-    const long long items = (long long)nf * NC;
-    // items are handed out by a counter (the first gridDim.x implicitly)
-    long long it = blockIdx.x;
-    __syncthreads();
-    while (it < items) {
-        const int f = (int)(it / NC);
-        const int q = (int)(it - (long long)f * NC);
-        if (tid == 0)
-            S.next = (long long)gridDim.x + (long long)atomicAdd(&P.hdr->next_resolve, 1u);
-        if (tid < (int)(sizeof(RJob) / 16))
-            reinterpret_cast<uint4 *>(&S.job)[tid] =
-                __ldcg(reinterpret_cast<const uint4 *>(P.rjob + f) + tid);
-        __syncthreads();
-        const long long nx = S.next;  // read here: thread 0 rewrites it next iteration
-        resolve_chunk<DT>(S.job, q, P.V, P.rrec + (size_t)f * NC + q,
-                          P.rkink + (size_t)f * RKCAP, P.rkcnt + f, S);
-        __syncthreads();
-        it = nx;
-    }
-}
-
-// One CTA per listed sequence (grid-stride): the exact draw from the chunk
-// records, written to out_tokens[b][j].
-template <int DT, bool FILT>
-__global__ void __launch_bounds__(RFTH, 1) resolve_final_kernel(const Params P)
-{
-    __shared__ RFSmem S;
-    __shared__ RJob job;
-    const int tid = threadIdx.x;
-    load_exp2_table(S.tab);
-    wait_previous_kernel();  // chunk records come from the chunk kernel
-    const unsigned int nf = *reinterpret_cast<volatile unsigned int *>(&P.hdr->n_flag);
-    const long long NC = P.RNC;
-    for (unsigned int f = blockIdx.x; f < nf; f += gridDim.x) {
-        if (tid < (int)(sizeof(RJob) / 16))
-            reinterpret_cast<uint4 *>(&job)[tid] =
-                __ldcg(reinterpret_cast<const uint4 *>(P.rjob + f) + tid);
-        __syncthreads();
-        const unsigned int kc = __ldcg(P.rkcnt + f);
-        const int tok = resolve_finish<DT>(job, P.V, P.rrec + (size_t)f * NC,
-                                           P.rkink + (size_t)f * RKCAP, kc, S, P.hdr);
-        if (tid == 0) {
-            const int b = __ldcg(P.rlist + f);
-            if (tok >= 0)
-                P.out_tokens[(size_t)b * (P.k + 1) + job.j] = tok;
-            if (P.out_draw)
-                P.out_draw[(size_t)b * 4 + 2] = tok;
-        }
-        __syncthreads();
-    }
-}
-
 // ------------------------------------------------------------------ host side
 
 // Per-device launch facts, filled by the first call on each device.  Host
@@ -2793,15 +2727,14 @@ bool sizes_ok(int32_t B, int32_t k, int32_t V, int32_t dtype)
 int tile_elems(int32_t dtype) { return TILE_BYTES / (dtype == SPEC_F32 ? 4 : 2); }
 
 struct WsLayout {
-    size_t partials, jobs, chunks, rec, filt, rlist, rjob, rkcnt, rkink, rrec, total;
-    size_t NS, NSS, DS, chunk_stride, NCH, RNC;
+    size_t partials, jobs, chunks, rec, filt, resolve, total;
+    size_t NS, NSS, DS, chunk_stride, NCH;
 };
 
 // header | one 16-byte partial per super-tile [B][2k+1][NSS] | draw jobs [B] |
 // inverse-CDF chunk totals [B][chunk_stride] | bonus-row chunk records [B][NCH]
-// | top-k / top-p records [B][2k+1] (filtered calls) | exact-draw list [B],
-// their records [B], undecided counts [B], groups of undecided elements
-// [B][RKCAP], chunk records [B][RNC]
+// | top-k / top-p records [B][2k+1] (filtered calls) | the exact draws of up
+// to B listed sequences (resolve.cuh: records, counts, groups, chunk records)
 WsLayout ws_layout(int32_t B, int32_t k, int32_t V, int32_t dtype)
 {
     WsLayout w;
@@ -2817,13 +2750,8 @@ WsLayout ws_layout(int32_t B, int32_t k, int32_t V, int32_t dtype)
     w.chunk_stride = align_up(w.DS * UD * NCW, 32);  // floats, 128-byte rows
     w.rec = align_up(w.chunks + (size_t)B * w.chunk_stride * 4, 256);
     w.filt = align_up(w.rec + (size_t)B * w.NCH * sizeof(float2), 256);
-    w.RNC = ((size_t)V + RCH - 1) / RCH;
-    w.rlist = align_up(w.filt + (size_t)B * (2 * (size_t)k + 1) * sizeof(FiltRec), 256);
-    w.rjob = align_up(w.rlist + (size_t)B * 4, 256);
-    w.rkcnt = align_up(w.rjob + (size_t)B * sizeof(RJob), 256);
-    w.rkink = align_up(w.rkcnt + (size_t)B * 4, 256);
-    w.rrec = align_up(w.rkink + (size_t)B * RKCAP * sizeof(RkRec), 256);
-    w.total = w.rrec + (size_t)B * w.RNC * sizeof(RzRec);
+    w.resolve = align_up(w.filt + (size_t)B * (2 * (size_t)k + 1) * sizeof(FiltRec), 256);
+    w.total = w.resolve + resolve_bytes((size_t)B, V, true);
     return w;
 }
 
@@ -2835,8 +2763,8 @@ size_t ws_bytes(int32_t B, int32_t k, int32_t V, int32_t dtype)
 // `events` (nullable): cudaEvent_t recorded after each kernel (five, or six
 // with the filter kernels of a filtered call).
 template <int DT, bool FILT>
-int launch_all(const Params &P, unsigned int grid1, unsigned int gridf, unsigned int gridr,
-               unsigned int gridrf, cudaStream_t st, void *const *events)
+int launch_all(const Params &P, const RParams &RP, unsigned int grid1, unsigned int gridf,
+               unsigned int gridr, unsigned int gridrf, cudaStream_t st, void *const *events)
 {
     // filtered calls record one more event, after the filter kernel
     auto mark = [&](int i) {
@@ -2885,9 +2813,7 @@ int launch_all(const Params &P, unsigned int grid1, unsigned int gridf, unsigned
     if (dependent(final_kernel<DT, FILT>, gs, SCAN_WARPS * 32) != cudaSuccess)
         return SPEC_ECUDA;
     mark(3);
-    if (dependent(resolve_kernel<DT, FILT>, gridr, RTH) != cudaSuccess)
-        return SPEC_ECUDA;
-    if (dependent(resolve_final_kernel<DT, FILT>, gridrf, RFTH) != cudaSuccess)
+    if (launch_resolve<DT>(RP, gridr, gridrf, st, pdl) != cudaSuccess)
         return SPEC_ECUDA;
     mark(4);
     if (cudaPeekAtLastError() != cudaSuccess) {
@@ -2997,12 +2923,13 @@ int launch(const void *target, const void *draft, const int32_t *tokens, const f
     P.top_k = top_k;
     P.top_p = top_p;
     P.filt = reinterpret_cast<FiltRec *>(w + lay.filt);
-    P.rlist = reinterpret_cast<int *>(w + lay.rlist);
-    P.rjob = reinterpret_cast<RJob *>(w + lay.rjob);
-    P.rkcnt = reinterpret_cast<unsigned int *>(w + lay.rkcnt);
-    P.rkink = reinterpret_cast<RkRec *>(w + lay.rkink);
-    P.rrec = reinterpret_cast<RzRec *>(w + lay.rrec);
-    P.RNC = (int)lay.RNC;
+    RParams RP;
+    resolve_regions(RP, w + lay.resolve, (size_t)B, V, true);
+    RP.hdr = P.hdr;
+    RP.out = out_tokens;
+    RP.out_draw = out_draw;
+    P.rjob = const_cast<RJob *>(RP.rjob);
+    P.rkcnt = RP.rkcnt;
     P.guard_abs = resolve_all ? INFINITY : GUARD_ABS;
     P.guard_rel = resolve_all ? INFINITY : GUARD_REL;
     P.out_draw = out_draw;
@@ -3021,15 +2948,15 @@ int launch(const void *target, const void *draft, const int32_t *tokens, const f
     P.draft_bytes = (unsigned long long)B * k * (unsigned long long)V * es;
 
     // the exact draws: two CTAs per SM, at most one work item each to begin with
-    const size_t ritems = (size_t)B * lay.RNC;
+    const size_t ritems = (size_t)B * (size_t)RP.RNC;
     const unsigned int gridr = (unsigned int)(ritems < 3 * n_sms ? ritems : 3 * n_sms);
     const unsigned int gridrf = (unsigned int)((size_t)B < n_sms ? (size_t)B : n_sms);
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
     if (filtered)
-        return (dtype == SPEC_F32) ? launch_all<SPEC_F32, true>(P, grid1, gridf, gridr, gridrf, st, events)
-                                   : launch_all<SPEC_BF16, true>(P, grid1, gridf, gridr, gridrf, st, events);
-    return (dtype == SPEC_F32) ? launch_all<SPEC_F32, false>(P, grid1, 0, gridr, gridrf, st, events)
-                               : launch_all<SPEC_BF16, false>(P, grid1, 0, gridr, gridrf, st, events);
+        return (dtype == SPEC_F32) ? launch_all<SPEC_F32, true>(P, RP, grid1, gridf, gridr, gridrf, st, events)
+                                   : launch_all<SPEC_BF16, true>(P, RP, grid1, gridf, gridr, gridrf, st, events);
+    return (dtype == SPEC_F32) ? launch_all<SPEC_F32, false>(P, RP, grid1, 0, gridr, gridrf, st, events)
+                               : launch_all<SPEC_BF16, false>(P, RP, grid1, 0, gridr, gridrf, st, events);
 }
 
 }  // namespace

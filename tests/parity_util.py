@@ -3,14 +3,34 @@
 Integer outputs must match exactly.  The only allowed difference is a
 sequence whose first diverging decision had the oracle's uniform within
 BAND of its threshold (accept test: |u - min(1, P/Q)|) or of its draw cell's
-boundary (|u - C(x-1)/R| or |C(x)/R - u|); such sequences are counted.  Greedy
-decisions are exact comparisons and get no band.
+boundary (|u - C(x-1)/R| or |C(x)/R - u|); such sequences are counted, and
+the count must stay under MAX_EXEMPT_FRACTION (0.01 %) of the decisions
+(check_bound).  Greedy decisions are exact comparisons and get no band.
 """
 from __future__ import annotations
 
 import numpy as np
 
 BAND = 1e-5
+MAX_EXEMPT_FRACTION = 1e-4
+
+
+def check_bound(rep, accept_allowance=1):
+    """Exempt mismatches against the 0.01 % bound, per call.  Draw mismatches:
+    at most MAX_EXEMPT_FRACTION of the call's decisions, so none in a call of
+    fewer than 1e4 decisions (draws within 2e-6 of a cell edge are recomputed
+    exactly, leaving only uniforms within ~1e-12 of an edge).  Accept-test
+    mismatches: at most max(accept_allowance, the same fraction) per call; the
+    fp32 ratio p/q is good to ~1e-6, and about 2e-6 of accept decisions have a
+    uniform that close to it, so one per call is tolerated and the aggregate
+    rate is checked over >1e5 decisions in tests/test_exact_draw_gpu.py."""
+    kinds = [m[1] for m in rep["mismatched"]]
+    draws = sum(1 for k in kinds if k != "accept")
+    accepts = sum(1 for k in kinds if k == "accept")
+    cap = MAX_EXEMPT_FRACTION * rep["decisions"]
+    assert draws <= cap, f"{draws} draw mismatches in {rep['decisions']} decisions: {rep}"
+    assert accepts <= max(accept_allowance, cap), \
+        f"{accepts} accept-test mismatches in {rep['decisions']} decisions: {rep}"
 
 
 def decisions_of(n_ref, k, greedy):

@@ -69,16 +69,12 @@ def test_workspace_size(lib, B, k, V, dt, ok):
     chunks = up(jobs + 80 * B, 256)
     rec = up(chunks + B * up(ds * 4 * 8, 32) * 4, 256)
     filt = up(rec + B * nch * 8, 256)
-    # the exact draw: per sequence a list entry, a 96-byte draw record, a
-    # group count, 64 groups of 32 bytes, and a 32-byte record per 2048
-    # elements
+    # the exact draw: per sequence a 96-byte draw record, a group count, 64
+    # groups of 32 bytes, and a 32-byte record per 2048 elements
     rnc = -(-V // 2048)
-    rlist = up(filt + B * (2 * k + 1) * 16, 256)
-    rjob = up(rlist + 4 * B, 256)
-    rkcnt = up(rjob + 96 * B, 256)
-    rkink = up(rkcnt + 4 * B, 256)
-    rrec = up(rkink + 32 * 64 * B, 256)
-    assert n == rrec + B * rnc * 32
+    resolve = up(filt + B * (2 * k + 1) * 16, 256)
+    assert n == resolve + up(96 * B, 256) + up(4 * B, 256) + up(32 * 64 * B, 256) + \
+        up(32 * rnc * B, 256)
 
 
 def _call(lib, ptrs, B=1, k=1, V=8, dt=0, wsb=1 << 20):
@@ -155,8 +151,12 @@ def test_sample_workspace_size(lib, R, V, dt, ok):
         assert n == 0
         return
     es = 4 if dt == 0 else 2
+    up = lambda x: -(-x // 256) * 256
     chunks = -(-(V * es) // 4096)  # one 8-byte record per 4 KB chunk of a row
-    assert n == -(-(256 + R * chunks * 8) // 256) * 256
+    # the exact draw of every row: a 96-byte draw record, a 4-byte count and a
+    # 32-byte record per 2048 elements
+    rnc = -(-V // 2048)
+    assert n == up(256 + R * chunks * 8) + up(96 * R) + up(4 * R) + up(32 * rnc * R)
 
 
 def _scall(lib, ptrs, R=2, V=100, dt=0, wsb=1 << 20):

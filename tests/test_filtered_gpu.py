@@ -3,8 +3,12 @@ the fp64 oracle (oracle.verify_filtered).
 
 Integer outputs must equal the oracle's.  Exempt, and counted: a sequence
 whose oracle decision had its uniform within BAND of a threshold or draw-cell
-boundary (as for the unfiltered path), or whose top-p cut had a running mass
-within BAND of P times the top-k mass (fp32 masses may cut there differently).
+boundary (as for the unfiltered path, and held to the same 0.01 % bound by
+parity_util.check_bound), or whose top-p cut had a running mass within BAND
+of P times the top-k mass (the kept set is decided from masses in 2^-40 fixed
+point of ex2.approx weights, so a cut that close may keep a different last
+token; mismatches among such sequences are counted apart, at most one per
+call or 0.01 % of its decisions).
 Draft tokens are drawn from the filtered draft distribution, as a draft model
 sampling with the same parameters would.
 """
@@ -19,7 +23,7 @@ pytestmark = pytest.mark.gpu
 import oracle  # noqa: E402
 import speculative_decoding_verification_65_gb300 as sv  # noqa: E402
 from speculative_decoding_verification_65_gb300 import synth  # noqa: E402
-from tests.parity_util import compare  # noqa: E402
+from tests.parity_util import MAX_EXEMPT_FRACTION, check_bound, compare  # noqa: E402
 
 BAND = 1e-5
 NTHREADS = os.cpu_count() or 1
@@ -64,9 +68,9 @@ def check(case, tokens, top_k, top_p):
     sub = case.subset(keep)
     sub.tokens = tokens[keep]
     rep = compare(sub, gt[keep], gn[keep], rt[keep], rn[keep], tr[keep][:, :case.k + 3])
-    exempt = rep["exempt"] + int(np.sum(near & ((gn != rn) | np.any(gt != rt, axis=1))))
-    draws = max(1, int(np.sum(rn >= 0)))
-    assert exempt <= max(1, 0.02 * draws), (exempt, draws)
+    check_bound(rep)
+    cut = int(np.sum(near & ((gn != rn) | np.any(gt != rt, axis=1))))
+    assert cut <= max(1, MAX_EXEMPT_FRACTION * rep["decisions"]), (cut, rep["decisions"])
     return gn, rn
 
 

@@ -2,9 +2,12 @@
 
 Integer outputs (accept counts, tokens) must match exactly; the only
 exemption is a decision whose uniform lies within 1e-5 of the oracle's
-threshold or draw-cell boundary (tests/parity_util.py), counted, and below
-0.01% of decisions.  Intermediate probabilities P = p(g), Q = q(g) must agree
-with the oracle within 1e-5 relative.
+threshold or draw-cell boundary (tests/parity_util.py).  Exempt mismatches
+are counted and held to 0.01 % of decisions by parity_util.check_bound: no
+draw mismatch in a call under 1e4 decisions, at most one accept-test
+mismatch per call (the aggregate rate over >1e5 decisions is checked in
+tests/test_exact_draw_gpu.py).  Intermediate probabilities P = p(g),
+Q = q(g) must agree with the oracle within 1e-5 relative.
 """
 import os
 
@@ -41,12 +44,6 @@ def run_oracle(case):
                          case.temperature, nthreads=NTHR)
 
 
-# Exempt (in-band) mismatches allowed per call, as a fraction of its draws.
-# fp32 arithmetic cannot resolve inverse-CDF cells narrower than its rounding,
-# and over ~1e5-token vocabularies the CDF's tail cells are ~1e-6 wide.
-MAX_EXEMPT_PER_DRAW = 0.02
-
-
 def check(case, tag=None):
     g_t, g_n = run_gpu(case)
     r_t, r_n, tr = run_oracle(case)
@@ -58,7 +55,7 @@ def check(case, tag=None):
         os.makedirs(out, exist_ok=True)
         with open(os.path.join(out, f"parity_{tag}.json"), "w") as f:
             json.dump(rep, f)
-    assert rep["exempt"] <= max(1, MAX_EXEMPT_PER_DRAW * rep["draws"]), rep
+    pu.check_bound(rep)
     return rep, g_t, g_n
 
 

@@ -2,9 +2,10 @@
 
 Tokens must match exactly, except a sampled row whose uniform sits within
 BAND = 1e-5 of its oracle draw cell's boundary (|u - C(x-1)/R| or
-|C(x)/R - u|): there fp32 rounding of the running sums may pick the
-neighbouring token; such rows are counted and capped at 2 % of the draws.
-Greedy rows (T = 0) and error rows get no band.
+|C(x)/R - u|).  Such rows are counted and held to 0.01 % of the draws: the
+fp32 pick lists every row within 2e-6 of R of an edge for the exact draw, so
+a mismatch needs a uniform within ~1e-12 of an edge.  Greedy rows (T = 0) and
+error rows get no band.
 """
 import os
 
@@ -19,7 +20,7 @@ import speculative_decoding_verification_65_gb300 as sv  # noqa: E402
 from speculative_decoding_verification_65_gb300 import synth  # noqa: E402
 
 BAND = 1e-5
-MAX_EXEMPT = 0.02
+MAX_EXEMPT = 1e-4
 NTHREADS = os.cpu_count() or 1
 
 
@@ -42,7 +43,7 @@ def compare(sc, g):
         assert margin < BAND, f"mismatch outside the band (margin {margin:.3g}): " + why
         exempt.append(int(i))
     draws = int(np.count_nonzero((sc.temperature > 0) & (r >= 0)))
-    assert len(exempt) <= max(1, MAX_EXEMPT * draws), (len(exempt), draws)
+    assert len(exempt) <= MAX_EXEMPT * draws, (len(exempt), draws)
     return r, exempt
 
 
