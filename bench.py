@@ -1,7 +1,8 @@
 """Benchmark of batched speculative-sampling verification on GB300.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                    [--config 4] [--op verify|sample]
+                    [--config 4] [--op verify|sample|filtered|lmhead]
+                    [--per-config 5,1,2,3]
 
 A step is one verification call over one batch of the workload (all accept
 tests, first-rejection scans and correction / bonus draws of every sequence).
@@ -10,6 +11,11 @@ positions, V=151936, fp32 logits, per-sequence temperature from
 {0, 0.5, 1.0, 1.3} (2.6 GB of logits per step, far larger than the 129 MB L2,
 so no L2 flush is needed between steps).  Inputs are synthetic (seeded numpy,
 see speculative_decoding_verification_65_gb300/synth.py).
+
+The verify run also measures the other workloads in the same process and
+reports them under `per_config`: workload 5 at full size (one call per step)
+and workloads 1-3 under CUDA graph replay (they are launch-bound), each with
+its roofline, stage times, clocks and oracle baseline.
 
 Metric: verified draft positions per second (B*k / step time), summed over
 ranks.  Under torchrun every rank verifies its own batch of B sequences
@@ -157,7 +163,7 @@ class ClockSampler:
             self.out = open(self.path, "w")
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
-                 "--format=csv,noheader,nounits", "-lms", "200"],
+                 "--format=csv,noheader,nounits", "-lms", "50"],
                 stdout=self.out, stderr=subprocess.DEVNULL)
         except OSError:
             self.proc = None
@@ -280,6 +286,197 @@ def run_reference(args):
     print(json.dumps(line), flush=True)
 
 
+def nvtx_range(name):
+    """An NVTX range around the timed calls, so a profiler can select them."""
+    import contextlib
+
+    import torch
+    try:
+        rng = torch.cuda.nvtx.range(name)
+    except (AttributeError, RuntimeError):
+        rng = contextlib.nullcontext()
+    return rng
+
+
+def measure_verify(case, dev, steps: int, warmup: int, graph: bool, barrier=lambda: None,
+                   min_staged_s: float = 0.0):
+    """Times `steps` whole spec_verify calls on one batch (CUDA events on the
+    launch stream; a barrier and a device synchronise on both sides), then
+    per-stage durations over further calls with stage events (at least
+    `min_staged_s` seconds of them, so the clock sampler sees the same work).
+    Returns the measurements and the staged loop's clock record."""
+    import torch
+
+    import speculative_decoding_verification_65_gb300 as sv
+    from speculative_decoding_verification_65_gb300 import synth
+
+    B, k, V = case.B, case.k, case.V
+    d = sv.to_device(case, dev)
+    dt_code = sv.SPEC_F32 if case.dtype == synth.F32 else sv.SPEC_BF16
+    stream = torch.cuda.current_stream(dev)
+    ws = sv.workspace(B, k, V, dt_code, dev, stream)
+    out_t = torch.empty((B, k + 1), dtype=torch.int32, device=dev)
+    out_n = torch.empty((B,), dtype=torch.int32, device=dev)
+
+    def step(events=None):
+        if events is None:
+            sv.spec_verify(**d, out_tokens=out_t, out_num_accepted=out_n, ws=ws, stream=stream)
+        else:
+            sv.spec_verify_timed(**d, out_tokens=out_t, out_num_accepted=out_n, ws=ws,
+                                 stage_events=events, stream=stream)
+
+    for _ in range(max(warmup, 3)):
+        step()
+    torch.cuda.synchronize(dev)
+    if sv.spec_verify_read_status(ws) != sv.SPEC_DEV_OK:
+        raise RuntimeError("device status nonzero after warm-up")
+
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    g, per_graph = None, 1
+    if graph:
+        # a batch of whole calls captured into one CUDA graph and replayed:
+        # for launch-bound sizes this removes the host's launch cost per call
+        per_graph = min(steps, 50)
+        while steps % per_graph:
+            per_graph -= 1
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            for _ in range(per_graph):
+                sv.spec_verify(**d, out_tokens=out_t, out_num_accepted=out_n, ws=ws)
+        g.replay()
+        torch.cuda.synchronize(dev)
+    barrier()
+    torch.cuda.synchronize(dev)
+    # the timed region: K whole verification calls, as a user issues them
+    with ClockSampler(dev.index) as clk_timed, nvtx_range("spec_verify timed region"):
+        t0.record(stream)
+        if g is not None:
+            for _ in range(steps // per_graph):
+                g.replay()
+        else:
+            for _ in range(steps):
+                step()
+        t1.record(stream)
+        torch.cuda.synchronize(dev)
+    barrier()
+    total_ms = t0.elapsed_time(t1)
+    del g
+
+    # per-stage durations: further calls, each with an event before it and one
+    # after each stage (statistics, accept scan, draw tiles, final search,
+    # exact draws) on the launch stream; stage events keep the kernels plainly
+    # ordered.  Run for at least min_staged_s so that the clock sampler, which
+    # polls every 50 ms, sees the same work under load.
+    per_step_s = max(total_ms / steps / 1e3, 1e-6)
+    n_staged = max(steps, int(min_staged_s / per_step_s) + 1)
+    n_staged = min(n_staged, 20000)
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(n_staged)]
+    stages = [[torch.cuda.Event(enable_timing=True) for _ in range(sv.SPEC_STAGES)]
+              for _ in range(n_staged)]
+    for ev in [e for row in stages for e in row]:
+        ev.record(stream)  # creates the underlying CUDA events
+    torch.cuda.synchronize(dev)
+    with ClockSampler(dev.index) as clk_staged:
+        for i in range(n_staged):
+            starts[i].record(stream)
+            step(stages[i])
+        torch.cuda.synchronize(dev)
+    kern_ms = [s_.elapsed_time(e[0]) for s_, e in zip(starts, stages)]  # statistics kernel
+    stage_ms = [statistics.mean(
+        (starts[i] if j == 0 else stages[i][j - 1]).elapsed_time(stages[i][j])
+        for i in range(n_staged)) for j in range(sv.SPEC_STAGES)]
+    status = sv.spec_verify_read_status(ws)
+    n_host = out_n.cpu().numpy()  # the last call's accept counts
+    ok_rows = n_host >= 0
+    acceptance = {"mean_accepted": float(n_host[ok_rows].mean()) if ok_rows.any() else None,
+                  "error_sequences": int((~ok_rows).sum()), "sequences": int(B)}
+    staged_median = statistics.median(s_.elapsed_time(e[-1]) for s_, e in zip(starts, stages))
+    del d, ws, out_t, out_n
+    torch.cuda.empty_cache()
+    return dict(total_ms=total_ms, per_graph=per_graph, kern_ms=kern_ms, stage_ms=stage_ms,
+                n_staged=n_staged, status=status, acceptance=acceptance,
+                staged_median=staged_median, clocks_timed=clk_timed.summary(),
+                clocks_staged=clk_staged.summary())
+
+
+def stage_dict(stage_ms):
+    return {"stats": stage_ms[0], "scan": stage_ms[1], "draw": stage_ms[2],
+            "final": stage_ms[3], "exact_draws": stage_ms[4]}
+
+
+def merged_clocks(m):
+    """The timed region's clock record; where it holds no sample (a region
+    shorter than the 50 ms poll), the staged loop's (the same calls, under
+    load, right after it), said so."""
+    c = dict(m["clocks_timed"])
+    if c.get("sm_mhz") is None:
+        st = dict(m["clocks_staged"])
+        st["source"] = (f"staged-timing loop right after the timed region "
+                        f"({m['n_staged']} calls of the same work)")
+        return st
+    c["source"] = "timed region"
+    return c
+
+
+def roofline_of(kern_ms, alg_bytes, peak, peak_src, workload, read_gbs=None):
+    kern_avg_s = statistics.mean(kern_ms) / 1e3
+    achieved = alg_bytes / kern_avg_s / 1e9
+    r = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+         "frac": achieved / peak, "traffic": recorded_traffic(workload),
+         "peak_source": f"{peak_src} copy bandwidth (MEASURED_PEAKS.json hbm_gbs)"
+         if peak_src == "measured" else "fallback 6.8 TB/s",
+         "kernel": "stats_kernel (row statistics, the HBM-bound stage)",
+         "kernel_timing": "CUDA events after each stage, further steps",
+         "kernel_ms_avg": kern_avg_s * 1e3, "kernel_ms_min": min(kern_ms),
+         "frac_of_nominal_8TBs": achieved / 8000.0}
+    if read_gbs:
+        r["read_probe_gbs"] = read_gbs
+        r["frac_of_read_probe"] = achieved / read_gbs
+    return r
+
+
+def per_config_block(args, dev, peak, peak_src):
+    """Workload 5 at full size (one call per step) and workloads 1-3 under
+    CUDA graph replay (launch-bound sizes), measured in the same process as
+    the headline, each with its roofline, stage times and oracle baseline."""
+    from speculative_decoding_verification_65_gb300 import synth
+
+    out = {}
+    for cfg in args.per_config:
+        if cfg == args.config:
+            continue
+        case = make_workload(cfg, 0, None)
+        graph = cfg in (1, 2, 3)
+        steps = max(args.steps, 200) if graph else max(args.steps, 100)
+        m = measure_verify(case, dev, steps, args.warmup, graph, min_staged_s=0.3)
+        alg_bytes = synth.algorithmic_bytes(case)
+        ms = m["total_ms"] / steps
+        workload = synth.CONFIG_NAMES[cfg]
+        entry = {
+            "workload": workload, "B": case.B, "k": case.k, "V": case.V,
+            "input_dtype": case.dtype, "steps": steps, "ms_per_step": ms,
+            "value": case.B * case.k / (ms / 1e3), "unit": UNIT,
+            "launch": f"CUDA graph replay of {m['per_graph']} calls" if graph
+            else "one library call per step",
+            "algorithmic_bytes_per_step": alg_bytes,
+            "roofline": roofline_of(m["kern_ms"], alg_bytes, peak, peak_src, workload),
+            "stage_ms": stage_dict(m["stage_ms"]),
+            "ms_per_step_median_staged": m["staged_median"],
+            "clocks": merged_clocks(m), "acceptance": m["acceptance"],
+            "device_status": m["status"],
+        }
+        if not args.no_cpu_baseline:
+            cores = host_cores()
+            v, n_seq, used = time_oracle(case, min(args.cpu_budget, 4.0), cores)
+            entry["cpu_baseline"] = {"value": v, "unit": UNIT, "cores": cores, "kind": "oracle",
+                                     "sample": f"{n_seq} of {case.B} sequences of {workload}, "
+                                               f"{used:.1f} s on {cores} threads"}
+        out[f"cfg{cfg}"] = entry
+        del case
+    return out
+
+
 def run_ours(args):
     import torch
 
@@ -294,91 +491,22 @@ def run_ours(args):
     dev = torch.device("cuda", local)
     torch.cuda.set_device(dev)
 
-    case = make_workload(args.config, rank, args.batch)
-    B, k, V = case.B, case.k, case.V
-    d = sv.to_device(case, dev)
-    dt_code = sv.SPEC_F32 if case.dtype == synth.F32 else sv.SPEC_BF16
-    stream = torch.cuda.current_stream(dev)
-    ws = sv.workspace(B, k, V, dt_code, dev, stream)
-    out_t = torch.empty((B, k + 1), dtype=torch.int32, device=dev)
-    out_n = torch.empty((B,), dtype=torch.int32, device=dev)
-    alg_bytes = synth.algorithmic_bytes(case)
-
-    def step(events=None):
-        if events is None:
-            sv.spec_verify(**d, out_tokens=out_t, out_num_accepted=out_n, ws=ws, stream=stream)
-        else:
-            sv.spec_verify_timed(**d, out_tokens=out_t, out_num_accepted=out_n, ws=ws,
-                                 stage_events=events, stream=stream)
-
     def barrier():
         if world > 1:
             import torch.distributed as dist
             dist.barrier()
 
-    for _ in range(max(args.warmup, 3)):
-        step()
-    torch.cuda.synchronize(dev)
-    if sv.spec_verify_read_status(ws) != sv.SPEC_DEV_OK:
-        raise RuntimeError("device status nonzero after warm-up")
-
-    t0 = torch.cuda.Event(enable_timing=True)
-    t1 = torch.cuda.Event(enable_timing=True)
-    graph, per_graph = None, 1
-    if args.graph:
-        # capture a batch of whole calls into one CUDA graph and replay it:
-        # for launch-bound sizes this removes the host's launch cost per call
-        per_graph = min(args.steps, 50)
-        while args.steps % per_graph:
-            per_graph -= 1
-        graph = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(graph):
-            for _ in range(per_graph):
-                sv.spec_verify(**d, out_tokens=out_t, out_num_accepted=out_n, ws=ws)
-        graph.replay()
-        torch.cuda.synchronize(dev)
-    barrier()
-    torch.cuda.synchronize(dev)
-    # the timed region: K whole verification calls, as a user issues them
-    with ClockSampler(local) as clk:
-        t0.record(stream)
-        if graph is not None:
-            for _ in range(args.steps // per_graph):
-                graph.replay()
-        else:
-            for i in range(args.steps):
-                step()
-        t1.record(stream)
-        torch.cuda.synchronize(dev)
-    barrier()
-    total_ms = t0.elapsed_time(t1)
-    del graph
-
-    # per-kernel durations: K more calls, each with an event before it and one
-    # after each stage (statistics, accept scan, draw tiles, final search) on
-    # the launch stream; stage events keep the kernels plainly ordered
-    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
-    stages = [[torch.cuda.Event(enable_timing=True) for _ in range(sv.SPEC_STAGES)]
-              for _ in range(args.steps)]
-    for ev in [e for row in stages for e in row]:
-        ev.record(stream)  # creates the underlying CUDA events
-    torch.cuda.synchronize(dev)
-    for i in range(args.steps):
-        starts[i].record(stream)
-        step(stages[i])
-    torch.cuda.synchronize(dev)
-    kern_ms = [s.elapsed_time(e[0]) for s, e in zip(starts, stages)]  # statistics kernel
-    stage_ms = [statistics.mean(
-        (starts[i] if j == 0 else stages[i][j - 1]).elapsed_time(stages[i][j])
-        for i in range(args.steps)) for j in range(sv.SPEC_STAGES)]
-    total_ms = reduce_max(total_ms, world, dev)
+    case = make_workload(args.config, rank, args.batch)
+    B, k, V = case.B, case.k, case.V
+    dt_code = sv.SPEC_F32 if case.dtype == synth.F32 else sv.SPEC_BF16
+    stream = torch.cuda.current_stream(dev)
+    alg_bytes = synth.algorithmic_bytes(case)
+    m = measure_verify(case, dev, args.steps, args.warmup, args.graph, barrier,
+                       min_staged_s=0.5)
+    total_ms = reduce_max(m["total_ms"], world, dev)
     ms_per_step = total_ms / args.steps
     value = aggregate_rate(B * k, args.steps, world, total_ms / 1e3)
-    status = sv.spec_verify_read_status(ws)
-    n_host = out_n.cpu().numpy()  # the last call's accept counts
-    ok_rows = n_host >= 0
-    acceptance = {"mean_accepted": float(n_host[ok_rows].mean()) if ok_rows.any() else None,
-                  "error_sequences": int((~ok_rows).sum()), "sequences": int(B)}
+    kern_ms, stage_ms = m["kern_ms"], m["stage_ms"]
 
     # end to end through the public API on host buffers (pinned), every step
     # copies the inputs in and the results out
@@ -392,8 +520,6 @@ def run_ours(args):
         pin(case.temperature)
     h_ot = torch.empty((B, k + 1), dtype=torch.int32).pin_memory()
     h_on = torch.empty((B,), dtype=torch.int32).pin_memory()
-    del d
-    torch.cuda.empty_cache()
     arena = torch.empty(sv.spec_verify_host_arena_size(B, k, V, dt_code), dtype=torch.uint8,
                         device=dev)
     e2e_steps = max(1, min(args.steps, 20))
@@ -406,6 +532,8 @@ def run_ours(args):
     e2e_value = aggregate_rate(B * k, e2e_steps, world, e2e_s)
     h2d = sum(int(x.numel() * x.element_size()) for x in (h_t, h_d, h_g, h_ua, h_ur, h_T))
     d2h = int(h_ot.numel() * 4 + h_on.numel() * 4)
+    del arena
+    torch.cuda.empty_cache()
 
     if rank != 0:
         if world > 1:
@@ -414,11 +542,10 @@ def run_ours(args):
         return
 
     peaks, peak_src = measured_peaks()
-    kern_avg_s = statistics.mean(kern_ms) / 1e3
-    achieved = alg_bytes / kern_avg_s / 1e9
     peak = float(peaks.get("hbm_gbs", 6800.0))
     workload = synth.CONFIG_NAMES[args.config] if args.batch is None else case.name
     read_gbs = None if args.no_read_probe else read_probe_gbs(dev)
+    acceptance = m["acceptance"]
     cpu = None
     if world == 1 and not args.no_cpu_baseline:
         cores = host_cores()
@@ -431,6 +558,8 @@ def run_ours(args):
         a, n_pos = oracle_alpha(case, 16)
         acceptance["oracle_alpha"] = a
         acceptance["oracle_alpha_sample"] = f"{n_pos} drafted positions of the first 16 sampling sequences"
+    roof = roofline_of(kern_ms, alg_bytes, peak, peak_src, workload, read_gbs)
+    roof["step_GBps"] = alg_bytes / (ms_per_step / 1e3) / 1e9
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
         "steps": args.steps, "warmup": max(args.warmup, 3), "ms_per_step": ms_per_step,
@@ -441,31 +570,23 @@ def run_ours(args):
                    "algorithmic_bytes_per_step": alg_bytes,
                    "l2": "inputs larger than L2 (no flush)" if alg_bytes > (129 << 20)
                    else "inputs smaller than L2 (no flush; launch-bound size)",
-                   "launch": f"CUDA graph replay of {per_graph} calls" if args.graph
+                   "launch": f"CUDA graph replay of {m['per_graph']} calls" if args.graph
                    else "one library call per step", "parallelism": f"dp{world}"},
-        "gpu_launches": sv.SPEC_STAGES * args.steps,
-        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
-                     "frac": achieved / peak, "traffic": recorded_traffic(workload),
-                     "peak_source": f"{peak_src} copy bandwidth (MEASURED_PEAKS.json hbm_gbs)"
-                     if peak_src == "measured" else "fallback 6.8 TB/s",
-                     "kernel": "stats_kernel (row statistics, the HBM-bound stage)",
-                     "kernel_timing": "CUDA events after each stage, K further steps",
-                     "kernel_ms_avg": kern_avg_s * 1e3, "kernel_ms_min": min(kern_ms),
-                     "frac_of_nominal_8TBs": achieved / 8000.0,
-                     "read_probe_gbs": read_gbs,
-                     "frac_of_read_probe": achieved / read_gbs if read_gbs else None,
-                     "step_GBps": alg_bytes / (ms_per_step / 1e3) / 1e9},
-        "stage_ms": {"stats": stage_ms[0], "scan": stage_ms[1], "draw": stage_ms[2],
-                     "final": stage_ms[3], "exact_draws": stage_ms[4]},
-        "ms_per_step_median_staged": statistics.median(
-            s.elapsed_time(e[-1]) for s, e in zip(starts, stages)),
-        "clocks": clk.summary(),
+        "gpu_launches": (sv.SPEC_STAGES + 1) * args.steps,
+        "roofline": roof,
+        "stage_ms": stage_dict(stage_ms),
+        "stage_calls": m["n_staged"],
+        "ms_per_step_median_staged": m["staged_median"],
+        "clocks": merged_clocks(m),
+        "clocks_timed_region": m["clocks_timed"],
         "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "steps": e2e_steps},
         "cpu_baseline": cpu,
         "acceptance": acceptance,
-        "device_status": status,
+        "device_status": m["status"],
     }
+    if world == 1 and args.batch is None and args.per_config:
+        line["per_config"] = per_config_block(args, dev, peak, peak_src)
     print(json.dumps(line), flush=True)
     if world > 1:
         import torch.distributed as dist
@@ -1179,9 +1300,13 @@ def main():
     ap.add_argument("--no-read-probe", action="store_true")
     ap.add_argument("--graph", action="store_true",
                     help="time CUDA-graph replays of the verification calls")
+    ap.add_argument("--per-config", default="5,1,2,3",
+                    help="verify: other workloads measured in the same run and reported "
+                         "under per_config (comma list; empty for none)")
     args = ap.parse_args()
     if args.config is None:
         args.config = 4 if args.op == "verify" else 5
+    args.per_config = [int(x) for x in args.per_config.split(",") if x.strip()]
     if args.op == "sample":
         if args.impl == "reference":
             run_reference_sample(args)

@@ -39,6 +39,15 @@ int32_t spec_bench_read_sink_words(void);
  */
 int32_t spec_selftest_wait_timeout(void *workspace, uint64_t limit_ns, void *stream);
 
+/*
+ * The same self-test on the scratch array of spec_verify_noalloc (on the
+ * current device): the timed-out wait writes SPEC_DEV_WAIT_TIMEOUT into that
+ * scratch's status word, which spec_verify_noalloc_read_status reports.
+ * Returns SPEC_OK once launched, SPEC_EINVAL for a bad limit, SPEC_ECUDA if the
+ * scratch's address cannot be looked up.
+ */
+int32_t spec_selftest_wait_timeout_noalloc(uint64_t limit_ns, void *stream);
+
 #ifdef __cplusplus
 }
 #endif

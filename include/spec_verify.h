@@ -252,12 +252,16 @@ int32_t spec_verify_timed(const void *target_logits, const void *draft_logits,
  *
  * The first call on a device looks up the array's device address with that
  * device current (cudaGetSymbolAddress) and keeps it; make that first call
- * before any stream capture.  Every call clears the array's status word on
- * `stream` before launching.  All calls, on every stream, share the one
- * array, which keeps the last call's contents: calls that overlap on the GPU
- * race and give undefined outputs, so run them one after another (on one
+ * before any stream capture.  The address is never looked up again, so do
+ * not call this after cudaDeviceReset in the same process (the reset unloads
+ * the module that holds the array).  Every call clears the array's status
+ * word on `stream` before launching.  All calls, on every stream, share the
+ * one array, which keeps the last call's contents: calls that overlap on the
+ * GPU race and give undefined outputs, so run them one after another (on one
  * stream, or with your own ordering between streams).  Inputs, outputs,
- * return codes and device-side sequence errors are as for spec_verify.
+ * return codes and device-side sequence errors are as for spec_verify; a
+ * kernel that stopped after a bounded wait ran out is reported by
+ * spec_verify_noalloc_read_status (the outputs of that call are undefined).
  */
 int32_t spec_verify_noalloc(const void *target_logits, const void *draft_logits,
                             const int32_t *draft_tokens, const float *u_accept,
@@ -267,6 +271,16 @@ int32_t spec_verify_noalloc(const void *target_logits, const void *draft_logits,
 
 /* Size in bytes of the scratch array spec_verify_noalloc uses. */
 size_t spec_verify_noalloc_max_bytes(void);
+
+/*
+ * The device status word of spec_verify_noalloc's scratch array on the
+ * current device, copied to *status (host) after synchronising `stream`:
+ * SPEC_DEV_OK after a complete call, SPEC_DEV_WAIT_TIMEOUT if a kernel of the
+ * last call stopped after a bounded wait ran out.  The next spec_verify_noalloc
+ * call clears it.  Returns SPEC_EINVAL for a null `status`, SPEC_ECUDA if the
+ * address cannot be looked up or the copy fails.
+ */
+int32_t spec_verify_noalloc_read_status(int32_t *status, void *stream);
 
 /*
  * Copy the workspace's device status word to *status (host) and synchronise

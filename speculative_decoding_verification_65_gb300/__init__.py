@@ -100,6 +100,10 @@ def library():
         lib.spec_bench_read_sink_words.argtypes = []
         lib.spec_selftest_wait_timeout.restype = i32
         lib.spec_selftest_wait_timeout.argtypes = [vp, ctypes.c_uint64, vp]
+        lib.spec_selftest_wait_timeout_noalloc.restype = i32
+        lib.spec_selftest_wait_timeout_noalloc.argtypes = [ctypes.c_uint64, vp]
+        lib.spec_verify_noalloc_read_status.restype = i32
+        lib.spec_verify_noalloc_read_status.argtypes = [vp, vp]
         lib.spec_verify_lmhead_workspace_size.restype = sz
         lib.spec_verify_lmhead_workspace_size.argtypes = [i32] * 5
         lib.spec_verify_lmhead.restype = i32
@@ -130,6 +134,12 @@ def _dtype_code(t) -> int:
     if t.dtype == torch.bfloat16:
         return SPEC_BF16
     raise TypeError(f"logits must be float32 or bfloat16, got {t.dtype}")
+
+
+def _on(device):
+    """The library takes the device from the CUDA runtime's current device, so
+    every call is made with the tensors' device current."""
+    return _torch().cuda.device(device)
 
 
 def _stream_handle(stream, device):
@@ -185,16 +195,18 @@ def _cached_workspace(need: int, device, s):
 
 
 def spec_verify_workspace_reset(ws, stream=None):
-    _check(library().spec_verify_workspace_reset(_ptr(ws), ws.numel(),
-                                                 _stream_handle(stream, ws.device)),
-           "spec_verify_workspace_reset")
+    with _on(ws.device):
+        _check(library().spec_verify_workspace_reset(_ptr(ws), ws.numel(),
+                                                     _stream_handle(stream, ws.device)),
+               "spec_verify_workspace_reset")
 
 
 def spec_verify_read_status(ws, stream=None) -> int:
     st = ctypes.c_int32(-99)
-    _check(library().spec_verify_read_status(_ptr(ws), ctypes.byref(st),
-                                             _stream_handle(stream, ws.device)),
-           "spec_verify_read_status")
+    with _on(ws.device):
+        _check(library().spec_verify_read_status(_ptr(ws), ctypes.byref(st),
+                                                 _stream_handle(stream, ws.device)),
+               "spec_verify_read_status")
     return int(st.value)
 
 
@@ -269,10 +281,11 @@ def spec_verify(target, draft, tokens, u_accept, u_resample, temperature,
     if ws is None:
         ws = workspace(B, k, V, dt, dev, stream)
     _check_ws(ws, dev)
-    rc = library().spec_verify(_ptr(target), _ptr(draft), _ptr(tokens), _ptr(u_accept),
-                               _ptr(u_resample), _ptr(temperature), _ptr(out_tokens),
-                               _ptr(out_num_accepted), B, k, V, dt, _ptr(ws), ws.numel(),
-                               _stream_handle(stream, dev))
+    with _on(dev):
+        rc = library().spec_verify(_ptr(target), _ptr(draft), _ptr(tokens), _ptr(u_accept),
+                                   _ptr(u_resample), _ptr(temperature), _ptr(out_tokens),
+                                   _ptr(out_num_accepted), B, k, V, dt, _ptr(ws), ws.numel(),
+                                   _stream_handle(stream, dev))
     _check(rc, "spec_verify")
     return out_tokens, out_num_accepted
 
@@ -306,11 +319,12 @@ def spec_verify_filtered(target, draft, tokens, u_accept, u_resample, temperatur
     if ws is None:
         ws = workspace(B, k, V, dt, dev, stream)
     _check_ws(ws, dev)
-    rc = library().spec_verify_filtered(_ptr(target), _ptr(draft), _ptr(tokens), _ptr(u_accept),
-                                        _ptr(u_resample), _ptr(temperature), _ptr(top_k),
-                                        _ptr(top_p), _ptr(out_tokens), _ptr(out_num_accepted),
-                                        _ptr(probs), B, k, V, dt, _ptr(ws), ws.numel(),
-                                        _stream_handle(stream, dev))
+    with _on(dev):
+        rc = library().spec_verify_filtered(_ptr(target), _ptr(draft), _ptr(tokens), _ptr(u_accept),
+                                            _ptr(u_resample), _ptr(temperature), _ptr(top_k),
+                                            _ptr(top_p), _ptr(out_tokens), _ptr(out_num_accepted),
+                                            _ptr(probs), B, k, V, dt, _ptr(ws), ws.numel(),
+                                            _stream_handle(stream, dev))
     _check(rc, "spec_verify_filtered")
     if want_probs:
         return out_tokens, out_num_accepted, probs
@@ -332,10 +346,11 @@ def spec_verify_filtered_timed(target, draft, tokens, u_accept, u_resample, temp
     _check_ws(ws, dev)
     handles = (ctypes.c_void_p * SPEC_FILTERED_STAGES)(
         *[ctypes.c_void_p(e.cuda_event) for e in stage_events])
-    rc = library().spec_verify_filtered_timed(
-        _ptr(target), _ptr(draft), _ptr(tokens), _ptr(u_accept), _ptr(u_resample),
-        _ptr(temperature), _ptr(top_k), _ptr(top_p), _ptr(out_tokens), _ptr(out_num_accepted),
-        B, k, V, dt, _ptr(ws), ws.numel(), _stream_handle(stream, target.device), handles)
+    with _on(target.device):
+        rc = library().spec_verify_filtered_timed(
+            _ptr(target), _ptr(draft), _ptr(tokens), _ptr(u_accept), _ptr(u_resample),
+            _ptr(temperature), _ptr(top_k), _ptr(top_p), _ptr(out_tokens), _ptr(out_num_accepted),
+            B, k, V, dt, _ptr(ws), ws.numel(), _stream_handle(stream, target.device), handles)
     _check(rc, "spec_verify_filtered_timed")
     return out_tokens, out_num_accepted
 
@@ -352,10 +367,11 @@ def spec_verify_timed(target, draft, tokens, u_accept, u_resample, temperature,
     _dev_out("out_num_accepted", out_num_accepted, (B,), torch.int32, dev)
     _check_ws(ws, dev)
     handles = (ctypes.c_void_p * SPEC_STAGES)(*[ctypes.c_void_p(e.cuda_event) for e in stage_events])
-    rc = library().spec_verify_timed(_ptr(target), _ptr(draft), _ptr(tokens), _ptr(u_accept),
-                                     _ptr(u_resample), _ptr(temperature), _ptr(out_tokens),
-                                     _ptr(out_num_accepted), B, k, V, dt, _ptr(ws), ws.numel(),
-                                     _stream_handle(stream, target.device), handles)
+    with _on(target.device):
+        rc = library().spec_verify_timed(_ptr(target), _ptr(draft), _ptr(tokens), _ptr(u_accept),
+                                         _ptr(u_resample), _ptr(temperature), _ptr(out_tokens),
+                                         _ptr(out_num_accepted), B, k, V, dt, _ptr(ws), ws.numel(),
+                                         _stream_handle(stream, target.device), handles)
     _check(rc, "spec_verify_timed")
     return out_tokens, out_num_accepted
 
@@ -371,12 +387,39 @@ def spec_verify_noalloc(target, draft, tokens, u_accept, u_resample, temperature
     B, k, V, dt = _marshal(target, draft, tokens, u_accept, u_resample, temperature)
     _dev_out("out_tokens", out_tokens, (B, k + 1), torch.int32, target.device)
     _dev_out("out_num_accepted", out_num_accepted, (B,), torch.int32, target.device)
-    rc = library().spec_verify_noalloc(_ptr(target), _ptr(draft), _ptr(tokens), _ptr(u_accept),
-                                       _ptr(u_resample), _ptr(temperature), _ptr(out_tokens),
-                                       _ptr(out_num_accepted), B, k, V, dt,
-                                       _stream_handle(stream, target.device))
+    with _on(target.device):
+        rc = library().spec_verify_noalloc(_ptr(target), _ptr(draft), _ptr(tokens), _ptr(u_accept),
+                                           _ptr(u_resample), _ptr(temperature), _ptr(out_tokens),
+                                           _ptr(out_num_accepted), B, k, V, dt,
+                                           _stream_handle(stream, target.device))
     _check(rc, "spec_verify_noalloc")
     return out_tokens, out_num_accepted
+
+
+def spec_verify_noalloc_read_status(stream=None, device=None) -> int:
+    """The device status word of spec_verify_noalloc's scratch (SPEC_DEV_*)."""
+    torch = _torch()
+    dev = torch.device(device if device is not None else "cuda")
+    if dev.index is None:
+        dev = torch.device("cuda", torch.cuda.current_device())
+    st = ctypes.c_int32(-99)
+    with torch.cuda.device(dev):
+        _check(library().spec_verify_noalloc_read_status(ctypes.byref(st),
+                                                         _stream_handle(stream, dev)),
+               "spec_verify_noalloc_read_status")
+    return int(st.value)
+
+
+def spec_selftest_wait_timeout_noalloc(limit_ns: int, stream=None, device=None):
+    """spec_selftest_wait_timeout on spec_verify_noalloc's scratch."""
+    torch = _torch()
+    dev = torch.device(device if device is not None else "cuda")
+    if dev.index is None:
+        dev = torch.device("cuda", torch.cuda.current_device())
+    with torch.cuda.device(dev):
+        _check(library().spec_selftest_wait_timeout_noalloc(int(limit_ns),
+                                                            _stream_handle(stream, dev)),
+               "spec_selftest_wait_timeout_noalloc")
 
 
 def spec_verify_noalloc_max_bytes() -> int:
@@ -396,10 +439,11 @@ def spec_verify_probs(target, draft, tokens, u_accept, u_resample, temperature,
     if ws is None:
         ws = workspace(B, k, V, dt, dev, stream)
     _check_ws(ws, dev)
-    rc = library().spec_verify_probs(_ptr(target), _ptr(draft), _ptr(tokens), _ptr(u_accept),
-                                     _ptr(u_resample), _ptr(temperature), _ptr(out_tokens),
-                                     _ptr(out_n), _ptr(probs), B, k, V, dt, _ptr(ws),
-                                     ws.numel(), _stream_handle(stream, dev))
+    with _on(dev):
+        rc = library().spec_verify_probs(_ptr(target), _ptr(draft), _ptr(tokens), _ptr(u_accept),
+                                         _ptr(u_resample), _ptr(temperature), _ptr(out_tokens),
+                                         _ptr(out_n), _ptr(probs), B, k, V, dt, _ptr(ws),
+                                         ws.numel(), _stream_handle(stream, dev))
     _check(rc, "spec_verify_probs")
     return out_tokens, out_n, probs
 
@@ -422,11 +466,12 @@ def spec_verify_trace(target, draft, tokens, u_accept, u_resample, temperature,
     if ws is None:
         ws = workspace(B, k, V, dt, dev, stream)
     _check_ws(ws, dev)
-    rc = library().spec_verify_trace(_ptr(target), _ptr(draft), _ptr(tokens), _ptr(u_accept),
-                                     _ptr(u_resample), _ptr(temperature), _ptr(out_tokens),
-                                     _ptr(out_n), _ptr(probs), _ptr(draw),
-                                     1 if resolve_all else 0, B, k, V, dt, _ptr(ws),
-                                     ws.numel(), _stream_handle(stream, dev))
+    with _on(dev):
+        rc = library().spec_verify_trace(_ptr(target), _ptr(draft), _ptr(tokens), _ptr(u_accept),
+                                         _ptr(u_resample), _ptr(temperature), _ptr(out_tokens),
+                                         _ptr(out_n), _ptr(probs), _ptr(draw),
+                                         1 if resolve_all else 0, B, k, V, dt, _ptr(ws),
+                                         ws.numel(), _stream_handle(stream, dev))
     _check(rc, "spec_verify_trace")
     return out_tokens, out_n, draw, probs
 
@@ -454,10 +499,11 @@ def spec_verify_host(target, draft, tokens, u_accept, u_resample, temperature,
         out_tokens = torch.empty((B, k + 1), dtype=torch.int32, pin_memory=True)
     if out_num_accepted is None:
         out_num_accepted = torch.empty((B,), dtype=torch.int32, pin_memory=True)
-    rc = library().spec_verify_host(_ptr(target), _ptr(draft), _ptr(tokens), _ptr(u_accept),
-                                    _ptr(u_resample), _ptr(temperature), _ptr(out_tokens),
-                                    _ptr(out_num_accepted), B, k, V, dt, _ptr(arena),
-                                    arena.numel(), _stream_handle(stream, arena.device))
+    with _on(arena.device):
+        rc = library().spec_verify_host(_ptr(target), _ptr(draft), _ptr(tokens), _ptr(u_accept),
+                                        _ptr(u_resample), _ptr(temperature), _ptr(out_tokens),
+                                        _ptr(out_num_accepted), B, k, V, dt, _ptr(arena),
+                                        arena.numel(), _stream_handle(stream, arena.device))
     _check(rc, "spec_verify_host")
     return out_tokens, out_num_accepted
 
@@ -517,8 +563,9 @@ def spec_sample(logits, u, temperature, out=None, ws=None, stream=None):
     if ws is None:
         ws = sample_workspace(R, V, dt, dev, stream)
     _check_ws(ws, dev)
-    rc = library().spec_sample(_ptr(logits), _ptr(u), _ptr(temperature), _ptr(out), R, V, dt,
-                               _ptr(ws), ws.numel(), _stream_handle(stream, dev))
+    with _on(dev):
+        rc = library().spec_sample(_ptr(logits), _ptr(u), _ptr(temperature), _ptr(out), R, V, dt,
+                                   _ptr(ws), ws.numel(), _stream_handle(stream, dev))
     _check(rc, "spec_sample")
     return out
 
@@ -533,9 +580,10 @@ def spec_sample_timed(logits, u, temperature, out, ws, stage_events, stream=None
     _check_ws(ws, logits.device)
     handles = (ctypes.c_void_p * SPEC_SAMPLE_STAGES)(
         *[ctypes.c_void_p(e.cuda_event) for e in stage_events])
-    rc = library().spec_sample_timed(_ptr(logits), _ptr(u), _ptr(temperature), _ptr(out), R, V,
-                                     dt, _ptr(ws), ws.numel(),
-                                     _stream_handle(stream, logits.device), handles)
+    with _on(logits.device):
+        rc = library().spec_sample_timed(_ptr(logits), _ptr(u), _ptr(temperature), _ptr(out), R, V,
+                                         dt, _ptr(ws), ws.numel(),
+                                         _stream_handle(stream, logits.device), handles)
     _check(rc, "spec_sample_timed")
     return out
 
@@ -580,9 +628,10 @@ def spec_sample_host(logits, u, temperature, arena, out=None, stream=None):
             raise ValueError("out must be a host tensor")
     else:
         out = torch.empty((R,), dtype=torch.int32, pin_memory=True)
-    rc = library().spec_sample_host(_ptr(logits), _ptr(u), _ptr(temperature), _ptr(out), R, V,
-                                    dt, _ptr(arena), arena.numel(),
-                                    _stream_handle(stream, arena.device))
+    with _on(arena.device):
+        rc = library().spec_sample_host(_ptr(logits), _ptr(u), _ptr(temperature), _ptr(out), R, V,
+                                        dt, _ptr(arena), arena.numel(),
+                                        _stream_handle(stream, arena.device))
     _check(rc, "spec_sample_host")
     return out
 
@@ -591,17 +640,19 @@ def spec_bench_read(buf, sink, stream=None):
     """The benchmark's read-only probe over a CUDA tensor `buf` (16-byte
     aligned, size a multiple of 16 bytes); `sink` is an int32 CUDA tensor of
     at least spec_bench_read_sink_words() elements."""
-    rc = library().spec_bench_read(_ptr(buf), buf.numel() * buf.element_size(), _ptr(sink),
-                                   _stream_handle(stream, buf.device))
+    with _on(buf.device):
+        rc = library().spec_bench_read(_ptr(buf), buf.numel() * buf.element_size(), _ptr(sink),
+                                       _stream_handle(stream, buf.device))
     _check(rc, "spec_bench_read")
 
 
 def spec_selftest_wait_timeout(ws, limit_ns: int, stream=None):
     """Launch the bounded-wait self-test on workspace `ws` (see
     include/spec_bench.h); read its outcome with spec_verify_read_status."""
-    _check(library().spec_selftest_wait_timeout(_ptr(ws), int(limit_ns),
-                                                _stream_handle(stream, ws.device)),
-           "spec_selftest_wait_timeout")
+    with _on(ws.device):
+        _check(library().spec_selftest_wait_timeout(_ptr(ws), int(limit_ns),
+                                                    _stream_handle(stream, ws.device)),
+               "spec_selftest_wait_timeout")
 
 
 def spec_bench_read_sink_words() -> int:
@@ -693,16 +744,17 @@ def spec_verify_lmhead(hidden, lm_head, draft, tokens, u_accept, u_resample, tem
     _check_ws(ws, dev)
     probs = torch.empty((B, k, 2), dtype=torch.float32, device=dev) if want_probs else None
     h = _stream_handle(stream, dev)
-    if want_probs:
-        rc = library().spec_verify_lmhead_timed(
-            _ptr(hidden), _ptr(lm_head), _ptr(draft), _ptr(tokens), _ptr(u_accept),
-            _ptr(u_resample), _ptr(temperature), _ptr(out_tokens), _ptr(out_num_accepted),
-            _ptr(probs), B, k, V, d, ddt, _ptr(ws), ws.numel(), h, None)
-    else:
-        rc = library().spec_verify_lmhead(
-            _ptr(hidden), _ptr(lm_head), _ptr(draft), _ptr(tokens), _ptr(u_accept),
-            _ptr(u_resample), _ptr(temperature), _ptr(out_tokens), _ptr(out_num_accepted),
-            B, k, V, d, ddt, _ptr(ws), ws.numel(), h)
+    with _on(dev):
+        if want_probs:
+            rc = library().spec_verify_lmhead_timed(
+                _ptr(hidden), _ptr(lm_head), _ptr(draft), _ptr(tokens), _ptr(u_accept),
+                _ptr(u_resample), _ptr(temperature), _ptr(out_tokens), _ptr(out_num_accepted),
+                _ptr(probs), B, k, V, d, ddt, _ptr(ws), ws.numel(), h, None)
+        else:
+            rc = library().spec_verify_lmhead(
+                _ptr(hidden), _ptr(lm_head), _ptr(draft), _ptr(tokens), _ptr(u_accept),
+                _ptr(u_resample), _ptr(temperature), _ptr(out_tokens), _ptr(out_num_accepted),
+                B, k, V, d, ddt, _ptr(ws), ws.numel(), h)
     _check(rc, "spec_verify_lmhead")
     if want_probs:
         return out_tokens, out_num_accepted, probs
@@ -723,10 +775,11 @@ def spec_verify_lmhead_timed(hidden, lm_head, draft, tokens, u_accept, u_resampl
     _check_ws(ws, dev)
     handles = (ctypes.c_void_p * SPEC_LMHEAD_STAGES)(
         *[ctypes.c_void_p(e.cuda_event) for e in stage_events])
-    rc = library().spec_verify_lmhead_timed(
-        _ptr(hidden), _ptr(lm_head), _ptr(draft), _ptr(tokens), _ptr(u_accept), _ptr(u_resample),
-        _ptr(temperature), _ptr(out_tokens), _ptr(out_num_accepted), None, B, k, V, d, ddt,
-        _ptr(ws), ws.numel(), _stream_handle(stream, hidden.device), handles)
+    with _on(hidden.device):
+        rc = library().spec_verify_lmhead_timed(
+            _ptr(hidden), _ptr(lm_head), _ptr(draft), _ptr(tokens), _ptr(u_accept), _ptr(u_resample),
+            _ptr(temperature), _ptr(out_tokens), _ptr(out_num_accepted), None, B, k, V, d, ddt,
+            _ptr(ws), ws.numel(), _stream_handle(stream, hidden.device), handles)
     _check(rc, "spec_verify_lmhead_timed")
     return out_tokens, out_num_accepted
 
@@ -748,7 +801,8 @@ def spec_lmhead_logits(hidden, lm_head, out=None, stream=None):
         out = torch.empty((M, V), dtype=torch.float32, device=hidden.device)
     _dev_out("out", out, (M, V), torch.float32, hidden.device)
     status = _zeros_on(stream, hidden.device, 1, torch.int32)
-    rc = library().spec_lmhead_logits(_ptr(hidden), _ptr(lm_head), _ptr(out), M, V, d,
-                                      _ptr(status), _stream_handle(stream, hidden.device))
+    with _on(hidden.device):
+        rc = library().spec_lmhead_logits(_ptr(hidden), _ptr(lm_head), _ptr(out), M, V, d,
+                                          _ptr(status), _stream_handle(stream, hidden.device))
     _check(rc, "spec_lmhead_logits")
     return out, status

@@ -12,6 +12,7 @@
 #include "spec_bench.h"
 #include "spec_verify.h"
 #include "device_common.cuh"
+#include "internal.h"
 
 namespace {
 
@@ -91,6 +92,15 @@ int32_t spec_bench_read(const void *buf, size_t bytes, uint32_t *sink, void *str
     read_kernel<<<grid, THREADS, 0, reinterpret_cast<cudaStream_t>(stream)>>>(
         reinterpret_cast<const uint4 *>(buf), bytes / 16, sink);
     return cudaPeekAtLastError() == cudaSuccess ? SPEC_OK : SPEC_ECUDA;
+}
+
+int32_t spec_selftest_wait_timeout_noalloc(uint64_t limit_ns, void *stream)
+{
+    void *ws = nullptr;
+    const int rc = spec_internal::noalloc_scratch(&ws);
+    if (rc != SPEC_OK)
+        return rc;
+    return spec_selftest_wait_timeout(ws, limit_ns, stream);
 }
 
 int32_t spec_selftest_wait_timeout(void *workspace, uint64_t limit_ns, void *stream)

@@ -25,6 +25,10 @@ SPEC_HIDDEN int chunk_records(const void *logits, const float *temperature, int3
                               float2 *rec, void *hdr, int32_t R, int32_t V, int32_t dtype,
                               cudaStream_t stream);
 
+// The device address of spec_verify_noalloc's scratch array on the current
+// device (looked up once per device and kept).  Returns a SPEC_* status.
+SPEC_HIDDEN int noalloc_scratch(void **addr);
+
 }  // namespace spec_internal
 
 #endif

@@ -43,6 +43,7 @@
 #include "spec_verify.h"
 #include "device_common.cuh"
 #include "resolve.cuh"
+#include "internal.h"
 
 namespace {
 
@@ -2974,6 +2975,27 @@ constexpr size_t NOALLOC_SCRATCH_BYTES = (size_t)8 << 20;
 static __device__ __align__(256) uint8_t g_noalloc_scratch[NOALLOC_SCRATCH_BYTES];
 static std::atomic<void *> g_noalloc_addr[64];
 
+namespace spec_internal {
+
+// The scratch array's device address on the current device: looked up the
+// first time (cudaGetSymbolAddress, with that device current) and kept.
+int noalloc_scratch(void **addr)
+{
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64)
+        return SPEC_ECUDA;
+    void *ws = g_noalloc_addr[dev].load(std::memory_order_relaxed);
+    if (!ws) {
+        if (cudaGetSymbolAddress(&ws, g_noalloc_scratch) != cudaSuccess || !ws)
+            return SPEC_ECUDA;
+        g_noalloc_addr[dev].store(ws, std::memory_order_relaxed);
+    }
+    *addr = ws;
+    return SPEC_OK;
+}
+
+}  // namespace spec_internal
+
 // ---------------------------------------------------------------- C ABI
 
 extern "C" {
@@ -3104,15 +3126,10 @@ int32_t spec_verify_noalloc(const void *target_logits, const void *draft_logits,
         return SPEC_OK;
     if (ws_bytes(B, k, V, dtype) > NOALLOC_SCRATCH_BYTES)
         return SPEC_ENOSPACE;
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64)
-        return SPEC_ECUDA;
-    void *ws = g_noalloc_addr[dev].load(std::memory_order_relaxed);
-    if (!ws) {
-        if (cudaGetSymbolAddress(&ws, g_noalloc_scratch) != cudaSuccess || !ws)
-            return SPEC_ECUDA;
-        g_noalloc_addr[dev].store(ws, std::memory_order_relaxed);
-    }
+    void *ws = nullptr;
+    const int rc = spec_internal::noalloc_scratch(&ws);
+    if (rc != SPEC_OK)
+        return rc;
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
     // the status word is the only scratch contents a call reads before writing
     if (cudaMemsetAsync(ws, 0, sizeof(WsHeader), st) != cudaSuccess)
@@ -3123,6 +3140,17 @@ int32_t spec_verify_noalloc(const void *target_logits, const void *draft_logits,
 }
 
 size_t spec_verify_noalloc_max_bytes(void) { return NOALLOC_SCRATCH_BYTES; }
+
+int32_t spec_verify_noalloc_read_status(int32_t *status, void *stream)
+{
+    if (!status)
+        return SPEC_EINVAL;
+    void *ws = nullptr;
+    const int rc = spec_internal::noalloc_scratch(&ws);
+    if (rc != SPEC_OK)
+        return rc;
+    return spec_verify_read_status(ws, status, stream);
+}
 
 int32_t spec_verify_read_status(const void *workspace, int32_t *status, void *stream)
 {

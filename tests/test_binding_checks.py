@@ -44,6 +44,18 @@ class _FakeCuda:
     def is_contiguous(self):
         return self._contiguous
 
+    def data_ptr(self):
+        return 0x10000
+
+    def dim(self):
+        return len(self.shape)
+
+    def numel(self):
+        n = 1
+        for x in self.shape:
+            n *= int(x)
+        return n
+
 
 ARENA = _FakeCuda((1 << 20,), torch.uint8)
 
@@ -87,3 +99,41 @@ def test_output_and_workspace_checks():
                 torch.zeros(1 << 20, dtype=torch.uint8)):
         with pytest.raises(ValueError):
             sv._check_ws(bad, dev)
+
+
+def test_library_calls_run_with_the_tensors_device_current(monkeypatch):
+    """The C library takes the device from the CUDA runtime's current device
+    (its per-device caches and the noalloc scratch address are keyed by it),
+    so the binding makes every call with the tensors' device current: here a
+    call on cuda:1 tensors enters that device around the library call."""
+    seen = []
+
+    class Rec:
+        def __init__(self, dev):
+            self.dev = str(dev)
+
+        def __enter__(self):
+            seen.append(("enter", self.dev))
+
+        def __exit__(self, *exc):
+            seen.append(("exit", self.dev))
+
+    class Lib:
+        def spec_verify(self, *args):
+            seen.append(("call", None))
+            return sv.SPEC_OK
+
+    monkeypatch.setattr(sv, "_on", lambda d: Rec(d))
+    monkeypatch.setattr(sv, "library", lambda: Lib())
+    monkeypatch.setattr(sv, "_stream_handle", lambda s, d: None)
+    B, k, V, dev = 3, 2, 50, "cuda:1"
+    x = dict(target=_FakeCuda((B, k + 1, V), torch.float32, dev),
+             draft=_FakeCuda((B, k, V), torch.float32, dev),
+             tokens=_FakeCuda((B, k), torch.int32, dev),
+             u_accept=_FakeCuda((B, k), torch.float32, dev),
+             u_resample=_FakeCuda((B,), torch.float32, dev),
+             temperature=_FakeCuda((B,), torch.float32, dev))
+    sv.spec_verify(**x, out_tokens=_FakeCuda((B, k + 1), torch.int32, dev),
+                   out_num_accepted=_FakeCuda((B,), torch.int32, dev),
+                   ws=_FakeCuda((1 << 20,), torch.uint8, dev))
+    assert seen == [("enter", "cuda:1"), ("call", None), ("exit", "cuda:1")]

@@ -142,8 +142,13 @@ def test_bad_parameters_fail_the_sequence():
     assert np.all(gn[1:] == -1)
 
 
-def test_filtered_intermediates_within_tolerance():
-    case = synth.make_config(5, B=12)
+@pytest.mark.parametrize("cfg", [5, 4])
+def test_filtered_intermediates_within_tolerance(cfg):
+    """The filtered P, Q at the full vocabulary of workloads 5 (bf16) and 4
+    (fp32, temperatures 0, 0.5, 1, 1.3), on 12 sequences of each recipe."""
+    case = synth.make_config(cfg, B=12)
+    if cfg == 4:
+        case.temperature[:] = np.array([0.5, 1.0, 1.3, 0.0] * 3, np.float32)
     top_k = np.full(case.B, 40, np.int32)
     top_p = np.full(case.B, 0.9, np.float32)
     tokens = filtered_tokens(case, top_k, top_p, seed=8)
@@ -151,6 +156,9 @@ def test_filtered_intermediates_within_tolerance():
     d = synth.decode(case.target), synth.decode(case.draft)
     for b in range(case.B):
         T = float(case.temperature[b])
+        if T == 0.0:
+            assert np.all(np.isnan(probs[b]))  # greedy sequences have no P, Q
+            continue
         for i in range(case.k):
             p, _, mp = oracle.filtered_softmax(d[0][b, i].astype(np.float64), T, 40, 0.9)
             q, _, mq = oracle.filtered_softmax(d[1][b, i].astype(np.float64), T, 40, 0.9)

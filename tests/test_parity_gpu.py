@@ -204,6 +204,37 @@ def test_intermediate_probabilities(cfg):
     assert rel[big].max() < 1e-5, rel[big].max()
 
 
+@pytest.mark.parametrize("cfg", [4, 5])
+def test_intermediate_probabilities_full_size(cfg):
+    """The two largest workloads at full size, as the benchmark launches them
+    (fp32 V = 151936 with T in {0, 0.5, 1, 1.3}; bf16 V = 128256 with its three
+    classes): the GPU runs the whole batch, and the fp64 oracle checks a sample
+    of 12 sequences of every sampling temperature (workload 4) or class
+    (workload 5), every drafted position.  Greedy sequences have no P, Q."""
+    case = synth.make_config(cfg)
+    d = sv.to_device(case)
+    _, _, probs = sv.spec_verify_probs(**d)
+    torch.cuda.synchronize()
+    rng = np.random.default_rng(100 + cfg)
+    if cfg == 4:
+        groups = [np.flatnonzero(case.temperature == T) for T in (0.5, 1.0, 1.3)]
+    else:
+        groups = [np.arange(c, case.B, 3) for c in range(3)]
+    assert all(g.size for g in groups)
+    idx = np.sort(np.concatenate([rng.choice(g, size=min(12, g.size), replace=False)
+                                  for g in groups]))
+    sub = case.subset(idx)
+    ref = oracle.probs(sub.target, sub.draft, sub.tokens, sub.temperature)
+    got = probs.cpu().numpy()[idx].astype(np.float64)
+    ok = np.isfinite(ref)
+    assert ok.sum() == idx.size * case.k * 2
+    assert np.all(np.isfinite(got[ok]))
+    rel = np.abs(got[ok] - ref[ok]) / np.maximum(ref[ok], 1e-300)
+    big = ref[ok] > 1e-30  # fp32 flushes values below its normal range
+    print(f"cfg{cfg}: {idx.size} sequences, max relative error {rel[big].max():.3g}")
+    assert rel[big].max() < 1e-5, rel[big].max()
+
+
 # ---------------------------------------------------- determinism, workspace
 
 def test_deterministic_across_calls_and_workspaces():
