@@ -61,7 +61,7 @@ size_t spec_sample_workspace_size(int32_t R, int32_t V, int32_t dtype);
  *   stream       cudaStream_t as void*.
  * Four kernels run in order on `stream`: chunk records (the one read of the
  * logits), the per-row pick, and the exact draws (two kernels) of the rows
- * whose fp32 pick landed within 2e-6 of R of a cell edge: their weights in
+ * whose fp32 pick landed within 1.2e-6 of R of a cell edge: their weights in
  * float-float arithmetic and exact fixed-point sums (about 1e-12 of R), so a
  * token equals the exactly rounded draw unless u lies within ~1e-12 of an
  * edge.  With no row listed the last two only read the count.  Returns

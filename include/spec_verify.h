@@ -20,7 +20,7 @@
  *   - a draw is inverse-CDF with u_resample[b]: the smallest token x whose
  *     running mass C(x) exceeds u * R, R the total mass (the pages say
  *     "sample"; this is the plain reading).  Draws are computed in fp32; a
- *     draw whose u * R falls within a few 1e-6 of its cell's edge in fp32 is
+ *     draw whose u * R falls within ~1e-6 of its cell's edge in fp32 is
  *     computed again in float-float arithmetic with exact fixed-point sums
  *     (about 1e-12 of R), so the token equals the exactly rounded result
  *     except for uniforms within ~1e-12 of an edge;

@@ -534,9 +534,10 @@ int setup_chunks(SParams &P, unsigned int &grid1, const void *logits, const floa
 
 // The fp32 draw's guard: a draw whose u * R lies within this fraction of R
 // of the chosen cell's edges is drawn again exactly.  The fp32 record sums
-// err by under 3e-7 of R (measured against the fp64 oracle on the sampled
-// rows of the synthetic workloads).
-constexpr float SAMPLE_GUARD = 2e-6f;
+// err by under 3e-7 of R (measured against the fp64 oracle over ~2100 bonus
+// draws of the synthetic workloads, the same record search); the guard
+// leaves a factor of 4.
+constexpr float SAMPLE_GUARD = 1.2e-6f;
 
 int launch(const void *logits, const float *u, const float *temp, int32_t *out, int32_t R,
            int32_t V, int32_t dtype, void *ws, size_t ws_size, void *stream,

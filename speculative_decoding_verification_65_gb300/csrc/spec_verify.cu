@@ -2494,26 +2494,29 @@ __device__ int locate(const Params &P, const JobRec &J, int mode, const float *c
     }
     __syncwarp();
     // the row level: an inclusive prefix of the block totals, left to right,
-    // by one lane; then the first block whose prefix exceeds u * R, found by
-    // the whole warp (the same additions as a sequential walk)
+    // by one lane, carried as a float pair (each addition's rounding error is
+    // kept and added back, so the running sum is good to about one rounding
+    // whatever the number of blocks); then the first block whose prefix
+    // exceeds u * R, found by the whole warp
     if (lane == 0) {
-        float acc = 0.0f;
+        float acc = 0.0f, err = 0.0f;
+        auto add = [&](float x) {
+            const float t = __fadd_rn(acc, x);
+            const float bv = __fsub_rn(t, acc);
+            err = __fadd_rn(err, __fadd_rn(__fsub_rn(acc, __fsub_rn(t, bv)), __fsub_rn(x, bv)));
+            acc = t;
+            return __fadd_rn(acc, err);
+        };
         int blk = 0;
         for (; blk + 4 <= nblk; blk += 4) {
             const float4 t4 = *reinterpret_cast<const float4 *>(btot + blk);
-            acc = acc + t4.x;
-            btot[blk] = acc;
-            acc = acc + t4.y;
-            btot[blk + 1] = acc;
-            acc = acc + t4.z;
-            btot[blk + 2] = acc;
-            acc = acc + t4.w;
-            btot[blk + 3] = acc;
+            btot[blk] = add(t4.x);
+            btot[blk + 1] = add(t4.y);
+            btot[blk + 2] = add(t4.z);
+            btot[blk + 3] = add(t4.w);
         }
-        for (; blk < nblk; ++blk) {
-            acc = acc + btot[blk];
-            btot[blk] = acc;
-        }
+        for (; blk < nblk; ++blk)
+            btot[blk] = add(btot[blk]);
     }
     __syncwarp();
     const float R = btot[nblk - 1];
@@ -2825,13 +2828,14 @@ int launch_all(const Params &P, const RParams &RP, unsigned int grid1, unsigned 
 }
 
 // Guards of the fp32 draw, below which a draw is redone exactly.  The fp32
-// running sums carry errors below 8e-7 of R (ex2.approx, the fp32 exponent,
-// the fp32 masses and sums; measured against the fp64 oracle over ~6000
-// draws of the synthetic workloads): residual weights are probabilities
-// (R <= 1), so their guard is absolute; target-row weights are relative to
-// their total R.
-constexpr float GUARD_ABS = 2e-6f;
-constexpr float GUARD_REL = 2e-6f;
+// edges of a cell (ex2.approx weights, fp32 masses and chunk sums, the
+// compensated running sum over blocks) were measured against the fp64
+// oracle over ~5900 draws of the synthetic workloads: residual draws within
+// 1.7e-7 in probability units (their weights are probabilities, so their
+// guard is absolute), target-row draws within 3e-7 of R (relative).  The
+// guards leave a factor of 4.
+constexpr float GUARD_ABS = 7e-7f;
+constexpr float GUARD_REL = 1.2e-6f;
 
 int launch(const void *target, const void *draft, const int32_t *tokens, const float *ua,
            const float *ur, const float *temp, int32_t *out_tokens, int32_t *out_n,

@@ -18,7 +18,7 @@ MAX_EXEMPT_FRACTION = 1e-4
 def check_bound(rep, accept_allowance=1):
     """Exempt mismatches against the 0.01 % bound, per call.  Draw mismatches:
     at most MAX_EXEMPT_FRACTION of the call's decisions, so none in a call of
-    fewer than 1e4 decisions (draws within 2e-6 of a cell edge are recomputed
+    fewer than 1e4 decisions (draws within ~1e-6 of a cell edge are recomputed
     exactly, leaving only uniforms within ~1e-12 of an edge).  Accept-test
     mismatches: at most max(accept_allowance, the same fraction) per call; the
     fp32 ratio p/q is good to ~1e-6, and about 2e-6 of accept decisions have a

@@ -3,7 +3,7 @@
 Tokens must match exactly, except a sampled row whose uniform sits within
 BAND = 1e-5 of its oracle draw cell's boundary (|u - C(x-1)/R| or
 |C(x)/R - u|).  Such rows are counted and held to 0.01 % of the draws: the
-fp32 pick lists every row within 2e-6 of R of an edge for the exact draw, so
+fp32 pick lists every row within 1.2e-6 of R of an edge for the exact draw, so
 a mismatch needs a uniform within ~1e-12 of an edge.  Greedy rows (T = 0) and
 error rows get no band.
 """
