@@ -9,7 +9,9 @@ The arithmetic lives in ``spec_ref.c`` (plain C, fp64, sequential loops); this
 module only compiles it with gcc and marshals numpy arrays through ctypes.
 Every function there cites the passage of the pages it follows.
 
-Parity pins for each function are in ``tests/test_oracle_pins.py``.
+Parity pins for each function are in ``tests/test_oracle_pins.py`` (and, per
+path, ``tests/test_sample_oracle.py``, ``tests/test_filtered_oracle.py``,
+``tests/test_lmhead_oracle.py``, ``tests/test_tree_oracle.py``).
 """
 from __future__ import annotations
 
@@ -267,3 +269,46 @@ def verify_lmhead(hidden, lm_head, draft, tokens, u_accept, u_resample, temperat
         d = (d.astype(np.uint32) << 16).view(np.float32)
     return verify(t, d, tokens, u_accept, u_resample, temperature, nthreads=nthreads,
                   want_trace=want_trace)
+
+
+# ------------------------------------------------------- tree verification
+
+def verify_tree(target, draft, parent, tokens, n_nodes, u_accept, u_resample, temperature,
+                nthreads: int = 1, want_trace: bool = True):
+    """Tree verification (spec_verify_tree_ref_mt in spec_ref.c).  Logits
+    [B, N, V] float32 or uint16 (bf16 bits); parent, tokens [B, N] int32;
+    n_nodes [B]; u_accept [B, N]; u_resample, temperature [B].  Returns
+    (out_tokens [B, N], out_nodes [B, N], num_accepted [B], trace [B, N+3] or
+    None)."""
+    lib = _load()
+    if not hasattr(lib, "_tree_ready"):
+        vp, i64, i32 = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int
+        lib.spec_verify_tree_ref_mt.argtypes = [vp, vp, i32, vp, vp, vp, vp, vp, vp,
+                                                i64, i64, i64, vp, vp, vp, vp, i32]
+        lib.spec_verify_tree_ref_mt.restype = i32
+        lib._tree_ready = True
+    target, dt = _logits_and_dtype(target)
+    draft, dd = _logits_and_dtype(draft)
+    if dt != dd:
+        raise TypeError("target and draft must share a dtype")
+    B, N, V = target.shape
+    if draft.shape != (B, N, V):
+        raise ValueError(f"draft shape {draft.shape} != {(B, N, V)}")
+    par = np.ascontiguousarray(parent, dtype=np.int32).reshape(B, N)
+    tok = np.ascontiguousarray(tokens, dtype=np.int32).reshape(B, N)
+    nn = np.ascontiguousarray(n_nodes, dtype=np.int32).reshape(B)
+    ua = np.ascontiguousarray(u_accept, dtype=np.float64).reshape(B, N)
+    ur = np.ascontiguousarray(u_resample, dtype=np.float64).reshape(B)
+    tt = np.ascontiguousarray(temperature, dtype=np.float64).reshape(B)
+    out_tokens = np.empty((B, N), np.int32)
+    out_nodes = np.empty((B, N), np.int32)
+    out_n = np.empty((B,), np.int32)
+    trace = np.empty((B, N + 3), np.float64) if want_trace else None
+    rc = lib.spec_verify_tree_ref_mt(_ptr(target), _ptr(draft), dt, _ptr(par), _ptr(tok),
+                                     _ptr(nn), _ptr(ua), _ptr(ur), _ptr(tt), B, N, V,
+                                     _ptr(out_tokens), _ptr(out_nodes), _ptr(out_n),
+                                     _ptr(trace) if trace is not None else None,
+                                     int(nthreads))
+    if rc != 0:
+        raise RuntimeError(f"spec_verify_tree_ref failed with status {rc}")
+    return out_tokens, out_nodes, out_n, trace

@@ -50,6 +50,10 @@
  * row errors (token -1): T invalid as above, a NaN or +inf logit, or every
  * logit -inf.
  *
+ * Tree verification (spec_verify_tree_ref_mt): several candidate
+ * continuations per sequence; the reading of its sibling rule is stated
+ * above that function.
+ *
  * Everything is fp64 with plain sequential loops; no blocking, no fusion, no
  * reordering beyond the definition.
  */
@@ -747,6 +751,298 @@ int spec_sample_ref_mt(const void *logits, int dtype, const double *u,
         pthread_join(th[w], NULL);
     for (int w = started; w < nthreads; ++w)
         ref_sample_worker(&jobs[w]);
+    int status = REF_OK;
+    for (int w = 0; w < nthreads; ++w)
+        if (jobs[w].status != REF_OK)
+            status = jobs[w].status;
+    free(jobs);
+    free(th);
+    return status;
+}
+
+/* ------------------------------------------------------- tree verification */
+
+/*
+ * Tree verification: several candidate continuations per sequence, verified
+ * together ("Speculative Decoding and the Art of Fast LLM Inference", "Where
+ * the Draft Comes From", "EAGLE: drafting in feature space", on EAGLE-2/3;
+ * techaiinterview, "Drafts and limits", the tree-verification line).  The
+ * pages name the idea but give no rule for choosing among siblings; the
+ * thelatentsource page ("Choosing who does the drafting", on Medusa) warns
+ * that tree acceptance variants need not preserve the target distribution.
+ * The reading taken here is the one that keeps the exactness argument of the
+ * first page ("Why It Stays Exact") node by node:
+ *
+ *   - node 0 is the root (the last committed position); node n >= 1 holds
+ *     draft token tokens[n] and hangs below parent[n] < n.  Target row n is
+ *     the target's logits after the path to node n; draft row n is the
+ *     draft's logits there, from which node n's children were drawn
+ *     independently (with replacement).
+ *   - the walk starts at the root.  At node c with children x_1..x_m (in
+ *     node-index order), child i is one ordinary accept test against the
+ *     current distribution p_i of the target, with the draft q = q_c:
+ *     accept with probability min(1, p_i(x_i) / q(x_i)); p_1 = p_c and after
+ *     a rejection p_{i+1} = norm(max(0, p_i - q)) (the correction of the
+ *     first page's step "Stop at the first rejection", applied to the next
+ *     sibling instead of ending the round).  Written with running constants:
+ *     p_i = max(0, p - C_i q) / M_i, C_1 = 0, M_1 = 1,
+ *     C_{i+1} = C_i + M_i, M_{i+1} = sum_x max(0, p - C_{i+1} q).
+ *   - an accepted child becomes the current node (its token is emitted);
+ *     when every child is rejected, or c is a leaf, one token is drawn from
+ *     the current distribution p_{m+1} (for a leaf: p_c, the bonus token) and
+ *     the walk ends.  Every sibling test is one speculative-sampling step of
+ *     target p_i against draft q, whose output law is p_i, so by induction
+ *     the emitted token at each node follows p_c.
+ *   - a tree in which every node has at most one child is the chain: the
+ *     walk then equals spec_verify_ref_mt step for step.
+ *   - T == 0: at node c the child (lowest index) whose token is the target's
+ *     argmax is accepted; if none, the argmax is emitted and the walk ends.
+ *   - rows are read (and checked) only as the walk visits them: target row c
+ *     at every visited node, draft row c at a visited node with children when
+ *     T > 0.  Sequence errors: T invalid (as spec_verify_ref_mt); n_nodes
+ *     outside [1, N]; for 1 <= n < n_nodes, parent[n] outside [0, n) or
+ *     tokens[n] outside [0, V); a visited row that holds NaN or +inf or is
+ *     all -inf; q(x_i) <= 0 for a tested child.
+ *   - M_{i+1} <= 0 after a rejection (impossible in exact arithmetic, where
+ *     M_{i+1} >= M_2 (1 - q(S)) > 0 with S = {x : p(x) > q(x)}) ends the
+ *     sibling tests and the draw falls back to p_c, like the chain's
+ *     rounding fallback.
+ */
+typedef struct {
+    const void *target;       /* [B, N, V] */
+    const void *draft;        /* [B, N, V] */
+    int dtype;
+    const int32_t *parent;    /* [B, N] */
+    const int32_t *tokens;    /* [B, N] */
+    const int32_t *n_nodes;   /* [B] */
+    const double *u_accept;   /* [B, N] */
+    const double *u_resample; /* [B] */
+    const double *temperature;/* [B] */
+    int64_t N, V;
+    int32_t *out_tokens;      /* [B, N] */
+    int32_t *out_nodes;       /* [B, N] */
+    int32_t *out_num_accepted;/* [B] */
+    double *trace;            /* [B, N+3] or NULL */
+    int64_t b0, b1;
+    int status;
+} ref_tree_job_t;
+
+/* max(0, p - C q) into w; returns the total.  C == 0 copies p. */
+static double ref_tree_residual(const double *p, const double *q, double C, int64_t V,
+                                double *w)
+{
+    double M = 0.0;
+    for (int64_t x = 0; x < V; ++x) {
+        double d = (C == 0.0) ? p[x] : p[x] - C * q[x];
+        w[x] = d > 0.0 ? d : 0.0;
+        M += w[x];
+    }
+    return M;
+}
+
+/* Returns 0 on success, 1 if the sequence is an error row. */
+static int ref_tree_sequence(ref_tree_job_t *J, int64_t b, double *t, double *d, double *p,
+                             double *q, double *w)
+{
+    const int64_t N = J->N, V = J->V;
+    const double T = J->temperature[b];
+    const int32_t *par = J->parent + b * N, *tok = J->tokens + b * N;
+    int32_t *ot = J->out_tokens + b * N, *on = J->out_nodes + b * N;
+    double *tr = J->trace ? J->trace + b * (N + 3) : NULL;
+    if (tr)
+        for (int64_t i = 0; i < N + 3; ++i)
+            tr[i] = NAN;
+
+    if (isnan(T) || T < 0 || isinf(T) || (T > 0 && T < (double)FLT_MIN))
+        return 1;
+    const int64_t n = J->n_nodes[b];
+    if (n < 1 || n > N)
+        return 1;
+    for (int64_t i = 1; i < n; ++i) {
+        if (par[i] < 0 || par[i] >= i)
+            return 1;
+        if (tok[i] < 0 || tok[i] >= V)
+            return 1;
+    }
+
+    int64_t c = 0, depth = 0, token = -1;
+    for (;;) {
+        ref_load_row(J->target, J->dtype, (size_t)(b * N + c), V, t);
+        if (ref_row_invalid(t, V))
+            return 1;
+        int64_t first_child = -1;
+        for (int64_t i = c + 1; i < n; ++i)
+            if (par[i] == c) {
+                first_child = i;
+                break;
+            }
+        int64_t next = -1;
+        if (T == 0) {
+            int64_t a;
+            ref_max_argmax(t, V, &a);
+            for (int64_t i = c + 1; i < n; ++i)
+                if (par[i] == c && tok[i] == a) {
+                    next = i;
+                    break;
+                }
+            if (next < 0) {
+                token = a;
+                break;
+            }
+        } else {
+            spec_ref_softmax(t, V, T, p);
+            double C = 0.0, M = 1.0;
+            if (first_child >= 0) {
+                ref_load_row(J->draft, J->dtype, (size_t)(b * N + c), V, d);
+                if (ref_row_invalid(d, V))
+                    return 1;
+                spec_ref_softmax(d, V, T, q);
+                for (int64_t i = first_child; i < n; ++i) {
+                    if (par[i] != c)
+                        continue;
+                    const double Q = q[tok[i]];
+                    if (Q <= 0.0)
+                        return 1;
+                    double num = p[tok[i]] - C * Q;
+                    if (num < 0.0)
+                        num = 0.0;
+                    const double ratio = num / (M * Q);
+                    if (tr)
+                        tr[i] = ratio < 1.0 ? ratio : 1.0;
+                    if (ratio >= 1.0 || J->u_accept[b * N + i] < ratio) {
+                        next = i;
+                        break;
+                    }
+                    C += M;
+                    M = ref_tree_residual(p, q, C, V, w);
+                    if (!(M > 0.0)) {
+                        C = 0.0; /* rounding-only fallback: draw from p_c */
+                        break;
+                    }
+                }
+            }
+            if (next < 0) {
+                double R = ref_tree_residual(p, q, C, V, w);
+                if (!(R > 0.0))
+                    memcpy(w, p, (size_t)V * sizeof(double));
+                double cell[3];
+                token = spec_ref_inverse_cdf(w, V, J->u_resample[b], cell);
+                if (token < 0)
+                    return 1;
+                if (tr) {
+                    tr[N] = cell[0];
+                    tr[N + 1] = cell[1];
+                    tr[N + 2] = cell[2];
+                }
+                break;
+            }
+        }
+        on[depth] = (int32_t)next;
+        ot[depth] = tok[next];
+        ++depth;
+        c = next;
+    }
+    ot[depth] = (int32_t)token;
+    for (int64_t i = depth + 1; i < N; ++i)
+        ot[i] = -1;
+    for (int64_t i = depth; i < N; ++i)
+        on[i] = -1;
+    J->out_num_accepted[b] = (int32_t)depth;
+    return 0;
+}
+
+static void *ref_tree_worker(void *arg)
+{
+    ref_tree_job_t *J = (ref_tree_job_t *)arg;
+    size_t n = (size_t)J->V;
+    double *buf = (double *)malloc(5 * n * sizeof(double));
+    if (!buf) {
+        J->status = REF_ENOMEM;
+        return NULL;
+    }
+    double *t = buf, *d = buf + n, *p = buf + 2 * n, *q = buf + 3 * n, *w = buf + 4 * n;
+    for (int64_t b = J->b0; b < J->b1; ++b) {
+        if (ref_tree_sequence(J, b, t, d, p, q, w)) {
+            for (int64_t i = 0; i < J->N; ++i) {
+                J->out_tokens[b * J->N + i] = -1;
+                J->out_nodes[b * J->N + i] = -1;
+            }
+            J->out_num_accepted[b] = -1;
+        }
+    }
+    free(buf);
+    J->status = REF_OK;
+    return NULL;
+}
+
+/*
+ * Tree verification of B sequences of up to N nodes each (see above), split
+ * over `nthreads` host threads.  target and draft are [B, N, V] (fp32 or bf16
+ * bit patterns); parent, tokens [B, N] int32 (entry 0 unused); n_nodes [B];
+ * u_accept [B, N] (entry n drives node n's test); u_resample [B]; T [B].
+ * Outputs: out_tokens [B, N] (the accepted path's tokens, the drawn token,
+ * then -1), out_nodes [B, N] (the accepted path's node indices, then -1),
+ * out_num_accepted [B] (path length; -1 on a sequence error).  trace
+ * (nullable) [B, N+3]: min(1, ratio) of each tested node (NaN elsewhere),
+ * then the draw's cell [lo, hi) in u-units and its total (NaN for greedy).
+ */
+int spec_verify_tree_ref_mt(const void *target, const void *draft, int dtype,
+                            const int32_t *parent, const int32_t *tokens,
+                            const int32_t *n_nodes, const double *u_accept,
+                            const double *u_resample, const double *temperature,
+                            int64_t B, int64_t N, int64_t V,
+                            int32_t *out_tokens, int32_t *out_nodes,
+                            int32_t *out_num_accepted, double *trace, int nthreads)
+{
+    if (!target || !draft || !parent || !tokens || !n_nodes || !u_accept || !u_resample ||
+        !temperature || !out_tokens || !out_nodes || !out_num_accepted)
+        return REF_EINVAL;
+    if (B < 0 || N < 1 || V < 2 || (dtype != REF_F32 && dtype != REF_BF16))
+        return REF_EINVAL;
+    if (B == 0)
+        return REF_OK;
+    if (nthreads < 1)
+        nthreads = 1;
+    if (nthreads > B)
+        nthreads = (int)B;
+    ref_tree_job_t *jobs = (ref_tree_job_t *)calloc((size_t)nthreads, sizeof *jobs);
+    pthread_t *th = (pthread_t *)calloc((size_t)nthreads, sizeof(pthread_t));
+    if (!jobs || !th) {
+        free(jobs);
+        free(th);
+        return REF_ENOMEM;
+    }
+    for (int w = 0; w < nthreads; ++w) {
+        ref_tree_job_t *J = &jobs[w];
+        J->target = target;
+        J->draft = draft;
+        J->dtype = dtype;
+        J->parent = parent;
+        J->tokens = tokens;
+        J->n_nodes = n_nodes;
+        J->u_accept = u_accept;
+        J->u_resample = u_resample;
+        J->temperature = temperature;
+        J->N = N;
+        J->V = V;
+        J->out_tokens = out_tokens;
+        J->out_nodes = out_nodes;
+        J->out_num_accepted = out_num_accepted;
+        J->trace = trace;
+        J->b0 = B * w / nthreads;
+        J->b1 = B * (w + 1) / nthreads;
+    }
+    int started = 0;
+    if (nthreads > 1)
+        for (int w = 0; w < nthreads; ++w) {
+            if (pthread_create(&th[w], NULL, ref_tree_worker, &jobs[w]) != 0)
+                break;
+            ++started;
+        }
+    for (int w = 0; w < started; ++w)
+        pthread_join(th[w], NULL);
+    for (int w = started; w < nthreads; ++w)
+        ref_tree_worker(&jobs[w]);
     int status = REF_OK;
     for (int w = 0; w < nthreads; ++w)
         if (jobs[w].status != REF_OK)

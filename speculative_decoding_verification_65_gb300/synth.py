@@ -444,3 +444,191 @@ def make_lmhead_case(B: int, k: int, V: int, d: int, dtype: str = BF16, recipe: 
 def lmhead_flops(c: LmheadCase) -> int:
     """Multiply-add flops of the statistics GEMM (2 per product, B(k+1) rows)."""
     return 2 * c.B * (c.k + 1) * c.V * c.d
+
+
+# ------------------------------------------------------- tree verification
+
+@dataclass
+class TreeCase:
+    """One batch of tree-verification inputs (host numpy arrays).  Node 0 is
+    the root; node n >= 1 holds tokens[b, n] below parent[b, n] < n."""
+    target: np.ndarray       # [B, N, V] float32, or uint16 bf16 bit patterns
+    draft: np.ndarray        # [B, N, V] same dtype
+    parent: np.ndarray       # [B, N] int32 (entry 0: -1)
+    tokens: np.ndarray       # [B, N] int32 (entry 0: -1)
+    n_nodes: np.ndarray      # [B] int32
+    u_accept: np.ndarray     # [B, N] float32 in [0, 1)
+    u_resample: np.ndarray   # [B] float32 in [0, 1)
+    temperature: np.ndarray  # [B] float32 >= 0
+    dtype: str
+    name: str = ""
+    meta: dict = field(default_factory=dict)
+
+    @property
+    def B(self) -> int:
+        return int(self.target.shape[0])
+
+    @property
+    def N(self) -> int:
+        return int(self.target.shape[1])
+
+    @property
+    def V(self) -> int:
+        return int(self.target.shape[2])
+
+    @property
+    def elem_size(self) -> int:
+        return 4 if self.dtype == F32 else 2
+
+    def subset(self, idx) -> "TreeCase":
+        idx = np.asarray(idx)
+        c = lambda a: np.ascontiguousarray(a[idx])
+        return TreeCase(c(self.target), c(self.draft), c(self.parent), c(self.tokens),
+                        c(self.n_nodes), c(self.u_accept), c(self.u_resample),
+                        c(self.temperature), self.dtype, self.name + "[subset]",
+                        dict(self.meta))
+
+
+def tree_shape(branching) -> np.ndarray:
+    """Parent array of the full tree whose depth-l nodes each have
+    branching[l] children, nodes numbered breadth first (root 0, parent[0] =
+    -1)."""
+    parent = [-1]
+    level = [0]
+    for w in branching:
+        nxt = []
+        for c in level:
+            for _ in range(int(w)):
+                parent.append(c)
+                nxt.append(len(parent) - 1)
+        level = nxt
+    return np.asarray(parent, np.int32)
+
+
+TREE_CONFIGS = {
+    # small: the oracle finishes in well under a second
+    1: dict(B=8, V=1024, dtype=F32, branching=(2, 2, 1), recipe="gauss", sigma_d=3.0,
+            sigma_n=0.7, temps=(0.0, 1.0), ragged=True),
+    # full size: a 29-node tree (4 first-level candidates, 2 below each, two
+    # more levels of single continuations) over a 128256-token vocabulary
+    2: dict(B=512, V=128256, dtype=BF16, branching=(4, 2, 1, 1), recipe="gauss",
+            sigma_d=2.0, sigma_n=0.5, temps=(0.0, 0.7, 1.0), ragged=False),
+}
+
+TREE_CONFIG_NAMES = {
+    1: "tree_B8_N15_V1024_fp32",
+    2: "tree_B512_N29_V128256_bf16",
+}
+
+
+def _tree_children_tokens(rng, drow, m, T):
+    """m children of a node: independent Gumbel-max draws from softmax(d/T),
+    or the m largest draft logits (distinct, descending) when T == 0."""
+    if m == 0:
+        return np.empty(0, np.int32)
+    row = drow.astype(np.float64)
+    if T == 0.0:
+        order = np.lexsort((np.arange(row.size), -row))
+        return order[:m].astype(np.int32)
+    out = np.empty(m, np.int32)
+    for i in range(m):
+        e = rng.standard_exponential(row.size)
+        out[i] = int(np.argmax(row / float(T) - np.log(e)))
+    return out
+
+
+def make_tree_case(params: dict, seed: int, name: str = "",
+                   threads: int | None = None) -> TreeCase:
+    """Generate one batch of trees.  Every node's draft row follows the recipe
+    (gauss: N(0, sigma_d^2); peaks: as workload 2) and its target row is the
+    draft row plus N(0, sigma_n^2).  Children are drawn from their parent's
+    draft row (_tree_children_tokens).  With ragged=True each sequence keeps a
+    random breadth-first prefix of the tree (n_nodes in [1, N]), the rest
+    padded with parent/token -1 and zero rows."""
+    B, V, dtype = int(params["B"]), int(params["V"]), params["dtype"]
+    shape = tree_shape(params["branching"])
+    N = int(shape.size)
+    st = np.dtype(np.float32) if dtype == F32 else np.dtype(np.uint16)
+    target = np.zeros((B, N, V), st)
+    draft = np.zeros((B, N, V), st)
+    parent = np.tile(shape, (B, 1))
+    tokens = np.full((B, N), -1, np.int32)
+
+    urng = np.random.default_rng(seed + 2)
+    u_accept = urng.random((B, N), dtype=np.float32)
+    u_resample = urng.random(B, dtype=np.float32)
+    temps = np.asarray(params["temps"], np.float32)
+    temperature = temps[urng.integers(0, temps.size, size=B)]
+    if params.get("ragged"):
+        n_nodes = urng.integers(1, N + 1, size=B).astype(np.int32)
+        n_nodes[0] = N
+    else:
+        n_nodes = np.full(B, N, np.int32)
+
+    lseeds = np.random.SeedSequence(seed).spawn(B)
+    tseeds = np.random.SeedSequence(seed + 1).spawn(B)
+
+    def one(b):
+        rng = np.random.default_rng(lseeds[b])
+        trng = np.random.default_rng(tseeds[b])
+        n = int(n_nodes[b])
+        T = float(temperature[b])
+        for c in range(n):
+            if params["recipe"] == "peaks":
+                d, _ = _peaks_row(rng, V, params["sigma_d"], params["n_peaks"], params["peak"])
+            else:
+                d = _normal(rng, V, params["sigma_d"])
+            t = d + _normal(rng, V, params["sigma_n"])
+            if dtype == BF16:
+                draft[b, c] = f32_to_bf16_bits(d)
+                target[b, c] = f32_to_bf16_bits(t)
+                dd = bf16_bits_to_f32(draft[b, c])
+            else:
+                draft[b, c] = d
+                target[b, c] = t
+                dd = d
+            kids = [i for i in range(c + 1, n) if shape[i] == c]
+            tokens[b, kids] = _tree_children_tokens(trng, dd, len(kids), T)
+        parent[b, n:] = -1
+
+    nthr = threads or min(32, os.cpu_count() or 1)
+    if nthr <= 1 or B == 1:
+        for b in range(B):
+            one(b)
+    else:
+        with ThreadPoolExecutor(nthr) as ex:
+            list(ex.map(one, range(B)))
+    return TreeCase(target, draft, parent, tokens, n_nodes, u_accept, u_resample, temperature,
+                    dtype, name or params.get("name", ""), dict(params, seed=seed))
+
+
+def make_tree_config(cfg: int, B: int | None = None, V: int | None = None,
+                     seed_offset: int = 0, threads: int | None = None) -> TreeCase:
+    """Tree workload `cfg` (TREE_CONFIGS); B/V overrides keep the recipe."""
+    p = dict(TREE_CONFIGS[cfg])
+    if B is not None:
+        p["B"] = B
+    if V is not None:
+        p["V"] = V
+    name = TREE_CONFIG_NAMES[cfg] if B is None and V is None else \
+        f"tree{cfg}-recipe B{p['B']} V{p['V']}"
+    return make_tree_case(p, seed=5000 + 1000 * cfg + seed_offset, name=name, threads=threads)
+
+
+def tree_bytes(tc: TreeCase, out_nodes: np.ndarray, num_accepted: np.ndarray) -> int:
+    """Bytes a tree verification must read once, given the walk's result:
+    the target row of every visited node (the root and the accepted path)
+    and, at T > 0, the draft row of every visited node that has children."""
+    rows = 0
+    for b in range(tc.B):
+        na = int(num_accepted[b])
+        if na < 0:
+            continue
+        visited = [0] + [int(x) for x in out_nodes[b, :na]]
+        n = int(tc.n_nodes[b])
+        par = tc.parent[b, :n]
+        for c in visited:
+            rows += 1
+            if tc.temperature[b] > 0 and np.any(par[c + 1:] == c):
+                rows += 1
+    return rows * tc.V * tc.elem_size
