@@ -2,7 +2,7 @@
 
 Thin Python binding over the C ABI of ``libspecverify.so`` (declared in
 ``include/spec_verify.h``, ``include/spec_sample.h`` and
-``include/spec_lmhead.h``).  Every function here only checks and marshals
+``include/spec_lmhead.h``, ``include/spec_tree.h``).  Every function here only checks and marshals
 arguments (shapes, dtypes, device pointers, the current CUDA stream) and calls
 the function of the same name in the library; all arithmetic runs in the CUDA
 kernels.  PyTorch is used for device memory and streams only.
@@ -31,6 +31,7 @@ SPEC_STAGES = 5
 SPEC_SAMPLE_STAGES = 3
 SPEC_FILTERED_STAGES = 6
 SPEC_LMHEAD_STAGES = 5
+SPEC_TREE_MAX_NODES = 1024
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "libspecverify.so")
@@ -112,6 +113,8 @@ def library():
         lib.spec_verify_lmhead_timed.argtypes = [vp] * 10 + [i32] * 5 + [vp, sz, vp, vp]
         lib.spec_lmhead_logits.restype = i32
         lib.spec_lmhead_logits.argtypes = [vp, vp, vp, i32, i32, i32, vp, vp]
+        lib.spec_verify_tree.restype = i32
+        lib.spec_verify_tree.argtypes = [vp] * 11 + [i32] * 4 + [vp]
         _lib = lib
         return lib
 
@@ -806,3 +809,70 @@ def spec_lmhead_logits(hidden, lm_head, out=None, stream=None):
                                           _ptr(status), _stream_handle(stream, hidden.device))
     _check(rc, "spec_lmhead_logits")
     return out, status
+
+
+# ------------------------------------------------------- tree verification
+
+def spec_verify_tree(target, draft, parent, tokens, n_nodes, u_accept, u_resample, temperature,
+                     out_tokens=None, out_nodes=None, out_num_accepted=None, stream=None):
+    """Tree verification (include/spec_tree.h) on the current (or given)
+    stream.  target and draft [B, N, V]: float32 or bfloat16 CUDA tensors;
+    parent, tokens int32 [B, N]; n_nodes int32 [B]; u_accept float32 [B, N];
+    u_resample, temperature float32 [B].  Returns (out_tokens int32 [B, N],
+    out_nodes int32 [B, N], out_num_accepted int32 [B]); asynchronous like
+    any CUDA op."""
+    torch = _torch()
+    if target.dim() != 3 or tuple(draft.shape) != tuple(target.shape):
+        raise ValueError("target and draft must both be [B, N, V]")
+    B, N, V = target.shape
+    dt = _dtype_code(target)
+    if draft.dtype != target.dtype:
+        raise TypeError("target and draft must share a dtype")
+    dev = target.device
+    for name, t, shape, dtype in (("parent", parent, (B, N), torch.int32),
+                                  ("tokens", tokens, (B, N), torch.int32),
+                                  ("n_nodes", n_nodes, (B,), torch.int32),
+                                  ("u_accept", u_accept, (B, N), torch.float32),
+                                  ("u_resample", u_resample, (B,), torch.float32),
+                                  ("temperature", temperature, (B,), torch.float32)):
+        if tuple(t.shape) != shape or t.dtype != dtype:
+            raise ValueError(f"{name} must be {dtype} {shape}, got {t.dtype} {tuple(t.shape)}")
+    for t in (target, draft, parent, tokens, n_nodes, u_accept, u_resample, temperature):
+        if not t.is_cuda or not t.is_contiguous() or t.device != dev:
+            raise ValueError(f"all inputs must be contiguous CUDA tensors on {dev}")
+    if out_tokens is None:
+        out_tokens = torch.empty((B, N), dtype=torch.int32, device=dev)
+    if out_nodes is None:
+        out_nodes = torch.empty((B, N), dtype=torch.int32, device=dev)
+    if out_num_accepted is None:
+        out_num_accepted = torch.empty((B,), dtype=torch.int32, device=dev)
+    _dev_out("out_tokens", out_tokens, (B, N), torch.int32, dev)
+    _dev_out("out_nodes", out_nodes, (B, N), torch.int32, dev)
+    _dev_out("out_num_accepted", out_num_accepted, (B,), torch.int32, dev)
+    with _on(dev):
+        rc = library().spec_verify_tree(_ptr(target), _ptr(draft), _ptr(parent), _ptr(tokens),
+                                        _ptr(n_nodes), _ptr(u_accept), _ptr(u_resample),
+                                        _ptr(temperature), _ptr(out_tokens), _ptr(out_nodes),
+                                        _ptr(out_num_accepted), B, N, V, dt,
+                                        _stream_handle(stream, dev))
+    _check(rc, "spec_verify_tree")
+    return out_tokens, out_nodes, out_num_accepted
+
+
+def tree_to_device(tc, device="cuda"):
+    """Copy a synth.TreeCase's host arrays to device tensors."""
+    import numpy as np
+    torch = _torch()
+
+    def logits(a):
+        if a.dtype == np.uint16:
+            return torch.from_numpy(a.view(np.int16)).view(torch.bfloat16).to(device)
+        return torch.from_numpy(a).to(device)
+
+    return dict(target=logits(tc.target), draft=logits(tc.draft),
+                parent=torch.from_numpy(tc.parent).to(device),
+                tokens=torch.from_numpy(tc.tokens).to(device),
+                n_nodes=torch.from_numpy(tc.n_nodes).to(device),
+                u_accept=torch.from_numpy(tc.u_accept).to(device),
+                u_resample=torch.from_numpy(tc.u_resample).to(device),
+                temperature=torch.from_numpy(tc.temperature).to(device))

@@ -1,7 +1,7 @@
 """Build libspecverify.so in-tree with nvcc for sm_103a (GB300).
 
-Four translation units (verification, sampling, the LM-head-fused
-verification, the benchmark's read probe), one -gencode, no cmake: each
+Five translation units (verification, sampling, the LM-head-fused
+verification, tree verification, the benchmark's read probe), one -gencode, no cmake: each
 is compiled by its own nvcc process in parallel, then one nvcc call links the
 shared library.  The library links the CUDA runtime statically so it only
 needs the driver at run time; PyTorch's own runtime is not involved.
@@ -17,13 +17,15 @@ PKG = os.path.dirname(os.path.abspath(__file__))
 ROOT = os.path.dirname(PKG)
 CSRC = os.path.join(PKG, "csrc")
 SRCS = [os.path.join(CSRC, "spec_verify.cu"), os.path.join(CSRC, "spec_sample.cu"),
-        os.path.join(CSRC, "spec_lmhead.cu"), os.path.join(CSRC, "bench_read.cu")]
+        os.path.join(CSRC, "spec_lmhead.cu"), os.path.join(CSRC, "spec_tree.cu"),
+        os.path.join(CSRC, "bench_read.cu")]
 DEPS = [os.path.join(CSRC, "device_common.cuh"), os.path.join(CSRC, "internal.h"),
         os.path.join(CSRC, "resolve.cuh"), os.path.join(CSRC, "exp2_table.h"),
         os.path.join(ROOT, "include", "spec_lmhead.h"),
         os.path.join(ROOT, "include", "spec_verify.h"),
         os.path.join(ROOT, "include", "spec_sample.h"),
-        os.path.join(ROOT, "include", "spec_bench.h")]
+        os.path.join(ROOT, "include", "spec_bench.h"),
+        os.path.join(ROOT, "include", "spec_tree.h")]
 SRC = SRCS[0]
 LIB = os.path.join(PKG, "libspecverify.so")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]

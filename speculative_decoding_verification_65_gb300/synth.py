@@ -523,13 +523,14 @@ TREE_CONFIG_NAMES = {
 
 def _tree_children_tokens(rng, drow, m, T):
     """m children of a node: independent Gumbel-max draws from softmax(d/T),
-    or the m largest draft logits (distinct, descending) when T == 0."""
+    or the m largest draft logits (distinct, descending; repeated cyclically
+    when m exceeds the vocabulary) when T == 0."""
     if m == 0:
         return np.empty(0, np.int32)
     row = drow.astype(np.float64)
     if T == 0.0:
         order = np.lexsort((np.arange(row.size), -row))
-        return order[:m].astype(np.int32)
+        return order[np.arange(m) % row.size].astype(np.int32)
     out = np.empty(m, np.int32)
     for i in range(m):
         e = rng.standard_exponential(row.size)

@@ -98,3 +98,75 @@ def check_invariants(case, g_tokens, g_n):
         assert 0 <= g_tokens[b, n] < V, b
         assert np.all(g_tokens[b, n + 1:] == -1), b
     assert np.all(g_tokens[~ok] == -1)
+
+
+def compare_tree(tc, g_tokens, g_nodes, g_n, r_tokens, r_nodes, r_n, trace, band=BAND):
+    """Tree-verification outputs against the oracle's.  Decisions per
+    sequence: the sibling tests the oracle traced plus its one draw (greedy:
+    one argmax comparison per visited node).  A mismatch is allowed only at
+    a sampled sequence's first differing decision with the oracle's uniform
+    within `band` of it: the sibling test one side accepted and the other
+    rejected (|u - threshold|), or the draw (distance to the cell's edges).
+    Returns the report of compare()."""
+    g_tokens, g_nodes, g_n = map(np.asarray, (g_tokens, g_nodes, g_n))
+    N = tc.N
+    report = dict(sequences=tc.B, decisions=0, exempt=0, mismatched=[])
+    for b in range(tc.B):
+        greedy = tc.temperature[b] == 0
+        rn = int(r_n[b])
+        if rn < 0:
+            report["decisions"] += 1
+        elif greedy:
+            report["decisions"] += rn + 1
+        else:
+            report["decisions"] += int(np.count_nonzero(~np.isnan(trace[b, 1:N]))) + 1
+        same = (g_n[b] == r_n[b] and np.array_equal(g_tokens[b], r_tokens[b])
+                and np.array_equal(g_nodes[b], r_nodes[b]))
+        if same:
+            continue
+        why = (f"b={b} T={tc.temperature[b]} gpu n={g_n[b]} nodes {g_nodes[b][:max(0, g_n[b])].tolist()} "
+               f"tokens {g_tokens[b][:max(0, g_n[b]) + 1].tolist()} oracle n={rn} "
+               f"nodes {r_nodes[b][:max(0, rn)].tolist()} tokens {r_tokens[b][:max(0, rn) + 1].tolist()}")
+        if greedy or g_n[b] < 0 or rn < 0:
+            raise AssertionError("mismatch without exemption: " + why)
+        gn = int(g_n[b])
+        i = 0
+        while i < min(gn, rn) and g_nodes[b, i] == r_nodes[b, i]:
+            i += 1
+        if i == gn == rn:
+            lo, hi = trace[b, N], trace[b, N + 1]
+            u = float(tc.u_resample[b])
+            margin = min(u - lo, hi - u)
+            kind = "draw"
+        else:
+            g = int(g_nodes[b, i]) if i < gn else 1 << 30
+            o = int(r_nodes[b, i]) if i < rn else 1 << 30
+            x = min(g, o)
+            assert x < N and not np.isnan(trace[b, x]), "first differing test not traced: " + why
+            margin = abs(float(tc.u_accept[b, x]) - trace[b, x])
+            kind = "accept"
+        if not margin < band:
+            raise AssertionError(f"mismatch outside the {band} band (margin {margin:.3g}): " + why)
+        report["exempt"] += 1
+        report["mismatched"].append((b, kind, float(margin)))
+    return report
+
+
+def check_tree_invariants(tc, g_tokens, g_nodes, g_n):
+    """Properties of any correct tree output: the path descends from the
+    root through children, its tokens are the nodes' tokens, one emitted
+    token in range, -1 padding after it."""
+    g_tokens, g_nodes, g_n = map(np.asarray, (g_tokens, g_nodes, g_n))
+    for b in range(tc.B):
+        n = int(g_n[b])
+        if n < 0:
+            assert np.all(g_tokens[b] == -1) and np.all(g_nodes[b] == -1), b
+            continue
+        prev = 0
+        for i in range(n):
+            x = int(g_nodes[b, i])
+            assert 0 < x < tc.n_nodes[b] and tc.parent[b, x] == prev, (b, i)
+            assert g_tokens[b, i] == tc.tokens[b, x], (b, i)
+            prev = x
+        assert 0 <= g_tokens[b, n] < tc.V, b
+        assert np.all(g_tokens[b, n + 1:] == -1) and np.all(g_nodes[b, n:] == -1), b

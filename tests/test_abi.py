@@ -268,3 +268,32 @@ def test_lmhead_bad_sizes_and_small_workspace(lib):
     assert lib.spec_lmhead_logits(vp(LGOOD[0]), vp(LGOOD[1]), vp(LGOOD[2]), 1 << 26, 1 << 20, 64,
                                   vp(LGOOD[3]), None) == sv.SPEC_EINVAL
 
+
+
+def test_tree_host_checks(lib):
+    """spec_verify_tree rejects bad sizes, null pointers and misaligned
+    arrays before any CUDA call; B = 0 is a no-op."""
+    buf = (ctypes.c_uint8 * 4096)()
+    base = ctypes.addressof(buf)
+    a16 = (base + 15) // 16 * 16
+    good = [a16] * 11
+
+    def call(ptrs, B=1, N=4, V=16, dt=0):
+        return lib.spec_verify_tree(*[ctypes.c_void_p(p) if p else None for p in ptrs],
+                                    B, N, V, dt, None)
+    assert call([0] * 11, B=0) == 0
+    for B, N, V, dt in ((-1, 4, 16, 0), (1, 0, 16, 0), (1, 1025, 16, 0), (1, 4, 1, 0),
+                        (1, 4, (1 << 20) + 1, 0), (1, 4, 16, 2)):
+        assert call(good, B, N, V, dt) == 1, (B, N, V, dt)
+    for i in range(11):
+        ptrs = list(good)
+        ptrs[i] = 0
+        assert call(ptrs) == 1, i
+    for i in range(2):  # logits must be 16-byte aligned
+        ptrs = list(good)
+        ptrs[i] = a16 + 4
+        assert call(ptrs) == 1, i
+    for i in range(2, 11):  # the rest 4-byte aligned
+        ptrs = list(good)
+        ptrs[i] = a16 + 2
+        assert call(ptrs) == 1, i
