@@ -1,7 +1,7 @@
 """Benchmark of batched speculative-sampling verification on GB300.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                    [--config 4] [--op verify|sample|filtered|lmhead]
+                    [--config 4] [--op verify|sample|filtered|lmhead|tree]
                     [--per-config 5,1,2,3]
 
 A step is one verification call over one batch of the workload (all accept
@@ -31,6 +31,13 @@ softmax(logits / T), the draft model's step before verification): a step is
 one spec_sample call over the draft rows of a workload (default workload 5:
 4096 rows of V=128256 bf16, 1.05 GB), metric sampled tokens per second.
 
+`--op tree` benchmarks tree verification (several candidate continuations
+per sequence): a step is one spec_verify_tree call over 512 trees of 29
+nodes (4 first-level candidates, 2 below each, then two single
+continuations) over V=128256 bf16, T from {0, 0.7, 1}; metric verified tree
+candidates per second (B*(N-1) / step time).  Its roofline counts the bytes
+the walk must read once: the rows of the nodes it visits.
+
 Prints one JSON line on rank 0.
 """
 from __future__ import annotations
@@ -59,6 +66,7 @@ KERNEL_SRCS = {
     "chunk_kernel": [os.path.join(CSRC, "spec_sample.cu"), os.path.join(CSRC, "device_common.cuh")],
     "wfilter_kernel": [os.path.join(CSRC, "spec_verify.cu"), os.path.join(CSRC, "device_common.cuh")],
     "gemm_kernel": [os.path.join(CSRC, "spec_lmhead.cu"), os.path.join(CSRC, "device_common.cuh")],
+    "tree_kernel": [os.path.join(CSRC, "spec_tree.cu"), os.path.join(CSRC, "device_common.cuh")],
 }
 SAMPLE_METRIC = "sampled tokens/sec"
 SAMPLE_UNIT = "tokens/s"
@@ -1282,6 +1290,216 @@ def run_reference_lmhead(args):
     print(json.dumps(line), flush=True)
 
 
+# ------------------------------------------------------- tree verification
+
+TREE_METRIC = "verified tree candidates/sec"
+TREE_UNIT = "candidates/s"
+
+
+def make_tree_workload(cfg: int, rank: int, batch=None):
+    from speculative_decoding_verification_65_gb300 import synth
+    return synth.make_tree_config(cfg, B=batch, seed_offset=100 * rank)
+
+
+def tree_workload_name(args, tc):
+    return tc.name if args.batch is None else \
+        f"{tc.name} (B={args.batch} of tree workload {args.tree_config})"
+
+
+def time_oracle_tree(tc, budget_s: float, threads: int):
+    """Oracle throughput (candidates/s) on a bounded sample: blocks of
+    sequences until the time budget is spent or every sequence is done."""
+    import oracle
+    done, t_used = 0, 0.0
+    block = max(2 * threads, 32)
+    while done < tc.B and t_used < budget_s:
+        sub = tc.subset(np.arange(done, min(tc.B, done + block)))
+        t0 = time.perf_counter()
+        oracle.verify_tree(sub.target, sub.draft, sub.parent, sub.tokens, sub.n_nodes,
+                           sub.u_accept, sub.u_resample, sub.temperature, nthreads=threads,
+                           want_trace=False)
+        t_used += time.perf_counter() - t0
+        done += sub.B
+    return done * (tc.N - 1) / t_used, done, t_used
+
+
+def run_reference_tree(args):
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return
+    import oracle
+    oracle.build()
+    tc = make_tree_workload(args.tree_config, 0, args.batch)
+    cores = host_cores()
+    per_step = min(tc.B, max(2 * cores, 32))
+    sub = tc.subset(np.arange(per_step))
+    run = lambda: oracle.verify_tree(sub.target, sub.draft, sub.parent, sub.tokens, sub.n_nodes,
+                                     sub.u_accept, sub.u_resample, sub.temperature,
+                                     nthreads=cores, want_trace=False)
+    for _ in range(args.warmup):
+        run()
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        run()
+    dt = time.perf_counter() - t0
+    value = per_step * (tc.N - 1) * args.steps / dt
+    line = {
+        "impl": "reference", "metric": TREE_METRIC, "value": value, "unit": TREE_UNIT,
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": dt / args.steps * 1e3, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": tree_workload_name(args, tc), "B": per_step, "N": tc.N,
+                   "V": tc.V, "input_dtype": tc.dtype,
+                   "what": "fp64 CPU oracle (plain C, threads over sequences)"},
+        "cpu_baseline": {"value": value, "unit": TREE_UNIT, "cores": cores, "kind": "oracle",
+                         "sample": f"first {per_step} of {tc.B} trees per step"},
+        "e2e": {"value": value, "unit": TREE_UNIT, "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def run_ours_tree(args):
+    import torch
+
+    import speculative_decoding_verification_65_gb300 as sv
+    from speculative_decoding_verification_65_gb300 import synth
+
+    rank, world, local = dist_env()
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+
+    def barrier():
+        if world > 1:
+            import torch.distributed as dist
+            dist.barrier()
+
+    tc = make_tree_workload(args.tree_config, rank, args.batch)
+    B, N, V = tc.B, tc.N, tc.V
+    d = sv.tree_to_device(tc, dev)
+    stream = torch.cuda.current_stream(dev)
+    ot = torch.empty((B, N), dtype=torch.int32, device=dev)
+    on = torch.empty((B, N), dtype=torch.int32, device=dev)
+    na = torch.empty((B,), dtype=torch.int32, device=dev)
+
+    def step():
+        sv.spec_verify_tree(**d, out_tokens=ot, out_nodes=on, out_num_accepted=na, stream=stream)
+
+    for _ in range(max(args.warmup, 3)):
+        step()
+    torch.cuda.synchronize(dev)
+    nodes_h, n_h = on.cpu().numpy(), na.cpu().numpy()
+    alg_bytes = synth.tree_bytes(tc, nodes_h, n_h)
+    emitted = int(np.sum(n_h[n_h >= 0] + 1))
+
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    barrier()
+    torch.cuda.synchronize(dev)
+    with ClockSampler(local) as clk, nvtx_range("spec_verify_tree timed region"):
+        t0.record(stream)
+        for _ in range(args.steps):
+            step()
+        t1.record(stream)
+        torch.cuda.synchronize(dev)
+    barrier()
+    total_ms = reduce_max(t0.elapsed_time(t1), world, dev)
+    ms_per_step = total_ms / args.steps
+    value = aggregate_rate(B * (N - 1), args.steps, world, total_ms / 1e3)
+
+    # one event pair around each call: the kernel's own duration
+    pairs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+             for _ in range(args.steps)]
+    for a, b in pairs:
+        a.record(stream)
+        step()
+        b.record(stream)
+    torch.cuda.synchronize(dev)
+    kern_ms = [a.elapsed_time(b) for a, b in pairs]
+
+    # end to end: pinned host inputs copied in, outputs copied back, every step
+    def pinned(a):
+        if a.dtype == np.uint16:
+            return torch.from_numpy(a.view(np.int16)).pin_memory().view(torch.bfloat16)
+        return torch.from_numpy(np.ascontiguousarray(a)).pin_memory()
+    host = dict(target=pinned(tc.target), draft=pinned(tc.draft), parent=pinned(tc.parent),
+                tokens=pinned(tc.tokens), n_nodes=pinned(tc.n_nodes),
+                u_accept=pinned(tc.u_accept), u_resample=pinned(tc.u_resample),
+                temperature=pinned(tc.temperature))
+    h_out = [torch.empty_like(x, device="cpu").pin_memory() for x in (ot, on, na)]
+
+    def e2e_step():
+        for k_, v in host.items():
+            d[k_].copy_(v, non_blocking=True)
+        step()
+        for h, g in zip(h_out, (ot, on, na)):
+            h.copy_(g, non_blocking=True)
+        torch.cuda.synchronize(dev)
+    e2e_step()
+    e2e_steps = max(1, min(args.steps, 5))
+    barrier()
+    e0 = time.perf_counter()
+    for _ in range(e2e_steps):
+        e2e_step()
+    e2e_s = reduce_max(time.perf_counter() - e0, world, dev)
+    e2e_value = aggregate_rate(B * (N - 1), e2e_steps, world, e2e_s)
+    h2d = sum(int(x.numel() * x.element_size()) for x in host.values())
+    d2h = sum(int(x.numel() * x.element_size()) for x in h_out)
+
+    if rank != 0:
+        if world > 1:
+            import torch.distributed as dist
+            dist.destroy_process_group()
+        return
+    peaks, peak_src = measured_peaks()
+    kern_avg_s = statistics.mean(kern_ms) / 1e3
+    achieved = alg_bytes / kern_avg_s / 1e9
+    peak = float(peaks.get("hbm_gbs", 6800.0))
+    workload = tree_workload_name(args, tc)
+    cpu = None
+    if world == 1 and not args.no_cpu_baseline:
+        cores = host_cores()
+        v, n_seq, used = time_oracle_tree(tc, args.cpu_budget, cores)
+        cpu = {"value": v, "unit": TREE_UNIT, "cores": cores, "kind": "oracle",
+               "sample": f"{n_seq} of {B} trees of {workload}, {used:.1f} s on {cores} threads"}
+    line = {
+        "metric": TREE_METRIC, "value": value, "unit": TREE_UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": max(args.warmup, 3), "ms_per_step": ms_per_step,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "f32", "data": "synthetic",
+        "config": {"workload": workload, "B_per_gpu": B, "N": N, "V": V,
+                   "input_dtype": tc.dtype, "branching": list(tc.meta.get("branching", [])),
+                   "algorithmic_bytes_per_step": alg_bytes,
+                   "emitted_tokens_per_step": emitted,
+                   "l2": "rows read per step far larger than L2 (no flush)",
+                   "parallelism": f"dp{world}"},
+        "emitted_tokens_per_s": emitted * args.steps * world / (total_ms / 1e3),
+        "mean_accepted": float(np.mean(n_h[n_h >= 0])),
+        "gpu_launches": args.steps,
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                     "frac": achieved / peak,
+                     "traffic": recorded_traffic(workload, "tree_kernel"),
+                     "peak_source": f"{peak_src} copy bandwidth (MEASURED_PEAKS.json hbm_gbs)"
+                     if peak_src == "measured" else "fallback 6.8 TB/s",
+                     "kernel": "tree_kernel (the whole step)",
+                     "kernel_timing": "CUDA events around each call, K further steps",
+                     "kernel_ms_avg": kern_avg_s * 1e3, "kernel_ms_min": min(kern_ms),
+                     "frac_of_nominal_8TBs": achieved / 8000.0},
+        "clocks": clk.summary(),
+        "e2e": {"value": e2e_value, "unit": TREE_UNIT, "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h, "steps": e2e_steps},
+        "cpu_baseline": cpu,
+    }
+    print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -1290,7 +1508,10 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--config", type=int, default=None, choices=[1, 2, 3, 4, 5],
                     help="workload (default 4 for verify, 5 for sample)")
-    ap.add_argument("--op", choices=["verify", "sample", "filtered", "lmhead"], default="verify")
+    ap.add_argument("--op", choices=["verify", "sample", "filtered", "lmhead", "tree"],
+                    default="verify")
+    ap.add_argument("--tree-config", type=int, default=2, choices=[1, 2],
+                    help="tree workload of --op tree")
     ap.add_argument("--top-k", type=int, default=50, help="top-k of --op filtered (0: none)")
     ap.add_argument("--top-p", type=float, default=0.9, help="top-p of --op filtered (1: none)")
     ap.add_argument("--batch", type=int, default=None,
@@ -1322,6 +1543,11 @@ def main():
             run_reference_lmhead(args)
         else:
             run_ours_lmhead(args)
+    elif args.op == "tree":
+        if args.impl == "reference":
+            run_reference_tree(args)
+        else:
+            run_ours_tree(args)
     elif args.impl == "reference":
         run_reference(args)
     else:

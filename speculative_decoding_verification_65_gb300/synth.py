@@ -516,7 +516,7 @@ TREE_CONFIGS = {
 }
 
 TREE_CONFIG_NAMES = {
-    1: "tree_B8_N15_V1024_fp32",
+    1: "tree_B8_N11_V1024_fp32",
     2: "tree_B512_N29_V128256_bf16",
 }
 

@@ -1,8 +1,8 @@
 """The benchmark's reference-arm JSON line, on the CPU.
 
 `bench.py --impl reference` times the fp64 oracle on the host cores and
-prints one JSON line.  For the verify, filtered and sample ops on their
-smallest workload, the line must carry every key of the benchmark's
+prints one JSON line.  For the verify, filtered, sample and tree ops on
+their smallest workload, the line must carry every key of the benchmark's
 contract: the metric and its unit, the steps and warm-up it ran, a
 `cpu_baseline` that describes the same run, and an `e2e` object with no host
 copies.  (The LM-head arm draws a 1 GB weight matrix and is left to the
@@ -26,13 +26,14 @@ KEYS = {"impl", "metric", "value", "unit", "n_gpus", "steps", "warmup", "ms_per_
 
 
 @pytest.mark.parametrize("op,metric", [("verify", bench.METRIC), ("filtered", bench.METRIC),
-                                       ("sample", bench.SAMPLE_METRIC)])
+                                       ("sample", bench.SAMPLE_METRIC),
+                                       ("tree", bench.TREE_METRIC)])
 def test_reference_line(op, metric, monkeypatch):
     for var in ("RANK", "WORLD_SIZE", "LOCAL_RANK"):
         monkeypatch.delenv(var, raising=False)
     monkeypatch.setattr(sys, "argv", ["bench.py", "--impl", "reference", "--op", op,
-                                      "--config", "1", "--steps", "2", "--warmup", "3",
-                                      "--cpu-budget", "5"])
+                                      "--config", "1", "--tree-config", "1", "--steps", "2",
+                                      "--warmup", "3", "--cpu-budget", "5"])
     buf = io.StringIO()
     with redirect_stdout(buf):
         bench.main()
