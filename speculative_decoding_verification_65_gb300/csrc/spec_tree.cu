@@ -14,11 +14,14 @@
 // A pass splits the row into 16 contiguous segments of 16-byte vectors, one
 // per warp (lane l takes vectors l, l+32, ... of its warp's segment), so the
 // per-warp totals of a residual pass are the row's running mass at segment
-// granularity.  The draw takes u * R against those totals in segment order,
-// and the one warp whose segment crosses reads it again in index order (a
+// granularity.  For a draw from p_c itself (a leaf's bonus token) the
+// statistics pass's per-warp partials already are those totals, and no
+// residual pass runs.  The draw takes u * R against the segment totals in
+// order, splits the crossing segment into 16 sub-ranges that the 16 warps
+// sum at once, and one warp reads the crossing sub-range in index order (a
 // Kogge-Stone scan over the 32 lanes of each step, elements left to right
-// inside a lane).  A threshold that rounding leaves past the segment's own
-// running total takes the segment's last positive weight, the clamp the
+// inside a lane).  A threshold that rounding leaves past a range's own
+// running total takes the range's last positive weight, the clamp the
 // method's draw already has for the whole row.
 //
 // Rows start anywhere: vector a of a row covers the 16-byte-aligned elements
@@ -40,7 +43,7 @@ namespace {
 using namespace spec_dev;
 
 constexpr int TW = 16;         // warps per CTA
-constexpr int TTH = TW * 32;   // threads per CTA (one CTA per sequence)
+constexpr int TTH = TW * 32;   // threads per CTA (one CTA per sequence, 2 per SM)
 constexpr int MAXN = SPEC_TREE_MAX_NODES;
 
 struct TParams {
@@ -59,7 +62,8 @@ struct TSmem {
     int path[MAXN];
     float red_m[TW], red_s[TW], red_s2[TW], red_m2[TW];
     int red_i[TW];
-    float wtot[TW];   // per-segment residual mass of the last pass
+    float wtot[TW];   // per-segment mass of the current draw weights
+    float wsub[TW];   // per-warp sub-range masses inside the crossing segment
     int nk, next, pick;
 };
 
@@ -151,15 +155,14 @@ __device__ bool row_stats(const TParams &P, size_t off, float c, TSmem &S, int w
     const uint4 ninf = neg_inf_vec(Lg<DT>::NEG_INF_WORD);
     float m0 = -INFINITY, s0 = 0.0f, m1 = -INFINITY, s1 = 0.0f;
     bool bad = false;
+    // two vectors of each row per step (software prefetch of the next step
+    // measured slower: the registers it takes cost resident warps)
+    auto ld = [&](const void *arr, int a) {
+        return a < sp.s1 ? tvec<DT>(arr, off, P.V, sp.A0, a) : ninf;
+    };
     for (int a = sp.s0 + lane; a < sp.s1; a += 64) {
-        const bool two = a + 32 < sp.s1;
-        const uint4 t0 = tvec<DT>(P.target, off, P.V, sp.A0, a);
-        const uint4 t1 = two ? tvec<DT>(P.target, off, P.V, sp.A0, a + 32) : ninf;
-        uint4 d0 = ninf, d1 = ninf;
-        if (TWO) {
-            d0 = tvec<DT>(P.draft, off, P.V, sp.A0, a);
-            d1 = two ? tvec<DT>(P.draft, off, P.V, sp.A0, a + 32) : ninf;
-        }
+        const uint4 t0 = ld(P.target, a), t1 = ld(P.target, a + 32);
+        const uint4 d0 = TWO ? ld(P.draft, a) : ninf, d1 = TWO ? ld(P.draft, a + 32) : ninf;
         online2<DT>(t0, t1, c, c2, m0, s0, bad);
         if (TWO)
             online2<DT>(d0, d1, c, c2, m1, s1, bad);
@@ -261,15 +264,12 @@ __device__ float residual_pass(const TParams &P, size_t off, const Wt &w, TSmem 
     const uint4 ninf = neg_inf_vec(L::NEG_INF_WORD);
     const bool with_d = w.C > 0.0f;
     float acc = 0.0f;
+    auto ld = [&](const void *arr, int a) {
+        return a < sp.s1 ? tvec<DT>(arr, off, P.V, sp.A0, a) : ninf;
+    };
     for (int a = sp.s0 + lane; a < sp.s1; a += 64) {
-        const bool two = a + 32 < sp.s1;
-        const uint4 t0 = tvec<DT>(P.target, off, P.V, sp.A0, a);
-        const uint4 t1 = two ? tvec<DT>(P.target, off, P.V, sp.A0, a + 32) : ninf;
-        uint4 d0 = ninf, d1 = ninf;
-        if (with_d) {
-            d0 = tvec<DT>(P.draft, off, P.V, sp.A0, a);
-            d1 = two ? tvec<DT>(P.draft, off, P.V, sp.A0, a + 32) : ninf;
-        }
+        const uint4 t0 = ld(P.target, a), t1 = ld(P.target, a + 32);
+        const uint4 d0 = with_d ? ld(P.draft, a) : ninf, d1 = with_d ? ld(P.draft, a + 32) : ninf;
         float x0[L::VEC], x1[L::VEC];
         weights<DT>(t0, d0, w, x0);
         weights<DT>(t1, d1, w, x1);
@@ -292,42 +292,89 @@ __device__ float residual_pass(const TParams &P, size_t off, const Wt &w, TSmem 
     return R;
 }
 
-// The draw from the last residual pass's weights with uniform u: returns the
-// row element (every thread).
+// The range a mass threshold tau falls in, given the ranges' totals in
+// order: the first whose running total exceeds tau, else (rounding left tau
+// past the end) the last with a positive total; rem = tau minus the mass of
+// the ranges before it.  Every thread computes the same.
+__device__ __forceinline__ int pick_range(const float *tot, float tau, float &rem)
+{
+    int sel = -1, last = 0;
+    float pre = 0.0f, pre_sel = 0.0f;
+    for (int i = 0; i < TW; ++i) {
+        if (tot[i] > 0.0f)
+            last = i;
+        if (sel < 0 && pre + tot[i] > tau) {
+            sel = i;
+            pre_sel = pre;
+        }
+        pre += tot[i];
+    }
+    if (sel < 0) {
+        sel = last;
+        pre_sel = 0.0f;
+        for (int i = 0; i < last; ++i)
+            pre_sel += tot[i];
+    }
+    rem = tau - pre_sel;
+    return sel;
+}
+
+// The draw with uniform u from the current weights, whose per-segment masses
+// are in S.wtot (total R): the segment whose running mass crosses u * R; the
+// warp sub-range of that segment that crosses (all warps sum one sub-range
+// each); then that sub-range in index order (one warp, a Kogge-Stone scan over
+// the lanes of each step, elements left to right in a lane, the next step's
+// vectors loaded ahead).  Returns the row element (every thread).
 template <int DT>
 __device__ int draw_from(const TParams &P, size_t off, const Wt &w, float R, float u, TSmem &S,
                          int warp, int lane)
 {
     using L = Lg<DT>;
-    const float tau = u * R;
-    int seg = -1, last = -1;
-    float pre = 0.0f, pre_seg = 0.0f;
-    for (int i = 0; i < TW; ++i) {
-        if (S.wtot[i] > 0.0f)
-            last = i;
-        if (seg < 0 && pre + S.wtot[i] > tau) {
-            seg = i;
-            pre_seg = pre;
+    const uint4 ninf = neg_inf_vec(L::NEG_INF_WORD);
+    const bool with_d = w.C > 0.0f;
+    float tau1;
+    const int seg = pick_range(S.wtot, u * R, tau1);
+    const Span sp = span_of<DT>(off, P.V, seg);
+    const int nv = sp.s1 - sp.s0;
+    const int sub = (nv + TW - 1) / TW;
+
+    // level 2: warp w sums sub-range w of the segment
+    {
+        const int a0 = sp.s0 + min(nv, warp * sub), a1 = sp.s0 + min(nv, warp * sub + sub);
+        float acc = 0.0f;
+        for (int a = a0 + lane; a < a1; a += 32) {
+            const uint4 t = tvec<DT>(P.target, off, P.V, sp.A0, a);
+            const uint4 d = with_d ? tvec<DT>(P.draft, off, P.V, sp.A0, a) : ninf;
+            float x[L::VEC];
+            weights<DT>(t, d, w, x);
+#pragma unroll
+            for (int j = 0; j < L::VEC; ++j)
+                acc += x[j];
         }
-        pre += S.wtot[i];
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1)
+            acc += __shfl_xor_sync(0xffffffffu, acc, o);
+        if (lane == 0)
+            S.wsub[warp] = acc;
     }
-    if (seg < 0) {  // rounding left u * R past the last total: the last positive segment
-        seg = last;
-        pre_seg = 0.0f;
-        for (int i = 0; i < seg; ++i)
-            pre_seg += S.wtot[i];
-    }
-    if (warp == seg) {
-        const Span sp = span_of<DT>(off, P.V, seg);
-        const float tw = tau - pre_seg;
-        const uint4 ninf = neg_inf_vec(L::NEG_INF_WORD);
+    __syncthreads();
+    float tw;
+    const int ss = pick_range(S.wsub, tau1, tw);
+
+    // level 3: warp ss walks its sub-range in index order
+    if (warp == ss) {
+        const int b0 = sp.s0 + min(nv, ss * sub), b1 = sp.s0 + min(nv, ss * sub + sub);
         float base = 0.0f;
         int found = -1, lastpos = -1;
-        for (int a0 = sp.s0; a0 < sp.s1; a0 += 32) {
+        uint4 tn = (b0 + lane < b1) ? tvec<DT>(P.target, off, P.V, sp.A0, b0 + lane) : ninf;
+        uint4 dn = (with_d && b0 + lane < b1) ? tvec<DT>(P.draft, off, P.V, sp.A0, b0 + lane)
+                                                : ninf;
+        for (int a0 = b0; a0 < b1; a0 += 32) {
             const int a = a0 + lane;
-            const bool in = a < sp.s1;
-            const uint4 t = in ? tvec<DT>(P.target, off, P.V, sp.A0, a) : ninf;
-            const uint4 d = (in && w.C > 0.0f) ? tvec<DT>(P.draft, off, P.V, sp.A0, a) : ninf;
+            const uint4 t = tn, d = dn;
+            const int an = a + 32;
+            tn = (an < b1) ? tvec<DT>(P.target, off, P.V, sp.A0, an) : ninf;
+            dn = (with_d && an < b1) ? tvec<DT>(P.draft, off, P.V, sp.A0, an) : ninf;
             float x[L::VEC];
             weights<DT>(t, d, w, x);
             const int e0 = (int)((long long)(sp.A0 + (size_t)a * L::VEC) - (long long)off);
@@ -498,11 +545,16 @@ __global__ void __launch_bounds__(TTH, 2) tree_kernel(const TParams P)
             if (err)
                 break;
             if (next < 0) {
-                if (!fresh)
-                    R = residual_pass<DT>(P, off, w, S, warp, lane);
-                if (!(R > 0.0f) && w.C > 0.0f) {
+                if (!(fresh && R > 0.0f)) {
+                    // draw from p_c (a leaf, or the rounding fallback): the
+                    // statistics pass's per-warp partials are the segment masses
                     w.C = 0.0f;
-                    R = residual_pass<DT>(P, off, w, S, warp, lane);
+                    if (tid < TW)
+                        S.wtot[tid] = rescale(S.red_s[tid], S.red_m[tid], mt, c) * w.it;
+                    __syncthreads();
+                    R = 0.0f;
+                    for (int i = 0; i < TW; ++i)
+                        R += S.wtot[i];
                 }
                 if (!(R > 0.0f)) {
                     err = true;
