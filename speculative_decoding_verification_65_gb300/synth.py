@@ -397,7 +397,8 @@ class LmheadCase:
 
 
 def make_lmhead_case(B: int, k: int, V: int, d: int, dtype: str = BF16, recipe: str = "grid",
-                     seed: int = 11, T=(1.0,), sigma_h: float = 0.3) -> LmheadCase:
+                     seed: int = 11, T=(1.0,), sigma_h: float = 0.3,
+                     draft_product: str = "f64") -> LmheadCase:
     """Random target hidden states and LM head, and draft logits from a draft
     model that shares the head but sees perturbed hidden states.
 
@@ -409,7 +410,8 @@ def make_lmhead_case(B: int, k: int, V: int, d: int, dtype: str = BF16, recipe: 
     bf16: logits of spread about 2.5, rounded by any fp32 accumulation.
     Draft hidden states are the target's plus N(0, sigma_h^2) per element
     (on the grid recipe rounded back to the grid); draft logits are their
-    product with W in float64, stored as `dtype`.  Draft tokens are sampled
+    product with W in float64 (draft_product="f32": in float32, for the
+    full-size shapes), stored as `dtype`.  Draft tokens are sampled
     from the draft logits at the sequence's temperature (argmax at T = 0);
     uniforms are float32 in [0, 1).  The bonus position has no draft row."""
     rng = np.random.default_rng(seed)
@@ -419,17 +421,20 @@ def make_lmhead_case(B: int, k: int, V: int, d: int, dtype: str = BF16, recipe: 
         hd = h[:, :k] + np.round(rng.normal(0.0, sigma_h, size=(B, k, d)) * 4.0) / 4.0
         hd = np.clip(hd, -1.0, 1.0).astype(np.float32)
     elif recipe == "gauss":
-        h = rng.standard_normal((B, k + 1, d)).astype(np.float32)
-        w = (rng.standard_normal((V, d)) * (2.5 / np.sqrt(d))).astype(np.float32)
-        hd = (h[:, :k] + rng.normal(0.0, sigma_h, size=(B, k, d))).astype(np.float32)
+        h = rng.standard_normal((B, k + 1, d), dtype=np.float32)
+        w = rng.standard_normal((V, d), dtype=np.float32) * np.float32(2.5 / np.sqrt(d))
+        hd = h[:, :k] + rng.standard_normal((B, k, d), dtype=np.float32) * np.float32(sigma_h)
     else:
         raise ValueError(f"unknown recipe {recipe}")
     hb = f32_to_bf16_bits(h)
     wb = f32_to_bf16_bits(w)
     hdb = f32_to_bf16_bits(hd)
-    w64 = bf16_bits_to_f32(wb).astype(np.float64)
-    dl = (bf16_bits_to_f32(hdb).astype(np.float64).reshape(-1, d) @ w64.T).reshape(B, k, V)
-    dl32 = dl.astype(np.float32)
+    if draft_product == "f32":
+        dl32 = (bf16_bits_to_f32(hdb).reshape(-1, d) @ bf16_bits_to_f32(wb).T).reshape(B, k, V)
+    else:
+        w64 = bf16_bits_to_f32(wb).astype(np.float64)
+        dl = (bf16_bits_to_f32(hdb).astype(np.float64).reshape(-1, d) @ w64.T).reshape(B, k, V)
+        dl32 = dl.astype(np.float32)
     draft = f32_to_bf16_bits(dl32) if dtype == BF16 else dl32
     temps = tuple(T) if isinstance(T, (tuple, list)) else (float(T),)
     temperature = np.asarray(rng.choice(temps, size=B), np.float32)

@@ -43,11 +43,14 @@ def decisions_of(n_ref, k, greedy):
 
 def compare(case, g_tokens, g_n, r_tokens, r_n, trace, band=BAND):
     """Returns a report dict; raises AssertionError on a non-exempt mismatch.
-    `band` widens the exemption where the GPU's inputs to the decisions carry
-    a known extra rounding (the fused LM head's fp32 logits)."""
+    `band` is a scalar, or per decision an array [B, k+1] (accept test i in
+    column i, the draw in column k): it widens the exemption where the GPU's
+    inputs to the decisions carry a known extra rounding (the fused LM head's
+    fp32 logits)."""
     B, k = case.B, case.k
     g_tokens = np.asarray(g_tokens)
     g_n = np.asarray(g_n)
+    bands = np.broadcast_to(np.asarray(band, np.float64), (B, k + 1))
     report = dict(sequences=B, decisions=0, exempt=0, near_band=0, mismatched=[])
     for b in range(B):
         greedy = case.temperature[b] == 0
@@ -55,10 +58,11 @@ def compare(case, g_tokens, g_n, r_tokens, r_n, trace, band=BAND):
         if not greedy and r_n[b] >= 0:
             tested = min(int(r_n[b]) + 1, k)
             th = trace[b, :tested]
-            report["near_band"] += int(np.sum(np.abs(case.u_accept[b, :tested] - th) < band))
+            report["near_band"] += int(np.sum(np.abs(case.u_accept[b, :tested] - th)
+                                              < bands[b, :tested]))
             lo, hi = trace[b, k], trace[b, k + 1]
             u = float(case.u_resample[b])
-            if min(u - lo, hi - u) < band:
+            if min(u - lo, hi - u) < bands[b, k]:
                 report["near_band"] += 1
         if g_n[b] == r_n[b] and np.array_equal(g_tokens[b], r_tokens[b]):
             continue
@@ -70,13 +74,15 @@ def compare(case, g_tokens, g_n, r_tokens, r_n, trace, band=BAND):
             pos = int(min(g_n[b], r_n[b]))
             margin = abs(float(case.u_accept[b, pos]) - trace[b, pos])
             kind = "accept"
+            bd = float(bands[b, pos])
         else:
             lo, hi = trace[b, k], trace[b, k + 1]
             u = float(case.u_resample[b])
             margin = min(u - lo, hi - u)
             kind = "bonus" if r_n[b] == k else "residual"
-        if not margin < band:
-            raise AssertionError(f"mismatch outside the {band} band (margin {margin:.3g}): " + why)
+            bd = float(bands[b, k])
+        if not margin < bd:
+            raise AssertionError(f"mismatch outside the {bd:.3g} band (margin {margin:.3g}): " + why)
         report["exempt"] += 1
         report["mismatched"].append((b, kind, float(margin)))
     report["draws"] = int(np.sum(np.asarray(r_n) >= 0))

@@ -3,9 +3,15 @@ tensor-core product (spec_lmhead_logits) with the fp64 oracle.
 
 On the grid recipe every partial sum of h.W is exact in fp32, so the GPU's
 logits equal the oracle's and the integer outputs must match with the usual
-1e-5 exemption band.  On the gauss recipe the fp32 accumulation rounds: the
-product is checked against a bound on that rounding, and the decisions get a
-band widened by its effect on the probabilities.
+1e-5 exemption band, the exempt count held to 0.01 % of the decisions.  On the
+gauss recipe the fp32 accumulation rounds: the product is checked against a
+bound on that rounding, and each decision gets its own band, the effect of
+its row's per-logit bounds on the threshold or on the draw's cell edges.
+Every mismatch must lie inside its band.  Accept-test mismatches stay under
+the 0.01 % cap; draw mismatches are counted and held to 8 % of the draws: the
+GPU's logits are a different fp32 rounding of the same dot products (about
+1e-6), and on a 128256-token row of this spread that moves u * R across a
+cell edge in a few percent of the draws (9 of 256 measured at full size).
 """
 import os
 
@@ -18,7 +24,8 @@ pytestmark = pytest.mark.gpu
 import oracle  # noqa: E402
 import speculative_decoding_verification_65_gb300 as sv  # noqa: E402
 from speculative_decoding_verification_65_gb300 import synth  # noqa: E402
-from tests.parity_util import compare, check_invariants  # noqa: E402
+from tests.parity_util import (BAND, MAX_EXEMPT_FRACTION, check_bound,  # noqa: E402
+                               check_invariants, compare)
 
 NTHREADS = os.cpu_count() or 1
 
@@ -91,7 +98,7 @@ def test_parity_grid(B, k, V, d, dtype, T):
                                       c.u_resample, c.temperature, nthreads=NTHREADS)
     check_invariants(c, gt, gn)
     rep = compare(c, gt, gn, rt, rn, tr)
-    assert rep["exempt"] <= max(1, rep["decisions"] // 1000), rep
+    check_bound(rep)
 
 
 def test_probs_equal_the_oracle_on_the_grid():
@@ -104,21 +111,102 @@ def test_probs_equal_the_oracle_on_the_grid():
     np.testing.assert_allclose(probs[..., 1], PQ[..., 1], rtol=1e-5, atol=1e-30)
 
 
-def test_parity_gauss_with_widened_band():
-    # fp32 rounding of the logits moves P and Q by at most about 2 log(2) c
-    # times the rounding bound (numerator and normaliser); the band is that
-    # relative change, taken over the batch's largest bound
+def _softmax(t, T):
+    x = t / T
+    e = np.exp(x - x.max())
+    return e / e.sum()
+
+
+def logit_bounds(hidden_bits, w_bits):
+    """rounding_bound with |h|.|W| taken in float32, scaled by 1 + 1e-3 to
+    cover that product's own rounding (all its terms are positive)."""
+    h = np.abs(synth.bf16_bits_to_f32(hidden_bits))
+    w = np.abs(synth.bf16_bits_to_f32(w_bits))
+    d = h.shape[-1]
+    return (d / 16 + 16) * 2.0 ** -24 * (h.reshape(-1, d) @ w.T).astype(np.float64) * (1 + 1e-3)
+
+
+def decision_bands(c, t64, eps, rn, tr):
+    """Per decision, how far the logits' fp32 rounding can move it.  Logits
+    perturbed by |delta_x| <= eps_x move log p(g) by at most
+    (eps_g + E_p[eps]) / T to first order (the numerator and the normaliser),
+    so an accept threshold min(1, P/Q) by min(1, r) (exp(that) - 1); they
+    move the total variation sum |dp| by at most 2 E_p[eps] / T, so a draw
+    cell edge C/R by at most twice that over R.  A factor 1.25 covers the
+    second order; the floor is the usual 1e-5."""
+    B, k = c.B, c.k
+    band = np.full((B, k + 1), BAND)
+    for b in range(B):
+        T = float(c.temperature[b])
+        if T == 0 or rn[b] < 0:
+            continue
+        for i in range(min(int(rn[b]) + 1, k)):
+            p = _softmax(t64[b, i], T)
+            g = int(c.tokens[b, i])
+            delta = (eps[b, i, g] + p @ eps[b, i]) / T
+            band[b, i] = max(BAND, 1.25 * min(1.0, tr[b, i]) * np.expm1(delta))
+        j = int(rn[b])
+        p = _softmax(t64[b, j], T)
+        R = 1.0 if j == k else tr[b, k + 2]
+        band[b, k] = max(BAND, 1.25 * 4.0 * float(p @ eps[b, j]) / (T * R))
+    return band
+
+
+def _check_gauss(c, gt, gn, idx, max_draw_fraction=0.08):
+    """Parity of sequences `idx` of a gauss-recipe call with per-decision
+    bands: every mismatch inside its band, accept-test mismatches under the
+    0.01 % cap, draw mismatches under `max_draw_fraction` of the draws."""
+    s = synth.LmheadCase(c.hidden[idx], c.lm_head, c.draft[idx], c.tokens[idx],
+                         c.u_accept[idx], c.u_resample[idx], c.temperature[idx], c.dtype, c.name)
+    rt, rn, tr = oracle.verify_lmhead(s.hidden, s.lm_head, s.draft, s.tokens, s.u_accept,
+                                      s.u_resample, s.temperature, nthreads=NTHREADS)
+    t64 = oracle.lmhead_logits(s.hidden, s.lm_head).astype(np.float32).astype(np.float64)
+    eps = logit_bounds(s.hidden, s.lm_head).reshape(s.B, s.k + 1, s.V)
+    band = decision_bands(s, t64, eps, rn, tr)
+    check_invariants(s, gt[idx], gn[idx])
+    rep = compare(s, gt[idx], gn[idx], rt, rn, tr, band=band)
+    kinds = [m[1] for m in rep["mismatched"]]
+    accepts = kinds.count("accept")
+    draws = len(kinds) - accepts
+    assert accepts <= max(1, MAX_EXEMPT_FRACTION * rep["decisions"]), rep
+    assert draws <= max(1, max_draw_fraction * rep["draws"]), rep
+    print(f"{c.name}: {rep['decisions']} decisions, {accepts} accept and {draws} draw "
+          f"mismatches inside their bands (median draw band {np.median(band[:, s.k]):.2g})")
+    return rep
+
+
+def test_parity_gauss_per_logit_band():
     B, k, V, d = 32, 4, 8000, 1024
-    c = synth.make_lmhead_case(B, k, V, d, "bf16", recipe="gauss", seed=21, T=(1.0,))
+    c = synth.make_lmhead_case(B, k, V, d, "bf16", recipe="gauss", seed=21, T=(0.7, 1.0, 1.3))
     gt, gn = run(c)
-    rt, rn, tr = oracle.verify_lmhead(c.hidden, c.lm_head, c.draft, c.tokens, c.u_accept,
-                                      c.u_resample, c.temperature, nthreads=NTHREADS)
-    eps = float(rounding_bound(c.hidden.reshape(-1, d), c.lm_head).max())
-    band = max(1e-5, 4.0 * eps / float(np.min(c.temperature)))
-    assert band < 0.01
-    check_invariants(c, gt, gn)
-    rep = compare(c, gt, gn, rt, rn, tr, band=band)
-    assert rep["exempt"] <= max(1, rep["draws"] // 50), rep
+    _check_gauss(c, gt, gn, np.arange(B))
+
+
+def test_parity_gauss_full_size():
+    """The benchmarked shape, B1024 k4 V128256 d4096 on gaussian inputs: the
+    GEMM runs over every row; the first 256 sequences are checked against
+    the oracle."""
+    B, k, V, d = 1024, 4, 128256, 4096
+    c = synth.make_lmhead_case(B, k, V, d, "bf16", recipe="gauss", seed=6, T=(0.7, 1.0, 1.3),
+                               draft_product="f32")
+    gt, gn = run(c)
+    _check_gauss(c, gt, gn, np.arange(256))
+
+
+def test_parity_grid_full_size():
+    """The benchmarked shape on the grid recipe (exact fp32 logits): the
+    first 256 sequences against the oracle, held to the 0.01 % cap."""
+    B, k, V, d = 1024, 4, 128256, 4096
+    c = synth.make_lmhead_case(B, k, V, d, "bf16", recipe="grid", seed=5, T=(0.7, 1.0, 1.3),
+                               draft_product="f32")
+    gt, gn = run(c)
+    idx = np.arange(256)
+    s = synth.LmheadCase(c.hidden[idx], c.lm_head, c.draft[idx], c.tokens[idx],
+                         c.u_accept[idx], c.u_resample[idx], c.temperature[idx], c.dtype, c.name)
+    rt, rn, tr = oracle.verify_lmhead(s.hidden, s.lm_head, s.draft, s.tokens, s.u_accept,
+                                      s.u_resample, s.temperature, nthreads=NTHREADS)
+    check_invariants(s, gt[idx], gn[idx])
+    check_bound(compare(s, gt[idx], gn[idx], rt, rn, tr))
 
 
 def test_error_sequences():
@@ -170,8 +258,7 @@ def test_explicit_side_stream():
     rt, rn, tr = oracle.verify_lmhead(c.hidden, c.lm_head, c.draft, c.tokens, c.u_accept,
                                       c.u_resample, c.temperature, nthreads=NTHREADS)
     check_invariants(c, gt, gn)
-    rep = compare(c, gt, gn, rt, rn, tr)
-    assert rep["exempt"] <= max(1, rep["decisions"] // 1000), rep
+    check_bound(compare(c, gt, gn, rt, rn, tr))
     # grid inputs: every logit is exact in fp32
     want = oracle.lmhead_logits(c.hidden, c.lm_head).reshape(-1, c.V)
     assert int(status.item()) == 0
