@@ -712,51 +712,66 @@ def run_ours_filtered(args):
     top_p = torch.full((B,), args.top_p, dtype=torch.float32, device=dev)
     dt_code = sv.SPEC_F32 if case.dtype == synth.F32 else sv.SPEC_BF16
     stream = torch.cuda.current_stream(dev)
-    ws = sv.workspace(B, k, V, dt_code, dev, stream)
+    # the binding's default workspace has room for the group maxima (top-k rows
+    # cut from them); the smaller one sends every row through the streaming
+    # filter, timed too
+    ws = sv.filtered_workspace(B, k, V, dt_code, dev, stream)
+    ws_stream = torch.zeros(sv.spec_verify_workspace_size(B, k, V, dt_code), dtype=torch.uint8,
+                            device=dev)
     out_t = torch.empty((B, k + 1), dtype=torch.int32, device=dev)
     out_n = torch.empty((B,), dtype=torch.int32, device=dev)
     alg_bytes = synth.algorithmic_bytes(case)
 
-    def step(events=None):
+    def step(events=None, w=None):
+        w = ws if w is None else w
         if events is None:
             sv.spec_verify_filtered(**d, top_k=top_k, top_p=top_p, out_tokens=out_t,
-                                    out_num_accepted=out_n, ws=ws, stream=stream)
+                                    out_num_accepted=out_n, ws=w, stream=stream)
         else:
             sv.spec_verify_filtered_timed(**d, top_k=top_k, top_p=top_p, out_tokens=out_t,
-                                          out_num_accepted=out_n, ws=ws, stage_events=events,
+                                          out_num_accepted=out_n, ws=w, stage_events=events,
                                           stream=stream)
 
-    for _ in range(max(args.warmup, 3)):
-        step()
-    torch.cuda.synchronize(dev)
-    if sv.spec_verify_read_status(ws) != sv.SPEC_DEV_OK:
-        raise RuntimeError("device status nonzero after warm-up")
-    n_err = int((out_n < 0).sum().item())
-    t0 = torch.cuda.Event(enable_timing=True)
-    t1 = torch.cuda.Event(enable_timing=True)
-    barrier()
-    torch.cuda.synchronize(dev)
-    with ClockSampler(local) as clk:
-        t0.record(stream)
-        for _ in range(args.steps):
-            step()
-        t1.record(stream)
+    def measure(w):
+        """K timed calls (one event pair, clocks sampled), then K calls with an
+        event after each stage: (ms for K calls, mean ms per stage, clocks)."""
+        for _ in range(max(args.warmup, 3)):
+            step(w=w)
         torch.cuda.synchronize(dev)
-    barrier()
-    total_ms = reduce_max(t0.elapsed_time(t1), world, dev)
-    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
-    stages = [[torch.cuda.Event(enable_timing=True) for _ in range(sv.SPEC_FILTERED_STAGES)]
-              for _ in range(args.steps)]
-    for ev in [e for row in stages for e in row]:
-        ev.record(stream)
-    torch.cuda.synchronize(dev)
-    for i in range(args.steps):
-        starts[i].record(stream)
-        step(stages[i])
-    torch.cuda.synchronize(dev)
-    stage_ms = [statistics.mean(
-        (starts[i] if j == 0 else stages[i][j - 1]).elapsed_time(stages[i][j])
-        for i in range(args.steps)) for j in range(sv.SPEC_FILTERED_STAGES)]
+        if sv.spec_verify_read_status(w) != sv.SPEC_DEV_OK:
+            raise RuntimeError("device status nonzero after warm-up")
+        t0 = torch.cuda.Event(enable_timing=True)
+        t1 = torch.cuda.Event(enable_timing=True)
+        barrier()
+        torch.cuda.synchronize(dev)
+        with ClockSampler(local) as clk, nvtx_range("spec_verify_filtered timed region"):
+            t0.record(stream)
+            for _ in range(args.steps):
+                step(w=w)
+            t1.record(stream)
+            torch.cuda.synchronize(dev)
+        barrier()
+        tot = reduce_max(t0.elapsed_time(t1), world, dev)
+        starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+        stages = [[torch.cuda.Event(enable_timing=True) for _ in range(sv.SPEC_FILTERED_STAGES)]
+                  for _ in range(args.steps)]
+        for ev in [e for row in stages for e in row]:
+            ev.record(stream)
+        torch.cuda.synchronize(dev)
+        for i in range(args.steps):
+            starts[i].record(stream)
+            step(stages[i], w=w)
+        torch.cuda.synchronize(dev)
+        sm = [statistics.mean(
+            (starts[i] if j == 0 else stages[i][j - 1]).elapsed_time(stages[i][j])
+            for i in range(args.steps)) for j in range(sv.SPEC_FILTERED_STAGES)]
+        return tot, sm, clk.summary()
+
+    stream_ms, stream_stage_ms, stream_clk = measure(ws_stream)
+    stream_out = (out_t.clone(), out_n.clone())
+    total_ms, stage_ms, clocks = measure(ws)
+    same_as_streaming = bool(torch.equal(stream_out[0], out_t) and torch.equal(stream_out[1], out_n))
+    n_err = int((out_n < 0).sum().item())
     ms_per_step = total_ms / args.steps
     value = aggregate_rate(B * k, args.steps, world, total_ms / 1e3)
     status = sv.spec_verify_read_status(ws)
@@ -788,14 +803,14 @@ def run_ours_filtered(args):
         return
     peaks, peak_src = measured_peaks()
     peak = float(peaks.get("hbm_gbs", 6800.0))
-    # the dominant kernel is the filter: its algorithmic bytes are one read of
-    # every row it filters (all 2k+1 rows of a sampled sequence whose filters
-    # are on; greedy sequences are not read)
+    # the streaming filter's algorithmic bytes are one read of every row it
+    # filters (all 2k+1 rows of a sampled sequence whose filters are on;
+    # greedy sequences are not read)
     filt_on = (args.top_k > 0 and args.top_k < V) or args.top_p < 1.0
     n_sampled = int(np.sum(case.temperature > 0)) if filt_on else 0
     filt_bytes = n_sampled * (2 * k + 1) * V * (2 if case.dtype == "bf16" else 4)
-    achieved = filt_bytes / (stage_ms[1] / 1e3) / 1e9
-    stats_achieved = alg_bytes / (stage_ms[0] / 1e3) / 1e9
+    stream_achieved = filt_bytes / (stream_stage_ms[1] / 1e3) / 1e9
+    achieved = alg_bytes / (stage_ms[0] / 1e3) / 1e9  # the statistics kernel
     workload = synth.CONFIG_NAMES[args.config] if args.batch is None else case.name
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
@@ -807,24 +822,34 @@ def run_ours_filtered(args):
                    "draft_tokens": "drawn from the filtered draft distribution",
                    "error_sequences": n_err, "algorithmic_bytes_per_step": alg_bytes,
                    "l2": "inputs larger than L2 (no flush)", "parallelism": f"dp{world}"},
-        "gpu_launches": sv.SPEC_FILTERED_STAGES * args.steps,
+        "gpu_launches": (sv.SPEC_FILTERED_STAGES + 3) * args.steps,  # nine kernels a call
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak,
                      "traffic": recorded_traffic(f"{workload}_top{args.top_k}_p{args.top_p}",
-                                                 "wfilter_kernel"),
+                                                 "stats_kernel"),
                      "peak_source": f"{peak_src} copy bandwidth (MEASURED_PEAKS.json hbm_gbs)"
                      if peak_src == "measured" else "fallback 6.8 TB/s",
-                     "kernel": "wfilter_kernel + filter_kernel (top-k / top-p cut per row: "
-                               "one read of each filtered row; the second kernel only "
-                               "finishes rows the first flags)",
-                     "algorithmic_bytes_per_launch": filt_bytes,
+                     "kernel": "stats_kernel (one read of every logit, with the group maxima "
+                               "of the top-k cut)",
                      "kernel_timing": "CUDA events after each kernel, K further steps",
-                     "step_GBps": alg_bytes / (ms_per_step / 1e3) / 1e9,
-                     "stats_kernel": {"achieved": stats_achieved,
-                                      "frac": stats_achieved / peak}},
+                     "step_GBps": alg_bytes / (ms_per_step / 1e3) / 1e9},
         "stage_ms": {"stats": stage_ms[0], "filter": stage_ms[1], "scan": stage_ms[2],
                      "draw": stage_ms[3], "final": stage_ms[4], "exact_draws": stage_ms[5]},
-        "clocks": clk.summary(),
+        "streaming_filter": {
+            "what": "the same calls with a workspace without room for group maxima: every "
+                    "row cut by the streaming window filter (wfilter_kernel, then "
+                    "filter_kernel for the rows it flags)",
+            "ms_per_step": stream_ms / args.steps, "same_outputs": same_as_streaming,
+            "stage_ms": {"stats": stream_stage_ms[0], "filter": stream_stage_ms[1],
+                         "scan": stream_stage_ms[2], "draw": stream_stage_ms[3],
+                         "final": stream_stage_ms[4], "exact_draws": stream_stage_ms[5]},
+            "roofline": {"bound": "hbm", "achieved": stream_achieved, "peak": peak,
+                         "unit": "GB/s", "frac": stream_achieved / peak,
+                         "algorithmic_bytes_per_launch": filt_bytes,
+                         "traffic": recorded_traffic(
+                             f"{workload}_top{args.top_k}_p{args.top_p}", "wfilter_kernel")},
+            "clocks": stream_clk},
+        "clocks": clocks,
         "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": int(B * (k + 2) * 4), "steps": e2e_steps,
                 "path": "torch copies of pinned host tensors around spec_verify_filtered"},

@@ -174,6 +174,14 @@ int32_t spec_verify_trace(const void *target_logits, const void *draft_logits,
                           void *workspace, size_t workspace_bytes, void *stream);
 
 /*
+ * Bytes of workspace with which spec_verify_filtered cuts top-k rows from
+ * group maxima: spec_verify_workspace_size rounded up to 256, plus 4 bytes per
+ * 64 bf16 (32 fp32) logits of every row, B (2k+1) rows.  Returns 0 for sizes
+ * out of range.  Host-only; needs no GPU.
+ */
+size_t spec_verify_filtered_workspace_size(int32_t B, int32_t k, int32_t V, int32_t dtype);
+
+/*
  * spec_verify with top-k / top-p filtered distributions.  The pages require
  * draft and target to share their sampling parameters, top-p among them
  * ("Speculative Decoding and the Art of Fast LLM Inference", "Why It Stays
@@ -189,11 +197,15 @@ int32_t spec_verify_trace(const void *target_logits, const void *draft_logits,
  *   out_probs  device float32 [B, k, 2] or NULL: the filtered P = p~_i(g_i),
  *          Q = q~_i(g_i) (NaN for greedy and error sequences)
  * A draft token outside the draft's kept set (q~(g) = 0) is a sequence error.
- * Other arguments, the workspace (spec_verify_workspace_size) and errors as
- * spec_verify.  Seven kernels run: statistics; the filter in two (per row,
- * the end of the kept set: one streaming pass over the row in the common
- * case, then the rows it could not cut, by a second pass or a radix search
- * over the order key); accept scan; draw tiles; final search; exact draws.
+ * Other arguments and errors as spec_verify.  The workspace is at least
+ * spec_verify_workspace_size bytes; with spec_verify_filtered_workspace_size
+ * bytes the rows with top-k (1 <= K <= 256) are cut from per-group maxima the
+ * statistics kernel leaves in the extra room (only the groups that can hold
+ * a kept token are read again), otherwise every row takes the streaming
+ * filter.  The kernels: statistics; the filter (the group-maximum cut of
+ * top-k rows when there is room; one streaming pass over each other row;
+ * then the rows neither could cut, by a second pass or a radix search over
+ * the order key); accept scan; draw tiles; final search; exact draws.
  */
 int32_t spec_verify_filtered(const void *target_logits, const void *draft_logits,
                              const int32_t *draft_tokens, const float *u_accept,

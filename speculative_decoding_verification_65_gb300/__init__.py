@@ -113,6 +113,8 @@ def library():
         lib.spec_verify_lmhead_timed.argtypes = [vp] * 10 + [i32] * 5 + [vp, sz, vp, vp]
         lib.spec_lmhead_logits.restype = i32
         lib.spec_lmhead_logits.argtypes = [vp, vp, vp, i32, i32, i32, vp, vp]
+        lib.spec_verify_filtered_workspace_size.restype = sz
+        lib.spec_verify_filtered_workspace_size.argtypes = [i32, i32, i32, i32]
         lib.spec_verify_tree.restype = i32
         lib.spec_verify_tree.argtypes = [vp] * 11 + [i32] * 4 + [vp]
         _lib = lib
@@ -181,6 +183,24 @@ def workspace(B: int, k: int, V: int, dtype: int, device=None, stream=None):
         device = torch.device("cuda", torch.cuda.current_device())
     s = stream if stream is not None else torch.cuda.current_stream(device)
     need = spec_verify_workspace_size(B, k, V, dtype)
+    if need == 0:
+        raise ValueError(f"sizes out of range: B={B} k={k} V={V} dtype={dtype}")
+    return _cached_workspace(need, device, s)
+
+
+def spec_verify_filtered_workspace_size(B: int, k: int, V: int, dtype: int) -> int:
+    return int(library().spec_verify_filtered_workspace_size(B, k, V, dtype))
+
+
+def filtered_workspace(B: int, k: int, V: int, dtype: int, device=None, stream=None):
+    """workspace() with room for the top-k cut from group maxima
+    (spec_verify_filtered_workspace_size)."""
+    torch = _torch()
+    device = torch.device(device if device is not None else "cuda")
+    if device.index is None:
+        device = torch.device("cuda", torch.cuda.current_device())
+    s = stream if stream is not None else torch.cuda.current_stream(device)
+    need = spec_verify_filtered_workspace_size(B, k, V, dtype)
     if need == 0:
         raise ValueError(f"sizes out of range: B={B} k={k} V={V} dtype={dtype}")
     return _cached_workspace(need, device, s)
@@ -320,7 +340,7 @@ def spec_verify_filtered(target, draft, tokens, u_accept, u_resample, temperatur
     _dev_out("out_num_accepted", out_num_accepted, (B,), torch.int32, dev)
     probs = torch.empty((B, k, 2), dtype=torch.float32, device=dev) if want_probs else None
     if ws is None:
-        ws = workspace(B, k, V, dt, dev, stream)
+        ws = filtered_workspace(B, k, V, dt, dev, stream)
     _check_ws(ws, dev)
     with _on(dev):
         rc = library().spec_verify_filtered(_ptr(target), _ptr(draft), _ptr(tokens), _ptr(u_accept),
@@ -338,7 +358,7 @@ def spec_verify_filtered_timed(target, draft, tokens, u_accept, u_resample, temp
                                top_k, top_p, out_tokens, out_num_accepted, ws, stage_events,
                                stream=None):
     """spec_verify_filtered recording SPEC_FILTERED_STAGES events: after the
-    statistics, the filter (both of its kernels), the accept scan, the draw
+    statistics, the filter (all of its kernels), the accept scan, the draw
     tiles, the final search and the exact draws."""
     torch = _torch()
     B, k, V, dt = _marshal(target, draft, tokens, u_accept, u_resample, temperature)

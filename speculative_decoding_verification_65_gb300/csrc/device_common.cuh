@@ -26,7 +26,9 @@ struct WsHeader {
     unsigned int next_resolve;  // work-item counter of the exact draws (likewise)
     unsigned int n_slow_ratio;  // exact draws whose fp32 mass ratio was too far off (diagnostic)
     unsigned int n_slow_kinks;  // exact draws with too many undecided elements (diagnostic)
-    unsigned int pad[57];
+    unsigned int n_stream_rows; // filtered rows the group-maximum cut left to the streaming filter
+    unsigned int n_radix_rows;  // filtered rows left to the radix kernel
+    unsigned int pad[55];
 };
 static_assert(sizeof(WsHeader) == 256, "header is 256 bytes");
 

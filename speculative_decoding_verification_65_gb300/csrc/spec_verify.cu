@@ -151,6 +151,8 @@ struct Params {
     const int32_t *top_k;  // [B] or null (filtered calls)
     const float *top_p;    // [B] or null (filtered calls)
     FiltRec *filt;     // [B][rows] (filtered calls)
+    unsigned int *gkey;  // [B][rows][NS * NT] lane-group maximum keys (filtered calls
+                         // with room for them; null otherwise)
     // exact draws of the rows whose fp32 draw is near a cell boundary
     RJob *rjob;            // [B] the listed draws (count in hdr->n_flag)
     unsigned int *rkcnt;   // [B] their counts of groups of undecided elements
@@ -191,10 +193,12 @@ struct LaneStat {
 
 // Consumer warp w owns the contiguous 4 KB chunk w of a tile: lane l reads the
 // tile's vectors 256*w + 32*u + l, u < U.  `rec` (nullable) receives the
-// chunk's record (maximum, sum of 2^((x - max) * c)) on a bonus row.
+// chunk's record (maximum, sum of 2^((x - max) * c)) on a bonus row; `gk`
+// (nullable, the warp's 32 slots) the order key of the maximum of each lane's
+// U vectors, for the top-k cut of a filtered call.
 template <int DT>
 __device__ __forceinline__ void tile_accumulate(const Seg &g, int warp, int lane, int mode, float c,
-                                                LaneStat &st, float2 *rec)
+                                                LaneStat &st, float2 *rec, unsigned int *gk)
 {
     using L = Lg<DT>;
     constexpr int VEC = L::VEC;
@@ -225,6 +229,8 @@ __device__ __forceinline__ void tile_accumulate(const Seg &g, int warp, int lane
 #pragma unroll
         for (int u = 1; u < U; ++u)
             mt = fmax_nan(mt, vmax[u]);
+        if (gk)
+            __stcg(gk + lane, key_of<DT>(mt));
         // the lane's indices grow with u, and the first occurrence over the
         // super-tile lies in the earliest tile holding a strictly larger maximum
         if (mt > st.m) {
@@ -248,6 +254,8 @@ __device__ __forceinline__ void tile_accumulate(const Seg &g, int warp, int lane
     // sampling: the tile's sum against the lane's tile maximum, folded into the
     // running (m, s) with one rescale of each side
     const float mt = L::tile_max(raw);
+    if (gk)
+        __stcg(gk + lane, key_of<DT>(mt));
     float ts = 0.0f;
     if (mt != -INFINITY) {
         const unsigned long long c2 = f2(c, c);
@@ -297,6 +305,8 @@ __global__ void __launch_bounds__(NTHREADS, 2) stats_kernel(const Params P)
             P.hdr->next_resolve = 0u;
             P.hdr->n_slow_ratio = 0u;
             P.hdr->n_slow_kinks = 0u;
+            P.hdr->n_stream_rows = 0u;
+            P.hdr->n_radix_rows = 0u;
         }
         for (int s = 0; s < STAGES; ++s) {
             mbar_init(&S.full[s], 1);
@@ -424,7 +434,10 @@ __global__ void __launch_bounds__(NTHREADS, 2) stats_kernel(const Params P)
             if (q < P.NCH)
                 rec = P.rec + (size_t)ti.b * P.NCH + q;
         }
-        tile_accumulate<DT>(g, warp, lane, ti.mode, ti.c, st, rec);
+        unsigned int *gk = P.gkey ? P.gkey + ((size_t)ti.b * P.rows + ti.rsq) * (size_t)P.NS * NT +
+                                        (size_t)ti.seg * NT + (size_t)warp * 32
+                                  : nullptr;
+        tile_accumulate<DT>(g, warp, lane, ti.mode, ti.c, st, rec, gk);
         if (!ti.last) {
             // the slot is free once every warp has read it
             __syncwarp();
@@ -620,6 +633,8 @@ __global__ void __launch_bounds__(FTH, 2) filter_kernel(const Params P)
     bool failed = false;    // a bulk copy never landed: stop this CTA
     allow_next_kernel();
     wait_previous_kernel();  // partials come from the statistics kernel
+    if (__ldcg(&P.hdr->n_radix_rows) == 0u)
+        return;  // no row was left to the radix search
 
     // This kernel finishes the rows the window kernel recorded FILT_RADIX
     // (its buffer overflowed, or its window ended short of the cut).  Rows
@@ -1473,6 +1488,327 @@ __global__ void __launch_bounds__(FTH, 2) filter_kernel(const Params P)
     }
 }
 
+// ------------------------------------------- top-k: the cut from group maxima
+//
+// In a filtered call whose workspace has room for them, the statistics kernel
+// leaves, per row, the order key of the maximum of each lane's 8 vectors of
+// each tile (64 logits of bf16, 32 of fp32): a group.  For a row with top-k,
+// K <= KF_KMAX, the K-th largest group key tau is at most the key of the
+// row's K-th largest logit (K groups have a maximum >= tau, each of them a
+// logit >= tau), so every kept token lies in a group whose key is >= tau.
+// Only those groups are read again: their logits with key >= tau are
+// gathered, sorted by (key desc, index asc), and the cut is read off the
+// sorted list exactly as the window kernel reads it off its sorted window
+// (top-k mass, then the top-p end by the fixed-point masses).  tau is found
+// by a radix search over the row's group keys, 8 bits per pass (two passes
+// for bf16 keys, whose low 16 bits are zero).  A row with more selected
+// groups or gathered tokens than the buffers hold (many ties at tau) is left
+// to the radix kernel (FILT_RADIX).  The window kernel skips these rows.
+constexpr int KF_TH = 128;
+constexpr int KF_KMAX = 256;
+constexpr int KF_GCAP = 512;   // selected groups at most
+constexpr int KF_CAP = 512;    // gathered tokens at most (the sort's size)
+constexpr int KF_LB = 8;       // group-key loads in flight per thread
+static_assert(KF_KMAX <= KF_CAP && (KF_CAP & (KF_CAP - 1)) == 0,
+              "the kept set fits the buffer, whose size the sort pads to");
+
+// The rows the group-maximum cut takes (the same test in the window kernel).
+__device__ __forceinline__ bool kf_row(const Params &P, float T, int K, float Pp)
+{
+    const bool bad = K < 0 || isnan(Pp) || !(Pp > 0.0f);
+    return P.gkey != nullptr && temperature_valid(T) && T > 0.0f && !bad && K > 0 && K < P.V &&
+           K <= KF_KMAX;
+}
+
+struct KfSmem {
+    unsigned long long key[KF_CAP], mass[KF_CAP];  // gathered tokens, sorted padded to 2^n
+    int glist[KF_GCAP];
+    unsigned int hist[256];
+    unsigned int ng, nc;
+    unsigned int sel, need;
+    unsigned long long red[KF_TH / 32];
+};
+
+template <int DT>
+__global__ void __launch_bounds__(KF_TH) kfilter_kernel(const Params P)
+{
+    using L = Lg<DT>;
+    constexpr int VEC = L::VEC;
+    constexpr int VPT = TILE_BYTES / 16;                   // vectors per tile
+    constexpr int LOW = (DT == SPEC_F32) ? 0 : 16;          // bf16 keys end at bit 16
+    __shared__ KfSmem S;
+    const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
+    const int V = P.V;
+    const int items = P.B * P.rows;
+    const size_t NG = (size_t)P.NS * NT;
+    allow_next_kernel();
+    wait_previous_kernel();  // the partials and the group keys
+
+    for (int item = blockIdx.x; item < items; item += gridDim.x) {
+        const int b = item / P.rows, rsq = item - b * P.rows;
+        const float T = __ldg(P.temperature + b);
+        const int K = P.top_k ? __ldg(P.top_k + b) : 0;
+        const float Pp = P.top_p ? __ldg(P.top_p + b) : 1.0f;
+        if (!kf_row(P, T, K, Pp)) {
+            // rows with nothing to cut get their record here (as the window
+            // kernel writes it); the others are left to the streaming filter
+            const bool bad = K < 0 || isnan(Pp) || !(Pp > 0.0f);
+            const bool topk = K > 0 && K < V, topp = Pp < 1.0f;
+            if (!temperature_valid(T) || T == 0.0f || (!topk && !topp) || bad) {
+                if (t == 0) {
+                    FiltRec o;
+                    o.kappa = 0u;
+                    o.iota = INT_MAX;
+                    o.zt = 0.0f;
+                    o.flags = (temperature_valid(T) && bad) ? FILT_ERR : FILT_OFF;
+                    P.filt[item] = o;
+                }
+            } else if (t == 0) {
+                atomicAdd(&P.hdr->n_stream_rows, 1u);
+            }
+            continue;
+        }
+        const bool topp = Pp < 1.0f;
+        const float c = LOG2E / T;
+        const float4 *pp = P.part + (size_t)item * P.NSS;
+        float m = -INFINITY;
+        for (int q = lane; q < P.NSS; q += 32)
+            m = fmax_nan(m, __ldcg(pp + q).x);
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1)
+            m = fmax_nan(m, __shfl_xor_sync(0xffffffffu, m, o));
+        FiltRec out;
+        out.kappa = 0u;
+        out.iota = INT_MAX;
+        out.zt = 0.0f;
+        out.flags = FILT_OFF;
+        if (!(isnan(m) || isinf(m))) {  // else the scan reports the row as an error
+            const unsigned int *gk = P.gkey + (size_t)item * NG;
+            // the group keys, KF_LB loads in flight per thread (from L2 after
+            // the first pass).  NG is a multiple of the block, so every lane
+            // takes each step.
+            auto for_keys = [&](auto fn) {
+                for (size_t g0 = 0; g0 < NG; g0 += (size_t)KF_TH * KF_LB) {
+                    unsigned int key[KF_LB];
+#pragma unroll
+                    for (int q = 0; q < KF_LB; ++q) {
+                        const size_t g = g0 + (size_t)q * KF_TH + t;
+                        key[q] = (g < NG) ? __ldcg(gk + g) : 0u;
+                    }
+#pragma unroll
+                    for (int q = 0; q < KF_LB; ++q)
+                        if (g0 + (size_t)q * KF_TH < NG)  // the same in every lane
+                            fn(g0 + (size_t)q * KF_TH + t, key[q]);
+                }
+            };
+            // ---- tau: the K-th largest group key, 8 bits per pass
+            unsigned int prefix = 0u, pmask = 0u, need = (unsigned int)K;
+            for (int shift = 24; shift >= LOW; shift -= 8) {
+                for (int i = t; i < 256; i += KF_TH)
+                    S.hist[i] = 0u;
+                __syncthreads();
+                // lanes with the same bin add once, through their leader
+                for_keys([&](size_t, unsigned int key) {
+                    const bool in = (key & pmask) == prefix;
+                    const unsigned int bin = (key >> shift) & 255u;
+                    const unsigned int act = __ballot_sync(0xffffffffu, in);
+                    if (in) {
+                        const unsigned int peers = __match_any_sync(act, bin);
+                        if (lane == __ffs(peers) - 1)
+                            atomicAdd(&S.hist[bin], (unsigned int)__popc(peers));
+                    }
+                });
+                __syncthreads();
+                if (warp == 0) {
+                    // lane l holds bins 255 - 8l down to 248 - 8l
+                    unsigned int h[8], sum = 0u;
+#pragma unroll
+                    for (int j = 0; j < 8; ++j) {
+                        h[j] = S.hist[255 - 8 * lane - j];
+                        sum += h[j];
+                    }
+                    unsigned int incl = sum;
+#pragma unroll
+                    for (int o = 1; o < 32; o <<= 1) {
+                        const unsigned int y = __shfl_up_sync(0xffffffffu, incl, o);
+                        if (lane >= o)
+                            incl += y;
+                    }
+                    const unsigned int excl = incl - sum;
+                    const unsigned int hit = __ballot_sync(0xffffffffu, incl >= need);
+                    // at least `need` keys match the prefix: some lane hits
+                    const int hl = hit ? __ffs(hit) - 1 : 31;
+                    if (lane == hl) {
+                        unsigned int cum = excl;
+                        int sel = 248 - 8 * lane;
+#pragma unroll
+                        for (int j = 0; j < 8; ++j) {
+                            if (cum + h[j] >= need) {
+                                sel = 255 - 8 * lane - j;
+                                break;
+                            }
+                            cum += h[j];
+                        }
+                        S.sel = (unsigned int)sel;
+                        S.need = need - cum;
+                    }
+                }
+                __syncthreads();
+                prefix |= S.sel << shift;
+                pmask |= 255u << shift;
+                need = S.need;
+                __syncthreads();
+            }
+            const unsigned int tau = prefix;
+            // ---- the groups holding a key >= tau, then their tokens >= tau
+            if (t == 0) {
+                S.ng = 0u;
+                S.nc = 0u;
+            }
+            __syncthreads();
+            for_keys([&](size_t g, unsigned int key) {
+                const bool sel = key >= tau;
+                const unsigned int slot = warp_slot(sel, &S.ng, lane);
+                if (sel && slot < (unsigned int)KF_GCAP)
+                    S.glist[slot] = (int)g;
+            });
+            __syncthreads();
+            const unsigned int ng = S.ng;
+            bool over = ng > (unsigned int)KF_GCAP;
+            if (!over) {
+                const bool is_target = rsq <= P.k;
+                const void *arr = is_target ? P.target : P.draft;
+                const size_t row = is_target ? (size_t)b * (P.k + 1) + rsq
+                                             : (size_t)b * P.k + (rsq - P.k - 1);
+                const int nw = (int)ng * U;
+                // the row's vectors are 16-byte aligned in memory when its first
+                // element is (the array base is)
+                const bool aligned = ((row * (size_t)V) % VEC) == 0;
+                for (int w0 = 0; w0 < nw; w0 += KF_TH) {  // every lane takes each step
+                    const int w = w0 + t;
+                    int v = -1;
+                    if (w < nw) {
+                        const int g = S.glist[w / U], u = w - (w / U) * U;
+                        const int seg = g / NT, gw = (g % NT) / 32, gl = g % 32;
+                        v = seg * VPT + 256 * gw + 32 * u + gl;  // the group lane's vector u
+                    }
+                    float x[VEC];
+                    if (v >= 0 && aligned && (v + 1) * VEC <= V) {
+                        L::unpack(__ldg(reinterpret_cast<const uint4 *>(arr) +
+                                        (row * (size_t)V) / VEC + v), x);
+                    } else {
+#pragma unroll
+                        for (int j = 0; j < VEC; ++j) {
+                            const int e = v * VEC + j;
+                            x[j] = (v >= 0 && e < V) ? L::load1(arr, row * (size_t)V + e)
+                                                     : -INFINITY;
+                        }
+                    }
+#pragma unroll
+                    for (int j = 0; j < VEC; ++j) {
+                        const int e = v * VEC + j;
+                        const bool want = v >= 0 && e < V && key_of<DT>(x[j]) >= tau;
+                        const unsigned int slot = warp_slot(want, &S.nc, lane);
+                        if (want && slot < (unsigned int)KF_CAP) {
+                            S.key[slot] = sortkey(key_of<DT>(x[j]), e);
+                            S.mass[slot] = fixmass(x[j], m, c);
+                        }
+                    }
+                }
+                __syncthreads();
+                over = S.nc > (unsigned int)KF_CAP;
+            }
+            if (over) {
+                out.flags = FILT_RADIX;
+                if (t == 0)
+                    atomicAdd(&P.hdr->n_radix_rows, 1u);
+            } else {
+                // ---- sort descending (bitonic, padded with zero entries)
+                const int n = (int)S.nc;
+                int n2 = 1;
+                while (n2 < n)
+                    n2 <<= 1;
+                for (int i = n + t; i < n2; i += KF_TH) {
+                    S.key[i] = 0ull;
+                    S.mass[i] = 0ull;
+                }
+                __syncthreads();
+                for (int size = 2; size <= n2; size <<= 1) {
+                    for (int stride = size >> 1; stride > 0; stride >>= 1) {
+                        for (int i = t; i < n2 / 2; i += KF_TH) {
+                            const int lo = 2 * stride * (i / stride) + (i % stride), hi = lo + stride;
+                            const bool down = (lo & size) == 0;  // this pair's block ends descending
+                            const unsigned long long a = S.key[lo], bb = S.key[hi];
+                            if (down ? (a < bb) : (a > bb)) {
+                                S.key[lo] = bb;
+                                S.key[hi] = a;
+                                const unsigned long long ma = S.mass[lo];
+                                S.mass[lo] = S.mass[hi];
+                                S.mass[hi] = ma;
+                            }
+                        }
+                        __syncthreads();
+                    }
+                }
+                // ---- the cut: the top-k mass, then the top-p end (K <= n)
+                const int nk = min(K, n);
+                unsigned long long ms = 0ull;
+                for (int i = t; i < nk; i += KF_TH)
+                    ms += S.mass[i];
+#pragma unroll
+                for (int o = 16; o > 0; o >>= 1)
+                    ms += __shfl_xor_sync(0xffffffffu, ms, o);
+                if (lane == 0)
+                    S.red[warp] = ms;
+                __syncthreads();
+                unsigned long long ZK = 0ull;
+                for (int w = 0; w < KF_TH / 32; ++w)
+                    ZK += S.red[w];
+                int last = nk - 1;
+                unsigned long long Zt = ZK;
+                if (topp && warp == 0) {
+                    unsigned long long target = (unsigned long long)((double)Pp * (double)ZK);
+                    if (target == 0ull)
+                        target = 1ull;
+                    unsigned long long run = 0ull;
+                    int istar = -1;
+                    for (int i0 = 0; i0 < nk && istar < 0; i0 += 32) {
+                        const int i = i0 + lane;
+                        unsigned long long x = (i < nk) ? S.mass[i] : 0ull;
+#pragma unroll
+                        for (int o = 1; o < 32; o <<= 1) {
+                            const unsigned long long y = __shfl_up_sync(0xffffffffu, x, o);
+                            if (lane >= o)
+                                x += y;
+                        }
+                        const unsigned long long inc = run + x;
+                        const unsigned int hit = __ballot_sync(0xffffffffu, i < nk && inc >= target);
+                        if (hit) {
+                            const int hl = __ffs(hit) - 1;
+                            istar = i0 + hl;
+                            run = __shfl_sync(0xffffffffu, inc, hl);
+                        } else {
+                            run = __shfl_sync(0xffffffffu, inc, 31);
+                        }
+                    }
+                    if (istar < 0)
+                        istar = nk - 1;  // rounding: all of them
+                    last = istar;
+                    Zt = run;
+                }
+                const unsigned long long e = S.key[last];
+                out.kappa = (unsigned int)(e >> 32);
+                out.iota = (int)(0xffffffffu - (unsigned int)(e & 0xffffffffu));
+                out.zt = (float)((double)Zt * (1.0 / 1099511627776.0));
+                out.flags = FILT_ON;
+            }
+        }
+        if (t == 0)
+            P.filt[item] = out;
+        __syncthreads();  // the row's shared state is free again
+    }
+}
+
 // ------------------------------------ top-k / top-p: the one-pass window kernel
 //
 // The common case of the filter, warp-specialized like the statistics kernel:
@@ -1552,6 +1888,8 @@ __global__ void __launch_bounds__(WTH, 2) wfilter_kernel(const Params P)
     __syncthreads();
     allow_next_kernel();
     wait_previous_kernel();  // the partials and the zeroed row counter
+    if (P.gkey && __ldcg(&P.hdr->n_stream_rows) == 0u)
+        return;  // the group-maximum cut took every row that needed a cut
 
     if (warp == WPW) {
         // ---------------------------------------------------------- producer
@@ -1570,6 +1908,8 @@ __global__ void __launch_bounds__(WTH, 2) wfilter_kernel(const Params P)
             const bool topk = K > 0 && K < V;
             const bool topp = Pp < 1.0f;
             const bool bad = K < 0 || isnan(Pp) || !(Pp > 0.0f);
+            if (kf_row(P, T, K, Pp))
+                continue;  // cut from the group maxima (kfilter_kernel)
             if (!temperature_valid(T) || T == 0.0f || (!topk && !topp) || bad) {
                 FiltRec out;
                 out.kappa = 0u;
@@ -2150,8 +2490,11 @@ __global__ void __launch_bounds__(WTH, 2) wfilter_kernel(const Params P)
                 out.flags = FILT_ON;
             }
         }
-        if (t == 0)
+        if (t == 0) {
             P.filt[item] = out;
+            if (out.flags == FILT_RADIX)
+                atomicAdd(&P.hdr->n_radix_rows, 1u);
+        }
         cbar();  // every warp is done with the row's shared state
     }
 }
@@ -2732,6 +3075,7 @@ int tile_elems(int32_t dtype) { return TILE_BYTES / (dtype == SPEC_F32 ? 4 : 2);
 
 struct WsLayout {
     size_t partials, jobs, chunks, rec, filt, resolve, total;
+    size_t gkey, total_filtered;  // filtered calls: the lane-group maximum keys after it
     size_t NS, NSS, DS, chunk_stride, NCH;
 };
 
@@ -2739,6 +3083,8 @@ struct WsLayout {
 // inverse-CDF chunk totals [B][chunk_stride] | bonus-row chunk records [B][NCH]
 // | top-k / top-p records [B][2k+1] (filtered calls) | the exact draws of up
 // to B listed sequences (resolve.cuh: records, counts, groups, chunk records)
+// | and, when a filtered call's workspace has room, one 4-byte group key per
+// 8 vectors of every tile of every row [B][2k+1][NS * 256]
 WsLayout ws_layout(int32_t B, int32_t k, int32_t V, int32_t dtype)
 {
     WsLayout w;
@@ -2756,6 +3102,8 @@ WsLayout ws_layout(int32_t B, int32_t k, int32_t V, int32_t dtype)
     w.filt = align_up(w.rec + (size_t)B * w.NCH * sizeof(float2), 256);
     w.resolve = align_up(w.filt + (size_t)B * (2 * (size_t)k + 1) * sizeof(FiltRec), 256);
     w.total = w.resolve + resolve_bytes((size_t)B, V, true);
+    w.gkey = align_up(w.total, 256);
+    w.total_filtered = w.gkey + (size_t)B * (2 * (size_t)k + 1) * w.NS * NT * 4;
     return w;
 }
 
@@ -2768,7 +3116,8 @@ size_t ws_bytes(int32_t B, int32_t k, int32_t V, int32_t dtype)
 // with the filter kernels of a filtered call).
 template <int DT, bool FILT>
 int launch_all(const Params &P, const RParams &RP, unsigned int grid1, unsigned int gridf,
-               unsigned int gridr, unsigned int gridrf, cudaStream_t st, void *const *events)
+               unsigned int gridk, unsigned int gridr, unsigned int gridrf, cudaStream_t st,
+               void *const *events)
 {
     // filtered calls record one more event, after the filter kernel
     auto mark = [&](int i) {
@@ -2798,8 +3147,11 @@ int launch_all(const Params &P, const RParams &RP, unsigned int grid1, unsigned 
     stats_kernel<DT><<<grid1, NTHREADS, SMEM_BYTES, st>>>(P);
     mark(0);
     if constexpr (FILT) {
-        // the window kernel cuts most rows in one pass; the radix kernel
-        // finishes the rows it flagged
+        // top-k rows are cut from the group maxima; the window kernel cuts
+        // most other rows in one pass; the radix kernel finishes the rows
+        // either of them flagged
+        if (P.gkey && dependent(kfilter_kernel<DT>, gridk, KF_TH) != cudaSuccess)
+            return SPEC_ECUDA;
         if (dependent(wfilter_kernel<DT>, gridf, WTH, WFILT_SMEM) != cudaSuccess)
             return SPEC_ECUDA;
         if (dependent(filter_kernel<DT>, gridf, FTH, FILT_SMEM) != cudaSuccess)
@@ -2928,6 +3280,9 @@ int launch(const void *target, const void *draft, const int32_t *tokens, const f
     P.top_k = top_k;
     P.top_p = top_p;
     P.filt = reinterpret_cast<FiltRec *>(w + lay.filt);
+    P.gkey = (filtered && ws_size >= lay.total_filtered)
+                 ? reinterpret_cast<unsigned int *>(w + lay.gkey)
+                 : nullptr;
     RParams RP;
     resolve_regions(RP, w + lay.resolve, (size_t)B, V, true);
     RP.hdr = P.hdr;
@@ -2957,11 +3312,16 @@ int launch(const void *target, const void *draft, const int32_t *tokens, const f
     const unsigned int gridr = (unsigned int)(ritems < 3 * n_sms ? ritems : 3 * n_sms);
     const unsigned int gridrf = (unsigned int)((size_t)B < n_sms ? (size_t)B : n_sms);
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    // the group-maximum cut: sixteen CTAs of 128 threads per SM (a full SM;
+    // its 12 KB of shared memory allow it), rows dealt round robin
+    const size_t nrows = (size_t)B * (2 * (size_t)k + 1);
+    const unsigned int gridk = (unsigned int)(nrows < 16 * n_sms ? nrows : 16 * n_sms);
     if (filtered)
-        return (dtype == SPEC_F32) ? launch_all<SPEC_F32, true>(P, RP, grid1, gridf, gridr, gridrf, st, events)
-                                   : launch_all<SPEC_BF16, true>(P, RP, grid1, gridf, gridr, gridrf, st, events);
-    return (dtype == SPEC_F32) ? launch_all<SPEC_F32, false>(P, RP, grid1, 0, gridr, gridrf, st, events)
-                               : launch_all<SPEC_BF16, false>(P, RP, grid1, 0, gridr, gridrf, st, events);
+        return (dtype == SPEC_F32)
+                   ? launch_all<SPEC_F32, true>(P, RP, grid1, gridf, gridk, gridr, gridrf, st, events)
+                   : launch_all<SPEC_BF16, true>(P, RP, grid1, gridf, gridk, gridr, gridrf, st, events);
+    return (dtype == SPEC_F32) ? launch_all<SPEC_F32, false>(P, RP, grid1, 0, 0, gridr, gridrf, st, events)
+                               : launch_all<SPEC_BF16, false>(P, RP, grid1, 0, 0, gridr, gridrf, st, events);
 }
 
 }  // namespace
@@ -3022,6 +3382,13 @@ size_t spec_verify_workspace_size(int32_t B, int32_t k, int32_t V, int32_t dtype
     if (!sizes_ok(B, k, V, dtype))
         return 0;
     return ws_bytes(B, k, V, dtype);
+}
+
+size_t spec_verify_filtered_workspace_size(int32_t B, int32_t k, int32_t V, int32_t dtype)
+{
+    if (!sizes_ok(B, k, V, dtype))
+        return 0;
+    return ws_layout(B, k, V, dtype).total_filtered;
 }
 
 int32_t spec_verify_workspace_reset(void *workspace, size_t workspace_bytes, void *stream)

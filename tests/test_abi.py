@@ -58,6 +58,7 @@ def test_workspace_size(lib, B, k, V, dt, ok):
     n = sv.spec_verify_workspace_size(B, k, V, dt)
     if not ok:
         assert n == 0
+        assert sv.spec_verify_filtered_workspace_size(B, k, V, dt) == 0
         return
     tile = 32768 // (4 if dt == 0 else 2)
     ns = -(-V // tile)          # tiles per row
@@ -75,6 +76,10 @@ def test_workspace_size(lib, B, k, V, dt, ok):
     resolve = up(filt + B * (2 * k + 1) * 16, 256)
     assert n == resolve + up(96 * B, 256) + up(4 * B, 256) + up(32 * 64 * B, 256) + \
         up(32 * rnc * B, 256)
+    # filtered calls with room for the group maxima: one 4-byte key per 8
+    # vectors (256 per 32 KB tile) of every row
+    assert sv.spec_verify_filtered_workspace_size(B, k, V, dt) == \
+        up(n, 256) + B * (2 * k + 1) * ns * 256 * 4
 
 
 def _call(lib, ptrs, B=1, k=1, V=8, dt=0, wsb=1 << 20):

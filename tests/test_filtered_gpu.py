@@ -58,8 +58,16 @@ def run_gpu(case, tokens, top_k, top_p, want_probs=False, ws=None):
     return tuple(x.cpu().numpy() for x in out)
 
 
-def check(case, tokens, top_k, top_p):
-    gt, gn = run_gpu(case, tokens, top_k, top_p)
+def window_ws(case):
+    """A workspace without room for group maxima: every row takes the
+    streaming (window / radix) filter."""
+    dt = sv.SPEC_F32 if case.dtype == synth.F32 else sv.SPEC_BF16
+    need = sv.spec_verify_workspace_size(case.B, case.k, case.V, dt)
+    return torch.zeros(need, dtype=torch.uint8, device="cuda")
+
+
+def check(case, tokens, top_k, top_p, ws=None):
+    gt, gn = run_gpu(case, tokens, top_k, top_p, ws=ws)
     rt, rn, tr = oracle.verify_filtered(case.target, case.draft, tokens, case.u_accept,
                                         case.u_resample, case.temperature, top_k, top_p,
                                         nthreads=NTHREADS)
@@ -83,14 +91,51 @@ PARAMS = {
 }
 
 
+@pytest.mark.parametrize("path", ["group", "window"])
 @pytest.mark.parametrize("params", list(PARAMS))
 @pytest.mark.parametrize("cfg,B", [(2, 12), (3, 8), (4, 8), (5, 24)])
-def test_workloads(cfg, B, params):
+def test_workloads(cfg, B, params, path):
+    """Both cuts of top-k rows: from group maxima (the default workspace of the
+    binding) and by the streaming filter (a workspace without their room)."""
     case = synth.make_config(cfg, B=B)
     top_k, top_p = PARAMS[params](B, np.random.default_rng(cfg))
     tokens = filtered_tokens(case, top_k, top_p, seed=cfg + 17)
-    gn, rn = check(case, tokens, top_k, top_p)
+    gn, rn = check(case, tokens, top_k, top_p, ws=window_ws(case) if path == "window" else None)
     assert np.all(rn[case.temperature > 0] >= 0)  # drawn from the filtered q: no errors
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("V", [37, 1000, 40000])
+def test_group_cut_equals_streaming_cut(dtype, V):
+    """The cut from group maxima and the streaming cut compute the same exact
+    record (fixed-point masses, the same sort and cut), so the outputs are
+    identical; K spans 1 .. 256 (the group cut's limit) and 257 (streaming)."""
+    rng = np.random.default_rng(V)
+    B, k = 24, 3
+    case = synth.gauss_case(B=B, k=k, V=V, dtype=dtype, seed=V + 1, T=(0.6, 1.0, 1.4))
+    top_k = rng.choice([1, 2, 7, 50, 255, 256, 257], B).astype(np.int32)
+    top_k = np.minimum(top_k, V - 1)
+    top_p = rng.choice([1.0, 0.9, 0.5], B).astype(np.float32)
+    tokens = filtered_tokens(case, top_k, top_p, seed=3)
+    g = run_gpu(case, tokens, top_k, top_p)
+    w = run_gpu(case, tokens, top_k, top_p, ws=window_ws(case))
+    assert np.array_equal(g[0], w[0]) and np.array_equal(g[1], w[1])
+    check(case, tokens, top_k, top_p)
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_group_cut_with_massive_ties(dtype):
+    """Integer-valued logits: thousands of tokens share the K-th key, more than
+    the group cut's buffers hold, so the radix kernel finishes those rows."""
+    B, k, V = 6, 2, 40000
+    rng = np.random.default_rng(21)
+    case = synth.gauss_case(B=B, k=k, V=V, dtype=dtype, seed=22, T=(1.0,))
+    for arr in (case.target, case.draft):
+        vals = np.round(rng.normal(0.0, 0.3, arr.shape)).astype(np.float32)  # ~5 % are 1
+        arr[...] = synth.f32_to_bf16_bits(vals) if dtype == "bf16" else vals
+    top_k = np.full(B, 100, np.int32)
+    tokens = filtered_tokens(case, top_k, None, seed=6)
+    check(case, tokens, top_k, None)
 
 
 @pytest.mark.parametrize("dtype", ["f32", "bf16"])
