@@ -202,10 +202,12 @@ size_t spec_verify_filtered_workspace_size(int32_t B, int32_t k, int32_t V, int3
  * bytes the rows with top-k (1 <= K <= 256) are cut from per-group maxima the
  * statistics kernel leaves in the extra room (only the groups that can hold
  * a kept token are read again), otherwise every row takes the streaming
- * filter.  The kernels: statistics; the filter (the group-maximum cut of
- * top-k rows when there is room; one streaming pass over each other row;
- * then the rows neither could cut, by a second pass or a radix search over
- * the order key); accept scan; draw tiles; final search; exact draws.
+ * filter, and those rows' draws come from their kept sets (fp64 weights over
+ * at most K tokens) instead of a pass over the row.  The kernels: statistics;
+ * the filter (the group-maximum cut of top-k rows when there is room; one
+ * streaming pass over each other row; then the rows neither could cut, by a
+ * second pass or a radix search over the order key); accept scan; draw tiles
+ * and the kept-set draws; final search; exact draws.
  */
 int32_t spec_verify_filtered(const void *target_logits, const void *draft_logits,
                              const int32_t *draft_tokens, const float *u_accept,
@@ -217,9 +219,9 @@ int32_t spec_verify_filtered(const void *target_logits, const void *draft_logits
 
 /*
  * spec_verify_filtered with stage events as in spec_verify_timed:
- * SPEC_FILTERED_STAGES of them, after the statistics, the filter (both of
- * its kernels), the accept scan, the draw tiles, the final search and the
- * exact draws.
+ * SPEC_FILTERED_STAGES of them, after the statistics, the filter (all of
+ * its kernels), the accept scan, the draw tiles (with the kept-set draws),
+ * the final search and the exact draws.
  */
 #define SPEC_FILTERED_STAGES 6
 int32_t spec_verify_filtered_timed(const void *target_logits, const void *draft_logits,

@@ -28,7 +28,8 @@ struct WsHeader {
     unsigned int n_slow_kinks;  // exact draws with too many undecided elements (diagnostic)
     unsigned int n_stream_rows; // filtered rows the group-maximum cut left to the streaming filter
     unsigned int n_radix_rows;  // filtered rows left to the radix kernel
-    unsigned int pad[55];
+    unsigned int n_stream_draws;  // filtered draws left to the streaming draw kernel
+    unsigned int pad[54];
 };
 static_assert(sizeof(WsHeader) == 256, "header is 256 bytes");
 

@@ -307,6 +307,7 @@ __global__ void __launch_bounds__(NTHREADS, 2) stats_kernel(const Params P)
             P.hdr->n_slow_kinks = 0u;
             P.hdr->n_stream_rows = 0u;
             P.hdr->n_radix_rows = 0u;
+            P.hdr->n_stream_draws = 0u;
         }
         for (int s = 0; s < STAGES; ++s) {
             mbar_init(&S.full[s], 1);
@@ -2679,7 +2680,13 @@ __global__ void __launch_bounds__(SCAN_WARPS * 32) scan_kernel(const Params P)
                 J.it = riota[warp][j];
                 J.kd = (j < k) ? rkap[warp][k + 1 + j] : J.kt;
                 J.id = (j < k) ? riota[warp][k + 1 + j] : J.it;
+                // top-k rows with group maxima: drawn from the kept sets alone
+                const int K = P.top_k ? __ldg(P.top_k + b) : 0;
+                J.pad0 = (P.gkey && K > 0 && K < V && K <= KF_KMAX) ? 1 : 0;
             }
+            // the draws the streaming draw kernel still has to serve
+            if (lane == 0 && !J.pad0 && (J.mode == DRAW_RESIDUAL || J.filt))
+                atomicAdd(&P.hdr->n_stream_draws, 1u);
         }
     }
     if (lane < JOB_VECS)
@@ -2762,35 +2769,266 @@ __global__ void __launch_bounds__(NT, FILT ? 4 : 6) draw_kernel(const Params P)
 {
     using L = Lg<DT>;
     constexpr int VEC = L::VEC;
-    const int b = (int)(blockIdx.x / (unsigned int)P.DS);
-    const int seg = (int)(blockIdx.x - (unsigned int)b * (unsigned int)P.DS);
     allow_next_kernel();
     wait_previous_kernel();  // the job comes from the scan kernel
-    const JobRec J = load_job(P, b);
-    if (J.mode == DRAW_NONE || (J.mode == DRAW_TARGET && !(FILT && J.filt)))
-        return;  // unfiltered bonus draws use the statistics kernel's chunk records
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    float *out = P.chunks + (size_t)b * P.chunk_stride + (size_t)seg * UD * NCW;
-    uint4 rt[UD], rd[UD];
+    // one draw tile per CTA, or (a grid smaller than the tiles) a stride over
+    // them: when most sequences draw from their kept sets, launching a CTA
+    // per tile costs more than the tiles left
+    const unsigned int items = (unsigned int)P.DS * (unsigned int)P.B;
+    if (FILT && P.gkey && __ldcg(&P.hdr->n_stream_draws) == 0u)
+        return;  // every draw of the call comes from the kept sets
+    for (unsigned int item = blockIdx.x; item < items; item += gridDim.x) {
+        const int b = (int)(item / (unsigned int)P.DS);
+        const int seg = (int)(item - (unsigned int)b * (unsigned int)P.DS);
+        const JobRec J = load_job(P, b);
+        if (J.mode == DRAW_NONE || (J.mode == DRAW_TARGET && !(FILT && J.filt)))
+            continue;  // unfiltered bonus draws use the statistics kernel's chunk records
+        if (FILT && J.pad0)
+            continue;  // drawn from the kept sets (kdraw_kernel)
+        float *out = P.chunks + (size_t)b * P.chunk_stride + (size_t)seg * UD * NCW;
+        uint4 rt[UD], rd[UD];
 #pragma unroll
-    for (int u = 0; u < UD; ++u) {
-        const int v = (seg * UD + u) * NT + warp * 32 + lane;
-        rt[u] = row_vec<DT>(P.target, (size_t)J.t_row, v, P.V);
-        rd[u] = (J.mode == DRAW_RESIDUAL) ? row_vec<DT>(P.draft, (size_t)J.d_row, v, P.V) : rt[u];
+        for (int u = 0; u < UD; ++u) {
+            const int v = (seg * UD + u) * NT + warp * 32 + lane;
+            rt[u] = row_vec<DT>(P.target, (size_t)J.t_row, v, P.V);
+            rd[u] = (J.mode == DRAW_RESIDUAL) ? row_vec<DT>(P.draft, (size_t)J.d_row, v, P.V) : rt[u];
+        }
+        (void)VEC;
+#pragma unroll
+        for (int u = 0; u < UD; ++u) {
+            float w[VEC];
+            draw_weights<DT, FILT>(J, J.mode, rt[u], rd[u], w, ((seg * UD + u) * NT + warp * 32 + lane) * VEC);
+            float tau = 0.0f;
+#pragma unroll
+            for (int j = 0; j < VEC; ++j)
+                tau = tau + w[j];
+            float incl, excl;
+            warp_scan(tau, lane, incl, excl);
+            if (lane == 31)
+                out[u * NCW + warp] = incl;
+        }
     }
-    (void)VEC;
+}
+
+// ------------------------------------------- top-k draws from the kept sets
+//
+// A filtered sequence whose rows have top-k (K <= KF_KMAX) in a call with
+// group maxima draws its correction or bonus token from the kept sets alone:
+// the residual max(0, p~ - q~) and the bonus p~ are zero outside the target's
+// kept set, which holds at most K tokens.  A kept set is gathered through the
+// group maxima as the cut gathers it (the groups whose key is >= kappa; their
+// tokens with key > kappa, or == kappa up to index iota), or, when more
+// groups than the buffer holds reach kappa (ties), by a pass over the row.
+// The weights are computed in fp64 as the fp64 reference computes them:
+// exp((x - m) / T) over each kept set, normalised by its sum; the inverse CDF
+// runs over the target's kept tokens in index order.
+constexpr int KD_TH = 128;
+constexpr int KD_CAP = 512;  // kept tokens at most (K <= KF_KMAX <= KD_CAP)
+static_assert(KF_KMAX <= KD_CAP, "a kept set fits the buffer");
+
+struct KdSmem {
+    int gl[KF_GCAP];                   // groups reaching kappa
+    int tidx[KD_CAP], didx[KD_CAP];    // kept tokens of the target / draft row
+    float tval[KD_CAP], dval[KD_CAP];  // their logits
+    double w[KD_CAP];                  // the target kept tokens' weights
+    int order[KD_CAP];                 // target kept tokens by index
+    double red[KD_TH / 32];
+    unsigned int ng, n;
+};
+
+// The kept set of one row into (oidx, oval); returns its size (every thread).
+template <int DT>
+__device__ int kd_gather(const Params &P, const void *arr, size_t row, const unsigned int *gk,
+                         unsigned int kap, int iota, int *oidx, float *oval, KdSmem &S, int t,
+                         int lane)
+{
+    using L = Lg<DT>;
+    constexpr int VEC = L::VEC;
+    constexpr int VPT = TILE_BYTES / 16;
+    const size_t NG = (size_t)P.NS * NT;
+    const int V = P.V;
+    auto keep = [&](float x, int e) {
+        const unsigned int key = key_of<DT>(x);
+        return key > kap || (key == kap && e <= iota);
+    };
+    if (t == 0) {
+        S.ng = 0u;
+        S.n = 0u;
+    }
+    __syncthreads();
+    // NG is a multiple of the block, so every lane takes each step; KF_LB key
+    // loads in flight per thread
+    for (size_t g0 = 0; g0 < NG; g0 += (size_t)KD_TH * KF_LB) {
+        unsigned int key[KF_LB];
 #pragma unroll
-    for (int u = 0; u < UD; ++u) {
-        float w[VEC];
-        draw_weights<DT, FILT>(J, J.mode, rt[u], rd[u], w, ((seg * UD + u) * NT + warp * 32 + lane) * VEC);
-        float tau = 0.0f;
+        for (int q = 0; q < KF_LB; ++q) {
+            const size_t g = g0 + (size_t)q * KD_TH + t;
+            key[q] = (g < NG) ? __ldcg(gk + g) : 0u;
+        }
 #pragma unroll
-        for (int j = 0; j < VEC; ++j)
-            tau = tau + w[j];
-        float incl, excl;
-        warp_scan(tau, lane, incl, excl);
-        if (lane == 31)
-            out[u * NCW + warp] = incl;
+        for (int q = 0; q < KF_LB; ++q) {
+            if (g0 + (size_t)q * KD_TH < NG) {  // the same in every lane
+                const bool sel = key[q] >= kap;
+                const unsigned int slot = warp_slot(sel, &S.ng, lane);
+                if (sel && slot < (unsigned int)KF_GCAP)
+                    S.gl[slot] = (int)(g0 + (size_t)q * KD_TH + t);
+            }
+        }
+    }
+    __syncthreads();
+    const unsigned int ng = S.ng;
+    if (ng <= (unsigned int)KF_GCAP) {
+        const int nw = (int)ng * U;
+        const bool aligned = ((row * (size_t)V) % VEC) == 0;
+        for (int w0 = 0; w0 < nw; w0 += KD_TH) {  // every lane takes each step
+            const int w = w0 + t;
+            int v = -1;
+            if (w < nw) {
+                const int g = S.gl[w / U], u = w - (w / U) * U;
+                const int seg = g / NT, gw = (g % NT) / 32, gl = g % 32;
+                v = seg * VPT + 256 * gw + 32 * u + gl;
+            }
+            float x[VEC];
+            if (v >= 0 && aligned && (v + 1) * VEC <= V) {
+                L::unpack(__ldg(reinterpret_cast<const uint4 *>(arr) + (row * (size_t)V) / VEC + v),
+                          x);
+            } else {
+#pragma unroll
+                for (int j = 0; j < VEC; ++j) {
+                    const int e = v * VEC + j;
+                    x[j] = (v >= 0 && e < V) ? L::load1(arr, row * (size_t)V + e) : -INFINITY;
+                }
+            }
+#pragma unroll
+            for (int j = 0; j < VEC; ++j) {
+                const int e = v * VEC + j;
+                const bool want = v >= 0 && e < V && keep(x[j], e);
+                const unsigned int slot = warp_slot(want, &S.n, lane);
+                if (want && slot < (unsigned int)KD_CAP) {
+                    oidx[slot] = e;
+                    oval[slot] = x[j];
+                }
+            }
+        }
+    } else {
+        for (int e0 = 0; e0 < V; e0 += KD_TH) {  // every lane takes each step
+            const int e = e0 + t;
+            const float x = (e < V) ? L::load1(arr, row * (size_t)V + e) : -INFINITY;
+            const bool want = e < V && keep(x, e);
+            const unsigned int slot = warp_slot(want, &S.n, lane);
+            if (want && slot < (unsigned int)KD_CAP) {
+                oidx[slot] = e;
+                oval[slot] = x;
+            }
+        }
+    }
+    __syncthreads();
+    const int n = min((int)S.n, KD_CAP);
+    __syncthreads();
+    return n;
+}
+
+// Block-wide sum of one double per thread, in a fixed order (every thread).
+__device__ __forceinline__ double kd_sum(double x, KdSmem &S, int t, int lane)
+{
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1)
+        x += __shfl_xor_sync(0xffffffffu, x, o);
+    if (lane == 0)
+        S.red[t >> 5] = x;
+    __syncthreads();
+    double s = 0.0;
+    for (int w = 0; w < KD_TH / 32; ++w)
+        s += S.red[w];
+    __syncthreads();
+    return s;
+}
+
+template <int DT>
+__global__ void __launch_bounds__(KD_TH) kdraw_kernel(const Params P)
+{
+    using L = Lg<DT>;
+    __shared__ KdSmem S;
+    const int b = blockIdx.x;
+    const int t = threadIdx.x, lane = t & 31;
+    allow_next_kernel();
+    wait_previous_kernel();  // the jobs come from the scan kernel (before the draw kernel)
+    if (b >= P.B)
+        return;
+    const JobRec J = load_job(P, b);
+    if (J.mode == DRAW_NONE || !J.filt || !J.pad0)
+        return;
+    const int k = P.k;
+    const size_t NG = (size_t)P.NS * NT;
+    const double T = (double)__ldg(P.temperature + b);
+    const bool resid = J.mode == DRAW_RESIDUAL;
+    // the target's kept set at row j (its bonus row when j == k)
+    const unsigned int *gkt = P.gkey + ((size_t)b * P.rows + J.j) * NG;
+    const int nt = kd_gather<DT>(P, P.target, (size_t)J.t_row, gkt, J.kt, J.it, S.tidx, S.tval,
+                                 S, t, lane);
+    double zd = 1.0;
+    int nd = 0;
+    if (resid) {
+        const unsigned int *gkd = P.gkey + ((size_t)b * P.rows + k + 1 + J.j) * NG;
+        nd = kd_gather<DT>(P, P.draft, (size_t)J.d_row, gkd, J.kd, J.id, S.didx, S.dval, S, t,
+                           lane);
+        double z = 0.0;
+        for (int i = t; i < nd; i += KD_TH)
+            z += exp(((double)S.dval[i] - (double)J.md) / T);
+        zd = kd_sum(z, S, t, lane);
+    }
+    double zt = 0.0;
+    for (int i = t; i < nt; i += KD_TH)
+        zt += exp(((double)S.tval[i] - (double)J.mt) / T);
+    zt = kd_sum(zt, S, t, lane);
+    // weights of the target's kept tokens, and their order by index
+    double r = 0.0;
+    for (int i = t; i < nt; i += KD_TH) {
+        const int x = S.tidx[i];
+        const double p = exp(((double)S.tval[i] - (double)J.mt) / T) / zt;
+        double q = 0.0;
+        if (resid) {
+            const float dx = L::load1(P.draft, (size_t)J.d_row * P.V + x);
+            const unsigned int key = key_of<DT>(dx);
+            if (key > J.kd || (key == J.kd && x <= J.id))
+                q = exp(((double)dx - (double)J.md) / T) / zd;
+        }
+        const double w = resid ? fmax(p - q, 0.0) : p;
+        S.w[i] = w;
+        r += w;
+        int rank = 0;
+        for (int q2 = 0; q2 < nt; ++q2)
+            rank += S.tidx[q2] < x ? 1 : 0;
+        S.order[rank] = i;
+    }
+    const double R = kd_sum(r, S, t, lane);
+    if (!(R > 0.0)) {
+        // the residual vanished by rounding alone: draw from p~ instead
+        for (int i = t; i < nt; i += KD_TH)
+            S.w[i] = exp(((double)S.tval[i] - (double)J.mt) / T) / zt;
+        __syncthreads();
+    }
+    if (t == 0) {
+        double tot = 0.0;
+        for (int q2 = 0; q2 < nt; ++q2)
+            tot += S.w[S.order[q2]];
+        const double target = (double)J.u * tot;
+        double c = 0.0;
+        int tok = -1, last = -1;
+        for (int q2 = 0; q2 < nt; ++q2) {
+            const int i = S.order[q2];
+            if (S.w[i] > 0.0)
+                last = S.tidx[i];
+            c += S.w[i];
+            if (c > target && S.w[i] > 0.0) {
+                tok = S.tidx[i];
+                break;
+            }
+        }
+        if (tok < 0)
+            tok = last;  // rounding left u * R at the total: the last positive weight
+        P.out_tokens[(size_t)b * (k + 1) + J.j] = tok;
     }
 }
 
@@ -3002,6 +3240,16 @@ __global__ void __launch_bounds__(SCAN_WARPS * 32) final_kernel(const Params P)
     if (J.mode == DRAW_NONE)
         return;
     const int k = P.k;
+    if (FILT && J.pad0) {
+        // drawn from the kept sets: kdraw_kernel wrote out_tokens[b][j]
+        for (int i = lane; i <= k; i += 32)
+            if (i != J.j)
+                P.out_tokens[(size_t)b * (k + 1) + i] =
+                    (i < J.j) ? __ldg(P.tokens + (size_t)b * k + i) : -1;
+        if (lane == 0)
+            P.out_num_accepted[b] = J.j;
+        return;
+    }
     const int nblk = P.DS * UD;
     float *ch = P.chunks + (size_t)b * P.chunk_stride;
     int tok;
@@ -3116,8 +3364,8 @@ size_t ws_bytes(int32_t B, int32_t k, int32_t V, int32_t dtype)
 // with the filter kernels of a filtered call).
 template <int DT, bool FILT>
 int launch_all(const Params &P, const RParams &RP, unsigned int grid1, unsigned int gridf,
-               unsigned int gridk, unsigned int gridr, unsigned int gridrf, cudaStream_t st,
-               void *const *events)
+               unsigned int gridk, unsigned int gridk_draw, unsigned int gridr,
+               unsigned int gridrf, cudaStream_t st, void *const *events)
 {
     // filtered calls record one more event, after the filter kernel
     auto mark = [&](int i) {
@@ -3163,8 +3411,14 @@ int launch_all(const Params &P, const RParams &RP, unsigned int grid1, unsigned 
     if (dependent(scan_kernel<DT, FILT>, gs, SCAN_WARPS * 32) != cudaSuccess)
         return SPEC_ECUDA;
     mark(1);
-    if (dependent(draw_kernel<DT, FILT>, (unsigned int)P.DS * (unsigned int)P.B, NT) != cudaSuccess)
+    const unsigned int draw_tiles = (unsigned int)P.DS * (unsigned int)P.B;
+    const unsigned int gridd = (FILT && P.gkey && draw_tiles > gridk_draw) ? gridk_draw : draw_tiles;
+    if (dependent(draw_kernel<DT, FILT>, gridd, NT) != cudaSuccess)
         return SPEC_ECUDA;
+    if constexpr (FILT) {
+        if (P.gkey && dependent(kdraw_kernel<DT>, (unsigned int)P.B, KD_TH) != cudaSuccess)
+            return SPEC_ECUDA;
+    }
     mark(2);
     if (dependent(final_kernel<DT, FILT>, gs, SCAN_WARPS * 32) != cudaSuccess)
         return SPEC_ECUDA;
@@ -3316,12 +3570,18 @@ int launch(const void *target, const void *draft, const int32_t *tokens, const f
     // its 12 KB of shared memory allow it), rows dealt round robin
     const size_t nrows = (size_t)B * (2 * (size_t)k + 1);
     const unsigned int gridk = (unsigned int)(nrows < 16 * n_sms ? nrows : 16 * n_sms);
+    // with kept-set draws, the draw kernel strides over its tiles with the
+    // CTAs that fit at once (four per SM)
+    const unsigned int gridk_draw = (unsigned int)(4 * n_sms);
     if (filtered)
         return (dtype == SPEC_F32)
-                   ? launch_all<SPEC_F32, true>(P, RP, grid1, gridf, gridk, gridr, gridrf, st, events)
-                   : launch_all<SPEC_BF16, true>(P, RP, grid1, gridf, gridk, gridr, gridrf, st, events);
-    return (dtype == SPEC_F32) ? launch_all<SPEC_F32, false>(P, RP, grid1, 0, 0, gridr, gridrf, st, events)
-                               : launch_all<SPEC_BF16, false>(P, RP, grid1, 0, 0, gridr, gridrf, st, events);
+                   ? launch_all<SPEC_F32, true>(P, RP, grid1, gridf, gridk, gridk_draw, gridr, gridrf,
+                                                st, events)
+                   : launch_all<SPEC_BF16, true>(P, RP, grid1, gridf, gridk, gridk_draw, gridr, gridrf,
+                                                 st, events);
+    return (dtype == SPEC_F32)
+               ? launch_all<SPEC_F32, false>(P, RP, grid1, 0, 0, 0, gridr, gridrf, st, events)
+               : launch_all<SPEC_BF16, false>(P, RP, grid1, 0, 0, 0, gridr, gridrf, st, events);
 }
 
 }  // namespace
