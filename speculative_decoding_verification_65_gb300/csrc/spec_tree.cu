@@ -24,6 +24,12 @@
 // running total takes the range's last positive weight, the clamp the
 // method's draw already has for the whole row.
 //
+// The statistics and residual passes stream each warp segment with every
+// thread keeping three vectors of each row in flight by cp.async into shared
+// memory slots only it reads (no barrier; the copies are waited for with
+// cp.async.wait_group, no spin).  CTA x walks the x-th sampled sequence, then
+// the greedy ones, so the longer walks start first.
+//
 // Rows start anywhere: vector a of a row covers the 16-byte-aligned elements
 // [A0 + a VEC, A0 + (a+1) VEC) of the array, A0 the row's first element
 // rounded down to a multiple of VEC; the elements outside the row read as
@@ -33,6 +39,8 @@
 #include <limits.h>
 #include <math.h>
 #include <stdint.h>
+
+#include <atomic>
 
 #include "spec_tree.h"
 #include "spec_verify.h"
@@ -85,6 +93,19 @@ __device__ __forceinline__ uint4 tvec(const void *arr, size_t off, int V, size_t
     return r;
 }
 
+constexpr int STG = 3;  // vectors of each row in flight per thread (cp.async stages;
+                        // 4 and 6 measured slower: their shared memory costs occupancy)
+constexpr size_t RING_BYTES = (size_t)STG * 2 * TTH * 16;  // dynamic shared memory
+
+__device__ __forceinline__ void cp16(void *dst, const void *src)
+{
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_addr(dst)), "l"(src)
+                 : "memory");
+}
+__device__ __forceinline__ void cp_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory"); }
+
 struct Span {
     size_t off, A0;
     int s0, s1;  // this warp's vectors [s0, s1)
@@ -102,6 +123,91 @@ __device__ __forceinline__ Span span_of(size_t off, int V, int seg)
     s.s0 = min(nvv, seg * per);
     s.s1 = min(nvv, s.s0 + per);
     return s;
+}
+
+// Vectors a, a + 32, ... of a warp segment of one or two rows, each thread
+// keeping STG of them in flight with cp.async into slots only it reads (no
+// barrier needed; a warp's lanes use consecutive 16 bytes of a slot row, so
+// the reads are free of bank conflicts).  Vectors not wholly inside the row
+// are read element by element when used.
+template <int DT, bool TWO>
+struct Stream {
+    const void *arr0, *arr1;
+    size_t off, A0;
+    int V, s1;
+    uint8_t *ring;
+    int tid;
+    __device__ __forceinline__ bool full(int a) const
+    {
+        using L = Lg<DT>;
+        const size_t e0 = A0 + (size_t)a * L::VEC;
+        return e0 >= off && e0 + L::VEC <= off + (size_t)V;
+    }
+    __device__ __forceinline__ uint8_t *slot(int q, int r) const
+    {
+        return ring + ((size_t)(q * 2 + r) * TTH + tid) * 16;
+    }
+    __device__ __forceinline__ void issue(int a, int q) const
+    {
+        using L = Lg<DT>;
+        if (a < s1 && full(a)) {
+            const size_t vi = (A0 + (size_t)a * L::VEC) / L::VEC;
+            cp16(slot(q, 0), reinterpret_cast<const uint4 *>(arr0) + vi);
+            if (TWO)
+                cp16(slot(q, 1), reinterpret_cast<const uint4 *>(arr1) + vi);
+        }
+        cp_commit();
+    }
+    __device__ __forceinline__ void get(int a, int q, uint4 &x0, uint4 &x1) const
+    {
+        if (full(a)) {
+            x0 = ld_shared_v4(slot(q, 0));
+            if (TWO)
+                x1 = ld_shared_v4(slot(q, 1));
+        } else {
+            x0 = tvec<DT>(arr0, off, V, A0, a);
+            if (TWO)
+                x1 = tvec<DT>(arr1, off, V, A0, a);
+        }
+    }
+};
+
+// Streams a warp segment through Stream, calling fn(a, x0, x1) per vector.
+template <int DT, bool TWO, typename F>
+__device__ __forceinline__ void stream_segment(const Stream<DT, TWO> &st, int s0, int lane, F fn)
+{
+    const int a0 = s0 + lane;
+#pragma unroll
+    for (int q = 0; q < STG - 1; ++q)
+        st.issue(a0 + 32 * q, q);
+    int q = 0;
+    for (int a = a0; a < st.s1; a += 32) {
+        st.issue(a + 32 * (STG - 1), (q + STG - 1) % STG);
+        cp_wait<STG - 1>();
+        uint4 x0, x1 = x0;
+        st.get(a, q, x0, x1);
+        fn(a, x0, x1);
+        q = (q + 1 == STG) ? 0 : q + 1;
+    }
+    cp_wait<0>();
+}
+
+template <int DT>
+__device__ __forceinline__ void online1(const uint4 &x0, float c, unsigned long long c2, float &m,
+                                        float &s, bool &bad)
+{
+    using L = Lg<DT>;
+    const float vm = L::vmax(x0);
+    bad |= !(vm < INFINITY);
+    if (vm > m) {
+        s = rescale(s, m, vm, c);
+        m = vm;
+    }
+    if (m > -INFINITY) {
+        float lo, hi;
+        f2_split(L::expsum2(x0, -m, c2), lo, hi);
+        s += lo + hi;
+    }
 }
 
 // One online softmax partial (m, s) over a vector pair.
@@ -148,25 +254,18 @@ __device__ __forceinline__ void block_ms(float &m, float &s, float c, float *rm,
 // Returns true (every thread) if a row read holds NaN or +inf or is all -inf.
 template <int DT, bool TWO>
 __device__ bool row_stats(const TParams &P, size_t off, float c, TSmem &S, int warp, int lane,
-                          float &mt, float &zt, float &md, float &zd)
+                          float &mt, float &zt, float &md, float &zd, uint8_t *ring)
 {
     const Span sp = span_of<DT>(off, P.V, warp);
     const unsigned long long c2 = f2(c, c);
-    const uint4 ninf = neg_inf_vec(Lg<DT>::NEG_INF_WORD);
     float m0 = -INFINITY, s0 = 0.0f, m1 = -INFINITY, s1 = 0.0f;
     bool bad = false;
-    // two vectors of each row per step (software prefetch of the next step
-    // measured slower: the registers it takes cost resident warps)
-    auto ld = [&](const void *arr, int a) {
-        return a < sp.s1 ? tvec<DT>(arr, off, P.V, sp.A0, a) : ninf;
-    };
-    for (int a = sp.s0 + lane; a < sp.s1; a += 64) {
-        const uint4 t0 = ld(P.target, a), t1 = ld(P.target, a + 32);
-        const uint4 d0 = TWO ? ld(P.draft, a) : ninf, d1 = TWO ? ld(P.draft, a + 32) : ninf;
-        online2<DT>(t0, t1, c, c2, m0, s0, bad);
+    const Stream<DT, TWO> st{P.target, P.draft, off, sp.A0, P.V, sp.s1, ring, (int)threadIdx.x};
+    stream_segment<DT, TWO>(st, sp.s0, lane, [&](int, const uint4 &t0, const uint4 &d0) {
+        online1<DT>(t0, c, c2, m0, s0, bad);
         if (TWO)
-            online2<DT>(d0, d1, c, c2, m1, s1, bad);
-    }
+            online1<DT>(d0, c, c2, m1, s1, bad);
+    });
     bad = __syncthreads_or(bad) != 0;
     block_ms(m0, s0, c, S.red_m, S.red_s, warp, lane);
     if (TWO)
@@ -257,27 +356,26 @@ __device__ __forceinline__ void weights(const uint4 &t, const uint4 &d, const Wt
 // (sum of the segment totals in segment order), the same in every thread.
 template <int DT>
 __device__ float residual_pass(const TParams &P, size_t off, const Wt &w, TSmem &S, int warp,
-                               int lane)
+                               int lane, uint8_t *ring)
 {
     using L = Lg<DT>;
     const Span sp = span_of<DT>(off, P.V, warp);
-    const uint4 ninf = neg_inf_vec(L::NEG_INF_WORD);
-    const bool with_d = w.C > 0.0f;
     float acc = 0.0f;
-    auto ld = [&](const void *arr, int a) {
-        return a < sp.s1 ? tvec<DT>(arr, off, P.V, sp.A0, a) : ninf;
-    };
-    for (int a = sp.s0 + lane; a < sp.s1; a += 64) {
-        const uint4 t0 = ld(P.target, a), t1 = ld(P.target, a + 32);
-        const uint4 d0 = with_d ? ld(P.draft, a) : ninf, d1 = with_d ? ld(P.draft, a + 32) : ninf;
-        float x0[L::VEC], x1[L::VEC];
+    auto add = [&](int, const uint4 &t0, const uint4 &d0) {
+        float x0[L::VEC];
         weights<DT>(t0, d0, w, x0);
-        weights<DT>(t1, d1, w, x1);
         float v = 0.0f;
 #pragma unroll
         for (int j = 0; j < L::VEC; ++j)
-            v += x0[j] + x1[j];
+            v += x0[j];
         acc += v;
+    };
+    if (w.C > 0.0f) {  // residual weights read both rows
+        const Stream<DT, true> st{P.target, P.draft, off, sp.A0, P.V, sp.s1, ring, (int)threadIdx.x};
+        stream_segment<DT, true>(st, sp.s0, lane, add);
+    } else {
+        const Stream<DT, false> st{P.target, P.draft, off, sp.A0, P.V, sp.s1, ring, (int)threadIdx.x};
+        stream_segment<DT, false>(st, sp.s0, lane, add);
     }
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1)
@@ -427,12 +525,64 @@ __device__ int draw_from(const TParams &P, size_t off, const Wt &w, float R, flo
     return x;
 }
 
+// The sequence CTA x walks: the sampled sequences (T != 0) first, in index
+// order, then the greedy ones.  CTAs start roughly in index order, and a
+// sampled walk reads two rows per node and a residual per rejection where a
+// greedy walk reads one row, so the longer walks start first and the shorter
+// ones fill the tail (longest first).  Batches above ORDER_MAX keep the
+// identity order (the prefix count would cost more than it saves).
+constexpr int ORDER_MAX = 16384;
+
+__device__ int walk_order(const TParams &P, TSmem &S, int tid, int warp, int lane)
+{
+    const int x = blockIdx.x, nb = (int)gridDim.x;
+    if (nb > ORDER_MAX)
+        return x;
+    // block-wide count of the sequences matching `sampled` in [c0, c0 + TTH)
+    auto count = [&](int c0, bool sampled, int &excl) -> int {
+        const int i = c0 + tid;
+        const bool m = i < nb && ((P.temperature[i] != 0.0f) == sampled);
+        const unsigned int bm = __ballot_sync(0xffffffffu, m);
+        if (lane == 0)
+            S.red_i[warp] = __popc(bm);
+        __syncthreads();
+        int before = 0, tot = 0;
+        for (int w = 0; w < TW; ++w) {
+            before += (w < warp) ? S.red_i[w] : 0;
+            tot += S.red_i[w];
+        }
+        __syncthreads();
+        excl = before + __popc(bm & ((1u << lane) - 1u));
+        return tot;
+    };
+    int ns = 0, ex;
+    for (int c0 = 0; c0 < nb; c0 += TTH)
+        ns += count(c0, true, ex);
+    const bool sampled = x < ns;
+    const int rank = sampled ? x : x - ns;
+    int base = 0;
+    for (int c0 = 0; c0 < nb; c0 += TTH) {
+        const int tot = count(c0, sampled, ex);
+        const int i = c0 + tid;
+        if (i < nb && ((P.temperature[i] != 0.0f) == sampled) && base + ex == rank)
+            S.pick = i;
+        base += tot;
+        if (base > rank)
+            break;  // the same in every thread
+    }
+    __syncthreads();
+    const int b = S.pick;
+    __syncthreads();
+    return b;
+}
+
 template <int DT>
 __global__ void __launch_bounds__(TTH, 2) tree_kernel(const TParams P)
 {
     __shared__ TSmem S;
-    const int b = blockIdx.x;
+    extern __shared__ __align__(16) uint8_t ring[];
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int b = walk_order(P, S, tid, warp, lane);
     const int N = P.N, V = P.V;
     const float T = P.temperature[b];
     const bool greedy = (T == 0.0f);
@@ -496,8 +646,9 @@ __global__ void __launch_bounds__(TTH, 2) tree_kernel(const TParams P)
             }
         } else {
             float mt, zt, md = 0.0f, zd = 1.0f;
-            const bool rowbad = (nk > 0) ? row_stats<DT, true>(P, off, c, S, warp, lane, mt, zt, md, zd)
-                                         : row_stats<DT, false>(P, off, c, S, warp, lane, mt, zt, md, zd);
+            const bool rowbad =
+                (nk > 0) ? row_stats<DT, true>(P, off, c, S, warp, lane, mt, zt, md, zd, ring)
+                         : row_stats<DT, false>(P, off, c, S, warp, lane, mt, zt, md, zd, ring);
             if (rowbad) {
                 err = true;
                 break;
@@ -533,7 +684,7 @@ __global__ void __launch_bounds__(TTH, 2) tree_kernel(const TParams P)
                     break;
                 }
                 w.C += M;
-                M = residual_pass<DT>(P, off, w, S, warp, lane);
+                M = residual_pass<DT>(P, off, w, S, warp, lane, ring);
                 R = M;
                 fresh = true;
                 if (!(M > 0.0f)) {  // rounding only: draw from p_c
@@ -588,6 +739,8 @@ __global__ void __launch_bounds__(TTH, 2) tree_kernel(const TParams P)
         P.out_n[b] = err ? -1 : depth;
 }
 
+std::atomic<bool> g_attr[64][2];  // the kernel's shared-memory limit raised, per device and dtype
+
 bool aligned(const void *p, uintptr_t a)
 {
     return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0;
@@ -632,10 +785,25 @@ int32_t spec_verify_tree(const void *target_logits, const void *draft_logits,
     P.N = N;
     P.V = V;
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    // the per-thread cp.async slots take the kernel above the 48 KB of shared
+    // memory a launch gets by default: raised once per device and dtype
+    // (published with release order; racing threads repeat the same call)
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64)
+        return SPEC_ECUDA;
+    const int di = (dtype == SPEC_F32) ? 0 : 1;
+    if (!g_attr[dev][di].load(std::memory_order_acquire)) {
+        const void *fn = (dtype == SPEC_F32) ? (const void *)tree_kernel<SPEC_F32>
+                                             : (const void *)tree_kernel<SPEC_BF16>;
+        if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 (int)RING_BYTES) != cudaSuccess)
+            return SPEC_ECUDA;
+        g_attr[dev][di].store(true, std::memory_order_release);
+    }
     if (dtype == SPEC_F32)
-        tree_kernel<SPEC_F32><<<(unsigned int)B, TTH, 0, st>>>(P);
+        tree_kernel<SPEC_F32><<<(unsigned int)B, TTH, RING_BYTES, st>>>(P);
     else
-        tree_kernel<SPEC_BF16><<<(unsigned int)B, TTH, 0, st>>>(P);
+        tree_kernel<SPEC_BF16><<<(unsigned int)B, TTH, RING_BYTES, st>>>(P);
     if (cudaPeekAtLastError() != cudaSuccess) {
         (void)cudaGetLastError();
         return SPEC_ECUDA;
