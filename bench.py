@@ -847,7 +847,8 @@ def run_ours_filtered(args):
                          "unit": "GB/s", "frac": stream_achieved / peak,
                          "algorithmic_bytes_per_launch": filt_bytes,
                          "traffic": recorded_traffic(
-                             f"{workload}_top{args.top_k}_p{args.top_p}", "wfilter_kernel")},
+                             f"{workload}_top{args.top_k}_p{args.top_p}_streaming",
+                             "wfilter_kernel")},
             "clocks": stream_clk},
         "clocks": clocks,
         "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d,
