@@ -529,9 +529,10 @@ __device__ int draw_from(const TParams &P, size_t off, const Wt &w, float R, flo
 // order, then the greedy ones.  CTAs start roughly in index order, and a
 // sampled walk reads two rows per node and a residual per rejection where a
 // greedy walk reads one row, so the longer walks start first and the shorter
-// ones fill the tail (longest first).  Batches above ORDER_MAX keep the
-// identity order (the prefix count would cost more than it saves).
-constexpr int ORDER_MAX = 16384;
+// ones fill the tail (longest first).  Every CTA reads the batch's
+// temperatures, so the order costs O(B^2) loads in all: batches above
+// ORDER_MAX keep the index order.
+constexpr int ORDER_MAX = 2048;
 
 __device__ int walk_order(const TParams &P, TSmem &S, int tid, int warp, int lane)
 {

@@ -183,4 +183,4 @@ def test_concurrent_first_calls_from_host_threads(tmp_path):
                                               nthreads=NTHREADS)
             check_invariants(c, out[0], out[1])
             rep = compare(c, out[0], out[1], rt, rn, tr)
-            assert rep["exempt"] <= max(1, rep["decisions"] // 1000), rep
+            check_bound(rep)  # grid inputs: the logits are exact in fp32

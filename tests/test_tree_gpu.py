@@ -178,3 +178,12 @@ def test_exempt_rate_below_bound():
         seed += 1
     print(f"{total} decisions over {seed} batches, {exempt} exempt")
     assert exempt <= MAX_EXEMPT_FRACTION * total
+
+
+def test_many_small_trees_past_the_order_limit():
+    """2049 trees (one more than the kernel orders by temperature; past it
+    CTAs keep their index order) of a 2-1 tree over V = 16, greedy and
+    sampled, against the oracle."""
+    p = dict(B=2049, V=16, dtype=synth.F32, branching=(2, 1), recipe="gauss", sigma_d=1.5,
+             sigma_n=0.8, temps=(0.0, 1.0), ragged=True)
+    check(synth.make_tree_case(p, seed=123), allowance=2)
