@@ -1498,8 +1498,9 @@ __global__ void __launch_bounds__(FTH, 2) filter_kernel(const Params P)
 // row's K-th largest logit (K groups have a maximum >= tau, each of them a
 // logit >= tau), so every kept token lies in a group whose key is >= tau.
 // Only those groups are read again: their logits with key >= tau are
-// gathered, sorted by (key desc, index asc), and the cut is read off the
-// sorted list exactly as the window kernel reads it off its sorted window
+// gathered, ordered by (key desc, index asc) -- each token's rank is the
+// number of larger keys -- and the cut is read off that order exactly as the
+// window kernel reads it off its sorted window
 // (top-k mass, then the top-p end by the fixed-point masses).  tau is found
 // by a radix search over the row's group keys, 8 bits per pass (two passes
 // for bf16 keys, whose low 16 bits are zero).  A row with more selected
@@ -1508,10 +1509,11 @@ __global__ void __launch_bounds__(FTH, 2) filter_kernel(const Params P)
 constexpr int KF_TH = 128;
 constexpr int KF_KMAX = 256;
 constexpr int KF_GCAP = 512;   // selected groups at most
-constexpr int KF_CAP = 512;    // gathered tokens at most (the sort's size)
+constexpr int KF_CAP = 512;    // gathered tokens at most
 constexpr int KF_LB = 8;       // group-key loads in flight per thread
-static_assert(KF_KMAX <= KF_CAP && (KF_CAP & (KF_CAP - 1)) == 0,
-              "the kept set fits the buffer, whose size the sort pads to");
+constexpr int KF_GB = 1;       // row vectors in flight per thread while gathering
+static_assert(KF_KMAX <= KF_CAP && KF_CAP <= KF_GCAP,
+              "the kept set fits the buffer, and the group list holds its order");
 
 // The rows the group-maximum cut takes (the same test in the window kernel).
 __device__ __forceinline__ bool kf_row(const Params &P, float T, int K, float Pp)
@@ -1522,8 +1524,8 @@ __device__ __forceinline__ bool kf_row(const Params &P, float T, int K, float Pp
 }
 
 struct KfSmem {
-    unsigned long long key[KF_CAP], mass[KF_CAP];  // gathered tokens, sorted padded to 2^n
-    int glist[KF_GCAP];
+    unsigned long long key[KF_CAP], mass[KF_CAP];  // gathered tokens, in gathering order
+    int glist[KF_GCAP];                            // selected groups, then the tokens' order
     unsigned int hist[256];
     unsigned int ng, nc;
     unsigned int sel, need;
@@ -1669,9 +1671,11 @@ __global__ void __launch_bounds__(KF_TH) kfilter_kernel(const Params P)
             __syncthreads();
             for_keys([&](size_t g, unsigned int key) {
                 const bool sel = key >= tau;
-                const unsigned int slot = warp_slot(sel, &S.ng, lane);
-                if (sel && slot < (unsigned int)KF_GCAP)
-                    S.glist[slot] = (int)g;
+                if (__ballot_sync(0xffffffffu, sel)) {  // most steps select nothing
+                    const unsigned int slot = warp_slot(sel, &S.ng, lane);
+                    if (sel && slot < (unsigned int)KF_GCAP)
+                        S.glist[slot] = (int)g;
+                }
             });
             __syncthreads();
             const unsigned int ng = S.ng;
@@ -1685,34 +1689,72 @@ __global__ void __launch_bounds__(KF_TH) kfilter_kernel(const Params P)
                 // the row's vectors are 16-byte aligned in memory when its first
                 // element is (the array base is)
                 const bool aligned = ((row * (size_t)V) % VEC) == 0;
-                for (int w0 = 0; w0 < nw; w0 += KF_TH) {  // every lane takes each step
-                    const int w = w0 + t;
-                    int v = -1;
-                    if (w < nw) {
-                        const int g = S.glist[w / U], u = w - (w / U) * U;
-                        const int seg = g / NT, gw = (g % NT) / 32, gl = g % 32;
-                        v = seg * VPT + 256 * gw + 32 * u + gl;  // the group lane's vector u
+                const uint4 *rv = reinterpret_cast<const uint4 *>(arr) + (row * (size_t)V) / VEC;
+                // KF_GB vectors a thread in flight; every lane takes each step
+                for (int w0 = 0; w0 < nw; w0 += KF_TH * KF_GB) {
+                    int vv[KF_GB];
+                    uint4 raw[KF_GB];
+#pragma unroll
+                    for (int q = 0; q < KF_GB; ++q) {
+                        const int w = w0 + q * KF_TH + t;
+                        int v = -1;
+                        if (w < nw) {
+                            const int g = S.glist[w / U], u = w - (w / U) * U;
+                            const int seg = g / NT, gw = (g % NT) / 32, gl = g % 32;
+                            v = seg * VPT + 256 * gw + 32 * u + gl;  // the group lane's vector u
+                        }
+                        vv[q] = v;
+                        if (v >= 0 && aligned && (v + 1) * VEC <= V)
+                            raw[q] = __ldg(rv + v);
                     }
-                    float x[VEC];
-                    if (v >= 0 && aligned && (v + 1) * VEC <= V) {
-                        L::unpack(__ldg(reinterpret_cast<const uint4 *>(arr) +
-                                        (row * (size_t)V) / VEC + v), x);
-                    } else {
+#pragma unroll
+                    for (int q = 0; q < KF_GB; ++q) {
+                        if (w0 + q * KF_TH >= nw)
+                            break;  // the same in every lane
+                        const int v = vv[q];
+                        float x[VEC];
+                        if (v >= 0 && aligned && (v + 1) * VEC <= V) {
+                            L::unpack(raw[q], x);
+                        } else {
+#pragma unroll
+                            for (int j = 0; j < VEC; ++j) {
+                                const int e = v * VEC + j;
+                                x[j] = (v >= 0 && e < V) ? L::load1(arr, row * (size_t)V + e)
+                                                         : -INFINITY;
+                            }
+                        }
+                        // the lane's tokens >= tau, then one range of slots per lane:
+                        // a warp scan of the counts and one shared atomic
+                        unsigned int mask = 0u;
 #pragma unroll
                         for (int j = 0; j < VEC; ++j) {
                             const int e = v * VEC + j;
-                            x[j] = (v >= 0 && e < V) ? L::load1(arr, row * (size_t)V + e)
-                                                     : -INFINITY;
+                            if (v >= 0 && e < V && key_of<DT>(x[j]) >= tau)
+                                mask |= 1u << j;
                         }
-                    }
+                        const unsigned int cnt = (unsigned int)__popc(mask);
+                        if (__ballot_sync(0xffffffffu, cnt != 0u)) {
+                            unsigned int incl = cnt;
 #pragma unroll
-                    for (int j = 0; j < VEC; ++j) {
-                        const int e = v * VEC + j;
-                        const bool want = v >= 0 && e < V && key_of<DT>(x[j]) >= tau;
-                        const unsigned int slot = warp_slot(want, &S.nc, lane);
-                        if (want && slot < (unsigned int)KF_CAP) {
-                            S.key[slot] = sortkey(key_of<DT>(x[j]), e);
-                            S.mass[slot] = fixmass(x[j], m, c);
+                            for (int o = 1; o < 32; o <<= 1) {
+                                const unsigned int y = __shfl_up_sync(0xffffffffu, incl, o);
+                                if (lane >= o)
+                                    incl += y;
+                            }
+                            unsigned int base = 0u;
+                            if (lane == 31)
+                                base = atomicAdd(&S.nc, incl);
+                            unsigned int slot = __shfl_sync(0xffffffffu, base, 31) + incl - cnt;
+#pragma unroll
+                            for (int j = 0; j < VEC; ++j) {
+                                if ((mask >> j) & 1u) {
+                                    if (slot < (unsigned int)KF_CAP) {
+                                        S.key[slot] = sortkey(key_of<DT>(x[j]), v * VEC + j);
+                                        S.mass[slot] = fixmass(x[j], m, c);
+                                    }
+                                    ++slot;
+                                }
+                            }
                         }
                     }
                 }
@@ -1724,38 +1766,24 @@ __global__ void __launch_bounds__(KF_TH) kfilter_kernel(const Params P)
                 if (t == 0)
                     atomicAdd(&P.hdr->n_radix_rows, 1u);
             } else {
-                // ---- sort descending (bitonic, padded with zero entries)
+                // ---- order descending: a token's rank is the number of larger
+                // keys (keys are distinct: the index is in them); order[rank]
+                // takes the group list's place, no longer needed
                 const int n = (int)S.nc;
-                int n2 = 1;
-                while (n2 < n)
-                    n2 <<= 1;
-                for (int i = n + t; i < n2; i += KF_TH) {
-                    S.key[i] = 0ull;
-                    S.mass[i] = 0ull;
+                int *order = S.glist;
+                for (int i = t; i < n; i += KF_TH) {
+                    const unsigned long long ki = S.key[i];
+                    int r = 0;
+                    for (int j = 0; j < n; ++j)
+                        r += (S.key[j] > ki) ? 1 : 0;
+                    order[r] = i;
                 }
                 __syncthreads();
-                for (int size = 2; size <= n2; size <<= 1) {
-                    for (int stride = size >> 1; stride > 0; stride >>= 1) {
-                        for (int i = t; i < n2 / 2; i += KF_TH) {
-                            const int lo = 2 * stride * (i / stride) + (i % stride), hi = lo + stride;
-                            const bool down = (lo & size) == 0;  // this pair's block ends descending
-                            const unsigned long long a = S.key[lo], bb = S.key[hi];
-                            if (down ? (a < bb) : (a > bb)) {
-                                S.key[lo] = bb;
-                                S.key[hi] = a;
-                                const unsigned long long ma = S.mass[lo];
-                                S.mass[lo] = S.mass[hi];
-                                S.mass[hi] = ma;
-                            }
-                        }
-                        __syncthreads();
-                    }
-                }
                 // ---- the cut: the top-k mass, then the top-p end (K <= n)
                 const int nk = min(K, n);
                 unsigned long long ms = 0ull;
                 for (int i = t; i < nk; i += KF_TH)
-                    ms += S.mass[i];
+                    ms += S.mass[order[i]];
 #pragma unroll
                 for (int o = 16; o > 0; o >>= 1)
                     ms += __shfl_xor_sync(0xffffffffu, ms, o);
@@ -1775,7 +1803,7 @@ __global__ void __launch_bounds__(KF_TH) kfilter_kernel(const Params P)
                     int istar = -1;
                     for (int i0 = 0; i0 < nk && istar < 0; i0 += 32) {
                         const int i = i0 + lane;
-                        unsigned long long x = (i < nk) ? S.mass[i] : 0ull;
+                        unsigned long long x = (i < nk) ? S.mass[order[i]] : 0ull;
 #pragma unroll
                         for (int o = 1; o < 32; o <<= 1) {
                             const unsigned long long y = __shfl_up_sync(0xffffffffu, x, o);
@@ -1797,7 +1825,7 @@ __global__ void __launch_bounds__(KF_TH) kfilter_kernel(const Params P)
                     last = istar;
                     Zt = run;
                 }
-                const unsigned long long e = S.key[last];
+                const unsigned long long e = S.key[order[last]];
                 out.kappa = (unsigned int)(e >> 32);
                 out.iota = (int)(0xffffffffu - (unsigned int)(e & 0xffffffffu));
                 out.zt = (float)((double)Zt * (1.0 / 1099511627776.0));

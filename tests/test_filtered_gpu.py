@@ -139,6 +139,33 @@ def test_group_cut_with_massive_ties(dtype):
 
 
 @pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_group_cut_far_maximum_and_negative_rows(dtype):
+    """The group cut's first histogram covers the 256 16-bit key prefixes at
+    and below the row maximum's (two binades).  Rows with three logits far
+    above the rest hold fewer than K group keys there, so tau comes from the
+    radix search from the top; rows of only negative logits run the window
+    pass on negative keys.  Both must give the streaming cut's records."""
+    rng = np.random.default_rng(31)
+    B, k, V = 12, 2, 30000
+    case = synth.gauss_case(B=B, k=k, V=V, dtype=dtype, seed=32, T=(0.8, 1.0))
+    for arr in (case.target, case.draft):
+        vals = rng.normal(0.0, 1.0, arr.shape).astype(np.float32)
+        far = rng.integers(0, V, size=(B, arr.shape[1], 3))
+        for b in range(B // 2):
+            for i in range(arr.shape[1]):
+                vals[b, i, far[b, i]] = 40.0
+        vals[B // 2:] -= 30.0
+        arr[...] = synth.f32_to_bf16_bits(vals) if dtype == "bf16" else vals
+    top_k = rng.choice([2, 5, 50, 256], B).astype(np.int32)
+    top_p = rng.choice([1.0, 0.9], B).astype(np.float32)
+    tokens = filtered_tokens(case, top_k, top_p, seed=8)
+    g = run_gpu(case, tokens, top_k, top_p)
+    w = run_gpu(case, tokens, top_k, top_p, ws=window_ws(case))
+    assert np.array_equal(g[0], w[0]) and np.array_equal(g[1], w[1])
+    check(case, tokens, top_k, top_p)
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
 def test_filters_off_equal_spec_verify(dtype):
     case = synth.gauss_case(B=16, k=4, V=5000, dtype=dtype, seed=3, T=(0.0, 0.7, 1.2))
     d = sv.to_device(case)
