@@ -175,9 +175,11 @@ int32_t spec_verify_trace(const void *target_logits, const void *draft_logits,
 
 /*
  * Bytes of workspace with which spec_verify_filtered cuts top-k rows from
- * group maxima: spec_verify_workspace_size rounded up to 256, plus 4 bytes per
- * 64 bf16 (32 fp32) logits of every row, B (2k+1) rows.  Returns 0 for sizes
- * out of range.  Host-only; needs no GPU.
+ * group maxima: spec_verify_workspace_size rounded up to 256, plus, for each
+ * of the B (2k+1) rows, 4 bytes per 64 bf16 (32 fp32) logits (the group
+ * maxima), 2048 bytes (up to 256 kept tokens, which the kept-set draws read
+ * back) and 4 bytes (their count), each region starting on a 256-byte
+ * boundary.  Returns 0 for sizes out of range.  Host-only; needs no GPU.
  */
 size_t spec_verify_filtered_workspace_size(int32_t B, int32_t k, int32_t V, int32_t dtype);
 

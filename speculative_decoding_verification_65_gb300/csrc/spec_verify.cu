@@ -119,6 +119,14 @@ __device__ __forceinline__ unsigned int key_of(float x)
     return okey(__float_as_uint(x)) & ((DT == SPEC_BF16) ? 0xffff0000u : 0xffffffffu);
 }
 
+// The logit a key was made from (a bf16 value's low 16 bits are zero).
+template <int DT>
+__device__ __forceinline__ float val_of_key(unsigned int key)
+{
+    const unsigned int b = (key & 0x80000000u) ? (key & 0x7fffffffu) : ~key;
+    return __uint_as_float(b & ((DT == SPEC_BF16) ? 0xffff0000u : 0xffffffffu));
+}
+
 struct TileInfo {
     int kind;
     int b;         // sequence
@@ -153,6 +161,9 @@ struct Params {
     FiltRec *filt;     // [B][rows] (filtered calls)
     unsigned int *gkey;  // [B][rows][NS * NT] lane-group maximum keys (filtered calls
                          // with room for them; null otherwise)
+    unsigned long long *kept;  // [B][rows][KF_KMAX] the kept tokens of the rows cut from
+                               // group maxima, as sort keys in rank order (with gkey)
+    int *kcount;               // [B][rows] their number; -1: the row was not cut there
     // exact draws of the rows whose fp32 draw is near a cell boundary
     RJob *rjob;            // [B] the listed draws (count in hdr->n_flag)
     unsigned int *rkcnt;   // [B] their counts of groups of undecided elements
@@ -1506,6 +1517,8 @@ __global__ void __launch_bounds__(FTH, 2) filter_kernel(const Params P)
 // for bf16 keys, whose low 16 bits are zero).  A row with more selected
 // groups or gathered tokens than the buffers hold (many ties at tau) is left
 // to the radix kernel (FILT_RADIX).  The window kernel skips these rows.
+// The kept set of every row cut here is stored in rank order for the
+// kept-set draw, which would otherwise gather it again.
 constexpr int KF_TH = 128;
 constexpr int KF_KMAX = 256;
 constexpr int KF_GCAP = 512;   // selected groups at most
@@ -1533,7 +1546,7 @@ struct KfSmem {
 };
 
 template <int DT>
-__global__ void __launch_bounds__(KF_TH) kfilter_kernel(const Params P)
+__global__ void __launch_bounds__(KF_TH, 16) kfilter_kernel(const Params P)
 {
     using L = Lg<DT>;
     constexpr int VEC = L::VEC;
@@ -1569,6 +1582,8 @@ __global__ void __launch_bounds__(KF_TH) kfilter_kernel(const Params P)
             } else if (t == 0) {
                 atomicAdd(&P.hdr->n_stream_rows, 1u);
             }
+            if (t == 0)
+                P.kcount[item] = -1;
             continue;
         }
         const bool topp = Pp < 1.0f;
@@ -1585,6 +1600,7 @@ __global__ void __launch_bounds__(KF_TH) kfilter_kernel(const Params P)
         out.iota = INT_MAX;
         out.zt = 0.0f;
         out.flags = FILT_OFF;
+        int kc = -1;  // kept tokens stored for the kept-set draw (-1: none)
         if (!(isnan(m) || isinf(m))) {  // else the scan reports the row as an error
             const unsigned int *gk = P.gkey + (size_t)item * NG;
             // the group keys, KF_LB loads in flight per thread (from L2 after
@@ -1771,12 +1787,17 @@ __global__ void __launch_bounds__(KF_TH) kfilter_kernel(const Params P)
                 // takes the group list's place, no longer needed
                 const int n = (int)S.nc;
                 int *order = S.glist;
+                // the first KF_KMAX in rank order are also stored for the
+                // kept-set draw (the kept set is a prefix of them: K <= KF_KMAX)
+                unsigned long long *kp = P.kept + (size_t)item * KF_KMAX;
                 for (int i = t; i < n; i += KF_TH) {
                     const unsigned long long ki = S.key[i];
                     int r = 0;
                     for (int j = 0; j < n; ++j)
                         r += (S.key[j] > ki) ? 1 : 0;
                     order[r] = i;
+                    if (r < KF_KMAX)
+                        kp[r] = ki;
                 }
                 __syncthreads();
                 // ---- the cut: the top-k mass, then the top-p end (K <= n)
@@ -1826,14 +1847,17 @@ __global__ void __launch_bounds__(KF_TH) kfilter_kernel(const Params P)
                     Zt = run;
                 }
                 const unsigned long long e = S.key[order[last]];
+                kc = last + 1;  // thread 0's is the one stored
                 out.kappa = (unsigned int)(e >> 32);
                 out.iota = (int)(0xffffffffu - (unsigned int)(e & 0xffffffffu));
                 out.zt = (float)((double)Zt * (1.0 / 1099511627776.0));
                 out.flags = FILT_ON;
             }
         }
-        if (t == 0)
+        if (t == 0) {
             P.filt[item] = out;
+            P.kcount[item] = kc;
+        }
         __syncthreads();  // the row's shared state is free again
     }
 }
@@ -2844,10 +2868,12 @@ __global__ void __launch_bounds__(NT, FILT ? 4 : 6) draw_kernel(const Params P)
 // A filtered sequence whose rows have top-k (K <= KF_KMAX) in a call with
 // group maxima draws its correction or bonus token from the kept sets alone:
 // the residual max(0, p~ - q~) and the bonus p~ are zero outside the target's
-// kept set, which holds at most K tokens.  A kept set is gathered through the
-// group maxima as the cut gathers it (the groups whose key is >= kappa; their
-// tokens with key > kappa, or == kappa up to index iota), or, when more
-// groups than the buffer holds reach kappa (ties), by a pass over the row.
+// kept set, which holds at most K tokens.  A kept set is read back as the
+// group cut stored it (its tokens in rank order); for a row the cut left to
+// the streaming filter it is gathered through the group maxima as the cut
+// gathers them (the groups whose key is >= kappa; their tokens with key >
+// kappa, or == kappa up to index iota), or, when more groups than the buffer
+// holds reach kappa (ties), by a pass over the row.
 // The weights are computed in fp64 as the fp64 reference computes them:
 // exp((x - m) / T) over each kept set, normalised by its sum; the inverse CDF
 // runs over the target's kept tokens in index order.
@@ -2860,6 +2886,7 @@ struct KdSmem {
     int tidx[KD_CAP], didx[KD_CAP];    // kept tokens of the target / draft row
     float tval[KD_CAP], dval[KD_CAP];  // their logits
     double w[KD_CAP];                  // the target kept tokens' weights
+    double ed[KD_CAP];                 // the draft kept tokens' exponentials
     int order[KD_CAP];                 // target kept tokens by index
     double red[KD_TH / 32];
     unsigned int ng, n;
@@ -2957,6 +2984,25 @@ __device__ int kd_gather(const Params &P, const void *arr, size_t row, const uns
     return n;
 }
 
+// The kept set of row `item` as the group cut stored it (rank order) into
+// (oidx, oval); returns its size, or -1 when the cut left the row to the
+// streaming filter (every thread).
+template <int DT>
+__device__ int kd_stored(const Params &P, size_t item, int *oidx, float *oval, int t)
+{
+    const int n = __ldcg(P.kcount + item);
+    if (n < 0)
+        return -1;
+    const unsigned long long *kp = P.kept + item * KF_KMAX;
+    for (int i = t; i < n; i += KD_TH) {
+        const unsigned long long e = __ldcg(kp + i);
+        oidx[i] = (int)(0xffffffffu - (unsigned int)(e & 0xffffffffu));
+        oval[i] = val_of_key<DT>((unsigned int)(e >> 32));
+    }
+    __syncthreads();
+    return n;
+}
+
 // Block-wide sum of one double per thread, in a fixed order (every thread).
 __device__ __forceinline__ double kd_sum(double x, KdSmem &S, int t, int lane)
 {
@@ -2991,36 +3037,52 @@ __global__ void __launch_bounds__(KD_TH) kdraw_kernel(const Params P)
     const size_t NG = (size_t)P.NS * NT;
     const double T = (double)__ldg(P.temperature + b);
     const bool resid = J.mode == DRAW_RESIDUAL;
-    // the target's kept set at row j (its bonus row when j == k)
-    const unsigned int *gkt = P.gkey + ((size_t)b * P.rows + J.j) * NG;
-    const int nt = kd_gather<DT>(P, P.target, (size_t)J.t_row, gkt, J.kt, J.it, S.tidx, S.tval,
-                                 S, t, lane);
+    // the target's kept set at row j (its bonus row when j == k): as the
+    // group cut stored it, else gathered through the group maxima
+    const size_t it_t = (size_t)b * P.rows + J.j;
+    int nt = kd_stored<DT>(P, it_t, S.tidx, S.tval, t);
+    if (nt < 0)
+        nt = kd_gather<DT>(P, P.target, (size_t)J.t_row, P.gkey + it_t * NG, J.kt, J.it, S.tidx,
+                           S.tval, S, t, lane);
     double zd = 1.0;
     int nd = 0;
     if (resid) {
-        const unsigned int *gkd = P.gkey + ((size_t)b * P.rows + k + 1 + J.j) * NG;
-        nd = kd_gather<DT>(P, P.draft, (size_t)J.d_row, gkd, J.kd, J.id, S.didx, S.dval, S, t,
-                           lane);
+        const size_t it_d = (size_t)b * P.rows + k + 1 + J.j;
+        nd = kd_stored<DT>(P, it_d, S.didx, S.dval, t);
+        if (nd < 0)
+            nd = kd_gather<DT>(P, P.draft, (size_t)J.d_row, P.gkey + it_d * NG, J.kd, J.id,
+                               S.didx, S.dval, S, t, lane);
         double z = 0.0;
-        for (int i = t; i < nd; i += KD_TH)
-            z += exp(((double)S.dval[i] - (double)J.md) / T);
+        for (int i = t; i < nd; i += KD_TH) {
+            const double e = exp(((double)S.dval[i] - (double)J.md) / T);
+            S.ed[i] = e;
+            z += e;
+        }
         zd = kd_sum(z, S, t, lane);
     }
+    // each exponential once (the fp64 pipe is narrow): the target's in S.w
+    // until its weight replaces it, the draft's in S.ed
     double zt = 0.0;
-    for (int i = t; i < nt; i += KD_TH)
-        zt += exp(((double)S.tval[i] - (double)J.mt) / T);
+    for (int i = t; i < nt; i += KD_TH) {
+        const double e = exp(((double)S.tval[i] - (double)J.mt) / T);
+        S.w[i] = e;
+        zt += e;
+    }
     zt = kd_sum(zt, S, t, lane);
     // weights of the target's kept tokens, and their order by index
     double r = 0.0;
     for (int i = t; i < nt; i += KD_TH) {
         const int x = S.tidx[i];
-        const double p = exp(((double)S.tval[i] - (double)J.mt) / T) / zt;
+        const double p = S.w[i] / zt;
         double q = 0.0;
         if (resid) {
-            const float dx = L::load1(P.draft, (size_t)J.d_row * P.V + x);
-            const unsigned int key = key_of<DT>(dx);
-            if (key > J.kd || (key == J.kd && x <= J.id))
-                q = exp(((double)dx - (double)J.md) / T) / zd;
+            // q~(x) is nonzero exactly when x is in the draft's kept set
+            for (int j = 0; j < nd; ++j) {
+                if (S.didx[j] == x) {
+                    q = S.ed[j] / zd;
+                    break;
+                }
+            }
         }
         const double w = resid ? fmax(p - q, 0.0) : p;
         S.w[i] = w;
@@ -3351,7 +3413,7 @@ int tile_elems(int32_t dtype) { return TILE_BYTES / (dtype == SPEC_F32 ? 4 : 2);
 
 struct WsLayout {
     size_t partials, jobs, chunks, rec, filt, resolve, total;
-    size_t gkey, total_filtered;  // filtered calls: the lane-group maximum keys after it
+    size_t gkey, kept, kcount, total_filtered;  // filtered calls: the group-maximum regions
     size_t NS, NSS, DS, chunk_stride, NCH;
 };
 
@@ -3360,7 +3422,9 @@ struct WsLayout {
 // | top-k / top-p records [B][2k+1] (filtered calls) | the exact draws of up
 // to B listed sequences (resolve.cuh: records, counts, groups, chunk records)
 // | and, when a filtered call's workspace has room, one 4-byte group key per
-// 8 vectors of every tile of every row [B][2k+1][NS * 256]
+// 8 vectors of every tile of every row [B][2k+1][NS * 256], the kept tokens
+// of the rows cut from them [B][2k+1][256] (8 bytes each) and their counts
+// [B][2k+1]
 WsLayout ws_layout(int32_t B, int32_t k, int32_t V, int32_t dtype)
 {
     WsLayout w;
@@ -3378,8 +3442,11 @@ WsLayout ws_layout(int32_t B, int32_t k, int32_t V, int32_t dtype)
     w.filt = align_up(w.rec + (size_t)B * w.NCH * sizeof(float2), 256);
     w.resolve = align_up(w.filt + (size_t)B * (2 * (size_t)k + 1) * sizeof(FiltRec), 256);
     w.total = w.resolve + resolve_bytes((size_t)B, V, true);
+    const size_t rows = (size_t)B * (2 * (size_t)k + 1);
     w.gkey = align_up(w.total, 256);
-    w.total_filtered = w.gkey + (size_t)B * (2 * (size_t)k + 1) * w.NS * NT * 4;
+    w.kept = align_up(w.gkey + rows * w.NS * NT * 4, 256);
+    w.kcount = align_up(w.kept + rows * KF_KMAX * 8, 256);
+    w.total_filtered = w.kcount + rows * 4;
     return w;
 }
 
@@ -3562,9 +3629,10 @@ int launch(const void *target, const void *draft, const int32_t *tokens, const f
     P.top_k = top_k;
     P.top_p = top_p;
     P.filt = reinterpret_cast<FiltRec *>(w + lay.filt);
-    P.gkey = (filtered && ws_size >= lay.total_filtered)
-                 ? reinterpret_cast<unsigned int *>(w + lay.gkey)
-                 : nullptr;
+    const bool groups = filtered && ws_size >= lay.total_filtered;
+    P.gkey = groups ? reinterpret_cast<unsigned int *>(w + lay.gkey) : nullptr;
+    P.kept = groups ? reinterpret_cast<unsigned long long *>(w + lay.kept) : nullptr;
+    P.kcount = groups ? reinterpret_cast<int *>(w + lay.kcount) : nullptr;
     RParams RP;
     resolve_regions(RP, w + lay.resolve, (size_t)B, V, true);
     RP.hdr = P.hdr;

@@ -77,9 +77,12 @@ def test_workspace_size(lib, B, k, V, dt, ok):
     assert n == resolve + up(96 * B, 256) + up(4 * B, 256) + up(32 * 64 * B, 256) + \
         up(32 * rnc * B, 256)
     # filtered calls with room for the group maxima: one 4-byte key per 8
-    # vectors (256 per 32 KB tile) of every row
+    # vectors (256 per 32 KB tile) of every row, then per row up to 256 kept
+    # tokens of 8 bytes and their 4-byte count
+    rows = B * (2 * k + 1)
+    kept = up(up(n, 256) + rows * ns * 256 * 4, 256)
     assert sv.spec_verify_filtered_workspace_size(B, k, V, dt) == \
-        up(n, 256) + B * (2 * k + 1) * ns * 256 * 4
+        up(kept + rows * 256 * 8, 256) + rows * 4
 
 
 def _call(lib, ptrs, B=1, k=1, V=8, dt=0, wsb=1 << 20):
