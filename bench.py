@@ -538,7 +538,9 @@ def run_ours(args):
         sv.spec_verify_host(h_t, h_d, h_g, h_ua, h_ur, h_T, arena, h_ot, h_on, stream=stream)
     e2e_s = reduce_max(time.perf_counter() - e0, world, dev)
     e2e_value = aggregate_rate(B * k, e2e_steps, world, e2e_s)
-    h2d = sum(int(x.numel() * x.element_size()) for x in (h_t, h_d, h_g, h_ua, h_ur, h_T))
+    # the draft rows of greedy sequences stay on the host (never read)
+    h2d = sum(int(x.numel() * x.element_size()) for x in (h_t, h_g, h_ua, h_ur, h_T)) + \
+        int(np.count_nonzero(case.temperature != 0)) * k * V * h_d.element_size()
     d2h = int(h_ot.numel() * 4 + h_on.numel() * 4)
     del arena
     torch.cuda.empty_cache()

@@ -312,10 +312,12 @@ size_t spec_verify_host_arena_size(int32_t B, int32_t k, int32_t V, int32_t dtyp
 
 /*
  * End-to-end variant on HOST buffers: copies the inputs host->device into the
- * caller's device arena (one cudaMemcpyAsync per buffer), runs spec_verify,
- * and copies out_tokens / out_num_accepted back to the host buffers, all on
- * `stream`; synchronises the stream before returning so the host outputs are
- * ready.  Pinned host memory makes the copies asynchronous DMA.  The arena
+ * caller's device arena (one cudaMemcpyAsync per buffer; the draft rows only
+ * of sequences whose host temperature is not 0, one copy per run of such
+ * sequences, since the greedy rule never reads draft rows), runs
+ * spec_verify, and copies out_tokens / out_num_accepted back to the host
+ * buffers, all on `stream`; synchronises the stream before returning so the
+ * host outputs are ready.  Pinned host memory makes the copies asynchronous DMA.  The arena
  * must be >= spec_verify_host_arena_size(...) bytes and 256-byte aligned; the
  * status word of its workspace part is zeroed by this call.  Host pointers follow the device
  * entry point's shapes.

@@ -3949,12 +3949,30 @@ int32_t spec_verify_host(const void *target_logits, const void *draft_logits,
         void *dst;
         const void *src;
         size_t n;
-    } cps[] = {{d_t, target_logits, bt},       {d_d, draft_logits, bd},
+    } cps[] = {{d_t, target_logits, bt},
                {d_g, draft_tokens, (size_t)B * k * 4}, {d_ua, u_accept, (size_t)B * k * 4},
                {d_ur, u_resample, (size_t)B * 4},    {d_T, temperature, (size_t)B * 4}};
     for (const auto &c : cps)
         if (cudaMemcpyAsync(c.dst, c.src, c.n, cudaMemcpyHostToDevice, st) != cudaSuccess)
             return SPEC_ECUDA;
+    // A greedy sequence's draft rows are never read (the greedy rule compares
+    // argmaxes of the target alone), so only the other sequences' draft rows
+    // cross the host link: one copy per run of consecutive such sequences.
+    const size_t drow = (size_t)k * V * es;
+    for (int b0 = 0; b0 < B;) {
+        if (temperature[b0] == 0.0f) {
+            ++b0;
+            continue;
+        }
+        int b1 = b0 + 1;
+        while (b1 < B && !(temperature[b1] == 0.0f))
+            ++b1;
+        if (cudaMemcpyAsync(d_d + (size_t)b0 * drow,
+                            reinterpret_cast<const uint8_t *>(draft_logits) + (size_t)b0 * drow,
+                            (size_t)(b1 - b0) * drow, cudaMemcpyHostToDevice, st) != cudaSuccess)
+            return SPEC_ECUDA;
+        b0 = b1;
+    }
     if (cudaMemsetAsync(d_ws, 0, sizeof(WsHeader), st) != cudaSuccess)
         return SPEC_ECUDA;
     int rc = launch(d_t, d_d, reinterpret_cast<const int32_t *>(d_g),

@@ -297,3 +297,23 @@ def test_host_entry_matches_device_entry():
                                pin(case.u_resample), pin(case.temperature), arena)
     np.testing.assert_array_equal(t.numpy(), g_t)
     np.testing.assert_array_equal(n.numpy(), g_n)
+
+
+def test_host_entry_leaves_greedy_draft_rows_on_the_host():
+    """spec_verify_host copies draft rows only for sequences with T != 0: NaN
+    in a greedy sequence's host draft rows (never copied, never read) changes
+    nothing, and a run pattern with greedy sequences at both ends and between
+    runs gives the oracle's outputs."""
+    case = synth.gauss_case(B=11, k=3, V=3001, dtype=synth.F32, seed=61, T=(0.0, 1.0))
+    case.temperature[:] = np.array([0, 1, 1, 0, 0.7, 0, 1.3, 1, 1, 0, 0], np.float32)
+    B, k, V = case.B, case.k, case.V
+    dft = case.draft.copy()
+    dft[case.temperature == 0] = np.nan
+    arena = torch.zeros(sv.spec_verify_host_arena_size(B, k, V, sv.SPEC_F32),
+                        dtype=torch.uint8, device="cuda")
+    pin = lambda a: torch.from_numpy(np.ascontiguousarray(a)).pin_memory()
+    t, n = sv.spec_verify_host(pin(case.target), pin(dft), pin(case.tokens), pin(case.u_accept),
+                               pin(case.u_resample), pin(case.temperature), arena)
+    r_t, r_n, tr = run_oracle(case)
+    pu.compare(case, t.numpy(), n.numpy(), r_t, r_n, tr)
+    assert np.all(n.numpy() >= 0)
