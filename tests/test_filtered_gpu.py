@@ -166,6 +166,28 @@ def test_group_cut_far_maximum_and_negative_rows(dtype):
 
 
 @pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_kept_set_draws_stored_and_gathered(dtype):
+    """The kept-set draws read a row's kept tokens back as the group cut
+    stored them, or gather them when the cut left the row to the streaming
+    filter.  Draft rows of integer logits (ties past the cut's buffers) next
+    to gaussian target rows make both happen within one sequence; K spans 1
+    to 256; both cuts must give the oracle's tokens and the streaming cut's."""
+    rng = np.random.default_rng(41)
+    B, k, V = 16, 3, 20000
+    case = synth.gauss_case(B=B, k=k, V=V, dtype=dtype, seed=42, T=(0.7, 1.0))
+    vals = np.round(rng.normal(0.0, 0.3, case.draft.shape)).astype(np.float32)
+    vals[B // 2:] = rng.normal(0.0, 2.0, vals[B // 2:].shape).astype(np.float32)
+    case.draft[...] = synth.f32_to_bf16_bits(vals) if dtype == "bf16" else vals
+    top_k = rng.choice([1, 3, 40, 200, 256], B).astype(np.int32)
+    top_p = rng.choice([1.0, 0.95, 0.6], B).astype(np.float32)
+    tokens = filtered_tokens(case, top_k, top_p, seed=9)
+    g = run_gpu(case, tokens, top_k, top_p)
+    w = run_gpu(case, tokens, top_k, top_p, ws=window_ws(case))
+    assert np.array_equal(g[0], w[0]) and np.array_equal(g[1], w[1])
+    check(case, tokens, top_k, top_p)
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
 def test_filters_off_equal_spec_verify(dtype):
     case = synth.gauss_case(B=16, k=4, V=5000, dtype=dtype, seed=3, T=(0.0, 0.7, 1.2))
     d = sv.to_device(case)
